@@ -1,0 +1,362 @@
+/*
+ * lrscan oracle -- TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+ *
+ * A plain, slow, obviously correct CPU statement of the differentiable
+ * diagonal linear-recurrence scan.  Only the test-suite, the smoke check and
+ * the CPU-baseline leg of the benchmark may load this library; the CUDA
+ * library never links, includes or calls it, and it shares no code, header or
+ * helper with the CUDA sources.
+ *
+ * What is computed (per batch row b and channel lane d, contiguous [B,T,D]
+ * layout with D fastest, as in triton_training_scan.py, _real_forward, where
+ * the element offset is (batch*length + t)*width + lane):
+ *
+ *   forward   h_{-1} = 0,  h_t = a_t * h_{t-1} + b_t   (t = 0..T-1)
+ *             out_t = h_t stored in the storage dtype, last = h_{T-1} in fp32
+ *             (triton_training_scan.py, _real_forward and real_scan_with_last)
+ *
+ *   backward  loss L = sum_t grad_out_t * h_t, with h read back from `out`:
+ *             g_{T-1} = grad_out_{T-1}
+ *             g_t     = grad_out_t + a_{t+1} * g_{t+1}
+ *             grad_b_t = g_t
+ *             grad_a_t = g_t * out_{t-1}   (out_{-1} = 0)
+ *             (triton_training_scan.py, _real_backward)
+ *
+ * Readings taken where the page is silent (each is listed in the design
+ * notes of the repository):
+ *   - one rounding per recurrence step: h = fma(a, h, b) and
+ *     g = fma(a_{t+1}, g_{t+1}, grad_out_t); grad_a is one rounded product;
+ *   - state and accumulation are fp32 whatever the storage dtype; fp32 ->
+ *     bf16 is round-to-nearest-even;
+ *   - in the bf16 variant the backward reads h_{t-1} from the bf16-stored out.
+ *
+ * The "chunk" variants restate the two-level affine-map decomposition of the
+ * same page (_real_chunk_summary, _real_chunk_prefix, _real_chunk_replay and
+ * their _real_reverse_* mirrors) step by step in the page's own order, with
+ * the page's reverse carry (the adjoint that leaves a step, a_t*(k+grad_out_t)).
+ * They exist only so the tests can check the algebra of that decomposition
+ * against the sequential definition.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math: the
+ * rounding of every operation above is part of the contract).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define LRO_OK 0
+#define LRO_EINVAL (-1)
+#define LRO_ENOMEM (-2)
+
+/* ---------------------------------------------------------------------- */
+/* bf16 storage: the top 16 bits of an IEEE-754 binary32 value.            */
+/* ---------------------------------------------------------------------- */
+
+/* Widening is exact: the bf16 bits become the high half of a binary32. */
+float lro_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Narrowing by round-to-nearest, ties-to-even on the 16 discarded bits.
+ * NaN stays NaN (quiet bit forced so the truncation cannot make an inf). */
+uint16_t lro_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep_lsb = (u >> 16) & 1u;    /* parity of the kept part */
+    u += 0x7fffu + keep_lsb;               /* > half rounds up; == half to even */
+    return (uint16_t)(u >> 16);
+}
+
+void lro_f32_to_bf16_array(const float *src, uint16_t *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = lro_f32_to_bf16(src[i]);
+}
+
+void lro_bf16_to_f32_array(const uint16_t *src, float *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = lro_bf16_to_f32(src[i]);
+}
+
+static int bad_shape(int64_t B, int64_t T, int64_t D)
+{
+    return B < 0 || T < 0 || D < 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Sequential forward                                                      */
+/* ---------------------------------------------------------------------- */
+
+int lro_fwd_f32(const float *a, const float *b, float *out, float *last,
+                int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    float *h = calloc((size_t)(D > 0 ? D : 1), sizeof *h);
+    if (!h) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t d = 0; d < D; ++d) h[d] = 0.0f;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                h[d] = fmaf(a[i], h[d], b[i]);
+                out[i] = h[d];
+            }
+        }
+        if (last)
+            for (int64_t d = 0; d < D; ++d) last[bb * D + d] = h[d];
+    }
+    free(h);
+    return LRO_OK;
+}
+
+int lro_fwd_bf16(const uint16_t *a, const uint16_t *b, uint16_t *out,
+                 float *last, int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    float *h = calloc((size_t)(D > 0 ? D : 1), sizeof *h);
+    if (!h) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t d = 0; d < D; ++d) h[d] = 0.0f;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                h[d] = fmaf(lro_bf16_to_f32(a[i]), h[d], lro_bf16_to_f32(b[i]));
+                out[i] = lro_f32_to_bf16(h[d]);
+            }
+        }
+        if (last)
+            for (int64_t d = 0; d < D; ++d) last[bb * D + d] = h[d];
+    }
+    free(h);
+    return LRO_OK;
+}
+
+int lro_fwd_f64(const double *a, const double *b, double *out, double *last,
+                int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    double *h = calloc((size_t)(D > 0 ? D : 1), sizeof *h);
+    if (!h) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t d = 0; d < D; ++d) h[d] = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                h[d] = fma(a[i], h[d], b[i]);
+                out[i] = h[d];
+            }
+        }
+        if (last)
+            for (int64_t d = 0; d < D; ++d) last[bb * D + d] = h[d];
+    }
+    free(h);
+    return LRO_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Sequential backward                                                     */
+/* ---------------------------------------------------------------------- */
+
+int lro_bwd_f32(const float *a, const float *out, const float *grad_out,
+                float *grad_a, float *grad_b, int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    float *g = calloc((size_t)(D > 0 ? D : 1), sizeof *g);
+    if (!g) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t t = T - 1; t >= 0; --t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                if (t == T - 1)
+                    g[d] = grad_out[i];
+                else
+                    g[d] = fmaf(a[i + D], g[d], grad_out[i]); /* a_{t+1} */
+                float h_prev = (t > 0) ? out[i - D] : 0.0f;   /* out_{t-1} */
+                grad_b[i] = g[d];
+                grad_a[i] = g[d] * h_prev;
+            }
+        }
+    }
+    free(g);
+    return LRO_OK;
+}
+
+int lro_bwd_bf16(const uint16_t *a, const uint16_t *out,
+                 const uint16_t *grad_out, uint16_t *grad_a, uint16_t *grad_b,
+                 int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    float *g = calloc((size_t)(D > 0 ? D : 1), sizeof *g);
+    if (!g) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t t = T - 1; t >= 0; --t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                float go = lro_bf16_to_f32(grad_out[i]);
+                if (t == T - 1)
+                    g[d] = go;
+                else
+                    g[d] = fmaf(lro_bf16_to_f32(a[i + D]), g[d], go);
+                float h_prev = (t > 0) ? lro_bf16_to_f32(out[i - D]) : 0.0f;
+                grad_b[i] = lro_f32_to_bf16(g[d]);
+                grad_a[i] = lro_f32_to_bf16(g[d] * h_prev);
+            }
+        }
+    }
+    free(g);
+    return LRO_OK;
+}
+
+int lro_bwd_f64(const double *a, const double *out, const double *grad_out,
+                double *grad_a, double *grad_b, int64_t B, int64_t T, int64_t D)
+{
+    if (bad_shape(B, T, D)) return LRO_EINVAL;
+    double *g = calloc((size_t)(D > 0 ? D : 1), sizeof *g);
+    if (!g) return LRO_ENOMEM;
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t t = T - 1; t >= 0; --t) {
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t i = (bb * T + t) * D + d;
+                if (t == T - 1)
+                    g[d] = grad_out[i];
+                else
+                    g[d] = fma(a[i + D], g[d], grad_out[i]);
+                double h_prev = (t > 0) ? out[i - D] : 0.0;
+                grad_b[i] = g[d];
+                grad_a[i] = g[d] * h_prev;
+            }
+        }
+    }
+    free(g);
+    return LRO_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Two-level (chunked) decomposition, in the page's order.                 */
+/* A chunk c covers steps [c*C, min((c+1)*C, T)); a short last chunk is    */
+/* simply shorter (equivalent to padding it with identity steps a=1, b=0). */
+/* ---------------------------------------------------------------------- */
+
+#define CHUNK_BODY_FWD(REAL, FMA)                                              \
+    int64_t nc = (T + C - 1) / C;                                              \
+    REAL *P = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));               \
+    REAL *Q = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));               \
+    REAL *hin = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));             \
+    if (!P || !Q || !hin) { free(P); free(Q); free(hin); return LRO_ENOMEM; } \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            /* chunk summary: h -> P*h + Q over the chunk */                   \
+            for (int64_t c = 0; c < nc; ++c) {                                 \
+                REAL prod = 1, state = 0;                                      \
+                for (int64_t t = c * C; t < T && t < (c + 1) * C; ++t) {       \
+                    int64_t i = (bb * T + t) * D + d;                          \
+                    prod = a[i] * prod;                                        \
+                    state = FMA(a[i], state, b[i]);                            \
+                }                                                              \
+                P[c] = prod;                                                   \
+                Q[c] = state;                                                  \
+            }                                                                  \
+            /* serial exclusive prefix over chunks */                          \
+            REAL state = 0;                                                    \
+            for (int64_t c = 0; c < nc; ++c) {                                 \
+                hin[c] = state;                                                \
+                state = FMA(P[c], state, Q[c]);                                \
+            }                                                                  \
+            /* replay every chunk from its entry state */                      \
+            for (int64_t c = 0; c < nc; ++c) {                                 \
+                REAL h = hin[c];                                               \
+                for (int64_t t = c * C; t < T && t < (c + 1) * C; ++t) {       \
+                    int64_t i = (bb * T + t) * D + d;                          \
+                    h = FMA(a[i], h, b[i]);                                    \
+                    out[i] = h;                                                \
+                }                                                              \
+                if (c == nc - 1 && last) last[bb * D + d] = h;                 \
+            }                                                                  \
+            if (T == 0 && last) last[bb * D + d] = 0;                          \
+        }                                                                      \
+    }                                                                          \
+    free(P); free(Q); free(hin);                                               \
+    return LRO_OK;
+
+#define CHUNK_BODY_BWD(REAL)                                                   \
+    int64_t nc = (T + C - 1) / C;                                              \
+    REAL *P = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));               \
+    REAL *Q = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));               \
+    REAL *fut = malloc(sizeof(REAL) * (size_t)(nc > 0 ? nc : 1));             \
+    if (!P || !Q || !fut) { free(P); free(Q); free(fut); return LRO_ENOMEM; } \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            /* reverse summary: carry k leaving the chunk's first step */      \
+            for (int64_t c = 0; c < nc; ++c) {                                 \
+                REAL prod = 1, k = 0;                                          \
+                int64_t hi = (c + 1) * C < T ? (c + 1) * C : T;                \
+                for (int64_t t = hi - 1; t >= c * C; --t) {                    \
+                    int64_t i = (bb * T + t) * D + d;                          \
+                    prod = a[i] * prod;                                        \
+                    k = a[i] * k + a[i] * grad_out[i];                         \
+                }                                                              \
+                P[c] = prod;                                                   \
+                Q[c] = k;                                                      \
+            }                                                                  \
+            /* serial exclusive prefix from the last chunk down */             \
+            REAL k = 0;                                                        \
+            for (int64_t c = nc - 1; c >= 0; --c) {                            \
+                fut[c] = k;                                                    \
+                k = P[c] * k + Q[c];                                           \
+            }                                                                  \
+            /* replay: the sequential reverse body inside every chunk */      \
+            for (int64_t c = 0; c < nc; ++c) {                                 \
+                REAL adj = fut[c];                                             \
+                int64_t hi = (c + 1) * C < T ? (c + 1) * C : T;                \
+                for (int64_t t = hi - 1; t >= c * C; --t) {                    \
+                    int64_t i = (bb * T + t) * D + d;                          \
+                    adj = adj + grad_out[i];                                   \
+                    REAL prev = (t > 0) ? out[i - D] : 0;                      \
+                    grad_a[i] = adj * prev;                                    \
+                    grad_b[i] = adj;                                           \
+                    adj = adj * a[i];                                          \
+                }                                                              \
+            }                                                                  \
+        }                                                                      \
+    }                                                                          \
+    free(P); free(Q); free(fut);                                               \
+    return LRO_OK;
+
+int lro_chunk_fwd_f32(const float *a, const float *b, float *out, float *last,
+                      int64_t B, int64_t T, int64_t D, int64_t C)
+{
+    if (bad_shape(B, T, D) || C <= 0) return LRO_EINVAL;
+    CHUNK_BODY_FWD(float, fmaf)
+}
+
+int lro_chunk_fwd_f64(const double *a, const double *b, double *out,
+                      double *last, int64_t B, int64_t T, int64_t D, int64_t C)
+{
+    if (bad_shape(B, T, D) || C <= 0) return LRO_EINVAL;
+    CHUNK_BODY_FWD(double, fma)
+}
+
+int lro_chunk_bwd_f32(const float *a, const float *out, const float *grad_out,
+                      float *grad_a, float *grad_b, int64_t B, int64_t T,
+                      int64_t D, int64_t C)
+{
+    if (bad_shape(B, T, D) || C <= 0) return LRO_EINVAL;
+    CHUNK_BODY_BWD(float)
+}
+
+int lro_chunk_bwd_f64(const double *a, const double *out,
+                      const double *grad_out, double *grad_a, double *grad_b,
+                      int64_t B, int64_t T, int64_t D, int64_t C)
+{
+    if (bad_shape(B, T, D) || C <= 0) return LRO_EINVAL;
+    CHUNK_BODY_BWD(double)
+}

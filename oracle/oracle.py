@@ -1,0 +1,185 @@
+"""Python face of the lrscan oracle -- TEST INFRASTRUCTURE ONLY.
+
+The oracle is the plain C statement of the diagonal linear-recurrence scan in
+``lrscan_oracle.c`` (forward h_t = a_t*h_{t-1} + b_t and its reverse-mode
+gradient, as defined by triton_training_scan.py, _real_forward and
+_real_backward).  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It never touches the
+CUDA library, and the CUDA library never touches it.
+
+Arrays are numpy, contiguous, shaped [B, T, D] (``last`` is [B, D]):
+  * ``"f32"``  -- float32 storage, fp32 state, fused multiply-add steps;
+  * ``"bf16"`` -- uint16 arrays holding bf16 bit patterns, fp32 state,
+                  round-to-nearest-even on every store;
+  * ``"f64"``  -- float64 storage and state.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lrscan_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liblrscan_oracle.so")
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+
+
+def compile_library(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc; returns the path of the shared object."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build() -> str:
+    """Build the oracle if the shared object is missing or older than its source."""
+    if (not os.path.exists(_LIB_PATH)
+            or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_library()
+    return _LIB_PATH
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    for name in ("lro_fwd_f32", "lro_fwd_bf16", "lro_fwd_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_bwd_f32", "lro_bwd_bf16", "lro_bwd_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_chunk_fwd_f32", "lro_chunk_fwd_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_chunk_bwd_f32", "lro_chunk_bwd_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    lib.lro_f32_to_bf16_array.argtypes = [_P, _P, _I64]
+    lib.lro_bf16_to_f32_array.argtypes = [_P, _P, _I64]
+    lib.lro_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.lro_f32_to_bf16.restype = ctypes.c_uint16
+    lib.lro_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.lro_bf16_to_f32.restype = ctypes.c_float
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle library.
+
+    ``path`` selects another build of the same source, which the mutation
+    tests use to check that the pins catch planted mistakes.
+    """
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+        return _lib
+
+
+_NP = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}
+_LAST = {"f32": np.float32, "bf16": np.float32, "f64": np.float64}
+
+
+def _c(x: np.ndarray, dtype: str) -> np.ndarray:
+    want = _NP[dtype]
+    if x.dtype != want:
+        raise TypeError(f"oracle {dtype} expects {np.dtype(want).name}, got {x.dtype}")
+    if x.ndim != 3:
+        raise ValueError("oracle expects [B, T, D] arrays")
+    return np.ascontiguousarray(x)
+
+
+def _ptr(x: np.ndarray) -> int:
+    return x.ctypes.data
+
+
+class Oracle:
+    """Bound view of one build of the oracle library."""
+
+    def __init__(self, lib: ctypes.CDLL | None = None):
+        self.lib = lib if lib is not None else load()
+
+    def fwd(self, a: np.ndarray, b: np.ndarray, dtype: str = "f32"):
+        """Sequential forward scan; returns ``(out, last)``."""
+        a, b = _c(a, dtype), _c(b, dtype)
+        if a.shape != b.shape:
+            raise ValueError("a and b must have the same [B, T, D] shape")
+        B, T, D = a.shape
+        out = np.empty_like(a)
+        last = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_fwd_{dtype}")(_ptr(a), _ptr(b), _ptr(out), _ptr(last), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle forward failed ({rc})")
+        return out, last
+
+    def bwd(self, a: np.ndarray, out: np.ndarray, grad_out: np.ndarray, dtype: str = "f32"):
+        """Sequential reverse scan; returns ``(grad_a, grad_b)``."""
+        a, out, grad_out = _c(a, dtype), _c(out, dtype), _c(grad_out, dtype)
+        if not (a.shape == out.shape == grad_out.shape):
+            raise ValueError("a, out and grad_out must have the same [B, T, D] shape")
+        B, T, D = a.shape
+        ga, gb = np.empty_like(a), np.empty_like(a)
+        rc = getattr(self.lib, f"lro_bwd_{dtype}")(_ptr(a), _ptr(out), _ptr(grad_out),
+                                                    _ptr(ga), _ptr(gb), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle backward failed ({rc})")
+        return ga, gb
+
+    def chunk_fwd(self, a: np.ndarray, b: np.ndarray, chunk: int, dtype: str = "f64"):
+        """Two-level (summary, serial prefix, replay) forward; ``(out, last)``."""
+        a, b = _c(a, dtype), _c(b, dtype)
+        B, T, D = a.shape
+        out = np.empty_like(a)
+        last = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_chunk_fwd_{dtype}")(_ptr(a), _ptr(b), _ptr(out), _ptr(last),
+                                                          B, T, D, chunk)
+        if rc:
+            raise RuntimeError(f"oracle chunk forward failed ({rc})")
+        return out, last
+
+    def chunk_bwd(self, a: np.ndarray, out: np.ndarray, grad_out: np.ndarray, chunk: int,
+                  dtype: str = "f64"):
+        """Two-level reverse scan; ``(grad_a, grad_b)``."""
+        a, out, grad_out = _c(a, dtype), _c(out, dtype), _c(grad_out, dtype)
+        B, T, D = a.shape
+        ga, gb = np.empty_like(a), np.empty_like(a)
+        rc = getattr(self.lib, f"lro_chunk_bwd_{dtype}")(_ptr(a), _ptr(out), _ptr(grad_out),
+                                                          _ptr(ga), _ptr(gb), B, T, D, chunk)
+        if rc:
+            raise RuntimeError(f"oracle chunk backward failed ({rc})")
+        return ga, gb
+
+    def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.uint16)
+        self.lib.lro_f32_to_bf16_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def bf16_to_f32(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        y = np.empty(x.shape, dtype=np.float32)
+        self.lib.lro_bf16_to_f32_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

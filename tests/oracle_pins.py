@@ -1,0 +1,420 @@
+"""Pins that tie the CPU oracle to facts other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when that build disagrees with something the definition of the scan or plain
+mathematics fixes: a hand-worked example, closed forms, exact rational brute
+force, finite differences, adjoint identities, the IEEE rounding contract and
+the padding contract.  ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutants.py`` runs them on builds with planted mistakes and
+checks that at least one of them fails for every mistake.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers --
+
+def read_golden(name: str) -> dict[str, np.ndarray]:
+    blocks: dict[str, list[list[float]]] = {}
+    cur = None
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if line.startswith("["):
+                cur = line.strip("[]")
+                blocks[cur] = []
+            else:
+                blocks[cur].append([float(x) for x in line.split()])
+    return {k: np.array(v, dtype=np.float64) for k, v in blocks.items()}
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _case(seed, B, T, D, lo=0.5, hi=0.999, dtype=np.float64):
+    r = _rng(seed)
+    a = r.uniform(lo, hi, (B, T, D)).astype(dtype)
+    b = r.standard_normal((B, T, D)).astype(dtype)
+    g = r.standard_normal((B, T, D)).astype(dtype)
+    return a, b, g
+
+
+# ------------------------------------------------------------ worked case --
+
+def pin_golden_worked_example(o):
+    """The hand-worked T=4, D=2 example, in every storage dtype, bit for bit."""
+    gd = read_golden("hand_worked_T4_D2.txt")
+    shape = (1, 4, 2)
+    for dt in ("f64", "f32", "bf16"):
+        if dt == "bf16":
+            enc = lambda x: o.f32_to_bf16(x.astype(np.float32)).reshape(shape)  # noqa: E731
+            dec = lambda x: o.bf16_to_f32(x).astype(np.float64)  # noqa: E731
+        else:
+            npdt = np.float64 if dt == "f64" else np.float32
+            enc = lambda x, npdt=npdt: x.astype(npdt).reshape(shape)  # noqa: E731
+            dec = lambda x: x.astype(np.float64)  # noqa: E731
+        a, b, g = enc(gd["a"]), enc(gd["b"]), enc(gd["grad_out"])
+        out, last = o.fwd(a, b, dt)
+        assert np.array_equal(dec(out).reshape(4, 2), gd["out"]), (dt, "out")
+        assert np.array_equal(last.astype(np.float64).reshape(1, 2), gd["last"]), (dt, "last")
+        ga, gb = o.bwd(a, out, g, dt)
+        assert np.array_equal(dec(gb).reshape(4, 2), gd["grad_b"]), (dt, "grad_b")
+        assert np.array_equal(dec(ga).reshape(4, 2), gd["grad_a"]), (dt, "grad_a")
+
+
+# ------------------------------------------------------------ closed forms --
+
+def pin_unit_decay_is_prefix_sum(o):
+    """a == 1: h is the running sum of b; g is the suffix sum of grad_out."""
+    r = _rng(1)
+    B, T, D = 2, 37, 5
+    b = r.integers(-8, 9, (B, T, D)).astype(np.float64)
+    g = r.integers(-8, 9, (B, T, D)).astype(np.float64)
+    a = np.ones((B, T, D))
+    for dt, npdt in (("f64", np.float64), ("f32", np.float32)):
+        out, last = o.fwd(a.astype(npdt), b.astype(npdt), dt)
+        assert np.array_equal(out.astype(np.float64), np.cumsum(b, axis=1)), dt
+        assert np.array_equal(last.astype(np.float64), b.sum(axis=1)), dt
+        ga, gb = o.bwd(a.astype(npdt), out, g.astype(npdt), dt)
+        suffix = np.flip(np.cumsum(np.flip(g, axis=1), axis=1), axis=1)
+        assert np.array_equal(gb.astype(np.float64), suffix), dt
+        prev = np.concatenate([np.zeros((B, 1, D)), np.cumsum(b, axis=1)[:, :-1]], axis=1)
+        assert np.array_equal(ga.astype(np.float64), suffix * prev), dt
+
+
+def pin_zero_decay_is_identity(o):
+    """a == 0: out = b, g = grad_out and grad_a_t = grad_out_t * b_{t-1}."""
+    a0, b, g = _case(2, 3, 11, 4)
+    a = np.zeros_like(a0)
+    for dt, npdt in (("f64", np.float64), ("f32", np.float32)):
+        bb, gg = b.astype(npdt), g.astype(npdt)
+        out, last = o.fwd(a.astype(npdt), bb, dt)
+        assert np.array_equal(out, bb), dt
+        assert np.array_equal(last, bb[:, -1, :]), dt
+        ga, gb = o.bwd(a.astype(npdt), out, gg, dt)
+        assert np.array_equal(gb, gg), dt
+        want = np.zeros_like(gg)
+        want[:, 1:] = gg[:, 1:] * bb[:, :-1]
+        assert np.array_equal(ga, want), dt
+
+
+def pin_constant_decay_geometric(o):
+    """a == c, b == 1: h_t = (1 - c^{t+1}) / (1 - c)."""
+    T = 200
+    for c in (0.3, 0.9, 0.999, -0.7):
+        a = np.full((1, T, 1), c)
+        b = np.ones((1, T, 1))
+        out, last = o.fwd(a, b, "f64")
+        t = np.arange(T)
+        want = (1.0 - c ** (t + 1)) / (1.0 - c)
+        np.testing.assert_allclose(out[0, :, 0], want, rtol=1e-12, atol=0)
+        assert abs(last[0, 0] - want[-1]) <= 1e-12 * abs(want[-1])
+
+
+def pin_constant_decay_direct_sum(o):
+    """a == c, general b: h_t = sum_{s<=t} c^{t-s} b_s (direct O(T^2) sum)."""
+    r = _rng(3)
+    T, D, c = 64, 3, 0.93
+    b = r.standard_normal((1, T, D))
+    a = np.full_like(b, c)
+    out, _ = o.fwd(a, b, "f64")
+    for t in range(T):
+        want = sum(c ** (t - s) * b[0, s] for s in range(t + 1))
+        np.testing.assert_allclose(out[0, t], want, rtol=1e-12, atol=1e-13)
+
+
+def pin_exact_rational_bruteforce(o):
+    """Varying a, dyadic inputs: exact rational h_t = sum_s (prod_{u=s+1..t} a_u) b_s
+    and exact gradients from their closed sums; the f64 oracle must match exactly."""
+    r = _rng(4)
+    B, T, D = 2, 7, 3
+    a = r.integers(-8, 9, (B, T, D)) / 8.0
+    b = r.integers(-16, 17, (B, T, D)) / 4.0
+    g = r.integers(-16, 17, (B, T, D)) / 4.0
+    out, last = o.fwd(a, b, "f64")
+    ga, gb = o.bwd(a, out, g, "f64")
+    for bb in range(B):
+        for d in range(D):
+            A = [Fraction(x) for x in a[bb, :, d]]
+            Bv = [Fraction(x) for x in b[bb, :, d]]
+            G = [Fraction(x) for x in g[bb, :, d]]
+
+            def span(lo, hi):          # prod_{u=lo..hi} a_u (empty -> 1)
+                p = Fraction(1)
+                for u in range(lo, hi + 1):
+                    p *= A[u]
+                return p
+            H = [sum(span(s + 1, t) * Bv[s] for s in range(t + 1)) for t in range(T)]
+            # dL/db_s = sum_{t>=s} grad_out_t * prod_{u=s+1..t} a_u
+            Gb = [sum(G[t] * span(s + 1, t) for t in range(s, T)) for s in range(T)]
+            # dL/da_s = (dL/db_s) * h_{s-1}
+            Ga = [Gb[s] * (H[s - 1] if s > 0 else 0) for s in range(T)]
+            for t in range(T):
+                assert Fraction(out[bb, t, d]) == H[t], ("h", bb, t, d)
+                assert Fraction(gb[bb, t, d]) == Gb[t], ("grad_b", bb, t, d)
+                assert Fraction(ga[bb, t, d]) == Ga[t], ("grad_a", bb, t, d)
+            assert Fraction(last[bb, d]) == H[-1]
+
+
+def pin_symbolic_small_T(o):
+    """T <= 4: expand the recurrence symbolically, differentiate, evaluate."""
+    import sympy as sp
+    r = _rng(5)
+    for T in (1, 2, 3, 4):
+        av = sp.symbols(f"a0:{T}")
+        bv = sp.symbols(f"b0:{T}")
+        gv = sp.symbols(f"g0:{T}")
+        h, hs = 0, []
+        for t in range(T):
+            h = av[t] * h + bv[t]
+            hs.append(sp.expand(h))
+        loss = sum(gv[t] * hs[t] for t in range(T))
+        a = r.uniform(-1.2, 1.2, (1, T, 1))
+        b = r.standard_normal((1, T, 1))
+        g = r.standard_normal((1, T, 1))
+        subs = {**{av[t]: a[0, t, 0] for t in range(T)},
+                **{bv[t]: b[0, t, 0] for t in range(T)},
+                **{gv[t]: g[0, t, 0] for t in range(T)}}
+        out, _ = o.fwd(a, b, "f64")
+        ga, gb = o.bwd(a, out, g, "f64")
+        for t in range(T):
+            assert abs(float(hs[t].subs(subs)) - out[0, t, 0]) <= 1e-12 * (1 + abs(out[0, t, 0]))
+            dla = float(sp.diff(loss, av[t]).subs(subs))
+            dlb = float(sp.diff(loss, bv[t]).subs(subs))
+            assert abs(dla - ga[0, t, 0]) <= 1e-12 * (1 + abs(dla)), ("grad_a", T, t)
+            assert abs(dlb - gb[0, t, 0]) <= 1e-12 * (1 + abs(dlb)), ("grad_b", T, t)
+
+
+# ------------------------------------------------------------ derivatives --
+
+def pin_finite_difference_jacobian(o):
+    """Central differences of L = sum grad_out*h against the backward (fp64)."""
+    a, b, g = _case(6, 2, 8, 3, lo=-0.95, hi=0.95)
+    out, _ = o.fwd(a, b, "f64")
+    ga, gb = o.bwd(a, out, g, "f64")
+    eps = 1e-6
+
+    def loss(aa, bb):
+        h, _ = o.fwd(aa, bb, "f64")
+        return float(np.sum(g * h))
+    for idx in np.ndindex(a.shape):
+        ap, am = a.copy(), a.copy()
+        ap[idx] += eps
+        am[idx] -= eps
+        fd_a = (loss(ap, b) - loss(am, b)) / (2 * eps)
+        bp, bm = b.copy(), b.copy()
+        bp[idx] += eps
+        bm[idx] -= eps
+        fd_b = (loss(a, bp) - loss(a, bm)) / (2 * eps)
+        assert abs(fd_a - ga[idx]) <= 1e-7 * (1 + abs(fd_a)), ("grad_a", idx, fd_a, ga[idx])
+        assert abs(fd_b - gb[idx]) <= 1e-7 * (1 + abs(fd_b)), ("grad_b", idx, fd_b, gb[idx])
+
+
+def pin_adjoint_dot_products(o):
+    """<grad_out, J_b v> = <grad_b, v> and <grad_out, J_a u> = <grad_a, u>.
+
+    The scan is linear in b, so J_b v = scan(a, v); the tangent of a in
+    direction u is scan(a, u * h_{t-1})."""
+    a, b, g = _case(7, 3, 50, 4)
+    r = _rng(8)
+    v = r.standard_normal(a.shape)
+    u = r.standard_normal(a.shape)
+    out, _ = o.fwd(a, b, "f64")
+    ga, gb = o.bwd(a, out, g, "f64")
+    jv, _ = o.fwd(a, v, "f64")
+    lhs, rhs = np.sum(g * jv), np.sum(gb * v)
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(lhs))
+    hprev = np.concatenate([np.zeros_like(out[:, :1]), out[:, :-1]], axis=1)
+    ju, _ = o.fwd(a, u * hprev, "f64")
+    lhs, rhs = np.sum(g * ju), np.sum(ga * u)
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(lhs))
+
+
+def pin_linearity_in_b(o):
+    a, b1, b2 = _case(9, 2, 40, 3)
+    o1, _ = o.fwd(a, b1, "f64")
+    o2, _ = o.fwd(a, b2, "f64")
+    o3, _ = o.fwd(a, 2.5 * b1 - 0.75 * b2, "f64")
+    np.testing.assert_allclose(o3, 2.5 * o1 - 0.75 * o2, rtol=1e-11, atol=1e-12)
+
+
+def pin_reverse_scan_identity(o):
+    """grad_b is the forward scan of reversed grad_out with decays shifted by one
+    (A'_s = a_{T-s}, A'_0 = 0): bit for bit in fp32, because each reverse step
+    is the same single-rounding fused step as a forward step."""
+    a, _, g = _case(10, 3, 33, 5, dtype=np.float32)
+    out = np.zeros_like(a)
+    ga, gb = o.bwd(a, out, g, "f32")
+    ra = np.zeros_like(a)
+    ra[:, 1:] = np.flip(a, axis=1)[:, :-1]
+    h, _ = o.fwd(ra, np.ascontiguousarray(np.flip(g, axis=1)), "f32")
+    assert np.array_equal(np.flip(h, axis=1), gb)
+    assert np.array_equal(ga, np.zeros_like(ga))
+
+
+# ------------------------------------------------------ rounding contract --
+
+def _f32_midpoint(x64: np.ndarray) -> np.ndarray:
+    """True where a float64 value lies exactly halfway between two float32s."""
+    lo = x64.astype(np.float32)
+    other = np.nextafter(lo, np.where(x64 > lo, np.float32(np.inf), np.float32(-np.inf)))
+    return (lo.astype(np.float64) + other.astype(np.float64)) / 2 == x64
+
+
+def pin_f32_single_rounding_steps(o):
+    """Every fp32 step is the correctly rounded value of a_t*h_{t-1} + b_t
+    (and of a_{t+1}*g_{t+1} + grad_out_t), i.e. one fused rounding.
+
+    The float64 evaluation of a*h (exact) + b can be off the exact value only
+    where it lands exactly on an fp32 midpoint; such points are skipped."""
+    a, b, g = _case(11, 2, 300, 16, lo=0.3, hi=1.05, dtype=np.float32)
+    out, _ = o.fwd(a, b, "f32")
+    prev = np.concatenate([np.zeros_like(out[:, :1]), out[:, :-1]], axis=1)
+    exact = a.astype(np.float64) * prev.astype(np.float64) + b.astype(np.float64)
+    ok = ~_f32_midpoint(exact)
+    assert np.array_equal(out[ok], exact.astype(np.float32)[ok])
+    ga, gb = o.bwd(a, out, g, "f32")
+    nxt = np.concatenate([gb[:, 1:], np.zeros_like(gb[:, :1])], axis=1)
+    anext = np.concatenate([a[:, 1:], np.zeros_like(a[:, :1])], axis=1)
+    exact = anext.astype(np.float64) * nxt.astype(np.float64) + g.astype(np.float64)
+    ok = ~_f32_midpoint(exact)
+    assert np.array_equal(gb[ok], exact.astype(np.float32)[ok])
+    prod = (gb.astype(np.float64) * prev.astype(np.float64))
+    ok = ~_f32_midpoint(prod)
+    assert np.array_equal(ga[ok], prod.astype(np.float32)[ok])
+
+
+def pin_bf16_rne_against_torch(o):
+    """fp32 -> bf16 narrowing is IEEE round-to-nearest-even, as torch's cast."""
+    import torch
+    r = _rng(12)
+    vals = np.concatenate([
+        r.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        (r.standard_normal(5000) * 1e-38).astype(np.float32),      # subnormal range
+        (r.standard_normal(5000) * 1e37).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 3.3895314e38, -3.3895314e38,
+                  1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9,
+                  -(1.0 + 2.0 ** -8), 2.0 ** -133, 2.0 ** -149, 65504.0],
+                 dtype=np.float32),
+    ])
+    # exact halfway cases between neighbouring bf16 values
+    base = (r.integers(0, 0x7f00, 4000).astype(np.uint32) << 16)
+    half = (base | 0x8000).view(np.float32)
+    vals = np.concatenate([vals, half, -half])
+    mine = o.f32_to_bf16(vals)
+    ref = torch.from_numpy(vals.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mine, ref)
+    nan = o.f32_to_bf16(np.array([np.nan], dtype=np.float32))
+    assert np.isnan(o.bf16_to_f32(nan)).all()
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    widened = o.bf16_to_f32(bits)
+    ref_w = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    fin = np.isfinite(ref_w)
+    assert np.array_equal(widened[fin], ref_w[fin])
+
+
+def pin_bf16_storage_is_fp32_state(o):
+    """bf16 storage changes only what is stored: the bf16 oracle equals the fp32
+    oracle on widened inputs with its stores rounded to nearest even."""
+    a, b, g = _case(13, 2, 97, 24, lo=0.8, hi=0.999, dtype=np.float32)
+    a16, b16, g16 = o.f32_to_bf16(a), o.f32_to_bf16(b), o.f32_to_bf16(g)
+    out16, last16 = o.fwd(a16, b16, "bf16")
+    out32, last32 = o.fwd(o.bf16_to_f32(a16), o.bf16_to_f32(b16), "f32")
+    assert np.array_equal(out16, o.f32_to_bf16(out32))
+    assert np.array_equal(last16, last32)
+    ga16, gb16 = o.bwd(a16, out16, g16, "bf16")
+    ga32, gb32 = o.bwd(o.bf16_to_f32(a16), o.bf16_to_f32(out16), o.bf16_to_f32(g16), "f32")
+    assert np.array_equal(ga16, o.f32_to_bf16(ga32))
+    assert np.array_equal(gb16, o.f32_to_bf16(gb32))
+
+
+# ------------------------------------------------- decomposition algebra --
+
+def pin_chunked_equals_sequential(o):
+    """The two-level decomposition reaches the sequential result: to rounding
+    in fp64 for any chunk length (ragged last chunk included), bit for bit in
+    fp32 forward when C = 1 or C >= T."""
+    a, b, g = _case(14, 2, 150, 6, lo=0.6, hi=1.0)
+    out, last = o.fwd(a, b, "f64")
+    ga, gb = o.bwd(a, out, g, "f64")
+    for C in (1, 7, 16, 64, 150, 400):
+        co, cl = o.chunk_fwd(a, b, C, "f64")
+        np.testing.assert_allclose(co, out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(cl, last, rtol=1e-12, atol=1e-12)
+        cga, cgb = o.chunk_bwd(a, out, g, C, "f64")
+        np.testing.assert_allclose(cgb, gb, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(cga, ga, rtol=1e-12, atol=1e-12)
+    a32, b32 = a.astype(np.float32), b.astype(np.float32)
+    out32, last32 = o.fwd(a32, b32, "f32")
+    for C in (1, 150, 1000):
+        co, cl = o.chunk_fwd(a32, b32, C, "f32")
+        assert np.array_equal(co, out32), C
+        assert np.array_equal(cl, last32), C
+
+
+# ------------------------------------------------------------ padding ------
+
+def pin_identity_padding_bit_exact(o):
+    """Identity steps (a=1, b=0, grad_out=0) after a row's valid length carry
+    the state bit for bit: last == out[L-1], out[t>=L] == out[L-1]; the
+    gradients there are exactly zero."""
+    r = _rng(15)
+    B, T, D = 6, 40, 8
+    a, b, g = _case(16, B, T, D, dtype=np.float32)
+    L = r.integers(1, T + 1, B)
+    L[0] = T
+    for bb in range(B):
+        a[bb, L[bb]:] = 1.0
+        b[bb, L[bb]:] = 0.0
+        g[bb, L[bb]:] = 0.0
+    for dt in ("f32", "bf16"):
+        aa, bb_, gg = (a, b, g) if dt == "f32" else (o.f32_to_bf16(a), o.f32_to_bf16(b),
+                                                        o.f32_to_bf16(g))
+        out, last = o.fwd(aa, bb_, dt)
+        ga, gb = o.bwd(aa, out, gg, dt)
+        for bb in range(B):
+            n = L[bb]
+            ref = out[bb, n - 1]
+            assert np.array_equal(out[bb, n:], np.broadcast_to(ref, out[bb, n:].shape))
+            if dt == "f32":
+                assert np.array_equal(last[bb], ref)
+            else:
+                assert np.array_equal(o.f32_to_bf16(last[bb]), ref)
+            dec = (lambda x: x) if dt == "f32" else o.bf16_to_f32
+            assert not np.any(dec(gb[bb, n:]))      # +0 or -0 only
+            assert not np.any(dec(ga[bb, n:]))
+
+
+def pin_rows_are_independent(o):
+    """Each batch row starts from h = 0: row results do not depend on the others."""
+    a, b, g = _case(17, 4, 25, 3)
+    out, last = o.fwd(a, b, "f64")
+    ga, gb = o.bwd(a, out, g, "f64")
+    for bb in range(4):
+        o1, l1 = o.fwd(a[bb:bb + 1], b[bb:bb + 1], "f64")
+        assert np.array_equal(o1[0], out[bb]) and np.array_equal(l1[0], last[bb])
+        a1, b1 = o.bwd(a[bb:bb + 1], out[bb:bb + 1], g[bb:bb + 1], "f64")
+        assert np.array_equal(a1[0], ga[bb]) and np.array_equal(b1[0], gb[bb])
+
+
+def pin_empty_shapes(o):
+    """Empty inputs are valid: no output, and last = h_{-1} = 0 when T == 0."""
+    for shape in ((0, 5, 3), (2, 0, 3), (2, 5, 0)):
+        a = np.zeros(shape)
+        out, last = o.fwd(a, a, "f64")
+        assert out.shape == shape and last.shape == (shape[0], shape[2])
+        if shape[1] == 0:
+            assert not np.any(last)
+        o.bwd(a, a, a, "f64")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

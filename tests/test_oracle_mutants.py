@@ -1,0 +1,70 @@
+"""The pins must bite: each planted mistake in a copy of the oracle's C source
+(a dropped term, a wrong index, a sign, a wrong rounding, a missing reset, an
+inclusive-for-exclusive prefix) has to make at least one pin fail.
+
+Mistakes are planted in a temporary copy of the source, on the CPU, never in
+the oracle that the other tests use.
+"""
+import os
+
+import pytest
+
+import oracle_pins
+from oracle import Oracle, load
+from oracle.oracle import _SRC, compile_library
+
+MUTANTS = {
+    "fwd_f64_drops_b": ("h[d] = fma(a[i], h[d], b[i]);", "h[d] = a[i] * h[d];"),
+    "fwd_f64_no_row_reset": ("for (int64_t d = 0; d < D; ++d) h[d] = 0.0;\n", "\n"),
+    "fwd_f32_two_roundings": ("h[d] = fmaf(a[i], h[d], b[i]);", "h[d] = a[i] * h[d] + b[i];"),
+    "bwd_f64_uses_a_t": ("g[d] = fma(a[i + D], g[d], grad_out[i]);",
+                         "g[d] = fma(a[i], g[d], grad_out[i]);"),
+    "bwd_f64_uses_h_t": ("double h_prev = (t > 0) ? out[i - D] : 0.0;",
+                         "double h_prev = out[i];"),
+    "bwd_f64_sign": ("grad_a[i] = g[d] * h_prev;\n            }\n        }\n    }\n    free(g);\n"
+                     "    return LRO_OK;\n}\n\n/* ---",
+                     "grad_a[i] = -g[d] * h_prev;\n            }\n        }\n    }\n    free(g);\n"
+                     "    return LRO_OK;\n}\n\n/* ---"),
+    "bwd_f32_drops_carry": ("g[d] = fmaf(a[i + D], g[d], grad_out[i]); /* a_{t+1} */",
+                            "g[d] = grad_out[i];"),
+    "bf16_round_half_up": ("u += 0x7fffu + keep_lsb;", "u += 0x8000u;"),
+    "bf16_bwd_prev_from_state": ("float h_prev = (t > 0) ? lro_bf16_to_f32(out[i - D]) : 0.0f;",
+                                 "float h_prev = (t > 0) ? lro_bf16_to_f32(out[i]) : 0.0f;"),
+    "chunk_prefix_inclusive": ("hin[c] = state;                                                \\\n"
+                               "                state = FMA(P[c], state, Q[c]);",
+                               "state = FMA(P[c], state, Q[c]);                                \\\n"
+                               "                hin[c] = state;"),
+    "chunk_reverse_summary_drops_direct": ("k = a[i] * k + a[i] * grad_out[i];", "k = a[i] * k;"),
+}
+
+
+def _run_all_pins(o):
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        if pin.__name__ == "pin_symbolic_small_T":
+            try:
+                import sympy  # noqa: F401
+            except ImportError:
+                continue
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(src.replace(old, new))
+    so = compile_library(str(mutant_src), str(tmp_path / "libmutant.so"))
+    failed = _run_all_pins(Oracle(load(so)))
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    so = compile_library(_SRC, str(tmp_path / "libcopy.so"))
+    assert _run_all_pins(Oracle(load(so))) == []
