@@ -1,0 +1,409 @@
+"""Benchmark of the diagonal linear-recurrence scan (forward + backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+
+One step = one forward scan and one backward scan over one batch of the
+workload (default: the gated bf16 workload, B=8 T=2048 D=2560, bf16 storage,
+fp32 state).  Inputs are resident in HBM before the timed region.  Three
+independent buffer sets rotate so that no kernel reads what the previous
+kernels left in L2 (each set is larger than a third of the 126 MB L2 and
+the rotation touches 3x that between reuses).
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas: the scan's lanes shard with
+no exchange), and the value is the whole job's elements/s over the slowest
+rank's time.
+
+`--impl reference` times the CPU oracle (the reference arm) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scan fwd+bwd elements/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def algorithmic_bytes(w) -> tuple[int, int]:
+    """Forward reads a, b and writes out (+ the fp32 final state); backward
+    reads a, out, grad_out and writes grad_a, grad_b."""
+    E, s = w.elements, w.storage_bytes
+    return 3 * E * s + 4 * w.B * w.D, 5 * E * s
+
+
+# --------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """Samples nvidia-smi during the timed region (SM clock, reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ reference ----
+def run_reference(args, w) -> dict:
+    """The CPU oracle on the host cores: the reference arm of this benchmark."""
+    import numpy as np
+
+    import oracle
+    from linear_recurrence_scan_lrscan_gb300.workloads import make_inputs, to_numpy_storage
+
+    o = oracle.default()
+    # A bounded sample: whole batch rows of the workload, every step of T,
+    # a slice of the lanes sized for about a second of single-core work per step.
+    lanes = max(1, min(w.D, int(args.ref_elements // max(1, w.T))))
+    inp = make_inputs(w.cid, B=1, D=lanes)
+    a, b, g = (to_numpy_storage(inp[k]) for k in ("a", "b", "grad_out"))
+    E = a.size
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        out, _ = o.fwd(a, b, w.dtype)
+        o.bwd(a, out, g, w.dtype)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_step = sum(times) / len(times)
+    value = E / per_step
+    sample = f"B=1 T={w.T} D={lanes} of {w.describe()} (fwd+bwd, single thread)"
+    return {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "elements/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": config_of(w, None, None),
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(w, seconds: float = 12.0) -> dict:
+    """The oracle as it stands, single-threaded, on a bounded sample."""
+    import oracle
+    from linear_recurrence_scan_lrscan_gb300.workloads import make_inputs, to_numpy_storage
+
+    o = oracle.default()
+    lanes = max(1, min(w.D, 2_000_000 // max(1, w.T)))
+    inp = make_inputs(w.cid, B=1, D=lanes)
+    a, b, g = (to_numpy_storage(inp[k]) for k in ("a", "b", "grad_out"))
+    E = a.size
+    t_end = time.perf_counter() + seconds
+    n, t_tot = 0, 0.0
+    while n < 3 or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        out, _ = o.fwd(a, b, w.dtype)
+        o.bwd(a, out, g, w.dtype)
+        t_tot += time.perf_counter() - t0
+        n += 1
+    return {"value": E * n / t_tot, "unit": "elements/s", "cores": 1, "kind": "oracle",
+            "sample": f"B=1 T={w.T} D={lanes} of {w.describe()}, fwd+bwd, {n} repetitions, single thread"}
+
+
+def config_of(w, pf, pb) -> dict:
+    c = {"workload": w.describe(), "B": w.B, "T": w.T, "D": w.D, "storage": w.dtype, "state": "f32",
+         "elements_per_step": w.elements,
+         "l2": "three rotating buffer sets; every kernel's inputs were last touched >= 2 kernels "
+               "(> 126 MB of traffic) earlier"}
+    if w.chunk:
+        c["chunk"] = w.chunk
+    if pf is not None:
+        c["fwd_kernel"] = pf["name"]
+        c["bwd_kernel"] = pb["name"]
+    return c
+
+
+# ------------------------------------------------------------------ ours ----
+def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    from linear_recurrence_scan_lrscan_gb300.workloads import make_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    inp = make_inputs(w.cid)
+    a_h, b_h, g_h = inp["a"], inp["b"], inp["grad_out"]
+    opts = {}
+    if args.path:
+        opts["path"] = args.path
+    if args.variant:
+        opts["tile_variant"] = args.variant
+    if w.chunk and args.path == "chunk":
+        opts["chunk_len"] = w.chunk
+    pf = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", **opts)
+    pb = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", **opts)
+
+    nsets = 3
+    sets = []
+    for i in range(nsets):
+        a = a_h.to(dev)
+        b = b_h.to(dev)
+        g = g_h.to(dev)
+        sets.append({"a": a, "b": b, "g": g, "out": torch.empty_like(a), "ga": torch.empty_like(a),
+                     "gb": torch.empty_like(a),
+                     "last": torch.empty(w.B, w.D, device=dev, dtype=torch.float32)})
+    for s in sets:   # every set holds a valid forward output before the loop
+        L.lrscan_fwd(s["a"], s["b"], s["out"], s["last"], **opts)
+    torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        f = sets[i % nsets]
+        bset = sets[(i + nsets - 1) % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
+        if ev is not None:
+            ev[1].record(stream)
+        L.lrscan_bwd(bset["a"], bset["out"], bset["g"], bset["ga"], bset["gb"], **opts)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert L.lrscan_sync_check() == 0
+
+    # device-timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[dev.index]))
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    rc = L.lrscan_sync_check()
+    if rc != 0:
+        raise RuntimeError(f"device error during the timed region: {rc}")
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if dist is not None:
+        t = torch.tensor([total_ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_ms, bwd_ms = t.tolist()
+    ms_per_step = total_ms / args.steps
+
+    # end to end: host (pinned) inputs -> device -> fwd+bwd -> host outputs
+    e2e = None
+    if not args.no_e2e:
+        pa, pbuf, pg = a_h.pin_memory(), b_h.pin_memory(), g_h.pin_memory()
+        ho = torch.empty_like(pa).pin_memory()
+        hga, hgb = torch.empty_like(pa).pin_memory(), torch.empty_like(pa).pin_memory()
+        hl = torch.empty(w.B, w.D, dtype=torch.float32).pin_memory()
+        s0 = sets[0]
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            s0["a"].copy_(pa, non_blocking=True)
+            s0["b"].copy_(pbuf, non_blocking=True)
+            s0["g"].copy_(pg, non_blocking=True)
+            L.lrscan_fwd(s0["a"], s0["b"], s0["out"], s0["last"], **opts)
+            L.lrscan_bwd(s0["a"], s0["out"], s0["g"], s0["ga"], s0["gb"], **opts)
+            ho.copy_(s0["out"], non_blocking=True)
+            hl.copy_(s0["last"], non_blocking=True)
+            hga.copy_(s0["ga"], non_blocking=True)
+            hgb.copy_(s0["gb"], non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = t.item()
+        s = w.storage_bytes
+        e2e = {"value": world * w.elements / (e2e_ms * 1e-3), "unit": "elements/s",
+               "h2d_bytes_per_step": 3 * w.elements * s,
+               "d2h_bytes_per_step": 3 * w.elements * s + 4 * w.B * w.D,
+               "ms_per_step": e2e_ms,
+               "path": "pinned host -> device copies, lrscan_fwd + lrscan_bwd (C ABI), device -> pinned host"}
+        assert L.lrscan_sync_check() == 0
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    bf, bb = algorithmic_bytes(w)
+    gbs_f = bf / (fwd_ms * 1e-3) / 1e9
+    gbs_b = bb / (bwd_ms * 1e-3) / 1e9
+    dominant = ("bwd", bb, bwd_ms, gbs_b) if bwd_ms >= fwd_ms else ("fwd", bf, fwd_ms, gbs_f)
+    traffic = load_traffic(w, dominant[0], pb["name"] if dominant[0] == "bwd" else pf["name"])
+    line = {
+        "metric": METRIC,
+        "value": world * w.elements / (ms_per_step * 1e-3),
+        "unit": "elements/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config_of(w, pf, pb),
+        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]}:{(pb if dominant[0] == 'bwd' else pf)['name']}",
+                     "achieved": dominant[3], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": dominant[3] / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "algorithmic_bytes_per_launch": dominant[1], "traffic": traffic},
+        "fwd": {"ms": fwd_ms, "GB/s": gbs_f, "frac": gbs_f / peaks["hbm_gbs"],
+                "elements/s": w.elements / (fwd_ms * 1e-3), "kernel": pf["name"], "path": pf["path"]},
+        "bwd": {"ms": bwd_ms, "GB/s": gbs_b, "frac": gbs_b / peaks["hbm_gbs"],
+                "elements/s": w.elements / (bwd_ms * 1e-3), "kernel": pb["name"], "path": pb["path"]},
+        "step_GB/s": (bf + bb) / (ms_per_step * 1e-3) / 1e9,
+        "gpu_launches": args.steps * (pf["kernels"] + pb["kernels"]),
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+def load_traffic(w, direction: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if one exists for
+    this exact kernel and workload (profiles/traffic.json)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    key = f"{w.name}:{direction}:{kernel}"
+    return d.get(key)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, help="workload id 1..5 (default 2)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default=None, choices=[None, "auto", "seq", "window", "chunk", "plain"])
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-elements", type=float, default=2e6)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.config]
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, w, rank, world, dist)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * lrscan -- differentiable diagonal linear-recurrence scan on NVIDIA GB300
+ * (sm_103a).  C ABI of liblrscan.so.
+ *
+ * The operation (triton_training_scan.py, _real_forward / _real_backward;
+ * same definition in the scan's design notes): for every batch row b and
+ * channel lane d of contiguous [B, T, D] tensors (D fastest; element
+ * (b, t, d) at offset (b*T + t)*D + d),
+ *
+ *   forward   h_{-1} = 0,  h_t = a_t * h_{t-1} + b_t            t = 0..T-1
+ *             out[b,t,d] = h_t (in the storage dtype), last[b,d] = h_{T-1} (fp32)
+ *
+ *   backward  with the loss L = sum_t grad_out_t * h_t and h read back from out:
+ *             g_{T-1} = grad_out_{T-1},  g_t = grad_out_t + a_{t+1} * g_{t+1}
+ *             grad_b[b,t,d] = g_t,  grad_a[b,t,d] = g_t * out[b,t-1,d]  (0 at t=0)
+ *
+ * State and accumulation are fp32 whatever the storage dtype; each
+ * recurrence step is one fused multiply-add (one rounding); stores to bf16
+ * round to nearest even.  The sequential paths reproduce that order
+ * exactly; the chunked and windowed paths reassociate the recurrence through
+ * affine maps h -> P*h + Q (triton_training_scan.py, _real_chunk_summary,
+ * _real_chunk_prefix, _real_chunk_replay and the _real_reverse_* mirror) and
+ * agree to rounding.
+ *
+ * Common rules for every entry point below:
+ *   - All tensor pointers are caller-owned DEVICE pointers (cudaMalloc,
+ *     torch, ...) on the calling thread's current CUDA device, contiguous
+ *     [B, T, D]; `last` is contiguous [B, D] fp32.  The library never frees
+ *     or keeps them after the call's kernels finish.
+ *   - Outputs must not overlap inputs or each other (undefined otherwise).
+ *   - B, T, D >= 0.  An empty problem is valid: nothing is written, except
+ *     that T == 0 with B*D > 0 sets last to 0 (h_{-1}).  Pointers may be NULL
+ *     when the problem is empty; otherwise every pointer but `last` (forward,
+ *     optional) must be non-NULL.
+ *   - Calls are asynchronous on the selected stream (see lrscan_set_stream).
+ *     A return of LRSCAN_OK means the kernels were launched; errors found on
+ *     the device (a bounded wait that gave up) are reported by the next call
+ *     to lrscan_sync_check().
+ *   - Any pointer alignment and any D are accepted.  Rows that are 16-byte
+ *     aligned (D*sizeof(storage) % 16 == 0 and 16-byte aligned base
+ *     pointers) take the bulk-copy (TMA) paths; others take plain-load
+ *     kernels.
+ *   - Return value: LRSCAN_OK (0) or one of the negative codes below.
+ */
+#ifndef LRSCAN_H
+#define LRSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LRSCAN_VERSION 1
+
+/* error codes */
+#define LRSCAN_OK            0
+#define LRSCAN_EINVAL       (-1)  /* NULL required pointer, negative size, byte size overflow, bad option */
+#define LRSCAN_EDTYPE       (-2)  /* dtype is not LRSCAN_F32 or LRSCAN_BF16 */
+#define LRSCAN_ECUDA        (-3)  /* a CUDA runtime call or kernel launch failed */
+#define LRSCAN_ENOMEM       (-4)  /* the chunked path's workspace could not be allocated / is too small */
+#define LRSCAN_ETIMEOUT     (-5)  /* a bounded device wait gave up (reported by lrscan_sync_check) */
+#define LRSCAN_ENODEVICE    (-6)  /* no usable sm_103 device is current */
+
+/* storage dtypes: applies to a, b, out, grad_out, grad_a, grad_b (last is always fp32) */
+#define LRSCAN_F32   0
+#define LRSCAN_BF16  1
+
+/* execution paths (lrscan_opts.path) */
+#define LRSCAN_PATH_AUTO    0  /* occupancy rule picks one of the below */
+#define LRSCAN_PATH_SEQ     1  /* register-resident sequential-in-T, bulk-copied time tiles */
+#define LRSCAN_PATH_CHUNK   2  /* three phases: chunk summary -> warp-shuffle prefix -> replay */
+#define LRSCAN_PATH_WINDOW  3  /* single pass: time windows in shared memory, split in time inside the CTA */
+#define LRSCAN_PATH_PLAIN   4  /* sequential, plain loads; any alignment */
+
+typedef struct lrscan_opts {
+    int path;               /* LRSCAN_PATH_*; 0 = auto */
+    int chunk_len;          /* chunked path: 16, 32 or 64; 0 = 64 */
+    void *workspace;        /* chunked path: optional caller-owned device workspace ... */
+    size_t workspace_bytes; /* ... of at least lrscan_workspace_bytes() bytes; NULL = library-owned */
+    int tile_variant;       /* >= 1 forces one kernel tile variant of the path (lrscan_plan lists them); 0 = auto */
+} lrscan_opts;
+
+/* What the dispatcher chose (filled by lrscan_plan). */
+typedef struct lrscan_plan_info {
+    int path;               /* LRSCAN_PATH_* actually taken */
+    int tile_variant;       /* variant id within the path */
+    int lanes_per_cta;      /* channel lanes one CTA owns */
+    int rows_per_window;    /* time steps per shared-memory window (SEQ/WINDOW) or chunk length (CHUNK) */
+    int subchunks;          /* time splits inside a window (WINDOW), 1 otherwise */
+    int stages;             /* shared-memory pipeline depth */
+    int ctas;               /* CTAs of the main kernel */
+    int threads_per_cta;
+    int smem_bytes;         /* dynamic shared memory per CTA */
+    int kernels;            /* kernel launches per call */
+    size_t workspace_bytes; /* device workspace the call needs */
+    char name[64];          /* variant name */
+} lrscan_plan_info;
+
+/*
+ * Forward scan.  a, b: [B,T,D] inputs; out: [B,T,D] output (every h_t);
+ * last: [B,D] fp32 final state h_{T-1}, or NULL to skip it.
+ * Runs on the thread's current stream (lrscan_set_stream).
+ */
+int lrscan_fwd(const void *a, const void *b, void *out, float *last,
+               int64_t B, int64_t T, int64_t D, int dtype);
+
+/*
+ * Backward scan.  a: [B,T,D] forward decays; out: [B,T,D] forward output
+ * (h_{t-1} is read from it); grad_out: [B,T,D] dL/dout; grad_a, grad_b:
+ * [B,T,D] outputs dL/da, dL/db.  b is not needed.  No gradient flows into
+ * `last` or into an initial state (there is none).
+ */
+int lrscan_bwd(const void *a, const void *out, const void *grad_out,
+               void *grad_a, void *grad_b,
+               int64_t B, int64_t T, int64_t D, int dtype);
+
+/* As above with an explicit stream (cudaStream_t; NULL = the thread's
+ * current stream) and options (NULL = defaults). */
+int lrscan_fwd_ex(const void *a, const void *b, void *out, float *last,
+                  int64_t B, int64_t T, int64_t D, int dtype,
+                  void *stream, const lrscan_opts *opts);
+int lrscan_bwd_ex(const void *a, const void *out, const void *grad_out,
+                  void *grad_a, void *grad_b,
+                  int64_t B, int64_t T, int64_t D, int dtype,
+                  void *stream, const lrscan_opts *opts);
+
+/* Sets the calling thread's stream (a cudaStream_t; NULL = legacy default
+ * stream) used by lrscan_fwd / lrscan_bwd and by _ex calls given NULL. */
+int lrscan_set_stream(void *stream);
+
+/* Device bytes the chunked path needs for this shape (two fp32 [B, ceil(T/C), D]
+ * buffers); chunk_len 0 means 64.  Other paths need none. */
+size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len);
+
+/* Host-only: what a call with these arguments would run (no launch, no
+ * device memory touched beyond reading device attributes).  dir: 0 forward,
+ * 1 backward.  aligned16: whether the call's pointers are 16-byte aligned. */
+int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
+                const lrscan_opts *opts, lrscan_plan_info *info);
+
+/* Number of tile variants of a path (for sweeps); names via lrscan_plan. */
+int lrscan_num_variants(int path, int dtype, int dir);
+
+/* Waits for the thread's current stream, then returns and clears the first
+ * error any kernel of this library recorded on the current device since the
+ * last check (LRSCAN_ETIMEOUT for a wait that gave up), else the stream's
+ * CUDA error as LRSCAN_ECUDA, else LRSCAN_OK. */
+int lrscan_sync_check(void);
+
+/* Limit on every bounded device-side wait, in nanoseconds (default 1e9).
+ * Applies to launches made after the call, on every device. */
+int lrscan_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the bounded wait: launches one CTA that waits, with the given
+ * limit, on a shared-memory barrier that nothing will ever complete.  The
+ * wait must give up, record LRSCAN_ETIMEOUT and return; this call
+ * synchronizes and returns what lrscan_sync_check() reports (so
+ * LRSCAN_ETIMEOUT is the expected, healthy result). */
+int lrscan_selftest_wait_timeout(uint64_t timeout_ns);
+
+/* Human-readable text for an error code (static storage). */
+const char *lrscan_strerror(int code);
+
+int lrscan_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRSCAN_H */

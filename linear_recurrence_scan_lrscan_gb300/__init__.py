@@ -1,0 +1,24 @@
+"""GB300-native differentiable diagonal linear-recurrence scan.
+
+    h_t = a_t * h_{t-1} + b_t          (forward, h_{-1} = 0)
+    g_t = grad_out_t + a_{t+1} g_{t+1} (backward; grad_b = g, grad_a = g * h_{t-1})
+
+The compute path is liblrscan.so (hand-written sm_103a CUDA kernels behind a C
+ABI, ``include/lrscan.h``); ``lrscan`` is its Python binding.  Importing this
+package does not load the library; the first call does, and fails loudly if
+it has not been built.
+"""
+from .lrscan import (  # noqa: F401
+    LinearRecurrenceScan,
+    LrscanError,
+    LrscanUnavailable,
+    lrscan_bwd,
+    lrscan_fwd,
+    lrscan_num_variants,
+    lrscan_plan,
+    lrscan_selftest_wait_timeout,
+    lrscan_set_wait_timeout_ns,
+    lrscan_sync_check,
+    lrscan_workspace_bytes,
+    scan,
+)

@@ -1,0 +1,320 @@
+// Three-phase chunked scan (triton_training_scan.py, _real_chunk_summary /
+// _real_chunk_prefix / _real_chunk_replay and the _real_reverse_* mirror),
+// for shapes whose B*D lanes are too few to fill the GPU with a sequential
+// walk: time is cut into chunks of C steps and every (row, chunk, lane) is
+// an independent thread in phases 1 and 3.
+//
+//   phase 1  summary: chunk c of lane (b,d) as the affine map h -> P*h + Q
+//            (P = product of the decays, Q = the chunk's scan from zero);
+//   phase 2  prefix:  one warp per lane scans the maps of 32 chunks at a time
+//            with shuffles (Kogge-Stone, composition current∘previous =
+//            (Pc*Pp, Pc*Qp + Qc)) and carries the running state across
+//            blocks of 32; the exclusive result (each chunk's entry state) is
+//            written over Q;
+//   phase 3  replay:  each chunk reruns the sequential body from its entry
+//            state and writes the outputs.
+//
+// The backward runs the same three phases on the reverse recurrence
+// g_t = fma(a_{t+1}, g_{t+1}, grad_out_t), chunks walked last to first;
+// a_{t+1} at the last step of a chunk comes from the next chunk (0 past T)
+// and h_{t-1} at a chunk's first step from the previous chunk (0 before 0).
+// A short last chunk (T % C != 0) simply has fewer steps, which equals
+// padding it with identity steps (a=1, b=0).
+//
+// P and Q are fp32 [B, Nc, D] in a caller- or library-owned workspace.
+#pragma once
+
+#include "scan_common.cuh"
+
+namespace lrscan {
+
+struct ChunkGeom {
+    int T, D, Nc, nlb;  // nlb: lane blocks per (row, chunk)
+};
+
+// Linear CTA index -> (row, chunk, lane block); consecutive CTAs take
+// neighbouring lanes of the same chunk.
+__device__ __forceinline__ void chunk_coords(const ChunkGeom &g, int &brow, int &c, int &lb) {
+    const unsigned idx = blockIdx.x;
+    lb = static_cast<int>(idx % g.nlb);
+    const unsigned rc = idx / g.nlb;
+    c = static_cast<int>(rc % g.Nc);
+    brow = static_cast<int>(rc / g.Nc);
+}
+
+template <int V>
+__device__ __forceinline__ void store_f32_lanes(float *p, const float (&x)[V]) {
+    store_lanes<float, V>(p, x);
+}
+
+// ---------------------------------------------------------------- phase 1 --
+template <typename St, int V, int C>
+__global__ void __launch_bounds__(128)
+chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__restrict__ P,
+                  float *__restrict__ Q, ChunkGeom g) {
+    int brow, c, lb;
+    chunk_coords(g, brow, c, lb);
+    const int d = (lb * 128 + threadIdx.x) * V;
+    if (d >= g.D) return;
+    const int t0 = c * C;
+    const int n = min(C, g.T - t0);
+    const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
+    float p[V], q[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { p[v] = 1.0f; q[v] = 0.0f; }
+    if (n == C) {
+#pragma unroll 16
+        for (int j = 0; j < C; ++j) {
+            float x[V], y[V];
+            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
+#pragma unroll
+            for (int v = 0; v < V; ++v) { p[v] = __fmul_rn(x[v], p[v]); q[v] = __fmaf_rn(x[v], q[v], y[v]); }
+        }
+    } else {
+        for (int j = 0; j < n; ++j) {
+            float x[V], y[V];
+            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
+#pragma unroll
+            for (int v = 0; v < V; ++v) { p[v] = __fmul_rn(x[v], p[v]); q[v] = __fmaf_rn(x[v], q[v], y[v]); }
+        }
+    }
+    const size_t so = (static_cast<size_t>(brow) * g.Nc + c) * g.D + d;
+    store_f32_lanes<V>(P + so, p);
+    store_f32_lanes<V>(Q + so, q);
+}
+
+template <typename St, int V, int C>
+__global__ void __launch_bounds__(128)
+chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, float *__restrict__ P,
+                  float *__restrict__ Q, ChunkGeom g) {
+    int brow, c, lb;
+    chunk_coords(g, brow, c, lb);
+    const int d = (lb * 128 + threadIdx.x) * V;
+    if (d >= g.D) return;
+    const int t0 = c * C;
+    const int n = min(C, g.T - t0);
+    const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
+    float p[V], q[V], x[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { p[v] = 1.0f; q[v] = 0.0f; }
+    // a_{t+1} for the chunk's last step: first step of the next chunk, 0 past T
+    if (t0 + n < g.T) {
+        load_lanes_global<St, V>(a + base + static_cast<size_t>(n) * g.D, x);
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[v] = 0.0f;
+    }
+    for (int j = n - 1; j >= 0; --j) {
+        float y[V], xn[V];
+        load_lanes_global<St, V>(grad_out + base + static_cast<size_t>(j) * g.D, y);
+        load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, xn);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            p[v] = __fmul_rn(x[v], p[v]);
+            q[v] = __fmaf_rn(x[v], q[v], y[v]);
+            x[v] = xn[v];
+        }
+    }
+    const size_t so = (static_cast<size_t>(brow) * g.Nc + c) * g.D + d;
+    store_f32_lanes<V>(P + so, p);
+    store_f32_lanes<V>(Q + so, q);
+}
+
+// ---------------------------------------------------------------- phase 2 --
+// One warp per (row, lane); chunks taken in processing order (ascending for
+// the forward, descending for the backward), 32 per step, UNROLL steps of
+// loads in flight.  Q is overwritten with each chunk's entry state.
+template <bool REVERSE, int UNROLL>
+__global__ void __launch_bounds__(256)
+chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, long long lanes) {
+    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= lanes) return;
+    const long long brow = wid / D;
+    const int d = static_cast<int>(wid - brow * D);
+    const size_t base = static_cast<size_t>(brow) * Nc * D + d;
+    float carry = 0.0f;
+    for (int c0 = 0; c0 < Nc; c0 += 32 * UNROLL) {
+        float p[UNROLL], q[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int idx = c0 + u * 32 + lane;
+            const int c = REVERSE ? Nc - 1 - idx : idx;
+            if (idx < Nc) {
+                p[u] = __ldcg(P + base + static_cast<size_t>(c) * D);
+                q[u] = __ldcg(Q + base + static_cast<size_t>(c) * D);
+            } else {
+                p[u] = 1.0f;
+                q[u] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            float pu = p[u], qu = q[u];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float pp = __shfl_up_sync(0xffffffffu, pu, off);
+                const float qp = __shfl_up_sync(0xffffffffu, qu, off);
+                if (lane >= off) {
+                    qu = __fmaf_rn(pu, qp, qu);
+                    pu = __fmul_rn(pu, pp);
+                }
+            }
+            const float pin = __shfl_up_sync(0xffffffffu, pu, 1);
+            const float qin = __shfl_up_sync(0xffffffffu, qu, 1);
+            const float entry = (lane == 0) ? carry : __fmaf_rn(pin, carry, qin);
+            const float pall = __shfl_sync(0xffffffffu, pu, 31);
+            const float qall = __shfl_sync(0xffffffffu, qu, 31);
+            const int idx = c0 + u * 32 + lane;
+            if (idx < Nc) {
+                const int c = REVERSE ? Nc - 1 - idx : idx;
+                Q[base + static_cast<size_t>(c) * D] = entry;
+            }
+            carry = __fmaf_rn(pall, carry, qall);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- phase 3 --
+template <typename St, int V, int C>
+__global__ void __launch_bounds__(128)
+chunk_replay_fwd(const St *__restrict__ a, const St *__restrict__ b, const float *__restrict__ Hin,
+                 St *__restrict__ out, float *__restrict__ last, ChunkGeom g) {
+    int brow, c, lb;
+    chunk_coords(g, brow, c, lb);
+    const int d = (lb * 128 + threadIdx.x) * V;
+    if (d >= g.D) return;
+    const int t0 = c * C;
+    const int n = min(C, g.T - t0);
+    const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
+    float h[V];
+    {
+        const float *hp = Hin + (static_cast<size_t>(brow) * g.Nc + c) * g.D + d;
+#pragma unroll
+        for (int v = 0; v < V; ++v) h[v] = __ldcg(hp + v);
+    }
+    if (n == C) {
+#pragma unroll 16
+        for (int j = 0; j < C; ++j) {
+            float x[V], y[V];
+            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
+#pragma unroll
+            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
+            store_lanes<St, V>(out + base + static_cast<size_t>(j) * g.D, h);
+        }
+    } else {
+        for (int j = 0; j < n; ++j) {
+            float x[V], y[V];
+            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
+#pragma unroll
+            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
+            store_lanes<St, V>(out + base + static_cast<size_t>(j) * g.D, h);
+        }
+    }
+    if (last != nullptr && c == g.Nc - 1) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * g.D + d + v] = h[v];
+    }
+}
+
+template <typename St, int V, int C>
+__global__ void __launch_bounds__(128)
+chunk_replay_bwd(const St *__restrict__ a, const St *__restrict__ out, const St *__restrict__ grad_out,
+                 const float *__restrict__ Gin, St *__restrict__ grad_a, St *__restrict__ grad_b,
+                 ChunkGeom g) {
+    int brow, c, lb;
+    chunk_coords(g, brow, c, lb);
+    const int d = (lb * 128 + threadIdx.x) * V;
+    if (d >= g.D) return;
+    const int t0 = c * C;
+    const int n = min(C, g.T - t0);
+    const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
+    float gv[V], x[V];
+    {
+        const float *gp = Gin + (static_cast<size_t>(brow) * g.Nc + c) * g.D + d;
+#pragma unroll
+        for (int v = 0; v < V; ++v) gv[v] = __ldcg(gp + v);
+    }
+    if (t0 + n < g.T) {
+        load_lanes_global<St, V>(a + base + static_cast<size_t>(n) * g.D, x);
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[v] = 0.0f;
+    }
+    for (int j = n - 1; j >= 0; --j) {
+        float y[V], hp[V], xn[V], ga[V];
+        const size_t o = base + static_cast<size_t>(j) * g.D;
+        load_lanes_global<St, V>(grad_out + o, y);
+        load_lanes_global<St, V>(a + o, xn);
+        if (t0 + j > 0) {
+            load_lanes_global<St, V>(out + o - g.D, hp);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) hp[v] = 0.0f;
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            gv[v] = __fmaf_rn(x[v], gv[v], y[v]);
+            ga[v] = __fmul_rn(gv[v], hp[v]);
+            x[v] = xn[v];
+        }
+        store_lanes<St, V>(grad_b + o, gv);
+        store_lanes<St, V>(grad_a + o, ga);
+    }
+}
+
+// ------------------------------------------------- plain sequential kernels --
+// Thread per lane, plain loads, any alignment.  Same operation order as the
+// sequential definition (bit-identical results); used when rows are not
+// 16-byte aligned, so bulk tensor copies cannot be used.
+template <typename St>
+__global__ void __launch_bounds__(128)
+plain_fwd(const St *__restrict__ a, const St *__restrict__ b, St *__restrict__ out,
+          float *__restrict__ last, int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    if (d >= D) return;
+    size_t i = static_cast<size_t>(brow) * T * D + d;
+    float h = 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < T; ++t) {
+        float x[1], y[1];
+        load_lanes_global<St, 1>(a + i, x);
+        load_lanes_global<St, 1>(b + i, y);
+        h = __fmaf_rn(x[0], h, y[0]);
+        const float hv[1] = {h};
+        store_lanes<St, 1>(out + i, hv);
+        i += D;
+    }
+    if (last != nullptr) last[static_cast<size_t>(brow) * D + d] = h;
+}
+
+template <typename St>
+__global__ void __launch_bounds__(128)
+plain_bwd(const St *__restrict__ a, const St *__restrict__ out, const St *__restrict__ grad_out,
+          St *__restrict__ grad_a, St *__restrict__ grad_b, int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    if (d >= D) return;
+    const size_t row = static_cast<size_t>(brow) * T * D + d;
+    float g = 0.0f, x = 0.0f;
+#pragma unroll 8
+    for (int t = T - 1; t >= 0; --t) {
+        const size_t i = row + static_cast<size_t>(t) * D;
+        float y[1], hp[1] = {0.0f}, xn[1];
+        load_lanes_global<St, 1>(grad_out + i, y);
+        load_lanes_global<St, 1>(a + i, xn);
+        if (t > 0) load_lanes_global<St, 1>(out + i - D, hp);
+        g = __fmaf_rn(x, g, y[0]);
+        const float gb[1] = {g}, ga[1] = {__fmul_rn(g, hp[0])};
+        store_lanes<St, 1>(grad_b + i, gb);
+        store_lanes<St, 1>(grad_a + i, ga);
+        x = xn[0];
+    }
+}
+
+}  // namespace lrscan

@@ -1,0 +1,130 @@
+// Instantiations and launchers of the three-phase chunked kernels, the plain
+// sequential kernels and the bounded-wait self-test.
+#include "chunk_kernels.cuh"
+#include "launch.h"
+
+namespace lrscan {
+
+namespace {
+
+inline unsigned blocks_for(const ChunkGeom &g, int64_t B) {
+    return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Nc * B);
+}
+
+template <typename St, int V, int C>
+int chunk_fwd_t(const ChunkLaunch &L) {
+    ChunkGeom g;
+    g.T = static_cast<int>(L.T);
+    g.D = static_cast<int>(L.D);
+    g.Nc = static_cast<int>((L.T + C - 1) / C);
+    g.nlb = static_cast<int>((L.D / V + 127) / 128);
+    const unsigned nb = blocks_for(g, L.B);
+    chunk_summary_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
+                                                          static_cast<const St *>(L.in1), L.P, L.Q, g);
+    const long long lanes = static_cast<long long>(L.B) * L.D;
+    const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
+    chunk_prefix<false, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes);
+    chunk_replay_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
+                                                         static_cast<const St *>(L.in1), L.Q,
+                                                         static_cast<St *>(L.out0), L.last, g);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <typename St, int V, int C>
+int chunk_bwd_t(const ChunkLaunch &L) {
+    ChunkGeom g;
+    g.T = static_cast<int>(L.T);
+    g.D = static_cast<int>(L.D);
+    g.Nc = static_cast<int>((L.T + C - 1) / C);
+    g.nlb = static_cast<int>((L.D / V + 127) / 128);
+    const unsigned nb = blocks_for(g, L.B);
+    chunk_summary_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
+                                                          static_cast<const St *>(L.in2), L.P, L.Q, g);
+    const long long lanes = static_cast<long long>(L.B) * L.D;
+    const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
+    chunk_prefix<true, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes);
+    chunk_replay_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(
+        static_cast<const St *>(L.in0), static_cast<const St *>(L.in1), static_cast<const St *>(L.in2), L.Q,
+        static_cast<St *>(L.out0), static_cast<St *>(L.out1), g);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <typename St, int VMAX>
+int chunk_dispatch(const ChunkLaunch &L, bool fwd) {
+    const bool vec = L.vec == VMAX;
+#define LRSCAN_CHUNK_CASE(CC)                                                      \
+    if (L.chunk == CC) {                                                           \
+        if (vec) return fwd ? chunk_fwd_t<St, VMAX, CC>(L) : chunk_bwd_t<St, VMAX, CC>(L); \
+        return fwd ? chunk_fwd_t<St, 1, CC>(L) : chunk_bwd_t<St, 1, CC>(L);        \
+    }
+    LRSCAN_CHUNK_CASE(16)
+    LRSCAN_CHUNK_CASE(32)
+    LRSCAN_CHUNK_CASE(64)
+#undef LRSCAN_CHUNK_CASE
+    return -2;
+}
+
+__global__ void selftest_wait_kernel(DevStatus *status, uint64_t timeout_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtx wc{status, &abort_flag, timeout_ns};
+        // Nothing arrives on this barrier: the wait has to expire and report.
+        (void)mbar_wait(smem_addr(&bar), 0, wc, kSiteSelftest);
+    }
+}
+
+}  // namespace
+
+int chunk_fwd(const ChunkLaunch &L, int dtype) {
+    return dtype == 0 ? chunk_dispatch<float, 4>(L, true) : chunk_dispatch<bf16_t, 8>(L, true);
+}
+
+int chunk_bwd(const ChunkLaunch &L, int dtype) {
+    return dtype == 0 ? chunk_dispatch<float, 4>(L, false) : chunk_dispatch<bf16_t, 8>(L, false);
+}
+
+int plain_fwd_launch(const ChunkLaunch &L, int dtype) {
+    const int nlb = static_cast<int>((L.D + 127) / 128);
+    const unsigned nb = static_cast<unsigned>(nlb * L.B);
+    if (dtype == 0)
+        plain_fwd<float><<<nb, 128, 0, L.stream>>>(static_cast<const float *>(L.in0),
+                                                   static_cast<const float *>(L.in1),
+                                                   static_cast<float *>(L.out0), L.last,
+                                                   static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+    else
+        plain_fwd<bf16_t><<<nb, 128, 0, L.stream>>>(static_cast<const bf16_t *>(L.in0),
+                                                    static_cast<const bf16_t *>(L.in1),
+                                                    static_cast<bf16_t *>(L.out0), L.last,
+                                                    static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int plain_bwd_launch(const ChunkLaunch &L, int dtype) {
+    const int nlb = static_cast<int>((L.D + 127) / 128);
+    const unsigned nb = static_cast<unsigned>(nlb * L.B);
+    if (dtype == 0)
+        plain_bwd<float><<<nb, 128, 0, L.stream>>>(
+            static_cast<const float *>(L.in0), static_cast<const float *>(L.in1),
+            static_cast<const float *>(L.in2), static_cast<float *>(L.out0), static_cast<float *>(L.out1),
+            static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+    else
+        plain_bwd<bf16_t><<<nb, 128, 0, L.stream>>>(
+            static_cast<const bf16_t *>(L.in0), static_cast<const bf16_t *>(L.in1),
+            static_cast<const bf16_t *>(L.in2), static_cast<bf16_t *>(L.out0), static_cast<bf16_t *>(L.out1),
+            static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int selftest_wait_launch(DevStatus *status, uint64_t timeout_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace lrscan

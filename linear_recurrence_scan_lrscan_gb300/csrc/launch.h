@@ -1,0 +1,67 @@
+// Internal interface between the host dispatcher (lrscan_abi.cu) and the
+// translation units that instantiate and launch the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <mutex>
+
+namespace lrscan {
+
+struct DevStatus;
+
+enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3, kPathPlain = 4 };
+
+// Arguments of one time-tiled launch (forward: maps a,b / out0=out;
+// backward: maps a,out,grad_out / out0=grad_a, out1=grad_b).
+struct WinLaunch {
+    const CUtensorMap *maps[3];
+    void *out0;
+    void *out1;
+    float *last;
+    int64_t B, T, D;
+    DevStatus *status;
+    uint64_t timeout_ns;
+    cudaStream_t stream;
+    int device;
+};
+
+struct WinVariant {
+    const char *name;
+    int dt;          // lanes per CTA
+    int v;           // lanes per thread
+    int s;           // sub-chunks per window
+    int l;           // steps per sub-chunk
+    int w;           // rows per window
+    int nstage_fwd, nstage_bwd;
+    int threads;
+    int smem_fwd, smem_bwd;
+    int stage_bytes_fwd, stage_bytes_bwd;
+    int (*fwd)(const WinLaunch &);
+    int (*bwd)(const WinLaunch &);
+};
+
+// path: kPathSeq or kPathWindow; dtype 0 = f32, 1 = bf16
+const WinVariant *win_variants(int path, int dtype, int *count);
+
+// Three-phase chunked path and plain kernels (kernels_chunk.cu).
+struct ChunkLaunch {
+    const void *in0, *in1, *in2;  // fwd: a, b; bwd: a, out, grad_out
+    void *out0, *out1;            // fwd: out; bwd: grad_a, grad_b
+    float *last;
+    float *P, *Q;                 // workspace [B, Nc, D] each
+    int64_t B, T, D;
+    int chunk;                    // 16, 32, 64
+    int vec;                      // lanes per thread: 1, 2, 4 (f32) / 1, 2, 4, 8 (bf16)
+    cudaStream_t stream;
+};
+int chunk_fwd(const ChunkLaunch &L, int dtype);
+int chunk_bwd(const ChunkLaunch &L, int dtype);
+int plain_fwd_launch(const ChunkLaunch &L, int dtype);
+int plain_bwd_launch(const ChunkLaunch &L, int dtype);
+int selftest_wait_launch(DevStatus *status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace lrscan

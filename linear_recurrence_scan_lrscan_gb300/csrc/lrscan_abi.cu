@@ -1,0 +1,558 @@
+// Host side of liblrscan.so: argument checks, the occupancy rule that picks
+// a path, tensor-map encoding, workspace management and the exported C ABI
+// declared in include/lrscan.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "launch.h"
+#include "lrscan.h"
+#include "scan_common.cuh"
+
+namespace lrscan {
+
+// One status word per device (module globals are instantiated per device).
+__device__ DevStatus g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCtx {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_per_sm = 0;
+    int smem_optin = 0;
+    int max_threads_per_sm = 2048;
+    DevStatus *status = nullptr;
+    std::map<cudaStream_t, std::pair<void *, size_t>> workspace;  // library-owned, per stream
+};
+
+std::mutex g_mu;
+DeviceCtx g_dev[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+thread_local cudaStream_t t_stream = nullptr;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Description used when no device is visible (plans only): one GB300.
+constexpr int kRefSMs = 152, kRefSmemPerSM = 233472, kRefSmemOptin = 232448;
+
+int device_ctx(DeviceCtx **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return LRSCAN_ENODEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceCtx &c = g_dev[dev];
+    if (!c.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return LRSCAN_ENODEVICE;
+        }
+        if (major != 10 || minor != 3) return LRSCAN_ENODEVICE;  // kernels are built for sm_103a only
+        cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&c.max_threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+            cudaGetLastError();
+            return LRSCAN_ECUDA;
+        }
+        c.status = static_cast<DevStatus *>(p);
+        if (g_encode == nullptr) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                cudaGetLastError();
+                return LRSCAN_ECUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        c.ready = true;
+    }
+    *out = &c;
+    return LRSCAN_OK;
+}
+
+struct Geometry {
+    int sm_count, smem_per_sm, smem_optin, max_threads_per_sm;
+};
+
+Geometry geometry_of(const DeviceCtx *c) {
+    if (c) return {c->sm_count, c->smem_per_sm, c->smem_optin, c->max_threads_per_sm};
+    return {kRefSMs, kRefSmemPerSM, kRefSmemOptin, 2048};
+}
+
+int esize(int dtype) { return dtype == LRSCAN_F32 ? 4 : 2; }
+
+// -------------------------------------------------------------------------
+// Occupancy rule
+// -------------------------------------------------------------------------
+struct Choice {
+    int path = kPathSeq;
+    int vidx = 0;                 // index into the path's variant table
+    const WinVariant *var = nullptr;
+    int chunk = 64;
+    int vec = 1;
+    size_t workspace = 0;
+    long long ctas = 0;
+    int threads = 0, smem = 0, stages = 0, kernels = 1;
+};
+
+struct Occ {
+    long long ctas;
+    int resident;    // CTAs per SM that fit
+    bool one_wave;
+    double inflight; // bytes in flight per SM, estimated
+};
+
+Occ occupancy(const WinVariant &v, int dir, int64_t B, int64_t D, const Geometry &g) {
+    const int smem = dir == 0 ? v.smem_fwd : v.smem_bwd;
+    const int nst = dir == 0 ? v.nstage_fwd : v.nstage_bwd;
+    const int stage = dir == 0 ? v.stage_bytes_fwd : v.stage_bytes_bwd;
+    Occ o;
+    o.ctas = B * ((D + v.dt - 1) / v.dt);
+    int r_smem = smem > g.smem_optin ? 0 : g.smem_per_sm / (smem + 1024);
+    int r_thr = g.max_threads_per_sm / v.threads;
+    o.resident = std::min(std::min(r_smem, r_thr), 32);
+    o.one_wave = o.resident > 0 && o.ctas <= static_cast<long long>(o.resident) * g.sm_count;
+    const double per_sm = std::min<double>(static_cast<double>(o.ctas) / g.sm_count, o.resident);
+    o.inflight = per_sm * (nst - 1) * stage;
+    return o;
+}
+
+size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C) {
+    const int64_t nc = (T + C - 1) / C;
+    const size_t one = static_cast<size_t>(B) * nc * D * 4;
+    const size_t pad = (one + 255) / 256 * 256;
+    return pad * 2;
+}
+
+int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *vidx) {
+    int n = 0;
+    const WinVariant *tab = win_variants(path, dtype, &n);
+    int best = -1;
+    double best_score = -1;
+    for (int i = 0; i < n; ++i) {
+        Occ o = occupancy(tab[i], dir, B, D, g);
+        if (o.resident == 0) continue;
+        if (o.ctas < static_cast<long long>(0.9 * g.sm_count)) continue;
+        // Prefer a single wave (every CTA resident: no tail); past one wave,
+        // prefer the fullest last wave.  Then more bytes in flight per SM, then
+        // wider rows (longer DRAM bursts).
+        const double slots = static_cast<double>(o.resident) * g.sm_count;
+        const double waves = std::ceil(static_cast<double>(o.ctas) / slots);
+        const double fill = static_cast<double>(o.ctas) / (waves * slots);
+        const double score = (o.one_wave ? 2e6 : 1e6 * fill) + std::min(o.inflight, 96.0 * 1024) +
+                             tab[i].dt * sizeof(float);
+        if (score > best_score) {
+            best_score = score;
+            best = i;
+        }
+    }
+    *vidx = best;
+    return best >= 0;
+}
+
+int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
+              const Geometry &g, Choice *ch) {
+    const int want = opts ? opts->path : 0;
+    const int force_v = opts ? opts->tile_variant : 0;
+    int chunk = opts && opts->chunk_len ? opts->chunk_len : 64;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return LRSCAN_EINVAL;
+    ch->chunk = chunk;
+    const int vmax = dtype == LRSCAN_F32 ? 4 : 8;
+    ch->vec = (aligned16 && D % vmax == 0) ? vmax : 1;
+
+    int path = want;
+    if (want < kPathAuto || want > kPathPlain) return LRSCAN_EINVAL;
+    if ((path == kPathSeq || path == kPathWindow) && !aligned16) return LRSCAN_EINVAL;
+    if (path == kPathAuto) {
+        int vi = -1;
+        if (!aligned16) {
+            path = (B * D < 32LL * g.sm_count * 32 && T >= 16LL * chunk) ? kPathChunk : kPathPlain;
+        } else if (pick_window_variant(kPathSeq, dtype, dir, B, D, g, &vi)) {
+            path = kPathSeq;
+        } else if (pick_window_variant(kPathWindow, dtype, dir, B, D, g, &vi)) {
+            path = kPathWindow;
+        } else if (T >= 16LL * chunk) {
+            // too few lanes for a one-CTA-per-lane-tile walk to fill the GPU:
+            // parallelize over time chunks instead
+            path = kPathChunk;
+        } else {
+            path = kPathSeq;
+        }
+    }
+    ch->path = path;
+    if (path == kPathSeq || path == kPathWindow) {
+        int n = 0;
+        const WinVariant *tab = win_variants(path, dtype, &n);
+        int vi = -1;
+        if (force_v > 0) {
+            if (force_v > n) return LRSCAN_EINVAL;
+            vi = force_v - 1;
+        } else if (!pick_window_variant(path, dtype, dir, B, D, g, &vi)) {
+            // too few lanes to fill the GPU (or too many for one wave): take the
+            // variant with the most CTAs that still fits on an SM
+            long long most = -1;
+            for (int i = 0; i < n; ++i) {
+                Occ o = occupancy(tab[i], dir, B, D, g);
+                if (o.resident == 0) continue;
+                if (o.ctas > most) { most = o.ctas; vi = i; }
+            }
+        }
+        if (vi < 0) return LRSCAN_EINVAL;
+        ch->vidx = vi;
+        ch->var = &tab[vi];
+        Occ o = occupancy(tab[vi], dir, B, D, g);
+        if (o.resident == 0) return LRSCAN_EINVAL;
+        ch->ctas = o.ctas;
+        ch->threads = tab[vi].threads;
+        ch->smem = dir == 0 ? tab[vi].smem_fwd : tab[vi].smem_bwd;
+        ch->stages = dir == 0 ? tab[vi].nstage_fwd : tab[vi].nstage_bwd;
+        ch->kernels = 1;
+        ch->workspace = 0;
+    } else if (path == kPathChunk) {
+        if (force_v > 1) return LRSCAN_EINVAL;
+        const int64_t nc = (T + chunk - 1) / chunk;
+        ch->ctas = B * nc * ((D / ch->vec + 127) / 128);
+        ch->threads = 128;
+        ch->kernels = 3;
+        ch->workspace = chunk_workspace(B, T, D, chunk);
+    } else {  // plain
+        if (force_v > 1) return LRSCAN_EINVAL;
+        ch->ctas = B * ((D + 127) / 128);
+        ch->threads = 128;
+        ch->kernels = 1;
+        ch->vec = 1;
+    }
+    return LRSCAN_OK;
+}
+
+void fill_info(const Choice &c, lrscan_plan_info *info) {
+    std::memset(info, 0, sizeof *info);
+    info->path = c.path;
+    info->tile_variant = c.vidx + 1;
+    info->ctas = static_cast<int>(std::min<long long>(c.ctas, 0x7fffffff));
+    info->threads_per_cta = c.threads;
+    info->smem_bytes = c.smem;
+    info->stages = c.stages;
+    info->kernels = c.kernels;
+    info->workspace_bytes = c.workspace;
+    info->subchunks = 1;
+    if (c.var) {
+        info->lanes_per_cta = c.var->dt;
+        info->rows_per_window = c.var->w;
+        info->subchunks = c.var->s;
+        std::snprintf(info->name, sizeof info->name, "%s", c.var->name);
+    } else if (c.path == kPathChunk) {
+        info->lanes_per_cta = 128 * c.vec;
+        info->rows_per_window = c.chunk;
+        std::snprintf(info->name, sizeof info->name, "chunk%d_v%d", c.chunk, c.vec);
+    } else {
+        info->lanes_per_cta = 128;
+        std::snprintf(info->name, sizeof info->name, "plain");
+    }
+}
+
+// -------------------------------------------------------------------------
+// Tensor maps: a [B][T][D] tensor viewed as 3-D {D, T, B}; box {DT, W, 1}.
+// -------------------------------------------------------------------------
+int encode_map(CUtensorMap *m, const void *ptr, int dtype, int64_t B, int64_t T, int64_t D, int dt, int w) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esize(dtype),
+                                   static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(D) * esize(dtype)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(dt), static_cast<cuuint32_t>(w), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dtype == LRSCAN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LRSCAN_OK : LRSCAN_EINVAL;
+}
+
+int check_shape(int64_t B, int64_t T, int64_t D, int dtype) {
+    if (dtype != LRSCAN_F32 && dtype != LRSCAN_BF16) return LRSCAN_EDTYPE;
+    if (B < 0 || T < 0 || D < 0) return LRSCAN_EINVAL;
+    if (T > 0x7fffffffLL || D > 0x7fffffffLL) return LRSCAN_EINVAL;
+    int64_t e = 0, bytes = 0;
+    if (__builtin_mul_overflow(B, T, &e) || __builtin_mul_overflow(e, D, &e) ||
+        __builtin_mul_overflow(e, static_cast<int64_t>(esize(dtype)), &bytes))
+        return LRSCAN_EINVAL;
+    return LRSCAN_OK;
+}
+
+bool aligned16(std::initializer_list<const void *> ps, int64_t D, int dtype) {
+    if ((D * esize(dtype)) % 16 != 0) return false;
+    for (const void *p : ps)
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return false;
+    return true;
+}
+
+int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opts *opts, void **ws) {
+    if (opts && opts->workspace) {
+        if (opts->workspace_bytes < need || reinterpret_cast<uintptr_t>(opts->workspace) % 256 != 0)
+            return LRSCAN_ENOMEM;
+        *ws = opts->workspace;
+        return LRSCAN_OK;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto &slot = ctx->workspace[st];
+    if (slot.second < need) {
+        if (slot.first) {
+            cudaStreamSynchronize(st);  // the old buffer may still be in use by this stream
+            cudaFree(slot.first);
+            slot.first = nullptr;
+            slot.second = 0;
+        }
+        void *p = nullptr;
+        if (cudaMalloc(&p, need) != cudaSuccess) {
+            cudaGetLastError();
+            return LRSCAN_ENOMEM;
+        }
+        slot.first = p;
+        slot.second = need;
+    }
+    *ws = slot.first;
+    return LRSCAN_OK;
+}
+
+cudaStream_t pick_stream(void *stream) { return stream ? static_cast<cudaStream_t>(stream) : t_stream; }
+
+int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype,
+            void *stream, const lrscan_opts *opts) {
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
+    cudaStream_t st = pick_stream(stream);
+    if (T == 0) {
+        if (last && cudaMemsetAsync(last, 0, static_cast<size_t>(B) * D * 4, st) != cudaSuccess) return LRSCAN_ECUDA;
+        return LRSCAN_OK;
+    }
+    if (!a || !b || !out) return LRSCAN_EINVAL;
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({a, b, out}, D, dtype);
+    Choice ch;
+    if ((rc = plan_call(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
+    const size_t es = esize(dtype);
+    if (ch.path == kPathSeq || ch.path == kPathWindow) {
+        const WinVariant &v = *ch.var;
+        for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+            const int64_t nb = std::min<int64_t>(65535, B - b0);
+            const size_t off = static_cast<size_t>(b0) * T * D * es;
+            CUtensorMap ma, mb;
+            if (encode_map(&ma, static_cast<const char *>(a) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w))
+                return LRSCAN_EINVAL;
+            WinLaunch L{};
+            L.maps[0] = &ma;
+            L.maps[1] = &mb;
+            L.out0 = static_cast<char *>(out) + off;
+            L.last = last ? last + b0 * D : nullptr;
+            L.B = nb; L.T = T; L.D = D;
+            L.status = ctx->status;
+            L.timeout_ns = g_timeout_ns.load();
+            L.stream = st;
+            L.device = dev;
+            if (v.fwd(L)) return LRSCAN_ECUDA;
+        }
+        return LRSCAN_OK;
+    }
+    ChunkLaunch L{};
+    L.in0 = a; L.in1 = b; L.out0 = out; L.last = last;
+    L.B = B; L.T = T; L.D = D;
+    L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
+    if (ch.path == kPathPlain) return plain_fwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
+    void *ws = nullptr;
+    if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
+    L.P = static_cast<float *>(ws);
+    L.Q = reinterpret_cast<float *>(static_cast<char *>(ws) + ch.workspace / 2);
+    rc = chunk_fwd(L, dtype);
+    return rc == 0 ? LRSCAN_OK : (rc == -2 ? LRSCAN_EINVAL : LRSCAN_ECUDA);
+}
+
+int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B, int64_t T,
+            int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0 || T == 0) return LRSCAN_OK;
+    if (!a || !out || !grad_out || !grad_a || !grad_b) return LRSCAN_EINVAL;
+    cudaStream_t st = pick_stream(stream);
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({a, out, grad_out, grad_a, grad_b}, D, dtype);
+    Choice ch;
+    if ((rc = plan_call(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
+    const size_t es = esize(dtype);
+    if (ch.path == kPathSeq || ch.path == kPathWindow) {
+        const WinVariant &v = *ch.var;
+        for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+            const int64_t nb = std::min<int64_t>(65535, B - b0);
+            const size_t off = static_cast<size_t>(b0) * T * D * es;
+            CUtensorMap ma, mo, mg;
+            if (encode_map(&ma, static_cast<const char *>(a) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mo, static_cast<const char *>(out) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w))
+                return LRSCAN_EINVAL;
+            WinLaunch L{};
+            L.maps[0] = &ma;
+            L.maps[1] = &mo;
+            L.maps[2] = &mg;
+            L.out0 = static_cast<char *>(grad_a) + off;
+            L.out1 = static_cast<char *>(grad_b) + off;
+            L.B = nb; L.T = T; L.D = D;
+            L.status = ctx->status;
+            L.timeout_ns = g_timeout_ns.load();
+            L.stream = st;
+            L.device = dev;
+            if (v.bwd(L)) return LRSCAN_ECUDA;
+        }
+        return LRSCAN_OK;
+    }
+    ChunkLaunch L{};
+    L.in0 = a; L.in1 = out; L.in2 = grad_out; L.out0 = grad_a; L.out1 = grad_b;
+    L.B = B; L.T = T; L.D = D;
+    L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
+    if (ch.path == kPathPlain) return plain_bwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
+    void *ws = nullptr;
+    if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
+    L.P = static_cast<float *>(ws);
+    L.Q = reinterpret_cast<float *>(static_cast<char *>(ws) + ch.workspace / 2);
+    rc = chunk_bwd(L, dtype);
+    return rc == 0 ? LRSCAN_OK : (rc == -2 ? LRSCAN_EINVAL : LRSCAN_ECUDA);
+}
+
+}  // namespace
+}  // namespace lrscan
+
+using namespace lrscan;
+
+extern "C" {
+
+int lrscan_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype) {
+    return run_fwd(a, b, out, last, B, T, D, dtype, nullptr, nullptr);
+}
+
+int lrscan_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B,
+               int64_t T, int64_t D, int dtype) {
+    return run_bwd(a, out, grad_out, grad_a, grad_b, B, T, D, dtype, nullptr, nullptr);
+}
+
+int lrscan_fwd_ex(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype,
+                  void *stream, const lrscan_opts *opts) {
+    return run_fwd(a, b, out, last, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_bwd_ex(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B,
+                  int64_t T, int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    return run_bwd(a, out, grad_out, grad_a, grad_b, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_set_stream(void *stream) {
+    t_stream = static_cast<cudaStream_t>(stream);
+    return LRSCAN_OK;
+}
+
+size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len) {
+    const int C = chunk_len ? chunk_len : 64;
+    if (B <= 0 || T <= 0 || D <= 0 || (C != 16 && C != 32 && C != 64)) return 0;
+    return chunk_workspace(B, T, D, C);
+}
+
+int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16, const lrscan_opts *opts,
+                lrscan_plan_info *info) {
+    if (!info || (dir != 0 && dir != 1)) return LRSCAN_EINVAL;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    DeviceCtx *ctx = nullptr;
+    if (device_ctx(&ctx) != LRSCAN_OK) ctx = nullptr;  // no device: plan for one GB300
+    const bool al = is_aligned16 && (D * esize(dtype)) % 16 == 0;
+    Choice ch;
+    if ((rc = plan_call(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch)))
+        return rc;
+    fill_info(ch, info);
+    return LRSCAN_OK;
+}
+
+int lrscan_num_variants(int path, int dtype, int dir) {
+    (void)dir;
+    if (dtype != LRSCAN_F32 && dtype != LRSCAN_BF16) return LRSCAN_EDTYPE;
+    if (path == kPathSeq || path == kPathWindow) {
+        int n = 0;
+        win_variants(path, dtype, &n);
+        return n;
+    }
+    if (path == kPathChunk || path == kPathPlain) return 1;
+    return LRSCAN_EINVAL;
+}
+
+int lrscan_sync_check(void) {
+    DeviceCtx *ctx = nullptr;
+    int rc = device_ctx(&ctx);
+    if (rc) return rc;
+    cudaStream_t st = t_stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return LRSCAN_ECUDA;
+    }
+    DevStatus s{};
+    if (cudaMemcpyAsync(&s, ctx->status, sizeof s, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return LRSCAN_ECUDA;
+    }
+    if (s.code != 0) {
+        cudaMemsetAsync(ctx->status, 0, sizeof s, st);
+        cudaStreamSynchronize(st);
+        return s.code;
+    }
+    return LRSCAN_OK;
+}
+
+int lrscan_set_wait_timeout_ns(uint64_t ns) {
+    if (ns == 0) return LRSCAN_EINVAL;
+    g_timeout_ns.store(ns);
+    return LRSCAN_OK;
+}
+
+int lrscan_selftest_wait_timeout(uint64_t timeout_ns) {
+    DeviceCtx *ctx = nullptr;
+    int rc = device_ctx(&ctx);
+    if (rc) return rc;
+    if (timeout_ns == 0 || timeout_ns > 10ull * 1000000000ull) return LRSCAN_EINVAL;
+    if (selftest_wait_launch(ctx->status, timeout_ns, t_stream)) return LRSCAN_ECUDA;
+    return lrscan_sync_check();
+}
+
+const char *lrscan_strerror(int code) {
+    switch (code) {
+        case LRSCAN_OK: return "success";
+        case LRSCAN_EINVAL: return "invalid argument";
+        case LRSCAN_EDTYPE: return "unsupported dtype";
+        case LRSCAN_ECUDA: return "CUDA runtime error";
+        case LRSCAN_ENOMEM: return "workspace allocation failed or too small";
+        case LRSCAN_ETIMEOUT: return "a bounded device wait timed out";
+        case LRSCAN_ENODEVICE: return "no usable sm_103 device";
+        default: return "unknown error";
+    }
+}
+
+int lrscan_version(void) { return LRSCAN_VERSION; }
+
+}  // extern "C"

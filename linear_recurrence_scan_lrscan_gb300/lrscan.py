@@ -1,0 +1,278 @@
+"""Python binding of liblrscan.so (argument marshalling only).
+
+Every function here checks tensors, picks the stream and hands raw device
+pointers to the C ABI declared in ``include/lrscan.h``; all arithmetic runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+If the library has not been built (``__graft_entry__.build()`` or
+``python -m linear_recurrence_scan_lrscan_gb300.build``) every call raises
+``LrscanUnavailable``: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+LRSCAN_OK = 0
+LRSCAN_EINVAL = -1
+LRSCAN_EDTYPE = -2
+LRSCAN_ECUDA = -3
+LRSCAN_ENOMEM = -4
+LRSCAN_ETIMEOUT = -5
+LRSCAN_ENODEVICE = -6
+
+F32, BF16 = 0, 1
+PATHS = {"auto": 0, "seq": 1, "chunk": 2, "window": 3, "plain": 4}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+
+
+class LrscanUnavailable(RuntimeError):
+    """The CUDA library is missing or could not be loaded."""
+
+
+class LrscanError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("chunk_len", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("tile_variant", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("tile_variant", ctypes.c_int), ("lanes_per_cta", ctypes.c_int),
+                ("rows_per_window", ctypes.c_int), ("subchunks", ctypes.c_int), ("stages", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("threads_per_cta", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t), ("name", ctypes.c_char * 64)]
+
+    def as_dict(self) -> dict:
+        d = {k: getattr(self, k) for k, _ in self._fields_ if k != "name"}
+        d["name"] = self.name.decode()
+        d["path"] = PATH_NAMES.get(self.path, self.path)
+        return d
+
+
+EXPORTS = {
+    "lrscan_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
+    "lrscan_bwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
+    "lrscan_fwd_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_bwd_ex": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)],
+                      ctypes.c_int),
+    "lrscan_set_stream": ([_P], ctypes.c_int),
+    "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
+    "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
+                     ctypes.POINTER(PlanInfo)], ctypes.c_int),
+    "lrscan_num_variants": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+    "lrscan_sync_check": ([], ctypes.c_int),
+    "lrscan_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
+    "lrscan_selftest_wait_timeout": ([ctypes.c_uint64], ctypes.c_int),
+    "lrscan_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "lrscan_version": ([], ctypes.c_int),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.environ.get("LRSCAN_LIBRARY", _build.LIB)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises LrscanUnavailable if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise LrscanUnavailable(
+                    f"liblrscan.so not found at {path}; build it with "
+                    "`python -m linear_recurrence_scan_lrscan_gb300.build` (nvcc, sm_103a)")
+            try:
+                handle = ctypes.CDLL(path)
+            except OSError as e:  # pragma: no cover - depends on the machine
+                raise LrscanUnavailable(f"cannot load {path}: {e}") from e
+            for name, (argtypes, restype) in EXPORTS.items():
+                fn = getattr(handle, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = handle
+        return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().lrscan_strerror(code).decode()
+    except LrscanUnavailable:
+        return f"error {code}"
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != LRSCAN_OK:
+        raise LrscanError(rc, what)
+
+
+def _opts(path, chunk_len, tile_variant, workspace) -> Opts | None:
+    if path is None and chunk_len is None and tile_variant is None and workspace is None:
+        return None
+    o = Opts()
+    o.path = PATHS[path] if isinstance(path, str) else int(path or 0)
+    o.chunk_len = int(chunk_len or 0)
+    o.tile_variant = int(tile_variant or 0)
+    if workspace is not None:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    return o
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_tensors(shape, dtype, device, **tensors):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device")
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if name == "last":
+            if t.dtype != torch.float32 or tuple(t.shape) != (shape[0], shape[2]):
+                raise ValueError("last must be fp32 [B, D]")
+            continue
+        if t.dtype != dtype:
+            raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {t.dtype}; lrscan takes float32 or bfloat16 storage")
+    return _DTYPES[t.dtype]
+
+
+def lrscan_fwd(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+               last: torch.Tensor | None = None, *, want_last: bool = True, path=None,
+               chunk_len=None, tile_variant=None, workspace=None, stream=None):
+    """Forward scan h_t = a_t*h_{t-1} + b_t over [B, T, D]; returns (out, last)."""
+    if a.ndim != 3 or a.shape != b.shape:
+        raise ValueError("lrscan expects matching [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    if out is None:
+        out = torch.empty_like(b)
+    if last is None and want_last:
+        last = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    _check_tensors(a.shape, a.dtype, a.device, a=a, b=b, out=out, last=last)
+    with torch.cuda.device(a.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_fwd_ex(a.data_ptr(), b.data_ptr(), out.data_ptr(),
+                                 last.data_ptr() if last is not None else None, B, T, D, code,
+                                 _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_fwd")
+    return out, last
+
+
+def lrscan_bwd(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
+               grad_a: torch.Tensor | None = None, grad_b: torch.Tensor | None = None, *,
+               path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
+    """Reverse scan; returns (grad_a, grad_b) for the loss sum(grad_out * out)."""
+    if a.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    if grad_a is None:
+        grad_a = torch.empty_like(a)
+    if grad_b is None:
+        grad_b = torch.empty_like(a)
+    _check_tensors(a.shape, a.dtype, a.device, a=a, out=out, grad_out=grad_out, grad_a=grad_a,
+                   grad_b=grad_b)
+    with torch.cuda.device(a.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_bwd_ex(a.data_ptr(), out.data_ptr(), grad_out.data_ptr(), grad_a.data_ptr(),
+                                 grad_b.data_ptr(), B, T, D, code, _stream_ptr(stream),
+                                 ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_bwd")
+    return grad_a, grad_b
+
+
+def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
+                aligned: bool = True, path=None, chunk_len=None, tile_variant=None) -> dict:
+    """What the dispatcher would run for this call (host only; no launch)."""
+    code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
+    if code is None:
+        raise ValueError(f"unsupported dtype {dtype}")
+    info = PlanInfo()
+    o = _opts(path, chunk_len, tile_variant, None)
+    rc = lib().lrscan_plan(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
+                           ctypes.byref(o) if o is not None else None, ctypes.byref(info))
+    _check(rc, "lrscan_plan")
+    return info.as_dict()
+
+
+def lrscan_num_variants(path: str, dtype: str = "f32", direction: str = "fwd") -> int:
+    return lib().lrscan_num_variants(PATHS[path], {"f32": F32, "bf16": BF16}[dtype],
+                                     0 if direction == "fwd" else 1)
+
+
+def lrscan_workspace_bytes(B: int, T: int, D: int, chunk_len: int = 64) -> int:
+    return lib().lrscan_workspace_bytes(B, T, D, chunk_len)
+
+
+def lrscan_sync_check(stream=None) -> int:
+    """Synchronize the stream and return (and clear) any device-side error code."""
+    lib().lrscan_set_stream(_stream_ptr(stream))
+    return lib().lrscan_sync_check()
+
+
+def lrscan_set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().lrscan_set_wait_timeout_ns(ns), "lrscan_set_wait_timeout_ns")
+
+
+def lrscan_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    lib().lrscan_set_stream(_stream_ptr(stream))
+    return lib().lrscan_selftest_wait_timeout(timeout_ns)
+
+
+class LinearRecurrenceScan(torch.autograd.Function):
+    """Autograd wrapper: out = scan(a, b); backward through lrscan_bwd."""
+
+    @staticmethod
+    def forward(ctx, a, b, path=None, chunk_len=None):
+        a, b = a.contiguous(), b.contiguous()
+        out, _ = lrscan_fwd(a, b, want_last=False, path=path, chunk_len=chunk_len)
+        ctx.save_for_backward(a, out)
+        ctx.opts = (path, chunk_len)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        a, out = ctx.saved_tensors
+        path, chunk_len = ctx.opts
+        ga, gb = lrscan_bwd(a, out, grad_out.contiguous(), path=path, chunk_len=chunk_len)
+        return ga, gb, None, None
+
+
+def scan(a: torch.Tensor, b: torch.Tensor, path=None, chunk_len=None) -> torch.Tensor:
+    """Differentiable h_t = a_t*h_{t-1} + b_t over [B, T, D] (fp32 or bf16 storage)."""
+    return LinearRecurrenceScan.apply(a, b, path, chunk_len)

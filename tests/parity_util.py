@@ -1,0 +1,67 @@
+"""Comparison rules for GPU-vs-oracle parity.
+
+Tolerances (stated once, used by every parity test):
+  * fp32 storage: |got - ref| <= 1e-4 * (1 + |ref|), element by element;
+  * bf16 storage: at most 2 bf16 ulps from the oracle's fp32 result rounded
+    to bf16 (ulp distance = distance between the two bit patterns as ordered
+    integers; +0 and -0 are the same point);
+  * "exact": equal values (+0 == -0), used for the sequential paths, whose
+    operation order is the oracle's own, and for identity-step padding.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+F32_RTOL = 1e-4
+BF16_MAX_ULPS = 2
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def bf16_bits_to_f32(x: np.ndarray) -> np.ndarray:
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_ulp_distance(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    def key(b):
+        b = b.astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(key(x) - key(y))
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", exact: bool = False):
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if dtype == "bf16":
+        g, r = bf16_bits_to_f32(got), bf16_bits_to_f32(ref)
+        nan_ok = np.isnan(g) == np.isnan(r)
+        assert nan_ok.all(), f"{what}: NaN pattern differs"
+        if exact:
+            bad = ~((g == r) | (np.isnan(g) & np.isnan(r)))
+        else:
+            bad = (bf16_ulp_distance(got, ref) > BF16_MAX_ULPS) & ~np.isnan(r)
+    else:
+        g, r = got.astype(np.float64), ref.astype(np.float64)
+        nan_ok = np.isnan(g) == np.isnan(r)
+        assert nan_ok.all(), f"{what}: NaN pattern differs"
+        if exact:
+            bad = ~((g == r) | (np.isnan(g) & np.isnan(r)))
+        else:
+            with np.errstate(invalid="ignore"):
+                bad = ~(np.abs(g - r) <= F32_RTOL * (1.0 + np.abs(r))) & ~np.isnan(r)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = [(tuple(i), float(g[tuple(i)]), float(r[tuple(i)])) for i in idx]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance "
+                             f"({'exact' if exact else dtype}); first: {detail}")
+
+
+def assert_last_close(got: np.ndarray, ref: np.ndarray, what: str = "last", exact: bool = False):
+    """`last` is fp32 whatever the storage dtype: fp32 rule (or exact)."""
+    assert_close(got.astype(np.float32), ref.astype(np.float32), "f32", what, exact)

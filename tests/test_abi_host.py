@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point the header declares, rejects bad arguments before touching
+a device, and the occupancy rule picks the expected paths."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lrscan.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lrscan_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        return L.lib()
+    except L.LrscanUnavailable as e:
+        pytest.fail(f"CUDA library not built: {e}")
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("lrscan_fwd", "lrscan_bwd", "lrscan_fwd_ex", "lrscan_bwd_ex", "lrscan_set_stream",
+                     "lrscan_workspace_bytes", "lrscan_sync_check", "lrscan_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in _declared():
+        assert n in L.EXPORTS, f"binding does not declare {n}"
+
+
+def test_version_and_strerror(lib):
+    assert lib.lrscan_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.lrscan_strerror(code)
+    assert L.strerror(-5) == "a bounded device wait timed out"
+
+
+def _fwd(lib, a, b, out, last, B, T, D, dtype):
+    return lib.lrscan_fwd(a, b, out, last, B, T, D, dtype)
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    p = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails validation
+    assert _fwd(lib, p, p, p, None, 1, 8, 8, 7) == L.LRSCAN_EDTYPE
+    assert _fwd(lib, p, p, p, None, -1, 8, 8, 0) == L.LRSCAN_EINVAL
+    assert _fwd(lib, p, p, p, None, 1, -8, 8, 0) == L.LRSCAN_EINVAL
+    assert _fwd(lib, p, p, p, None, 1, 8, -8, 1) == L.LRSCAN_EINVAL
+    assert _fwd(lib, p, p, p, None, 1, 1 << 31, 8, 0) == L.LRSCAN_EINVAL          # T over int32
+    assert _fwd(lib, p, p, p, None, 1 << 40, 1 << 20, 1 << 20, 0) == L.LRSCAN_EINVAL  # byte overflow
+    assert _fwd(lib, None, p, p, None, 1, 8, 8, 0) == L.LRSCAN_EINVAL
+    assert _fwd(lib, p, None, p, None, 1, 8, 8, 0) == L.LRSCAN_EINVAL
+    assert _fwd(lib, p, p, None, None, 1, 8, 8, 0) == L.LRSCAN_EINVAL
+    assert lib.lrscan_bwd(p, p, p, None, p, 1, 8, 8, 0) == L.LRSCAN_EINVAL
+    assert lib.lrscan_bwd(p, p, p, p, p, 1, 8, 8, 3) == L.LRSCAN_EDTYPE
+
+
+def test_empty_problems_are_noops(lib):
+    # B == 0 or D == 0: nothing to do, NULL pointers allowed, no device needed
+    assert _fwd(lib, None, None, None, None, 0, 8, 8, 0) == L.LRSCAN_OK
+    assert _fwd(lib, None, None, None, None, 4, 8, 0, 1) == L.LRSCAN_OK
+    assert lib.lrscan_bwd(None, None, None, None, None, 0, 5, 5, 0) == L.LRSCAN_OK
+    assert lib.lrscan_bwd(None, None, None, None, None, 3, 0, 5, 0) == L.LRSCAN_OK
+
+
+def test_workspace_bytes(lib):
+    # two fp32 [B, ceil(T/C), D] buffers, each rounded up to 256 bytes
+    assert L.lrscan_workspace_bytes(1, 65536, 2560, 64) == 2 * 1024 * 2560 * 4
+    assert L.lrscan_workspace_bytes(2, 100, 3, 16) == 2 * ((2 * 7 * 3 * 4 + 255) // 256 * 256)
+    assert L.lrscan_workspace_bytes(1, 64, 8, 0) == L.lrscan_workspace_bytes(1, 64, 8, 64)
+    assert L.lrscan_workspace_bytes(1, 64, 8, 48) == 0
+
+
+@pytest.mark.parametrize("cid,expect", [(2, "seq"), (3, "window"), (4, "seq"), (5, "seq")])
+def test_occupancy_rule_on_the_named_workloads(lib, cid, expect):
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
+    w = WORKLOADS[cid]
+    for direction in ("fwd", "bwd"):
+        p = L.lrscan_plan(w.B, w.T, w.D, w.dtype, direction)
+        assert p["path"] == expect, (cid, direction, p)
+        # one wave: every CTA resident at once
+        assert p["ctas"] >= 0.9 * 152
+
+
+def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
+    assert p["path"] == "chunk" and p["kernels"] == 3
+    assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
+
+
+def test_unaligned_rows_take_plain_loads(lib):
+    p = L.lrscan_plan(4, 512, 1023, "f32", "fwd")          # D*4 not a multiple of 16
+    assert p["path"] == "plain"
+    p = L.lrscan_plan(4, 512, 1024, "bf16", "fwd", aligned=False)
+    assert p["path"] == "plain"
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(4, 512, 1023, "f32", "fwd", path="seq")   # TMA path cannot take it
+
+
+def test_forced_paths_and_variants(lib):
+    for path in ("seq", "window"):
+        for dt in ("f32", "bf16"):
+            n = L.lrscan_num_variants(path, dt)
+            assert n >= 2
+            names = set()
+            for v in range(1, n + 1):
+                p = L.lrscan_plan(8, 1000, 512, dt, "fwd", path=path, tile_variant=v)
+                assert p["path"] == path and p["tile_variant"] == v
+                names.add(p["name"])
+            assert len(names) == n
+            with pytest.raises(L.LrscanError):
+                L.lrscan_plan(8, 1000, 512, dt, "fwd", path=path, tile_variant=n + 1)
+    p = L.lrscan_plan(8, 1000, 512, "f32", "bwd", path="chunk", chunk_len=32)
+    assert p["path"] == "chunk" and p["rows_per_window"] == 32
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(8, 1000, 512, "f32", "bwd", path="chunk", chunk_len=48)
