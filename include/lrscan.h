@@ -163,6 +163,11 @@ int lrscan_selftest_wait_timeout(uint64_t timeout_ns);
 /* Human-readable text for an error code (static storage). */
 const char *lrscan_strerror(int code);
 
+/* Detail of the calling thread's last failed call (why an argument was
+ * rejected, which launch failed); empty after a successful call.  Valid
+ * until the thread's next call into the library. */
+const char *lrscan_last_error(void);
+
 int lrscan_version(void);
 
 #ifdef __cplusplus

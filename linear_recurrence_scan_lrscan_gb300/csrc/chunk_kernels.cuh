@@ -126,6 +126,12 @@ chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, flo
 // One warp per (row, lane); chunks taken in processing order (ascending for
 // the forward, descending for the backward), 32 per step, UNROLL steps of
 // loads in flight.  Q is overwritten with each chunk's entry state.
+//
+// Identity maps (P == 1, Q == 0 exactly, e.g. chunks made only of padding
+// steps a=1, b=0) are transparent: a chunk's entry state is the composite up
+// to the last non-identity chunk before it, applied to the block's carried
+// state, so every run of identity chunks receives bit-for-bit the same state
+// (a tree-shaped scan would otherwise round differently per lane).
 template <bool REVERSE, int UNROLL>
 __global__ void __launch_bounds__(256)
 chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, long long lanes) {
@@ -153,6 +159,8 @@ chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, 
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             float pu = p[u], qu = q[u];
+            const unsigned live = __ballot_sync(0xffffffffu, !(pu == 1.0f && qu == 0.0f));
+            // inclusive Kogge-Stone over the 32 maps: current ∘ previous
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float pp = __shfl_up_sync(0xffffffffu, pu, off);
@@ -162,17 +170,21 @@ chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, 
                     pu = __fmul_rn(pu, pp);
                 }
             }
-            const float pin = __shfl_up_sync(0xffffffffu, pu, 1);
-            const float qin = __shfl_up_sync(0xffffffffu, qu, 1);
-            const float entry = (lane == 0) ? carry : __fmaf_rn(pin, carry, qin);
-            const float pall = __shfl_sync(0xffffffffu, pu, 31);
-            const float qall = __shfl_sync(0xffffffffu, qu, 31);
+            // entry state: composite up to the last non-identity chunk before this one
+            const unsigned below = live & ((1u << lane) - 1u);
+            const int src = below ? 31 - __clz(below) : 0;
+            const float pin = __shfl_sync(0xffffffffu, pu, src);
+            const float qin = __shfl_sync(0xffffffffu, qu, src);
+            const float entry = below ? __fmaf_rn(pin, carry, qin) : carry;
+            const int last_live = live ? 31 - __clz(live) : 0;
+            const float pall = __shfl_sync(0xffffffffu, pu, last_live);
+            const float qall = __shfl_sync(0xffffffffu, qu, last_live);
             const int idx = c0 + u * 32 + lane;
             if (idx < Nc) {
                 const int c = REVERSE ? Nc - 1 - idx : idx;
                 Q[base + static_cast<size_t>(c) * D] = entry;
             }
-            carry = __fmaf_rn(pall, carry, qall);
+            if (live) carry = __fmaf_rn(pall, carry, qall);
         }
     }
 }

@@ -1,5 +1,5 @@
-// Instantiations and launchers of the time-tiled (TMA) kernels.  The host
-// dispatcher only sees the variant table at the bottom.
+// Instantiations and launchers of the time-tiled (TMA) kernels, and the table
+// of tile variants the host dispatcher chooses from.
 #include "launch.h"
 #include "window_kernels.cuh"
 
@@ -7,117 +7,122 @@ namespace lrscan {
 
 namespace {
 
-template <class C>
-__host__ int set_smem_attr(const void *fn, int dev) {
-    // Dynamic shared memory above 48 KB has to be opted into per device.
-    static unsigned long long done_mask = 0;  // devices done (up to 64)
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev < 64 && (done_mask >> dev) & 1ull) return 0;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return -1;
-    if (dev < 64) done_mask |= 1ull << dev;
+// Dynamic shared memory above 48 KB has to be opted into, per kernel and
+// device; the largest size any variant asks for is set once.
+int set_smem_attr(const void *fn, int dev, unsigned long long *mask, std::mutex *mu) {
+    std::lock_guard<std::mutex> lk(*mu);
+    if (dev < 64 && ((*mask >> dev) & 1ull)) return 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+        return -1;
+    if (dev < 64) *mask |= 1ull << dev;
     return 0;
 }
 
 template <class C>
-int launch_win_fwd(const WinLaunch &L) {
+int launch_win_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
     auto fn = win_fwd_kernel<C>;
-    if (set_smem_attr<C>(reinterpret_cast<const void *>(fn), L.device)) return -1;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.r, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const int nwin = static_cast<int>((L.T + C::W - 1) / C::W);
-    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), C::THREADS, C::SMEM_BYTES, L.stream>>>(
-        *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last, static_cast<int>(L.T),
-        static_cast<int>(L.D), nwin, L.status, L.timeout_ns);
+    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
+        *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last, g, L.status, L.timeout_ns);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 template <class C>
-int launch_win_bwd(const WinLaunch &L) {
+int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
     auto fn = win_bwd_kernel<C>;
-    if (set_smem_attr<C>(reinterpret_cast<const void *>(fn), L.device)) return -1;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.r, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const int nwin = static_cast<int>((L.T + C::W - 1) / C::W);
-    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), C::THREADS, C::SMEM_BYTES, L.stream>>>(
+    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
         *L.maps[0], *L.maps[1], *L.maps[2], static_cast<typename C::St *>(L.out0),
-        static_cast<typename C::St *>(L.out1), static_cast<int>(L.T), static_cast<int>(L.D), nwin,
-        L.status, L.timeout_ns);
+        static_cast<typename C::St *>(L.out1), g, L.status, L.timeout_ns);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-template <class Cf, class Cb>
-constexpr WinVariant make_variant(const char *name) {
-    return WinVariant{name,
-                      Cf::DT,
-                      Cf::V,
-                      Cf::S,
-                      Cf::L,
-                      Cf::W,
-                      Cf::NSTAGE,
-                      Cb::NSTAGE,
-                      Cf::THREADS,
-                      Cf::SMEM_BYTES,
-                      Cb::SMEM_BYTES,
-                      Cf::STAGE_BYTES,
-                      Cb::STAGE_BYTES,
-                      &launch_win_fwd<Cf>,
-                      &launch_win_bwd<Cb>};
+template <class C, bool FWD>
+WinDirCfg dir_cfg(int S, int R, int nstage) {
+    const WinGeom g = make_win_geom<C>(S, R, nstage, 1, 1);
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = S;
+    d.r = g.R;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = S * C::G + 32;
+    d.smem = g.smem_bytes;
+    d.stage_bytes = g.stage_bytes;
+    if constexpr (FWD) {
+        static_assert(C::NIN == 2, "forward tiles: a, b");
+        d.launch = &launch_win_fwd<C>;
+    } else {
+        static_assert(C::NIN == 3, "backward tiles: a, out, grad_out");
+        d.launch = &launch_win_bwd<C>;
+    }
+    return d;
 }
 
-// WinShape<St, DT, V, S, L, NSTAGE, NIN>
-// ---- sequential (S = 1) ----
-using F32_S1_A_f = WinShape<float, 32, 1, 1, 32, 4, 2>;
-using F32_S1_A_b = WinShape<float, 32, 1, 1, 32, 4, 3>;
-using F32_S1_B_f = WinShape<float, 64, 2, 1, 16, 4, 2>;
-using F32_S1_B_b = WinShape<float, 64, 2, 1, 16, 4, 3>;
-using F32_S1_C_f = WinShape<float, 64, 1, 1, 16, 4, 2>;
-using F32_S1_C_b = WinShape<float, 64, 1, 1, 16, 4, 3>;
-using F32_S1_D_f = WinShape<float, 128, 4, 1, 8, 6, 2>;
-using F32_S1_D_b = WinShape<float, 128, 4, 1, 8, 6, 3>;
+// WinShape<St, DT, V, L, NIN, MAXT, MINB>
+// forward shapes (NIN = 2)
+using BF_64_2_16 = WinShape<bf16_t, 64, 2, 16, 2, 64, 8>;
+using BF_128_4_8 = WinShape<bf16_t, 128, 4, 8, 2, 288, 1>;
+using BF_64_2_8 = WinShape<bf16_t, 64, 2, 8, 2, 288, 3>;
+using BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 2, 288, 3>;
+using FF_32_1_16 = WinShape<float, 32, 1, 16, 2, 64, 8>;
+using FF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 3>;
+using FF_128_4_8 = WinShape<float, 128, 4, 8, 2, 64, 4>;
+using FF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1>;
+using FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1>;
+// backward shapes (NIN = 3)
+using BB_64_2_8 = WinShape<bf16_t, 64, 2, 8, 3, 288, 2>;
+using BB_128_4_4 = WinShape<bf16_t, 128, 4, 4, 3, 288, 2>;
+using BB_128_4_8 = WinShape<bf16_t, 128, 4, 8, 3, 288, 1>;
+using BB_32_1_8 = WinShape<bf16_t, 32, 1, 8, 3, 288, 2>;
+using FB_32_1_16 = WinShape<float, 32, 1, 16, 3, 64, 8>;
+using FB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1>;
+using FB_128_4_4 = WinShape<float, 128, 4, 4, 3, 64, 4>;
+using FB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1>;
+using FB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1>;
 
-using B16_S1_A_f = WinShape<bf16_t, 64, 2, 1, 32, 4, 2>;
-using B16_S1_A_b = WinShape<bf16_t, 64, 2, 1, 32, 4, 3>;
-using B16_S1_B_f = WinShape<bf16_t, 128, 2, 1, 32, 4, 2>;
-using B16_S1_B_b = WinShape<bf16_t, 128, 2, 1, 32, 4, 3>;
-using B16_S1_C_f = WinShape<bf16_t, 128, 2, 1, 16, 6, 2>;
-using B16_S1_C_b = WinShape<bf16_t, 128, 2, 1, 16, 6, 3>;
-using B16_S1_D_f = WinShape<bf16_t, 256, 4, 1, 16, 4, 2>;
-using B16_S1_D_b = WinShape<bf16_t, 256, 4, 1, 16, 4, 3>;
+#define F(SH, S, R, N) dir_cfg<SH, true>(S, R, N)
+#define B(SH, S, R, N) dir_cfg<SH, false>(S, R, N)
 
-// ---- windowed (S > 1) ----
-using F32_W_A_f = WinShape<float, 16, 1, 16, 8, 4, 2>;
-using F32_W_A_b = WinShape<float, 16, 1, 16, 8, 4, 3>;
-using F32_W_B_f = WinShape<float, 32, 1, 16, 8, 3, 2>;
-using F32_W_B_b = WinShape<float, 32, 1, 16, 8, 3, 3>;
-using F32_W_C_f = WinShape<float, 16, 1, 32, 4, 4, 2>;
-using F32_W_C_b = WinShape<float, 16, 1, 32, 4, 4, 3>;
-
-using B16_W_A_f = WinShape<bf16_t, 32, 2, 16, 8, 4, 2>;
-using B16_W_A_b = WinShape<bf16_t, 32, 2, 16, 8, 4, 3>;
-using B16_W_B_f = WinShape<bf16_t, 64, 2, 8, 16, 4, 2>;
-using B16_W_B_b = WinShape<bf16_t, 64, 2, 8, 16, 4, 3>;
-
-const WinVariant kSeqF32[] = {
-    make_variant<F32_S1_A_f, F32_S1_A_b>("seq_f32_d32_v1_l32"),
-    make_variant<F32_S1_B_f, F32_S1_B_b>("seq_f32_d64_v2_l16"),
-    make_variant<F32_S1_C_f, F32_S1_C_b>("seq_f32_d64_v1_l16"),
-    make_variant<F32_S1_D_f, F32_S1_D_b>("seq_f32_d128_v4_l8"),
-};
 const WinVariant kSeqBF16[] = {
-    make_variant<B16_S1_A_f, B16_S1_A_b>("seq_bf16_d64_v2_l32"),
-    make_variant<B16_S1_B_f, B16_S1_B_b>("seq_bf16_d128_v2_l32"),
-    make_variant<B16_S1_C_f, B16_S1_C_b>("seq_bf16_d128_v2_l16_s6"),
-    make_variant<B16_S1_D_f, B16_S1_D_b>("seq_bf16_d256_v4_l16"),
-};
-const WinVariant kWinF32[] = {
-    make_variant<F32_W_A_f, F32_W_A_b>("win_f32_d16_s16_l8"),
-    make_variant<F32_W_B_f, F32_W_B_b>("win_f32_d32_s16_l8"),
-    make_variant<F32_W_C_f, F32_W_C_b>("win_f32_d16_s32_l4"),
+    {"seq_bf16_d64", F(BF_64_2_16, 1, 2, 8), B(BB_64_2_8, 1, 4, 6)},
+    {"seq_bf16_d128", F(BF_128_4_8, 1, 4, 6), B(BB_128_4_4, 1, 8, 4)},
+    {"seq_bf16_d64_deep", F(BF_64_2_8, 1, 4, 8), B(BB_64_2_8, 1, 2, 12)},
+    {"seq_bf16_d128_short", F(BF_128_4_8, 1, 2, 8), B(BB_128_4_4, 1, 4, 6)},
 };
 const WinVariant kWinBF16[] = {
-    make_variant<B16_W_A_f, B16_W_A_b>("win_bf16_d32_s16_l8"),
-    make_variant<B16_W_B_f, B16_W_B_b>("win_bf16_d64_s8_l16"),
+    {"win_bf16_d64_s4", F(BF_64_2_8, 4, 1, 8), B(BB_64_2_8, 4, 1, 6)},
+    {"win_bf16_d64_s8", F(BF_64_2_8, 8, 1, 4), B(BB_64_2_8, 8, 1, 3)},
+    {"win_bf16_d32_s8", F(BF_32_1_8, 8, 1, 4), B(BB_32_1_8, 8, 1, 3)},
+    {"win_bf16_d128_s4", F(BF_128_4_8, 4, 1, 6), B(BB_128_4_4, 8, 1, 4)},
+    {"win_bf16_d64_s2", F(BF_64_2_8, 2, 1, 12), B(BB_64_2_8, 2, 1, 10)},
 };
+const WinVariant kSeqF32[] = {
+    {"seq_f32_d32", F(FF_32_1_16, 1, 2, 8), B(FB_32_1_16, 1, 2, 6)},
+    {"seq_f32_d64", F(FF_64_2_8, 1, 4, 6), B(FB_64_2_8, 1, 4, 4)},
+    {"seq_f32_d128", F(FF_128_4_8, 1, 2, 6), B(FB_128_4_4, 1, 4, 4)},
+    {"seq_f32_d64_short", F(FF_64_2_8, 1, 2, 8), B(FB_64_2_8, 1, 2, 6)},
+};
+const WinVariant kWinF32[] = {
+    {"win_f32_d16_s16", F(FF_16_1_8, 16, 1, 4), B(FB_16_1_8, 16, 1, 4)},
+    {"win_f32_d32_s16", F(FF_32_1_8, 16, 1, 4), B(FB_32_1_8, 16, 1, 3)},
+    {"win_f32_d32_s8", F(FF_32_1_8, 8, 1, 8), B(FB_32_1_8, 8, 1, 6)},
+    {"win_f32_d16_s8", F(FF_16_1_8, 8, 1, 8), B(FB_16_1_8, 8, 1, 6)},
+    {"win_f32_d32_s4", F(FF_32_1_8, 4, 1, 12), B(FB_32_1_8, 4, 1, 10)},
+};
+
+#undef F
+#undef B
 
 }  // namespace
 

@@ -29,19 +29,25 @@ struct WinLaunch {
     int device;
 };
 
-struct WinVariant {
-    const char *name;
+// One direction of a tile variant: compiled shape (DT, V, L) plus the
+// launch-time sub-chunk count S, register batches R and pipeline depth.
+struct WinDirCfg {
     int dt;          // lanes per CTA
     int v;           // lanes per thread
+    int l;           // steps per sub-chunk (registers)
     int s;           // sub-chunks per window
-    int l;           // steps per sub-chunk
-    int w;           // rows per window
-    int nstage_fwd, nstage_bwd;
-    int threads;
-    int smem_fwd, smem_bwd;
-    int stage_bytes_fwd, stage_bytes_bwd;
-    int (*fwd)(const WinLaunch &);
-    int (*bwd)(const WinLaunch &);
+    int r;           // register batches per window (S == 1)
+    int w;           // rows per window = s*l*r
+    int nstage;      // pipeline depth
+    int threads;     // s*(dt/v) + 32
+    int smem;        // dynamic shared memory bytes
+    int stage_bytes;
+    int (*launch)(const WinLaunch &, const WinDirCfg &);
+};
+
+struct WinVariant {
+    const char *name;
+    WinDirCfg fwd, bwd;
 };
 
 // path: kPathSeq or kPathWindow; dtype 0 = f32, 1 = bf16

@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -37,6 +38,17 @@ std::mutex g_mu;
 DeviceCtx g_dev[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 thread_local cudaStream_t t_stream = nullptr;
+thread_local char t_detail[256] = "";
+
+// Records why a call failed (read back by lrscan_last_error) and returns code.
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(t_detail, sizeof t_detail, fmt, ap);
+    va_end(ap);
+    return code;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Description used when no device is visible (plans only): one GB300.
@@ -108,6 +120,7 @@ struct Choice {
     size_t workspace = 0;
     long long ctas = 0;
     int threads = 0, smem = 0, stages = 0, kernels = 1;
+    int dir = 0;
 };
 
 struct Occ {
@@ -117,10 +130,13 @@ struct Occ {
     double inflight; // bytes in flight per SM, estimated
 };
 
-Occ occupancy(const WinVariant &v, int dir, int64_t B, int64_t D, const Geometry &g) {
-    const int smem = dir == 0 ? v.smem_fwd : v.smem_bwd;
-    const int nst = dir == 0 ? v.nstage_fwd : v.nstage_bwd;
-    const int stage = dir == 0 ? v.stage_bytes_fwd : v.stage_bytes_bwd;
+const WinDirCfg &dir_of(const WinVariant &v, int dir) { return dir == 0 ? v.fwd : v.bwd; }
+
+Occ occupancy(const WinVariant &var, int dir, int64_t B, int64_t D, const Geometry &g) {
+    const WinDirCfg &v = dir_of(var, dir);
+    const int smem = v.smem;
+    const int nst = v.nstage;
+    const int stage = v.stage_bytes;
     Occ o;
     o.ctas = B * ((D + v.dt - 1) / v.dt);
     int r_smem = smem > g.smem_optin ? 0 : g.smem_per_sm / (smem + 1024);
@@ -155,7 +171,7 @@ int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, cons
         const double waves = std::ceil(static_cast<double>(o.ctas) / slots);
         const double fill = static_cast<double>(o.ctas) / (waves * slots);
         const double score = (o.one_wave ? 2e6 : 1e6 * fill) + std::min(o.inflight, 96.0 * 1024) +
-                             tab[i].dt * sizeof(float);
+                             dir_of(tab[i], dir).dt * sizeof(float);
         if (score > best_score) {
             best_score = score;
             best = i;
@@ -170,14 +186,15 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
     const int want = opts ? opts->path : 0;
     const int force_v = opts ? opts->tile_variant : 0;
     int chunk = opts && opts->chunk_len ? opts->chunk_len : 64;
-    if (chunk != 16 && chunk != 32 && chunk != 64) return LRSCAN_EINVAL;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return fail(LRSCAN_EINVAL, "chunk_len %d is not 16, 32 or 64", chunk);
     ch->chunk = chunk;
     const int vmax = dtype == LRSCAN_F32 ? 4 : 8;
     ch->vec = (aligned16 && D % vmax == 0) ? vmax : 1;
 
     int path = want;
-    if (want < kPathAuto || want > kPathPlain) return LRSCAN_EINVAL;
-    if ((path == kPathSeq || path == kPathWindow) && !aligned16) return LRSCAN_EINVAL;
+    if (want < kPathAuto || want > kPathPlain) return fail(LRSCAN_EINVAL, "unknown path %d", want);
+    if ((path == kPathSeq || path == kPathWindow) && !aligned16)
+        return fail(LRSCAN_EINVAL, "path %d needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)", path);
     if (path == kPathAuto) {
         int vi = -1;
         if (!aligned16) {
@@ -200,7 +217,7 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         const WinVariant *tab = win_variants(path, dtype, &n);
         int vi = -1;
         if (force_v > 0) {
-            if (force_v > n) return LRSCAN_EINVAL;
+            if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
             vi = force_v - 1;
         } else if (!pick_window_variant(path, dtype, dir, B, D, g, &vi)) {
             // too few lanes to fill the GPU (or too many for one wave): take the
@@ -212,26 +229,27 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
                 if (o.ctas > most) { most = o.ctas; vi = i; }
             }
         }
-        if (vi < 0) return LRSCAN_EINVAL;
+        if (vi < 0) return fail(LRSCAN_EINVAL, "no tile variant fits this device");
         ch->vidx = vi;
         ch->var = &tab[vi];
         Occ o = occupancy(tab[vi], dir, B, D, g);
-        if (o.resident == 0) return LRSCAN_EINVAL;
+        if (o.resident == 0) return fail(LRSCAN_EINVAL, "tile variant %s does not fit on an SM", tab[vi].name);
         ch->ctas = o.ctas;
-        ch->threads = tab[vi].threads;
-        ch->smem = dir == 0 ? tab[vi].smem_fwd : tab[vi].smem_bwd;
-        ch->stages = dir == 0 ? tab[vi].nstage_fwd : tab[vi].nstage_bwd;
+        ch->threads = dir_of(tab[vi], dir).threads;
+        ch->smem = dir_of(tab[vi], dir).smem;
+        ch->stages = dir_of(tab[vi], dir).nstage;
+        ch->dir = dir;
         ch->kernels = 1;
         ch->workspace = 0;
     } else if (path == kPathChunk) {
-        if (force_v > 1) return LRSCAN_EINVAL;
+        if (force_v > 1) return fail(LRSCAN_EINVAL, "the chunked path has one variant");
         const int64_t nc = (T + chunk - 1) / chunk;
         ch->ctas = B * nc * ((D / ch->vec + 127) / 128);
         ch->threads = 128;
         ch->kernels = 3;
         ch->workspace = chunk_workspace(B, T, D, chunk);
     } else {  // plain
-        if (force_v > 1) return LRSCAN_EINVAL;
+        if (force_v > 1) return fail(LRSCAN_EINVAL, "the plain path has one variant");
         ch->ctas = B * ((D + 127) / 128);
         ch->threads = 128;
         ch->kernels = 1;
@@ -252,9 +270,10 @@ void fill_info(const Choice &c, lrscan_plan_info *info) {
     info->workspace_bytes = c.workspace;
     info->subchunks = 1;
     if (c.var) {
-        info->lanes_per_cta = c.var->dt;
-        info->rows_per_window = c.var->w;
-        info->subchunks = c.var->s;
+        const WinDirCfg &d = dir_of(*c.var, c.dir);
+        info->lanes_per_cta = d.dt;
+        info->rows_per_window = d.w;
+        info->subchunks = d.s;
         std::snprintf(info->name, sizeof info->name, "%s", c.var->name);
     } else if (c.path == kPathChunk) {
         info->lanes_per_cta = 128 * c.vec;
@@ -279,17 +298,23 @@ int encode_map(CUtensorMap *m, const void *ptr, int dtype, int64_t B, int64_t T,
                           3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? LRSCAN_OK : LRSCAN_EINVAL;
+    if (r != CUDA_SUCCESS)
+        return fail(LRSCAN_EINVAL, "cuTensorMapEncodeTiled failed (%d) for ptr %p dims {%lld,%lld,%lld} box {%d,%d}",
+                    static_cast<int>(r), ptr, static_cast<long long>(D), static_cast<long long>(T),
+                    static_cast<long long>(B), dt, w);
+    return LRSCAN_OK;
 }
 
 int check_shape(int64_t B, int64_t T, int64_t D, int dtype) {
-    if (dtype != LRSCAN_F32 && dtype != LRSCAN_BF16) return LRSCAN_EDTYPE;
-    if (B < 0 || T < 0 || D < 0) return LRSCAN_EINVAL;
-    if (T > 0x7fffffffLL || D > 0x7fffffffLL) return LRSCAN_EINVAL;
+    if (dtype != LRSCAN_F32 && dtype != LRSCAN_BF16) return fail(LRSCAN_EDTYPE, "dtype %d", dtype);
+    if (B < 0 || T < 0 || D < 0)
+        return fail(LRSCAN_EINVAL, "negative size B=%lld T=%lld D=%lld", static_cast<long long>(B),
+                    static_cast<long long>(T), static_cast<long long>(D));
+    if (T > 0x7fffffffLL || D > 0x7fffffffLL) return fail(LRSCAN_EINVAL, "T or D above 2^31-1");
     int64_t e = 0, bytes = 0;
     if (__builtin_mul_overflow(B, T, &e) || __builtin_mul_overflow(e, D, &e) ||
         __builtin_mul_overflow(e, static_cast<int64_t>(esize(dtype)), &bytes))
-        return LRSCAN_EINVAL;
+        return fail(LRSCAN_EINVAL, "B*T*D*elem overflows int64");
     return LRSCAN_OK;
 }
 
@@ -303,7 +328,8 @@ bool aligned16(std::initializer_list<const void *> ps, int64_t D, int dtype) {
 int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opts *opts, void **ws) {
     if (opts && opts->workspace) {
         if (opts->workspace_bytes < need || reinterpret_cast<uintptr_t>(opts->workspace) % 256 != 0)
-            return LRSCAN_ENOMEM;
+            return fail(LRSCAN_ENOMEM, "caller workspace of %zu bytes (need %zu, 256-byte aligned)",
+                        opts->workspace_bytes, need);
         *ws = opts->workspace;
         return LRSCAN_OK;
     }
@@ -319,7 +345,7 @@ int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opt
         void *p = nullptr;
         if (cudaMalloc(&p, need) != cudaSuccess) {
             cudaGetLastError();
-            return LRSCAN_ENOMEM;
+            return fail(LRSCAN_ENOMEM, "cudaMalloc of %zu workspace bytes failed", need);
         }
         slot.first = p;
         slot.second = need;
@@ -332,6 +358,7 @@ cudaStream_t pick_stream(void *stream) { return stream ? static_cast<cudaStream_
 
 int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype,
             void *stream, const lrscan_opts *opts) {
+    t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
     if (B == 0 || D == 0) return LRSCAN_OK;
@@ -340,7 +367,7 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
         if (last && cudaMemsetAsync(last, 0, static_cast<size_t>(B) * D * 4, st) != cudaSuccess) return LRSCAN_ECUDA;
         return LRSCAN_OK;
     }
-    if (!a || !b || !out) return LRSCAN_EINVAL;
+    if (!a || !b || !out) return fail(LRSCAN_EINVAL, "NULL a, b or out");
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx))) return rc;
     int dev = 0;
@@ -350,7 +377,7 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
     if ((rc = plan_call(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
     const size_t es = esize(dtype);
     if (ch.path == kPathSeq || ch.path == kPathWindow) {
-        const WinVariant &v = *ch.var;
+        const WinDirCfg &v = ch.var->fwd;
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
             const size_t off = static_cast<size_t>(b0) * T * D * es;
@@ -368,7 +395,8 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
             L.timeout_ns = g_timeout_ns.load();
             L.stream = st;
             L.device = dev;
-            if (v.fwd(L)) return LRSCAN_ECUDA;
+            if (v.launch(L, v))
+                return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
         }
         return LRSCAN_OK;
     }
@@ -387,10 +415,11 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
 
 int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B, int64_t T,
             int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
     if (B == 0 || D == 0 || T == 0) return LRSCAN_OK;
-    if (!a || !out || !grad_out || !grad_a || !grad_b) return LRSCAN_EINVAL;
+    if (!a || !out || !grad_out || !grad_a || !grad_b) return fail(LRSCAN_EINVAL, "NULL a, out, grad_out, grad_a or grad_b");
     cudaStream_t st = pick_stream(stream);
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx))) return rc;
@@ -401,7 +430,7 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
     if ((rc = plan_call(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
     const size_t es = esize(dtype);
     if (ch.path == kPathSeq || ch.path == kPathWindow) {
-        const WinVariant &v = *ch.var;
+        const WinDirCfg &v = ch.var->bwd;
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
             const size_t off = static_cast<size_t>(b0) * T * D * es;
@@ -421,7 +450,8 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
             L.timeout_ns = g_timeout_ns.load();
             L.stream = st;
             L.device = dev;
-            if (v.bwd(L)) return LRSCAN_ECUDA;
+            if (v.launch(L, v))
+                return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
         }
         return LRSCAN_OK;
     }
@@ -554,5 +584,7 @@ const char *lrscan_strerror(int code) {
 }
 
 int lrscan_version(void) { return LRSCAN_VERSION; }
+
+const char *lrscan_last_error(void) { return t_detail; }
 
 }  // extern "C"

@@ -120,8 +120,12 @@ __device__ __forceinline__ void store_lanes(St *p, const float (&x)[V]) {
             p[0] = x[0];
         } else if constexpr (V == 2) {
             *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
-        } else {
+        } else if constexpr (V == 4) {
             *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        } else {
+            static_assert(V == 8, "fp32 stores of 1, 2, 4 or 8 lanes");
+            *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4 *>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
         }
     } else {
         if constexpr (V == 1) {

@@ -1,118 +1,143 @@
 // Time-tiled scan kernels: a CTA owns one batch row and DT channel lanes and
 // walks the whole sequence in windows of W = S*L time steps.  A producer warp
-// streams the windows' input tiles into a ring of NSTAGE shared-memory stages
-// with 3-D bulk tensor copies (TMA) completed on mbarriers; consumer threads
-// keep the recurrence state in fp32 registers.
+// streams the windows' input tiles into a ring of shared-memory stages with
+// 3-D bulk tensor copies (TMA) completed on mbarriers.  Consumer thread
+// (s, g) owns lanes [g*V, g*V+V) of sub-chunk s (rows s*L .. s*L+L-1 of the
+// window): it copies its rows into registers, releases the stage at once so
+// the producer can refill it, and keeps the recurrence state in fp32.
 //
-//  S == 1  ("seq"): each consumer thread owns V lanes and runs the recurrence
-//          straight through every window, one fused multiply-add per step --
-//          bit-identical to the sequential definition.
-//  S  > 1  ("window"): the W rows of a window are split into S sub-chunks of
-//          L steps.  Thread (s, lane group) summarizes its sub-chunk as the
-//          affine map h -> P*h + Q (triton_training_scan.py,
-//          _real_chunk_summary), the sub-chunk entry states follow from the
-//          window's carried state through the maps of the earlier sub-chunks
-//          (_real_chunk_prefix, here inside one CTA), and every thread
-//          replays its sub-chunk (_real_chunk_replay).  One pass over HBM:
-//          3 elements per (t, d) forward, 5 backward.
+//  S == 1  ("seq"): every thread runs the recurrence straight through all
+//          windows, one fused multiply-add per step, bit-identical to the
+//          sequential definition.  No barrier between consumer warps.
+//  S  > 1  ("window"): thread (s, g) summarizes its sub-chunk as the affine
+//          map h -> P*h + Q (triton_training_scan.py, _real_chunk_summary),
+//          pushes the window's carried state through the maps of sub-chunks
+//          0..s-1 (the serial prefix of _real_chunk_prefix, inside one CTA;
+//          identity maps leave the state bit-for-bit unchanged), and replays
+//          its sub-chunk (_real_chunk_replay).  One pass over HBM: 3 elements
+//          per (t, d) forward, 5 backward.
+//
+// With G = DT/V = 32 a warp is exactly one sub-chunk row range, so its
+// shared-memory reads of one row are 32 consecutive words (conflict-free).
 //
 // Backward windows run last-to-first.  The decay tile is loaded one row late
 // (a_{t+1}) and the out tile one row early (h_{t-1}), so the tensor copy's zero
 // fill supplies a_T = 0 and h_{-1} = 0 at the sequence ends; the reverse
 // recurrence g_t = fma(a_{t+1}, g_{t+1}, grad_out_t) then has the same shape
 // as the forward one.
+//
+// S and the stage count are launch-time parameters; DT, V and L are compiled.
 #pragma once
 
 #include "scan_common.cuh"
 
 namespace lrscan {
 
-template <typename St_, int DT_, int V_, int S_, int L_, int NSTAGE_, int NIN_>
+// Compile-time shape.  MAXT / MINB feed __launch_bounds__.
+template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_>
 struct WinShape {
     using St = St_;
-    static constexpr int DT = DT_;        // lanes per CTA
-    static constexpr int V = V_;          // lanes per thread
-    static constexpr int S = S_;          // sub-chunks per window
-    static constexpr int L = L_;          // steps per sub-chunk
-    static constexpr int NSTAGE = NSTAGE_;
-    static constexpr int NIN = NIN_;      // input tiles per window (2 fwd, 3 bwd)
-    static constexpr int G = DT / V;      // lane groups per row
-    static constexpr int NT = S * G;      // consumer threads
-    static constexpr int NWARP_C = NT / 32;
-    static constexpr int THREADS = NT + 32;  // + one producer warp
-    static constexpr int W = S * L;       // rows per window
-    static constexpr int TILE_BYTES = W * DT * (int)sizeof(St);
-    static constexpr int STAGE_BYTES = NIN * TILE_BYTES;
-    static constexpr int TILES_BYTES = NSTAGE * STAGE_BYTES;
-    static constexpr int BAR_OFF = TILES_BYTES;
-    static constexpr int SCAN_OFF = BAR_OFF + 2 * NSTAGE * 8;
-    static constexpr int SCAN_BYTES = (S > 1) ? (2 * 2 * S * DT + 2 * DT) * 4 : 0;
-    static constexpr int FLAG_OFF = SCAN_OFF + SCAN_BYTES;
-    static constexpr int SMEM_BYTES = FLAG_OFF + 16;
-
+    static constexpr int DT = DT_;    // lanes per CTA
+    static constexpr int V = V_;      // lanes per thread
+    static constexpr int L = L_;      // steps per sub-chunk (held in registers)
+    static constexpr int NIN = NIN_;  // input tiles per window (2 forward, 3 backward)
+    static constexpr int G = DT / V;  // lane groups per row
+    static constexpr int MAXT = MAXT_;
+    static constexpr int MINB = MINB_;
+    static constexpr int ROW_BYTES = DT * static_cast<int>(sizeof(St));
     static_assert(DT % V == 0, "lane tile must split into lane groups");
-    static_assert(NT % 32 == 0, "consumers must be whole warps");
-    static_assert(TILE_BYTES % 128 == 0, "tiles must stay 128-byte aligned");
-    static_assert((DT * (int)sizeof(St)) % 16 == 0, "tensor-copy rows are multiples of 16 bytes");
-    static_assert(DT <= 256 && W <= 256, "tensor-copy box limit");
-    static_assert(S == 1 || L <= 16, "window sub-chunks are held in registers");
+    static_assert(ROW_BYTES % 16 == 0, "tensor-copy rows are multiples of 16 bytes");
+    static_assert(DT <= 256, "tensor-copy box limit");
+    static_assert(L >= 1 && L <= 32, "sub-chunk rows are held in registers");
 };
+
+// Launch-time geometry (filled by the host from S and the stage count).
+struct WinGeom {
+    int S;             // sub-chunks per window
+    int R;             // register batches of L rows per window (S == 1 only; 1 otherwise)
+    int nstage;        // pipeline depth
+    int W;             // rows per window = S*L*R
+    int tile_bytes;    // W * ROW_BYTES
+    int stage_bytes;   // NIN * tile_bytes
+    int bar_off;       // byte offsets into dynamic shared memory
+    int scan_off;
+    int flag_off;
+    int smem_bytes;
+    int T, D, nwin;
+};
+
+template <class C>
+__host__ __device__ inline WinGeom make_win_geom(int S, int R, int nstage, int T, int D) {
+    WinGeom g{};
+    g.S = S;
+    g.R = S == 1 ? R : 1;
+    g.nstage = nstage;
+    g.W = S * C::L * g.R;
+    g.tile_bytes = g.W * C::ROW_BYTES;
+    g.stage_bytes = C::NIN * g.tile_bytes;
+    g.bar_off = nstage * g.stage_bytes;
+    g.scan_off = g.bar_off + 2 * nstage * 8;
+    // P,Q exchange [parity][S][DT] float2 and the carried state [parity][DT]
+    const int scan_bytes = S > 1 ? (2 * S * C::DT * 8 + 2 * C::DT * 4) : 0;
+    g.flag_off = g.scan_off + scan_bytes;
+    g.smem_bytes = g.flag_off + 16;
+    g.T = T;
+    g.D = D;
+    g.nwin = (T + g.W - 1) / g.W;
+    return g;
+}
 
 struct WinSmem {
     unsigned char *base;
+    const WinGeom *g;
     template <class C> __device__ __forceinline__ typename C::St *tile(int stage, int which) const {
-        return reinterpret_cast<typename C::St *>(base + stage * C::STAGE_BYTES + which * C::TILE_BYTES);
+        return reinterpret_cast<typename C::St *>(base + stage * g->stage_bytes + which * g->tile_bytes);
     }
-    template <class C> __device__ __forceinline__ uint32_t full_bar(int stage) const {
-        return smem_addr(base + C::BAR_OFF + stage * 8);
+    __device__ __forceinline__ uint32_t full_bar(int stage) const { return smem_addr(base + g->bar_off + stage * 8); }
+    __device__ __forceinline__ uint32_t empty_bar(int stage) const {
+        return smem_addr(base + g->bar_off + (g->nstage + stage) * 8);
     }
-    template <class C> __device__ __forceinline__ uint32_t empty_bar(int stage) const {
-        return smem_addr(base + C::BAR_OFF + (C::NSTAGE + stage) * 8);
-    }
-    // P,Q exchange buffers [parity][S][DT] and carried state [parity][DT]
-    template <class C> __device__ __forceinline__ float *sP(int par) const {
-        return reinterpret_cast<float *>(base + C::SCAN_OFF) + par * C::S * C::DT;
-    }
-    template <class C> __device__ __forceinline__ float *sQ(int par) const {
-        return reinterpret_cast<float *>(base + C::SCAN_OFF) + (2 + par) * C::S * C::DT;
+    template <class C> __device__ __forceinline__ float2 *sPQ(int par) const {
+        return reinterpret_cast<float2 *>(base + g->scan_off) + par * g->S * C::DT;
     }
     template <class C> __device__ __forceinline__ float *sCarry(int par) const {
-        return reinterpret_cast<float *>(base + C::SCAN_OFF) + 4 * C::S * C::DT + par * C::DT;
+        return reinterpret_cast<float *>(base + g->scan_off + 2 * g->S * C::DT * 8) + par * C::DT;
     }
-    template <class C> __device__ __forceinline__ volatile int *abort_flag() const {
-        return reinterpret_cast<volatile int *>(base + C::FLAG_OFF);
+    __device__ __forceinline__ volatile int *abort_flag() const {
+        return reinterpret_cast<volatile int *>(base + g->flag_off);
     }
 };
 
-// Producer: one elected lane streams `nwin` windows into the stage ring, in
-// processing order.  `row_of(k, i)` gives the time coordinate of input tile i
-// of the k-th processed window.  Before returning (normally or on abort) it
+// Producer: one elected lane streams the windows into the stage ring in
+// processing order; row_of(k, i) is the time coordinate of input tile i of
+// the k-th processed window.  Before returning (normally or on abort) it
 // waits, bounded, for every copy it issued, so none lands after the CTA exits.
 template <class C, class RowOf>
-__device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMap *const (&maps)[C::NIN],
-                                             int nwin, int x0, int z, RowOf row_of, const WaitCtx &wc) {
+__device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMap *const (&maps)[C::NIN], int x0,
+                                             int z, RowOf row_of, const WaitCtx &wc) {
+    const WinGeom &g = *sm.g;
     for (int i = 0; i < C::NIN; ++i) prefetch_tensormap(maps[i]);
     int issued = 0;
-    for (int k = 0; k < nwin; ++k) {
-        const int stage = k % C::NSTAGE;
-        const int use = k / C::NSTAGE;
-        if (use > 0 && !mbar_wait(sm.empty_bar<C>(stage), (use - 1) & 1, wc, kSiteProducerEmpty)) break;
-        const uint32_t fb = sm.full_bar<C>(stage);
-        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+    int stage = 0, use = 0;
+    for (int k = 0; k < g.nwin; ++k) {
+        if (use > 0 && !mbar_wait(sm.empty_bar(stage), (use - 1) & 1, wc, kSiteProducerEmpty)) break;
+        const uint32_t fb = sm.full_bar(stage);
+        mbar_arrive_expect_tx(fb, g.stage_bytes);
 #pragma unroll
         for (int i = 0; i < C::NIN; ++i)
             tma_load_3d(smem_addr(sm.tile<C>(stage, i)), maps[i], x0, row_of(k, i), z, fb);
         issued = k + 1;
+        if (++stage == g.nstage) { stage = 0; ++use; }
     }
     // Drain: the most recent fill of each stage must have landed.
-    const int first = issued > C::NSTAGE ? issued - C::NSTAGE : 0;
+    const int first = issued > g.nstage ? issued - g.nstage : 0;
     for (int k = first; k < issued; ++k) {
-        const int stage = k % C::NSTAGE;
-        const uint32_t fb = sm.full_bar<C>(stage);
-        if (mbar_try_wait(fb, (k / C::NSTAGE) & 1)) continue;
-        // A bounded wait that ignores the abort flag: copies in flight always land.
+        const uint32_t fb = sm.full_bar(k % g.nstage);
+        const uint32_t par = (k / g.nstage) & 1;
+        if (mbar_try_wait(fb, par)) continue;
+        // bounded, and deliberately blind to the abort flag: copies in flight always land
         const uint64_t start = global_timer_ns();
-        while (!mbar_try_wait(fb, (k / C::NSTAGE) & 1)) {
+        while (!mbar_try_wait(fb, par)) {
             if (global_timer_ns() - start > wc.timeout_ns) {
                 record_error(wc, kErrTimeout, kSiteDrain);
                 break;
@@ -121,19 +146,20 @@ __device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMa
     }
 }
 
-template <class C>
-__device__ __forceinline__ void win_init(const WinSmem &sm) {
+__device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S, int DT) {
+    const WinGeom &g = *sm.g;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NSTAGE; ++s) {
-            mbar_init(sm.full_bar<C>(s), 1);
-            mbar_init(sm.empty_bar<C>(s), C::NWARP_C);
+        for (int s = 0; s < g.nstage; ++s) {
+            mbar_init(sm.full_bar(s), 1);
+            mbar_init(sm.empty_bar(s), consumer_warps);
         }
-        *sm.abort_flag<C>() = 0;
+        *sm.abort_flag() = 0;
         fence_mbar_init();
     }
-    if constexpr (C::S > 1) {
+    if (S > 1) {
         // carried state starts at zero (h_{-1} = 0 forward, g_T = 0 backward)
-        for (int i = threadIdx.x; i < 2 * C::DT; i += blockDim.x) sm.sCarry<C>(0)[i] = 0.0f;
+        float *c = reinterpret_cast<float *>(sm.base + g.scan_off + 2 * g.S * DT * 8);
+        for (int i = threadIdx.x; i < 2 * DT; i += blockDim.x) c[i] = 0.0f;
     }
     __syncthreads();
 }
@@ -142,28 +168,32 @@ __device__ __forceinline__ void win_init(const WinSmem &sm) {
 // Forward
 // ============================================================================
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-               typename C::St *__restrict__ out, float *__restrict__ last, int T, int D, int nwin,
+               typename C::St *__restrict__ out, float *__restrict__ last, const __grid_constant__ WinGeom geom,
                DevStatus *status, uint64_t timeout_ns) {
     using St = typename C::St;
-    constexpr int V = C::V, L = C::L, S = C::S, DT = C::DT, G = C::G;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const WinSmem sm{smem_raw};
-    win_init<C>(sm);
-    const WaitCtx wc{status, sm.abort_flag<C>(), timeout_ns};
+    const WinSmem sm{smem_raw, &geom};
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init(sm, NT / 32, S, DT);
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = geom.T, D = geom.D;
 
-    if (warp == C::NWARP_C) {  // producer warp
-        if (lane == 0) {
+    if (static_cast<int>(threadIdx.x) >= NT) {  // producer warp
+        if (static_cast<int>(threadIdx.x) == NT) {
             const CUtensorMap *const maps[2] = {&tm_a, &tm_b};
-            win_producer<C>(sm, maps, nwin, d0, brow, [](int k, int) { return k * C::W; }, wc);
+            const int W = geom.W;
+            win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
         }
         return;
     }
 
+    const int lane = threadIdx.x & 31;
     const int s = threadIdx.x / G;
     const int lg = threadIdx.x - s * G;
     const int d = d0 + lg * V;
@@ -173,113 +203,106 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
     for (int v = 0; v < V; ++v) h[v] = 0.0f;
     bool failed = false;
+    int stage = 0, use = 0;
 
-    for (int k = 0; k < nwin; ++k) {
-        const int stage = k % C::NSTAGE;
-        const int t0 = k * C::W;
-        const int rbase = t0 + s * L;
-        const int n = min(max(T - rbase, 0), L);
+    for (int k = 0; k < geom.nwin; ++k) {
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
         const St *tb = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;
-        St *op = out + (row0 + rbase) * D + d;
-        bool ok = mbar_wait(sm.full_bar<C>(stage), (k / C::NSTAGE) & 1, wc, kSiteConsumerFull);
-
-        if constexpr (S == 1) {
+        if (S == 1) {
             if (!ok) { failed = true; break; }
-            if (n == L) {
+            // R register batches of L rows, straight through: one fma per step
+            for (int r = 0; r < geom.R; ++r) {
+                const int rbase = k * geom.W + r * L;
+                const int n = min(max(T - rbase, 0), L);
+                float xa[L][V], xb[L][V];
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
-                    float x[V], y[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(tb + j * DT, y);
-#pragma unroll
-                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
-                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
+                    unpack_lanes<St, V>(ta + (r * L + j) * DT, xa[j]);
+                    unpack_lanes<St, V>(tb + (r * L + j) * DT, xb[j]);
                 }
-            } else {
-                for (int j = 0; j < n; ++j) {
-                    float x[V], y[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(tb + j * DT, y);
-#pragma unroll
-                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
-                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty_bar<C>(stage));
-        } else {
-            float xa[L][V], xb[L][V];
-            if (ok) {
+                St *op = out + (row0 + rbase) * D + d;
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
-                    unpack_lanes<St, V>(ta + j * DT, xa[j]);
-                    unpack_lanes<St, V>(tb + j * DT, xb[j]);
-                }
-            }
-            __syncwarp();
-            if (ok && lane == 0) mbar_arrive(sm.empty_bar<C>(stage));
-            // sub-chunk summary h -> P*h + Q (empty tail sub-chunks are the identity map)
-            float P[V], Q[V];
+                    if (j < n) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
-#pragma unroll
-            for (int j = 0; j < L; ++j) {
-                if (j < n) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        P[v] = __fmul_rn(xa[j][v], P[v]);
-                        Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
+                        for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+                        if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
                     }
                 }
             }
-            const int par = k & 1;
-            float *sp = sm.sP<C>(par), *sq = sm.sQ<C>(par);
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                sp[s * DT + lg * V + v] = P[v];
-                sq[s * DT + lg * V + v] = Q[v];
-            }
-            if (bar_sync_or(1, C::NT, !ok)) { failed = true; break; }
-            // entry state of this sub-chunk: the window's carried state pushed
-            // through the maps of sub-chunks 0..s-1, in order
-            const float *carry = sm.sCarry<C>(par);
-#pragma unroll
-            for (int v = 0; v < V; ++v) h[v] = carry[lg * V + v];
-#pragma unroll
-            for (int sp_i = 0; sp_i < S - 1; ++sp_i) {
-                if (sp_i < s) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        h[v] = __fmaf_rn(sp[sp_i * DT + lg * V + v], h[v], sq[sp_i * DT + lg * V + v]);
-                }
-            }
-            // replay
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+            if (++stage == geom.nstage) { stage = 0; ++use; }
+            continue;
+        }
+
+        const int rbase = k * geom.W + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float xa[L][V], xb[L][V];
+        if (ok) {
 #pragma unroll
             for (int j = 0; j < L; ++j) {
-                if (j < n) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
-                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
-                }
-            }
-            if (s == S - 1) {
-                float *nc = sm.sCarry<C>(par ^ 1);
-#pragma unroll
-                for (int v = 0; v < V; ++v) nc[lg * V + v] = h[v];
-            }
-            // the thread whose sub-chunk holds step T-1 owns the final state
-            if (last != nullptr && lane_ok && n > 0 && rbase + n == T) {
-#pragma unroll
-                for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+                unpack_lanes<St, V>(ta + j * DT, xa[j]);
+                unpack_lanes<St, V>(tb + j * DT, xb[j]);
             }
         }
-    }
-    if constexpr (S == 1) {
-        if (!failed && last != nullptr && lane_ok) {
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == geom.nstage) { stage = 0; ++use; }
+        // sub-chunk summary h -> P*h + Q (an empty tail sub-chunk is the identity)
+        float P[V], Q[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            if (j < n) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    P[v] = __fmul_rn(xa[j][v], P[v]);
+                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
+                }
+            }
+        }
+        const int par = k & 1;
+        float2 *pq = sm.sPQ<C>(par);
+#pragma unroll
+        for (int v = 0; v < V; ++v) pq[s * DT + lg * V + v] = make_float2(P[v], Q[v]);
+        if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
+        // entry state: the carried state pushed through sub-chunks 0..s-1 in order
+        const float *carry = sm.sCarry<C>(par);
+#pragma unroll
+        for (int v = 0; v < V; ++v) h[v] = carry[lg * V + v];
+        for (int i = 0; i < s; ++i) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float2 m = pq[i * DT + lg * V + v];
+                h[v] = __fmaf_rn(m.x, h[v], m.y);
+            }
+        }
+        St *op = out + (row0 + rbase) * D + d;
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            if (j < n) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+                if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
+            }
+        }
+        if (s == S - 1) {
+            float *nc = sm.sCarry<C>(par ^ 1);
+#pragma unroll
+            for (int v = 0; v < V; ++v) nc[lg * V + v] = h[v];
+        }
+        // the thread whose sub-chunk holds step T-1 owns the final state
+        if (last != nullptr && lane_ok && n > 0 && rbase + n == T) {
 #pragma unroll
             for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
         }
+    }
+    if (S == 1 && !failed && last != nullptr && lane_ok) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
     }
 }
 
@@ -287,32 +310,60 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // Backward
 // ============================================================================
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const float (&xh)[C::L][C::V],
+                                         const float (&xg)[C::L][C::V], float (&g)[C::V], int n, bool lane_ok,
+                                         typename C::St *gb, typename C::St *ga, int D) {
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L;
+#pragma unroll
+    for (int j = L - 1; j >= 0; --j) {
+        if (j < n) {
+            float gav[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
+                gav[v] = __fmul_rn(g[v], xh[j][v]);
+            }
+            if (lane_ok) {
+                store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
+                store_lanes<St, V>(ga + static_cast<size_t>(j) * D, gav);
+            }
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_out,
                const __grid_constant__ CUtensorMap tm_go, typename C::St *__restrict__ grad_a,
-               typename C::St *__restrict__ grad_b, int T, int D, int nwin, DevStatus *status,
+               typename C::St *__restrict__ grad_b, const __grid_constant__ WinGeom geom, DevStatus *status,
                uint64_t timeout_ns) {
     using St = typename C::St;
-    constexpr int V = C::V, L = C::L, S = C::S, DT = C::DT, G = C::G;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const WinSmem sm{smem_raw};
-    win_init<C>(sm);
-    const WaitCtx wc{status, sm.abort_flag<C>(), timeout_ns};
+    const WinSmem sm{smem_raw, &geom};
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init(sm, NT / 32, S, DT);
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = geom.T, D = geom.D;
+    const int nwin = geom.nwin;
 
-    if (warp == C::NWARP_C) {
-        if (lane == 0) {
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
             const CUtensorMap *const maps[3] = {&tm_a, &tm_out, &tm_go};
-            // tile 0: a shifted one step later; tile 1: out one step earlier; tile 2: grad_out
-            win_producer<C>(sm, maps, nwin, d0, brow,
-                            [nwin](int k, int i) { return (nwin - 1 - k) * C::W + (i == 0 ? 1 : (i == 1 ? -1 : 0)); },
+            const int W = geom.W;
+            // tile 0: a one step later; tile 1: out one step earlier; tile 2: grad_out
+            win_producer<C>(sm, maps, d0, brow,
+                            [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i == 0 ? 1 : (i == 1 ? -1 : 0)); },
                             wc);
         }
         return;
     }
 
+    const int lane = threadIdx.x & 31;
     const int s = threadIdx.x / G;
     const int lg = threadIdx.x - s * G;
     const int d = d0 + lg * V;
@@ -321,123 +372,86 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float g[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) g[v] = 0.0f;
+    int stage = 0, use = 0;
 
     for (int k = 0; k < nwin; ++k) {
-        const int stage = k % C::NSTAGE;
-        const int t0 = (nwin - 1 - k) * C::W;
-        const int rbase = t0 + s * L;
-        const int n = min(max(T - rbase, 0), L);
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // a_{t+1}
         const St *th = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 2) + (s * L) * DT + lg * V;  // grad_out_t
-        const size_t gofs = (row0 + rbase) * D + d;
-        bool ok = mbar_wait(sm.full_bar<C>(stage), (k / C::NSTAGE) & 1, wc, kSiteConsumerFull);
-
-        if constexpr (S == 1) {
+        const int wbase = (nwin - 1 - k) * geom.W;
+        if (S == 1) {
             if (!ok) break;
-            if (n == L) {
-#pragma unroll
-                for (int j = L - 1; j >= 0; --j) {
-                    float x[V], hp[V], go[V], ga[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(th + j * DT, hp);
-                    unpack_lanes<St, V>(tg + j * DT, go);
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        g[v] = __fmaf_rn(x[v], g[v], go[v]);
-                        ga[v] = __fmul_rn(g[v], hp[v]);
-                    }
-                    if (lane_ok) {
-                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
-                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, ga);
-                    }
-                }
-            } else {
-                for (int j = n - 1; j >= 0; --j) {
-                    float x[V], hp[V], go[V], ga[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(th + j * DT, hp);
-                    unpack_lanes<St, V>(tg + j * DT, go);
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        g[v] = __fmaf_rn(x[v], g[v], go[v]);
-                        ga[v] = __fmul_rn(g[v], hp[v]);
-                    }
-                    if (lane_ok) {
-                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
-                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, ga);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty_bar<C>(stage));
-        } else {
-            float xa[L][V], xh[L][V], xg[L][V];
-            if (ok) {
+            for (int r = geom.R - 1; r >= 0; --r) {
+                const int rbase = wbase + r * L;
+                const int n = min(max(T - rbase, 0), L);
+                float xa[L][V], xh[L][V], xg[L][V];
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
-                    unpack_lanes<St, V>(ta + j * DT, xa[j]);
-                    unpack_lanes<St, V>(th + j * DT, xh[j]);
-                    unpack_lanes<St, V>(tg + j * DT, xg[j]);
+                    unpack_lanes<St, V>(ta + (r * L + j) * DT, xa[j]);
+                    unpack_lanes<St, V>(th + (r * L + j) * DT, xh[j]);
+                    unpack_lanes<St, V>(tg + (r * L + j) * DT, xg[j]);
                 }
+                const size_t gofs = (row0 + rbase) * D + d;
+                bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
             }
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(sm.empty_bar<C>(stage));
-            // reverse sub-chunk summary: g at the sub-chunk's first step as
-            // P * (g just after the sub-chunk) + Q
-            float P[V], Q[V];
+            if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+            if (++stage == geom.nstage) { stage = 0; ++use; }
+            continue;
+        }
+
+        const int rbase = wbase + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float xa[L][V], xh[L][V], xg[L][V];
+        if (ok) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+            for (int j = 0; j < L; ++j) {
+                unpack_lanes<St, V>(ta + j * DT, xa[j]);
+                unpack_lanes<St, V>(th + j * DT, xh[j]);
+                unpack_lanes<St, V>(tg + j * DT, xg[j]);
+            }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == geom.nstage) { stage = 0; ++use; }
+        // reverse sub-chunk summary: g at the sub-chunk's first step as
+        // P * (g just after the sub-chunk) + Q
+        float P[V], Q[V];
 #pragma unroll
-            for (int j = L - 1; j >= 0; --j) {
-                if (j < n) {
+        for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
 #pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        P[v] = __fmul_rn(xa[j][v], P[v]);
-                        Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
-                    }
+        for (int j = L - 1; j >= 0; --j) {
+            if (j < n) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    P[v] = __fmul_rn(xa[j][v], P[v]);
+                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
                 }
             }
-            const int par = k & 1;
-            float *sp = sm.sP<C>(par), *sq = sm.sQ<C>(par);
+        }
+        const int par = k & 1;
+        float2 *pq = sm.sPQ<C>(par);
+#pragma unroll
+        for (int v = 0; v < V; ++v) pq[s * DT + lg * V + v] = make_float2(P[v], Q[v]);
+        if (bar_sync_or(1, NT, !ok)) break;
+        const float *carry = sm.sCarry<C>(par);
+#pragma unroll
+        for (int v = 0; v < V; ++v) g[v] = carry[lg * V + v];
+        // push the carried adjoint through sub-chunks S-1 .. s+1
+        for (int i = S - 1; i > s; --i) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                sp[s * DT + lg * V + v] = P[v];
-                sq[s * DT + lg * V + v] = Q[v];
+                const float2 m = pq[i * DT + lg * V + v];
+                g[v] = __fmaf_rn(m.x, g[v], m.y);
             }
-            if (bar_sync_or(1, C::NT, !ok)) break;
-            const float *carry = sm.sCarry<C>(par);
+        }
+        const size_t gofs = (row0 + rbase) * D + d;
+        bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
+        if (s == 0) {
+            float *nc = sm.sCarry<C>(par ^ 1);
 #pragma unroll
-            for (int v = 0; v < V; ++v) g[v] = carry[lg * V + v];
-            // push the carried adjoint through sub-chunks S-1 .. s+1
-#pragma unroll
-            for (int i = S - 1; i > 0; --i) {
-                if (i > s) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        g[v] = __fmaf_rn(sp[i * DT + lg * V + v], g[v], sq[i * DT + lg * V + v]);
-                }
-            }
-#pragma unroll
-            for (int j = L - 1; j >= 0; --j) {
-                if (j < n) {
-                    float ga[V];
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
-                        ga[v] = __fmul_rn(g[v], xh[j][v]);
-                    }
-                    if (lane_ok) {
-                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
-                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, ga);
-                    }
-                }
-            }
-            if (s == 0) {
-                float *nc = sm.sCarry<C>(par ^ 1);
-#pragma unroll
-                for (int v = 0; v < V; ++v) nc[lg * V + v] = g[v];
-            }
+            for (int v = 0; v < V; ++v) nc[lg * V + v] = g[v];
         }
     }
 }

@@ -41,8 +41,14 @@ class LrscanUnavailable(RuntimeError):
 
 class LrscanError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {strerror(code)} ({code})")
+        detail = ""
+        try:
+            detail = lib().lrscan_last_error().decode()
+        except LrscanUnavailable:
+            pass
+        super().__init__(f"{what}: {strerror(code)} ({code})" + (f": {detail}" if detail else ""))
         self.code = code
+        self.detail = detail
 
 
 class Opts(ctypes.Structure):
@@ -79,6 +85,7 @@ EXPORTS = {
     "lrscan_selftest_wait_timeout": ([ctypes.c_uint64], ctypes.c_int),
     "lrscan_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "lrscan_version": ([], ctypes.c_int),
+    "lrscan_last_error": ([], ctypes.c_char_p),
 }
 
 _lock = threading.Lock()

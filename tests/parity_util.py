@@ -7,6 +7,13 @@ Tolerances (stated once, used by every parity test):
     integers; +0 and -0 are the same point);
   * "exact": equal values (+0 == -0), used for the sequential paths, whose
     operation order is the oracle's own, and for identity-step padding.
+
+Paths that re-associate the recurrence through affine maps (window, chunk)
+make an fp32 error of a few ulps of the running state's magnitude.  Where a
+stored bf16 value is far smaller than that state (a near-cancellation), this
+can exceed 2 ulps of the tiny stored value; there the fp32 rule above is the
+bound, and such points must stay rare (REASSOC_MAX_FRACTION).  The named bf16
+workloads run on the sequential path, which is exact.
 """
 from __future__ import annotations
 
@@ -15,6 +22,7 @@ import torch
 
 F32_RTOL = 1e-4
 BF16_MAX_ULPS = 2
+REASSOC_MAX_FRACTION = 1e-3
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -36,7 +44,8 @@ def bf16_ulp_distance(x: np.ndarray, y: np.ndarray) -> np.ndarray:
     return np.abs(key(x) - key(y))
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", exact: bool = False):
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", exact: bool = False,
+                 reassociated: bool = False):
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     if dtype == "bf16":
         g, r = bf16_bits_to_f32(got), bf16_bits_to_f32(ref)
@@ -46,6 +55,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", e
             bad = ~((g == r) | (np.isnan(g) & np.isnan(r)))
         else:
             bad = (bf16_ulp_distance(got, ref) > BF16_MAX_ULPS) & ~np.isnan(r)
+            if reassociated and bad.any():
+                gd, rd = g.astype(np.float64), r.astype(np.float64)
+                near_cancel = bad & (np.abs(gd - rd) <= F32_RTOL * (1.0 + np.abs(rd)))
+                assert near_cancel.sum() <= REASSOC_MAX_FRACTION * bad.size, (
+                    f"{what}: {int(near_cancel.sum())} near-cancellation points beyond 2 ulps")
+                bad = bad & ~near_cancel
     else:
         g, r = got.astype(np.float64), ref.astype(np.float64)
         nan_ok = np.isnan(g) == np.isnan(r)
