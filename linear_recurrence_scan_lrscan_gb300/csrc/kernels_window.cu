@@ -3,6 +3,8 @@
 #include "launch.h"
 #include "window_kernels.cuh"
 
+#include <cstdlib>
+
 namespace lrscan {
 
 namespace {
@@ -24,7 +26,7 @@ int launch_win_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static std::mutex mu;
     auto fn = win_fwd_kernel<C>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.r, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
         *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last, g, L.status, L.timeout_ns);
@@ -37,7 +39,7 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static std::mutex mu;
     auto fn = win_bwd_kernel<C>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.r, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
         *L.maps[0], *L.maps[1], *L.maps[2], static_cast<typename C::St *>(L.out0),
@@ -46,14 +48,14 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
 }
 
 template <class C, bool FWD>
-WinDirCfg dir_cfg(int S, int R, int nstage) {
-    const WinGeom g = make_win_geom<C>(S, R, nstage, 1, 1);
+WinDirCfg dir_cfg(int S, int nstage) {
+    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
+    if (C::SEQ != (S == 1)) std::abort();  // table error: sequential shapes take S == 1
     WinDirCfg d{};
     d.dt = C::DT;
     d.v = C::V;
     d.l = C::L;
     d.s = S;
-    d.r = g.R;
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
@@ -69,56 +71,64 @@ WinDirCfg dir_cfg(int S, int R, int nstage) {
     return d;
 }
 
-// WinShape<St, DT, V, L, NIN, MAXT, MINB>
-// forward shapes (NIN = 2)
-using BF_64_2_16 = WinShape<bf16_t, 64, 2, 16, 2, 64, 8>;
-using BF_128_4_8 = WinShape<bf16_t, 128, 4, 8, 2, 288, 1>;
-using BF_64_2_8 = WinShape<bf16_t, 64, 2, 8, 2, 288, 3>;
-using BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 2, 288, 3>;
-using FF_32_1_16 = WinShape<float, 32, 1, 16, 2, 64, 8>;
-using FF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 3>;
-using FF_128_4_8 = WinShape<float, 128, 4, 8, 2, 64, 4>;
-using FF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1>;
-using FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1>;
-// backward shapes (NIN = 3)
-using BB_64_2_8 = WinShape<bf16_t, 64, 2, 8, 3, 288, 2>;
-using BB_128_4_4 = WinShape<bf16_t, 128, 4, 4, 3, 288, 2>;
-using BB_128_4_8 = WinShape<bf16_t, 128, 4, 8, 3, 288, 1>;
-using BB_32_1_8 = WinShape<bf16_t, 32, 1, 8, 3, 288, 2>;
-using FB_32_1_16 = WinShape<float, 32, 1, 16, 3, 64, 8>;
-using FB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1>;
-using FB_128_4_4 = WinShape<float, 128, 4, 4, 3, 64, 4>;
-using FB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1>;
-using FB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1>;
+// WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
+// Sequential shapes (S = 1): L rows per window streamed from shared memory.
+using SBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 2, 64, 8, true>;
+using SBF_128_2_32 = WinShape<bf16_t, 128, 2, 32, 2, 96, 6, true>;
+using SBF_128_4_32 = WinShape<bf16_t, 128, 4, 32, 2, 64, 8, true>;
+using SBB_64_2_32 = WinShape<bf16_t, 64, 2, 32, 3, 64, 8, true>;
+using SBB_128_2_32 = WinShape<bf16_t, 128, 2, 32, 3, 96, 6, true>;
+using SBB_128_4_16 = WinShape<bf16_t, 128, 4, 16, 3, 64, 8, true>;
+using SFF_32_1_32 = WinShape<float, 32, 1, 32, 2, 64, 8, true>;
+using SFF_64_2_16 = WinShape<float, 64, 2, 16, 2, 64, 8, true>;
+using SFF_64_1_32 = WinShape<float, 64, 1, 32, 2, 96, 6, true>;
+using SFF_128_4_8 = WinShape<float, 128, 4, 8, 2, 64, 8, true>;
+using SFB_32_1_32 = WinShape<float, 32, 1, 32, 3, 64, 8, true>;
+using SFB_64_2_16 = WinShape<float, 64, 2, 16, 3, 64, 8, true>;
+using SFB_64_1_32 = WinShape<float, 64, 1, 32, 3, 96, 6, true>;
+using SFB_128_4_8 = WinShape<float, 128, 4, 8, 3, 64, 8, true>;
+// Windowed shapes (S > 1): each thread holds L rows of its sub-chunk in registers.
+using BF_64_2_8 = WinShape<bf16_t, 64, 2, 8, 2, 288, 3, false>;
+using BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 2, 288, 3, false>;
+using BF_128_4_8 = WinShape<bf16_t, 128, 4, 8, 2, 288, 1, false>;
+using BB_64_2_8 = WinShape<bf16_t, 64, 2, 8, 3, 288, 2, false>;
+using BB_32_2_8 = WinShape<bf16_t, 32, 2, 8, 3, 288, 2, false>;
+using BB_128_4_4 = WinShape<bf16_t, 128, 4, 4, 3, 288, 2, false>;
+using FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1, false>;
+using FF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false>;
+using FF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 2, false>;
+using FB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1, false>;
+using FB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false>;
+using FB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1, false>;
 
-#define F(SH, S, R, N) dir_cfg<SH, true>(S, R, N)
-#define B(SH, S, R, N) dir_cfg<SH, false>(S, R, N)
+#define F(SH, S, N) dir_cfg<SH, true>(S, N)
+#define B(SH, S, N) dir_cfg<SH, false>(S, N)
 
 const WinVariant kSeqBF16[] = {
-    {"seq_bf16_d64", F(BF_64_2_16, 1, 2, 8), B(BB_64_2_8, 1, 4, 6)},
-    {"seq_bf16_d128", F(BF_128_4_8, 1, 4, 6), B(BB_128_4_4, 1, 8, 4)},
-    {"seq_bf16_d64_deep", F(BF_64_2_8, 1, 4, 8), B(BB_64_2_8, 1, 2, 12)},
-    {"seq_bf16_d128_short", F(BF_128_4_8, 1, 2, 8), B(BB_128_4_4, 1, 4, 6)},
+    {"seq_bf16_d64", F(SBF_64_2_32, 1, 8), B(SBB_64_2_32, 1, 6)},
+    {"seq_bf16_d128", F(SBF_128_2_32, 1, 4), B(SBB_128_2_32, 1, 4)},
+    {"seq_bf16_d64_deep", F(SBF_64_2_32, 1, 12), B(SBB_64_2_32, 1, 8)},
+    {"seq_bf16_d128_v4", F(SBF_128_4_32, 1, 6), B(SBB_128_4_16, 1, 6)},
 };
 const WinVariant kWinBF16[] = {
-    {"win_bf16_d64_s4", F(BF_64_2_8, 4, 1, 8), B(BB_64_2_8, 4, 1, 6)},
-    {"win_bf16_d64_s8", F(BF_64_2_8, 8, 1, 4), B(BB_64_2_8, 8, 1, 3)},
-    {"win_bf16_d32_s8", F(BF_32_1_8, 8, 1, 4), B(BB_32_1_8, 8, 1, 3)},
-    {"win_bf16_d128_s4", F(BF_128_4_8, 4, 1, 6), B(BB_128_4_4, 8, 1, 4)},
-    {"win_bf16_d64_s2", F(BF_64_2_8, 2, 1, 12), B(BB_64_2_8, 2, 1, 10)},
+    {"win_bf16_d64_s8", F(BF_64_2_8, 8, 4), B(BB_64_2_8, 8, 3)},
+    {"win_bf16_d32_s16", F(BF_32_2_8, 16, 4), B(BB_32_2_8, 16, 4)},
+    {"win_bf16_d64_s4", F(BF_64_2_8, 4, 8), B(BB_64_2_8, 4, 6)},
+    {"win_bf16_d128_s4", F(BF_128_4_8, 4, 6), B(BB_128_4_4, 8, 4)},
+    {"win_bf16_d64_s8_deep", F(BF_64_2_8, 8, 6), B(BB_64_2_8, 8, 4)},
 };
 const WinVariant kSeqF32[] = {
-    {"seq_f32_d32", F(FF_32_1_16, 1, 2, 8), B(FB_32_1_16, 1, 2, 6)},
-    {"seq_f32_d64", F(FF_64_2_8, 1, 4, 6), B(FB_64_2_8, 1, 4, 4)},
-    {"seq_f32_d128", F(FF_128_4_8, 1, 2, 6), B(FB_128_4_4, 1, 4, 4)},
-    {"seq_f32_d64_short", F(FF_64_2_8, 1, 2, 8), B(FB_64_2_8, 1, 2, 6)},
+    {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},
+    {"seq_f32_d64", F(SFF_64_2_16, 1, 8), B(SFB_64_2_16, 1, 6)},
+    {"seq_f32_d64_v1", F(SFF_64_1_32, 1, 4), B(SFB_64_1_32, 1, 4)},
+    {"seq_f32_d128", F(SFF_128_4_8, 1, 8), B(SFB_128_4_8, 1, 6)},
 };
 const WinVariant kWinF32[] = {
-    {"win_f32_d16_s16", F(FF_16_1_8, 16, 1, 4), B(FB_16_1_8, 16, 1, 4)},
-    {"win_f32_d32_s16", F(FF_32_1_8, 16, 1, 4), B(FB_32_1_8, 16, 1, 3)},
-    {"win_f32_d32_s8", F(FF_32_1_8, 8, 1, 8), B(FB_32_1_8, 8, 1, 6)},
-    {"win_f32_d16_s8", F(FF_16_1_8, 8, 1, 8), B(FB_16_1_8, 8, 1, 6)},
-    {"win_f32_d32_s4", F(FF_32_1_8, 4, 1, 12), B(FB_32_1_8, 4, 1, 10)},
+    {"win_f32_d16_s16", F(FF_16_1_8, 16, 4), B(FB_16_1_8, 16, 4)},
+    {"win_f32_d32_s16", F(FF_32_1_8, 16, 4), B(FB_32_1_8, 16, 3)},
+    {"win_f32_d32_s16_deep", F(FF_32_1_8, 16, 6), B(FB_32_1_8, 16, 4)},
+    {"win_f32_d16_s32", F(FF_16_1_8, 32, 3), B(FB_16_1_8, 32, 2)},
+    {"win_f32_d64_s8", F(FF_64_2_8, 8, 4), B(FB_64_2_8, 8, 3)},
 };
 
 #undef F

@@ -30,14 +30,13 @@ struct WinLaunch {
 };
 
 // One direction of a tile variant: compiled shape (DT, V, L) plus the
-// launch-time sub-chunk count S, register batches R and pipeline depth.
+// launch-time sub-chunk count S and pipeline depth.
 struct WinDirCfg {
     int dt;          // lanes per CTA
     int v;           // lanes per thread
     int l;           // steps per sub-chunk (registers)
     int s;           // sub-chunks per window
-    int r;           // register batches per window (S == 1)
-    int w;           // rows per window = s*l*r
+    int w;           // rows per window = s*l
     int nstage;      // pipeline depth
     int threads;     // s*(dt/v) + 32
     int smem;        // dynamic shared memory bytes

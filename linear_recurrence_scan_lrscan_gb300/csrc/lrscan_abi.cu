@@ -54,11 +54,22 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Description used when no device is visible (plans only): one GB300.
 constexpr int kRefSMs = 152, kRefSmemPerSM = 233472, kRefSmemOptin = 232448;
 
+thread_local int t_ctx_dev = -1;
+
 int device_ctx(DeviceCtx **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return LRSCAN_ENODEVICE;
+    }
+    if (t_ctx_dev != dev) {
+        // A thread that has not touched the runtime yet (e.g. an autograd
+        // worker) has no current context; the tensor-map encoder needs one.
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            cudaGetLastError();
+            return LRSCAN_ENODEVICE;
+        }
+        t_ctx_dev = dev;
     }
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceCtx &c = g_dev[dev];

@@ -7,8 +7,9 @@
 // the producer can refill it, and keeps the recurrence state in fp32.
 //
 //  S == 1  ("seq"): every thread runs the recurrence straight through all
-//          windows, one fused multiply-add per step, bit-identical to the
-//          sequential definition.  No barrier between consumer warps.
+//          windows (L rows each, streamed from shared memory in a fully
+//          unrolled loop), one fused multiply-add per step, bit-identical to
+//          the sequential definition.  No barrier between consumer warps.
 //  S  > 1  ("window"): thread (s, g) summarizes its sub-chunk as the affine
 //          map h -> P*h + Q (triton_training_scan.py, _real_chunk_summary),
 //          pushes the window's carried state through the maps of sub-chunks
@@ -33,10 +34,13 @@
 
 namespace lrscan {
 
-// Compile-time shape.  MAXT / MINB feed __launch_bounds__.
-template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_>
+// Compile-time shape.  MAXT / MINB feed __launch_bounds__.  A shape is either
+// sequential (launched with S == 1, rows streamed from shared memory) or
+// windowed (S > 1, each thread's L rows held in registers).
+template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_, bool SEQ_>
 struct WinShape {
     using St = St_;
+    static constexpr bool SEQ = SEQ_;
     static constexpr int DT = DT_;    // lanes per CTA
     static constexpr int V = V_;      // lanes per thread
     static constexpr int L = L_;      // steps per sub-chunk (held in registers)
@@ -48,15 +52,15 @@ struct WinShape {
     static_assert(DT % V == 0, "lane tile must split into lane groups");
     static_assert(ROW_BYTES % 16 == 0, "tensor-copy rows are multiples of 16 bytes");
     static_assert(DT <= 256, "tensor-copy box limit");
-    static_assert(L >= 1 && L <= 32, "sub-chunk rows are held in registers");
+    static_assert(L >= 1 && L <= 64, "rows per window (sequential) or per sub-chunk");
+    static_assert(SEQ || L <= 16, "windowed sub-chunks are held in registers");
 };
 
 // Launch-time geometry (filled by the host from S and the stage count).
 struct WinGeom {
     int S;             // sub-chunks per window
-    int R;             // register batches of L rows per window (S == 1 only; 1 otherwise)
     int nstage;        // pipeline depth
-    int W;             // rows per window = S*L*R
+    int W;             // rows per window = S*L
     int tile_bytes;    // W * ROW_BYTES
     int stage_bytes;   // NIN * tile_bytes
     int bar_off;       // byte offsets into dynamic shared memory
@@ -67,12 +71,11 @@ struct WinGeom {
 };
 
 template <class C>
-__host__ __device__ inline WinGeom make_win_geom(int S, int R, int nstage, int T, int D) {
+__host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D) {
     WinGeom g{};
     g.S = S;
-    g.R = S == 1 ? R : 1;
     g.nstage = nstage;
-    g.W = S * C::L * g.R;
+    g.W = S * C::L;
     g.tile_bytes = g.W * C::ROW_BYTES;
     g.stage_bytes = C::NIN * g.tile_bytes;
     g.bar_off = nstage * g.stage_bytes;
@@ -209,34 +212,37 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
         const St *tb = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;
-        if (S == 1) {
+        if constexpr (C::SEQ) {
             if (!ok) { failed = true; break; }
-            // R register batches of L rows, straight through: one fma per step
-            for (int r = 0; r < geom.R; ++r) {
-                const int rbase = k * geom.W + r * L;
-                const int n = min(max(T - rbase, 0), L);
-                float xa[L][V], xb[L][V];
-#pragma unroll
+            // straight through the window's L rows, one fma per step; the loop
+            // is unrolled so the shared-memory loads run ahead of the chain
+            const int rbase = k * geom.W;
+            const int n = min(T - rbase, L);
+            St *op = out + (row0 + rbase) * D + d;
+            if (n == L) {
+#pragma unroll 8
                 for (int j = 0; j < L; ++j) {
-                    unpack_lanes<St, V>(ta + (r * L + j) * DT, xa[j]);
-                    unpack_lanes<St, V>(tb + (r * L + j) * DT, xb[j]);
+                    float x[V], y[V];
+                    unpack_lanes<St, V>(ta + j * DT, x);
+                    unpack_lanes<St, V>(tb + j * DT, y);
+#pragma unroll
+                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
+                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
                 }
-                St *op = out + (row0 + rbase) * D + d;
+            } else {
+                for (int j = 0; j < n; ++j) {
+                    float x[V], y[V];
+                    unpack_lanes<St, V>(ta + j * DT, x);
+                    unpack_lanes<St, V>(tb + j * DT, y);
 #pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    if (j < n) {
-#pragma unroll
-                        for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
-                        if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
-                    }
+                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
+                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stage));
             if (++stage == geom.nstage) { stage = 0; ++use; }
-            continue;
-        }
-
+        } else {
         const int rbase = k * geom.W + s * L;
         const int n = min(max(T - rbase, 0), L);
         float xa[L][V], xb[L][V];
@@ -299,8 +305,9 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
             for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
         }
+        }
     }
-    if (S == 1 && !failed && last != nullptr && lane_ok) {
+    if (C::SEQ && !failed && last != nullptr && lane_ok) {
 #pragma unroll
         for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
     }
@@ -380,27 +387,48 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const St *th = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 2) + (s * L) * DT + lg * V;  // grad_out_t
         const int wbase = (nwin - 1 - k) * geom.W;
-        if (S == 1) {
+        if constexpr (C::SEQ) {
             if (!ok) break;
-            for (int r = geom.R - 1; r >= 0; --r) {
-                const int rbase = wbase + r * L;
-                const int n = min(max(T - rbase, 0), L);
-                float xa[L][V], xh[L][V], xg[L][V];
+            const int n = min(T - wbase, L);
+            const size_t gofs = (row0 + wbase) * D + d;
+            if (n == L) {
+#pragma unroll 8
+                for (int j = L - 1; j >= 0; --j) {
+                    float x[V], hp[V], go[V], gav[V];
+                    unpack_lanes<St, V>(ta + j * DT, x);
+                    unpack_lanes<St, V>(th + j * DT, hp);
+                    unpack_lanes<St, V>(tg + j * DT, go);
 #pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    unpack_lanes<St, V>(ta + (r * L + j) * DT, xa[j]);
-                    unpack_lanes<St, V>(th + (r * L + j) * DT, xh[j]);
-                    unpack_lanes<St, V>(tg + (r * L + j) * DT, xg[j]);
+                    for (int v = 0; v < V; ++v) {
+                        g[v] = __fmaf_rn(x[v], g[v], go[v]);
+                        gav[v] = __fmul_rn(g[v], hp[v]);
+                    }
+                    if (lane_ok) {
+                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
+                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, gav);
+                    }
                 }
-                const size_t gofs = (row0 + rbase) * D + d;
-                bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
+            } else {
+                for (int j = n - 1; j >= 0; --j) {
+                    float x[V], hp[V], go[V], gav[V];
+                    unpack_lanes<St, V>(ta + j * DT, x);
+                    unpack_lanes<St, V>(th + j * DT, hp);
+                    unpack_lanes<St, V>(tg + j * DT, go);
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        g[v] = __fmaf_rn(x[v], g[v], go[v]);
+                        gav[v] = __fmul_rn(g[v], hp[v]);
+                    }
+                    if (lane_ok) {
+                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
+                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, gav);
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stage));
             if (++stage == geom.nstage) { stage = 0; ++use; }
-            continue;
-        }
-
+        } else {
         const int rbase = wbase + s * L;
         const int n = min(max(T - rbase, 0), L);
         float xa[L][V], xh[L][V], xg[L][V];
@@ -452,6 +480,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             float *nc = sm.sCarry<C>(par ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[lg * V + v] = g[v];
+        }
         }
     }
 }
