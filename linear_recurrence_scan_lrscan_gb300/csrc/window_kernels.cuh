@@ -90,24 +90,45 @@ __host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D
     return g;
 }
 
+// Shared-memory layout of one CTA, with the launch geometry copied into
+// registers once (reading it through a pointer to the parameter would turn
+// every access into a generic load through L1).
 struct WinSmem {
     unsigned char *base;
-    const WinGeom *g;
+    int stage_bytes, tile_bytes, bar_off, scan_off, flag_off, nstage, S, W, nwin;
+
+    static __device__ __forceinline__ WinSmem make(unsigned char *b, const WinGeom &g) {
+        WinSmem m;
+        m.base = b;
+        m.stage_bytes = g.stage_bytes;
+        m.tile_bytes = g.tile_bytes;
+        m.bar_off = g.bar_off;
+        m.scan_off = g.scan_off;
+        m.flag_off = g.flag_off;
+        m.nstage = g.nstage;
+        m.S = g.S;
+        m.W = g.W;
+        m.nwin = g.nwin;
+        return m;
+    }
     template <class C> __device__ __forceinline__ typename C::St *tile(int stage, int which) const {
-        return reinterpret_cast<typename C::St *>(base + stage * g->stage_bytes + which * g->tile_bytes);
+        return reinterpret_cast<typename C::St *>(base + stage * stage_bytes + which * tile_bytes);
     }
-    __device__ __forceinline__ uint32_t full_bar(int stage) const { return smem_addr(base + g->bar_off + stage * 8); }
+    __device__ __forceinline__ uint32_t full_bar(int stage) const { return smem_addr(base + bar_off + stage * 8); }
     __device__ __forceinline__ uint32_t empty_bar(int stage) const {
-        return smem_addr(base + g->bar_off + (g->nstage + stage) * 8);
+        return smem_addr(base + bar_off + (nstage + stage) * 8);
     }
+    // (P, Q) of sub-chunk s, lane v*G + g at [par][s][v][g]: a warp touches
+    // consecutive float2s (no bank conflicts)
     template <class C> __device__ __forceinline__ float2 *sPQ(int par) const {
-        return reinterpret_cast<float2 *>(base + g->scan_off) + par * g->S * C::DT;
+        return reinterpret_cast<float2 *>(base + scan_off) + par * S * C::DT;
     }
+    // carried state [par][v][g]
     template <class C> __device__ __forceinline__ float *sCarry(int par) const {
-        return reinterpret_cast<float *>(base + g->scan_off + 2 * g->S * C::DT * 8) + par * C::DT;
+        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8) + par * C::DT;
     }
     __device__ __forceinline__ volatile int *abort_flag() const {
-        return reinterpret_cast<volatile int *>(base + g->flag_off);
+        return reinterpret_cast<volatile int *>(base + flag_off);
     }
 };
 
@@ -118,7 +139,7 @@ struct WinSmem {
 template <class C, class RowOf>
 __device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMap *const (&maps)[C::NIN], int x0,
                                              int z, RowOf row_of, const WaitCtx &wc) {
-    const WinGeom &g = *sm.g;
+    const WinSmem &g = sm;
     for (int i = 0; i < C::NIN; ++i) prefetch_tensormap(maps[i]);
     int issued = 0;
     int stage = 0, use = 0;
@@ -150,7 +171,7 @@ __device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMa
 }
 
 __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S, int DT) {
-    const WinGeom &g = *sm.g;
+    const WinSmem &g = sm;
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.nstage; ++s) {
             mbar_init(sm.full_bar(s), 1);
@@ -178,7 +199,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const WinSmem sm{smem_raw, &geom};
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
     const int NT = S * G;
     win_init(sm, NT / 32, S, DT);
@@ -190,7 +211,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     if (static_cast<int>(threadIdx.x) >= NT) {  // producer warp
         if (static_cast<int>(threadIdx.x) == NT) {
             const CUtensorMap *const maps[2] = {&tm_a, &tm_b};
-            const int W = geom.W;
+            const int W = sm.W;
             win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
         }
         return;
@@ -208,7 +229,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     bool failed = false;
     int stage = 0, use = 0;
 
-    for (int k = 0; k < geom.nwin; ++k) {
+    for (int k = 0; k < sm.nwin; ++k) {
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
         const St *tb = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;
@@ -216,7 +237,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             if (!ok) { failed = true; break; }
             // straight through the window's L rows, one fma per step; the loop
             // is unrolled so the shared-memory loads run ahead of the chain
-            const int rbase = k * geom.W;
+            const int rbase = k * sm.W;
             const int n = min(T - rbase, L);
             St *op = out + (row0 + rbase) * D + d;
             if (n == L) {
@@ -241,9 +262,9 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stage));
-            if (++stage == geom.nstage) { stage = 0; ++use; }
+            if (++stage == sm.nstage) { stage = 0; ++use; }
         } else {
-        const int rbase = k * geom.W + s * L;
+        const int rbase = k * sm.W + s * L;
         const int n = min(max(T - rbase, 0), L);
         float xa[L][V], xb[L][V];
         if (ok) {
@@ -255,7 +276,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
-        if (++stage == geom.nstage) { stage = 0; ++use; }
+        if (++stage == sm.nstage) { stage = 0; ++use; }
         // sub-chunk summary h -> P*h + Q (an empty tail sub-chunk is the identity)
         float P[V], Q[V];
 #pragma unroll
@@ -273,16 +294,16 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int par = k & 1;
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[s * DT + lg * V + v] = make_float2(P[v], Q[v]);
+        for (int v = 0; v < V; ++v) pq[(s * V + v) * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
         // entry state: the carried state pushed through sub-chunks 0..s-1 in order
         const float *carry = sm.sCarry<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) h[v] = carry[lg * V + v];
+        for (int v = 0; v < V; ++v) h[v] = carry[v * G + lg];
         for (int i = 0; i < s; ++i) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float2 m = pq[i * DT + lg * V + v];
+                const float2 m = pq[(i * V + v) * G + lg];
                 h[v] = __fmaf_rn(m.x, h[v], m.y);
             }
         }
@@ -298,7 +319,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (s == S - 1) {
             float *nc = sm.sCarry<C>(par ^ 1);
 #pragma unroll
-            for (int v = 0; v < V; ++v) nc[lg * V + v] = h[v];
+            for (int v = 0; v < V; ++v) nc[v * G + lg] = h[v];
         }
         // the thread whose sub-chunk holds step T-1 owns the final state
         if (last != nullptr && lane_ok && n > 0 && rbase + n == T) {
@@ -348,7 +369,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const WinSmem sm{smem_raw, &geom};
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
     const int NT = S * G;
     win_init(sm, NT / 32, S, DT);
@@ -356,12 +377,12 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
     const int T = geom.T, D = geom.D;
-    const int nwin = geom.nwin;
+    const int nwin = sm.nwin;
 
     if (static_cast<int>(threadIdx.x) >= NT) {
         if (static_cast<int>(threadIdx.x) == NT) {
             const CUtensorMap *const maps[3] = {&tm_a, &tm_out, &tm_go};
-            const int W = geom.W;
+            const int W = sm.W;
             // tile 0: a one step later; tile 1: out one step earlier; tile 2: grad_out
             win_producer<C>(sm, maps, d0, brow,
                             [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i == 0 ? 1 : (i == 1 ? -1 : 0)); },
@@ -386,7 +407,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // a_{t+1}
         const St *th = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 2) + (s * L) * DT + lg * V;  // grad_out_t
-        const int wbase = (nwin - 1 - k) * geom.W;
+        const int wbase = (nwin - 1 - k) * sm.W;
         if constexpr (C::SEQ) {
             if (!ok) break;
             const int n = min(T - wbase, L);
@@ -427,7 +448,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stage));
-            if (++stage == geom.nstage) { stage = 0; ++use; }
+            if (++stage == sm.nstage) { stage = 0; ++use; }
         } else {
         const int rbase = wbase + s * L;
         const int n = min(max(T - rbase, 0), L);
@@ -442,7 +463,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
-        if (++stage == geom.nstage) { stage = 0; ++use; }
+        if (++stage == sm.nstage) { stage = 0; ++use; }
         // reverse sub-chunk summary: g at the sub-chunk's first step as
         // P * (g just after the sub-chunk) + Q
         float P[V], Q[V];
@@ -461,16 +482,16 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int par = k & 1;
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[s * DT + lg * V + v] = make_float2(P[v], Q[v]);
+        for (int v = 0; v < V; ++v) pq[(s * V + v) * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) break;
         const float *carry = sm.sCarry<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) g[v] = carry[lg * V + v];
+        for (int v = 0; v < V; ++v) g[v] = carry[v * G + lg];
         // push the carried adjoint through sub-chunks S-1 .. s+1
         for (int i = S - 1; i > s; --i) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float2 m = pq[i * DT + lg * V + v];
+                const float2 m = pq[(i * V + v) * G + lg];
                 g[v] = __fmaf_rn(m.x, g[v], m.y);
             }
         }
@@ -479,7 +500,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (s == 0) {
             float *nc = sm.sCarry<C>(par ^ 1);
 #pragma unroll
-            for (int v = 0; v < V; ++v) nc[lg * V + v] = g[v];
+            for (int v = 0; v < V; ++v) nc[v * G + lg] = g[v];
         }
         }
     }
