@@ -50,7 +50,7 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
 template <class C, bool FWD>
 WinDirCfg dir_cfg(int S, int nstage) {
     const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
-    if (C::SEQ != (S == 1)) std::abort();  // table error: sequential shapes take S == 1
+    if (C::SEQ != (S == 1) || S > C::SMAX) std::abort();  // table error: S out of the shape's range
     WinDirCfg d{};
     d.dt = C::DT;
     d.v = C::V;
@@ -73,27 +73,29 @@ WinDirCfg dir_cfg(int S, int nstage) {
 
 // WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
 // Sequential shapes (S = 1): L rows per window streamed from shared memory.
-using SBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 2, 64, 8, true>;
-using SBF_128_2_32 = WinShape<bf16_t, 128, 2, 32, 2, 96, 6, true>;
-using SBF_128_4_32 = WinShape<bf16_t, 128, 4, 32, 2, 64, 8, true>;
-using SBB_64_2_32 = WinShape<bf16_t, 64, 2, 32, 3, 64, 8, true>;
-using SBB_128_2_32 = WinShape<bf16_t, 128, 2, 32, 3, 96, 6, true>;
-using SBB_128_4_16 = WinShape<bf16_t, 128, 4, 16, 3, 64, 8, true>;
-using SFF_32_1_32 = WinShape<float, 32, 1, 32, 2, 64, 8, true>;
-using SFF_64_2_16 = WinShape<float, 64, 2, 16, 2, 64, 8, true>;
-using SFF_64_1_32 = WinShape<float, 64, 1, 32, 2, 96, 6, true>;
-using SFF_128_4_8 = WinShape<float, 128, 4, 8, 2, 64, 8, true>;
-using SFB_32_1_32 = WinShape<float, 32, 1, 32, 3, 64, 8, true>;
-using SFB_64_2_16 = WinShape<float, 64, 2, 16, 3, 64, 8, true>;
-using SFB_64_1_32 = WinShape<float, 64, 1, 32, 3, 96, 6, true>;
-using SFB_128_4_8 = WinShape<float, 128, 4, 8, 3, 64, 8, true>;
+using SBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 2, 64, 1, true>;
+using SBF_128_2_32 = WinShape<bf16_t, 128, 2, 32, 2, 96, 1, true>;
+using SBF_128_4_32 = WinShape<bf16_t, 128, 4, 32, 2, 64, 1, true>;
+using SBB_64_2_32 = WinShape<bf16_t, 64, 2, 32, 3, 64, 1, true>;
+using SBB_128_2_32 = WinShape<bf16_t, 128, 2, 32, 3, 96, 1, true>;
+using SBB_128_4_16 = WinShape<bf16_t, 128, 4, 16, 3, 64, 1, true>;
+using SFF_32_1_32 = WinShape<float, 32, 1, 32, 2, 64, 1, true>;
+using SFF_64_2_16 = WinShape<float, 64, 2, 16, 2, 64, 1, true>;
+using SFF_64_1_32 = WinShape<float, 64, 1, 32, 2, 96, 1, true>;
+using SFF_128_4_8 = WinShape<float, 128, 4, 8, 2, 64, 1, true>;
+using SFB_32_1_32 = WinShape<float, 32, 1, 32, 3, 64, 1, true>;
+using SFB_64_2_16 = WinShape<float, 64, 2, 16, 3, 64, 1, true>;
+using SFB_64_1_32 = WinShape<float, 64, 1, 32, 3, 96, 1, true>;
+using SFB_128_4_8 = WinShape<float, 128, 4, 8, 3, 64, 1, true>;
 // Windowed shapes (S > 1): each thread holds L rows of its sub-chunk in registers.
 using BF_64_2_8 = WinShape<bf16_t, 64, 2, 8, 2, 288, 3, false>;
 using BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 2, 288, 3, false>;
 using BF_128_4_8 = WinShape<bf16_t, 128, 4, 8, 2, 288, 1, false>;
+using BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 2, 544, 1, false>;
 using BB_64_2_8 = WinShape<bf16_t, 64, 2, 8, 3, 288, 2, false>;
 using BB_32_2_8 = WinShape<bf16_t, 32, 2, 8, 3, 288, 2, false>;
 using BB_128_4_4 = WinShape<bf16_t, 128, 4, 4, 3, 288, 2, false>;
+using BB_32_1_8 = WinShape<bf16_t, 32, 1, 8, 3, 544, 1, false>;
 using FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1, false>;
 using FF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false>;
 using FF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 2, false>;
@@ -107,15 +109,16 @@ using FB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1, false>;
 const WinVariant kSeqBF16[] = {
     {"seq_bf16_d64", F(SBF_64_2_32, 1, 8), B(SBB_64_2_32, 1, 6)},
     {"seq_bf16_d128", F(SBF_128_2_32, 1, 4), B(SBB_128_2_32, 1, 4)},
-    {"seq_bf16_d64_deep", F(SBF_64_2_32, 1, 12), B(SBB_64_2_32, 1, 8)},
+    {"seq_bf16_d64_s9", F(SBF_64_2_32, 1, 9), B(SBB_64_2_32, 1, 6)},
     {"seq_bf16_d128_v4", F(SBF_128_4_32, 1, 6), B(SBB_128_4_16, 1, 6)},
 };
 const WinVariant kWinBF16[] = {
     {"win_bf16_d64_s8", F(BF_64_2_8, 8, 4), B(BB_64_2_8, 8, 3)},
     {"win_bf16_d32_s16", F(BF_32_2_8, 16, 4), B(BB_32_2_8, 16, 4)},
-    {"win_bf16_d64_s4", F(BF_64_2_8, 4, 8), B(BB_64_2_8, 4, 6)},
-    {"win_bf16_d128_s4", F(BF_128_4_8, 4, 6), B(BB_128_4_4, 8, 4)},
+    {"win_bf16_d32_s12_wave", F(BF_32_2_8, 12, 3), B(BB_32_2_8, 8, 3)},
+    {"win_bf16_d32_v1_s16", F(BF_32_1_8, 16, 3), B(BB_32_1_8, 16, 2)},
     {"win_bf16_d64_s8_deep", F(BF_64_2_8, 8, 6), B(BB_64_2_8, 8, 4)},
+    {"win_bf16_d32_s16_n3", F(BF_32_2_8, 16, 3), B(BB_32_2_8, 16, 2)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},

@@ -49,6 +49,7 @@ struct WinShape {
     static constexpr int MAXT = MAXT_;
     static constexpr int MINB = MINB_;
     static constexpr int ROW_BYTES = DT * static_cast<int>(sizeof(St));
+    static constexpr int SMAX = SEQ ? 1 : (MAXT - 32) / G;  // most sub-chunks a launch may use
     static_assert(DT % V == 0, "lane tile must split into lane groups");
     static_assert(ROW_BYTES % 16 == 0, "tensor-copy rows are multiples of 16 bytes");
     static_assert(DT <= 256, "tensor-copy box limit");
@@ -236,12 +237,12 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if constexpr (C::SEQ) {
             if (!ok) { failed = true; break; }
             // straight through the window's L rows, one fma per step; the loop
-            // is unrolled so the shared-memory loads run ahead of the chain
+            // is fully unrolled so the shared-memory loads run ahead of the chain
             const int rbase = k * sm.W;
             const int n = min(T - rbase, L);
             St *op = out + (row0 + rbase) * D + d;
             if (n == L) {
-#pragma unroll 8
+#pragma unroll
                 for (int j = 0; j < L; ++j) {
                     float x[V], y[V];
                     unpack_lanes<St, V>(ta + j * DT, x);
@@ -300,11 +301,14 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const float *carry = sm.sCarry<C>(par);
 #pragma unroll
         for (int v = 0; v < V; ++v) h[v] = carry[v * G + lg];
-        for (int i = 0; i < s; ++i) {
+        // unrolled to the compile-time bound so every map load issues up front;
+        // sub-chunks at or after s contribute the identity map (exact)
+#pragma unroll
+        for (int i = 0; i < C::SMAX - 1; ++i) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float2 m = pq[(i * V + v) * G + lg];
-                h[v] = __fmaf_rn(m.x, h[v], m.y);
+                const float2 m = (i < s) ? pq[(i * V + v) * G + lg] : make_float2(1.0f, 0.0f);
+                if (i < s) h[v] = __fmaf_rn(m.x, h[v], m.y);
             }
         }
         St *op = out + (row0 + rbase) * D + d;
@@ -413,7 +417,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             const int n = min(T - wbase, L);
             const size_t gofs = (row0 + wbase) * D + d;
             if (n == L) {
-#pragma unroll 8
+#pragma unroll
                 for (int j = L - 1; j >= 0; --j) {
                     float x[V], hp[V], go[V], gav[V];
                     unpack_lanes<St, V>(ta + j * DT, x);
@@ -488,11 +492,13 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
         for (int v = 0; v < V; ++v) g[v] = carry[v * G + lg];
         // push the carried adjoint through sub-chunks S-1 .. s+1
-        for (int i = S - 1; i > s; --i) {
+#pragma unroll
+        for (int ii = 0; ii < C::SMAX - 1; ++ii) {
+            const int i = S - 1 - ii;
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float2 m = pq[(i * V + v) * G + lg];
-                g[v] = __fmaf_rn(m.x, g[v], m.y);
+                const float2 m = (i > s) ? pq[(i * V + v) * G + lg] : make_float2(1.0f, 0.0f);
+                if (i > s) g[v] = __fmaf_rn(m.x, g[v], m.y);
             }
         }
         const size_t gofs = (row0 + rbase) * D + d;
