@@ -36,6 +36,7 @@ struct WinDirCfg {
     int v;           // lanes per thread
     int l;           // steps per sub-chunk (registers)
     int s;           // sub-chunks per window
+    int lane_scan;   // windowed prefix by lane threads (1) or per thread (0)
     int w;           // rows per window = s*l
     int nstage;      // pipeline depth
     int threads;     // s*(dt/v) + 32

@@ -11,12 +11,16 @@
 //          unrolled loop), one fused multiply-add per step, bit-identical to
 //          the sequential definition.  No barrier between consumer warps.
 //  S  > 1  ("window"): thread (s, g) summarizes its sub-chunk as the affine
-//          map h -> P*h + Q (triton_training_scan.py, _real_chunk_summary),
-//          pushes the window's carried state through the maps of sub-chunks
-//          0..s-1 (the serial prefix of _real_chunk_prefix, inside one CTA;
-//          identity maps leave the state bit-for-bit unchanged), and replays
-//          its sub-chunk (_real_chunk_replay).  One pass over HBM: 3 elements
-//          per (t, d) forward, 5 backward.
+//          map h -> P*h + Q (triton_training_scan.py, _real_chunk_summary);
+//          the sub-chunk entry states follow from the window's carried state
+//          through the maps in order (the serial prefix of _real_chunk_prefix,
+//          inside one CTA; identity maps leave the state bit-for-bit
+//          unchanged), either by DT "lane" threads that walk all S maps of
+//          one lane and record every entry (few instructions, one extra
+//          barrier) or by every thread folding the maps before its own
+//          sub-chunk (short critical path); then every thread replays its
+//          sub-chunk (_real_chunk_replay).  One pass over HBM: 3 elements per
+//          (t, d) forward, 5 backward.
 //
 // With G = DT/V = 32 a warp is exactly one sub-chunk row range, so its
 // shared-memory reads of one row are 32 consecutive words (conflict-free).
@@ -60,6 +64,7 @@ struct WinShape {
 // Launch-time geometry (filled by the host from S and the stage count).
 struct WinGeom {
     int S;             // sub-chunks per window
+    int lane_scan;     // windowed prefix: 1 = lane threads scan the maps, 0 = every thread folds its own prefix
     int nstage;        // pipeline depth
     int W;             // rows per window = S*L
     int tile_bytes;    // W * ROW_BYTES
@@ -72,17 +77,20 @@ struct WinGeom {
 };
 
 template <class C>
-__host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D) {
+__host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D, int lane_scan = 1) {
     WinGeom g{};
     g.S = S;
+    g.lane_scan = lane_scan;
     g.nstage = nstage;
     g.W = S * C::L;
     g.tile_bytes = g.W * C::ROW_BYTES;
     g.stage_bytes = C::NIN * g.tile_bytes;
     g.bar_off = nstage * g.stage_bytes;
     g.scan_off = g.bar_off + 2 * nstage * 8;
-    // P,Q exchange [parity][S][DT] float2 and the carried state [parity][DT]
-    const int scan_bytes = S > 1 ? (2 * S * C::DT * 8 + 2 * C::DT * 4) : 0;
+    // sub-chunk maps (P,Q) [2][S][DT] float2, entry states [S][DT] float and
+    // the carried state [2][DT] float (the lane scan uses one map buffer and
+    // the entries; the per-thread prefix uses both map buffers and the carry)
+    const int scan_bytes = S > 1 ? (2 * S * C::DT * 8 + S * C::DT * 4 + 2 * C::DT * 4) : 0;
     g.flag_off = g.scan_off + scan_bytes;
     g.smem_bytes = g.flag_off + 16;
     g.T = T;
@@ -119,14 +127,18 @@ struct WinSmem {
     __device__ __forceinline__ uint32_t empty_bar(int stage) const {
         return smem_addr(base + bar_off + (nstage + stage) * 8);
     }
-    // (P, Q) of sub-chunk s, lane v*G + g at [par][s][v][g]: a warp touches
-    // consecutive float2s (no bank conflicts)
+    // (P, Q) of sub-chunk s for lane v*G + g at [par][s][v*G + g]: consecutive
+    // threads touch consecutive words (no bank conflicts)
     template <class C> __device__ __forceinline__ float2 *sPQ(int par) const {
         return reinterpret_cast<float2 *>(base + scan_off) + par * S * C::DT;
     }
-    // carried state [par][v][g]
+    // entry state of sub-chunk s for lane v*G + g at [s][v*G + g]
+    template <class C> __device__ __forceinline__ float *sEntry() const {
+        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8);
+    }
+    // carried state [par][v*G + g]
     template <class C> __device__ __forceinline__ float *sCarry(int par) const {
-        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8) + par * C::DT;
+        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8 + S * C::DT * 4) + par * C::DT;
     }
     __device__ __forceinline__ volatile int *abort_flag() const {
         return reinterpret_cast<volatile int *>(base + flag_off);
@@ -183,7 +195,7 @@ __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, 
     }
     if (S > 1) {
         // carried state starts at zero (h_{-1} = 0 forward, g_T = 0 backward)
-        float *c = reinterpret_cast<float *>(sm.base + g.scan_off + 2 * g.S * DT * 8);
+        float *c = reinterpret_cast<float *>(sm.base + g.scan_off + 2 * g.S * DT * 8 + g.S * DT * 4);
         for (int i = threadIdx.x; i < 2 * DT; i += blockDim.x) c[i] = 0.0f;
     }
     __syncthreads();
@@ -227,6 +239,8 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float h[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) h[v] = 0.0f;
+    float carry = 0.0f;  // window-to-window state of lane threadIdx.x (lane scan, threads < DT)
+    const bool lane_scan = geom.lane_scan != 0;
     bool failed = false;
     int stage = 0, use = 0;
 
@@ -292,23 +306,44 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        const int par = k & 1;
+        const int par = lane_scan ? 0 : (k & 1);
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[(s * V + v) * G + lg] = make_float2(P[v], Q[v]);
+        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
-        // entry state: the carried state pushed through sub-chunks 0..s-1 in order
-        const float *carry = sm.sCarry<C>(par);
+        if (lane_scan) {
+            // Threads 0..DT-1 each own one lane: push the carried state through
+            // the sub-chunk maps in order, recording every sub-chunk's entry
+            // state (_real_chunk_prefix within the window; identity maps exact).
+            float *entry = sm.sEntry<C>();
+            if (static_cast<int>(threadIdx.x) < DT) {
+                float c = carry;
 #pragma unroll
-        for (int v = 0; v < V; ++v) h[v] = carry[v * G + lg];
-        // unrolled to the compile-time bound so every map load issues up front;
-        // sub-chunks at or after s contribute the identity map (exact)
+                for (int i = 0; i < C::SMAX; ++i) {
+                    if (i < S) {
+                        const float2 m = pq[i * DT + threadIdx.x];
+                        entry[i * DT + threadIdx.x] = c;
+                        c = __fmaf_rn(m.x, c, m.y);
+                    }
+                }
+                carry = c;
+            }
+            bar_sync_or(1, NT, false);
 #pragma unroll
-        for (int i = 0; i < C::SMAX - 1; ++i) {
+            for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
+        } else {
+            // every thread folds the maps of sub-chunks 0..s-1 into the carried
+            // state itself (shorter critical path, more instructions)
+            const float *cs = sm.sCarry<C>(par);
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float2 m = (i < s) ? pq[(i * V + v) * G + lg] : make_float2(1.0f, 0.0f);
-                if (i < s) h[v] = __fmaf_rn(m.x, h[v], m.y);
+            for (int v = 0; v < V; ++v) h[v] = cs[v * G + lg];
+#pragma unroll
+            for (int i = 0; i < C::SMAX - 1; ++i) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float2 m = (i < s) ? pq[i * DT + v * G + lg] : make_float2(1.0f, 0.0f);
+                    if (i < s) h[v] = __fmaf_rn(m.x, h[v], m.y);
+                }
             }
         }
         St *op = out + (row0 + rbase) * D + d;
@@ -320,8 +355,8 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
             }
         }
-        if (s == S - 1) {
-            float *nc = sm.sCarry<C>(par ^ 1);
+        if (!lane_scan && s == S - 1) {
+            float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[v * G + lg] = h[v];
         }
@@ -404,6 +439,8 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float g[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) g[v] = 0.0f;
+    float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (lane scan, threads < DT)
+    const bool lane_scan = geom.lane_scan != 0;
     int stage = 0, use = 0;
 
     for (int k = 0; k < nwin; ++k) {
@@ -483,28 +520,48 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        const int par = k & 1;
+        const int par = lane_scan ? 0 : (k & 1);
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[(s * V + v) * G + lg] = make_float2(P[v], Q[v]);
+        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) break;
-        const float *carry = sm.sCarry<C>(par);
+        if (lane_scan) {
+            // lane threads push the carried adjoint through sub-chunks S-1 .. 0
+            float *entry = sm.sEntry<C>();
+            if (static_cast<int>(threadIdx.x) < DT) {
+                float c = carry;
 #pragma unroll
-        for (int v = 0; v < V; ++v) g[v] = carry[v * G + lg];
-        // push the carried adjoint through sub-chunks S-1 .. s+1
+                for (int ii = 0; ii < C::SMAX; ++ii) {
+                    const int i = S - 1 - ii;
+                    if (i >= 0) {
+                        const float2 m = pq[i * DT + threadIdx.x];
+                        entry[i * DT + threadIdx.x] = c;
+                        c = __fmaf_rn(m.x, c, m.y);
+                    }
+                }
+                carry = c;
+            }
+            bar_sync_or(1, NT, false);
 #pragma unroll
-        for (int ii = 0; ii < C::SMAX - 1; ++ii) {
-            const int i = S - 1 - ii;
+            for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
+        } else {
+            const float *cs = sm.sCarry<C>(par);
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float2 m = (i > s) ? pq[(i * V + v) * G + lg] : make_float2(1.0f, 0.0f);
-                if (i > s) g[v] = __fmaf_rn(m.x, g[v], m.y);
+            for (int v = 0; v < V; ++v) g[v] = cs[v * G + lg];
+#pragma unroll
+            for (int ii = 0; ii < C::SMAX - 1; ++ii) {
+                const int i = S - 1 - ii;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float2 m = (i > s) ? pq[i * DT + v * G + lg] : make_float2(1.0f, 0.0f);
+                    if (i > s) g[v] = __fmaf_rn(m.x, g[v], m.y);
+                }
             }
         }
         const size_t gofs = (row0 + rbase) * D + d;
         bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
-        if (s == 0) {
-            float *nc = sm.sCarry<C>(par ^ 1);
+        if (!lane_scan && s == 0) {
+            float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[v * G + lg] = g[v];
         }
