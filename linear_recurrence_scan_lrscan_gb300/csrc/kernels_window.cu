@@ -26,7 +26,7 @@ int launch_win_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static std::mutex mu;
     auto fn = win_fwd_kernel<C>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D), cfg.lane_scan);
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
         *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last, g, L.status, L.timeout_ns);
@@ -39,7 +39,7 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static std::mutex mu;
     auto fn = win_bwd_kernel<C>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D), cfg.lane_scan);
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
         *L.maps[0], *L.maps[1], *L.maps[2], static_cast<typename C::St *>(L.out0),
@@ -48,15 +48,15 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
 }
 
 template <class C, bool FWD>
-WinDirCfg dir_cfg(int S, int nstage, int lane_scan = 1) {
-    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1, lane_scan);
+WinDirCfg dir_cfg(int S, int nstage) {
+    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
     if (C::SEQ != (S == 1) || S > C::SMAX) std::abort();  // table error: S out of the shape's range
     WinDirCfg d{};
     d.dt = C::DT;
     d.v = C::V;
     d.l = C::L;
     d.s = S;
-    d.lane_scan = lane_scan;
+    d.lane_scan = (!C::SEQ && !C::PT) ? 1 : 0;
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
@@ -95,6 +95,11 @@ using BF_128_4_8 = WinShape<bf16_t, 128, 4, 8, 2, 288, 1, false>;
 using BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 2, 544, 1, false>;
 using BB_64_2_8 = WinShape<bf16_t, 64, 2, 8, 3, 288, 2, false>;
 using BB_32_2_8 = WinShape<bf16_t, 32, 2, 8, 3, 288, 2, false>;
+// per-thread-prefix shapes (parallel fold, short critical path)
+using PF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, true>;
+using PFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, true>;
+using PF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1, false, true>;
+using PFB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1, false, true>;
 using BB_128_4_4 = WinShape<bf16_t, 128, 4, 4, 3, 288, 2, false>;
 using BB_32_1_8 = WinShape<bf16_t, 32, 1, 8, 3, 544, 1, false>;
 using FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1, false>;
@@ -115,8 +120,7 @@ using WBB_64_2_16 = WinShape<bf16_t, 64, 2, 16, 3, 288, 1, false>;
 
 #define F(SH, S, N) dir_cfg<SH, true>(S, N)
 #define B(SH, S, N) dir_cfg<SH, false>(S, N)
-#define FP(SH, S, N) dir_cfg<SH, true>(S, N, 0)
-#define BP(SH, S, N) dir_cfg<SH, false>(S, N, 0)
+
 
 const WinVariant kSeqBF16[] = {
     {"seq_bf16_d64", F(SBF_64_2_32, 1, 8), B(SBB_64_2_32, 1, 6)},
@@ -126,11 +130,10 @@ const WinVariant kSeqBF16[] = {
 };
 const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s16", F(BF_32_2_8, 16, 3), B(BB_32_2_8, 16, 4)},
-    {"win_bf16_d32_s16_pt", FP(BF_32_2_8, 16, 3), BP(BB_32_2_8, 16, 4)},
     {"win_bf16_d64_s8", F(BF_64_2_8, 8, 4), B(BB_64_2_8, 8, 3)},
     {"win_bf16_d32_s16_n2", F(BF_32_2_8, 16, 2), B(BB_32_2_8, 16, 2)},
+    {"win_bf16_d32_s16_n4", F(BF_32_2_8, 16, 4), B(BB_32_2_8, 16, 3)},
     {"win_bf16_d32_l16_s8", F(WBF_32_2_16, 8, 4), B(WBB_32_2_16, 8, 4)},
-    {"win_bf16_d64_s8_pt", FP(BF_64_2_8, 8, 4), BP(BB_64_2_8, 8, 3)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},
@@ -139,18 +142,17 @@ const WinVariant kSeqF32[] = {
     {"seq_f32_d128", F(SFF_128_4_8, 1, 8), B(SFB_128_4_8, 1, 6)},
 };
 const WinVariant kWinF32[] = {
-    {"win_f32_d32_s16_pt", FP(FF_32_1_8, 16, 4), BP(FB_32_1_8, 16, 3)},
+    {"win_f32_d32_s16_pt", F(PF_32_1_8, 16, 4), B(PFB_32_1_8, 16, 3)},
     {"win_f32_d16_s16", F(FF_16_1_8, 16, 4), B(FB_16_1_8, 16, 4)},
     {"win_f32_d32_s16", F(FF_32_1_8, 16, 4), B(FB_32_1_8, 16, 3)},
-    {"win_f32_d16_s16_pt", FP(FF_16_1_8, 16, 4), BP(FB_16_1_8, 16, 4)},
+    {"win_f32_d16_s16_pt", F(PF_16_1_8, 16, 4), B(PFB_16_1_8, 16, 4)},
     {"win_f32_d64_s8", F(FF_64_2_8, 8, 4), B(FB_64_2_8, 8, 3)},
-    {"win_f32_d32_l16_s8_pt", FP(WF_32_1_16, 8, 4), BP(WFB_32_1_16, 8, 3)},
+    {"win_f32_d32_s8_pt", F(PF_32_1_8, 8, 8), B(PFB_32_1_8, 8, 6)},
 };
 
 #undef F
 #undef B
-#undef FP
-#undef BP
+
 
 }  // namespace
 

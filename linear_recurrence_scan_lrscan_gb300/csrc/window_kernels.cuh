@@ -41,10 +41,13 @@ namespace lrscan {
 // Compile-time shape.  MAXT / MINB feed __launch_bounds__.  A shape is either
 // sequential (launched with S == 1, rows streamed from shared memory) or
 // windowed (S > 1, each thread's L rows held in registers).
-template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_, bool SEQ_>
+template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_, bool SEQ_, bool PT_ = false>
 struct WinShape {
     using St = St_;
     static constexpr bool SEQ = SEQ_;
+    // windowed prefix: false = lane threads scan the maps, true = every thread
+    // folds the maps before its own sub-chunk
+    static constexpr bool PT = PT_;
     static constexpr int DT = DT_;    // lanes per CTA
     static constexpr int V = V_;      // lanes per thread
     static constexpr int L = L_;      // steps per sub-chunk (held in registers)
@@ -64,7 +67,6 @@ struct WinShape {
 // Launch-time geometry (filled by the host from S and the stage count).
 struct WinGeom {
     int S;             // sub-chunks per window
-    int lane_scan;     // windowed prefix: 1 = lane threads scan the maps, 0 = every thread folds its own prefix
     int nstage;        // pipeline depth
     int W;             // rows per window = S*L
     int tile_bytes;    // W * ROW_BYTES
@@ -77,20 +79,18 @@ struct WinGeom {
 };
 
 template <class C>
-__host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D, int lane_scan = 1) {
+__host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D) {
     WinGeom g{};
     g.S = S;
-    g.lane_scan = lane_scan;
     g.nstage = nstage;
     g.W = S * C::L;
     g.tile_bytes = g.W * C::ROW_BYTES;
     g.stage_bytes = C::NIN * g.tile_bytes;
     g.bar_off = nstage * g.stage_bytes;
     g.scan_off = g.bar_off + 2 * nstage * 8;
-    // sub-chunk maps (P,Q) [2][S][DT] float2, entry states [S][DT] float and
-    // the carried state [2][DT] float (the lane scan uses one map buffer and
-    // the entries; the per-thread prefix uses both map buffers and the carry)
-    const int scan_bytes = S > 1 ? (2 * S * C::DT * 8 + S * C::DT * 4 + 2 * C::DT * 4) : 0;
+    // lane scan: sub-chunk maps (P,Q) [S][DT] float2 and entry states [S][DT];
+    // per-thread prefix: maps [2][S][DT] float2 and carried state [2][DT]
+    const int scan_bytes = S <= 1 ? 0 : (C::PT ? 2 * S * C::DT * 8 + 2 * C::DT * 4 : S * C::DT * 12);
     g.flag_off = g.scan_off + scan_bytes;
     g.smem_bytes = g.flag_off + 16;
     g.T = T;
@@ -128,17 +128,18 @@ struct WinSmem {
         return smem_addr(base + bar_off + (nstage + stage) * 8);
     }
     // (P, Q) of sub-chunk s for lane v*G + g at [par][s][v*G + g]: consecutive
-    // threads touch consecutive words (no bank conflicts)
+    // threads touch consecutive words (no bank conflicts); par is 0 for the
+    // lane scan
     template <class C> __device__ __forceinline__ float2 *sPQ(int par) const {
         return reinterpret_cast<float2 *>(base + scan_off) + par * S * C::DT;
     }
-    // entry state of sub-chunk s for lane v*G + g at [s][v*G + g]
+    // lane scan: entry state of sub-chunk s for lane v*G + g at [s][v*G + g]
     template <class C> __device__ __forceinline__ float *sEntry() const {
-        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8);
+        return reinterpret_cast<float *>(base + scan_off + S * C::DT * 8);
     }
-    // carried state [par][v*G + g]
+    // per-thread prefix: carried state [par][v*G + g]
     template <class C> __device__ __forceinline__ float *sCarry(int par) const {
-        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8 + S * C::DT * 4) + par * C::DT;
+        return reinterpret_cast<float *>(base + scan_off + 2 * S * C::DT * 8) + par * C::DT;
     }
     __device__ __forceinline__ volatile int *abort_flag() const {
         return reinterpret_cast<volatile int *>(base + flag_off);
@@ -183,7 +184,9 @@ __device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMa
     }
 }
 
-__device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S, int DT) {
+template <class C>
+__device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S) {
+    constexpr int DT = C::DT;
     const WinSmem &g = sm;
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.nstage; ++s) {
@@ -193,9 +196,9 @@ __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, 
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
-    if (S > 1) {
+    if (C::PT && S > 1) {
         // carried state starts at zero (h_{-1} = 0 forward, g_T = 0 backward)
-        float *c = reinterpret_cast<float *>(sm.base + g.scan_off + 2 * g.S * DT * 8 + g.S * DT * 4);
+        float *c = reinterpret_cast<float *>(sm.base + g.scan_off + 2 * g.S * DT * 8);
         for (int i = threadIdx.x; i < 2 * DT; i += blockDim.x) c[i] = 0.0f;
     }
     __syncthreads();
@@ -215,7 +218,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
     const int NT = S * G;
-    win_init(sm, NT / 32, S, DT);
+    win_init<C>(sm, NT / 32, S);
     const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
@@ -240,7 +243,6 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
     for (int v = 0; v < V; ++v) h[v] = 0.0f;
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (lane scan, threads < DT)
-    const bool lane_scan = geom.lane_scan != 0;
     bool failed = false;
     int stage = 0, use = 0;
 
@@ -306,25 +308,23 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        const int par = lane_scan ? 0 : (k & 1);
+        const int par = C::PT ? (k & 1) : 0;
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
-        if (lane_scan) {
+        if constexpr (!C::PT) {
             // Threads 0..DT-1 each own one lane: push the carried state through
             // the sub-chunk maps in order, recording every sub-chunk's entry
             // state (_real_chunk_prefix within the window; identity maps exact).
             float *entry = sm.sEntry<C>();
             if (static_cast<int>(threadIdx.x) < DT) {
                 float c = carry;
-#pragma unroll
-                for (int i = 0; i < C::SMAX; ++i) {
-                    if (i < S) {
-                        const float2 m = pq[i * DT + threadIdx.x];
-                        entry[i * DT + threadIdx.x] = c;
-                        c = __fmaf_rn(m.x, c, m.y);
-                    }
+#pragma unroll 4
+                for (int i = 0; i < S; ++i) {
+                    const float2 m = pq[i * DT + threadIdx.x];
+                    entry[i * DT + threadIdx.x] = c;
+                    c = __fmaf_rn(m.x, c, m.y);
                 }
                 carry = c;
             }
@@ -355,7 +355,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
             }
         }
-        if (!lane_scan && s == S - 1) {
+        if (C::PT && s == S - 1) {
             float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[v * G + lg] = h[v];
@@ -411,7 +411,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
     const int NT = S * G;
-    win_init(sm, NT / 32, S, DT);
+    win_init<C>(sm, NT / 32, S);
     const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
@@ -440,7 +440,6 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
     for (int v = 0; v < V; ++v) g[v] = 0.0f;
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (lane scan, threads < DT)
-    const bool lane_scan = geom.lane_scan != 0;
     int stage = 0, use = 0;
 
     for (int k = 0; k < nwin; ++k) {
@@ -520,24 +519,21 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        const int par = lane_scan ? 0 : (k & 1);
+        const int par = C::PT ? (k & 1) : 0;
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) break;
-        if (lane_scan) {
+        if constexpr (!C::PT) {
             // lane threads push the carried adjoint through sub-chunks S-1 .. 0
             float *entry = sm.sEntry<C>();
             if (static_cast<int>(threadIdx.x) < DT) {
                 float c = carry;
-#pragma unroll
-                for (int ii = 0; ii < C::SMAX; ++ii) {
-                    const int i = S - 1 - ii;
-                    if (i >= 0) {
-                        const float2 m = pq[i * DT + threadIdx.x];
-                        entry[i * DT + threadIdx.x] = c;
-                        c = __fmaf_rn(m.x, c, m.y);
-                    }
+#pragma unroll 4
+                for (int i = S - 1; i >= 0; --i) {
+                    const float2 m = pq[i * DT + threadIdx.x];
+                    entry[i * DT + threadIdx.x] = c;
+                    c = __fmaf_rn(m.x, c, m.y);
                 }
                 carry = c;
             }
@@ -560,7 +556,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         const size_t gofs = (row0 + rbase) * D + d;
         bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
-        if (!lane_scan && s == 0) {
+        if (C::PT && s == 0) {
             float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[v * G + lg] = g[v];
