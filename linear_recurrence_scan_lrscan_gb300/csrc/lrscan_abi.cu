@@ -192,6 +192,50 @@ int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, cons
     return best >= 0;
 }
 
+// The occupancy rule.  For each (dtype, direction), tile variants in order of
+// preference, each with the fewest CTAs (as a multiple of the SM count) at
+// which it fills the GPU; the first that qualifies (and fits on an SM) wins.
+// The order comes from timing every variant on the five named workloads on
+// GB300: the forward prefers the sequential path (bit-identical to the
+// sequential definition, and as fast wherever the lanes give each SM at
+// least two CTAs); the backward prefers the windowed path, which splits time
+// inside the CTA and keeps far more warps busy on the same lanes.
+struct Pref {
+    int path;
+    const char *name;
+    double min_ctas_per_sm;
+};
+const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
+const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
+const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d64", 1.5}, {kPathWindow, "win_bf16_d32_s16", 0.9}};
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n2", 0.9}, {kPathWindow, "win_bf16_d64_s8", 0.45}};
+
+bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *path, int *vidx) {
+    const Pref *list;
+    int n;
+    if (dtype == LRSCAN_F32) {
+        list = dir == 0 ? kPrefF32Fwd : kPrefF32Bwd;
+        n = 2;
+    } else {
+        list = dir == 0 ? kPrefBF16Fwd : kPrefBF16Bwd;
+        n = 2;
+    }
+    for (int i = 0; i < n; ++i) {
+        int cnt = 0;
+        const WinVariant *tab = win_variants(list[i].path, dtype, &cnt);
+        for (int v = 0; v < cnt; ++v) {
+            if (std::strcmp(tab[v].name, list[i].name) != 0) continue;
+            const Occ o = occupancy(tab[v], dir, B, D, g);
+            if (o.resident > 0 && static_cast<double>(o.ctas) >= list[i].min_ctas_per_sm * g.sm_count) {
+                *path = list[i].path;
+                *vidx = v;
+                return true;
+            }
+        }
+    }
+    return false;
+}
+
 int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
               const Geometry &g, Choice *ch) {
     const int want = opts ? opts->path : 0;
@@ -206,20 +250,18 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
     if (want < kPathAuto || want > kPathPlain) return fail(LRSCAN_EINVAL, "unknown path %d", want);
     if ((path == kPathSeq || path == kPathWindow) && !aligned16)
         return fail(LRSCAN_EINVAL, "path %d needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)", path);
+    int auto_vi = -1;
     if (path == kPathAuto) {
-        int vi = -1;
         if (!aligned16) {
             path = (B * D < 32LL * g.sm_count * 32 && T >= 16LL * chunk) ? kPathChunk : kPathPlain;
-        } else if (pick_window_variant(kPathSeq, dtype, dir, B, D, g, &vi)) {
-            path = kPathSeq;
-        } else if (pick_window_variant(kPathWindow, dtype, dir, B, D, g, &vi)) {
-            path = kPathWindow;
+        } else if (auto_candidate(dtype, dir, B, D, g, &path, &auto_vi)) {
+            // measured preference list (see auto_candidate)
         } else if (T >= 16LL * chunk) {
-            // too few lanes for a one-CTA-per-lane-tile walk to fill the GPU:
-            // parallelize over time chunks instead
+            // too few lanes for a lane-tiled walk to fill the GPU: parallelize
+            // over time chunks instead
             path = kPathChunk;
         } else {
-            path = kPathSeq;
+            path = kPathSeq;  // small problem: latency-bound whatever runs it
         }
     }
     ch->path = path;
@@ -230,6 +272,8 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         if (force_v > 0) {
             if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
             vi = force_v - 1;
+        } else if (auto_vi >= 0) {
+            vi = auto_vi;
         } else if (!pick_window_variant(path, dtype, dir, B, D, g, &vi)) {
             // too few lanes to fill the GPU (or too many for one wave): take the
             // variant with the most CTAs that still fits on an SM

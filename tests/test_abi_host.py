@@ -83,15 +83,30 @@ def test_workspace_bytes(lib):
     assert L.lrscan_workspace_bytes(1, 64, 8, 48) == 0
 
 
-@pytest.mark.parametrize("cid,expect", [(2, "seq"), (3, "window"), (4, "seq"), (5, "seq")])
-def test_occupancy_rule_on_the_named_workloads(lib, cid, expect):
+EXPECTED_AUTO = {
+    # workload: (forward tile, backward tile) the occupancy rule must pick
+    2: ("seq_bf16_d64", "win_bf16_d32_s16_n2"),
+    3: ("win_f32_d32_s16_pt", "win_f32_d32_s16_pt"),
+    4: ("seq_bf16_d64", "win_bf16_d32_s16_n2"),
+    5: ("seq_f32_d32", "win_f32_d64_s8"),
+}
+
+
+@pytest.mark.parametrize("cid", sorted(EXPECTED_AUTO))
+def test_occupancy_rule_on_the_named_workloads(lib, cid):
     from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
     w = WORKLOADS[cid]
-    for direction in ("fwd", "bwd"):
+    for direction, want in zip(("fwd", "bwd"), EXPECTED_AUTO[cid]):
         p = L.lrscan_plan(w.B, w.T, w.D, w.dtype, direction)
-        assert p["path"] == expect, (cid, direction, p)
-        # one wave: every CTA resident at once
-        assert p["ctas"] >= 0.9 * 152
+        assert p["name"] == want, (cid, direction, p)
+        assert p["kernels"] == 1
+        # every lane tile of the GPU-filling variants gets a CTA of its own
+        assert p["ctas"] == w.B * -(-w.D // p["lanes_per_cta"])
+
+
+def test_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
+    for (B, T, D, dt) in [(8, 2048, 2560, "bf16"), (64, 512, 1024, "f32"), (32, 1000, 4096, "f32")]:
+        assert L.lrscan_plan(B, T, D, dt, "fwd")["path"] == "seq"
 
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
