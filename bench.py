@@ -349,16 +349,30 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     return line
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; DRAM counters recorded for another hash are stale."""
+    import hashlib
+    csrc = os.path.join(ROOT, "linear_recurrence_scan_lrscan_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(w, direction: str, kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if one exists for
-    this exact kernel and workload (profiles/traffic.json)."""
+    """DRAM bytes (read + write) per launch of this kernel on this workload from
+    a committed ncu summary (profiles/traffic.json), or None when there is none
+    or the kernel sources changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    key = f"{w.name}:{direction}:{kernel}"
-    return d.get(key)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("entries", {}).get(f"{w.name}:{direction}:{kernel}")
 
 
 def main():
