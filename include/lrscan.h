@@ -170,6 +170,38 @@ const char *lrscan_last_error(void);
 
 int lrscan_version(void);
 
+/*
+ * Chunked forward scan that allocates nothing.
+ *
+ * No counterpart in the paper: this entry point exists for callers that
+ * cannot call cudaMalloc while they run (code inside an allocator or
+ * memory-pool callback, where a nested allocation would re-enter the
+ * allocator; latency-critical loops that ban allocation because cudaMalloc
+ * may synchronize the device; hosts that only hand the library pre-sized
+ * buffers).  It runs the same three chunked phases as LRSCAN_PATH_CHUNK with
+ * the same arguments and results as lrscan_fwd_ex(..., path = chunk,
+ * chunk_len), but its scratch (the chunk summaries P and Q) lives in one
+ * fixed device array of LRSCAN_NOALLOC_SCRATCH_BYTES that the library owns.
+ *   - Every GPU that loads the library holds that array until the process
+ *     exits.
+ *   - A problem needs 2 * B * ceil(T / chunk_len) * D * 4 bytes of it (each
+ *     half rounded up to 256 bytes); larger problems are rejected with
+ *     LRSCAN_ENOMEM (see lrscan_last_error) before anything is launched.
+ *   - All calls on a device share the array: calls whose kernels overlap on
+ *     the GPU (different streams, no ordering between them) race and produce
+ *     wrong results.  Calls on one stream are safe.  Nothing has to be cleared
+ *     between calls: each call writes all the scratch it reads.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture begins.
+ *   - a, b, out, last, sizes and dtype as in lrscan_fwd; chunk_len 16, 32 or
+ *     64 (0 means 64); stream is a cudaStream_t (NULL = legacy default stream).
+ */
+#define LRSCAN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int lrscan_fwd_chunk_noalloc(const void *a, const void *b, void *out, float *last,
+                             int64_t B, int64_t T, int64_t D, int dtype,
+                             int chunk_len, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

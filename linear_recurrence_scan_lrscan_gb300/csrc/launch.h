@@ -70,4 +70,7 @@ int plain_fwd_launch(const ChunkLaunch &L, int dtype);
 int plain_bwd_launch(const ChunkLaunch &L, int dtype);
 int selftest_wait_launch(DevStatus *status, uint64_t timeout_ns, cudaStream_t stream);
 
+// Records the detail text lrscan_last_error() returns and passes code through.
+int report_error(int code, const char *msg);
+
 }  // namespace lrscan

@@ -524,6 +524,10 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
 }
 
 }  // namespace
+
+// Lets other translation units of the library report why a call failed.
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 }  // namespace lrscan
 
 using namespace lrscan;

@@ -86,6 +86,7 @@ EXPORTS = {
     "lrscan_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "lrscan_version": ([], ctypes.c_int),
     "lrscan_last_error": ([], ctypes.c_char_p),
+    "lrscan_fwd_chunk_noalloc": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
 }
 
 _lock = threading.Lock()
