@@ -78,6 +78,10 @@ using SBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 2, 64, 1, true>;
 using SBF_128_2_32 = WinShape<bf16_t, 128, 2, 32, 2, 96, 1, true>;
 using SBF_128_4_32 = WinShape<bf16_t, 128, 4, 32, 2, 64, 1, true>;
 using SBB_64_2_32 = WinShape<bf16_t, 64, 2, 32, 3, 64, 1, true>;
+using SBF_32_1_32 = WinShape<bf16_t, 32, 1, 32, 2, 64, 1, true>;
+using SBF_64_1_32 = WinShape<bf16_t, 64, 1, 32, 2, 96, 1, true>;
+using SBB_32_1_32 = WinShape<bf16_t, 32, 1, 32, 3, 64, 1, true>;
+using SBB_64_1_32 = WinShape<bf16_t, 64, 1, 32, 3, 96, 1, true>;
 using SBB_128_2_32 = WinShape<bf16_t, 128, 2, 32, 3, 96, 1, true>;
 using SBB_128_4_16 = WinShape<bf16_t, 128, 4, 16, 3, 64, 1, true>;
 using SFF_32_1_32 = WinShape<float, 32, 1, 32, 2, 64, 1, true>;
@@ -127,6 +131,8 @@ const WinVariant kSeqBF16[] = {
     {"seq_bf16_d128", F(SBF_128_2_32, 1, 4), B(SBB_128_2_32, 1, 4)},
     {"seq_bf16_d64_s9", F(SBF_64_2_32, 1, 9), B(SBB_64_2_32, 1, 6)},
     {"seq_bf16_d128_v4", F(SBF_128_4_32, 1, 6), B(SBB_128_4_16, 1, 6)},
+    {"seq_bf16_d32_v1", F(SBF_32_1_32, 1, 8), B(SBB_32_1_32, 1, 6)},
+    {"seq_bf16_d64_v1", F(SBF_64_1_32, 1, 8), B(SBB_64_1_32, 1, 6)},
 };
 const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s16", F(BF_32_2_8, 16, 3), B(BB_32_2_8, 16, 4)},

@@ -74,6 +74,38 @@ __device__ __forceinline__ void unpack_lanes(const St *p, float (&x)[V]) {
     }
 }
 
+// V storage elements as one packed register-sized value, and its widening.
+template <typename St, int V> struct RawOf;
+template <> struct RawOf<float, 1> { using T = float; };
+template <> struct RawOf<float, 2> { using T = float2; };
+template <> struct RawOf<float, 4> { using T = float4; };
+template <> struct RawOf<bf16_t, 1> { using T = unsigned short; };
+template <> struct RawOf<bf16_t, 2> { using T = uint32_t; };
+template <> struct RawOf<bf16_t, 4> { using T = uint2; };
+template <> struct RawOf<bf16_t, 8> { using T = uint4; };
+
+template <typename St, int V>
+__device__ __forceinline__ typename RawOf<St, V>::T load_raw(const St *p) {
+    return *reinterpret_cast<const typename RawOf<St, V>::T *>(p);
+}
+
+// Widening works on the value (taking its address would force it to memory).
+__device__ __forceinline__ void widen2(uint32_t u, float &lo, float &hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+}
+__device__ __forceinline__ void widen_raw(float r, float (&x)[1]) { x[0] = r; }
+__device__ __forceinline__ void widen_raw(float2 r, float (&x)[2]) { x[0] = r.x; x[1] = r.y; }
+__device__ __forceinline__ void widen_raw(float4 r, float (&x)[4]) { x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w; }
+__device__ __forceinline__ void widen_raw(unsigned short r, float (&x)[1]) {
+    x[0] = __uint_as_float(static_cast<uint32_t>(r) << 16);
+}
+__device__ __forceinline__ void widen_raw(uint32_t r, float (&x)[2]) { widen2(r, x[0], x[1]); }
+__device__ __forceinline__ void widen_raw(uint2 r, float (&x)[4]) { widen2(r.x, x[0], x[1]); widen2(r.y, x[2], x[3]); }
+__device__ __forceinline__ void widen_raw(uint4 r, float (&x)[8]) {
+    widen2(r.x, x[0], x[1]); widen2(r.y, x[2], x[3]); widen2(r.z, x[4], x[5]); widen2(r.w, x[6], x[7]);
+}
+
 // Read-only global variant (non-coherent path, may be cached in L1).
 template <typename St, int V>
 __device__ __forceinline__ void load_lanes_global(const St *__restrict__ p, float (&x)[V]) {
@@ -109,8 +141,10 @@ __device__ __forceinline__ void load_lanes_global(const St *__restrict__ p, floa
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x -> low half
-    return *reinterpret_cast<uint32_t *>(&v);
+    // round-to-nearest-even of both halves; lo lands in the low 16 bits
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 template <typename St, int V>

@@ -298,14 +298,23 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         float P[V], Q[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+        if (n < L) {
+            // tail sub-chunk: steps past T become exact identity steps (a=1, b=0)
 #pragma unroll
-        for (int j = 0; j < L; ++j) {
-            if (j < n) {
+            for (int j = 0; j < L; ++j) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    P[v] = __fmul_rn(xa[j][v], P[v]);
-                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
+                    xa[j][v] = j < n ? xa[j][v] : 1.0f;
+                    xb[j][v] = j < n ? xb[j][v] : 0.0f;
                 }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                P[v] = __fmul_rn(xa[j][v], P[v]);
+                Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
             }
         }
         const int par = C::PT ? (k & 1) : 0;
@@ -347,12 +356,20 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         St *op = out + (row0 + rbase) * D + d;
+        if (n == L) {
 #pragma unroll
-        for (int j = 0; j < L; ++j) {
-            if (j < n) {
+            for (int j = 0; j < L; ++j) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
                 if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
+            }
+        } else {
+            // identity steps past T leave h unchanged; their rows are not stored
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+                if (lane_ok && j < n) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
             }
         }
         if (C::PT && s == S - 1) {
@@ -382,19 +399,19 @@ __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const fl
                                          typename C::St *gb, typename C::St *ga, int D) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L;
+    // rows past T hold identity steps (a=1, grad_out=0), set by the caller: g
+    // passes through them unchanged and they are not stored
 #pragma unroll
     for (int j = L - 1; j >= 0; --j) {
-        if (j < n) {
-            float gav[V];
+        float gav[V];
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
-                gav[v] = __fmul_rn(g[v], xh[j][v]);
-            }
-            if (lane_ok) {
-                store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
-                store_lanes<St, V>(ga + static_cast<size_t>(j) * D, gav);
-            }
+        for (int v = 0; v < V; ++v) {
+            g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
+            gav[v] = __fmul_rn(g[v], xh[j][v]);
+        }
+        if (lane_ok && (n == L || j < n)) {
+            store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
+            store_lanes<St, V>(ga + static_cast<size_t>(j) * D, gav);
         }
     }
 }
@@ -509,14 +526,23 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         float P[V], Q[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+        if (n < L) {
+            // tail sub-chunk: steps past T become exact identity steps (a=1, grad_out=0)
 #pragma unroll
-        for (int j = L - 1; j >= 0; --j) {
-            if (j < n) {
+            for (int j = 0; j < L; ++j) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    P[v] = __fmul_rn(xa[j][v], P[v]);
-                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
+                    xa[j][v] = j < n ? xa[j][v] : 1.0f;
+                    xg[j][v] = j < n ? xg[j][v] : 0.0f;
                 }
+            }
+        }
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                P[v] = __fmul_rn(xa[j][v], P[v]);
+                Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
             }
         }
         const int par = C::PT ? (k & 1) : 0;
