@@ -28,9 +28,10 @@ int launch_win_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
-        *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last, g, L.status, L.timeout_ns);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last,
+                                     g, L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
 }
 
 template <class C>
@@ -41,10 +42,11 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    fn<<<dim3(ndt, static_cast<unsigned>(L.B)), cfg.threads, g.smem_bytes, L.stream>>>(
-        *L.maps[0], *L.maps[1], *L.maps[2], static_cast<typename C::St *>(L.out0),
-        static_cast<typename C::St *>(L.out1), g, L.status, L.timeout_ns);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2],
+                                     static_cast<typename C::St *>(L.out0), static_cast<typename C::St *>(L.out1), g,
+                                     L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
 }
 
 template <class C, bool FWD>

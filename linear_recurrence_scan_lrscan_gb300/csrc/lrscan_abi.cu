@@ -207,7 +207,7 @@ struct Pref {
 };
 const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
 const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
-const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d64", 1.5}, {kPathWindow, "win_bf16_d32_s16", 0.9}};
+const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d64_v1", 1.5}, {kPathWindow, "win_bf16_d32_s16", 0.9}};
 const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n2", 0.9}, {kPathWindow, "win_bf16_d64_s8", 0.45}};
 
 bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *path, int *vidx) {

@@ -222,6 +222,13 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Programmatic dependent launch: the next kernel in the stream may be launched
+// (and run its prologue) once every CTA of this one has triggered; each kernel
+// waits for the previous grid's completion, and its memory, before it reads
+// or writes any global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 3-D tiled bulk copy global -> shared; completion is counted in bytes on `bar`.
 // Coordinates are element indices {x: lane, y: time, z: batch row}; out-of-range
 // parts of the box are filled with zeros.

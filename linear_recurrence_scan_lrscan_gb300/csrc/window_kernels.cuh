@@ -219,6 +219,8 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const int S = geom.S;
     const int NT = S * G;
     win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();  // inputs may come from the previous kernel in the stream
     const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;
@@ -252,17 +254,25 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const St *tb = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;
         if constexpr (C::SEQ) {
             if (!ok) { failed = true; break; }
-            // straight through the window's L rows, one fma per step; the loop
-            // is fully unrolled so the shared-memory loads run ahead of the chain
+            // straight through the window's L rows, one fma per step
             const int rbase = k * sm.W;
             const int n = min(T - rbase, L);
             St *op = out + (row0 + rbase) * D + d;
             if (n == L) {
+                // full window: rows to registers as packed words first (all the
+                // shared-memory loads issue before the dependent chain starts)
+                using Raw = typename RawOf<St, V>::T;
+                Raw ra[L], rb[L];
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    ra[j] = load_raw<St, V>(ta + j * DT);
+                    rb[j] = load_raw<St, V>(tb + j * DT);
+                }
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
                     float x[V], y[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(tb + j * DT, y);
+                    widen_raw(ra[j], x);
+                    widen_raw(rb[j], y);
 #pragma unroll
                     for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
                     if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
@@ -429,6 +439,8 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const int S = geom.S;
     const int NT = S * G;
     win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();  // inputs may come from the previous kernel in the stream
     const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
     const int d0 = blockIdx.x * DT;
     const int brow = blockIdx.y;

@@ -85,9 +85,9 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("seq_bf16_d64", "win_bf16_d32_s16_n2"),
+    2: ("seq_bf16_d64_v1", "win_bf16_d32_s16_n2"),
     3: ("win_f32_d32_s16_pt", "win_f32_d32_s16_pt"),
-    4: ("seq_bf16_d64", "win_bf16_d32_s16_n2"),
+    4: ("seq_bf16_d64_v1", "win_bf16_d32_s16_n2"),
     5: ("seq_f32_d32", "win_f32_d64_s8"),
 }
 
