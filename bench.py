@@ -250,7 +250,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     t_start.record(stream)
     for i in range(args.steps):
         ev = None
-        if i % sample_every == sample_every // 2:
+        if i % sample_every == min(sample_every // 2, args.steps - 1):
             ev = evs[i] = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         step(args.warmup + i, ev)
     t_end.record(stream)
