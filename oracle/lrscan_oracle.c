@@ -360,3 +360,127 @@ int lro_chunk_bwd_f64(const double *a, const double *out,
     if (bad_shape(B, T, D) || C <= 0) return LRO_EINVAL;
     CHUNK_BODY_BWD(double)
 }
+
+/* ---------------------------------------------------------------------- */
+/* Carried state and segment resets.                                       */
+/*                                                                         */
+/* The state-carrying scans of triton_training_scan.py (_samu_tiled_serial */
+/* _forward and _samu_tiled_serial_backward: optional initial state h0, a  */
+/* per-token segment position whose zeros start a new segment, the         */
+/* gradient arriving at the final state, the gradient of the initial       */
+/* state) applied to the plain real recurrence; recurrence.py of the KDN    */
+/* page carries the same state across calls so that prefill and decode      */
+/* continue one sequence exactly.                                           */
+/*                                                                         */
+/*   forward   h_{-1} = h0 (0 when absent)                                 */
+/*             a'_t = 0 where segment_pos[b,t] == 0, else a_t               */
+/*             h_t = a'_t * h_{t-1} + b_t;  out_t = h_t;  last = h_{T-1}    */
+/*   backward  g_T = grad_last (0 when absent) entering through a'_T = 1    */
+/*             g_t = grad_out_t + a'_{t+1} * g_{t+1}    (one rounding)      */
+/*             grad_b_t = g_t                                               */
+/*             grad_a_t = +0 where step t resets (a_t is not used there),   */
+/*                        else g_t * out_{t-1}, with out_{-1} = h0          */
+/*             grad_h0  = a'_0 * g_0  (= grad_last when T == 0)             */
+/*                                                                         */
+/* h0, grad_last and grad_h0 are [B,D] in the state precision (fp32 for    */
+/* the fp32 and bf16 storage variants, fp64 for the fp64 one); segment_pos */
+/* is int32 [B,T].  Every pointer of the extension may be NULL.            */
+/* ---------------------------------------------------------------------- */
+
+static int resets(const int32_t *seg, int64_t bb, int64_t T, int64_t t)
+{
+    return seg != NULL && t >= 0 && t < T && seg[bb * T + t] == 0;
+}
+
+#define STATE_FWD_BODY(STATE, FMA, LOAD, STORE)                                \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE h = h0 ? h0[bb * D + d] : 0;                                 \
+            for (int64_t t = 0; t < T; ++t) {                                  \
+                int64_t i = (bb * T + t) * D + d;                              \
+                STATE x = resets(seg, bb, T, t) ? 0 : LOAD(a[i]);              \
+                h = FMA(x, h, LOAD(b[i]));                                     \
+                out[i] = STORE(h);                                             \
+            }                                                                  \
+            if (last) last[bb * D + d] = h;                                    \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define STATE_BWD_BODY(STATE, FMA, LOAD, STORE)                                \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE g = grad_last ? grad_last[bb * D + d] : 0;                   \
+            for (int64_t t = T - 1; t >= 0; --t) {                             \
+                int64_t i = (bb * T + t) * D + d;                              \
+                /* a'_{t+1}: 1 past the end (the grad_last entry), 0 at a      \
+                 * reset */                                                    \
+                STATE x_next = (t == T - 1) ? 1                                \
+                               : (resets(seg, bb, T, t + 1) ? 0 : LOAD(a[i + D])); \
+                g = FMA(x_next, g, LOAD(grad_out[i]));                         \
+                STATE h_prev = (t > 0) ? LOAD(out[i - D])                      \
+                               : (h0 ? h0[bb * D + d] : 0);                    \
+                grad_b[i] = STORE(g);                                          \
+                grad_a[i] = resets(seg, bb, T, t) ? STORE(0) : STORE(g * h_prev); \
+            }                                                                  \
+            if (grad_h0) {                                                     \
+                if (T == 0)                                                    \
+                    grad_h0[bb * D + d] = g;                                   \
+                else                                                           \
+                    grad_h0[bb * D + d] = resets(seg, bb, T, 0)                \
+                                          ? 0 : LOAD(a[bb * T * D + d]) * g;   \
+            }                                                                  \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define LRO_SAME(x) (x)
+
+int lro_fwd_state_f32(const float *a, const float *b, float *out, float *last,
+                      const float *h0, const int32_t *seg,
+                      int64_t B, int64_t T, int64_t D)
+{
+    STATE_FWD_BODY(float, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_fwd_state_bf16(const uint16_t *a, const uint16_t *b, uint16_t *out,
+                       float *last, const float *h0, const int32_t *seg,
+                       int64_t B, int64_t T, int64_t D)
+{
+    STATE_FWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_fwd_state_f64(const double *a, const double *b, double *out,
+                      double *last, const double *h0, const int32_t *seg,
+                      int64_t B, int64_t T, int64_t D)
+{
+    STATE_FWD_BODY(double, fma, LRO_SAME, LRO_SAME)
+}
+
+int lro_bwd_state_f32(const float *a, const float *out, const float *grad_out,
+                      const float *h0, const int32_t *seg,
+                      const float *grad_last, float *grad_a, float *grad_b,
+                      float *grad_h0, int64_t B, int64_t T, int64_t D)
+{
+    STATE_BWD_BODY(float, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_bwd_state_bf16(const uint16_t *a, const uint16_t *out,
+                       const uint16_t *grad_out, const float *h0,
+                       const int32_t *seg, const float *grad_last,
+                       uint16_t *grad_a, uint16_t *grad_b, float *grad_h0,
+                       int64_t B, int64_t T, int64_t D)
+{
+    STATE_BWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_bwd_state_f64(const double *a, const double *out,
+                      const double *grad_out, const double *h0,
+                      const int32_t *seg, const double *grad_last,
+                      double *grad_a, double *grad_b, double *grad_h0,
+                      int64_t B, int64_t T, int64_t D)
+{
+    STATE_BWD_BODY(double, fma, LRO_SAME, LRO_SAME)
+}

@@ -65,6 +65,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lro_chunk_bwd_f32", "lro_chunk_bwd_f64"):
         getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64]
         getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_fwd_state_f32", "lro_fwd_state_bf16", "lro_fwd_state_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_bwd_state_f32", "lro_bwd_state_bf16", "lro_bwd_state_f64"):
+        getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
     lib.lro_f32_to_bf16_array.argtypes = [_P, _P, _I64]
     lib.lro_bf16_to_f32_array.argtypes = [_P, _P, _I64]
     lib.lro_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -161,6 +167,59 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle chunk backward failed ({rc})")
         return ga, gb
+
+    def _state(self, x, dtype, shape, what):
+        if x is None:
+            return None
+        want = _LAST[dtype]
+        if x.dtype != want or tuple(x.shape) != tuple(shape):
+            raise TypeError(f"oracle {dtype} {what} must be {np.dtype(want).name} {tuple(shape)}")
+        return np.ascontiguousarray(x)
+
+    @staticmethod
+    def _seg(seg, B, T):
+        if seg is None:
+            return None
+        if seg.dtype != np.int32 or seg.shape != (B, T):
+            raise TypeError("segment_pos must be int32 [B, T]")
+        return np.ascontiguousarray(seg)
+
+    def fwd_state(self, a, b, dtype="f32", h0=None, segment_pos=None):
+        """Forward scan from the initial state h0 with segment resets
+        (steps where segment_pos == 0 ignore the previous state); ``(out, last)``."""
+        a, b = _c(a, dtype), _c(b, dtype)
+        if a.shape != b.shape:
+            raise ValueError("a and b must have the same [B, T, D] shape")
+        B, T, D = a.shape
+        h0 = self._state(h0, dtype, (B, D), "h0")
+        seg = self._seg(segment_pos, B, T)
+        out = np.empty_like(a)
+        last = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_fwd_state_{dtype}")(
+            _ptr(a), _ptr(b), _ptr(out), _ptr(last), None if h0 is None else _ptr(h0),
+            None if seg is None else _ptr(seg), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle state forward failed ({rc})")
+        return out, last
+
+    def bwd_state(self, a, out, grad_out, dtype="f32", h0=None, segment_pos=None, grad_last=None):
+        """Reverse scan of :meth:`fwd_state`; ``(grad_a, grad_b, grad_h0)``."""
+        a, out, grad_out = _c(a, dtype), _c(out, dtype), _c(grad_out, dtype)
+        if not (a.shape == out.shape == grad_out.shape):
+            raise ValueError("a, out and grad_out must have the same [B, T, D] shape")
+        B, T, D = a.shape
+        h0 = self._state(h0, dtype, (B, D), "h0")
+        gl = self._state(grad_last, dtype, (B, D), "grad_last")
+        seg = self._seg(segment_pos, B, T)
+        ga, gb = np.empty_like(a), np.empty_like(a)
+        gh0 = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_bwd_state_{dtype}")(
+            _ptr(a), _ptr(out), _ptr(grad_out), None if h0 is None else _ptr(h0),
+            None if seg is None else _ptr(seg), None if gl is None else _ptr(gl),
+            _ptr(ga), _ptr(gb), _ptr(gh0), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle state backward failed ({rc})")
+        return ga, gb, gh0
 
     def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
         x = np.ascontiguousarray(x, dtype=np.float32)

@@ -417,4 +417,258 @@ def pin_empty_shapes(o):
         o.bwd(a, a, a, "f64")
 
 
+# ------------------------------------------- carried state and resets ----
+# The state-carrying forms of the scan (initial state h0, segment resets
+# where segment_pos == 0, gradient grad_last arriving at the final state,
+# gradient grad_h0 of the initial state).
+
+def _segments(seed, B, T, p=0.15, first=None):
+    """int32 [B, T] segment positions with random segment starts (zeros)."""
+    r = _rng(seed)
+    starts = r.random((B, T)) < p
+    if first is not None:
+        starts[:, 0] = first
+    seg = np.zeros((B, T), dtype=np.int32)
+    for bb in range(B):
+        pos = 0
+        for t in range(T):
+            pos = 0 if starts[bb, t] else pos + 1 if t > 0 else 1
+            seg[bb, t] = pos
+    return seg
+
+
+def _state_case(seed, B, T, D, dtype):
+    a, b, g = _case(seed, B, T, D, lo=0.6, hi=1.0, dtype=np.float32)
+    r = _rng(seed + 1000)
+    h0 = r.standard_normal((B, D)).astype(np.float32)
+    gl = r.standard_normal((B, D)).astype(np.float32)
+    return a, b, g, h0, gl
+
+
+def _enc(o, dt, *xs):
+    if dt == "bf16":
+        return [o.f32_to_bf16(x) for x in xs]
+    npdt = np.float64 if dt == "f64" else np.float32
+    return [x.astype(npdt) for x in xs]
+
+
+def _dec(o, dt, x):
+    return o.bf16_to_f32(x).astype(np.float64) if dt == "bf16" else x.astype(np.float64)
+
+
+def pin_state_absent_is_plain_scan(o):
+    """No state, or a zero h0, no resets and a zero grad_last, gives the plain
+    scan bit for bit; grad_h0 is then a_0 * g_0."""
+    a, b, g, _, _ = _state_case(30, 2, 41, 5, np.float32)
+    B, T, D = a.shape
+    for dt in ("f32", "bf16", "f64"):
+        aa, bb_, gg = _enc(o, dt, a, b, g)
+        sdt = np.float64 if dt == "f64" else np.float32
+        out, last = o.fwd(aa, bb_, dt)
+        ga, gb = o.bwd(aa, out, gg, dt)
+        for h0, seg, gl in ((None, None, None),
+                            (np.zeros((B, D), sdt), np.arange(1, T + 1, dtype=np.int32)[None].repeat(B, 0),
+                             np.zeros((B, D), sdt))):
+            o2, l2 = o.fwd_state(aa, bb_, dt, h0=h0, segment_pos=seg)
+            assert np.array_equal(o2, out) and np.array_equal(l2, last), dt
+            ga2, gb2, gh0 = o.bwd_state(aa, out, gg, dt, h0=h0, segment_pos=seg, grad_last=gl)
+            assert np.array_equal(ga2, ga) and np.array_equal(gb2, gb), dt
+            want = _dec(o, dt, aa)[:, 0, :] * _dec(o, dt, gb)[:, 0, :] if dt != "bf16" else None
+            if dt == "f64":
+                assert np.array_equal(gh0, want)
+            elif dt == "f32":
+                assert np.array_equal(gh0, (a[:, 0, :].astype(np.float64) * gb[:, 0, :]).astype(np.float32))
+
+
+def pin_state_prefill_continues_exactly(o):
+    """Scanning a prefix, then the rest from the prefix's final state, equals
+    one scan of the whole sequence bit for bit (forward, every dtype, with
+    resets); the split backward (the suffix's grad_h0 fed to the prefix as
+    grad_last) equals the whole backward to rounding."""
+    a, b, g, h0, gl = _state_case(31, 3, 50, 4, np.float32)
+    seg = _segments(32, 3, 50)
+    for dt in ("f32", "bf16", "f64"):
+        aa, bb_, gg = _enc(o, dt, a, b, g)
+        sdt = np.float64 if dt == "f64" else np.float32
+        hh, gll = h0.astype(sdt), gl.astype(sdt)
+        out, last = o.fwd_state(aa, bb_, dt, h0=hh, segment_pos=seg)
+        for T1 in (1, 17, 49):
+            o1, l1 = o.fwd_state(np.ascontiguousarray(aa[:, :T1]), np.ascontiguousarray(bb_[:, :T1]), dt,
+                                 h0=hh, segment_pos=np.ascontiguousarray(seg[:, :T1]))
+            o2, l2 = o.fwd_state(np.ascontiguousarray(aa[:, T1:]), np.ascontiguousarray(bb_[:, T1:]), dt,
+                                 h0=l1, segment_pos=np.ascontiguousarray(seg[:, T1:]))
+            assert np.array_equal(np.concatenate([o1, o2], axis=1), out), (dt, T1)
+            assert np.array_equal(l2, last), (dt, T1)
+    a64, b64, g64 = (x.astype(np.float64) for x in (a, b, g))
+    h064, gl64 = h0.astype(np.float64), gl.astype(np.float64)
+    out, _ = o.fwd_state(a64, b64, "f64", h0=h064, segment_pos=seg)
+    ga, gb, gh0 = o.bwd_state(a64, out, g64, "f64", h0=h064, segment_pos=seg, grad_last=gl64)
+    for T1 in (1, 17, 49):
+        sl1, sl2 = (slice(None), slice(None, T1)), (slice(None), slice(T1, None))
+        c = np.ascontiguousarray
+        _, l1 = o.fwd_state(c(a64[sl1]), c(b64[sl1]), "f64", h0=h064, segment_pos=c(seg[sl1]))
+        ga2, gb2, gmid = o.bwd_state(c(a64[sl2]), c(out[sl2]), c(g64[sl2]), "f64", h0=l1,
+                                     segment_pos=c(seg[sl2]), grad_last=gl64)
+        ga1, gb1, g0 = o.bwd_state(c(a64[sl1]), c(out[sl1]), c(g64[sl1]), "f64", h0=h064,
+                                   segment_pos=c(seg[sl1]), grad_last=gmid)
+        np.testing.assert_allclose(np.concatenate([gb1, gb2], axis=1), gb, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(np.concatenate([ga1, ga2], axis=1), ga, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g0, gh0, rtol=1e-12, atol=1e-12)
+
+
+def pin_state_segments_are_independent_sequences(o):
+    """With resets, every segment is the plain scan of its own steps started
+    from zero (the first one from h0 unless step 0 resets); in the backward the
+    segments are independent too, grad_a is zero at a segment start, only the
+    last segment sees grad_last and only the first one feeds grad_h0."""
+    B, T, D = 4, 60, 3
+    a, b, g, h0, gl = _state_case(33, B, T, D, np.float32)
+    seg = _segments(34, B, T, p=0.1)
+    seg[0, 0] = 0           # row 0 starts with a reset: h0 is ignored
+    seg[1, 0] = 5           # row 1 continues h0
+    for dt in ("f32", "bf16", "f64"):
+        aa, bb_, gg = _enc(o, dt, a, b, g)
+        sdt = np.float64 if dt == "f64" else np.float32
+        hh, gll = h0.astype(sdt), gl.astype(sdt)
+        out, last = o.fwd_state(aa, bb_, dt, h0=hh, segment_pos=seg)
+        ga, gb, gh0 = o.bwd_state(aa, out, gg, dt, h0=hh, segment_pos=seg, grad_last=gll)
+        for r in range(B):
+            starts = [t for t in range(T) if seg[r, t] == 0]
+            bounds = sorted(set([0] + starts + [T]))
+            for k in range(len(bounds) - 1):
+                lo, hi = bounds[k], bounds[k + 1]
+                first = lo == 0 and seg[r, 0] != 0
+                c = np.ascontiguousarray
+                sa, sb, sg = c(aa[r:r + 1, lo:hi]), c(bb_[r:r + 1, lo:hi]), c(gg[r:r + 1, lo:hi])
+                h_in = hh[r:r + 1] if first else None
+                so, sl = o.fwd_state(sa, sb, dt, h0=h_in)
+                assert np.array_equal(so, out[r:r + 1, lo:hi]), (dt, r, lo)
+                if hi == T:
+                    assert np.array_equal(sl, last[r:r + 1]), (dt, r)
+                sga, sgb, sgh = o.bwd_state(sa, so, sg, dt, h0=h_in,
+                                            grad_last=gll[r:r + 1] if hi == T else None)
+                assert np.array_equal(sgb, gb[r:r + 1, lo:hi]), (dt, r, lo)
+                # isolated segment: grad_a at its first step is g * 0 (+-0)
+                assert np.array_equal(_dec(o, dt, sga), _dec(o, dt, ga[r:r + 1, lo:hi])), (dt, r, lo)
+                if lo > 0 or not first:
+                    assert _dec(o, dt, ga[r:r + 1, lo]).tolist() == [[0.0] * D]
+                    assert not np.signbit(_dec(o, dt, ga[r:r + 1, lo])).any(), "+0 at a reset"
+                if first:
+                    assert np.array_equal(sgh, gh0[r:r + 1]), (dt, r)
+            if seg[r, 0] == 0:
+                assert np.array_equal(gh0[r], np.zeros(D)), (dt, r)
+
+
+def pin_state_initial_state_closed_form(o):
+    """a == c, b == 0: h_t = c^{t+1} h0, and with L = sum_t g_t h_t + gl h_{T-1}
+    the initial-state gradient is sum_t g_t c^{t+1} + gl c^T; a reset at step r
+    cuts both sums at r."""
+    T = 40
+    r = _rng(35)
+    g = r.standard_normal((1, T, 1))
+    for c in (0.9, -0.8, 1.0):
+        a = np.full((1, T, 1), c)
+        b = np.zeros((1, T, 1))
+        h0 = np.array([[1.75]])
+        gl = np.array([[-0.5]])
+        out, last = o.fwd_state(a, b, "f64", h0=h0)
+        t = np.arange(T)
+        np.testing.assert_allclose(out[0, :, 0], c ** (t + 1) * 1.75, rtol=1e-12)
+        np.testing.assert_allclose(last[0, 0], c ** T * 1.75, rtol=1e-12)
+        _, _, gh0 = o.bwd_state(a, out, g, "f64", h0=h0, grad_last=gl)
+        want = np.sum(g[0, :, 0] * c ** (t + 1)) - 0.5 * c ** T
+        assert abs(gh0[0, 0] - want) <= 1e-12 * (1 + abs(want))
+        for cut in (0, 13):
+            seg = np.ones((1, T), dtype=np.int32)
+            seg[0, cut] = 0
+            out, last = o.fwd_state(a, b, "f64", h0=h0, segment_pos=seg)
+            want_h = np.where(t < cut, c ** (t + 1) * 1.75, 0.0)
+            np.testing.assert_allclose(out[0, :, 0], want_h, rtol=1e-12, atol=0)
+            _, _, gh0 = o.bwd_state(a, out, g, "f64", h0=h0, segment_pos=seg, grad_last=gl)
+            want = np.sum(g[0, :cut, 0] * c ** (t[:cut] + 1))
+            assert abs(gh0[0, 0] - want) <= 1e-12 * (1 + abs(want)), (c, cut)
+
+
+def pin_state_finite_difference_jacobian(o):
+    """Central differences of L = sum grad_out*h + sum grad_last*h_{T-1} with
+    an initial state and resets, against grad_a, grad_b and grad_h0 (fp64)."""
+    B, T, D = 2, 9, 2
+    a, b, g = _case(36, B, T, D, lo=-0.95, hi=0.95)
+    r = _rng(37)
+    h0 = r.standard_normal((B, D))
+    gl = r.standard_normal((B, D))
+    seg = np.ones((B, T), dtype=np.int32)
+    seg[0, 4] = 0
+    seg[1, 0] = 0
+    seg[1, 6] = 0
+    out, _ = o.fwd_state(a, b, "f64", h0=h0, segment_pos=seg)
+    ga, gb, gh0 = o.bwd_state(a, out, g, "f64", h0=h0, segment_pos=seg, grad_last=gl)
+    eps = 1e-6
+
+    def loss(aa, bb, hh):
+        h, last = o.fwd_state(aa, bb, "f64", h0=hh, segment_pos=seg)
+        return float(np.sum(g * h) + np.sum(gl * last))
+    for idx in np.ndindex(a.shape):
+        for arr, grad, name in ((a, ga, "grad_a"), (b, gb, "grad_b")):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            args_p = (p, b, h0) if name == "grad_a" else (a, p, h0)
+            args_m = (m, b, h0) if name == "grad_a" else (a, m, h0)
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * (1 + abs(fd)), (name, idx, fd, grad[idx])
+    for idx in np.ndindex(h0.shape):
+        p, m = h0.copy(), h0.copy()
+        p[idx] += eps
+        m[idx] -= eps
+        fd = (loss(a, b, p) - loss(a, b, m)) / (2 * eps)
+        assert abs(fd - gh0[idx]) <= 1e-7 * (1 + abs(fd)), ("grad_h0", idx, fd, gh0[idx])
+
+
+def pin_state_symbolic_small_T(o):
+    """T <= 3 with a symbolic initial state and every reset pattern: expand,
+    differentiate, evaluate."""
+    import sympy as sp
+    import itertools
+    r = _rng(38)
+    for T in (1, 2, 3):
+        av, bv, gv = sp.symbols(f"a0:{T}"), sp.symbols(f"b0:{T}"), sp.symbols(f"g0:{T}")
+        h0s, gls = sp.symbols("h0 gl")
+        for pattern in itertools.product((0, 1), repeat=T):
+            h, hs = h0s, []
+            for t in range(T):
+                h = (0 if pattern[t] else av[t]) * h + bv[t]
+                hs.append(sp.expand(h))
+            loss = sum(gv[t] * hs[t] for t in range(T)) + gls * hs[-1]
+            a = r.uniform(-1.2, 1.2, (1, T, 1))
+            b = r.standard_normal((1, T, 1))
+            g = r.standard_normal((1, T, 1))
+            h0 = r.standard_normal((1, 1))
+            gl = r.standard_normal((1, 1))
+            seg = np.array([[0 if p else 7 for p in pattern]], dtype=np.int32)
+            subs = {**{av[t]: a[0, t, 0] for t in range(T)}, **{bv[t]: b[0, t, 0] for t in range(T)},
+                    **{gv[t]: g[0, t, 0] for t in range(T)}, h0s: h0[0, 0], gls: gl[0, 0]}
+            out, _ = o.fwd_state(a, b, "f64", h0=h0, segment_pos=seg)
+            ga, gb, gh0 = o.bwd_state(a, out, g, "f64", h0=h0, segment_pos=seg, grad_last=gl)
+            close = lambda x, y: abs(x - y) <= 1e-12 * (1 + abs(x))  # noqa: E731
+            for t in range(T):
+                assert close(float(hs[t].subs(subs)), out[0, t, 0]), ("h", T, pattern, t)
+                assert close(float(sp.diff(loss, av[t]).subs(subs)), ga[0, t, 0]), ("grad_a", T, pattern, t)
+                assert close(float(sp.diff(loss, bv[t]).subs(subs)), gb[0, t, 0]), ("grad_b", T, pattern, t)
+            assert close(float(sp.diff(loss, h0s).subs(subs)), gh0[0, 0]), ("grad_h0", T, pattern)
+
+
+def pin_state_empty_sequence(o):
+    """T == 0: the final state is h0 and the initial-state gradient is grad_last."""
+    a = np.zeros((2, 0, 3))
+    h0 = np.arange(6.0).reshape(2, 3)
+    gl = -np.arange(6.0).reshape(2, 3)
+    _, last = o.fwd_state(a, a, "f64", h0=h0)
+    assert np.array_equal(last, h0)
+    _, _, gh0 = o.bwd_state(a, a, a, "f64", h0=h0, grad_last=gl)
+    assert np.array_equal(gh0, gl)
+    _, _, gh0 = o.bwd_state(a, a, a, "f64")
+    assert not np.any(gh0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -35,6 +35,18 @@ MUTANTS = {
                                "state = FMA(P[c], state, Q[c]);                                \\\n"
                                "                hin[c] = state;"),
     "chunk_reverse_summary_drops_direct": ("k = a[i] * k + a[i] * grad_out[i];", "k = a[i] * k;"),
+    "state_fwd_ignores_h0": ("STATE h = h0 ? h0[bb * D + d] : 0;", "STATE h = 0;"),
+    "state_fwd_ignores_resets": ("STATE x = resets(seg, bb, T, t) ? 0 : LOAD(a[i]);", "STATE x = LOAD(a[i]);"),
+    "state_bwd_reset_on_wrong_step": ("(resets(seg, bb, T, t + 1) ? 0 : LOAD(a[i + D]))",
+                                      "(resets(seg, bb, T, t) ? 0 : LOAD(a[i + D]))"),
+    "state_bwd_drops_grad_last": ("STATE g = grad_last ? grad_last[bb * D + d] : 0;", "STATE g = 0;"),
+    "state_bwd_prev_ignores_h0": (": (h0 ? h0[bb * D + d] : 0);", ": 0;"),
+    "state_grad_h0_drops_decay": ("? 0 : LOAD(a[bb * T * D + d]) * g;", "? 0 : g;"),
+    "state_grad_a_not_masked": ("grad_a[i] = resets(seg, bb, T, t) ? STORE(0) : STORE(g * h_prev);",
+                                "grad_a[i] = STORE(g * h_prev);"),
+    "state_grad_h0_ignores_first_reset": ("grad_h0[bb * D + d] = resets(seg, bb, T, 0)",
+                                          "grad_h0[bb * D + d] = 0"),
+    "state_empty_grad_h0_zero": ("grad_h0[bb * D + d] = g;", "grad_h0[bb * D + d] = 0;"),
 }
 
 
