@@ -126,6 +126,52 @@ int lrscan_bwd_ex(const void *a, const void *out, const void *grad_out,
                   int64_t B, int64_t T, int64_t D, int dtype,
                   void *stream, const lrscan_opts *opts);
 
+/*
+ * Carried state and segment resets.  The state-carrying serial scans of
+ * triton_training_scan.py (_samu_tiled_serial_forward and
+ * _samu_tiled_serial_backward: initial state, per-token segment positions,
+ * gradient at the final state, gradient of the initial state) applied to this
+ * scan; with it a sequence split across calls (prefill, then decode, as the
+ * state-carrying recurrences of the KDN page's recurrence.py do) continues
+ * exactly, and packed sequences restart at their first token.
+ *
+ *   forward   h_{-1} = h0;  a'_t = 0 where segment_pos[b,t] == 0, else a_t;
+ *             h_t = a'_t * h_{t-1} + b_t;  last = h_{T-1}
+ *   backward  with L = sum_t grad_out_t * h_t + sum grad_last * last:
+ *             g_T = grad_last, entering step T-1 through a'_T = 1,
+ *             g_t = grad_out_t + a'_{t+1} * g_{t+1}   (one rounding),
+ *             grad_b_t = g_t,
+ *             grad_a_t = +0 where step t starts a segment (a_t is unused
+ *                        there), else g_t * out_{t-1} with out_{-1} = h0,
+ *             grad_h0  = a'_0 * g_0   (grad_last when T == 0).
+ *
+ * Every member may be NULL (zeros / no resets / not written); the forward
+ * reads only h0 and segment_pos.  h0, grad_last and grad_h0 are fp32 [B, D]
+ * whatever the storage dtype (the state precision: `last` of one call can be
+ * the next call's h0); segment_pos is int32 [B, T], one position per token,
+ * shared by all D channels.  All are caller-owned device pointers, 4-byte
+ * aligned (else LRSCAN_EINVAL); grad_h0 must not overlap any input.
+ */
+typedef struct lrscan_state {
+    const float *h0;            /* [B, D] fp32: state before step 0 */
+    const int32_t *segment_pos; /* [B, T] int32: 0 marks the first step of a segment */
+    const float *grad_last;     /* backward: [B, D] fp32 gradient arriving at `last` */
+    float *grad_h0;             /* backward: [B, D] fp32 output, gradient of h0 */
+} lrscan_state;
+
+/* lrscan_fwd_ex / lrscan_bwd_ex with carried state (state NULL: the plain
+ * scan).  Same paths, options, streams and errors; with T == 0 the forward
+ * copies h0 (or zeros) into last and the backward grad_last (or zeros) into
+ * grad_h0. */
+int lrscan_fwd_state(const void *a, const void *b, void *out, float *last,
+                     const lrscan_state *state,
+                     int64_t B, int64_t T, int64_t D, int dtype,
+                     void *stream, const lrscan_opts *opts);
+int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
+                     void *grad_a, void *grad_b, const lrscan_state *state,
+                     int64_t B, int64_t T, int64_t D, int dtype,
+                     void *stream, const lrscan_opts *opts);
+
 /* Sets the calling thread's stream (a cudaStream_t; NULL = legacy default
  * stream) used by lrscan_fwd / lrscan_bwd and by _ex calls given NULL. */
 int lrscan_set_stream(void *stream);

@@ -3,6 +3,9 @@
     h_t = a_t * h_{t-1} + b_t          (forward, h_{-1} = 0)
     g_t = grad_out_t + a_{t+1} g_{t+1} (backward; grad_b = g, grad_a = g * h_{t-1})
 
+and its state-carrying form (initial state h0, segment resets, gradients of
+the final and initial states: ``scan_state``).
+
 The compute path is liblrscan.so (hand-written sm_103a CUDA kernels behind a C
 ABI, ``include/lrscan.h``); ``lrscan`` is its Python binding.  Importing this
 package does not load the library; the first call does, and fails loudly if
@@ -10,10 +13,13 @@ it has not been built.
 """
 from .lrscan import (  # noqa: F401
     LinearRecurrenceScan,
+    LinearRecurrenceScanState,
     LrscanError,
     LrscanUnavailable,
     lrscan_bwd,
+    lrscan_bwd_state,
     lrscan_fwd,
+    lrscan_fwd_state,
     lrscan_num_variants,
     lrscan_plan,
     lrscan_selftest_wait_timeout,
@@ -21,4 +27,5 @@ from .lrscan import (  # noqa: F401
     lrscan_sync_check,
     lrscan_workspace_bytes,
     scan,
+    scan_state,
 )

@@ -22,11 +22,34 @@
 // padding it with identity steps (a=1, b=0).
 //
 // P and Q are fp32 [B, Nc, D] in a caller- or library-owned workspace.
+//
+// Carried state and segment resets (StateArgs, every pointer may be null):
+// the forward prefix starts from h0 and a_t is zeroed where segment_pos is 0;
+// the backward prefix starts from grad_last, which enters step T-1 through
+// a'_T = 1; a'_{t+1} is zeroed where step t+1 starts a segment, grad_a is +0
+// where step t does, h_{-1} = h0 and chunk 0 writes grad_h0 = a'_0 * g_0.
 #pragma once
 
 #include "scan_common.cuh"
+#include "state_args.h"
 
 namespace lrscan {
+
+// Segment start flag of step t of batch row `brow` (false without positions).
+__device__ __forceinline__ bool seg_reset(const StateArgs &sx, int brow, int T, int t) {
+    return sx.seg != nullptr && __ldg(sx.seg + static_cast<size_t>(brow) * T + t) == 0;
+}
+
+// a'_t: the decay of step t, zero where step t starts a segment.
+template <typename St, int V>
+__device__ __forceinline__ void load_decay(const St *p, const StateArgs &sx, int brow, int T, int t,
+                                           float (&x)[V]) {
+    load_lanes_global<St, V>(p, x);
+    if (seg_reset(sx, brow, T, t)) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) x[v] = 0.0f;
+    }
+}
 
 struct ChunkGeom {
     int T, D, Nc, nlb;  // nlb: lane blocks per (row, chunk)
@@ -51,7 +74,7 @@ __device__ __forceinline__ void store_f32_lanes(float *p, const float (&x)[V]) {
 template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__restrict__ P,
-                  float *__restrict__ Q, ChunkGeom g) {
+                  float *__restrict__ Q, ChunkGeom g, const StateArgs sx) {
     int brow, c, lb;
     chunk_coords(g, brow, c, lb);
     const int d = (lb * 128 + threadIdx.x) * V;
@@ -66,7 +89,7 @@ chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__r
 #pragma unroll 16
         for (int j = 0; j < C; ++j) {
             float x[V], y[V];
-            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_decay<St, V>(a + base + static_cast<size_t>(j) * g.D, sx, brow, g.T, t0 + j, x);
             load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
 #pragma unroll
             for (int v = 0; v < V; ++v) { p[v] = __fmul_rn(x[v], p[v]); q[v] = __fmaf_rn(x[v], q[v], y[v]); }
@@ -74,7 +97,7 @@ chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__r
     } else {
         for (int j = 0; j < n; ++j) {
             float x[V], y[V];
-            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_decay<St, V>(a + base + static_cast<size_t>(j) * g.D, sx, brow, g.T, t0 + j, x);
             load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
 #pragma unroll
             for (int v = 0; v < V; ++v) { p[v] = __fmul_rn(x[v], p[v]); q[v] = __fmaf_rn(x[v], q[v], y[v]); }
@@ -88,7 +111,7 @@ chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__r
 template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, float *__restrict__ P,
-                  float *__restrict__ Q, ChunkGeom g) {
+                  float *__restrict__ Q, ChunkGeom g, const StateArgs sx) {
     int brow, c, lb;
     chunk_coords(g, brow, c, lb);
     const int d = (lb * 128 + threadIdx.x) * V;
@@ -99,17 +122,18 @@ chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, flo
     float p[V], q[V], x[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) { p[v] = 1.0f; q[v] = 0.0f; }
-    // a_{t+1} for the chunk's last step: first step of the next chunk, 0 past T
+    // a'_{t+1} for the chunk's last step: first step of the next chunk; past
+    // T, 1 when grad_last enters there, else 0
     if (t0 + n < g.T) {
-        load_lanes_global<St, V>(a + base + static_cast<size_t>(n) * g.D, x);
+        load_decay<St, V>(a + base + static_cast<size_t>(n) * g.D, sx, brow, g.T, t0 + n, x);
     } else {
 #pragma unroll
-        for (int v = 0; v < V; ++v) x[v] = 0.0f;
+        for (int v = 0; v < V; ++v) x[v] = sx.grad_last != nullptr ? 1.0f : 0.0f;
     }
     for (int j = n - 1; j >= 0; --j) {
         float y[V], xn[V];
         load_lanes_global<St, V>(grad_out + base + static_cast<size_t>(j) * g.D, y);
-        load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, xn);
+        load_decay<St, V>(a + base + static_cast<size_t>(j) * g.D, sx, brow, g.T, t0 + j, xn);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             p[v] = __fmul_rn(x[v], p[v]);
@@ -134,14 +158,16 @@ chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, flo
 // (a tree-shaped scan would otherwise round differently per lane).
 template <bool REVERSE, int UNROLL>
 __global__ void __launch_bounds__(256)
-chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, long long lanes) {
+chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, long long lanes,
+             const float *__restrict__ init) {
     const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= lanes) return;
     const long long brow = wid / D;
     const int d = static_cast<int>(wid - brow * D);
     const size_t base = static_cast<size_t>(brow) * Nc * D + d;
-    float carry = 0.0f;
+    // state entering the first processed chunk: h0 (forward) or grad_last (backward)
+    float carry = init != nullptr ? __ldg(init + wid) : 0.0f;
     for (int c0 = 0; c0 < Nc; c0 += 32 * UNROLL) {
         float p[UNROLL], q[UNROLL];
 #pragma unroll
@@ -193,7 +219,7 @@ chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, 
 template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_replay_fwd(const St *__restrict__ a, const St *__restrict__ b, const float *__restrict__ Hin,
-                 St *__restrict__ out, float *__restrict__ last, ChunkGeom g) {
+                 St *__restrict__ out, float *__restrict__ last, ChunkGeom g, const StateArgs sx) {
     int brow, c, lb;
     chunk_coords(g, brow, c, lb);
     const int d = (lb * 128 + threadIdx.x) * V;
@@ -211,7 +237,7 @@ chunk_replay_fwd(const St *__restrict__ a, const St *__restrict__ b, const float
 #pragma unroll 16
         for (int j = 0; j < C; ++j) {
             float x[V], y[V];
-            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_decay<St, V>(a + base + static_cast<size_t>(j) * g.D, sx, brow, g.T, t0 + j, x);
             load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
@@ -220,7 +246,7 @@ chunk_replay_fwd(const St *__restrict__ a, const St *__restrict__ b, const float
     } else {
         for (int j = 0; j < n; ++j) {
             float x[V], y[V];
-            load_lanes_global<St, V>(a + base + static_cast<size_t>(j) * g.D, x);
+            load_decay<St, V>(a + base + static_cast<size_t>(j) * g.D, sx, brow, g.T, t0 + j, x);
             load_lanes_global<St, V>(b + base + static_cast<size_t>(j) * g.D, y);
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
@@ -237,7 +263,7 @@ template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_replay_bwd(const St *__restrict__ a, const St *__restrict__ out, const St *__restrict__ grad_out,
                  const float *__restrict__ Gin, St *__restrict__ grad_a, St *__restrict__ grad_b,
-                 ChunkGeom g) {
+                 ChunkGeom g, const StateArgs sx) {
     int brow, c, lb;
     chunk_coords(g, brow, c, lb);
     const int d = (lb * 128 + threadIdx.x) * V;
@@ -252,30 +278,37 @@ chunk_replay_bwd(const St *__restrict__ a, const St *__restrict__ out, const St 
         for (int v = 0; v < V; ++v) gv[v] = __ldcg(gp + v);
     }
     if (t0 + n < g.T) {
-        load_lanes_global<St, V>(a + base + static_cast<size_t>(n) * g.D, x);
+        load_decay<St, V>(a + base + static_cast<size_t>(n) * g.D, sx, brow, g.T, t0 + n, x);
     } else {
 #pragma unroll
-        for (int v = 0; v < V; ++v) x[v] = 0.0f;
+        for (int v = 0; v < V; ++v) x[v] = sx.grad_last != nullptr ? 1.0f : 0.0f;
     }
     for (int j = n - 1; j >= 0; --j) {
         float y[V], hp[V], xn[V], ga[V];
         const size_t o = base + static_cast<size_t>(j) * g.D;
         load_lanes_global<St, V>(grad_out + o, y);
-        load_lanes_global<St, V>(a + o, xn);
+        load_decay<St, V>(a + o, sx, brow, g.T, t0 + j, xn);
         if (t0 + j > 0) {
             load_lanes_global<St, V>(out + o - g.D, hp);
         } else {
 #pragma unroll
-            for (int v = 0; v < V; ++v) hp[v] = 0.0f;
+            for (int v = 0; v < V; ++v)
+                hp[v] = sx.h0 != nullptr ? sx.h0[static_cast<size_t>(brow) * g.D + d + v] : 0.0f;
         }
+        const bool rz = seg_reset(sx, brow, g.T, t0 + j);  // a_t unused: grad_a = +0
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             gv[v] = __fmaf_rn(x[v], gv[v], y[v]);
-            ga[v] = __fmul_rn(gv[v], hp[v]);
+            ga[v] = rz ? 0.0f : __fmul_rn(gv[v], hp[v]);
             x[v] = xn[v];
         }
         store_lanes<St, V>(grad_b + o, gv);
         store_lanes<St, V>(grad_a + o, ga);
+    }
+    if (c == 0 && sx.grad_h0 != nullptr) {
+        // x holds a'_0
+#pragma unroll
+        for (int v = 0; v < V; ++v) sx.grad_h0[static_cast<size_t>(brow) * g.D + d + v] = __fmul_rn(x[v], gv[v]);
     }
 }
 
@@ -286,16 +319,16 @@ chunk_replay_bwd(const St *__restrict__ a, const St *__restrict__ out, const St 
 template <typename St>
 __global__ void __launch_bounds__(128)
 plain_fwd(const St *__restrict__ a, const St *__restrict__ b, St *__restrict__ out,
-          float *__restrict__ last, int T, int D, int nlb) {
+          float *__restrict__ last, int T, int D, int nlb, const StateArgs sx) {
     const int brow = blockIdx.x / nlb;
     const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
     if (d >= D) return;
     size_t i = static_cast<size_t>(brow) * T * D + d;
-    float h = 0.0f;
+    float h = sx.h0 != nullptr ? sx.h0[static_cast<size_t>(brow) * D + d] : 0.0f;
 #pragma unroll 8
     for (int t = 0; t < T; ++t) {
         float x[1], y[1];
-        load_lanes_global<St, 1>(a + i, x);
+        load_decay<St, 1>(a + i, sx, brow, T, t, x);
         load_lanes_global<St, 1>(b + i, y);
         h = __fmaf_rn(x[0], h, y[0]);
         const float hv[1] = {h};
@@ -308,25 +341,30 @@ plain_fwd(const St *__restrict__ a, const St *__restrict__ b, St *__restrict__ o
 template <typename St>
 __global__ void __launch_bounds__(128)
 plain_bwd(const St *__restrict__ a, const St *__restrict__ out, const St *__restrict__ grad_out,
-          St *__restrict__ grad_a, St *__restrict__ grad_b, int T, int D, int nlb) {
+          St *__restrict__ grad_a, St *__restrict__ grad_b, int T, int D, int nlb, const StateArgs sx) {
     const int brow = blockIdx.x / nlb;
     const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
     if (d >= D) return;
     const size_t row = static_cast<size_t>(brow) * T * D + d;
-    float g = 0.0f, x = 0.0f;
+    const size_t sd = static_cast<size_t>(brow) * D + d;
+    // g_T = grad_last enters step T-1 through a'_T = 1 (without it, a'_T = 0)
+    float g = sx.grad_last != nullptr ? sx.grad_last[sd] : 0.0f;
+    float x = sx.grad_last != nullptr ? 1.0f : 0.0f;
 #pragma unroll 8
     for (int t = T - 1; t >= 0; --t) {
         const size_t i = row + static_cast<size_t>(t) * D;
         float y[1], hp[1] = {0.0f}, xn[1];
         load_lanes_global<St, 1>(grad_out + i, y);
-        load_lanes_global<St, 1>(a + i, xn);
+        load_decay<St, 1>(a + i, sx, brow, T, t, xn);
         if (t > 0) load_lanes_global<St, 1>(out + i - D, hp);
+        else if (sx.h0 != nullptr) hp[0] = sx.h0[sd];
         g = __fmaf_rn(x, g, y[0]);
-        const float gb[1] = {g}, ga[1] = {__fmul_rn(g, hp[0])};
+        const float gb[1] = {g}, ga[1] = {seg_reset(sx, brow, T, t) ? 0.0f : __fmul_rn(g, hp[0])};
         store_lanes<St, 1>(grad_b + i, gb);
         store_lanes<St, 1>(grad_a + i, ga);
         x = xn[0];
     }
+    if (sx.grad_h0 != nullptr) sx.grad_h0[sd] = T > 0 ? __fmul_rn(x, g) : g;  // x holds a'_0
 }
 
 }  // namespace lrscan

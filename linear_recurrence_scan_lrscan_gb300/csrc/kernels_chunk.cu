@@ -20,13 +20,13 @@ int chunk_fwd_t(const ChunkLaunch &L) {
     g.nlb = static_cast<int>((L.D / V + 127) / 128);
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
-                                                          static_cast<const St *>(L.in1), L.P, L.Q, g);
+                                                          static_cast<const St *>(L.in1), L.P, L.Q, g, L.sx);
     const long long lanes = static_cast<long long>(L.B) * L.D;
     const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
-    chunk_prefix<false, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes);
+    chunk_prefix<false, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes, L.sx.h0);
     chunk_replay_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                          static_cast<const St *>(L.in1), L.Q,
-                                                         static_cast<St *>(L.out0), L.last, g);
+                                                         static_cast<St *>(L.out0), L.last, g, L.sx);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -39,13 +39,13 @@ int chunk_bwd_t(const ChunkLaunch &L) {
     g.nlb = static_cast<int>((L.D / V + 127) / 128);
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
-                                                          static_cast<const St *>(L.in2), L.P, L.Q, g);
+                                                          static_cast<const St *>(L.in2), L.P, L.Q, g, L.sx);
     const long long lanes = static_cast<long long>(L.B) * L.D;
     const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
-    chunk_prefix<true, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes);
+    chunk_prefix<true, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes, L.sx.grad_last);
     chunk_replay_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(
         static_cast<const St *>(L.in0), static_cast<const St *>(L.in1), static_cast<const St *>(L.in2), L.Q,
-        static_cast<St *>(L.out0), static_cast<St *>(L.out1), g);
+        static_cast<St *>(L.out0), static_cast<St *>(L.out1), g, L.sx);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -97,12 +97,12 @@ int plain_fwd_launch(const ChunkLaunch &L, int dtype) {
         plain_fwd<float><<<nb, 128, 0, L.stream>>>(static_cast<const float *>(L.in0),
                                                    static_cast<const float *>(L.in1),
                                                    static_cast<float *>(L.out0), L.last,
-                                                   static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+                                                   static_cast<int>(L.T), static_cast<int>(L.D), nlb, L.sx);
     else
         plain_fwd<bf16_t><<<nb, 128, 0, L.stream>>>(static_cast<const bf16_t *>(L.in0),
                                                     static_cast<const bf16_t *>(L.in1),
                                                     static_cast<bf16_t *>(L.out0), L.last,
-                                                    static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+                                                    static_cast<int>(L.T), static_cast<int>(L.D), nlb, L.sx);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -113,12 +113,12 @@ int plain_bwd_launch(const ChunkLaunch &L, int dtype) {
         plain_bwd<float><<<nb, 128, 0, L.stream>>>(
             static_cast<const float *>(L.in0), static_cast<const float *>(L.in1),
             static_cast<const float *>(L.in2), static_cast<float *>(L.out0), static_cast<float *>(L.out1),
-            static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+            static_cast<int>(L.T), static_cast<int>(L.D), nlb, L.sx);
     else
         plain_bwd<bf16_t><<<nb, 128, 0, L.stream>>>(
             static_cast<const bf16_t *>(L.in0), static_cast<const bf16_t *>(L.in1),
             static_cast<const bf16_t *>(L.in2), static_cast<bf16_t *>(L.out0), static_cast<bf16_t *>(L.out1),
-            static_cast<int>(L.T), static_cast<int>(L.D), nlb);
+            static_cast<int>(L.T), static_cast<int>(L.D), nlb, L.sx);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -9,6 +9,8 @@
 
 #include <mutex>
 
+#include "state_args.h"
+
 namespace lrscan {
 
 // Launches a kernel that may overlap the tail of the previous kernel in the
@@ -46,6 +48,7 @@ struct WinLaunch {
     uint64_t timeout_ns;
     cudaStream_t stream;
     int device;
+    StateArgs sx;  // carried state and resets (used by the EXT launchers only)
 };
 
 // One direction of a tile variant: compiled shape (DT, V, L) plus the
@@ -61,7 +64,8 @@ struct WinDirCfg {
     int threads;     // s*(dt/v) + 32
     int smem;        // dynamic shared memory bytes
     int stage_bytes;
-    int (*launch)(const WinLaunch &, const WinDirCfg &);
+    int (*launch)(const WinLaunch &, const WinDirCfg &);        // plain scan
+    int (*launch_state)(const WinLaunch &, const WinDirCfg &);  // with carried state / resets
 };
 
 struct WinVariant {
@@ -82,6 +86,7 @@ struct ChunkLaunch {
     int chunk;                    // 16, 32, 64
     int vec;                      // lanes per thread: 1, 2, 4 (f32) / 1, 2, 4, 8 (bf16)
     cudaStream_t stream;
+    StateArgs sx;                 // carried state and resets (all null: plain scan)
 };
 int chunk_fwd(const ChunkLaunch &L, int dtype);
 int chunk_bwd(const ChunkLaunch &L, int dtype);

@@ -411,17 +411,59 @@ int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opt
 
 cudaStream_t pick_stream(void *stream) { return stream ? static_cast<cudaStream_t>(stream) : t_stream; }
 
+// The state members a direction uses, checked: fp32 / int32 device pointers
+// must be 4-byte aligned.  *any is set when the call carries state.
+int check_state(const lrscan_state *s, bool bwd, bool *any) {
+    *any = false;
+    if (!s) return LRSCAN_OK;
+    const void *ps[4] = {s->h0, s->segment_pos, bwd ? s->grad_last : nullptr, bwd ? s->grad_h0 : nullptr};
+    for (const void *p : ps) {
+        if (!p) continue;
+        if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return fail(LRSCAN_EINVAL, "state pointer %p is not 4-byte aligned", p);
+        *any = true;
+    }
+    return LRSCAN_OK;
+}
+
+// Kernel view of the state for batch rows [b0, ...).
+StateArgs state_slice(const lrscan_state *s, bool bwd, const void *a, int64_t b0, int64_t T, int64_t D, size_t es) {
+    StateArgs x{};
+    if (!s) return x;
+    const size_t sd = static_cast<size_t>(b0) * D;
+    x.h0 = s->h0 ? s->h0 + sd : nullptr;
+    x.seg = s->segment_pos ? s->segment_pos + static_cast<size_t>(b0) * T : nullptr;
+    if (bwd) {
+        x.grad_last = s->grad_last ? s->grad_last + sd : nullptr;
+        x.grad_h0 = s->grad_h0 ? s->grad_h0 + sd : nullptr;
+        x.a = static_cast<const char *>(a) + static_cast<size_t>(b0) * T * D * es;
+    }
+    return x;
+}
+
+// T == 0: the final state is h0 (forward) and the initial-state gradient is
+// grad_last (backward); zeros without them.
+int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_t st) {
+    if (!dst) return LRSCAN_OK;
+    const size_t bytes = static_cast<size_t>(B) * D * 4;
+    const cudaError_t e = src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st)
+                              : cudaMemsetAsync(dst, 0, bytes, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LRSCAN_ECUDA, "T == 0 state copy: %s", cudaGetErrorString(e));
+    }
+    return LRSCAN_OK;
+}
+
 int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype,
-            void *stream, const lrscan_opts *opts) {
+            void *stream, const lrscan_opts *opts, const lrscan_state *state = nullptr) {
     t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
+    bool ext = false;
+    if ((rc = check_state(state, false, &ext))) return rc;
     if (B == 0 || D == 0) return LRSCAN_OK;
     cudaStream_t st = pick_stream(stream);
-    if (T == 0) {
-        if (last && cudaMemsetAsync(last, 0, static_cast<size_t>(B) * D * 4, st) != cudaSuccess) return LRSCAN_ECUDA;
-        return LRSCAN_OK;
-    }
+    if (T == 0) return copy_or_zero(last, ext ? state->h0 : nullptr, B, D, st);
     if (!a || !b || !out) return fail(LRSCAN_EINVAL, "NULL a, b or out");
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx))) return rc;
@@ -450,7 +492,8 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
             L.timeout_ns = g_timeout_ns.load();
             L.stream = st;
             L.device = dev;
-            if (v.launch(L, v))
+            L.sx = state_slice(ext ? state : nullptr, false, a, b0, T, D, es);
+            if ((ext ? v.launch_state : v.launch)(L, v))
                 return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
         }
         return LRSCAN_OK;
@@ -459,6 +502,7 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
     L.in0 = a; L.in1 = b; L.out0 = out; L.last = last;
     L.B = B; L.T = T; L.D = D;
     L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
+    L.sx = state_slice(ext ? state : nullptr, false, a, 0, T, D, es);
     if (ch.path == kPathPlain) return plain_fwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
     void *ws = nullptr;
     if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
@@ -469,13 +513,16 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
 }
 
 int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B, int64_t T,
-            int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+            int64_t D, int dtype, void *stream, const lrscan_opts *opts, const lrscan_state *state = nullptr) {
     t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
-    if (B == 0 || D == 0 || T == 0) return LRSCAN_OK;
-    if (!a || !out || !grad_out || !grad_a || !grad_b) return fail(LRSCAN_EINVAL, "NULL a, out, grad_out, grad_a or grad_b");
+    bool ext = false;
+    if ((rc = check_state(state, true, &ext))) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
     cudaStream_t st = pick_stream(stream);
+    if (T == 0) return ext ? copy_or_zero(state->grad_h0, state->grad_last, B, D, st) : LRSCAN_OK;
+    if (!a || !out || !grad_out || !grad_a || !grad_b) return fail(LRSCAN_EINVAL, "NULL a, out, grad_out, grad_a or grad_b");
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx))) return rc;
     int dev = 0;
@@ -505,7 +552,8 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
             L.timeout_ns = g_timeout_ns.load();
             L.stream = st;
             L.device = dev;
-            if (v.launch(L, v))
+            L.sx = state_slice(ext ? state : nullptr, true, a, b0, T, D, es);
+            if ((ext ? v.launch_state : v.launch)(L, v))
                 return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
         }
         return LRSCAN_OK;
@@ -514,6 +562,7 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
     L.in0 = a; L.in1 = out; L.in2 = grad_out; L.out0 = grad_a; L.out1 = grad_b;
     L.B = B; L.T = T; L.D = D;
     L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
+    L.sx = state_slice(ext ? state : nullptr, true, a, 0, T, D, es);
     if (ch.path == kPathPlain) return plain_bwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
     void *ws = nullptr;
     if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
@@ -551,6 +600,17 @@ int lrscan_fwd_ex(const void *a, const void *b, void *out, float *last, int64_t 
 int lrscan_bwd_ex(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b, int64_t B,
                   int64_t T, int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
     return run_bwd(a, out, grad_out, grad_a, grad_b, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_fwd_state(const void *a, const void *b, void *out, float *last, const lrscan_state *state, int64_t B,
+                     int64_t T, int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    return run_fwd(a, b, out, last, B, T, D, dtype, stream, opts, state);
+}
+
+int lrscan_bwd_state(const void *a, const void *out, const void *grad_out, void *grad_a, void *grad_b,
+                     const lrscan_state *state, int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+                     const lrscan_opts *opts) {
+    return run_bwd(a, out, grad_out, grad_a, grad_b, B, T, D, dtype, stream, opts, state);
 }
 
 int lrscan_set_stream(void *stream) {

@@ -32,9 +32,19 @@
 // as the forward one.
 //
 // S and the stage count are launch-time parameters; DT, V and L are compiled.
+//
+// EXT instantiations add the carried state and segment resets (StateArgs):
+// the forward starts from h0 and zeroes a_t where a segment starts; the
+// backward starts from grad_last (entering through a'_T = 1), zeroes
+// a'_{t+1} where step t+1 starts a segment, writes grad_a = +0 where step t
+// starts one, reads h0 as h_{-1} and writes grad_h0 = a'_0 * g_0.  Each warp
+// turns the segment positions of its rows into a bit mask with one ballot
+// per window (loaded one window ahead).  The plain instantiations are
+// unchanged.
 #pragma once
 
 #include "scan_common.cuh"
+#include "state_args.h"
 
 namespace lrscan {
 
@@ -184,6 +194,23 @@ __device__ __forceinline__ void win_producer(const WinSmem &sm, const CUtensorMa
     }
 }
 
+// Segment positions of one batch row: rows outside [0, T), and every row when
+// there is no position tensor, read as 1 (no reset).
+struct SegRow {
+    const int32_t *p;
+    int T;
+    __device__ __forceinline__ int32_t at(int t) const {
+        return (p != nullptr && t >= 0 && t < T) ? __ldg(p + t) : 1;
+    }
+};
+
+// Lane threads of the in-window prefix own lane index i of the [DT] scan
+// arrays, i.e. channel d0 + (i % G) * V + i / G.
+template <class C>
+__device__ __forceinline__ int lane_channel(int d0, int i) {
+    return d0 + (i % C::G) * C::V + i / C::G;
+}
+
 template <class C>
 __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S) {
     constexpr int DT = C::DT;
@@ -207,11 +234,11 @@ __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, 
 // ============================================================================
 // Forward
 // ============================================================================
-template <class C>
+template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                typename C::St *__restrict__ out, float *__restrict__ last, const __grid_constant__ WinGeom geom,
-               DevStatus *status, uint64_t timeout_ns) {
+               DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StateArgs sx) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -247,9 +274,37 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (lane scan, threads < DT)
     bool failed = false;
     int stage = 0, use = 0;
+    // EXT: this warp's rows start at window row wrow; bit j of rbits is a
+    // reset at row s*L + j of the current window
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
+    const int wrow = ((threadIdx.x & ~31u) / G) * L;
+    int32_t pos_next = 1;
+    if constexpr (EXT) {
+        static_assert((G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
+        if (sx.h0 != nullptr) {
+            const float *h0 = sx.h0 + static_cast<size_t>(brow) * D;
+            if (lane_ok) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) h[v] = h0[d + v];
+            }
+            if (!C::SEQ && static_cast<int>(threadIdx.x) < DT) {
+                const int ch = lane_channel<C>(d0, threadIdx.x);
+                const float c0 = ch < D ? h0[ch] : 0.0f;
+                if constexpr (C::PT) sm.sCarry<C>(0)[threadIdx.x] = c0;  // read after the first barrier
+                else carry = c0;
+            }
+        }
+        pos_next = seg.at(wrow + lane);
+    }
 
     for (int k = 0; k < sm.nwin; ++k) {
-        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        uint32_t rbits = 0;
+        if constexpr (EXT) {
+            rbits = __ballot_sync(0xffffffffu, pos_next == 0) >> (s * L - wrow);
+            pos_next = seg.at((k + 1) * sm.W + wrow + lane);
+        }
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if constexpr (EXT && C::SEQ) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
         const St *tb = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;
         if constexpr (C::SEQ) {
@@ -273,6 +328,10 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     float x[V], y[V];
                     widen_raw(ra[j], x);
                     widen_raw(rb[j], y);
+                    if constexpr (EXT) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) x[v] = ((rbits >> j) & 1u) ? 0.0f : x[v];
+                    }
 #pragma unroll
                     for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
                     if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
@@ -282,6 +341,10 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     float x[V], y[V];
                     unpack_lanes<St, V>(ta + j * DT, x);
                     unpack_lanes<St, V>(tb + j * DT, y);
+                    if constexpr (EXT) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) x[v] = ((rbits >> j) & 1u) ? 0.0f : x[v];
+                    }
 #pragma unroll
                     for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
                     if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
@@ -308,6 +371,15 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         float P[V], Q[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+        if constexpr (EXT) {
+            if (rbits != 0) {
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) xa[j][v] = ((rbits >> j) & 1u) ? 0.0f : xa[j][v];
+                }
+            }
+        }
         if (n < L) {
             // tail sub-chunk: steps past T become exact identity steps (a=1, b=0)
 #pragma unroll
@@ -403,10 +475,10 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // ============================================================================
 // Backward
 // ============================================================================
-template <class C>
+template <class C, bool EXT>
 __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const float (&xh)[C::L][C::V],
                                          const float (&xg)[C::L][C::V], float (&g)[C::V], int n, bool lane_ok,
-                                         typename C::St *gb, typename C::St *ga, int D) {
+                                         typename C::St *gb, typename C::St *ga, int D, uint32_t rbits) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L;
     // rows past T hold identity steps (a=1, grad_out=0), set by the caller: g
@@ -418,6 +490,7 @@ __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const fl
         for (int v = 0; v < V; ++v) {
             g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
             gav[v] = __fmul_rn(g[v], xh[j][v]);
+            if constexpr (EXT) gav[v] = ((rbits >> j) & 1u) ? 0.0f : gav[v];  // a_t unused at a reset
         }
         if (lane_ok && (n == L || j < n)) {
             store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
@@ -426,12 +499,25 @@ __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const fl
     }
 }
 
+// grad_h0 = a'_0 * g_0 for the V lanes of the thread that finished step 0.
 template <class C>
+__device__ __forceinline__ void store_grad_h0(const StateArgs &sx, const SegRow &seg, size_t row0, int brow, int d,
+                                              int D, const float (&g)[C::V]) {
+    using St = typename C::St;
+    float a0[C::V];
+    load_lanes_global<St, C::V>(static_cast<const St *>(sx.a) + row0 * D + d, a0);
+    const bool r0 = seg.at(0) == 0;
+#pragma unroll
+    for (int v = 0; v < C::V; ++v)
+        sx.grad_h0[static_cast<size_t>(brow) * D + d + v] = r0 ? 0.0f : __fmul_rn(a0[v], g[v]);
+}
+
+template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_out,
                const __grid_constant__ CUtensorMap tm_go, typename C::St *__restrict__ grad_a,
                typename C::St *__restrict__ grad_b, const __grid_constant__ WinGeom geom, DevStatus *status,
-               uint64_t timeout_ns) {
+               uint64_t timeout_ns, const __grid_constant__ StateArgs sx) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -470,15 +556,55 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     for (int v = 0; v < V; ++v) g[v] = 0.0f;
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (lane scan, threads < DT)
     int stage = 0, use = 0;
+    bool failed = false;
+    // EXT: bit j of r0bits / r1bits is a reset at row s*L + j / s*L + j + 1
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
+    const int wrow = ((threadIdx.x & ~31u) / G) * L;
+    int32_t pos0_next = 1, pos1_next = 1;
+    float h0v[V];  // h_{-1}
+#pragma unroll
+    for (int v = 0; v < V; ++v) h0v[v] = 0.0f;
+    if constexpr (EXT) {
+        static_assert((G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
+        if (sx.h0 != nullptr && lane_ok) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) h0v[v] = sx.h0[static_cast<size_t>(brow) * D + d + v];
+        }
+        if (sx.grad_last != nullptr) {
+            const float *gl = sx.grad_last + static_cast<size_t>(brow) * D;
+            if (lane_ok) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) g[v] = gl[d + v];
+            }
+            if (!C::SEQ && static_cast<int>(threadIdx.x) < DT) {
+                const int ch = lane_channel<C>(d0, threadIdx.x);
+                const float c0 = ch < D ? gl[ch] : 0.0f;
+                if constexpr (C::PT) sm.sCarry<C>(0)[threadIdx.x] = c0;  // read after the first barrier
+                else carry = c0;
+            }
+        }
+        const int wb0 = (nwin - 1) * sm.W + wrow + lane;
+        pos0_next = seg.at(wb0);
+        pos1_next = seg.at(wb0 + 1);
+    }
 
     for (int k = 0; k < nwin; ++k) {
-        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        uint32_t r0bits = 0, r1bits = 0;
+        if constexpr (EXT) {
+            r0bits = __ballot_sync(0xffffffffu, pos0_next == 0) >> (s * L - wrow);
+            r1bits = __ballot_sync(0xffffffffu, pos1_next == 0) >> (s * L - wrow);
+            const int wb = (nwin - 2 - k) * sm.W + wrow + lane;
+            pos0_next = seg.at(wb);
+            pos1_next = seg.at(wb + 1);
+        }
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if constexpr (EXT && C::SEQ) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
         const St *ta = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // a_{t+1}
         const St *th = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 2) + (s * L) * DT + lg * V;  // grad_out_t
         const int wbase = (nwin - 1 - k) * sm.W;
         if constexpr (C::SEQ) {
-            if (!ok) break;
+            if (!ok) { failed = true; break; }
             const int n = min(T - wbase, L);
             const size_t gofs = (row0 + wbase) * D + d;
             if (n == L) {
@@ -488,10 +614,20 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     unpack_lanes<St, V>(ta + j * DT, x);
                     unpack_lanes<St, V>(th + j * DT, hp);
                     unpack_lanes<St, V>(tg + j * DT, go);
+                    if constexpr (EXT) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            // row T-1 takes grad_last through a'_T = 1; a'_{t+1} = 0 at a reset
+                            if (j == L - 1) x[v] = k == 0 ? 1.0f : x[v];
+                            x[v] = ((r1bits >> j) & 1u) ? 0.0f : x[v];
+                            if (j == 0) hp[v] = wbase == 0 ? h0v[v] : hp[v];
+                        }
+                    }
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
                         g[v] = __fmaf_rn(x[v], g[v], go[v]);
                         gav[v] = __fmul_rn(g[v], hp[v]);
+                        if constexpr (EXT) gav[v] = ((r0bits >> j) & 1u) ? 0.0f : gav[v];
                     }
                     if (lane_ok) {
                         store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
@@ -504,10 +640,19 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     unpack_lanes<St, V>(ta + j * DT, x);
                     unpack_lanes<St, V>(th + j * DT, hp);
                     unpack_lanes<St, V>(tg + j * DT, go);
+                    if constexpr (EXT) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            if (j == n - 1) x[v] = 1.0f;  // row T-1 (this is the last window)
+                            x[v] = ((r1bits >> j) & 1u) ? 0.0f : x[v];
+                            if (j == 0 && wbase == 0) hp[v] = h0v[v];
+                        }
+                    }
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
                         g[v] = __fmaf_rn(x[v], g[v], go[v]);
                         gav[v] = __fmul_rn(g[v], hp[v]);
+                        if constexpr (EXT) gav[v] = ((r0bits >> j) & 1u) ? 0.0f : gav[v];
                     }
                     if (lane_ok) {
                         store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
@@ -538,13 +683,30 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         float P[V], Q[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
-        if (n < L) {
+        // rows from na on take a' = 1: steps past T (identity steps) and, with
+        // the carried state, step T-1 (grad_last enters through a'_T = 1)
+        int na = n;
+        if constexpr (EXT) {
+            if (n > 0 && rbase + n == T) na = n - 1;
+            if (r1bits != 0) {
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) xa[j][v] = ((r1bits >> j) & 1u) ? 0.0f : xa[j][v];
+                }
+            }
+            if (rbase == 0) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) xh[0][v] = h0v[v];
+            }
+        }
+        if (na < L) {
             // tail sub-chunk: steps past T become exact identity steps (a=1, grad_out=0)
 #pragma unroll
             for (int j = 0; j < L; ++j) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    xa[j][v] = j < n ? xa[j][v] : 1.0f;
+                    xa[j][v] = j < na ? xa[j][v] : 1.0f;
                     xg[j][v] = j < n ? xg[j][v] : 0.0f;
                 }
             }
@@ -561,7 +723,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         float2 *pq = sm.sPQ<C>(par);
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
-        if (bar_sync_or(1, NT, !ok)) break;
+        if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
         if constexpr (!C::PT) {
             // lane threads push the carried adjoint through sub-chunks S-1 .. 0
             float *entry = sm.sEntry<C>();
@@ -593,14 +755,21 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         const size_t gofs = (row0 + rbase) * D + d;
-        bwd_rows<C>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D);
+        bwd_rows<C, EXT>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, r0bits);
         if (C::PT && s == 0) {
             float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
             for (int v = 0; v < V; ++v) nc[v * G + lg] = g[v];
         }
+        if constexpr (EXT) {
+            if (rbase == 0 && sx.grad_h0 != nullptr && lane_ok) store_grad_h0<C>(sx, seg, row0, brow, d, D, g);
+        }
         }
     }
+    if constexpr (EXT && C::SEQ) {
+        if (!failed && sx.grad_h0 != nullptr && lane_ok) store_grad_h0<C>(sx, seg, row0, brow, d, D, g);
+    }
+    (void)failed;
 }
 
 }  // namespace lrscan

@@ -69,12 +69,21 @@ class PlanInfo(ctypes.Structure):
         return d
 
 
+class State(ctypes.Structure):
+    _fields_ = [("h0", ctypes.c_void_p), ("segment_pos", ctypes.c_void_p), ("grad_last", ctypes.c_void_p),
+                ("grad_h0", ctypes.c_void_p)]
+
+
 EXPORTS = {
     "lrscan_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
     "lrscan_bwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
     "lrscan_fwd_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_bwd_ex": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)],
                       ctypes.c_int),
+    "lrscan_fwd_state": ([_P, _P, _P, _P, ctypes.POINTER(State), _I64, _I64, _I64, ctypes.c_int, _P,
+                          ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_bwd_state": ([_P, _P, _P, _P, _P, ctypes.POINTER(State), _I64, _I64, _I64, ctypes.c_int, _P,
+                          ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_set_stream": ([_P], ctypes.c_int),
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
@@ -224,6 +233,80 @@ def lrscan_bwd(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
     return grad_a, grad_b
 
 
+def _check_state_tensor(name, t, shape, dtype, device):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _state(a, h0=None, segment_pos=None, grad_last=None, grad_h0=None) -> State:
+    B, T, D = a.shape
+    st = State()
+    st.h0 = _check_state_tensor("h0", h0, (B, D), torch.float32, a.device)
+    st.segment_pos = _check_state_tensor("segment_pos", segment_pos, (B, T), torch.int32, a.device)
+    st.grad_last = _check_state_tensor("grad_last", grad_last, (B, D), torch.float32, a.device)
+    st.grad_h0 = _check_state_tensor("grad_h0", grad_h0, (B, D), torch.float32, a.device)
+    return st
+
+
+def lrscan_fwd_state(a: torch.Tensor, b: torch.Tensor, h0: torch.Tensor | None = None,
+                     segment_pos: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                     last: torch.Tensor | None = None, *, path=None, chunk_len=None, tile_variant=None,
+                     workspace=None, stream=None):
+    """Forward scan from the fp32 [B, D] state h0, restarting where the int32
+    [B, T] segment_pos is 0; returns (out, last)."""
+    if a.ndim != 3 or a.shape != b.shape:
+        raise ValueError("lrscan expects matching [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    if out is None:
+        out = torch.empty_like(b)
+    if last is None:
+        last = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    _check_tensors(a.shape, a.dtype, a.device, a=a, b=b, out=out, last=last)
+    st = _state(a, h0=h0, segment_pos=segment_pos)
+    with torch.cuda.device(a.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_fwd_state(a.data_ptr(), b.data_ptr(), out.data_ptr(), last.data_ptr(),
+                                    ctypes.byref(st), B, T, D, code, _stream_ptr(stream),
+                                    ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_fwd_state")
+    return out, last
+
+
+def lrscan_bwd_state(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
+                     h0: torch.Tensor | None = None, segment_pos: torch.Tensor | None = None,
+                     grad_last: torch.Tensor | None = None, grad_a: torch.Tensor | None = None,
+                     grad_b: torch.Tensor | None = None, grad_h0: torch.Tensor | None = None, *,
+                     path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
+    """Reverse scan of :func:`lrscan_fwd_state` for the loss
+    sum(grad_out * out) + sum(grad_last * last); returns (grad_a, grad_b, grad_h0)."""
+    if a.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    if grad_a is None:
+        grad_a = torch.empty_like(a)
+    if grad_b is None:
+        grad_b = torch.empty_like(a)
+    if grad_h0 is None:
+        grad_h0 = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    _check_tensors(a.shape, a.dtype, a.device, a=a, out=out, grad_out=grad_out, grad_a=grad_a,
+                   grad_b=grad_b)
+    st = _state(a, h0=h0, segment_pos=segment_pos, grad_last=grad_last, grad_h0=grad_h0)
+    with torch.cuda.device(a.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_bwd_state(a.data_ptr(), out.data_ptr(), grad_out.data_ptr(), grad_a.data_ptr(),
+                                    grad_b.data_ptr(), ctypes.byref(st), B, T, D, code, _stream_ptr(stream),
+                                    ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_bwd_state")
+    return grad_a, grad_b, grad_h0
+
+
 def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
                 aligned: bool = True, path=None, chunk_len=None, tile_variant=None) -> dict:
     """What the dispatcher would run for this call (host only; no launch)."""
@@ -284,3 +367,36 @@ class LinearRecurrenceScan(torch.autograd.Function):
 def scan(a: torch.Tensor, b: torch.Tensor, path=None, chunk_len=None) -> torch.Tensor:
     """Differentiable h_t = a_t*h_{t-1} + b_t over [B, T, D] (fp32 or bf16 storage)."""
     return LinearRecurrenceScan.apply(a, b, path, chunk_len)
+
+
+class LinearRecurrenceScanState(torch.autograd.Function):
+    """Autograd wrapper of the state-carrying scan: (out, last) = scan(a, b, h0,
+    segment_pos); gradients flow to a, b and h0 from both outputs."""
+
+    @staticmethod
+    def forward(ctx, a, b, h0, segment_pos, path=None, chunk_len=None):
+        a, b = a.contiguous(), b.contiguous()
+        h0c = h0.contiguous() if h0 is not None else None
+        seg = segment_pos.contiguous() if segment_pos is not None else None
+        out, last = lrscan_fwd_state(a, b, h0=h0c, segment_pos=seg, path=path, chunk_len=chunk_len)
+        ctx.save_for_backward(a, out, h0c, seg)
+        ctx.opts = (path, chunk_len)
+        ctx.mark_non_differentiable(*(() if seg is None else (seg,)))
+        return out, last
+
+    @staticmethod
+    def backward(ctx, grad_out, grad_last):
+        a, out, h0, seg = ctx.saved_tensors
+        path, chunk_len = ctx.opts
+        if grad_out is None:
+            grad_out = torch.zeros_like(out)
+        ga, gb, gh0 = lrscan_bwd_state(a, out, grad_out.contiguous(), h0=h0, segment_pos=seg,
+                                       grad_last=grad_last.contiguous() if grad_last is not None else None,
+                                       path=path, chunk_len=chunk_len)
+        return ga, gb, (gh0 if h0 is not None else None), None, None, None
+
+
+def scan_state(a: torch.Tensor, b: torch.Tensor, h0: torch.Tensor | None = None,
+               segment_pos: torch.Tensor | None = None, path=None, chunk_len=None):
+    """Differentiable state-carrying scan; returns (out, last) with last fp32 [B, D]."""
+    return LinearRecurrenceScanState.apply(a, b, h0, segment_pos, path, chunk_len)

@@ -141,3 +141,20 @@ def test_forced_paths_and_variants(lib):
     assert p["path"] == "chunk" and p["rows_per_window"] == 32
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(8, 1000, 512, "f32", "bwd", path="chunk", chunk_len=48)
+
+
+def test_state_entry_points_validate_before_any_launch(lib):
+    p = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails validation or is empty
+    bad = L.State(h0=0x1002)      # not 4-byte aligned
+    assert lib.lrscan_fwd_state(p, p, p, None, ctypes.byref(bad), 1, 8, 8, 0, None, None) == L.LRSCAN_EINVAL
+    assert lib.lrscan_bwd_state(p, p, p, p, p, ctypes.byref(L.State(grad_h0=0x1001)), 1, 8, 8, 0, None,
+                                None) == L.LRSCAN_EINVAL
+    # the forward reads neither grad_last nor grad_h0
+    fwd_only = L.State(grad_last=0x1003, grad_h0=0x1001)
+    assert lib.lrscan_fwd_state(p, p, p, None, ctypes.byref(fwd_only), 0, 8, 8, 0, None, None) == L.LRSCAN_OK
+    # empty batch or width: nothing to do, no device touched
+    ok = L.State(h0=0x1000, segment_pos=0x2000, grad_last=0x3000, grad_h0=0x4000)
+    for B, T, D in ((0, 8, 8), (2, 8, 0)):
+        assert lib.lrscan_fwd_state(p, p, p, None, ctypes.byref(ok), B, T, D, 1, None, None) == L.LRSCAN_OK
+        assert lib.lrscan_bwd_state(p, p, p, p, p, ctypes.byref(ok), B, T, D, 1, None, None) == L.LRSCAN_OK
+    assert lib.lrscan_fwd_state(p, p, p, None, None, 1, 8, 8, 5, None, None) == L.LRSCAN_EDTYPE
