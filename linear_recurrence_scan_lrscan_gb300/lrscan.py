@@ -282,9 +282,11 @@ def lrscan_bwd_state(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
                      h0: torch.Tensor | None = None, segment_pos: torch.Tensor | None = None,
                      grad_last: torch.Tensor | None = None, grad_a: torch.Tensor | None = None,
                      grad_b: torch.Tensor | None = None, grad_h0: torch.Tensor | None = None, *,
-                     path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
+                     want_grad_h0: bool = True, path=None, chunk_len=None, tile_variant=None, workspace=None,
+                     stream=None):
     """Reverse scan of :func:`lrscan_fwd_state` for the loss
-    sum(grad_out * out) + sum(grad_last * last); returns (grad_a, grad_b, grad_h0)."""
+    sum(grad_out * out) + sum(grad_last * last); returns (grad_a, grad_b, grad_h0)
+    (grad_h0 None when not wanted)."""
     if a.ndim != 3:
         raise ValueError("lrscan expects [B, T, D] tensors")
     code = _dtype_code(a)
@@ -293,7 +295,7 @@ def lrscan_bwd_state(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
         grad_a = torch.empty_like(a)
     if grad_b is None:
         grad_b = torch.empty_like(a)
-    if grad_h0 is None:
+    if grad_h0 is None and want_grad_h0:
         grad_h0 = torch.empty((B, D), device=a.device, dtype=torch.float32)
     _check_tensors(a.shape, a.dtype, a.device, a=a, out=out, grad_out=grad_out, grad_a=grad_a,
                    grad_b=grad_b)

@@ -91,7 +91,8 @@ def check_state_case(inp, path=None, use=("h0", "seg", "grad_last"), want_grad_h
     exb = exact_path(path, planb["path"])
     gh0 = torch.full((B, D), float("nan"), device="cuda") if want_grad_h0 else None
     ga, gb, gh0_out = L.lrscan_bwd_state(a.cuda(), from_np(ref_out, dt).cuda(), g.cuda(), h0=cu(h0),
-                                         segment_pos=cu(seg), grad_last=cu(gl), grad_h0=gh0, path=path, **kw)
+                                         segment_pos=cu(seg), grad_last=cu(gl), grad_h0=gh0,
+                                         want_grad_h0=want_grad_h0, path=path, **kw)
     assert L.lrscan_sync_check() == 0
     tagb = f"{planb['name']} {'+'.join(use)}"
     ga, gb = to_np(ga), to_np(gb)
