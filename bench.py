@@ -107,6 +107,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------- multi-rank job ----
+def max_over_ranks(values, dist, device) -> list[float]:
+    """Every rank's values replaced by the slowest rank's (element-wise max):
+    the job's step ends when its slowest rank's does."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world: int, units_per_rank: int, ms: float) -> float:
+    """Whole-job units per second: every rank processes its own units (weak
+    scaling, independent replicas) in the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------ reference ----
 def run_reference(args, w) -> dict:
     """The CPU oracle on the host cores: the reference arm of this benchmark."""
@@ -264,10 +282,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
-    if dist is not None:
-        t = torch.tensor([total_ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_ms, bwd_ms = t.tolist()
+    total_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms], dist, dev)
     ms_per_step = total_ms / args.steps
 
     # end to end: host (pinned) inputs -> device -> fwd+bwd -> host outputs
@@ -303,12 +318,9 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = t.item()
+        (e2e_ms,) = max_over_ranks([e2e_ms], dist, dev)
         s = w.storage_bytes
-        e2e = {"value": world * w.elements / (e2e_ms * 1e-3), "unit": "elements/s",
+        e2e = {"value": job_throughput(world, w.elements, e2e_ms), "unit": "elements/s",
                "h2d_bytes_per_step": 3 * w.elements * s,
                "d2h_bytes_per_step": 3 * w.elements * s + 4 * w.B * w.D,
                "ms_per_step": e2e_ms,
@@ -325,7 +337,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     traffic = load_traffic(w, dominant[0], pb["name"] if dominant[0] == "bwd" else pf["name"])
     line = {
         "metric": METRIC,
-        "value": world * w.elements / (ms_per_step * 1e-3),
+        "value": job_throughput(world, w.elements, ms_per_step),
         "unit": "elements/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -353,9 +365,80 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_extensions:
+        line["extensions"] = run_extensions(args, w, dev, sets, opts, peaks["hbm_gbs"])
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
+
+
+# ------------------------------------------------------------ extensions ----
+def time_launches(fn, iters: int, stream) -> float:
+    """Mean device time of one call of fn(i) over `iters` back-to-back calls
+    (after 3 untimed ones), CUDA events on the launching stream."""
+    import torch
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(iters):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def run_extensions(args, w, dev, sets, opts, peak) -> dict:
+    """The state-carrying scan on the same workload and buffer sets: initial
+    state h0, a segment start every 512 tokens on average, grad_last in and
+    grad_h0 out.  Each direction is timed over back-to-back launches rotating
+    the three buffer sets; GB/s counts the bytes the operation must move."""
+    import numpy as np
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    stream = torch.cuda.current_stream()
+    iters = max(10, min(args.steps, 200))
+    B, T, D, E, s = w.B, w.T, w.D, w.elements, w.storage_bytes
+    r = np.random.default_rng(7)
+    pos = np.zeros((B, T), dtype=np.int32)
+    starts = r.random((B, T)) < 1.0 / 512
+    for t in range(1, T):
+        pos[:, t] = np.where(starts[:, t], 0, pos[:, t - 1] + 1)
+    seg = torch.from_numpy(pos).to(dev)
+    h0 = torch.randn(B, D, device=dev)
+    gl = torch.randn(B, D, device=dev)
+    gh0 = torch.empty(B, D, device=dev)
+    n = len(sets)
+
+    def fwd(i):
+        f = sets[i % n]
+        L.lrscan_fwd_state(f["a"], f["b"], h0=h0, segment_pos=seg, out=f["out"], last=f["last"], **opts)
+
+    def bwd(i):
+        f = sets[i % n]
+        L.lrscan_bwd_state(f["a"], f["out"], f["g"], h0=h0, segment_pos=seg, grad_last=gl, grad_a=f["ga"],
+                           grad_b=f["gb"], grad_h0=gh0, **opts)
+    fms = time_launches(fwd, iters, stream)
+    bms = time_launches(bwd, iters, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the state-carrying scan")
+    fb = 3 * E * s + 4 * B * T + 2 * 4 * B * D
+    bb = 5 * E * s + 4 * B * T + 3 * 4 * B * D
+    for f in sets:   # leave every set with the plain forward's output
+        L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
+    torch.cuda.synchronize()
+    return {"state": {
+        "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
+                "grad_last in, grad_h0 out",
+        "launches_per_direction": iters,
+        "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                "algorithmic_bytes": fb},
+        "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                "algorithmic_bytes": bb},
+        "elements/s": 2 * E / ((fms + bms) * 1e-3)}}
 
 
 def kernel_source_hash() -> str:
@@ -396,6 +479,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extensions", action="store_true",
+                    help="skip the timing of the state-carrying scan")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=float, default=2e6)
     args = ap.parse_args()

@@ -172,6 +172,39 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
                      int64_t B, int64_t T, int64_t D, int dtype,
                      void *stream, const lrscan_opts *opts);
 
+/*
+ * Whole-sequence affine summary of every lane (the chunk summary of
+ * triton_training_scan.py, _real_chunk_summary and its reverse mirror, with
+ * one chunk spanning all T steps).  With a'_t = 0 where segment_pos[b,t] == 0
+ * (segment_pos may be NULL), P = prod_t a'_t and
+ *   dir 0 (forward):  x = b;         h_{T-1} = P * h0 + Q,       Q = h_{T-1} from h0 = 0
+ *   dir 1 (backward): x = grad_out;  grad_h0 = P * grad_last + Q, Q = grad_h0 from grad_last = 0
+ * P and Q are caller-owned fp32 [B, D] device outputs.  This is the local
+ * step of a sequence split across devices: each device summarizes its time
+ * segment, the maps are exchanged and composed in order, and each device
+ * then scans its segment with lrscan_fwd_state / lrscan_bwd_state from the
+ * composed h0 / grad_last.  T == 0 gives the identity map (P = 1, Q = 0).
+ * Reads a and x once (2 elements per (t, d)); one thread per lane.
+ */
+int lrscan_summary(const void *a, const void *x, float *P, float *Q,
+                   const int32_t *segment_pos, int64_t B, int64_t T, int64_t D,
+                   int dtype, int dir, void *stream);
+
+/*
+ * Composition of per-segment maps, the exchange step's arithmetic for a
+ * sequence split across devices (the serial prefix over chunk maps of
+ * triton_training_scan.py, _real_chunk_prefix, with one chunk per segment).
+ * maps: fp32 [W][2][B][D] device array, maps[r][0] = P_r and maps[r][1] = Q_r
+ * of segment r (lrscan_summary); init: fp32 [B, D] or NULL (zeros); out: fp32
+ * [B, D].  out = the fold of h -> fma(P_r, h, Q_r) over
+ *   dir 0: r = 0, 1, ..., rank-1   (state entering segment `rank`, init = h0)
+ *   dir 1: r = W-1, ..., rank+1    (adjoint entering segment `rank` from the
+ *                                   later ones, init = grad_last)
+ * applied to init.  0 <= rank < W.
+ */
+int lrscan_compose_maps(const float *maps, int64_t W, int64_t rank, const float *init,
+                        float *out, int64_t B, int64_t D, int dir, void *stream);
+
 /* Sets the calling thread's stream (a cudaStream_t; NULL = legacy default
  * stream) used by lrscan_fwd / lrscan_bwd and by _ex calls given NULL. */
 int lrscan_set_stream(void *stream);

@@ -1,5 +1,7 @@
 // Instantiations and launchers of the three-phase chunked kernels, the plain
 // sequential kernels and the bounded-wait self-test.
+#include <algorithm>
+
 #include "chunk_kernels.cuh"
 #include "launch.h"
 
@@ -64,6 +66,26 @@ int chunk_dispatch(const ChunkLaunch &L, bool fwd) {
     return -2;
 }
 
+// h = init (0 if null); then h = fma(P_r, h, Q_r) for r = r0, r0+step, ...
+// (n maps); maps is [W][2][n_lanes] fp32.
+__global__ void compose_maps_kernel(const float *__restrict__ maps, const float *__restrict__ init,
+                                    float *__restrict__ out, long long lanes, int r0, int step, int n) {
+    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (i >= lanes) return;
+    float h = init != nullptr ? init[i] : 0.0f;
+    for (int k = 0, r = r0; k < n; ++k, r += step) {
+        const float *m = maps + static_cast<size_t>(r) * 2 * lanes;
+        h = __fmaf_rn(m[i], h, m[lanes + i]);
+    }
+    out[i] = h;
+}
+
+__global__ void fill_f32_kernel(float *p, size_t n, float v) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
 __global__ void selftest_wait_kernel(DevStatus *status, uint64_t timeout_ns) {
     __shared__ __align__(8) unsigned long long bar;
     __shared__ int abort_flag;
@@ -119,6 +141,37 @@ int plain_bwd_launch(const ChunkLaunch &L, int dtype) {
             static_cast<const bf16_t *>(L.in0), static_cast<const bf16_t *>(L.in1),
             static_cast<const bf16_t *>(L.in2), static_cast<bf16_t *>(L.out0), static_cast<bf16_t *>(L.out1),
             static_cast<int>(L.T), static_cast<int>(L.D), nlb, L.sx);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int summary_launch(const ChunkLaunch &L, int dtype, int dir) {
+    const int nlb = static_cast<int>((L.D + 127) / 128);
+    const unsigned nb = static_cast<unsigned>(nlb * L.B);
+    const int T = static_cast<int>(L.T), D = static_cast<int>(L.D);
+    if (dtype == 0) {
+        auto fn = dir == 0 ? summary_fwd<float> : summary_bwd<float>;
+        fn<<<nb, 128, 0, L.stream>>>(static_cast<const float *>(L.in0), static_cast<const float *>(L.in1), L.P, L.Q,
+                                     T, D, nlb, L.sx);
+    } else {
+        auto fn = dir == 0 ? summary_fwd<bf16_t> : summary_bwd<bf16_t>;
+        fn<<<nb, 128, 0, L.stream>>>(static_cast<const bf16_t *>(L.in0), static_cast<const bf16_t *>(L.in1), L.P,
+                                     L.Q, T, D, nlb, L.sx);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int compose_maps_launch(const float *maps, const float *init, float *out, long long lanes, int r0, int step, int n,
+                        cudaStream_t stream) {
+    if (lanes == 0) return 0;
+    const unsigned nb = static_cast<unsigned>((lanes + 255) / 256);
+    compose_maps_kernel<<<nb, 256, 0, stream>>>(maps, init, out, lanes, r0, step, n);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int fill_f32_launch(float *p, size_t n, float v, cudaStream_t stream) {
+    if (n == 0) return 0;
+    const unsigned nb = static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 4096));
+    fill_f32_kernel<<<nb, 256, 0, stream>>>(p, n, v);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -92,6 +92,13 @@ int chunk_fwd(const ChunkLaunch &L, int dtype);
 int chunk_bwd(const ChunkLaunch &L, int dtype);
 int plain_fwd_launch(const ChunkLaunch &L, int dtype);
 int plain_bwd_launch(const ChunkLaunch &L, int dtype);
+// Whole-sequence affine summary per lane (dir 0: forward, 1: backward);
+// in0 = a, in1 = b or grad_out, P and Q = [B, D] outputs.
+int summary_launch(const ChunkLaunch &L, int dtype, int dir);
+int fill_f32_launch(float *p, size_t n, float v, cudaStream_t stream);
+// out = fold of h -> P_r*h + Q_r over n maps r = r0, r0+step, ... of maps [W][2][lanes].
+int compose_maps_launch(const float *maps, const float *init, float *out, long long lanes, int r0, int step, int n,
+                        cudaStream_t stream);
 int selftest_wait_launch(DevStatus *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Records the detail text lrscan_last_error() returns and passes code through.

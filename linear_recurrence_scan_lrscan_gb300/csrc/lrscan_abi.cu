@@ -613,6 +613,70 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out, void 
     return run_bwd(a, out, grad_out, grad_a, grad_b, B, T, D, dtype, stream, opts, state);
 }
 
+int lrscan_summary(const void *a, const void *x, float *P, float *Q, const int32_t *segment_pos, int64_t B,
+                   int64_t T, int64_t D, int dtype, int dir, void *stream) {
+    t_detail[0] = 0;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (dir != 0 && dir != 1) return fail(LRSCAN_EINVAL, "dir %d is not 0 (forward) or 1 (backward)", dir);
+    lrscan_state st{};
+    st.segment_pos = segment_pos;
+    bool ext = false;
+    if ((rc = check_state(&st, false, &ext))) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
+    if (!P || !Q) return fail(LRSCAN_EINVAL, "NULL P or Q");
+    if (reinterpret_cast<uintptr_t>(P) % 4 || reinterpret_cast<uintptr_t>(Q) % 4)
+        return fail(LRSCAN_EINVAL, "P and Q must be 4-byte aligned");
+    cudaStream_t s = pick_stream(stream);
+    if (T == 0) {
+        // the identity map h -> 1*h + 0
+        if (cudaMemsetAsync(Q, 0, static_cast<size_t>(B) * D * 4, s) != cudaSuccess ||
+            fill_f32_launch(P, static_cast<size_t>(B) * D, 1.0f, s)) {
+            cudaGetLastError();
+            return fail(LRSCAN_ECUDA, "T == 0 summary fill failed");
+        }
+        return LRSCAN_OK;
+    }
+    if (!a || !x) return fail(LRSCAN_EINVAL, "NULL a or x");
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    ChunkLaunch L{};
+    L.in0 = a; L.in1 = x; L.P = P; L.Q = Q;
+    L.B = B; L.T = T; L.D = D; L.stream = s;
+    L.sx = state_slice(&st, false, a, 0, T, D, esize(dtype));
+    if (summary_launch(L, dtype, dir))
+        return fail(LRSCAN_ECUDA, "summary launch: %s", cudaGetErrorString(cudaGetLastError()));
+    return LRSCAN_OK;
+}
+
+int lrscan_compose_maps(const float *maps, int64_t W, int64_t rank, const float *init, float *out, int64_t B,
+                        int64_t D, int dir, void *stream) {
+    t_detail[0] = 0;
+    if (W < 1 || rank < 0 || rank >= W || B < 0 || D < 0 || W > 0x7fffffffLL)
+        return fail(LRSCAN_EINVAL, "W=%lld rank=%lld B=%lld D=%lld", static_cast<long long>(W),
+                    static_cast<long long>(rank), static_cast<long long>(B), static_cast<long long>(D));
+    if (dir != 0 && dir != 1) return fail(LRSCAN_EINVAL, "dir %d is not 0 (forward) or 1 (backward)", dir);
+    int64_t lanes = 0, total = 0;
+    if (__builtin_mul_overflow(B, D, &lanes) || __builtin_mul_overflow(lanes, 2 * W, &total) ||
+        __builtin_mul_overflow(total, static_cast<int64_t>(4), &total))
+        return fail(LRSCAN_EINVAL, "W*2*B*D*4 overflows int64");
+    if (lanes == 0) return LRSCAN_OK;
+    if (!maps || !out) return fail(LRSCAN_EINVAL, "NULL maps or out");
+    for (const void *p : {static_cast<const void *>(maps), static_cast<const void *>(init),
+                          static_cast<const void *>(out)})
+        if (reinterpret_cast<uintptr_t>(p) % 4) return fail(LRSCAN_EINVAL, "pointers must be 4-byte aligned");
+    DeviceCtx *ctx = nullptr;
+    int rc = device_ctx(&ctx);
+    if (rc) return rc;
+    // forward: maps 0..rank-1 in order; backward: maps W-1..rank+1
+    const int r0 = dir == 0 ? 0 : static_cast<int>(W - 1);
+    const int step = dir == 0 ? 1 : -1;
+    const int n = dir == 0 ? static_cast<int>(rank) : static_cast<int>(W - 1 - rank);
+    if (compose_maps_launch(maps, init, out, lanes, r0, step, n, pick_stream(stream)))
+        return fail(LRSCAN_ECUDA, "compose launch: %s", cudaGetErrorString(cudaGetLastError()));
+    return LRSCAN_OK;
+}
+
 int lrscan_set_stream(void *stream) {
     t_stream = static_cast<cudaStream_t>(stream);
     return LRSCAN_OK;

@@ -84,6 +84,8 @@ EXPORTS = {
                           ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_bwd_state": ([_P, _P, _P, _P, _P, ctypes.POINTER(State), _I64, _I64, _I64, ctypes.c_int, _P,
                           ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_summary": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
+    "lrscan_compose_maps": ([_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
     "lrscan_set_stream": ([_P], ctypes.c_int),
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
@@ -307,6 +309,43 @@ def lrscan_bwd_state(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
                                     ctypes.byref(o) if o is not None else None)
     _check(rc, "lrscan_bwd_state")
     return grad_a, grad_b, grad_h0
+
+
+def lrscan_summary(a: torch.Tensor, x: torch.Tensor, segment_pos: torch.Tensor | None = None,
+                   direction: str = "fwd", stream=None):
+    """Per-lane affine map (P, Q), fp32 [B, D] each, of the whole sequence:
+    h_{T-1} = P*h0 + Q (direction "fwd", x = b) or grad_h0 = P*grad_last + Q
+    (direction "bwd", x = grad_out)."""
+    if a.ndim != 3 or a.shape != x.shape:
+        raise ValueError("lrscan expects matching [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    _check_tensors(a.shape, a.dtype, a.device, a=a, x=x)
+    seg = _check_state_tensor("segment_pos", segment_pos, (B, T), torch.int32, a.device)
+    P = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    Q = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    with torch.cuda.device(a.device):
+        rc = lib().lrscan_summary(a.data_ptr(), x.data_ptr(), P.data_ptr(), Q.data_ptr(), seg, B, T, D, code,
+                                  {"fwd": 0, "bwd": 1}[direction], _stream_ptr(stream))
+    _check(rc, "lrscan_summary")
+    return P, Q
+
+
+def lrscan_compose_maps(maps: torch.Tensor, rank: int, init: torch.Tensor | None = None,
+                        direction: str = "fwd", stream=None) -> torch.Tensor:
+    """Fold of the per-segment maps maps[r] = (P_r, Q_r) (fp32 [W, 2, B, D]) over
+    init: segments 0..rank-1 ("fwd") or W-1..rank+1 ("bwd"); returns [B, D]."""
+    if maps.ndim != 4 or maps.shape[1] != 2 or maps.dtype != torch.float32 or not maps.is_cuda:
+        raise ValueError("maps must be a CUDA fp32 [W, 2, B, D] tensor")
+    maps = maps.contiguous()
+    W, _, B, D = maps.shape
+    ip = _check_state_tensor("init", init, (B, D), torch.float32, maps.device)
+    out = torch.empty((B, D), device=maps.device, dtype=torch.float32)
+    with torch.cuda.device(maps.device):
+        rc = lib().lrscan_compose_maps(maps.data_ptr(), W, rank, ip, out.data_ptr(), B, D,
+                                       {"fwd": 0, "bwd": 1}[direction], _stream_ptr(stream))
+    _check(rc, "lrscan_compose_maps")
+    return out
 
 
 def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
