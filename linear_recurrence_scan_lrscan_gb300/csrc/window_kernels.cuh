@@ -323,19 +323,24 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     ra[j] = load_raw<St, V>(ta + j * DT);
                     rb[j] = load_raw<St, V>(tb + j * DT);
                 }
+                auto rows = [&](auto masked) {
 #pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    float x[V], y[V];
-                    widen_raw(ra[j], x);
-                    widen_raw(rb[j], y);
-                    if constexpr (EXT) {
+                    for (int j = 0; j < L; ++j) {
+                        float x[V], y[V];
+                        widen_raw(ra[j], x);
+                        widen_raw(rb[j], y);
+                        if constexpr (decltype(masked)::value) {
 #pragma unroll
-                        for (int v = 0; v < V; ++v) x[v] = ((rbits >> j) & 1u) ? 0.0f : x[v];
+                            for (int v = 0; v < V; ++v) x[v] = ((rbits >> j) & 1u) ? 0.0f : x[v];
+                        }
+#pragma unroll
+                        for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
+                        if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
                     }
-#pragma unroll
-                    for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(x[v], h[v], y[v]);
-                    if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
-                }
+                };
+                // a window without a segment start runs the plain loop (warp-uniform)
+                if (EXT && rbits != 0) rows(std::true_type{});
+                else rows(std::false_type{});
             } else {
                 for (int j = 0; j < n; ++j) {
                     float x[V], y[V];
@@ -475,7 +480,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // ============================================================================
 // Backward
 // ============================================================================
-template <class C, bool EXT>
+template <class C, bool MASK>
 __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const float (&xh)[C::L][C::V],
                                          const float (&xg)[C::L][C::V], float (&g)[C::V], int n, bool lane_ok,
                                          typename C::St *gb, typename C::St *ga, int D, uint32_t rbits) {
@@ -490,7 +495,7 @@ __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const fl
         for (int v = 0; v < V; ++v) {
             g[v] = __fmaf_rn(xa[j][v], g[v], xg[j][v]);
             gav[v] = __fmul_rn(g[v], xh[j][v]);
-            if constexpr (EXT) gav[v] = ((rbits >> j) & 1u) ? 0.0f : gav[v];  // a_t unused at a reset
+            if constexpr (MASK) gav[v] = ((rbits >> j) & 1u) ? 0.0f : gav[v];  // a_t unused at a reset
         }
         if (lane_ok && (n == L || j < n)) {
             store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
@@ -608,32 +613,38 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             const int n = min(T - wbase, L);
             const size_t gofs = (row0 + wbase) * D + d;
             if (n == L) {
+                auto rows = [&](auto special) {
 #pragma unroll
-                for (int j = L - 1; j >= 0; --j) {
-                    float x[V], hp[V], go[V], gav[V];
-                    unpack_lanes<St, V>(ta + j * DT, x);
-                    unpack_lanes<St, V>(th + j * DT, hp);
-                    unpack_lanes<St, V>(tg + j * DT, go);
-                    if constexpr (EXT) {
+                    for (int j = L - 1; j >= 0; --j) {
+                        float x[V], hp[V], go[V], gav[V];
+                        unpack_lanes<St, V>(ta + j * DT, x);
+                        unpack_lanes<St, V>(th + j * DT, hp);
+                        unpack_lanes<St, V>(tg + j * DT, go);
+                        if constexpr (decltype(special)::value) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                // row T-1 takes grad_last through a'_T = 1; a'_{t+1} = 0 at a reset
+                                if (j == L - 1) x[v] = k == 0 ? 1.0f : x[v];
+                                x[v] = ((r1bits >> j) & 1u) ? 0.0f : x[v];
+                                if (j == 0) hp[v] = wbase == 0 ? h0v[v] : hp[v];
+                            }
+                        }
 #pragma unroll
                         for (int v = 0; v < V; ++v) {
-                            // row T-1 takes grad_last through a'_T = 1; a'_{t+1} = 0 at a reset
-                            if (j == L - 1) x[v] = k == 0 ? 1.0f : x[v];
-                            x[v] = ((r1bits >> j) & 1u) ? 0.0f : x[v];
-                            if (j == 0) hp[v] = wbase == 0 ? h0v[v] : hp[v];
+                            g[v] = __fmaf_rn(x[v], g[v], go[v]);
+                            gav[v] = __fmul_rn(g[v], hp[v]);
+                            if constexpr (decltype(special)::value) gav[v] = ((r0bits >> j) & 1u) ? 0.0f : gav[v];
+                        }
+                        if (lane_ok) {
+                            store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
+                            store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, gav);
                         }
                     }
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        g[v] = __fmaf_rn(x[v], g[v], go[v]);
-                        gav[v] = __fmul_rn(g[v], hp[v]);
-                        if constexpr (EXT) gav[v] = ((r0bits >> j) & 1u) ? 0.0f : gav[v];
-                    }
-                    if (lane_ok) {
-                        store_lanes<St, V>(grad_b + gofs + static_cast<size_t>(j) * D, g);
-                        store_lanes<St, V>(grad_a + gofs + static_cast<size_t>(j) * D, gav);
-                    }
-                }
+                };
+                // only the sequence's two end windows and windows with a segment
+                // start need the state-carrying steps (warp-uniform)
+                if (EXT && ((r0bits | r1bits) != 0 || k == 0 || wbase == 0)) rows(std::true_type{});
+                else rows(std::false_type{});
             } else {
                 for (int j = n - 1; j >= 0; --j) {
                     float x[V], hp[V], go[V], gav[V];
@@ -755,7 +766,8 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         const size_t gofs = (row0 + rbase) * D + d;
-        bwd_rows<C, EXT>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, r0bits);
+        if (EXT && r0bits != 0) bwd_rows<C, true>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, r0bits);
+        else bwd_rows<C, false>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, 0u);
         if (C::PT && s == 0) {
             float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll

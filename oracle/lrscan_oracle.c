@@ -484,3 +484,123 @@ int lro_bwd_state_f64(const double *a, const double *out,
 {
     STATE_BWD_BODY(double, fma, LRO_SAME, LRO_SAME)
 }
+
+/* ---------------------------------------------------------------------- */
+/* Complex diagonal scan on separate real / imaginary planes.              */
+/*                                                                         */
+/* triton_training_scan.py, _complex_forward / _complex_backward and       */
+/* complex_scan_with_last: per lane, with complex a_t = ar + i*ai and      */
+/* b_t = br + i*bi,                                                        */
+/*   forward   h_{-1} = 0,  h_t = a_t * h_{t-1} + b_t;                      */
+/*             out_r/out_i = Re/Im h_t in the storage dtype, last_r/last_i  */
+/*             = Re/Im h_{T-1} in fp32                                      */
+/*   backward  loss L = sum_t Re(conj(grad_out_t) * h_t)                    */
+/*             = sum_t (go_r*h_r + go_i*h_i):                               */
+/*             g_{T-1} = grad_out_{T-1},                                    */
+/*             g_t = grad_out_t + conj(a_{t+1}) * g_{t+1}  (the adjoint     */
+/*                   carries the conjugate transition),                     */
+/*             grad_b_t = g_t,  grad_a_t = g_t * conj(h_{t-1})  (h_{-1} = 0) */
+/*             i.e. grad_ar = gr*pr + gi*pi, grad_ai = gi*pr - gr*pi.       */
+/* Rounding reading (the page leaves contraction to the compiler): each     */
+/* component is two nested fused multiply-adds,                             */
+/*   h_r = fma(ar, h_r, fma(-ai, h_i, br)),  h_i = fma(ai, h_r, fma(ar, h_i, bi)) */
+/*   g_r = fma(ar', g_r, fma(ai', g_i, go_r)), g_i = fma(ar', g_i, fma(-ai', g_r, go_i)) */
+/*   grad_ar = fma(gr, pr, gi*pi),  grad_ai = fma(gi, pr, -(gr*pi))         */
+/* (ar', ai' = a_{t+1}; the product inside is rounded once).               */
+/* ---------------------------------------------------------------------- */
+
+#define CPLX_FWD_BODY(STATE, FMA, LOAD, STORE)                                 \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE hr = 0, hi = 0;                                              \
+            for (int64_t t = 0; t < T; ++t) {                                  \
+                int64_t i = (bb * T + t) * D + d;                              \
+                STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);                      \
+                STATE nr = FMA(xr, hr, FMA(-xi, hi, LOAD(br[i])));             \
+                STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));              \
+                hr = nr;                                                       \
+                hi = ni;                                                       \
+                out_r[i] = STORE(hr);                                          \
+                out_i[i] = STORE(hi);                                          \
+            }                                                                  \
+            if (last_r) last_r[bb * D + d] = hr;                               \
+            if (last_i) last_i[bb * D + d] = hi;                               \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define CPLX_BWD_BODY(STATE, FMA, LOAD, STORE)                                 \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE gr = 0, gi = 0;                                              \
+            for (int64_t t = T - 1; t >= 0; --t) {                             \
+                int64_t i = (bb * T + t) * D + d;                              \
+                STATE yr = LOAD(go_r[i]), yi = LOAD(go_i[i]);                  \
+                if (t == T - 1) {                                              \
+                    gr = yr;                                                   \
+                    gi = yi;                                                   \
+                } else {                                                       \
+                    STATE xr = LOAD(ar[i + D]), xi = LOAD(ai[i + D]);          \
+                    STATE nr = FMA(xr, gr, FMA(xi, gi, yr));                   \
+                    STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));                  \
+                    gr = nr;                                                   \
+                    gi = ni;                                                   \
+                }                                                              \
+                STATE pr = (t > 0) ? LOAD(out_r[i - D]) : 0;                   \
+                STATE pi = (t > 0) ? LOAD(out_i[i - D]) : 0;                   \
+                grad_br[i] = STORE(gr);                                        \
+                grad_bi[i] = STORE(gi);                                        \
+                grad_ar[i] = STORE(FMA(gr, pr, gi * pi));                      \
+                grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));                   \
+            }                                                                  \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+int lro_cfwd_f32(const float *ar, const float *ai, const float *br,
+                 const float *bi, float *out_r, float *out_i, float *last_r,
+                 float *last_i, int64_t B, int64_t T, int64_t D)
+{
+    CPLX_FWD_BODY(float, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_cfwd_bf16(const uint16_t *ar, const uint16_t *ai, const uint16_t *br,
+                  const uint16_t *bi, uint16_t *out_r, uint16_t *out_i,
+                  float *last_r, float *last_i, int64_t B, int64_t T, int64_t D)
+{
+    CPLX_FWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_cfwd_f64(const double *ar, const double *ai, const double *br,
+                 const double *bi, double *out_r, double *out_i,
+                 double *last_r, double *last_i, int64_t B, int64_t T, int64_t D)
+{
+    CPLX_FWD_BODY(double, fma, LRO_SAME, LRO_SAME)
+}
+
+int lro_cbwd_f32(const float *ar, const float *ai, const float *out_r,
+                 const float *out_i, const float *go_r, const float *go_i,
+                 float *grad_ar, float *grad_ai, float *grad_br, float *grad_bi,
+                 int64_t B, int64_t T, int64_t D)
+{
+    CPLX_BWD_BODY(float, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_cbwd_bf16(const uint16_t *ar, const uint16_t *ai, const uint16_t *out_r,
+                  const uint16_t *out_i, const uint16_t *go_r,
+                  const uint16_t *go_i, uint16_t *grad_ar, uint16_t *grad_ai,
+                  uint16_t *grad_br, uint16_t *grad_bi, int64_t B, int64_t T,
+                  int64_t D)
+{
+    CPLX_BWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_cbwd_f64(const double *ar, const double *ai, const double *out_r,
+                 const double *out_i, const double *go_r, const double *go_i,
+                 double *grad_ar, double *grad_ai, double *grad_br,
+                 double *grad_bi, int64_t B, int64_t T, int64_t D)
+{
+    CPLX_BWD_BODY(double, fma, LRO_SAME, LRO_SAME)
+}

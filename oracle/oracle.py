@@ -71,6 +71,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lro_bwd_state_f32", "lro_bwd_state_bf16", "lro_bwd_state_f64"):
         getattr(lib, name).argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64]
         getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_cfwd_f32", "lro_cfwd_bf16", "lro_cfwd_f64"):
+        getattr(lib, name).argtypes = [_P] * 8 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_cbwd_f32", "lro_cbwd_bf16", "lro_cbwd_f64"):
+        getattr(lib, name).argtypes = [_P] * 10 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
     lib.lro_f32_to_bf16_array.argtypes = [_P, _P, _I64]
     lib.lro_bf16_to_f32_array.argtypes = [_P, _P, _I64]
     lib.lro_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -220,6 +226,33 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle state backward failed ({rc})")
         return ga, gb, gh0
+
+    def cfwd(self, ar, ai, br, bi, dtype="f32"):
+        """Complex forward scan on re/im planes; ``(out_r, out_i, last_r, last_i)``."""
+        xs = [_c(x, dtype) for x in (ar, ai, br, bi)]
+        if any(x.shape != xs[0].shape for x in xs):
+            raise ValueError("ar, ai, br, bi must have the same [B, T, D] shape")
+        B, T, D = xs[0].shape
+        out_r, out_i = np.empty_like(xs[0]), np.empty_like(xs[0])
+        last_r = np.empty((B, D), dtype=_LAST[dtype])
+        last_i = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_cfwd_{dtype}")(*[_ptr(x) for x in xs], _ptr(out_r), _ptr(out_i),
+                                                     _ptr(last_r), _ptr(last_i), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle complex forward failed ({rc})")
+        return out_r, out_i, last_r, last_i
+
+    def cbwd(self, ar, ai, out_r, out_i, go_r, go_i, dtype="f32"):
+        """Complex reverse scan; ``(grad_ar, grad_ai, grad_br, grad_bi)``."""
+        xs = [_c(x, dtype) for x in (ar, ai, out_r, out_i, go_r, go_i)]
+        if any(x.shape != xs[0].shape for x in xs):
+            raise ValueError("complex backward inputs must have the same [B, T, D] shape")
+        B, T, D = xs[0].shape
+        gs = [np.empty_like(xs[0]) for _ in range(4)]
+        rc = getattr(self.lib, f"lro_cbwd_{dtype}")(*[_ptr(x) for x in xs], *[_ptr(g) for g in gs], B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle complex backward failed ({rc})")
+        return tuple(gs)
 
     def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
         x = np.ascontiguousarray(x, dtype=np.float32)

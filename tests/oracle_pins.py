@@ -671,4 +671,168 @@ def pin_state_empty_sequence(o):
     assert not np.any(gh0)
 
 
+# ------------------------------------------------------- complex scan ----
+# Complex a, b on separate re/im planes; the backward's adjoint carries
+# conj(a_{t+1}) and grad_a = g * conj(h_{t-1}) (loss sum Re(conj(go) h)).
+
+def _ccase(seed, B, T, D, rho=(0.5, 0.999), dtype=np.float64):
+    r = _rng(seed)
+    rad = r.uniform(*rho, (B, T, D))
+    ang = r.uniform(-np.pi, np.pi, (B, T, D))
+    ar, ai = (rad * np.cos(ang)).astype(dtype), (rad * np.sin(ang)).astype(dtype)
+    br, bi, gr, gi = (r.standard_normal((B, T, D)).astype(dtype) for _ in range(4))
+    return ar, ai, br, bi, gr, gi
+
+
+def pin_complex_matches_numpy_complex(o):
+    """Forward against numpy complex128 arithmetic; backward against the
+    conjugate-transition adjoint evaluated in numpy complex128 (fp64)."""
+    ar, ai, br, bi, gr, gi = _ccase(40, 2, 70, 3)
+    out_r, out_i, last_r, last_i = o.cfwd(ar, ai, br, bi, "f64")
+    a, b, go = ar + 1j * ai, br + 1j * bi, gr + 1j * gi
+    h = np.zeros(a[:, 0].shape, complex)
+    hs = []
+    for t in range(a.shape[1]):
+        h = a[:, t] * h + b[:, t]
+        hs.append(h)
+    hs = np.stack(hs, 1)
+    np.testing.assert_allclose(out_r, hs.real, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out_i, hs.imag, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(last_r + 1j * last_i, hs[:, -1], rtol=1e-12, atol=1e-12)
+    g_ar, g_ai, g_br, g_bi = o.cbwd(ar, ai, out_r, out_i, gr, gi, "f64")
+    g = np.zeros_like(h)
+    gs = np.zeros_like(hs)
+    for t in range(a.shape[1] - 1, -1, -1):
+        g = go[:, t] + (np.conj(a[:, t + 1]) * g if t + 1 < a.shape[1] else 0)
+        gs[:, t] = g
+    prev = np.concatenate([np.zeros_like(hs[:, :1]), hs[:, :-1]], axis=1)
+    ga = gs * np.conj(prev)
+    np.testing.assert_allclose(g_br + 1j * g_bi, gs, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g_ar + 1j * g_ai, ga, rtol=1e-12, atol=1e-12)
+
+
+def pin_complex_constant_decay_geometric(o):
+    """a == c (complex), b == 1: h_t = (1 - c^{t+1}) / (1 - c)."""
+    T = 150
+    for c in (0.9 * np.exp(0.3j), 0.999 * np.exp(-2.0j), -0.5 + 0.5j):
+        ar = np.full((1, T, 1), c.real)
+        ai = np.full((1, T, 1), c.imag)
+        out_r, out_i, _, _ = o.cfwd(ar, ai, np.ones_like(ar), np.zeros_like(ar), "f64")
+        want = (1 - c ** (np.arange(T) + 1)) / (1 - c)
+        np.testing.assert_allclose(out_r[0, :, 0] + 1j * out_i[0, :, 0], want, rtol=1e-11, atol=1e-12)
+
+
+def pin_complex_exact_rational(o):
+    """Dyadic complex inputs: the fp64 forward and backward are exact, so they
+    equal the rational evaluation of the recurrences term by term."""
+    r = _rng(41)
+    B, T, D = 1, 6, 2
+    q = lambda n, s: r.integers(-n, n + 1, (B, T, D)) / s  # noqa: E731
+    ar, ai, br, bi, gr, gi = q(4, 8.0), q(4, 8.0), q(8, 4.0), q(8, 4.0), q(8, 4.0), q(8, 4.0)
+    out_r, out_i, _, _ = o.cfwd(ar, ai, br, bi, "f64")
+    g_ar, g_ai, g_br, g_bi = o.cbwd(ar, ai, out_r, out_i, gr, gi, "f64")
+    F = Fraction
+    for d in range(D):
+        A = [(F(ar[0, t, d]), F(ai[0, t, d])) for t in range(T)]
+        Bv = [(F(br[0, t, d]), F(bi[0, t, d])) for t in range(T)]
+        G = [(F(gr[0, t, d]), F(gi[0, t, d])) for t in range(T)]
+        mul = lambda x, y: (x[0] * y[0] - x[1] * y[1], x[0] * y[1] + x[1] * y[0])  # noqa: E731
+        conj = lambda x: (x[0], -x[1])  # noqa: E731
+        add = lambda x, y: (x[0] + y[0], x[1] + y[1])  # noqa: E731
+        H, h = [], (F(0), F(0))
+        for t in range(T):
+            h = add(mul(A[t], h), Bv[t])
+            H.append(h)
+        Gs, g = [None] * T, (F(0), F(0))
+        for t in range(T - 1, -1, -1):
+            g = add(G[t], mul(conj(A[t + 1]), g)) if t + 1 < T else G[t]
+            Gs[t] = g
+        for t in range(T):
+            assert (F(out_r[0, t, d]), F(out_i[0, t, d])) == H[t], ("h", t, d)
+            assert (F(g_br[0, t, d]), F(g_bi[0, t, d])) == Gs[t], ("grad_b", t, d)
+            prev = conj(H[t - 1]) if t > 0 else (F(0), F(0))
+            assert (F(g_ar[0, t, d]), F(g_ai[0, t, d])) == mul(Gs[t], prev), ("grad_a", t, d)
+
+
+def pin_complex_finite_difference_jacobian(o):
+    """Central differences of L = sum(go_r*h_r + go_i*h_i) against all four
+    gradient planes (fp64)."""
+    planes = list(_ccase(42, 1, 7, 2, rho=(0.4, 0.95)))
+    gr, gi = planes[4], planes[5]
+    out_r, out_i, _, _ = o.cfwd(*planes[:4], "f64")
+    grads = o.cbwd(planes[0], planes[1], out_r, out_i, gr, gi, "f64")
+    eps = 1e-6
+
+    def loss(ps):
+        hr, hi, _, _ = o.cfwd(*ps, "f64")
+        return float(np.sum(gr * hr + gi * hi))
+    for k in range(4):
+        for idx in np.ndindex(planes[0].shape):
+            p, m = [x.copy() for x in planes[:4]], [x.copy() for x in planes[:4]]
+            p[k][idx] += eps
+            m[k][idx] -= eps
+            fd = (loss(p) - loss(m)) / (2 * eps)
+            assert abs(fd - grads[k][idx]) <= 1e-7 * (1 + abs(fd)), (k, idx, fd, grads[k][idx])
+
+
+def pin_complex_reduces_to_real_scans(o):
+    """ai == 0: the real and imaginary planes are two independent real scans
+    with the same decays (bit for bit in fp32 forward and for grad_b), and
+    grad_ar is the sum of the two real grad_a."""
+    ar, _, br, bi, gr, gi = _ccase(43, 2, 40, 5, dtype=np.float32)
+    ar = np.abs(ar)
+    z = np.zeros_like(ar)
+    out_r, out_i, last_r, last_i = o.cfwd(ar, z, br, bi, "f32")
+    rr, lr = o.fwd(ar, br, "f32")
+    ri, li = o.fwd(ar, bi, "f32")
+    assert np.array_equal(out_r, rr) and np.array_equal(out_i, ri)
+    assert np.array_equal(last_r, lr) and np.array_equal(last_i, li)
+    g_ar, g_ai, g_br, g_bi = o.cbwd(ar, z, out_r, out_i, gr, gi, "f32")
+    gar, gbr = o.bwd(ar, rr, gr, "f32")
+    gai, gbi = o.bwd(ar, ri, gi, "f32")
+    assert np.array_equal(g_br, gbr) and np.array_equal(g_bi, gbi)
+    np.testing.assert_allclose(g_ar, gar.astype(np.float64) + gai, rtol=1e-6, atol=1e-6)
+    a64 = [x.astype(np.float64) for x in (ar, z, br, bi, gr, gi)]
+    o_r, o_i, _, _ = o.cfwd(*a64[:4], "f64")
+    _, g_ai64, _, _ = o.cbwd(a64[0], a64[1], o_r, o_i, a64[4], a64[5], "f64")
+    # grad_ai = g_i h_r - g_r h_i of the two real problems
+    _, gbr64 = o.bwd(a64[0], o_r, a64[4], "f64")
+    _, gbi64 = o.bwd(a64[0], o_i, a64[5], "f64")
+    pr = np.concatenate([np.zeros_like(o_r[:, :1]), o_r[:, :-1]], axis=1)
+    pi = np.concatenate([np.zeros_like(o_i[:, :1]), o_i[:, :-1]], axis=1)
+    np.testing.assert_allclose(g_ai64, gbi64 * pr - gbr64 * pi, rtol=1e-12, atol=1e-12)
+
+
+def pin_complex_bf16_storage_is_fp32_state(o):
+    """bf16 storage only rounds what is stored: the bf16 complex oracle equals
+    the fp32 one on widened inputs with its stores rounded to nearest even."""
+    planes = [o.f32_to_bf16(x) for x in _ccase(44, 2, 60, 8, dtype=np.float32)]
+    w = [o.bf16_to_f32(x) for x in planes]
+    r16 = o.cfwd(*planes[:4], "bf16")
+    r32 = o.cfwd(*w[:4], "f32")
+    for x16, x32 in zip(r16[:2], r32[:2]):
+        assert np.array_equal(x16, o.f32_to_bf16(x32))
+    assert np.array_equal(r16[2], r32[2]) and np.array_equal(r16[3], r32[3])
+    g16 = o.cbwd(planes[0], planes[1], r16[0], r16[1], planes[4], planes[5], "bf16")
+    g32 = o.cbwd(w[0], w[1], o.bf16_to_f32(r16[0]), o.bf16_to_f32(r16[1]), w[4], w[5], "f32")
+    for x16, x32 in zip(g16, g32):
+        assert np.array_equal(x16, o.f32_to_bf16(x32))
+
+
+def pin_complex_identity_padding(o):
+    """a = 1 + 0i, b = 0 after a row's valid length carries the state bit for bit."""
+    ar, ai, br, bi, gr, gi = _ccase(45, 3, 30, 4, dtype=np.float32)
+    L = [30, 11, 1]
+    for bb, n in enumerate(L):
+        ar[bb, n:], ai[bb, n:], br[bb, n:], bi[bb, n:] = 1.0, 0.0, 0.0, 0.0
+        gr[bb, n:], gi[bb, n:] = 0.0, 0.0
+    out_r, out_i, last_r, last_i = o.cfwd(ar, ai, br, bi, "f32")
+    g = o.cbwd(ar, ai, out_r, out_i, gr, gi, "f32")
+    for bb, n in enumerate(L):
+        assert (out_r[bb, n:] == out_r[bb, n - 1]).all() and (out_i[bb, n:] == out_i[bb, n - 1]).all()
+        assert np.array_equal(last_r[bb], out_r[bb, n - 1]) and np.array_equal(last_i[bb], out_i[bb, n - 1])
+        for x in g:
+            assert not np.any(x[bb, n:])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

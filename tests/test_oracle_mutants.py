@@ -47,6 +47,18 @@ MUTANTS = {
     "state_grad_h0_ignores_first_reset": ("grad_h0[bb * D + d] = resets(seg, bb, T, 0)",
                                           "grad_h0[bb * D + d] = 0"),
     "state_empty_grad_h0_zero": ("grad_h0[bb * D + d] = g;", "grad_h0[bb * D + d] = 0;"),
+    "complex_fwd_sign": ("STATE nr = FMA(xr, hr, FMA(-xi, hi, LOAD(br[i])));",
+                         "STATE nr = FMA(xr, hr, FMA(xi, hi, LOAD(br[i])));"),
+    "complex_fwd_swapped_parts": ("STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));",
+                                  "STATE ni = FMA(xi, hi, FMA(xr, hr, LOAD(bi[i])));"),
+    "complex_bwd_no_conjugate": ("STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));",
+                                 "STATE ni = FMA(xr, gi, FMA(xi, gr, yi));"),
+    "complex_bwd_uses_a_t": ("STATE xr = LOAD(ar[i + D]), xi = LOAD(ai[i + D]);",
+                             "STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);"),
+    "complex_grad_a_not_conjugated": ("grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));",
+                                      "grad_ai[i] = STORE(FMA(gi, pr, gr * pi));"),
+    "complex_grad_a_drops_cross_term": ("grad_ar[i] = STORE(FMA(gr, pr, gi * pi));",
+                                        "grad_ar[i] = STORE(gr * pr);"),
 }
 
 
