@@ -430,7 +430,7 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
     for f in sets:   # leave every set with the plain forward's output
         L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
     torch.cuda.synchronize()
-    return {"state": {
+    return {"complex": run_complex(iters, dev, peak), "state": {
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
         "launches_per_direction": iters,
@@ -439,6 +439,53 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
         "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
                 "algorithmic_bytes": bb},
         "elements/s": 2 * E / ((fms + bms) * 1e-3)}}
+
+
+def run_complex(iters: int, dev, peak) -> dict:
+    """The complex scan on its workload (re/im planes, the gated workload's
+    shape and decay magnitudes with random phases), three rotating buffer
+    sets; forward moves 6 elements per (t, d) (+ the fp32 final state),
+    backward 10."""
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    from linear_recurrence_scan_lrscan_gb300.workloads import COMPLEX_WORKLOAD as cw
+    from linear_recurrence_scan_lrscan_gb300.workloads import make_complex_inputs
+    stream = torch.cuda.current_stream()
+    host = make_complex_inputs()
+    sets = []
+    for _ in range(3):
+        st = {k: host[k].to(dev) for k in ("ar", "ai", "br", "bi", "go_r", "go_i")}
+        st["out"] = [torch.empty_like(st["ar"]) for _ in range(2)]
+        st["last"] = [torch.empty(cw.B, cw.D, device=dev) for _ in range(2)]
+        st["grads"] = [torch.empty_like(st["ar"]) for _ in range(4)]
+        sets.append(st)
+    del host
+
+    def fwd(i):
+        st = sets[i % 3]
+        L.lrscan_cfwd(st["ar"], st["ai"], st["br"], st["bi"], out_r=st["out"][0], out_i=st["out"][1],
+                      last_r=st["last"][0], last_i=st["last"][1])
+
+    def bwd(i):
+        st = sets[i % 3]
+        L.lrscan_cbwd(st["ar"], st["ai"], st["out"][0], st["out"][1], st["go_r"], st["go_i"], grads=st["grads"])
+    fms = time_launches(fwd, iters, stream)
+    bms = time_launches(bwd, iters, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the complex scan")
+    E, s = cw.elements, cw.storage_bytes
+    fb, bb = 6 * E * s + 8 * cw.B * cw.D, 10 * E * s
+    pf = L.lrscan_plan_complex(cw.B, cw.T, cw.D, cw.dtype, "fwd")
+    pb = L.lrscan_plan_complex(cw.B, cw.T, cw.D, cw.dtype, "bwd")
+    del sets
+    torch.cuda.empty_cache()
+    return {"workload": cw.describe() + " complex (re/im planes)", "launches_per_direction": iters,
+            "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                    "algorithmic_bytes": fb, "kernel": pf["name"]},
+            "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                    "algorithmic_bytes": bb, "kernel": pb["name"]},
+            "elements/s": 2 * E / ((fms + bms) * 1e-3)}
 
 
 def kernel_source_hash() -> str:
@@ -480,7 +527,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extensions", action="store_true",
-                    help="skip the timing of the state-carrying scan")
+                    help="skip the timing of the state-carrying and complex scans")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=float, default=2e6)
     args = ap.parse_args()

@@ -173,6 +173,41 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
                      void *stream, const lrscan_opts *opts);
 
 /*
+ * Complex diagonal scan on separate real / imaginary planes
+ * (triton_training_scan.py, _complex_forward / _complex_backward and
+ * complex_scan_with_last).  Per lane, with a_t = ar + i*ai, b_t = br + i*bi:
+ *
+ *   forward   h_{-1} = 0,  h_t = a_t * h_{t-1} + b_t
+ *             out_r / out_i = Re / Im h_t (storage dtype); last_r / last_i =
+ *             Re / Im h_{T-1} (fp32; either may be NULL)
+ *   backward  loss L = sum_t (grad_out_r * Re h_t + grad_out_i * Im h_t):
+ *             g_{T-1} = grad_out_{T-1},  g_t = grad_out_t + conj(a_{t+1}) * g_{t+1},
+ *             grad_b = g,  grad_a = g * conj(h_{t-1})  (h_{-1} = 0; h read from out)
+ *
+ * Each component is two nested fused multiply-adds:
+ *   Re h = fma(ar, Re h, fma(-ai, Im h, br)),  Im h = fma(ai, Re h, fma(ar, Im h, bi))
+ *   Re g = fma(ar', Re g, fma(ai', Im g, go_r)), Im g = fma(ar', Im g, fma(-ai', Re g, go_i))
+ *   grad_ar = fma(Re g, Re p, Im g * Im p),  grad_ai = fma(Im g, Re p, -(Re g * Im p))
+ * (a' = a_{t+1}, p = h_{t-1}); both paths use this order and agree bit for bit.
+ * All planes are caller-owned device [B, T, D] tensors of one storage dtype;
+ * paths: LRSCAN_PATH_SEQ (tiled, 16-byte aligned rows of every plane) or
+ * LRSCAN_PATH_PLAIN (any alignment); auto picks seq when it can.  Moves 6
+ * elements per (t, d) forward and 10 backward.  Other rules as lrscan_fwd_ex.
+ */
+int lrscan_cfwd(const void *ar, const void *ai, const void *br, const void *bi,
+                void *out_r, void *out_i, float *last_r, float *last_i,
+                int64_t B, int64_t T, int64_t D, int dtype,
+                void *stream, const lrscan_opts *opts);
+int lrscan_cbwd(const void *ar, const void *ai, const void *out_r, const void *out_i,
+                const void *grad_out_r, const void *grad_out_i,
+                void *grad_ar, void *grad_ai, void *grad_br, void *grad_bi,
+                int64_t B, int64_t T, int64_t D, int dtype,
+                void *stream, const lrscan_opts *opts);
+/* lrscan_plan for the complex scan (tile variants listed by tile_variant 1..) */
+int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
+                        const lrscan_opts *opts, lrscan_plan_info *info);
+
+/*
  * Whole-sequence affine summary of every lane (the chunk summary of
  * triton_training_scan.py, _real_chunk_summary and its reverse mirror, with
  * one chunk spanning all T steps).  With a'_t = 0 where segment_pos[b,t] == 0

@@ -3,8 +3,10 @@
     h_t = a_t * h_{t-1} + b_t          (forward, h_{-1} = 0)
     g_t = grad_out_t + a_{t+1} g_{t+1} (backward; grad_b = g, grad_a = g * h_{t-1})
 
-and its state-carrying form (initial state h0, segment resets, gradients of
-the final and initial states: ``scan_state``).
+its state-carrying form (initial state h0, segment resets, gradients of the
+final and initial states: ``scan_state``), the complex scan on re/im planes
+(``complex_scan``), and the pieces of a sequence split across devices
+(``lrscan_summary``, ``lrscan_compose_maps``, module ``tsplit``).
 
 The compute path is liblrscan.so (hand-written sm_103a CUDA kernels behind a C
 ABI, ``include/lrscan.h``); ``lrscan`` is its Python binding.  Importing this
@@ -12,18 +14,25 @@ package does not load the library; the first call does, and fails loudly if
 it has not been built.
 """
 from .lrscan import (  # noqa: F401
+    ComplexScan,
     LinearRecurrenceScan,
     LinearRecurrenceScanState,
     LrscanError,
     LrscanUnavailable,
+    complex_scan,
+    lrscan_cbwd,
+    lrscan_cfwd,
+    lrscan_compose_maps,
     lrscan_bwd,
     lrscan_bwd_state,
     lrscan_fwd,
     lrscan_fwd_state,
     lrscan_num_variants,
     lrscan_plan,
+    lrscan_plan_complex,
     lrscan_selftest_wait_timeout,
     lrscan_set_wait_timeout_ns,
+    lrscan_summary,
     lrscan_sync_check,
     lrscan_workspace_bytes,
     scan,

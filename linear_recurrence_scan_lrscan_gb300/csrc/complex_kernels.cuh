@@ -1,0 +1,274 @@
+// Complex diagonal scan on separate real / imaginary planes
+// (triton_training_scan.py, _complex_forward / _complex_backward):
+//
+//   forward   h_t = a_t * h_{t-1} + b_t               (complex, h_{-1} = 0)
+//   backward  g_t = go_t + conj(a_{t+1}) * g_{t+1},  grad_b = g,
+//             grad_a = g * conj(h_{t-1})
+//
+// with each component two nested fused multiply-adds (the oracle's order):
+//   h_r = fma(ar, h_r, fma(-ai, h_i, br)),   h_i = fma(ai, h_r, fma(ar, h_i, bi))
+//   g_r = fma(ar', g_r, fma(ai', g_i, go_r)), g_i = fma(ar', g_i, fma(-ai', g_r, go_i))
+//   grad_ar = fma(g_r, p_r, g_i*p_i),        grad_ai = fma(g_i, p_r, -(g_r*p_i))
+//
+// The tiled kernels are the sequential (S = 1) form of the time-tiled scan:
+// a producer warp streams NIN planes per window into the shared-memory stage
+// ring with bulk tensor copies (4 forward: ar, ai, br, bi; 6 backward: ar and
+// ai one row late, out_r and out_i one row early, go_r, go_i, so that the
+// copies' zero fill gives a_T = 0 and h_{-1} = 0), and every consumer thread
+// walks its V lanes through all windows in registers.
+#pragma once
+
+#include "window_kernels.cuh"
+
+namespace lrscan {
+
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
+                const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
+                typename C::St *__restrict__ out_r, typename C::St *__restrict__ out_i,
+                float *__restrict__ last_r, float *__restrict__ last_i, const __grid_constant__ WinGeom geom,
+                DevStatus *status, uint64_t timeout_ns) {
+    static_assert(C::SEQ && C::NIN == 4, "complex forward: sequential shape, four input planes");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int NT = G;
+    win_init<C>(sm, NT / 32, 1);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[4] = {&tm_ar, &tm_ai, &tm_br, &tm_bi};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
+        }
+        return;
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + threadIdx.x * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    float hr[V], hi[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) hr[v] = hi[v] = 0.0f;
+    bool failed = false;
+    int stage = 0, use = 0;
+    const int off = threadIdx.x * V;
+    for (int k = 0; k < sm.nwin; ++k) {
+        if (!mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull)) { failed = true; break; }
+        const St *tar = sm.tile<C>(stage, 0) + off;
+        const St *tai = sm.tile<C>(stage, 1) + off;
+        const St *tbr = sm.tile<C>(stage, 2) + off;
+        const St *tbi = sm.tile<C>(stage, 3) + off;
+        const int rbase = k * sm.W;
+        const int n = min(T - rbase, L);
+        const size_t o = (row0 + rbase) * D + d;
+        auto step = [&](int j) {
+            float xr[V], xi[V], yr[V], yi[V];
+            unpack_lanes<St, V>(tar + j * DT, xr);
+            unpack_lanes<St, V>(tai + j * DT, xi);
+            unpack_lanes<St, V>(tbr + j * DT, yr);
+            unpack_lanes<St, V>(tbi + j * DT, yi);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float nr = __fmaf_rn(xr[v], hr[v], __fmaf_rn(-xi[v], hi[v], yr[v]));
+                const float ni = __fmaf_rn(xi[v], hr[v], __fmaf_rn(xr[v], hi[v], yi[v]));
+                hr[v] = nr;
+                hi[v] = ni;
+            }
+            if (lane_ok) {
+                store_lanes<St, V>(out_r + o + static_cast<size_t>(j) * D, hr);
+                store_lanes<St, V>(out_i + o + static_cast<size_t>(j) * D, hi);
+            }
+        };
+        if (n == L) {
+#pragma unroll
+            for (int j = 0; j < L; ++j) step(j);
+        } else {
+            for (int j = 0; j < n; ++j) step(j);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+    }
+    if (!failed && lane_ok) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            if (last_r) last_r[static_cast<size_t>(brow) * D + d + v] = hr[v];
+            if (last_i) last_i[static_cast<size_t>(brow) * D + d + v] = hi[v];
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
+                const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
+                const __grid_constant__ CUtensorMap tm_gr, const __grid_constant__ CUtensorMap tm_gi,
+                typename C::St *__restrict__ grad_ar, typename C::St *__restrict__ grad_ai,
+                typename C::St *__restrict__ grad_br, typename C::St *__restrict__ grad_bi,
+                const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+    static_assert(C::SEQ && C::NIN == 6, "complex backward: sequential shape, six input planes");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int NT = G;
+    win_init<C>(sm, NT / 32, 1);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+    const int nwin = sm.nwin;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[6] = {&tm_ar, &tm_ai, &tm_or, &tm_oi, &tm_gr, &tm_gi};
+            const int W = sm.W;
+            // planes 0, 1: a one step later; 2, 3: out one step earlier; 4, 5: grad_out
+            win_producer<C>(sm, maps, d0, brow,
+                            [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i < 2 ? 1 : (i < 4 ? -1 : 0)); },
+                            wc);
+        }
+        return;
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + threadIdx.x * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    float gr[V], gi[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) gr[v] = gi[v] = 0.0f;
+    int stage = 0, use = 0;
+    const int off = threadIdx.x * V;
+    for (int k = 0; k < nwin; ++k) {
+        if (!mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull)) break;
+        const St *tar = sm.tile<C>(stage, 0) + off;  // a_{t+1}
+        const St *tai = sm.tile<C>(stage, 1) + off;
+        const St *tpr = sm.tile<C>(stage, 2) + off;  // h_{t-1}
+        const St *tpi = sm.tile<C>(stage, 3) + off;
+        const St *tgr = sm.tile<C>(stage, 4) + off;  // grad_out_t
+        const St *tgi = sm.tile<C>(stage, 5) + off;
+        const int wbase = (nwin - 1 - k) * sm.W;
+        const int n = min(T - wbase, L);
+        const size_t o = (row0 + wbase) * D + d;
+        auto step = [&](int j) {
+            float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V], far_[V], fai[V];
+            unpack_lanes<St, V>(tar + j * DT, xr);
+            unpack_lanes<St, V>(tai + j * DT, xi);
+            unpack_lanes<St, V>(tpr + j * DT, pr);
+            unpack_lanes<St, V>(tpi + j * DT, pi);
+            unpack_lanes<St, V>(tgr + j * DT, yr);
+            unpack_lanes<St, V>(tgi + j * DT, yi);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float nr = __fmaf_rn(xr[v], gr[v], __fmaf_rn(xi[v], gi[v], yr[v]));
+                const float ni = __fmaf_rn(xr[v], gi[v], __fmaf_rn(-xi[v], gr[v], yi[v]));
+                gr[v] = nr;
+                gi[v] = ni;
+                far_[v] = __fmaf_rn(gr[v], pr[v], __fmul_rn(gi[v], pi[v]));
+                fai[v] = __fmaf_rn(gi[v], pr[v], -__fmul_rn(gr[v], pi[v]));
+            }
+            if (lane_ok) {
+                const size_t oj = o + static_cast<size_t>(j) * D;
+                store_lanes<St, V>(grad_br + oj, gr);
+                store_lanes<St, V>(grad_bi + oj, gi);
+                store_lanes<St, V>(grad_ar + oj, far_);
+                store_lanes<St, V>(grad_ai + oj, fai);
+            }
+        };
+        if (n == L) {
+#pragma unroll
+            for (int j = L - 1; j >= 0; --j) step(j);
+        } else {
+            for (int j = n - 1; j >= 0; --j) step(j);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+    }
+}
+
+// Plain kernels: one lane per thread, plain loads, any alignment (same order
+// of operations, bit-identical to the tiled ones).
+template <typename St>
+__global__ void __launch_bounds__(128)
+cplain_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ br,
+           const St *__restrict__ bi, St *__restrict__ out_r, St *__restrict__ out_i, float *__restrict__ last_r,
+           float *__restrict__ last_i, int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    if (d >= D) return;
+    size_t i = static_cast<size_t>(brow) * T * D + d;
+    float hr = 0.0f, hi = 0.0f;
+#pragma unroll 4
+    for (int t = 0; t < T; ++t) {
+        float xr[1], xi[1], yr[1], yi[1];
+        load_lanes_global<St, 1>(ar + i, xr);
+        load_lanes_global<St, 1>(ai + i, xi);
+        load_lanes_global<St, 1>(br + i, yr);
+        load_lanes_global<St, 1>(bi + i, yi);
+        const float nr = __fmaf_rn(xr[0], hr, __fmaf_rn(-xi[0], hi, yr[0]));
+        const float ni = __fmaf_rn(xi[0], hr, __fmaf_rn(xr[0], hi, yi[0]));
+        hr = nr;
+        hi = ni;
+        const float vr[1] = {hr}, vi[1] = {hi};
+        store_lanes<St, 1>(out_r + i, vr);
+        store_lanes<St, 1>(out_i + i, vi);
+        i += D;
+    }
+    if (last_r) last_r[static_cast<size_t>(brow) * D + d] = hr;
+    if (last_i) last_i[static_cast<size_t>(brow) * D + d] = hi;
+}
+
+template <typename St>
+__global__ void __launch_bounds__(128)
+cplain_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ out_r,
+           const St *__restrict__ out_i, const St *__restrict__ go_r, const St *__restrict__ go_i,
+           St *__restrict__ grad_ar, St *__restrict__ grad_ai, St *__restrict__ grad_br, St *__restrict__ grad_bi,
+           int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    if (d >= D) return;
+    const size_t row = static_cast<size_t>(brow) * T * D + d;
+    float gr = 0.0f, gi = 0.0f, xr = 0.0f, xi = 0.0f;  // x: a_{t+1} (0 past T)
+#pragma unroll 4
+    for (int t = T - 1; t >= 0; --t) {
+        const size_t i = row + static_cast<size_t>(t) * D;
+        float yr[1], yi[1], pr[1] = {0.0f}, pi[1] = {0.0f}, nxr[1], nxi[1];
+        load_lanes_global<St, 1>(go_r + i, yr);
+        load_lanes_global<St, 1>(go_i + i, yi);
+        load_lanes_global<St, 1>(ar + i, nxr);
+        load_lanes_global<St, 1>(ai + i, nxi);
+        if (t > 0) {
+            load_lanes_global<St, 1>(out_r + i - D, pr);
+            load_lanes_global<St, 1>(out_i + i - D, pi);
+        }
+        const float nr = __fmaf_rn(xr, gr, __fmaf_rn(xi, gi, yr[0]));
+        const float ni = __fmaf_rn(xr, gi, __fmaf_rn(-xi, gr, yi[0]));
+        gr = nr;
+        gi = ni;
+        const float vbr[1] = {gr}, vbi[1] = {gi};
+        const float var[1] = {__fmaf_rn(gr, pr[0], __fmul_rn(gi, pi[0]))};
+        const float vai[1] = {__fmaf_rn(gi, pr[0], -__fmul_rn(gr, pi[0]))};
+        store_lanes<St, 1>(grad_br + i, vbr);
+        store_lanes<St, 1>(grad_bi + i, vbi);
+        store_lanes<St, 1>(grad_ar + i, var);
+        store_lanes<St, 1>(grad_ai + i, vai);
+        xr = nxr[0];
+        xi = nxi[0];
+    }
+}
+
+}  // namespace lrscan

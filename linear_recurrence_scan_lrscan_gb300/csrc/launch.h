@@ -39,10 +39,12 @@ enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3
 // Arguments of one time-tiled launch (forward: maps a,b / out0=out;
 // backward: maps a,out,grad_out / out0=grad_a, out1=grad_b).
 struct WinLaunch {
-    const CUtensorMap *maps[3];
+    const CUtensorMap *maps[6];   // input planes in kernel order (complex scan: up to 6)
     void *out0;
     void *out1;
+    void *out2, *out3;            // complex backward: grad_br, grad_bi
     float *last;
+    float *last_i;                // complex forward: Im of the final state
     int64_t B, T, D;
     DevStatus *status;
     uint64_t timeout_ns;
@@ -76,6 +78,9 @@ struct WinVariant {
 // path: kPathSeq or kPathWindow; dtype 0 = f32, 1 = bf16
 const WinVariant *win_variants(int path, int dtype, int *count);
 
+// Complex scan tile variants (kernels_complex.cu); dtype 0 = f32, 1 = bf16.
+const WinVariant *cwin_variants(int dtype, int *count);
+
 // Three-phase chunked path and plain kernels (kernels_chunk.cu).
 struct ChunkLaunch {
     const void *in0, *in1, *in2;  // fwd: a, b; bwd: a, out, grad_out
@@ -92,6 +97,12 @@ int chunk_fwd(const ChunkLaunch &L, int dtype);
 int chunk_bwd(const ChunkLaunch &L, int dtype);
 int plain_fwd_launch(const ChunkLaunch &L, int dtype);
 int plain_bwd_launch(const ChunkLaunch &L, int dtype);
+// Complex plain kernels: forward in0 = ar, in1 = br, out0 = out_r, last = last_r
+// plus the imaginary planes; backward in = {ar, ai, out_r, out_i, go_r, go_i},
+// out = {grad_ar, grad_ai, grad_br, grad_bi}.
+int cplain_fwd_launch(const ChunkLaunch &L, const void *ai, const void *bi, void *out_i, float *last_i, int dtype);
+int cplain_bwd_launch(const void *const in[6], void *const out[4], int64_t B, int64_t T, int64_t D, int dtype,
+                      cudaStream_t stream);
 // Whole-sequence affine summary per lane (dir 0: forward, 1: backward);
 // in0 = a, in1 = b or grad_out, P and Q = [B, D] outputs.
 int summary_launch(const ChunkLaunch &L, int dtype, int dir);

@@ -572,6 +572,161 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
     return rc == 0 ? LRSCAN_OK : (rc == -2 ? LRSCAN_EINVAL : LRSCAN_ECUDA);
 }
 
+// ---------------------------------------------------------------- complex --
+// Complex scan: the tiled sequential kernels when every plane's rows are
+// 16-byte aligned, else the plain kernels.  The tile variant is the first one
+// of the table that gives every SM 1.5 CTAs, else the one with the most CTAs.
+int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
+                 const Geometry &g, Choice *ch) {
+    (void)T;
+    const int want = opts ? opts->path : 0;
+    const int force_v = opts ? opts->tile_variant : 0;
+    if (want != kPathAuto && want != kPathSeq && want != kPathPlain)
+        return fail(LRSCAN_EINVAL, "the complex scan has the seq and plain paths only (path %d)", want);
+    if (want == kPathSeq && !aligned16)
+        return fail(LRSCAN_EINVAL, "path seq needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
+    const int path = want == kPathAuto ? (aligned16 ? kPathSeq : kPathPlain) : want;
+    ch->path = path;
+    ch->dir = dir;
+    ch->kernels = 1;
+    ch->vec = 1;
+    if (path == kPathPlain) {
+        if (force_v > 1) return fail(LRSCAN_EINVAL, "the plain path has one variant");
+        ch->ctas = B * ((D + 127) / 128);
+        ch->threads = 128;
+        return LRSCAN_OK;
+    }
+    int n = 0;
+    const WinVariant *tab = cwin_variants(dtype, &n);
+    int vi = -1;
+    if (force_v > 0) {
+        if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
+        vi = force_v - 1;
+    } else {
+        long long most = -1;
+        int most_i = -1;
+        for (int i = 0; i < n; ++i) {
+            const Occ o = occupancy(tab[i], dir, B, D, g);
+            if (o.resident == 0) continue;
+            if (vi < 0 && static_cast<double>(o.ctas) >= 1.5 * g.sm_count) vi = i;
+            if (o.ctas > most) { most = o.ctas; most_i = i; }
+        }
+        if (vi < 0) vi = most_i;
+    }
+    if (vi < 0) return fail(LRSCAN_EINVAL, "no complex tile variant fits this device");
+    const Occ o = occupancy(tab[vi], dir, B, D, g);
+    if (o.resident == 0) return fail(LRSCAN_EINVAL, "tile variant %s does not fit on an SM", tab[vi].name);
+    ch->vidx = vi;
+    ch->var = &tab[vi];
+    ch->ctas = o.ctas;
+    ch->threads = dir_of(tab[vi], dir).threads;
+    ch->smem = dir_of(tab[vi], dir).smem;
+    ch->stages = dir_of(tab[vi], dir).nstage;
+    return LRSCAN_OK;
+}
+
+int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, float *last_i, int64_t B, int64_t T,
+             int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    t_detail[0] = 0;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
+    cudaStream_t st = pick_stream(stream);
+    if (T == 0) {
+        if ((rc = copy_or_zero(last_r, nullptr, B, D, st)) || (rc = copy_or_zero(last_i, nullptr, B, D, st))) return rc;
+        return LRSCAN_OK;
+    }
+    if (!in[0] || !in[1] || !in[2] || !in[3] || !out_r || !out_i)
+        return fail(LRSCAN_EINVAL, "NULL ar, ai, br, bi, out_r or out_i");
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({in[0], in[1], in[2], in[3], out_r, out_i}, D, dtype);
+    Choice ch;
+    if ((rc = plan_complex(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
+    const size_t es = esize(dtype);
+    if (ch.path == kPathPlain) {
+        ChunkLaunch L{};
+        L.in0 = in[0]; L.in1 = in[2]; L.out0 = out_r; L.last = last_r;
+        L.B = B; L.T = T; L.D = D; L.stream = st;
+        return cplain_fwd_launch(L, in[1], in[3], out_i, last_i, dtype)
+                   ? fail(LRSCAN_ECUDA, "complex plain launch: %s", cudaGetErrorString(cudaGetLastError()))
+                   : LRSCAN_OK;
+    }
+    const WinDirCfg &v = ch.var->fwd;
+    for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+        const int64_t nb = std::min<int64_t>(65535, B - b0);
+        const size_t off = static_cast<size_t>(b0) * T * D * es;
+        CUtensorMap m[4];
+        for (int i = 0; i < 4; ++i)
+            if (encode_map(&m[i], static_cast<const char *>(in[i]) + off, dtype, nb, T, D, v.dt, v.w))
+                return LRSCAN_EINVAL;
+        WinLaunch L{};
+        for (int i = 0; i < 4; ++i) L.maps[i] = &m[i];
+        L.out0 = static_cast<char *>(out_r) + off;
+        L.out1 = static_cast<char *>(out_i) + off;
+        L.last = last_r ? last_r + b0 * D : nullptr;
+        L.last_i = last_i ? last_i + b0 * D : nullptr;
+        L.B = nb; L.T = T; L.D = D;
+        L.status = ctx->status;
+        L.timeout_ns = g_timeout_ns.load();
+        L.stream = st;
+        L.device = dev;
+        if (v.launch(L, v))
+            return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
+    }
+    return LRSCAN_OK;
+}
+
+int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+             const lrscan_opts *opts) {
+    t_detail[0] = 0;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0 || T == 0) return LRSCAN_OK;
+    for (int i = 0; i < 6; ++i)
+        if (!in[i]) return fail(LRSCAN_EINVAL, "NULL complex backward input %d", i);
+    for (int i = 0; i < 4; ++i)
+        if (!outp[i]) return fail(LRSCAN_EINVAL, "NULL complex gradient output %d", i);
+    cudaStream_t st = pick_stream(stream);
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({in[0], in[1], in[2], in[3], in[4], in[5], outp[0], outp[1], outp[2], outp[3]}, D, dtype);
+    Choice ch;
+    if ((rc = plan_complex(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
+    if (ch.path == kPathPlain)
+        return cplain_bwd_launch(in, outp, B, T, D, dtype, st)
+                   ? fail(LRSCAN_ECUDA, "complex plain launch: %s", cudaGetErrorString(cudaGetLastError()))
+                   : LRSCAN_OK;
+    const size_t es = esize(dtype);
+    const WinDirCfg &v = ch.var->bwd;
+    for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+        const int64_t nb = std::min<int64_t>(65535, B - b0);
+        const size_t off = static_cast<size_t>(b0) * T * D * es;
+        CUtensorMap m[6];
+        for (int i = 0; i < 6; ++i)
+            if (encode_map(&m[i], static_cast<const char *>(in[i]) + off, dtype, nb, T, D, v.dt, v.w))
+                return LRSCAN_EINVAL;
+        WinLaunch L{};
+        for (int i = 0; i < 6; ++i) L.maps[i] = &m[i];
+        L.out0 = static_cast<char *>(outp[0]) + off;
+        L.out1 = static_cast<char *>(outp[1]) + off;
+        L.out2 = static_cast<char *>(outp[2]) + off;
+        L.out3 = static_cast<char *>(outp[3]) + off;
+        L.B = nb; L.T = T; L.D = D;
+        L.status = ctx->status;
+        L.timeout_ns = g_timeout_ns.load();
+        L.stream = st;
+        L.device = dev;
+        if (v.launch(L, v))
+            return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
+    }
+    return LRSCAN_OK;
+}
+
 }  // namespace
 
 // Lets other translation units of the library report why a call failed.
@@ -674,6 +829,36 @@ int lrscan_compose_maps(const float *maps, int64_t W, int64_t rank, const float 
     const int n = dir == 0 ? static_cast<int>(rank) : static_cast<int>(W - 1 - rank);
     if (compose_maps_launch(maps, init, out, lanes, r0, step, n, pick_stream(stream)))
         return fail(LRSCAN_ECUDA, "compose launch: %s", cudaGetErrorString(cudaGetLastError()));
+    return LRSCAN_OK;
+}
+
+int lrscan_cfwd(const void *ar, const void *ai, const void *br, const void *bi, void *out_r, void *out_i,
+                float *last_r, float *last_i, int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+                const lrscan_opts *opts) {
+    const void *in[4] = {ar, ai, br, bi};
+    return run_cfwd(in, out_r, out_i, last_r, last_i, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_cbwd(const void *ar, const void *ai, const void *out_r, const void *out_i, const void *grad_out_r,
+                const void *grad_out_i, void *grad_ar, void *grad_ai, void *grad_br, void *grad_bi, int64_t B,
+                int64_t T, int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    const void *in[6] = {ar, ai, out_r, out_i, grad_out_r, grad_out_i};
+    void *const outp[4] = {grad_ar, grad_ai, grad_br, grad_bi};
+    return run_cbwd(in, outp, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
+                        const lrscan_opts *opts, lrscan_plan_info *info) {
+    if (!info || (dir != 0 && dir != 1)) return LRSCAN_EINVAL;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    DeviceCtx *ctx = nullptr;
+    if (device_ctx(&ctx) != LRSCAN_OK) ctx = nullptr;
+    const bool al = is_aligned16 && (D * esize(dtype)) % 16 == 0;
+    Choice ch;
+    if ((rc = plan_complex(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch)))
+        return rc;
+    fill_info(ch, info);
     return LRSCAN_OK;
 }
 

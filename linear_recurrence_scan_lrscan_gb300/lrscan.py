@@ -86,6 +86,10 @@ EXPORTS = {
                           ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_summary": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
     "lrscan_compose_maps": ([_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
+    "lrscan_cfwd": ([_P] * 8 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_cbwd": ([_P] * 10 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_plan_complex": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
+                             ctypes.POINTER(PlanInfo)], ctypes.c_int),
     "lrscan_set_stream": ([_P], ctypes.c_int),
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
@@ -348,6 +352,66 @@ def lrscan_compose_maps(maps: torch.Tensor, rank: int, init: torch.Tensor | None
     return out
 
 
+def lrscan_cfwd(ar, ai, br, bi, *, out_r=None, out_i=None, last_r=None, last_i=None, want_last: bool = True,
+                path=None, tile_variant=None, stream=None):
+    """Complex forward scan on re/im planes [B, T, D]; returns
+    (out_r, out_i, last_r, last_i) (last planes fp32 [B, D], or None)."""
+    if ar.ndim != 3 or any(t.shape != ar.shape for t in (ai, br, bi)):
+        raise ValueError("lrscan expects matching [B, T, D] planes")
+    code = _dtype_code(ar)
+    B, T, D = ar.shape
+    out_r = torch.empty_like(ar) if out_r is None else out_r
+    out_i = torch.empty_like(ar) if out_i is None else out_i
+    if want_last:
+        last_r = torch.empty((B, D), device=ar.device, dtype=torch.float32) if last_r is None else last_r
+        last_i = torch.empty((B, D), device=ar.device, dtype=torch.float32) if last_i is None else last_i
+    _check_tensors(ar.shape, ar.dtype, ar.device, ar=ar, ai=ai, br=br, bi=bi, out_r=out_r, out_i=out_i)
+    for name, t in (("last_r", last_r), ("last_i", last_i)):
+        if t is not None:
+            _check_state_tensor(name, t, (B, D), torch.float32, ar.device)
+    with torch.cuda.device(ar.device):
+        o = _opts(path, None, tile_variant, None)
+        rc = lib().lrscan_cfwd(ar.data_ptr(), ai.data_ptr(), br.data_ptr(), bi.data_ptr(), out_r.data_ptr(),
+                               out_i.data_ptr(), last_r.data_ptr() if last_r is not None else None,
+                               last_i.data_ptr() if last_i is not None else None, B, T, D, code,
+                               _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_cfwd")
+    return out_r, out_i, last_r, last_i
+
+
+def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, path=None, tile_variant=None,
+                stream=None):
+    """Complex reverse scan; returns (grad_ar, grad_ai, grad_br, grad_bi) for the
+    loss sum(grad_out_r * out_r + grad_out_i * out_i)."""
+    if ar.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] planes")
+    code = _dtype_code(ar)
+    B, T, D = ar.shape
+    grads = tuple(torch.empty_like(ar) for _ in range(4)) if grads is None else tuple(grads)
+    _check_tensors(ar.shape, ar.dtype, ar.device, ar=ar, ai=ai, out_r=out_r, out_i=out_i, grad_out_r=grad_out_r,
+                   grad_out_i=grad_out_i, grad_ar=grads[0], grad_ai=grads[1], grad_br=grads[2], grad_bi=grads[3])
+    with torch.cuda.device(ar.device):
+        o = _opts(path, None, tile_variant, None)
+        rc = lib().lrscan_cbwd(ar.data_ptr(), ai.data_ptr(), out_r.data_ptr(), out_i.data_ptr(),
+                               grad_out_r.data_ptr(), grad_out_i.data_ptr(), *[g.data_ptr() for g in grads],
+                               B, T, D, code, _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_cbwd")
+    return grads
+
+
+def lrscan_plan_complex(B: int, T: int, D: int, dtype="f32", direction: str = "fwd", aligned: bool = True,
+                        path=None, tile_variant=None) -> dict:
+    code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
+    if code is None:
+        raise ValueError(f"unsupported dtype {dtype}")
+    info = PlanInfo()
+    o = _opts(path, None, tile_variant, None)
+    rc = lib().lrscan_plan_complex(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
+                                   ctypes.byref(o) if o is not None else None, ctypes.byref(info))
+    _check(rc, "lrscan_plan_complex")
+    return info.as_dict()
+
+
 def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
                 aligned: bool = True, path=None, chunk_len=None, tile_variant=None) -> dict:
     """What the dispatcher would run for this call (host only; no launch)."""
@@ -441,3 +505,27 @@ def scan_state(a: torch.Tensor, b: torch.Tensor, h0: torch.Tensor | None = None,
                segment_pos: torch.Tensor | None = None, path=None, chunk_len=None):
     """Differentiable state-carrying scan; returns (out, last) with last fp32 [B, D]."""
     return LinearRecurrenceScanState.apply(a, b, h0, segment_pos, path, chunk_len)
+
+
+class ComplexScan(torch.autograd.Function):
+    """Autograd wrapper of the complex scan: (out_r, out_i) = scan(ar, ai, br, bi)."""
+
+    @staticmethod
+    def forward(ctx, ar, ai, br, bi, path=None):
+        ar, ai, br, bi = (t.contiguous() for t in (ar, ai, br, bi))
+        out_r, out_i, _, _ = lrscan_cfwd(ar, ai, br, bi, want_last=False, path=path)
+        ctx.save_for_backward(ar, ai, out_r, out_i)
+        ctx.path = path
+        return out_r, out_i
+
+    @staticmethod
+    def backward(ctx, grad_out_r, grad_out_i):
+        ar, ai, out_r, out_i = ctx.saved_tensors
+        gr = torch.zeros_like(out_r) if grad_out_r is None else grad_out_r.contiguous()
+        gi = torch.zeros_like(out_i) if grad_out_i is None else grad_out_i.contiguous()
+        return (*lrscan_cbwd(ar, ai, out_r, out_i, gr, gi, path=ctx.path), None)
+
+
+def complex_scan(ar, ai, br, bi, path=None):
+    """Differentiable complex diagonal scan on re/im planes; returns (out_r, out_i)."""
+    return ComplexScan.apply(ar, ai, br, bi, path)

@@ -151,6 +151,37 @@ def random_inputs(B: int, T: int, D: int, dtype: str = "f32", *, seed: int = 0,
             "lengths": torch.full((B,), T, dtype=torch.int64), "shape": shape}
 
 
+# Complex scan workload (re/im planes).  The pages fix no complex workload
+# sizes; this one has the shape and the decay magnitude of the gated bf16
+# workload, with a uniformly random phase per (b, t, d).
+COMPLEX_WORKLOAD = Workload(6, "complex-gated-bf16", 8, 2048, 2560, "bf16")
+
+
+def make_complex_inputs(B: int | None = None, T: int | None = None, D: int | None = None, dtype: str | None = None,
+                        *, seed: int | None = None) -> dict:
+    """Draw the six planes (ar, ai, br, bi, go_r, go_i) of a complex scan:
+    |a| = exp(-8*softplus(x)*r), x~N(0,1), r~U(0,1); arg a ~ U(-pi, pi);
+    b and grad_out planes ~N(0,1).  Drawn in fp32, stored in `dtype`."""
+    w = COMPLEX_WORKLOAD
+    B = w.B if B is None else B
+    T = w.T if T is None else T
+    D = w.D if D is None else D
+    dtype = w.dtype if dtype is None else dtype
+    gen = torch.Generator("cpu").manual_seed(SEED_BASE + w.cid if seed is None else seed)
+    shape = (B, T, D)
+    x = _normal(gen, shape)
+    r = _uniform(gen, shape, 0.0, 1.0)
+    rad = torch.exp(-8.0 * torch.nn.functional.softplus(x) * r)
+    del x, r
+    ang = _uniform(gen, shape, -3.141592653589793, 3.141592653589793)
+    planes = {"ar": rad * torch.cos(ang), "ai": rad * torch.sin(ang)}
+    del rad, ang
+    for k in ("br", "bi", "go_r", "go_i"):
+        planes[k] = _normal(gen, shape)
+    dt = TORCH_DTYPE[dtype]
+    return {k: v.to(dt).contiguous() for k, v in planes.items()} | {"shape": shape, "workload": w}
+
+
 def to_numpy_storage(t: torch.Tensor):
     """CPU tensor -> numpy array as the oracle takes it (bf16 as uint16 bits)."""
     t = t.detach().cpu().contiguous()

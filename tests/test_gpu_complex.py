@@ -1,0 +1,131 @@
+"""GPU parity of the complex diagonal scan (re/im planes) on both paths and
+every tile variant, against the oracle's complex scan.  Both paths keep the
+oracle's order of operations, so they are compared exactly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+from linear_recurrence_scan_lrscan_gb300.workloads import COMPLEX_WORKLOAD, make_complex_inputs
+from parity_util import assert_close, assert_last_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+PLANES = ("ar", "ai", "br", "bi", "go_r", "go_i")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L.lib()
+    yield
+    assert L.lrscan_sync_check() == 0
+
+
+def from_np(x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x))
+
+
+def check_complex(inp, dt, **kw):
+    B, T, D = inp["shape"]
+    np_in = {k: to_np(inp[k]) for k in PLANES}
+    o = oracle.default()
+    ref = o.cfwd(np_in["ar"], np_in["ai"], np_in["br"], np_in["bi"], dt)
+    cu = {k: inp[k].cuda() for k in PLANES}
+    got = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"], **kw)
+    assert L.lrscan_sync_check() == 0
+    plan = L.lrscan_plan_complex(B, T, D, dt, "fwd", **kw)
+    tag = plan["name"]
+    for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
+        assert_close(to_np(g), r, dt, f"{name}[{tag}]", exact=True)
+    for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
+        assert_last_close(g.cpu().numpy(), r, f"{name}[{tag}]", exact=True)
+    # backward from the oracle's forward output
+    out_r, out_i = from_np(ref[0], dt).cuda(), from_np(ref[1], dt).cuda()
+    gref = o.cbwd(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt)
+    ggot = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"], **kw)
+    assert L.lrscan_sync_check() == 0
+    planb = L.lrscan_plan_complex(B, T, D, dt, "bwd", **kw)
+    for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot, gref):
+        assert_close(to_np(g), r, dt, f"{name}[{planb['name']}]", exact=True)
+    return plan, planb
+
+
+SHAPES = [(3, 300, 200), (2, 77, 40), (1, 1, 8), (2, 257, 1000), (1, 33, 64)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_complex_every_variant(dt, shape):
+    B, T, D = shape
+    inp = make_complex_inputs(B, T, D, dt, seed=500 + T)
+    n = 1
+    while True:
+        try:
+            L.lrscan_plan_complex(B, T, D, dt, path="seq", tile_variant=n)
+        except L.LrscanError:
+            break
+        check_complex(inp, dt, path="seq", tile_variant=n)
+        n += 1
+    assert n > 3
+    check_complex(inp, dt, path="plain")
+    plan, _ = check_complex(inp, dt)
+    assert plan["path"] == "seq"
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_unaligned_takes_plain(dt):
+    inp = make_complex_inputs(2, 90, 37, dt, seed=510)
+    plan, planb = check_complex(inp, dt)
+    assert plan["path"] == "plain" and planb["path"] == "plain"
+
+
+def test_complex_empty_and_invalid():
+    a = torch.empty((2, 0, 16), device="cuda")
+    _, _, lr, li = L.lrscan_cfwd(a, a, a, a)
+    assert not lr.any() and not li.any()
+    x = torch.zeros((1, 4, 16), device="cuda")
+    with pytest.raises(L.LrscanError):
+        L.lrscan_cfwd(x, x, x, x, path="chunk")
+
+
+def test_complex_full_size_sampled_lanes():
+    """The complex workload at full size in the benchmark's launch
+    configuration, checked on sampled lanes the oracle computes one by one."""
+    w = COMPLEX_WORKLOAD
+    inp = make_complex_inputs()
+    cu = {k: inp[k].cuda() for k in PLANES}
+    out_r, out_i, last_r, last_i = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"])
+    grads = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"])
+    assert L.lrscan_sync_check() == 0
+    r = np.random.default_rng(520)
+    o = oracle.default()
+    for _ in range(6):
+        b = int(r.integers(w.B))
+        d = int(r.integers(w.D))
+        sl = lambda t: np.ascontiguousarray(to_np(t[b:b + 1, :, d:d + 1]))  # noqa: E731
+        ref = o.cfwd(sl(inp["ar"]), sl(inp["ai"]), sl(inp["br"]), sl(inp["bi"]), w.dtype)
+        assert_close(sl(out_r), ref[0], w.dtype, "out_r sampled", exact=True)
+        assert_close(sl(out_i), ref[1], w.dtype, "out_i sampled", exact=True)
+        assert last_r[b, d].item() == ref[2][0, 0] and last_i[b, d].item() == ref[3][0, 0]
+        gref = o.cbwd(sl(inp["ar"]), sl(inp["ai"]), ref[0], ref[1], sl(inp["go_r"]), sl(inp["go_i"]), w.dtype)
+        for g, gr_ in zip(grads, gref):
+            assert_close(sl(g), gr_, w.dtype, "complex grads sampled", exact=True)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_scan_autograd(dt):
+    inp = make_complex_inputs(2, 150, 64, dt, seed=530)
+    xs = [inp[k].cuda().requires_grad_() for k in ("ar", "ai", "br", "bi")]
+    out_r, out_i = L.complex_scan(*xs)
+    (out_r.float() * inp["go_r"].cuda().float() + out_i.float() * inp["go_i"].cuda().float()).sum().backward()
+    o = oracle.default()
+    np_in = {k: to_np(inp[k]) for k in PLANES}
+    ref = o.cfwd(np_in["ar"], np_in["ai"], np_in["br"], np_in["bi"], dt)
+    gref = o.cbwd(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt)
+    for x, r in zip(xs, gref):
+        assert_close(to_np(x.grad), r, dt, "complex autograd", exact=True)
