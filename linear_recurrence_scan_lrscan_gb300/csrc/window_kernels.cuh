@@ -275,10 +275,11 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     bool failed = false;
     int stage = 0, use = 0;
     // EXT: this warp's rows start at window row wrow; bit j of rbits is a
-    // reset at row s*L + j of the current window
+    // reset at row s*L + j of the current window.  Positions are loaded two
+    // windows ahead (pos_next: window k+1, pos_next2: window k+2).
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
-    int32_t pos_next = 1;
+    int32_t pos_next = 1, pos_next2 = 1;
     if constexpr (EXT) {
         static_assert((G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
         if (sx.h0 != nullptr) {
@@ -295,13 +296,15 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         pos_next = seg.at(wrow + lane);
+        pos_next2 = seg.at(sm.W + wrow + lane);
     }
 
     for (int k = 0; k < sm.nwin; ++k) {
         uint32_t rbits = 0;
         if constexpr (EXT) {
             rbits = __ballot_sync(0xffffffffu, pos_next == 0) >> (s * L - wrow);
-            pos_next = seg.at((k + 1) * sm.W + wrow + lane);
+            pos_next = pos_next2;
+            pos_next2 = seg.at((k + 2) * sm.W + wrow + lane);
         }
         bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         if constexpr (EXT && C::SEQ) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
@@ -565,7 +568,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     // EXT: bit j of r0bits / r1bits is a reset at row s*L + j / s*L + j + 1
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
-    int32_t pos0_next = 1, pos1_next = 1;
+    int32_t pos0_next = 1, pos1_next = 1, pos0_next2 = 1, pos1_next2 = 1;  // windows k+1, k+2
     float h0v[V];  // h_{-1}
 #pragma unroll
     for (int v = 0; v < V; ++v) h0v[v] = 0.0f;
@@ -591,6 +594,8 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int wb0 = (nwin - 1) * sm.W + wrow + lane;
         pos0_next = seg.at(wb0);
         pos1_next = seg.at(wb0 + 1);
+        pos0_next2 = seg.at(wb0 - sm.W);
+        pos1_next2 = seg.at(wb0 - sm.W + 1);
     }
 
     for (int k = 0; k < nwin; ++k) {
@@ -598,9 +603,11 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if constexpr (EXT) {
             r0bits = __ballot_sync(0xffffffffu, pos0_next == 0) >> (s * L - wrow);
             r1bits = __ballot_sync(0xffffffffu, pos1_next == 0) >> (s * L - wrow);
-            const int wb = (nwin - 2 - k) * sm.W + wrow + lane;
-            pos0_next = seg.at(wb);
-            pos1_next = seg.at(wb + 1);
+            pos0_next = pos0_next2;
+            pos1_next = pos1_next2;
+            const int wb = (nwin - 3 - k) * sm.W + wrow + lane;
+            pos0_next2 = seg.at(wb);
+            pos1_next2 = seg.at(wb + 1);
         }
         bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         if constexpr (EXT && C::SEQ) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
