@@ -15,14 +15,18 @@
 // ring with bulk tensor copies (4 forward: ar, ai, br, bi; 6 backward: ar and
 // ai one row late, out_r and out_i one row early, go_r, go_i, so that the
 // copies' zero fill gives a_T = 0 and h_{-1} = 0), and every consumer thread
-// walks its V lanes through all windows in registers.
+// walks its V lanes through all windows in registers.  Full windows are
+// taken CH rows at a time: the CH rows of every plane are copied from shared
+// memory into registers first, so all those loads issue before the dependent
+// chain (and before the chunk's global stores, which the compiler cannot
+// reorder them across).
 #pragma once
 
 #include "window_kernels.cuh"
 
 namespace lrscan {
 
-template <class C>
+template <class C, int CH>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                 const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
@@ -71,12 +75,8 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
         const int rbase = k * sm.W;
         const int n = min(T - rbase, L);
         const size_t o = (row0 + rbase) * D + d;
-        auto step = [&](int j) {
-            float xr[V], xi[V], yr[V], yi[V];
-            unpack_lanes<St, V>(tar + j * DT, xr);
-            unpack_lanes<St, V>(tai + j * DT, xi);
-            unpack_lanes<St, V>(tbr + j * DT, yr);
-            unpack_lanes<St, V>(tbi + j * DT, yi);
+        auto compute = [&](int j, const float (&xr)[V], const float (&xi)[V], const float (&yr)[V],
+                           const float (&yi)[V]) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const float nr = __fmaf_rn(xr[v], hr[v], __fmaf_rn(-xi[v], hi[v], yr[v]));
@@ -90,10 +90,36 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
             }
         };
         if (n == L) {
+            using Raw = typename RawOf<St, V>::T;
 #pragma unroll
-            for (int j = 0; j < L; ++j) step(j);
+            for (int j0 = 0; j0 < L; j0 += CH) {
+                Raw r0[CH], r1[CH], r2[CH], r3[CH];
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    r0[j] = load_raw<St, V>(tar + (j0 + j) * DT);
+                    r1[j] = load_raw<St, V>(tai + (j0 + j) * DT);
+                    r2[j] = load_raw<St, V>(tbr + (j0 + j) * DT);
+                    r3[j] = load_raw<St, V>(tbi + (j0 + j) * DT);
+                }
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    float xr[V], xi[V], yr[V], yi[V];
+                    widen_raw(r0[j], xr);
+                    widen_raw(r1[j], xi);
+                    widen_raw(r2[j], yr);
+                    widen_raw(r3[j], yi);
+                    compute(j0 + j, xr, xi, yr, yi);
+                }
+            }
         } else {
-            for (int j = 0; j < n; ++j) step(j);
+            for (int j = 0; j < n; ++j) {
+                float xr[V], xi[V], yr[V], yi[V];
+                unpack_lanes<St, V>(tar + j * DT, xr);
+                unpack_lanes<St, V>(tai + j * DT, xi);
+                unpack_lanes<St, V>(tbr + j * DT, yr);
+                unpack_lanes<St, V>(tbi + j * DT, yi);
+                compute(j, xr, xi, yr, yi);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty_bar(stage));
@@ -108,7 +134,7 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
     }
 }
 
-template <class C>
+template <class C, int CH>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                 const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
@@ -163,14 +189,9 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
         const int wbase = (nwin - 1 - k) * sm.W;
         const int n = min(T - wbase, L);
         const size_t o = (row0 + wbase) * D + d;
-        auto step = [&](int j) {
-            float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V], far_[V], fai[V];
-            unpack_lanes<St, V>(tar + j * DT, xr);
-            unpack_lanes<St, V>(tai + j * DT, xi);
-            unpack_lanes<St, V>(tpr + j * DT, pr);
-            unpack_lanes<St, V>(tpi + j * DT, pi);
-            unpack_lanes<St, V>(tgr + j * DT, yr);
-            unpack_lanes<St, V>(tgi + j * DT, yi);
+        auto compute = [&](int j, const float (&xr)[V], const float (&xi)[V], const float (&pr)[V],
+                           const float (&pi)[V], const float (&yr)[V], const float (&yi)[V]) {
+            float far_[V], fai[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const float nr = __fmaf_rn(xr[v], gr[v], __fmaf_rn(xi[v], gi[v], yr[v]));
@@ -189,10 +210,43 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
             }
         };
         if (n == L) {
+            using Raw = typename RawOf<St, V>::T;
 #pragma unroll
-            for (int j = L - 1; j >= 0; --j) step(j);
+            for (int j1 = L; j1 > 0; j1 -= CH) {  // rows j1-CH .. j1-1, last first
+                Raw r[6][CH];
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const int row = (j1 - CH + j) * DT;
+                    r[0][j] = load_raw<St, V>(tar + row);
+                    r[1][j] = load_raw<St, V>(tai + row);
+                    r[2][j] = load_raw<St, V>(tpr + row);
+                    r[3][j] = load_raw<St, V>(tpi + row);
+                    r[4][j] = load_raw<St, V>(tgr + row);
+                    r[5][j] = load_raw<St, V>(tgi + row);
+                }
+#pragma unroll
+                for (int j = CH - 1; j >= 0; --j) {
+                    float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V];
+                    widen_raw(r[0][j], xr);
+                    widen_raw(r[1][j], xi);
+                    widen_raw(r[2][j], pr);
+                    widen_raw(r[3][j], pi);
+                    widen_raw(r[4][j], yr);
+                    widen_raw(r[5][j], yi);
+                    compute(j1 - CH + j, xr, xi, pr, pi, yr, yi);
+                }
+            }
         } else {
-            for (int j = n - 1; j >= 0; --j) step(j);
+            for (int j = n - 1; j >= 0; --j) {
+                float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V];
+                unpack_lanes<St, V>(tar + j * DT, xr);
+                unpack_lanes<St, V>(tai + j * DT, xi);
+                unpack_lanes<St, V>(tpr + j * DT, pr);
+                unpack_lanes<St, V>(tpi + j * DT, pi);
+                unpack_lanes<St, V>(tgr + j * DT, yr);
+                unpack_lanes<St, V>(tgi + j * DT, yi);
+                compute(j, xr, xi, pr, pi, yr, yi);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty_bar(stage));

@@ -9,11 +9,15 @@ namespace lrscan {
 
 namespace {
 
+// rows staged in registers per step of a full window
+template <class C> constexpr int kStageRowsFwd = C::L < 16 ? C::L : 16;
+template <class C> constexpr int kStageRowsBwd = C::L < 8 ? C::L : 8;
+
 template <class C>
 int launch_cwin_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static unsigned long long mask = 0;
     static std::mutex mu;
-    auto fn = cwin_fwd_kernel<C>;
+    auto fn = cwin_fwd_kernel<C, kStageRowsFwd<C>>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
@@ -29,7 +33,7 @@ template <class C>
 int launch_cwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static unsigned long long mask = 0;
     static std::mutex mu;
-    auto fn = cwin_bwd_kernel<C>;
+    auto fn = cwin_bwd_kernel<C, kStageRowsBwd<C>>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
@@ -83,11 +87,15 @@ const WinVariant kCplxBF16[] = {
     {"cseq_bf16_d64_v1", F(CBF_64_1_32, 6), B(CBB_64_1_32, 4)},
     {"cseq_bf16_d64_v2", F(CBF_64_2_32, 6), B(CBB_64_2_16, 6)},
     {"cseq_bf16_d32_v1", F(CBF_32_1_32, 6), B(CBB_32_1_32, 4)},
+    {"cseq_bf16_d64_v1_n4", F(CBF_64_1_32, 4), B(CBB_64_1_32, 3)},
+    {"cseq_bf16_d64_v2_n4", F(CBF_64_2_32, 4), B(CBB_64_2_16, 5)},
 };
 const WinVariant kCplxF32[] = {
     {"cseq_f32_d32_v1", F(CFF_32_1_32, 6), B(CFB_32_1_32, 4)},
     {"cseq_f32_d64_v2", F(CFF_64_2_16, 8), B(CFB_64_2_16, 6)},
     {"cseq_f32_d64_v1", F(CFF_64_1_16, 8), B(CFB_64_1_16, 6)},
+    {"cseq_f32_d32_v1_n4", F(CFF_32_1_32, 4), B(CFB_32_1_32, 3)},
+    {"cseq_f32_d64_v1_n4", F(CFF_64_1_16, 4), B(CFB_64_1_16, 3)},
 };
 #undef F
 #undef B

@@ -166,9 +166,7 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C) {
     return pad * 2;
 }
 
-int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *vidx) {
-    int n = 0;
-    const WinVariant *tab = win_variants(path, dtype, &n);
+int pick_from_table(const WinVariant *tab, int n, int dir, int64_t B, int64_t D, const Geometry &g, int *vidx) {
     int best = -1;
     double best_score = -1;
     for (int i = 0; i < n; ++i) {
@@ -190,6 +188,12 @@ int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, cons
     }
     *vidx = best;
     return best >= 0;
+}
+
+int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *vidx) {
+    int n = 0;
+    const WinVariant *tab = win_variants(path, dtype, &n);
+    return pick_from_table(tab, n, dir, B, D, g, vidx);
 }
 
 // The occupancy rule.  For each (dtype, direction), tile variants in order of
@@ -574,8 +578,9 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
 
 // ---------------------------------------------------------------- complex --
 // Complex scan: the tiled sequential kernels when every plane's rows are
-// 16-byte aligned, else the plain kernels.  The tile variant is the first one
-// of the table that gives every SM 1.5 CTAs, else the one with the most CTAs.
+// 16-byte aligned, else the plain kernels.  The tile variant is chosen by the
+// window-variant rule (a single wave first, then the fullest last wave, then
+// bytes in flight), else the variant with the most CTAs.
 int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
                  const Geometry &g, Choice *ch) {
     (void)T;
@@ -602,16 +607,12 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
-    } else {
+    } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
-        int most_i = -1;
         for (int i = 0; i < n; ++i) {
             const Occ o = occupancy(tab[i], dir, B, D, g);
-            if (o.resident == 0) continue;
-            if (vi < 0 && static_cast<double>(o.ctas) >= 1.5 * g.sm_count) vi = i;
-            if (o.ctas > most) { most = o.ctas; most_i = i; }
+            if (o.resident > 0 && o.ctas > most) { most = o.ctas; vi = i; }
         }
-        if (vi < 0) vi = most_i;
     }
     if (vi < 0) return fail(LRSCAN_EINVAL, "no complex tile variant fits this device");
     const Occ o = occupancy(tab[vi], dir, B, D, g);
