@@ -577,6 +577,17 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
 }
 
 // ---------------------------------------------------------------- complex --
+// Index of the named variant when all its CTAs are resident at once (and
+// they are at least 0.9 per SM), else -1.
+int find_one_wave(const WinVariant *tab, int n, const char *name, int dir, int64_t B, int64_t D, const Geometry &g) {
+    for (int i = 0; i < n; ++i) {
+        if (std::strcmp(tab[i].name, name) != 0) continue;
+        const Occ o = occupancy(tab[i], dir, B, D, g);
+        if (o.one_wave && static_cast<double>(o.ctas) >= 0.9 * g.sm_count) return i;
+    }
+    return -1;
+}
+
 // Complex scan: the tiled sequential kernels when every plane's rows are
 // 16-byte aligned, else the plain kernels.  The tile variant is chosen by the
 // window-variant rule (a single wave first, then the fullest last wave, then
@@ -607,6 +618,8 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
+    } else if (dtype == LRSCAN_BF16 && (vi = find_one_wave(tab, n, "cseq_bf16_d64_v1_n4", dir, B, D, g)) >= 0) {
+        // measured best for both directions of the complex bf16 workload whenever it fits one wave
     } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
         for (int i = 0; i < n; ++i) {
