@@ -197,22 +197,31 @@ int pick_window_variant(int path, int dtype, int dir, int64_t B, int64_t D, cons
 }
 
 // The occupancy rule.  For each (dtype, direction), tile variants in order of
-// preference, each with the fewest CTAs (as a multiple of the SM count) at
-// which it fills the GPU; the first that qualifies (and fits on an SM) wins.
-// The order comes from timing every variant on the five named workloads on
-// GB300: the forward prefers the sequential path (bit-identical to the
-// sequential definition, and as fast wherever the lanes give each SM at
-// least two CTAs); the backward prefers the windowed path, which splits time
-// inside the CTA and keeps far more warps busy on the same lanes.
+// preference, each with the range of CTAs per SM (as multiples of the SM
+// count) in which it is the fastest measured choice; the first that
+// qualifies (and fits on an SM) wins.  The order comes from timing every
+// variant on the five named workloads on GB300: where the lanes alone give
+// each SM too little to do, the windowed path splits time inside the CTA and
+// keeps far more warps busy on the same lanes (the high-residency bf16
+// forward tile puts all 640 CTAs of the gated workload in one wave); the
+// fp32 forward prefers the sequential path, bit-identical to the sequential
+// definition and as fast wherever the lanes give each SM two CTAs.
 struct Pref {
     int path;
     const char *name;
     double min_ctas_per_sm;
+    double max_ctas_per_sm;
 };
-const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
-const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0}, {kPathWindow, "win_f32_d32_s16_pt", 0.45}};
-const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d64_v1", 1.5}, {kPathWindow, "win_bf16_d32_s16", 0.9}};
-const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n2", 0.9}, {kPathWindow, "win_bf16_d64_s8", 0.45}};
+constexpr double kAny = 1e30;
+const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s16_pt", 0.45, kAny}};
+const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny},
+                            {kPathWindow, "win_f32_d32_s16_pt", 0.45, kAny}};
+const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
+                             {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
+                             {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
+                             {kPathWindow, "win_bf16_d32_s16_n2", 0.9, kAny},
+                             {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
 
 bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *path, int *vidx) {
     const Pref *list;
@@ -222,7 +231,7 @@ bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g,
         n = 2;
     } else {
         list = dir == 0 ? kPrefBF16Fwd : kPrefBF16Bwd;
-        n = 2;
+        n = 3;
     }
     for (int i = 0; i < n; ++i) {
         int cnt = 0;
@@ -230,7 +239,8 @@ bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g,
         for (int v = 0; v < cnt; ++v) {
             if (std::strcmp(tab[v].name, list[i].name) != 0) continue;
             const Occ o = occupancy(tab[v], dir, B, D, g);
-            if (o.resident > 0 && static_cast<double>(o.ctas) >= list[i].min_ctas_per_sm * g.sm_count) {
+            const double per_sm = static_cast<double>(o.ctas) / g.sm_count;
+            if (o.resident > 0 && per_sm >= list[i].min_ctas_per_sm && per_sm <= list[i].max_ctas_per_sm) {
                 *path = list[i].path;
                 *vidx = v;
                 return true;

@@ -85,9 +85,9 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("seq_bf16_d64_v1", "win_bf16_d32_s16_n2"),
+    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s16_n4"),
     3: ("win_f32_d32_s16_pt", "win_f32_d32_s16_pt"),
-    4: ("seq_bf16_d64_v1", "win_bf16_d32_s16_n2"),
+    4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s16_n2"),
     5: ("seq_f32_d32", "win_f32_d64_s8"),
 }
 
@@ -104,9 +104,18 @@ def test_occupancy_rule_on_the_named_workloads(lib, cid):
         assert p["ctas"] == w.B * -(-w.D // p["lanes_per_cta"])
 
 
-def test_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
-    for (B, T, D, dt) in [(8, 2048, 2560, "bf16"), (64, 512, 1024, "f32"), (32, 1000, 4096, "f32")]:
+def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
+    for (B, T, D, dt) in [(64, 512, 1024, "f32"), (32, 1000, 4096, "f32")]:
         assert L.lrscan_plan(B, T, D, dt, "fwd")["path"] == "seq"
+
+
+def test_bf16_forward_takes_the_one_wave_window_tile(lib):
+    """The high-residency window tile puts every CTA of the lane tiling on
+    the GPU at once (5 per SM); it is the measured fastest bf16 forward."""
+    for (B, T, D) in [(8, 2048, 2560), (16, 4096, 4096)]:
+        p = L.lrscan_plan(B, T, D, "bf16", "fwd")
+        assert p["name"] == "win_bf16_d32_s8_m5_n2" and p["path"] == "window", p
+        assert p["threads_per_cta"] == 8 * 16 + 32
 
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
