@@ -430,7 +430,7 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
     for f in sets:   # leave every set with the plain forward's output
         L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
     torch.cuda.synchronize()
-    return {"complex": run_complex(iters, dev, peak), "state": {
+    return {"complex": run_complex(iters, dev, peak), "long_t": run_long_t(dev, peak), "state": {
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
         "launches_per_direction": iters,
@@ -488,6 +488,40 @@ def run_complex(iters: int, dev, peak) -> dict:
             "elements/s": 2 * E / ((fms + bms) * 1e-3)}
 
 
+def run_long_t(dev, peak) -> dict:
+    """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32, chunk 64 (65,536
+    chunk maps per lane, 64 lanes): the chunked path with the flat prefix (one
+    warp per lane walks all maps) and with the grouped prefix.  Inputs are
+    drawn on the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    B, T, D, C = 1, 1 << 22, 64, 64
+    gen = torch.Generator(device=dev).manual_seed(20299)
+    a = torch.empty(B, T, D, device=dev).uniform_(0.9, 0.9999, generator=gen)
+    b = torch.empty(B, T, D, device=dev).normal_(generator=gen)
+    g = torch.empty(B, T, D, device=dev).normal_(generator=gen)
+    out, ga, gb = torch.empty_like(a), torch.empty_like(a), torch.empty_like(a)
+    last = torch.empty(B, D, device=dev)
+    stream = torch.cuda.current_stream()
+    E = B * T * D
+    res = {"workload": f"B={B} T={T} D={D} fp32 chunk {C} (few lanes, long sequence)"}
+    for variant, name in ((1, "flat_prefix"), (2, "grouped_prefix")):
+        kw = dict(path="chunk", chunk_len=C, tile_variant=variant)
+        fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last, **kw), 10, stream)
+        bms = time_launches(lambda i: L.lrscan_bwd(a, out, g, ga, gb, **kw), 10, stream)
+        res[name] = {"fwd_ms": fms, "bwd_ms": bms,
+                     "fwd_frac": 3 * E * 4 / (fms * 1e-3) / 1e9 / peak,
+                     "bwd_frac": 5 * E * 4 / (bms * 1e-3) / 1e9 / peak,
+                     "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the long-sequence chunked path")
+    res["auto"] = L.lrscan_plan(B, T, D, "f32", "fwd")["name"]
+    del a, b, g, out, ga, gb
+    torch.cuda.empty_cache()
+    return res
+
+
 def kernel_source_hash() -> str:
     """Hash of the CUDA sources; DRAM counters recorded for another hash are stale."""
     import hashlib
@@ -527,7 +561,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extensions", action="store_true",
-                    help="skip the timing of the state-carrying and complex scans")
+                    help="skip the timing of the state-carrying, complex and long-sequence scans")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=float, default=2e6)
     args = ap.parse_args()

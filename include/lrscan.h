@@ -79,7 +79,9 @@ typedef struct lrscan_opts {
     int chunk_len;          /* chunked path: 16, 32 or 64; 0 = 64 */
     void *workspace;        /* chunked path: optional caller-owned device workspace ... */
     size_t workspace_bytes; /* ... of at least lrscan_workspace_bytes() bytes; NULL = library-owned */
-    int tile_variant;       /* >= 1 forces one kernel tile variant of the path (lrscan_plan lists them); 0 = auto */
+    int tile_variant;       /* >= 1 forces one kernel tile variant of the path (lrscan_plan lists them); 0 = auto.
+                               Chunked path: 1 = flat prefix (one warp per lane walks all chunk maps),
+                               2 = grouped prefix (group maps, their prefix, per-group rescan) */
 } lrscan_opts;
 
 /* What the dispatcher chose (filled by lrscan_plan). */
@@ -244,8 +246,10 @@ int lrscan_compose_maps(const float *maps, int64_t W, int64_t rank, const float 
  * stream) used by lrscan_fwd / lrscan_bwd and by _ex calls given NULL. */
 int lrscan_set_stream(void *stream);
 
-/* Device bytes the chunked path needs for this shape (two fp32 [B, ceil(T/C), D]
- * buffers); chunk_len 0 means 64.  Other paths need none. */
+/* Device bytes the chunked path needs for this shape: two fp32 [B, ceil(T/C), D]
+ * buffers, plus two fp32 [B, ceil(T/C/512), D] buffers for the grouped prefix
+ * (each rounded up to 256 bytes; the value covers both prefix variants);
+ * chunk_len 0 means 64.  Other paths need none. */
 size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len);
 
 /* Host-only: what a call with these arguments would run (no launch, no

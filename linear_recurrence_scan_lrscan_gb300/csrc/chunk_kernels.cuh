@@ -215,6 +215,115 @@ chunk_prefix(const float *__restrict__ P, float *__restrict__ Q, int Nc, int D, 
     }
 }
 
+// ------------------------------------------------- phase 2, grouped form --
+// For long chunk sequences with few lanes the prefix above is one warp per
+// lane walking all Nc maps.  The grouped form (the three-level scan of chunk
+// maps in triton_training_scan.py, _complex_affine_group_local / _outer /
+// _correct) splits every lane's chunks into groups of GC (processing order):
+//   (a) chunk_group_reduce: one warp per (lane, group) composes the group's
+//       maps into one map (P_g = product of P, Q_g = the group's scan from 0);
+//   (b) chunk_prefix over the [B, NG, D] group maps gives each group's entry
+//       state (from h0 / grad_last);
+//   (c) chunk_group_rescan: one warp per (lane, group) rescans its group's
+//       maps from that entry state and writes each chunk's entry over Q.
+// Group g holds processing-order indices [g*GC, (g+1)*GC); its map is stored
+// at group slot g in chunk order (REVERSE: slot NG-1-g), so (b) walks the
+// group maps in the same direction as the chunks.
+
+// Scan of the maps at processing-order indices [lo, hi) of one lane from
+// `carry`; writes every chunk's entry state over Q when WRITE.  Identity maps
+// are transparent (as in chunk_prefix).  Returns the state after the range.
+template <bool REVERSE, int UNROLL, bool WRITE>
+__device__ __forceinline__ float scan_map_range(const float *__restrict__ P, float *__restrict__ Q, size_t base, int D,
+                                                int Nc, int lo, int hi, float carry) {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = lo; c0 < hi; c0 += 32 * UNROLL) {
+        float p[UNROLL], q[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int idx = c0 + u * 32 + lane;
+            const int c = REVERSE ? Nc - 1 - idx : idx;
+            if (idx < hi) {
+                p[u] = __ldcg(P + base + static_cast<size_t>(c) * D);
+                q[u] = __ldcg(Q + base + static_cast<size_t>(c) * D);
+            } else {
+                p[u] = 1.0f;
+                q[u] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            float pu = p[u], qu = q[u];
+            const unsigned live = __ballot_sync(0xffffffffu, !(pu == 1.0f && qu == 0.0f));
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float pp = __shfl_up_sync(0xffffffffu, pu, off);
+                const float qp = __shfl_up_sync(0xffffffffu, qu, off);
+                if (lane >= off) {
+                    qu = __fmaf_rn(pu, qp, qu);
+                    pu = __fmul_rn(pu, pp);
+                }
+            }
+            if (WRITE) {
+                const unsigned below = live & ((1u << lane) - 1u);
+                const int src = below ? 31 - __clz(below) : 0;
+                const float pin = __shfl_sync(0xffffffffu, pu, src);
+                const float qin = __shfl_sync(0xffffffffu, qu, src);
+                const float entry = below ? __fmaf_rn(pin, carry, qin) : carry;
+                const int idx = c0 + u * 32 + lane;
+                if (idx < hi) Q[base + static_cast<size_t>(REVERSE ? Nc - 1 - idx : idx) * D] = entry;
+            }
+            const int last_live = live ? 31 - __clz(live) : 0;
+            const float pall = __shfl_sync(0xffffffffu, pu, last_live);
+            const float qall = __shfl_sync(0xffffffffu, qu, last_live);
+            if (live) carry = __fmaf_rn(pall, carry, qall);
+        }
+    }
+    return carry;
+}
+
+template <bool REVERSE, int UNROLL>
+__global__ void __launch_bounds__(256)
+chunk_group_reduce(const float *__restrict__ P, const float *__restrict__ Q, float *__restrict__ PG,
+                   float *__restrict__ QG, int Nc, int D, int GC, int NG, long long lanes) {
+    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (wid >= lanes * NG) return;
+    const int g = static_cast<int>(wid % NG);
+    const long long ln = wid / NG;
+    const long long brow = ln / D;
+    const int d = static_cast<int>(ln - brow * D);
+    const size_t base = static_cast<size_t>(brow) * Nc * D + d;
+    const int lo = g * GC, hi = min(Nc, lo + GC);
+    // Q_g: the group's scan from zero; P_g: the product of its decays
+    const float qg = scan_map_range<REVERSE, UNROLL, false>(P, const_cast<float *>(Q), base, D, Nc, lo, hi, 0.0f);
+    const int lane = threadIdx.x & 31;
+    float pg = 1.0f;
+    for (int idx = lo + lane; idx < hi; idx += 32) pg = __fmul_rn(pg, __ldcg(P + base + static_cast<size_t>(REVERSE ? Nc - 1 - idx : idx) * D));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) pg = __fmul_rn(pg, __shfl_xor_sync(0xffffffffu, pg, off));
+    if (lane == 0) {
+        const size_t gs = (static_cast<size_t>(brow) * NG + (REVERSE ? NG - 1 - g : g)) * D + d;
+        PG[gs] = pg;
+        QG[gs] = qg;
+    }
+}
+
+template <bool REVERSE, int UNROLL>
+__global__ void __launch_bounds__(256)
+chunk_group_rescan(const float *__restrict__ P, float *__restrict__ Q, const float *__restrict__ HG, int Nc, int D,
+                   int GC, int NG, long long lanes) {
+    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (wid >= lanes * NG) return;
+    const int g = static_cast<int>(wid % NG);
+    const long long ln = wid / NG;
+    const long long brow = ln / D;
+    const int d = static_cast<int>(ln - brow * D);
+    const size_t base = static_cast<size_t>(brow) * Nc * D + d;
+    const int lo = g * GC, hi = min(Nc, lo + GC);
+    const float entry = __ldcg(HG + (static_cast<size_t>(brow) * NG + (REVERSE ? NG - 1 - g : g)) * D + d);
+    scan_map_range<REVERSE, UNROLL, true>(P, Q, base, D, Nc, lo, hi, entry);
+}
+
 // ---------------------------------------------------------------- phase 3 --
 template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)

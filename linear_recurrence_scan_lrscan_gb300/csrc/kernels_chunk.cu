@@ -13,6 +13,24 @@ inline unsigned blocks_for(const ChunkGeom &g, int64_t B) {
     return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Nc * B);
 }
 
+// Phase 2: the flat warp-per-lane prefix, or (when the launch carries group
+// scratch) the grouped form: group maps, their prefix, the per-group rescan.
+template <bool REVERSE>
+void prefix_phase(const ChunkLaunch &L, const ChunkGeom &g, const float *init) {
+    const long long lanes = static_cast<long long>(L.B) * L.D;
+    if (L.PG == nullptr) {
+        const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
+        chunk_prefix<REVERSE, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes, init);
+        return;
+    }
+    const int NG = (g.Nc + kGroupChunks - 1) / kGroupChunks;
+    const unsigned gb = static_cast<unsigned>((lanes * NG * 32 + 255) / 256);
+    chunk_group_reduce<REVERSE, 4><<<gb, 256, 0, L.stream>>>(L.P, L.Q, L.PG, L.QG, g.Nc, g.D, kGroupChunks, NG, lanes);
+    const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
+    chunk_prefix<REVERSE, 4><<<pb, 256, 0, L.stream>>>(L.PG, L.QG, NG, g.D, lanes, init);
+    chunk_group_rescan<REVERSE, 4><<<gb, 256, 0, L.stream>>>(L.P, L.Q, L.QG, g.Nc, g.D, kGroupChunks, NG, lanes);
+}
+
 template <typename St, int V, int C>
 int chunk_fwd_t(const ChunkLaunch &L) {
     ChunkGeom g;
@@ -23,9 +41,7 @@ int chunk_fwd_t(const ChunkLaunch &L) {
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                           static_cast<const St *>(L.in1), L.P, L.Q, g, L.sx);
-    const long long lanes = static_cast<long long>(L.B) * L.D;
-    const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
-    chunk_prefix<false, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes, L.sx.h0);
+    prefix_phase<false>(L, g, L.sx.h0);
     chunk_replay_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                          static_cast<const St *>(L.in1), L.Q,
                                                          static_cast<St *>(L.out0), L.last, g, L.sx);
@@ -42,9 +58,7 @@ int chunk_bwd_t(const ChunkLaunch &L) {
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                           static_cast<const St *>(L.in2), L.P, L.Q, g, L.sx);
-    const long long lanes = static_cast<long long>(L.B) * L.D;
-    const unsigned pb = static_cast<unsigned>((lanes * 32 + 255) / 256);
-    chunk_prefix<true, 4><<<pb, 256, 0, L.stream>>>(L.P, L.Q, g.Nc, g.D, lanes, L.sx.grad_last);
+    prefix_phase<true>(L, g, L.sx.grad_last);
     chunk_replay_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(
         static_cast<const St *>(L.in0), static_cast<const St *>(L.in1), static_cast<const St *>(L.in2), L.Q,
         static_cast<St *>(L.out0), static_cast<St *>(L.out1), g, L.sx);

@@ -87,12 +87,15 @@ struct ChunkLaunch {
     void *out0, *out1;            // fwd: out; bwd: grad_a, grad_b
     float *last;
     float *P, *Q;                 // workspace [B, Nc, D] each
+    float *PG, *QG;               // grouped prefix: [B, ceil(Nc / kGroupChunks), D] each, or null (flat prefix)
     int64_t B, T, D;
     int chunk;                    // 16, 32, 64
     int vec;                      // lanes per thread: 1, 2, 4 (f32) / 1, 2, 4, 8 (bf16)
     cudaStream_t stream;
     StateArgs sx;                 // carried state and resets (all null: plain scan)
 };
+// Chunks per group of the grouped chunk prefix.
+constexpr int kGroupChunks = 512;
 int chunk_fwd(const ChunkLaunch &L, int dtype);
 int chunk_bwd(const ChunkLaunch &L, int dtype);
 int plain_fwd_launch(const ChunkLaunch &L, int dtype);

@@ -159,11 +159,31 @@ Occ occupancy(const WinVariant &var, int dir, int64_t B, int64_t D, const Geomet
     return o;
 }
 
-size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C) {
+// Chunk scratch: P and Q [B, Nc, D] fp32, then (grouped prefix) the group
+// maps PG and QG [B, NG, D]; each array rounded up to 256 bytes.
+struct ChunkScratch {
+    size_t pq;      // bytes of P (= of Q)
+    size_t group;   // bytes of PG (= of QG), 0 without groups
+    size_t total() const { return 2 * pq + 2 * group; }
+};
+ChunkScratch chunk_scratch(int64_t B, int64_t T, int64_t D, int C, bool grouped) {
     const int64_t nc = (T + C - 1) / C;
-    const size_t one = static_cast<size_t>(B) * nc * D * 4;
-    const size_t pad = (one + 255) / 256 * 256;
-    return pad * 2;
+    const int64_t ng = (nc + kGroupChunks - 1) / kGroupChunks;
+    auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
+    ChunkScratch s;
+    s.pq = pad(static_cast<size_t>(B) * nc * D * 4);
+    s.group = grouped ? pad(static_cast<size_t>(B) * ng * D * 4) : 0;
+    return s;
+}
+size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = true) {
+    return chunk_scratch(B, T, D, C, grouped).total();
+}
+
+// The grouped prefix pays when every lane has many chunks and the lanes alone
+// give the GPU few warps to run the flat per-lane prefix.
+bool use_grouped_prefix(int64_t B, int64_t T, int64_t D, int C, const Geometry &g) {
+    const int64_t nc = (T + C - 1) / C;
+    return nc >= 4 * kGroupChunks && B * D < 32LL * g.sm_count;
 }
 
 int pick_from_table(const WinVariant *tab, int n, int dir, int64_t B, int64_t D, const Geometry &g, int *vidx) {
@@ -311,12 +331,15 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         ch->kernels = 1;
         ch->workspace = 0;
     } else if (path == kPathChunk) {
-        if (force_v > 1) return fail(LRSCAN_EINVAL, "the chunked path has one variant");
+        // variant 1: flat per-lane prefix; variant 2: grouped prefix
+        if (force_v > 2) return fail(LRSCAN_EINVAL, "the chunked path has two variants (1 flat, 2 grouped prefix)");
+        const bool grouped = force_v ? force_v == 2 : use_grouped_prefix(B, T, D, chunk, g);
         const int64_t nc = (T + chunk - 1) / chunk;
+        ch->vidx = grouped ? 1 : 0;
         ch->ctas = B * nc * ((D / ch->vec + 127) / 128);
         ch->threads = 128;
-        ch->kernels = 3;
-        ch->workspace = chunk_workspace(B, T, D, chunk);
+        ch->kernels = grouped ? 5 : 3;
+        ch->workspace = chunk_workspace(B, T, D, chunk, grouped);
     } else {  // plain
         if (force_v > 1) return fail(LRSCAN_EINVAL, "the plain path has one variant");
         ch->ctas = B * ((D + 127) / 128);
@@ -347,7 +370,7 @@ void fill_info(const Choice &c, lrscan_plan_info *info) {
     } else if (c.path == kPathChunk) {
         info->lanes_per_cta = 128 * c.vec;
         info->rows_per_window = c.chunk;
-        std::snprintf(info->name, sizeof info->name, "chunk%d_v%d", c.chunk, c.vec);
+        std::snprintf(info->name, sizeof info->name, "chunk%d_v%d%s", c.chunk, c.vec, c.vidx == 1 ? "_grouped" : "");
     } else {
         info->lanes_per_cta = 128;
         std::snprintf(info->name, sizeof info->name, "plain");
@@ -424,6 +447,15 @@ int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opt
 }
 
 cudaStream_t pick_stream(void *stream) { return stream ? static_cast<cudaStream_t>(stream) : t_stream; }
+
+void set_chunk_scratch(ChunkLaunch *L, void *ws, const Choice &ch) {
+    const ChunkScratch sc = chunk_scratch(L->B, L->T, L->D, ch.chunk, ch.vidx == 1);
+    char *base = static_cast<char *>(ws);
+    L->P = reinterpret_cast<float *>(base);
+    L->Q = reinterpret_cast<float *>(base + sc.pq);
+    L->PG = sc.group ? reinterpret_cast<float *>(base + 2 * sc.pq) : nullptr;
+    L->QG = sc.group ? reinterpret_cast<float *>(base + 2 * sc.pq + sc.group) : nullptr;
+}
 
 // The state members a direction uses, checked: fp32 / int32 device pointers
 // must be 4-byte aligned.  *any is set when the call carries state.
@@ -520,8 +552,7 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
     if (ch.path == kPathPlain) return plain_fwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
     void *ws = nullptr;
     if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
-    L.P = static_cast<float *>(ws);
-    L.Q = reinterpret_cast<float *>(static_cast<char *>(ws) + ch.workspace / 2);
+    set_chunk_scratch(&L, ws, ch);
     rc = chunk_fwd(L, dtype);
     return rc == 0 ? LRSCAN_OK : (rc == -2 ? LRSCAN_EINVAL : LRSCAN_ECUDA);
 }
@@ -580,8 +611,7 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
     if (ch.path == kPathPlain) return plain_bwd_launch(L, dtype) ? LRSCAN_ECUDA : LRSCAN_OK;
     void *ws = nullptr;
     if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
-    L.P = static_cast<float *>(ws);
-    L.Q = reinterpret_cast<float *>(static_cast<char *>(ws) + ch.workspace / 2);
+    set_chunk_scratch(&L, ws, ch);
     rc = chunk_bwd(L, dtype);
     return rc == 0 ? LRSCAN_OK : (rc == -2 ? LRSCAN_EINVAL : LRSCAN_ECUDA);
 }

@@ -77,8 +77,10 @@ def test_empty_problems_are_noops(lib):
 
 def test_workspace_bytes(lib):
     # two fp32 [B, ceil(T/C), D] buffers, each rounded up to 256 bytes
-    assert L.lrscan_workspace_bytes(1, 65536, 2560, 64) == 2 * 1024 * 2560 * 4
-    assert L.lrscan_workspace_bytes(2, 100, 3, 16) == 2 * ((2 * 7 * 3 * 4 + 255) // 256 * 256)
+    pad = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # P and Q [B, Nc, D] plus the grouped prefix's PG and QG [B, ceil(Nc / 512), D]
+    assert L.lrscan_workspace_bytes(1, 65536, 2560, 64) == 2 * 1024 * 2560 * 4 + 2 * 2 * 2560 * 4
+    assert L.lrscan_workspace_bytes(2, 100, 3, 16) == 2 * pad(2 * 7 * 3 * 4) + 2 * pad(2 * 1 * 3 * 4)
     assert L.lrscan_workspace_bytes(1, 64, 8, 0) == L.lrscan_workspace_bytes(1, 64, 8, 64)
     assert L.lrscan_workspace_bytes(1, 64, 8, 48) == 0
 
@@ -120,8 +122,14 @@ def test_bf16_forward_takes_the_one_wave_window_tile(lib):
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
-    assert p["path"] == "chunk" and p["kernels"] == 3
+    # 16,384 chunks per lane and only 64 lanes: the grouped prefix (5 kernels)
+    assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
+    flat = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", path="chunk", tile_variant=1)
+    assert flat["kernels"] == 3 and flat["workspace_bytes"] == 2 * 16384 * 64 * 4
+    # few chunks per lane: the flat prefix
+    p = L.lrscan_plan(1, 4096, 64, "f32", "fwd", path="chunk")
+    assert p["kernels"] == 3 and not p["name"].endswith("_grouped")
 
 
 def test_unaligned_rows_take_plain_loads(lib):

@@ -363,3 +363,18 @@ def test_autograd_wrapper_matches_direct_calls():
     ga, gb = L.lrscan_bwd(a.detach(), out2, g)
     assert torch.equal(out, out2)
     assert torch.equal(a.grad, ga) and torch.equal(b.grad, gb)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape,chunk", [((2, 40000, 8), 16), ((1, 70001, 16), 32)])
+def test_chunk_grouped_prefix(dt, shape, chunk):
+    """The grouped chunk prefix (group maps, their prefix, per-group rescan;
+    several groups and a ragged last group) against the oracle, forced and
+    as the automatic choice, next to the flat prefix."""
+    B, T, D = shape
+    inp = random_inputs(B, T, D, dt, seed=600 + T, a_lo=0.9, a_hi=1.0)
+    plan, planb = check_case(inp, path="chunk", chunk_len=chunk, tile_variant=2)
+    assert plan["name"].endswith("_grouped") and plan["kernels"] == 5
+    check_case(inp, path="chunk", chunk_len=chunk, tile_variant=1)
+    auto = L.lrscan_plan(B, T, D, dt, "fwd", path="chunk", chunk_len=chunk)
+    assert auto["name"].endswith("_grouped")

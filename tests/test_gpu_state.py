@@ -226,3 +226,11 @@ def test_scan_state_autograd(dt):
     assert_close(to_np(a.grad), ref_ga, dt, "autograd grad_a", reassociated=True)
     assert_close(to_np(b.grad), ref_gb, dt, "autograd grad_b", reassociated=True)
     assert_last_close(h0.grad.cpu().numpy(), ref_gh0, "autograd grad_h0")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_state_on_the_grouped_chunk_prefix(dt):
+    """h0 and grad_last enter through the grouped prefix's group-level scan."""
+    inp = state_inputs(2, 40000, 8, dt, seed=390)
+    plan, planb = check_state_case(inp, path="chunk", chunk_len=16, tile_variant=2)
+    assert plan["kernels"] == 5 and planb["kernels"] == 5
