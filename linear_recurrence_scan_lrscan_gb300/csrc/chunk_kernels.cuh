@@ -52,17 +52,29 @@ __device__ __forceinline__ void load_decay(const St *p, const StateArgs &sx, int
 }
 
 struct ChunkGeom {
-    int T, D, Nc, nlb;  // nlb: lane blocks per (row, chunk)
+    int T, D, Nc;
+    int nlb;   // lane blocks per (row, chunk block)
+    int lt;    // threads per chunk row: 128, or ceil(D / V) when that is at most 64
+    int cpb;   // chunks per CTA: 128 / lt (several chunks share a CTA when D is small)
+    int Ncb;   // chunk blocks per row: ceil(Nc / cpb)
 };
 
-// Linear CTA index -> (row, chunk, lane block); consecutive CTAs take
-// neighbouring lanes of the same chunk.
-__device__ __forceinline__ void chunk_coords(const ChunkGeom &g, int &brow, int &c, int &lb) {
+// Linear CTA index -> (row, chunk block, lane block); consecutive CTAs take
+// neighbouring lanes of the same chunk block.  Within the CTA, thread t works
+// on chunk (block * cpb + t / lt) and lanes ((lane block * lt + t % lt) * V ...).
+// Returns false for threads with no chunk or lane.
+template <int V>
+__device__ __forceinline__ bool chunk_thread(const ChunkGeom &g, int &brow, int &c, int &d) {
     const unsigned idx = blockIdx.x;
-    lb = static_cast<int>(idx % g.nlb);
+    const int lb = static_cast<int>(idx % g.nlb);
     const unsigned rc = idx / g.nlb;
-    c = static_cast<int>(rc % g.Nc);
-    brow = static_cast<int>(rc / g.Nc);
+    const int cb = static_cast<int>(rc % g.Ncb);
+    brow = static_cast<int>(rc / g.Ncb);
+    const int sub = static_cast<int>(threadIdx.x) / g.lt;
+    if (sub >= g.cpb) return false;
+    c = cb * g.cpb + sub;
+    d = (lb * g.lt + static_cast<int>(threadIdx.x) - sub * g.lt) * V;
+    return c < g.Nc && d < g.D;
 }
 
 template <int V>
@@ -75,10 +87,8 @@ template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_summary_fwd(const St *__restrict__ a, const St *__restrict__ b, float *__restrict__ P,
                   float *__restrict__ Q, ChunkGeom g, const StateArgs sx) {
-    int brow, c, lb;
-    chunk_coords(g, brow, c, lb);
-    const int d = (lb * 128 + threadIdx.x) * V;
-    if (d >= g.D) return;
+    int brow, c, d;
+    if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
@@ -112,10 +122,8 @@ template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_summary_bwd(const St *__restrict__ a, const St *__restrict__ grad_out, float *__restrict__ P,
                   float *__restrict__ Q, ChunkGeom g, const StateArgs sx) {
-    int brow, c, lb;
-    chunk_coords(g, brow, c, lb);
-    const int d = (lb * 128 + threadIdx.x) * V;
-    if (d >= g.D) return;
+    int brow, c, d;
+    if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
@@ -329,10 +337,8 @@ template <typename St, int V, int C>
 __global__ void __launch_bounds__(128)
 chunk_replay_fwd(const St *__restrict__ a, const St *__restrict__ b, const float *__restrict__ Hin,
                  St *__restrict__ out, float *__restrict__ last, ChunkGeom g, const StateArgs sx) {
-    int brow, c, lb;
-    chunk_coords(g, brow, c, lb);
-    const int d = (lb * 128 + threadIdx.x) * V;
-    if (d >= g.D) return;
+    int brow, c, d;
+    if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
@@ -373,10 +379,8 @@ __global__ void __launch_bounds__(128)
 chunk_replay_bwd(const St *__restrict__ a, const St *__restrict__ out, const St *__restrict__ grad_out,
                  const float *__restrict__ Gin, St *__restrict__ grad_a, St *__restrict__ grad_b,
                  ChunkGeom g, const StateArgs sx) {
-    int brow, c, lb;
-    chunk_coords(g, brow, c, lb);
-    const int d = (lb * 128 + threadIdx.x) * V;
-    if (d >= g.D) return;
+    int brow, c, d;
+    if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;

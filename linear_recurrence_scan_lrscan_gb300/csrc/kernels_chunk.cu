@@ -10,7 +10,30 @@ namespace lrscan {
 namespace {
 
 inline unsigned blocks_for(const ChunkGeom &g, int64_t B) {
-    return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Nc * B);
+    return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Ncb * B);
+}
+
+// Chunk geometry: 128-thread CTAs; when a chunk row needs at most 64 threads
+// (D / V <= 64), one CTA takes 128 / lt chunks so that no thread idles.
+inline ChunkGeom chunk_geom(const ChunkLaunch &L, int C, int V) {
+    ChunkGeom g;
+    g.T = static_cast<int>(L.T);
+    g.D = static_cast<int>(L.D);
+    g.Nc = static_cast<int>((L.T + C - 1) / C);
+    const int row_threads = static_cast<int>((L.D + V - 1) / V);
+    if (row_threads <= 64) {
+        int lt = 1;
+        while (lt < row_threads) lt <<= 1;
+        g.lt = lt;
+        g.cpb = 128 / lt;
+        g.nlb = 1;
+    } else {
+        g.lt = 128;
+        g.cpb = 1;
+        g.nlb = (row_threads + 127) / 128;
+    }
+    g.Ncb = (g.Nc + g.cpb - 1) / g.cpb;
+    return g;
 }
 
 // Phase 2: the flat warp-per-lane prefix, or (when the launch carries group
@@ -33,11 +56,7 @@ void prefix_phase(const ChunkLaunch &L, const ChunkGeom &g, const float *init) {
 
 template <typename St, int V, int C>
 int chunk_fwd_t(const ChunkLaunch &L) {
-    ChunkGeom g;
-    g.T = static_cast<int>(L.T);
-    g.D = static_cast<int>(L.D);
-    g.Nc = static_cast<int>((L.T + C - 1) / C);
-    g.nlb = static_cast<int>((L.D / V + 127) / 128);
+    const ChunkGeom g = chunk_geom(L, C, V);
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_fwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                           static_cast<const St *>(L.in1), L.P, L.Q, g, L.sx);
@@ -50,11 +69,7 @@ int chunk_fwd_t(const ChunkLaunch &L) {
 
 template <typename St, int V, int C>
 int chunk_bwd_t(const ChunkLaunch &L) {
-    ChunkGeom g;
-    g.T = static_cast<int>(L.T);
-    g.D = static_cast<int>(L.D);
-    g.Nc = static_cast<int>((L.T + C - 1) / C);
-    g.nlb = static_cast<int>((L.D / V + 127) / 128);
+    const ChunkGeom g = chunk_geom(L, C, V);
     const unsigned nb = blocks_for(g, L.B);
     chunk_summary_bwd<St, V, C><<<nb, 128, 0, L.stream>>>(static_cast<const St *>(L.in0),
                                                           static_cast<const St *>(L.in2), L.P, L.Q, g, L.sx);

@@ -336,7 +336,13 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         const bool grouped = force_v ? force_v == 2 : use_grouped_prefix(B, T, D, chunk, g);
         const int64_t nc = (T + chunk - 1) / chunk;
         ch->vidx = grouped ? 1 : 0;
-        ch->ctas = B * nc * ((D / ch->vec + 127) / 128);
+        // 128-thread CTAs; several chunks per CTA when a chunk row needs <= 64 threads
+        const int64_t row_threads = (D + ch->vec - 1) / ch->vec;
+        int64_t lt = 1;
+        while (lt < row_threads && lt < 128) lt <<= 1;
+        const int64_t cpb = row_threads <= 64 ? 128 / lt : 1;
+        const int64_t nlb = row_threads <= 64 ? 1 : (row_threads + 127) / 128;
+        ch->ctas = B * ((nc + cpb - 1) / cpb) * nlb;
         ch->threads = 128;
         ch->kernels = grouped ? 5 : 3;
         ch->workspace = chunk_workspace(B, T, D, chunk, grouped);
