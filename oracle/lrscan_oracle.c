@@ -604,3 +604,111 @@ int lro_cbwd_f64(const double *ar, const double *ai, const double *out_r,
 {
     CPLX_BWD_BODY(double, fma, LRO_SAME, LRO_SAME)
 }
+
+/* ---------------------------------------------------------------------- */
+/* Generated (factorized) decay.                                           */
+/*                                                                         */
+/* triton_training_scan.py, _samu_forward / _samu_precompute_decay: the   */
+/* decay of mode d at token t is rebuilt from one value per token and one  */
+/* per mode instead of being read from memory,                             */
+/*   nu_d = exp(nu_log_d),  E_t = exp(eta_t),  a_{t,d} = exp(-nu_d * E_t)   */
+/* (the radius part of the page's transition), and the scan is the real    */
+/* one: h_t = a_t * h_{t-1} + b_t.  eta is [B,T], nu_log [D] (both in the  */
+/* state precision).  Backward, for L = sum_t grad_out_t * h_t:            */
+/*   g as in the plain backward; grad_b = g;                               */
+/*   with grad_a_t = g_t * out_{t-1} (out_{-1} = 0) and                     */
+/*   q_{t,d} = grad_a_{t,d} * a_{t,d} * (-nu_d * E_t)   (= d L / d log a),  */
+/*   grad_eta[b,t] = sum_d q,   grad_nu_log[d] = sum_{b,t} q.              */
+/* Every product is rounded in the state precision; the sums accumulate in  */
+/* double and are rounded once.                                             */
+/* ---------------------------------------------------------------------- */
+
+#define GATED_FWD_BODY(STATE, EXP, FMA, LOAD, STORE)                           \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE nu = EXP(nu_log[d]);                                         \
+            STATE h = 0;                                                       \
+            for (int64_t t = 0; t < T; ++t) {                                  \
+                int64_t i = (bb * T + t) * D + d;                              \
+                STATE e = EXP(eta[bb * T + t]);                                \
+                STATE la = -(nu * e);                                          \
+                h = FMA(EXP(la), h, LOAD(b[i]));                               \
+                out[i] = STORE(h);                                             \
+            }                                                                  \
+            if (last) last[bb * D + d] = h;                                    \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define GATED_BWD_BODY(STATE, EXP, FMA, LOAD, STORE)                           \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    double *acc_eta = calloc((size_t)(B * T > 0 ? B * T : 1), sizeof *acc_eta); \
+    double *acc_nu = calloc((size_t)(D > 0 ? D : 1), sizeof *acc_nu);          \
+    if (!acc_eta || !acc_nu) { free(acc_eta); free(acc_nu); return LRO_ENOMEM; } \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE nu = EXP(nu_log[d]);                                         \
+            STATE g = 0, a_next = 0;                                           \
+            for (int64_t t = T - 1; t >= 0; --t) {                             \
+                int64_t i = (bb * T + t) * D + d;                              \
+                STATE e = EXP(eta[bb * T + t]);                                \
+                STATE la = -(nu * e);                                          \
+                STATE a = EXP(la);                                             \
+                g = (t == T - 1) ? LOAD(grad_out[i])                           \
+                                 : FMA(a_next, g, LOAD(grad_out[i]));          \
+                STATE h_prev = (t > 0) ? LOAD(out[i - D]) : 0;                 \
+                STATE grad_a = g * h_prev;                                     \
+                STATE q = (grad_a * a) * la;                                   \
+                grad_b[i] = STORE(g);                                          \
+                acc_eta[bb * T + t] += (double)q;                              \
+                acc_nu[d] += (double)q;                                        \
+                a_next = a;                                                    \
+            }                                                                  \
+        }                                                                      \
+    }                                                                          \
+    for (int64_t k = 0; k < B * T; ++k) grad_eta[k] = (STATE)acc_eta[k];       \
+    for (int64_t d = 0; d < D; ++d) grad_nu_log[d] = (STATE)acc_nu[d];         \
+    free(acc_eta);                                                             \
+    free(acc_nu);                                                              \
+    return LRO_OK;
+
+int lro_gated_fwd_f32(const float *eta, const float *nu_log, const float *b,
+                      float *out, float *last, int64_t B, int64_t T, int64_t D)
+{
+    GATED_FWD_BODY(float, expf, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_gated_fwd_bf16(const float *eta, const float *nu_log, const uint16_t *b,
+                       uint16_t *out, float *last, int64_t B, int64_t T, int64_t D)
+{
+    GATED_FWD_BODY(float, expf, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_gated_fwd_f64(const double *eta, const double *nu_log, const double *b,
+                      double *out, double *last, int64_t B, int64_t T, int64_t D)
+{
+    GATED_FWD_BODY(double, exp, fma, LRO_SAME, LRO_SAME)
+}
+
+int lro_gated_bwd_f32(const float *eta, const float *nu_log, const float *out,
+                      const float *grad_out, float *grad_b, float *grad_eta,
+                      float *grad_nu_log, int64_t B, int64_t T, int64_t D)
+{
+    GATED_BWD_BODY(float, expf, fmaf, LRO_SAME, LRO_SAME)
+}
+
+int lro_gated_bwd_bf16(const float *eta, const float *nu_log, const uint16_t *out,
+                       const uint16_t *grad_out, uint16_t *grad_b, float *grad_eta,
+                       float *grad_nu_log, int64_t B, int64_t T, int64_t D)
+{
+    GATED_BWD_BODY(float, expf, fmaf, lro_bf16_to_f32, lro_f32_to_bf16)
+}
+
+int lro_gated_bwd_f64(const double *eta, const double *nu_log,
+                      const double *out, const double *grad_out,
+                      double *grad_b, double *grad_eta, double *grad_nu_log,
+                      int64_t B, int64_t T, int64_t D)
+{
+    GATED_BWD_BODY(double, exp, fma, LRO_SAME, LRO_SAME)
+}

@@ -77,6 +77,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lro_cbwd_f32", "lro_cbwd_bf16", "lro_cbwd_f64"):
         getattr(lib, name).argtypes = [_P] * 10 + [_I64, _I64, _I64]
         getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_gated_fwd_f32", "lro_gated_fwd_bf16", "lro_gated_fwd_f64"):
+        getattr(lib, name).argtypes = [_P] * 5 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_gated_bwd_f32", "lro_gated_bwd_bf16", "lro_gated_bwd_f64"):
+        getattr(lib, name).argtypes = [_P] * 7 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
     lib.lro_f32_to_bf16_array.argtypes = [_P, _P, _I64]
     lib.lro_bf16_to_f32_array.argtypes = [_P, _P, _I64]
     lib.lro_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -253,6 +259,41 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle complex backward failed ({rc})")
         return tuple(gs)
+
+    def _gated_params(self, eta, nu_log, dtype, B, T, D):
+        want = _LAST[dtype]
+        eta = np.ascontiguousarray(eta)
+        nu_log = np.ascontiguousarray(nu_log)
+        if eta.dtype != want or eta.shape != (B, T) or nu_log.dtype != want or nu_log.shape != (D,):
+            raise TypeError(f"eta must be {np.dtype(want).name} [B, T] and nu_log {np.dtype(want).name} [D]")
+        return eta, nu_log
+
+    def gated_fwd(self, eta, nu_log, b, dtype="f32"):
+        """Scan with the decay generated as exp(-exp(nu_log_d) * exp(eta_t)); ``(out, last)``."""
+        b = _c(b, dtype)
+        B, T, D = b.shape
+        eta, nu_log = self._gated_params(eta, nu_log, dtype, B, T, D)
+        out = np.empty_like(b)
+        last = np.empty((B, D), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_gated_fwd_{dtype}")(_ptr(eta), _ptr(nu_log), _ptr(b), _ptr(out), _ptr(last),
+                                                          B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle gated forward failed ({rc})")
+        return out, last
+
+    def gated_bwd(self, eta, nu_log, out, grad_out, dtype="f32"):
+        """Reverse of :meth:`gated_fwd`; ``(grad_b, grad_eta, grad_nu_log)``."""
+        out, grad_out = _c(out, dtype), _c(grad_out, dtype)
+        B, T, D = out.shape
+        eta, nu_log = self._gated_params(eta, nu_log, dtype, B, T, D)
+        gb = np.empty_like(out)
+        geta = np.empty((B, T), dtype=_LAST[dtype])
+        gnu = np.empty((D,), dtype=_LAST[dtype])
+        rc = getattr(self.lib, f"lro_gated_bwd_{dtype}")(_ptr(eta), _ptr(nu_log), _ptr(out), _ptr(grad_out),
+                                                          _ptr(gb), _ptr(geta), _ptr(gnu), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle gated backward failed ({rc})")
+        return gb, geta, gnu
 
     def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
         x = np.ascontiguousarray(x, dtype=np.float32)

@@ -835,4 +835,93 @@ def pin_complex_identity_padding(o):
             assert not np.any(x[bb, n:])
 
 
+# ---------------------------------------------- generated (factorized) decay --
+# a_{t,d} = exp(-exp(nu_log_d) * exp(eta_t)), rebuilt in the kernel from one
+# value per token and one per lane; gradients flow to b, eta and nu_log.
+
+def _gcase(seed, B, T, D, dtype=np.float64):
+    r = _rng(seed)
+    eta = r.uniform(-3.0, 1.0, (B, T)).astype(dtype)
+    nu_log = r.uniform(-3.0, 0.5, (D,)).astype(dtype)
+    b = r.standard_normal((B, T, D)).astype(dtype)
+    g = r.standard_normal((B, T, D)).astype(dtype)
+    return eta, nu_log, b, g
+
+
+def _decay(eta, nu_log):
+    return np.exp(-np.exp(nu_log)[None, None, :] * np.exp(eta)[:, :, None])
+
+
+def pin_gated_equals_materialized_decay(o):
+    """The generated-decay scan equals the plain scan of the materialized
+    decays (numpy), and its parameter gradients equal the chain rule applied
+    to the plain backward's grad_a: dL/dlog a = grad_a * a, d log a / d eta =
+    d log a / d nu_log = log a."""
+    eta, nu_log, b, g = _gcase(50, 2, 60, 5)
+    a = _decay(eta, nu_log)
+    out, last = o.gated_fwd(eta, nu_log, b, "f64")
+    ref, ref_last = o.fwd(a, b, "f64")
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(last, ref_last, rtol=1e-12, atol=1e-13)
+    gb, geta, gnu = o.gated_bwd(eta, nu_log, out, g, "f64")
+    ga, rgb = o.bwd(a, out, g, "f64")
+    np.testing.assert_allclose(gb, rgb, rtol=1e-12, atol=1e-13)
+    q = ga * a * np.log(a)
+    np.testing.assert_allclose(geta, q.sum(axis=2), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gnu, q.sum(axis=(0, 1)), rtol=1e-10, atol=1e-12)
+
+
+def pin_gated_finite_difference(o):
+    """Central differences of L = sum grad_out*h with respect to eta, nu_log
+    and b against the backward (fp64)."""
+    eta, nu_log, b, g = _gcase(51, 2, 7, 3)
+    out, _ = o.gated_fwd(eta, nu_log, b, "f64")
+    gb, geta, gnu = o.gated_bwd(eta, nu_log, out, g, "f64")
+    eps = 1e-6
+
+    def loss(e, n, bb):
+        h, _ = o.gated_fwd(e, n, bb, "f64")
+        return float(np.sum(g * h))
+    for arr, grad, k in ((eta, geta, 0), (nu_log, gnu, 1), (b, gb, 2)):
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            args_p = [eta, nu_log, b]
+            args_m = [eta, nu_log, b]
+            args_p[k], args_m[k] = p, m
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * (1 + abs(fd)), (k, idx, fd, grad[idx])
+
+
+def pin_gated_zero_rate_is_prefix_sum(o):
+    """nu = 0 (nu_log = -inf): every decay is exactly 1, h is the running sum
+    of b, and the rate gradients vanish exactly."""
+    r = _rng(52)
+    B, T, D = 2, 30, 4
+    b = r.integers(-8, 9, (B, T, D)).astype(np.float32)
+    g = r.integers(-8, 9, (B, T, D)).astype(np.float32)
+    eta = r.uniform(-2, 2, (B, T)).astype(np.float32)
+    nu_log = np.full((D,), -np.inf, dtype=np.float32)
+    out, last = o.gated_fwd(eta, nu_log, b, "f32")
+    assert np.array_equal(out, np.cumsum(b, axis=1))
+    gb, geta, gnu = o.gated_bwd(eta, nu_log, out, g, "f32")
+    assert np.array_equal(gb, np.flip(np.cumsum(np.flip(g, axis=1), axis=1), axis=1))
+    assert not np.any(geta) and not np.any(gnu)
+
+
+def pin_gated_bf16_storage_is_fp32_state(o):
+    """bf16 storage only rounds the stored tensors: the bf16 variant equals
+    the fp32 one on widened inputs with its stores rounded."""
+    eta, nu_log, b, g = _gcase(53, 2, 50, 8, dtype=np.float32)
+    b16, g16 = o.f32_to_bf16(b), o.f32_to_bf16(g)
+    out16, last16 = o.gated_fwd(eta, nu_log, b16, "bf16")
+    out32, last32 = o.gated_fwd(eta, nu_log, o.bf16_to_f32(b16), "f32")
+    assert np.array_equal(out16, o.f32_to_bf16(out32)) and np.array_equal(last16, last32)
+    r16 = o.gated_bwd(eta, nu_log, out16, g16, "bf16")
+    r32 = o.gated_bwd(eta, nu_log, o.bf16_to_f32(out16), o.bf16_to_f32(g16), "f32")
+    assert np.array_equal(r16[0], o.f32_to_bf16(r32[0]))
+    assert np.array_equal(r16[1], r32[1]) and np.array_equal(r16[2], r32[2])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -59,6 +59,13 @@ MUTANTS = {
                                       "grad_ai[i] = STORE(FMA(gi, pr, gr * pi));"),
     "complex_grad_a_drops_cross_term": ("grad_ar[i] = STORE(FMA(gr, pr, gi * pi));",
                                         "grad_ar[i] = STORE(gr * pr);"),
+    "gated_rate_sign": ("STATE la = -(nu * e);                                          \\\n                h = FMA",
+                        "STATE la = nu * e;                                             \\\n                h = FMA"),
+    "gated_bwd_rate_not_exponentiated": ("STATE nu = EXP(nu_log[d]);                                         \\\n            STATE g = 0",
+                                         "STATE nu = nu_log[d];                                              \\\n            STATE g = 0"),
+    "gated_q_drops_decay": ("STATE q = (grad_a * a) * la;", "STATE q = grad_a * la;"),
+    "gated_nu_overwrites": ("acc_nu[d] += (double)q;", "acc_nu[d] = (double)q;"),
+    "gated_carry_uses_a_t": (": FMA(a_next, g, LOAD(grad_out[i]));", ": FMA(a, g, LOAD(grad_out[i]));"),
 }
 
 
