@@ -210,6 +210,39 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
                         const lrscan_opts *opts, lrscan_plan_info *info);
 
 /*
+ * Scan with a generated decay (triton_training_scan.py, _samu_forward and
+ * _samu_precompute_decay, the radius part of the page's transition): the
+ * decay of lane d at token t is rebuilt in the kernel instead of being read,
+ *
+ *   a_{b,t,d} = exp(-exp(nu_log[d]) * exp(eta[b,t])),   h_t = a_t * h_{t-1} + b_t,
+ *
+ * eta fp32 [B, T] (one value per token, shared by all lanes), nu_log fp32 [D]
+ * (one per lane).  Forward moves 2 elements per (t, d) (b in, out out) instead
+ * of 3.  Backward, for L = sum_t grad_out_t * h_t (out read back for h_{t-1}),
+ * writes grad_b [B, T, D] (storage dtype) and the parameter gradients
+ *   grad_eta[b,t]  = sum_d q,   grad_nu_log[d] = sum_{b,t} q,
+ *   q = grad_a * a * log a,  grad_a = g_t * out_{t-1},  log a = -exp(nu_log) exp(eta),
+ * both fp32, summed in a fixed order (deterministic); it moves 3 elements per
+ * (t, d).  Exponentials take the hardware's fast path (relative error of a few
+ * 1e-7), so results agree with an exact evaluation to rounding, not bit for bit.
+ * The backward needs lrscan_gated_workspace_bytes(B, T, D) bytes of scratch:
+ * library-owned per (device, stream), or opts->workspace.  Paths:
+ * LRSCAN_PATH_SEQ (tiled, 16-byte aligned rows) or LRSCAN_PATH_PLAIN; auto
+ * picks seq when it can.  With T == 0 the forward sets last to 0 and the
+ * backward sets grad_nu_log to 0.
+ */
+int lrscan_fwd_gated(const float *eta, const float *nu_log, const void *b, void *out, float *last,
+                     int64_t B, int64_t T, int64_t D, int dtype,
+                     void *stream, const lrscan_opts *opts);
+int lrscan_bwd_gated(const float *eta, const float *nu_log, const void *out, const void *grad_out,
+                     void *grad_b, float *grad_eta, float *grad_nu_log,
+                     int64_t B, int64_t T, int64_t D, int dtype,
+                     void *stream, const lrscan_opts *opts);
+size_t lrscan_gated_workspace_bytes(int64_t B, int64_t T, int64_t D);
+int lrscan_plan_gated(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
+                      const lrscan_opts *opts, lrscan_plan_info *info);
+
+/*
  * Whole-sequence affine summary of every lane (the chunk summary of
  * triton_training_scan.py, _real_chunk_summary and its reverse mirror, with
  * one chunk spanning all T steps).  With a'_t = 0 where segment_pos[b,t] == 0

@@ -5,7 +5,8 @@
 
 its state-carrying form (initial state h0, segment resets, gradients of the
 final and initial states: ``scan_state``), the complex scan on re/im planes
-(``complex_scan``), and the pieces of a sequence split across devices
+(``complex_scan``), the scan with decays generated in the kernel from
+per-token and per-lane parameters (``gated_scan``), and the pieces of a sequence split across devices
 (``lrscan_summary``, ``lrscan_compose_maps``, module ``tsplit``).
 
 The compute path is liblrscan.so (hand-written sm_103a CUDA kernels behind a C
@@ -15,21 +16,27 @@ it has not been built.
 """
 from .lrscan import (  # noqa: F401
     ComplexScan,
+    GatedScan,
     LinearRecurrenceScan,
     LinearRecurrenceScanState,
     LrscanError,
     LrscanUnavailable,
     complex_scan,
+    gated_scan,
+    lrscan_bwd_gated,
     lrscan_cbwd,
     lrscan_cfwd,
     lrscan_compose_maps,
     lrscan_bwd,
     lrscan_bwd_state,
     lrscan_fwd,
+    lrscan_fwd_gated,
     lrscan_fwd_state,
+    lrscan_gated_workspace_bytes,
     lrscan_num_variants,
     lrscan_plan,
     lrscan_plan_complex,
+    lrscan_plan_gated,
     lrscan_selftest_wait_timeout,
     lrscan_set_wait_timeout_ns,
     lrscan_summary,

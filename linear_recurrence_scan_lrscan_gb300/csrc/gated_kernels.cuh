@@ -1,0 +1,328 @@
+// Scan with a generated decay (triton_training_scan.py, _samu_forward and
+// _samu_precompute_decay, radius part): the decay of lane d at token t is
+// rebuilt in the kernel from one value per token and one per lane,
+//
+//   nu_d = exp(nu_log_d),  E_t = exp(eta_t),  a_{t,d} = exp(-nu_d * E_t),
+//   h_t = a_t * h_{t-1} + b_t                  (one fma per step)
+//
+// so the forward streams b and out (2 elements per (t, d)) instead of a, b
+// and out, and the backward streams out and grad_out in and grad_b out (3
+// instead of 5).  Backward, with grad_a = g * out_{t-1} and
+// q = grad_a * a * (-nu * E) (= dL / dlog a):
+//   grad_eta[b,t] = sum_d q,   grad_nu_log[d] = sum_{b,t} q.
+// Exponentials use the fast hardware path (__expf), as the page's tl.exp does.
+//
+// Tiled sequential kernels (S = 1, L = 32 rows per window): lane j of each
+// warp computes E for row j of the window (its eta loaded two windows ahead)
+// and every row takes it with one shuffle.  The backward accumulates q per
+// row in registers and reduces the warp's 32 rows x 32 lanes with a
+// transpose-sum (31 shuffles per window: afterwards lane j holds row j's sum
+// over the warp's lanes), written as one partial per (row, warp); q is also
+// summed per thread over time for grad_nu_log, written per (batch row,
+// lane).  gated_finish sums both partial sets (fixed order: deterministic).
+#pragma once
+
+#include "window_kernels.cuh"
+
+namespace lrscan {
+
+__device__ __forceinline__ float eta_at(const float *row, int t, int T) {
+    return (t >= 0 && t < T) ? __ldg(row + t) : 0.0f;
+}
+
+// After the call, lane l holds sum over the warp's lanes of v[l] (v has 32
+// entries per lane): halves of the remaining entries are exchanged with the
+// partner lane at distance 16, 8, 4, 2, 1.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = upper ? v[i] : v[i + w];
+            const float keep = upper ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ eta,
+                const float *__restrict__ nu_log, typename C::St *__restrict__ out, float *__restrict__ last,
+                const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+    static_assert(C::SEQ && C::NIN == 1 && C::L == 32 && C::G % 32 == 0,
+                  "generated-decay forward: sequential, one plane, 32-row windows, whole warps");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int NT = G;
+    win_init<C>(sm, NT / 32, 1);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[1] = {&tm_b};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
+        }
+        return;
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + threadIdx.x * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    const float *eta_row = eta + row0;
+    float nu[V], h[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        h[v] = 0.0f;
+    }
+    float eta1 = eta_at(eta_row, lane, T), eta2 = eta_at(eta_row, L + lane, T);  // windows k, k+1
+    bool failed = false;
+    int stage = 0, use = 0;
+    const int off = threadIdx.x * V;
+    for (int k = 0; k < sm.nwin; ++k) {
+        const float e_lane = __expf(eta1);  // E of row k*L + lane
+        eta1 = eta2;
+        eta2 = eta_at(eta_row, (k + 2) * L + lane, T);
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) { failed = true; break; }
+        const St *tb = sm.tile<C>(stage, 0) + off;
+        const int rbase = k * L;
+        const int n = min(T - rbase, L);
+        const size_t o = (row0 + rbase) * D + d;
+        auto step = [&](int j, const float (&y)[V]) {
+            const float e = __shfl_sync(0xffffffffu, e_lane, j);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float a = __expf(-__fmul_rn(nu[v], e));
+                h[v] = __fmaf_rn(a, h[v], y[v]);
+            }
+            if (lane_ok) store_lanes<St, V>(out + o + static_cast<size_t>(j) * D, h);
+        };
+        if (n == L) {
+            using Raw = typename RawOf<St, V>::T;
+            Raw rb[L];
+#pragma unroll
+            for (int j = 0; j < L; ++j) rb[j] = load_raw<St, V>(tb + j * DT);
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                float y[V];
+                widen_raw(rb[j], y);
+                step(j, y);
+            }
+        } else {
+            for (int j = 0; j < n; ++j) {
+                float y[V];
+                unpack_lanes<St, V>(tb + j * DT, y);
+                step(j, y);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+    }
+    if (!failed && lane_ok && last != nullptr) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+    }
+}
+
+// Backward.  Tiles: out one row early (h_{t-1}; zero fill before t = 0) and
+// grad_out.  part_eta: [B*T][ncol] with ncol = gridDim.x * (G / 32) warp
+// columns; part_nu: [B][D].
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_go,
+                const float *__restrict__ eta, const float *__restrict__ nu_log, typename C::St *__restrict__ grad_b,
+                float *__restrict__ part_eta, float *__restrict__ part_nu, const __grid_constant__ WinGeom geom,
+                DevStatus *status, uint64_t timeout_ns) {
+    static_assert(C::SEQ && C::NIN == 2 && C::L == 32 && C::G % 32 == 0,
+                  "generated-decay backward: sequential, two planes, 32-row windows, whole warps");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int NT = G;
+    win_init<C>(sm, NT / 32, 1);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+    const int nwin = sm.nwin;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[2] = {&tm_out, &tm_go};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow,
+                            [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i == 0 ? -1 : 0); }, wc);
+        }
+        return;
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + threadIdx.x * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    const float *eta_row = eta + row0;
+    const int ncol = gridDim.x * (G / 32);
+    const int col = blockIdx.x * (G / 32) + static_cast<int>(threadIdx.x) / 32;
+    float nu[V], g[V], a_next[V], acc_nu[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        g[v] = 0.0f;
+        a_next[v] = 0.0f;  // a_T: nothing enters past the end
+        acc_nu[v] = 0.0f;
+    }
+    float eta1 = eta_at(eta_row, (nwin - 1) * L + lane, T), eta2 = eta_at(eta_row, (nwin - 2) * L + lane, T);
+    bool failed = false;
+    int stage = 0, use = 0;
+    const int off = threadIdx.x * V;
+    for (int k = 0; k < nwin; ++k) {
+        const float e_lane = __expf(eta1);
+        eta1 = eta2;
+        eta2 = eta_at(eta_row, (nwin - 3 - k) * L + lane, T);
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) { failed = true; break; }
+        const St *th = sm.tile<C>(stage, 0) + off;  // h_{t-1}
+        const St *tg = sm.tile<C>(stage, 1) + off;  // grad_out_t
+        const int wbase = (nwin - 1 - k) * L;
+        const int n = min(T - wbase, L);
+        const size_t o = (row0 + wbase) * D + d;
+        float qrow[L];
+        // rows past T (only in the sequence's last window) are zero-filled:
+        // g stays 0 through them and their q is 0; nothing of theirs is stored
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+            float hp[V], go[V], gav[V];
+            unpack_lanes<St, V>(th + j * DT, hp);
+            unpack_lanes<St, V>(tg + j * DT, go);
+            const float e = __shfl_sync(0xffffffffu, e_lane, j);
+            float qs = 0.0f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float la = -__fmul_rn(nu[v], e);
+                const float a = __expf(la);
+                g[v] = __fmaf_rn(a_next[v], g[v], go[v]);
+                gav[v] = __fmul_rn(g[v], hp[v]);
+                const float q = __fmul_rn(__fmul_rn(gav[v], a), la);
+                acc_nu[v] += q;
+                qs += q;
+                a_next[v] = a;
+            }
+            qrow[j] = qs;
+            if (lane_ok && (n == L || j < n)) store_lanes<St, V>(grad_b + o + static_cast<size_t>(j) * D, g);
+        }
+        const float rsum = warp_transpose_sum(qrow);  // row wbase + lane
+        if (lane < n) part_eta[(row0 + wbase + lane) * ncol + col] = rsum;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+    }
+    if (!failed && lane_ok) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) part_nu[static_cast<size_t>(brow) * D + d + v] = acc_nu[v];
+    }
+}
+
+// grad_eta[r] = sum over the ncol partials of row r (r < rows);
+// grad_nu_log[d] = sum over the B partials of lane d.
+__global__ void __launch_bounds__(256)
+gated_finish(const float *__restrict__ part_eta, const float *__restrict__ part_nu, float *__restrict__ grad_eta,
+             float *__restrict__ grad_nu_log, long long rows, int ncol, int B, int D) {
+    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (i < rows) {
+        const float *p = part_eta + i * ncol;
+        float s = 0.0f;
+        for (int c = 0; c < ncol; ++c) s += p[c];
+        grad_eta[i] = s;
+    } else if (i < rows + D) {
+        const int dd = static_cast<int>(i - rows);
+        float s = 0.0f;
+        for (int b = 0; b < B; ++b) s += part_nu[static_cast<size_t>(b) * D + dd];
+        grad_nu_log[dd] = s;
+    }
+}
+
+// Plain kernels (any alignment): thread per lane.  The backward's per-row
+// sums over lanes go through a warp shuffle reduction into the same
+// [B*T][ncol] partials (ncol = ceil(D / 32)).
+template <typename St>
+__global__ void __launch_bounds__(128)
+gplain_fwd(const float *__restrict__ eta, const float *__restrict__ nu_log, const St *__restrict__ b,
+           St *__restrict__ out, float *__restrict__ last, int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    if (d >= D) return;
+    const float nu = __expf(__ldg(nu_log + d));
+    size_t i = static_cast<size_t>(brow) * T * D + d;
+    float h = 0.0f;
+    for (int t = 0; t < T; ++t) {
+        float y[1];
+        load_lanes_global<St, 1>(b + i, y);
+        const float a = __expf(-__fmul_rn(nu, __expf(__ldg(eta + static_cast<size_t>(brow) * T + t))));
+        h = __fmaf_rn(a, h, y[0]);
+        const float hv[1] = {h};
+        store_lanes<St, 1>(out + i, hv);
+        i += D;
+    }
+    if (last != nullptr) last[static_cast<size_t>(brow) * D + d] = h;
+}
+
+template <typename St>
+__global__ void __launch_bounds__(128)
+gplain_bwd(const float *__restrict__ eta, const float *__restrict__ nu_log, const St *__restrict__ out,
+           const St *__restrict__ grad_out, St *__restrict__ grad_b, float *__restrict__ part_eta,
+           float *__restrict__ part_nu, int T, int D, int nlb) {
+    const int brow = blockIdx.x / nlb;
+    const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
+    const bool ok = d < D;  // every lane of a warp takes part in the row sums
+    const int ncol = (D + 31) / 32;
+    const int col = d / 32;
+    const float nu = ok ? __expf(__ldg(nu_log + d)) : 0.0f;
+    const size_t row = static_cast<size_t>(brow) * T * D + d;
+    float g = 0.0f, a_next = 0.0f, acc = 0.0f;
+    for (int t = T - 1; t >= 0; --t) {
+        const size_t i = row + static_cast<size_t>(t) * D;
+        float go[1] = {0.0f}, hp[1] = {0.0f};
+        if (ok) {
+            load_lanes_global<St, 1>(grad_out + i, go);
+            if (t > 0) load_lanes_global<St, 1>(out + i - D, hp);
+        }
+        const float la = -__fmul_rn(nu, __expf(__ldg(eta + static_cast<size_t>(brow) * T + t)));
+        const float a = __expf(la);
+        g = __fmaf_rn(a_next, g, go[0]);
+        const float q = ok ? __fmul_rn(__fmul_rn(__fmul_rn(g, hp[0]), a), la) : 0.0f;
+        acc += q;
+        a_next = a;
+        if (ok) {
+            const float gv[1] = {g};
+            store_lanes<St, 1>(grad_b + i, gv);
+        }
+        float s = q;
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+        if ((threadIdx.x & 31) == 0 && d < D)  // lane 0's lane is the warp's first: d < D iff the warp has lanes
+            part_eta[(static_cast<size_t>(brow) * T + t) * ncol + col] = s;
+    }
+    if (ok) part_nu[static_cast<size_t>(brow) * D + d] = acc;
+}
+
+}  // namespace lrscan

@@ -1,0 +1,130 @@
+// Instantiations and launchers of the generated-decay scan kernels, and their
+// tile variant table.
+#include <algorithm>
+
+#include "gated_kernels.cuh"
+#include "window_launch.cuh"
+
+namespace lrscan {
+
+namespace {
+
+template <class C>
+int launch_gwin_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gwin_fwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    using St = typename C::St;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], L.eta, L.nu_log, static_cast<St *>(L.out0), L.last, g,
+                                     L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C>
+int launch_gwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gwin_bwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    using St = typename C::St;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, static_cast<St *>(L.out0),
+                                     L.part_eta, L.part_nu, g, L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C, bool FWD>
+WinDirCfg gdir_cfg(int nstage) {
+    static_assert(C::NIN == (FWD ? 1 : 2), "generated-decay planes: b forward; out and grad_out backward");
+    const WinGeom g = make_win_geom<C>(1, nstage, 1, 1);
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = 1;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = C::G + 32;
+    d.smem = g.smem_bytes;
+    d.stage_bytes = g.stage_bytes;
+    if constexpr (FWD) d.launch = &launch_gwin_fwd<C>;
+    else d.launch = &launch_gwin_bwd<C>;
+    return d;
+}
+
+// WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
+using GBF_64_1 = WinShape<bf16_t, 64, 1, 32, 1, 96, 1, true>;
+using GBB_64_1 = WinShape<bf16_t, 64, 1, 32, 2, 96, 1, true>;
+using GBF_64_2 = WinShape<bf16_t, 64, 2, 32, 1, 64, 1, true>;
+using GBB_64_2 = WinShape<bf16_t, 64, 2, 32, 2, 64, 1, true>;
+using GFF_32_1 = WinShape<float, 32, 1, 32, 1, 64, 1, true>;
+using GFB_32_1 = WinShape<float, 32, 1, 32, 2, 64, 1, true>;
+using GFF_64_2 = WinShape<float, 64, 2, 32, 1, 64, 1, true>;
+using GFB_64_2 = WinShape<float, 64, 2, 32, 2, 64, 1, true>;
+
+#define F(SH, N) gdir_cfg<SH, true>(N)
+#define B(SH, N) gdir_cfg<SH, false>(N)
+const WinVariant kGatedBF16[] = {
+    {"gseq_bf16_d64_v1", F(GBF_64_1, 8), B(GBB_64_1, 6)},
+    {"gseq_bf16_d64_v2", F(GBF_64_2, 8), B(GBB_64_2, 6)},
+};
+const WinVariant kGatedF32[] = {
+    {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
+    {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
+};
+#undef F
+#undef B
+
+}  // namespace
+
+const WinVariant *gwin_variants(int dtype, int *count) {
+    if (dtype == 0) {
+        *count = sizeof(kGatedF32) / sizeof(kGatedF32[0]);
+        return kGatedF32;
+    }
+    *count = sizeof(kGatedBF16) / sizeof(kGatedBF16[0]);
+    return kGatedBF16;
+}
+
+int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
+                        long long rows, int ncol, int B, int D, cudaStream_t stream) {
+    const long long n = rows + D;
+    if (n == 0) return 0;
+    gated_finish<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(part_eta, part_nu, grad_eta,
+                                                                           grad_nu_log, rows, ncol, B, D);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int gplain_launch(const WinLaunch &L, int dtype, bool fwd) {
+    const int nlb = static_cast<int>((L.D + 127) / 128);
+    const unsigned nb = static_cast<unsigned>(nlb * L.B);
+    const int T = static_cast<int>(L.T), D = static_cast<int>(L.D);
+    if (fwd) {
+        if (dtype == 0)
+            gplain_fwd<float><<<nb, 128, 0, L.stream>>>(L.eta, L.nu_log, static_cast<const float *>(L.in0),
+                                                        static_cast<float *>(L.out0), L.last, T, D, nlb);
+        else
+            gplain_fwd<bf16_t><<<nb, 128, 0, L.stream>>>(L.eta, L.nu_log, static_cast<const bf16_t *>(L.in0),
+                                                         static_cast<bf16_t *>(L.out0), L.last, T, D, nlb);
+    } else {
+        if (dtype == 0)
+            gplain_bwd<float><<<nb, 128, 0, L.stream>>>(L.eta, L.nu_log, static_cast<const float *>(L.in0),
+                                                        static_cast<const float *>(L.in1),
+                                                        static_cast<float *>(L.out0), L.part_eta, L.part_nu, T, D,
+                                                        nlb);
+        else
+            gplain_bwd<bf16_t><<<nb, 128, 0, L.stream>>>(L.eta, L.nu_log, static_cast<const bf16_t *>(L.in0),
+                                                         static_cast<const bf16_t *>(L.in1),
+                                                         static_cast<bf16_t *>(L.out0), L.part_eta, L.part_nu, T,
+                                                         D, nlb);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace lrscan

@@ -51,6 +51,11 @@ struct WinLaunch {
     cudaStream_t stream;
     int device;
     StateArgs sx;  // carried state and resets (used by the EXT launchers only)
+    // generated-decay scan: per-token / per-lane parameters, backward partial
+    // sums, and the plain kernels' tensor inputs (in0 = b or out, in1 = grad_out)
+    const float *eta, *nu_log;
+    float *part_eta, *part_nu;
+    const void *in0, *in1;
 };
 
 // One direction of a tile variant: compiled shape (DT, V, L) plus the
@@ -80,6 +85,13 @@ const WinVariant *win_variants(int path, int dtype, int *count);
 
 // Complex scan tile variants (kernels_complex.cu); dtype 0 = f32, 1 = bf16.
 const WinVariant *cwin_variants(int dtype, int *count);
+
+// Generated-decay scan (kernels_gated.cu): tile variants, the plain
+// kernels, and the partial-sum reduction (part_eta [rows][ncol], part_nu [B][D]).
+const WinVariant *gwin_variants(int dtype, int *count);
+int gplain_launch(const WinLaunch &L, int dtype, bool fwd);
+int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
+                        long long rows, int ncol, int B, int D, cudaStream_t stream);
 
 // Three-phase chunked path and plain kernels (kernels_chunk.cu).
 struct ChunkLaunch {

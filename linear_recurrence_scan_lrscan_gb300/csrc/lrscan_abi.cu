@@ -787,6 +787,188 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
     return LRSCAN_OK;
 }
 
+// ------------------------------------------------------- generated decay --
+// Partial-sum columns per row of the backward: at most ceil(D/32) warp
+// columns plus the ragged last CTA's extra warps.
+int64_t gated_ncol_bound(int64_t D) { return (D + 31) / 32 + 4; }
+
+size_t gated_workspace(int64_t B, int64_t T, int64_t D) {
+    auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
+    return pad(static_cast<size_t>(B) * T * gated_ncol_bound(D) * 4) + pad(static_cast<size_t>(B) * D * 4);
+}
+
+// Tiled sequential kernels for 16-byte aligned rows, else plain kernels.
+int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrscan_opts *opts, const Geometry &g,
+               Choice *ch) {
+    const int want = opts ? opts->path : 0;
+    const int force_v = opts ? opts->tile_variant : 0;
+    if (want != kPathAuto && want != kPathSeq && want != kPathPlain)
+        return fail(LRSCAN_EINVAL, "the generated-decay scan has the seq and plain paths only (path %d)", want);
+    if (want == kPathSeq && !aligned)
+        return fail(LRSCAN_EINVAL, "path seq needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
+    const int path = want == kPathAuto ? (aligned ? kPathSeq : kPathPlain) : want;
+    ch->path = path;
+    ch->dir = dir;
+    ch->kernels = dir == 0 ? 1 : 2;
+    ch->vec = 1;
+    if (path == kPathPlain) {
+        if (force_v > 1) return fail(LRSCAN_EINVAL, "the plain path has one variant");
+        ch->ctas = B * ((D + 127) / 128);
+        ch->threads = 128;
+        return LRSCAN_OK;
+    }
+    int n = 0;
+    const WinVariant *tab = gwin_variants(dtype, &n);
+    int vi = -1;
+    if (force_v > 0) {
+        if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
+        vi = force_v - 1;
+    } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
+        long long most = -1;
+        for (int i = 0; i < n; ++i) {
+            const Occ o = occupancy(tab[i], dir, B, D, g);
+            if (o.resident > 0 && o.ctas > most) { most = o.ctas; vi = i; }
+        }
+    }
+    if (vi < 0) return fail(LRSCAN_EINVAL, "no generated-decay tile variant fits this device");
+    const Occ o = occupancy(tab[vi], dir, B, D, g);
+    ch->vidx = vi;
+    ch->var = &tab[vi];
+    ch->ctas = o.ctas;
+    ch->threads = dir_of(tab[vi], dir).threads;
+    ch->smem = dir_of(tab[vi], dir).smem;
+    ch->stages = dir_of(tab[vi], dir).nstage;
+    return LRSCAN_OK;
+}
+
+int check_params(const float *eta, const float *nu_log) {
+    if (!eta || !nu_log) return fail(LRSCAN_EINVAL, "NULL eta or nu_log");
+    if (reinterpret_cast<uintptr_t>(eta) % 4 || reinterpret_cast<uintptr_t>(nu_log) % 4)
+        return fail(LRSCAN_EINVAL, "eta and nu_log must be 4-byte aligned");
+    return LRSCAN_OK;
+}
+
+int run_gfwd(const float *eta, const float *nu_log, const void *b, void *out, float *last, int64_t B, int64_t T,
+             int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    t_detail[0] = 0;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
+    cudaStream_t st = pick_stream(stream);
+    if (T == 0) return copy_or_zero(last, nullptr, B, D, st);
+    if (!b || !out) return fail(LRSCAN_EINVAL, "NULL b or out");
+    if ((rc = check_params(eta, nu_log))) return rc;
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({b, out}, D, dtype);
+    Choice ch;
+    if ((rc = plan_gated(B, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
+    WinLaunch L{};
+    L.eta = eta;
+    L.nu_log = nu_log;
+    L.status = ctx->status;
+    L.timeout_ns = g_timeout_ns.load();
+    L.stream = st;
+    L.device = dev;
+    if (ch.path == kPathPlain) {
+        L.in0 = b; L.out0 = out; L.last = last;
+        L.B = B; L.T = T; L.D = D;
+        return gplain_launch(L, dtype, true) ? fail(LRSCAN_ECUDA, "generated-decay plain launch failed") : LRSCAN_OK;
+    }
+    const size_t es = esize(dtype);
+    const WinDirCfg &v = ch.var->fwd;
+    for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+        const int64_t nb = std::min<int64_t>(65535, B - b0);
+        const size_t off = static_cast<size_t>(b0) * T * D * es;
+        CUtensorMap mb;
+        if (encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+        L.maps[0] = &mb;
+        L.eta = eta + b0 * T;
+        L.out0 = static_cast<char *>(out) + off;
+        L.last = last ? last + b0 * D : nullptr;
+        L.B = nb; L.T = T; L.D = D;
+        if (v.launch(L, v))
+            return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
+    }
+    return LRSCAN_OK;
+}
+
+int run_gbwd(const float *eta, const float *nu_log, const void *out, const void *grad_out, void *grad_b,
+             float *grad_eta, float *grad_nu_log, int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+             const lrscan_opts *opts) {
+    t_detail[0] = 0;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    if (B == 0 || D == 0) {
+        if (D > 0 && grad_nu_log)  // no tokens: the rate gradient is zero
+            return copy_or_zero(grad_nu_log, nullptr, 1, D, pick_stream(stream));
+        return LRSCAN_OK;
+    }
+    cudaStream_t st = pick_stream(stream);
+    if (!grad_eta || !grad_nu_log) return fail(LRSCAN_EINVAL, "NULL grad_eta or grad_nu_log");
+    if (T == 0) return copy_or_zero(grad_nu_log, nullptr, 1, D, st);
+    if (!out || !grad_out || !grad_b) return fail(LRSCAN_EINVAL, "NULL out, grad_out or grad_b");
+    if ((rc = check_params(eta, nu_log))) return rc;
+    if (reinterpret_cast<uintptr_t>(grad_eta) % 4 || reinterpret_cast<uintptr_t>(grad_nu_log) % 4)
+        return fail(LRSCAN_EINVAL, "grad_eta and grad_nu_log must be 4-byte aligned");
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx))) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool al = aligned16({out, grad_out, grad_b}, D, dtype);
+    Choice ch;
+    if ((rc = plan_gated(B, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
+    const size_t need = gated_workspace(B, T, D);
+    void *ws = nullptr;
+    if ((rc = workspace_for(ctx, st, need, opts, &ws))) return rc;
+    float *part_eta = static_cast<float *>(ws);
+    const size_t eta_bytes = (static_cast<size_t>(B) * T * gated_ncol_bound(D) * 4 + 255) / 256 * 256;
+    float *part_nu = reinterpret_cast<float *>(static_cast<char *>(ws) + eta_bytes);
+    WinLaunch L{};
+    L.eta = eta;
+    L.nu_log = nu_log;
+    L.status = ctx->status;
+    L.timeout_ns = g_timeout_ns.load();
+    L.stream = st;
+    L.device = dev;
+    int ncol;
+    if (ch.path == kPathPlain) {
+        ncol = static_cast<int>((D + 31) / 32);
+        L.in0 = out; L.in1 = grad_out; L.out0 = grad_b;
+        L.part_eta = part_eta; L.part_nu = part_nu;
+        L.B = B; L.T = T; L.D = D;
+        if (gplain_launch(L, dtype, false)) return fail(LRSCAN_ECUDA, "generated-decay plain launch failed");
+    } else {
+        const WinDirCfg &v = ch.var->bwd;
+        ncol = static_cast<int>(((D + v.dt - 1) / v.dt) * (v.threads - 32) / 32);
+        const size_t es = esize(dtype);
+        for (int64_t b0 = 0; b0 < B; b0 += 65535) {
+            const int64_t nb = std::min<int64_t>(65535, B - b0);
+            const size_t off = static_cast<size_t>(b0) * T * D * es;
+            CUtensorMap mo, mg;
+            if (encode_map(&mo, static_cast<const char *>(out) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w))
+                return LRSCAN_EINVAL;
+            L.maps[0] = &mo;
+            L.maps[1] = &mg;
+            L.eta = eta + b0 * T;
+            L.out0 = static_cast<char *>(grad_b) + off;
+            L.part_eta = part_eta + static_cast<size_t>(b0) * T * ncol;
+            L.part_nu = part_nu + static_cast<size_t>(b0) * D;
+            L.B = nb; L.T = T; L.D = D;
+            if (v.launch(L, v))
+                return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
+        }
+    }
+    if (ncol > gated_ncol_bound(D)) return fail(LRSCAN_EINVAL, "internal: partial columns exceed the workspace");
+    if (gated_finish_launch(part_eta, part_nu, grad_eta, grad_nu_log, B * T, ncol, static_cast<int>(B),
+                            static_cast<int>(D), st))
+        return fail(LRSCAN_ECUDA, "generated-decay reduction launch failed");
+    return LRSCAN_OK;
+}
+
 }  // namespace
 
 // Lets other translation units of the library report why a call failed.
@@ -918,6 +1100,37 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
     Choice ch;
     if ((rc = plan_complex(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch)))
         return rc;
+    fill_info(ch, info);
+    return LRSCAN_OK;
+}
+
+int lrscan_fwd_gated(const float *eta, const float *nu_log, const void *b, void *out, float *last, int64_t B,
+                     int64_t T, int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+    return run_gfwd(eta, nu_log, b, out, last, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_bwd_gated(const float *eta, const float *nu_log, const void *out, const void *grad_out, void *grad_b,
+                     float *grad_eta, float *grad_nu_log, int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+                     const lrscan_opts *opts) {
+    return run_gbwd(eta, nu_log, out, grad_out, grad_b, grad_eta, grad_nu_log, B, T, D, dtype, stream, opts);
+}
+
+size_t lrscan_gated_workspace_bytes(int64_t B, int64_t T, int64_t D) {
+    if (B <= 0 || T <= 0 || D <= 0) return 0;
+    return gated_workspace(B, T, D);
+}
+
+int lrscan_plan_gated(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16, const lrscan_opts *opts,
+                      lrscan_plan_info *info) {
+    if (!info || (dir != 0 && dir != 1)) return LRSCAN_EINVAL;
+    int rc = check_shape(B, T, D, dtype);
+    if (rc) return rc;
+    DeviceCtx *ctx = nullptr;
+    if (device_ctx(&ctx) != LRSCAN_OK) ctx = nullptr;
+    const bool al = is_aligned16 && (D * esize(dtype)) % 16 == 0;
+    Choice ch;
+    if ((rc = plan_gated(B > 0 ? B : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch))) return rc;
+    if (dir == 1) ch.workspace = gated_workspace(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1);
     fill_info(ch, info);
     return LRSCAN_OK;
 }

@@ -90,6 +90,11 @@ EXPORTS = {
     "lrscan_cbwd": ([_P] * 10 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_plan_complex": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
                              ctypes.POINTER(PlanInfo)], ctypes.c_int),
+    "lrscan_fwd_gated": ([_P] * 5 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_bwd_gated": ([_P] * 7 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_gated_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
+    "lrscan_plan_gated": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
+                           ctypes.POINTER(PlanInfo)], ctypes.c_int),
     "lrscan_set_stream": ([_P], ctypes.c_int),
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
@@ -412,6 +417,72 @@ def lrscan_plan_complex(B: int, T: int, D: int, dtype="f32", direction: str = "f
     return info.as_dict()
 
 
+def _gated_params(eta, nu_log, B, T, D, device):
+    if not (isinstance(eta, torch.Tensor) and eta.is_cuda and eta.dtype == torch.float32
+            and tuple(eta.shape) == (B, T) and eta.is_contiguous() and eta.device == device):
+        raise ValueError(f"eta must be a contiguous CUDA fp32 tensor of shape {(B, T)}")
+    if not (isinstance(nu_log, torch.Tensor) and nu_log.is_cuda and nu_log.dtype == torch.float32
+            and tuple(nu_log.shape) == (D,) and nu_log.is_contiguous() and nu_log.device == device):
+        raise ValueError(f"nu_log must be a contiguous CUDA fp32 tensor of shape {(D,)}")
+
+
+def lrscan_fwd_gated(eta, nu_log, b, *, out=None, last=None, path=None, tile_variant=None, stream=None):
+    """Scan with the decay generated as exp(-exp(nu_log[d]) * exp(eta[b, t]));
+    eta fp32 [B, T], nu_log fp32 [D], b [B, T, D]; returns (out, last)."""
+    if b.ndim != 3:
+        raise ValueError("lrscan expects a [B, T, D] tensor b")
+    code = _dtype_code(b)
+    B, T, D = b.shape
+    _gated_params(eta, nu_log, B, T, D, b.device)
+    out = torch.empty_like(b) if out is None else out
+    last = torch.empty((B, D), device=b.device, dtype=torch.float32) if last is None else last
+    _check_tensors(b.shape, b.dtype, b.device, b=b, out=out, last=last)
+    with torch.cuda.device(b.device):
+        o = _opts(path, None, tile_variant, None)
+        rc = lib().lrscan_fwd_gated(eta.data_ptr(), nu_log.data_ptr(), b.data_ptr(), out.data_ptr(), last.data_ptr(),
+                                    B, T, D, code, _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_fwd_gated")
+    return out, last
+
+
+def lrscan_bwd_gated(eta, nu_log, out, grad_out, *, grad_b=None, path=None, tile_variant=None, workspace=None,
+                     stream=None):
+    """Reverse of :func:`lrscan_fwd_gated`; returns (grad_b, grad_eta, grad_nu_log)."""
+    if out.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] tensors")
+    code = _dtype_code(out)
+    B, T, D = out.shape
+    _gated_params(eta, nu_log, B, T, D, out.device)
+    grad_b = torch.empty_like(out) if grad_b is None else grad_b
+    _check_tensors(out.shape, out.dtype, out.device, out=out, grad_out=grad_out, grad_b=grad_b)
+    grad_eta = torch.empty((B, T), device=out.device, dtype=torch.float32)
+    grad_nu = torch.empty((D,), device=out.device, dtype=torch.float32)
+    with torch.cuda.device(out.device):
+        o = _opts(path, None, tile_variant, workspace)
+        rc = lib().lrscan_bwd_gated(eta.data_ptr(), nu_log.data_ptr(), out.data_ptr(), grad_out.data_ptr(),
+                                    grad_b.data_ptr(), grad_eta.data_ptr(), grad_nu.data_ptr(), B, T, D, code,
+                                    _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_bwd_gated")
+    return grad_b, grad_eta, grad_nu
+
+
+def lrscan_plan_gated(B: int, T: int, D: int, dtype="f32", direction: str = "fwd", aligned: bool = True,
+                      path=None, tile_variant=None) -> dict:
+    code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
+    if code is None:
+        raise ValueError(f"unsupported dtype {dtype}")
+    info = PlanInfo()
+    o = _opts(path, None, tile_variant, None)
+    rc = lib().lrscan_plan_gated(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
+                                 ctypes.byref(o) if o is not None else None, ctypes.byref(info))
+    _check(rc, "lrscan_plan_gated")
+    return info.as_dict()
+
+
+def lrscan_gated_workspace_bytes(B: int, T: int, D: int) -> int:
+    return lib().lrscan_gated_workspace_bytes(B, T, D)
+
+
 def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
                 aligned: bool = True, path=None, chunk_len=None, tile_variant=None) -> dict:
     """What the dispatcher would run for this call (host only; no launch)."""
@@ -529,3 +600,27 @@ class ComplexScan(torch.autograd.Function):
 def complex_scan(ar, ai, br, bi, path=None):
     """Differentiable complex diagonal scan on re/im planes; returns (out_r, out_i)."""
     return ComplexScan.apply(ar, ai, br, bi, path)
+
+
+class GatedScan(torch.autograd.Function):
+    """Autograd wrapper of the generated-decay scan: out = scan(eta, nu_log, b)."""
+
+    @staticmethod
+    def forward(ctx, eta, nu_log, b, path=None):
+        eta, nu_log, b = eta.contiguous(), nu_log.contiguous(), b.contiguous()
+        out, _ = lrscan_fwd_gated(eta, nu_log, b, path=path)
+        ctx.save_for_backward(eta, nu_log, out)
+        ctx.path = path
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        eta, nu_log, out = ctx.saved_tensors
+        gb, geta, gnu = lrscan_bwd_gated(eta, nu_log, out, grad_out.contiguous(), path=ctx.path)
+        return geta, gnu, gb, None
+
+
+def gated_scan(eta, nu_log, b, path=None):
+    """Differentiable scan whose decays exp(-exp(nu_log[d]) * exp(eta[b, t])) are
+    generated in the kernel; returns out [B, T, D]."""
+    return GatedScan.apply(eta, nu_log, b, path)

@@ -182,6 +182,31 @@ def make_complex_inputs(B: int | None = None, T: int | None = None, D: int | Non
     return {k: v.to(dt).contiguous() for k, v in planes.items()} | {"shape": shape, "workload": w}
 
 
+# Generated-decay workload: the gated workload's shape, with the decay
+# parametrized per token (eta) and per lane (nu_log) instead of stored.
+GATED_WORKLOAD = Workload(7, "generated-decay-bf16", 8, 2048, 2560, "bf16")
+
+
+def make_gated_inputs(B: int | None = None, T: int | None = None, D: int | None = None, dtype: str | None = None,
+                      *, seed: int | None = None) -> dict:
+    """eta ~ N(-1, 1) fp32 [B, T], nu_log ~ U(-2, 1) fp32 [D] (so decays spread
+    over (0, 1) like the gated workload's), b and grad_out ~ N(0, 1) [B, T, D]
+    in `dtype`."""
+    w = GATED_WORKLOAD
+    B = w.B if B is None else B
+    T = w.T if T is None else T
+    D = w.D if D is None else D
+    dtype = w.dtype if dtype is None else dtype
+    gen = torch.Generator("cpu").manual_seed(SEED_BASE + w.cid if seed is None else seed)
+    eta = _normal(gen, (B, T)) - 1.0
+    nu_log = _uniform(gen, (D,), -2.0, 1.0)
+    b = _normal(gen, (B, T, D))
+    g = _normal(gen, (B, T, D))
+    dt = TORCH_DTYPE[dtype]
+    return {"eta": eta.contiguous(), "nu_log": nu_log.contiguous(), "b": b.to(dt).contiguous(),
+            "grad_out": g.to(dt).contiguous(), "shape": (B, T, D), "workload": w}
+
+
 def to_numpy_storage(t: torch.Tensor):
     """CPU tensor -> numpy array as the oracle takes it (bf16 as uint16 bits)."""
     t = t.detach().cpu().contiguous()

@@ -1,0 +1,138 @@
+"""GPU parity of the scan with generated decays exp(-exp(nu_log_d) exp(eta_t))
+against the oracle.  The kernels use the hardware's fast exponential, so
+every output is held to the tolerances of parity_util (fp32 rule, 2 bf16 ulps
+with the near-cancellation clause); grad_eta and grad_nu_log are fp32 sums
+compared with the fp32 rule against the oracle's double-accumulated sums."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+from linear_recurrence_scan_lrscan_gb300.workloads import GATED_WORKLOAD, make_gated_inputs
+from parity_util import assert_close, assert_last_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L.lib()
+    yield
+    assert L.lrscan_sync_check() == 0
+
+
+def from_np(x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x))
+
+
+def check_gated(inp, dt, **kw):
+    B, T, D = inp["shape"]
+    eta, nu = inp["eta"].numpy(), inp["nu_log"].numpy()
+    b, g = to_np(inp["b"]), to_np(inp["grad_out"])
+    o = oracle.default()
+    ref_out, ref_last = o.gated_fwd(eta, nu, b, dt)
+    etad, nud = inp["eta"].cuda(), inp["nu_log"].cuda()
+    out, last = L.lrscan_fwd_gated(etad, nud, inp["b"].cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    plan = L.lrscan_plan_gated(B, T, D, dt, "fwd", **kw)
+    assert_close(to_np(out), ref_out, dt, f"out[{plan['name']}]", reassociated=True)
+    assert_last_close(last.cpu().numpy(), ref_last, f"last[{plan['name']}]")
+    ref_gb, ref_geta, ref_gnu = o.gated_bwd(eta, nu, ref_out, g, dt)
+    gb, geta, gnu = L.lrscan_bwd_gated(etad, nud, from_np(ref_out, dt).cuda(), inp["grad_out"].cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    planb = L.lrscan_plan_gated(B, T, D, dt, "bwd", **kw)
+    assert_close(to_np(gb), ref_gb, dt, f"grad_b[{planb['name']}]", reassociated=True)
+    assert_last_close(geta.cpu().numpy(), ref_geta, f"grad_eta[{planb['name']}]")
+    assert_last_close(gnu.cpu().numpy(), ref_gnu, f"grad_nu_log[{planb['name']}]")
+    return plan, planb
+
+
+SHAPES = [(3, 300, 200), (2, 77, 40), (1, 1, 8), (2, 257, 1000), (1, 33, 64)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_gated_every_variant_and_plain(dt, shape):
+    B, T, D = shape
+    inp = make_gated_inputs(B, T, D, dt, seed=700 + T)
+    v = 1
+    while True:
+        try:
+            L.lrscan_plan_gated(B, T, D, dt, path="seq", tile_variant=v)
+        except L.LrscanError:
+            break
+        check_gated(inp, dt, path="seq", tile_variant=v)
+        v += 1
+    assert v > 2
+    check_gated(inp, dt, path="plain")
+    plan, planb = check_gated(inp, dt)
+    assert plan["path"] == "seq" and planb["path"] == "seq" and planb["kernels"] == 2
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_gated_unaligned_rows_take_plain(dt):
+    inp = make_gated_inputs(2, 90, 37, dt, seed=710)
+    plan, planb = check_gated(inp, dt)
+    assert plan["path"] == "plain" and planb["path"] == "plain"
+
+
+def test_gated_empty_sequence():
+    b = torch.empty((2, 0, 16), device="cuda")
+    eta = torch.empty((2, 0), device="cuda")
+    nu = torch.zeros(16, device="cuda")
+    _, last = L.lrscan_fwd_gated(eta, nu, b)
+    assert not last.any()
+    _, geta, gnu = L.lrscan_bwd_gated(eta, nu, b, b)
+    assert not gnu.any() and geta.numel() == 0
+
+
+def test_gated_full_size_sampled_lanes():
+    """The generated-decay workload at full size in the benchmark's launch
+    configuration: out and grad_b checked on sampled lanes; grad_eta on
+    sampled tokens (the oracle sums the whole lane range of those tokens);
+    grad_nu_log on sampled lanes (sums over every token)."""
+    w = GATED_WORKLOAD
+    inp = make_gated_inputs()
+    etad, nud = inp["eta"].cuda(), inp["nu_log"].cuda()
+    out, last = L.lrscan_fwd_gated(etad, nud, inp["b"].cuda())
+    gb, geta, gnu = L.lrscan_bwd_gated(etad, nud, out, inp["grad_out"].cuda())
+    assert L.lrscan_sync_check() == 0
+    o = oracle.default()
+    r = np.random.default_rng(720)
+    eta, nu = inp["eta"].numpy(), inp["nu_log"].numpy()
+    for _ in range(4):
+        bb, d = int(r.integers(w.B)), int(r.integers(w.D))
+        sl = lambda t: np.ascontiguousarray(to_np(t[bb:bb + 1, :, d:d + 1]))  # noqa: E731
+        ref_out, _ = o.gated_fwd(eta[bb:bb + 1], nu[d:d + 1], sl(inp["b"]), w.dtype)
+        assert_close(sl(out), ref_out, w.dtype, "gated out sampled", reassociated=True)
+        ref_gb, _, ref_gnu_b = o.gated_bwd(eta[bb:bb + 1], nu[d:d + 1], ref_out, sl(inp["grad_out"]), w.dtype)
+        assert_close(sl(gb), ref_gb, w.dtype, "gated grad_b sampled", reassociated=True)
+    # one whole batch row for grad_eta (all lanes) and for a per-row share of grad_nu_log
+    bb = int(r.integers(w.B))
+    row = lambda t: np.ascontiguousarray(to_np(t[bb:bb + 1]))  # noqa: E731
+    ref_out, _ = o.gated_fwd(eta[bb:bb + 1], nu, row(inp["b"]), w.dtype)
+    _, ref_geta, _ = o.gated_bwd(eta[bb:bb + 1], nu, ref_out, row(inp["grad_out"]), w.dtype)
+    assert_last_close(geta[bb:bb + 1].cpu().numpy(), ref_geta, "gated grad_eta, one batch row")
+    assert torch.isfinite(gnu).all()
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_gated_scan_autograd(dt):
+    inp = make_gated_inputs(2, 150, 64, dt, seed=730)
+    eta = inp["eta"].cuda().requires_grad_()
+    nu = inp["nu_log"].cuda().requires_grad_()
+    b = inp["b"].cuda().requires_grad_()
+    out = L.gated_scan(eta, nu, b)
+    (out.float() * inp["grad_out"].cuda().float()).sum().backward()
+    o = oracle.default()
+    ref_out, _ = o.gated_fwd(inp["eta"].numpy(), inp["nu_log"].numpy(), to_np(inp["b"]), dt)
+    ref_gb, ref_geta, ref_gnu = o.gated_bwd(inp["eta"].numpy(), inp["nu_log"].numpy(), ref_out,
+                                            to_np(inp["grad_out"]), dt)
+    assert_close(to_np(b.grad), ref_gb, dt, "autograd grad_b", reassociated=True)
+    assert_last_close(eta.grad.cpu().numpy(), ref_geta, "autograd grad_eta")
+    assert_last_close(nu.grad.cpu().numpy(), ref_gnu, "autograd grad_nu_log")
