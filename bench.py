@@ -430,7 +430,8 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
     for f in sets:   # leave every set with the plain forward's output
         L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
     torch.cuda.synchronize()
-    return {"complex": run_complex(iters, dev, peak), "long_t": run_long_t(dev, peak), "state": {
+    return {"complex": run_complex(iters, dev, peak), "generated_decay": run_gated(iters, dev, peak),
+            "long_t": run_long_t(dev, peak), "state": {
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
         "launches_per_direction": iters,
@@ -485,6 +486,55 @@ def run_complex(iters: int, dev, peak) -> dict:
                     "algorithmic_bytes": fb, "kernel": pf["name"]},
             "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
                     "algorithmic_bytes": bb, "kernel": pb["name"]},
+            "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+
+
+def run_gated(iters: int, dev, peak) -> dict:
+    """The scan with decays generated in the kernel (exp(-exp(nu_log_d) exp(eta_t)))
+    on the gated workload's shape, three rotating buffer sets.  Forward moves b
+    in and out out (2 elements per (t, d)) plus eta, nu_log and the fp32 final
+    state; backward moves out, grad_out in and grad_b out (3 elements) plus
+    eta, nu_log in and grad_eta, grad_nu_log out."""
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    from linear_recurrence_scan_lrscan_gb300.workloads import GATED_WORKLOAD as gw
+    from linear_recurrence_scan_lrscan_gb300.workloads import make_gated_inputs
+    stream = torch.cuda.current_stream()
+    host = make_gated_inputs()
+    sets = []
+    for _ in range(3):
+        st = {k: host[k].to(dev) for k in ("eta", "nu_log", "b", "grad_out")}
+        st["out"], st["gb"] = torch.empty_like(st["b"]), torch.empty_like(st["b"])
+        st["last"] = torch.empty(gw.B, gw.D, device=dev)
+        L.lrscan_fwd_gated(st["eta"], st["nu_log"], st["b"], out=st["out"], last=st["last"])
+        sets.append(st)
+    del host
+
+    def fwd(i):
+        st = sets[i % 3]
+        L.lrscan_fwd_gated(st["eta"], st["nu_log"], st["b"], out=st["out"], last=st["last"])
+
+    def bwd(i):
+        st = sets[i % 3]
+        L.lrscan_bwd_gated(st["eta"], st["nu_log"], st["out"], st["grad_out"], grad_b=st["gb"])
+    fms = time_launches(fwd, iters, stream)
+    bms = time_launches(bwd, iters, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the generated-decay scan")
+    B, T, D, E, s = gw.B, gw.T, gw.D, gw.elements, gw.storage_bytes
+    fb = 2 * E * s + 4 * B * T + 4 * D + 4 * B * D
+    bb = 3 * E * s + 2 * (4 * B * T + 4 * D)
+    pf = L.lrscan_plan_gated(B, T, D, gw.dtype, "fwd")
+    pb = L.lrscan_plan_gated(B, T, D, gw.dtype, "bwd")
+    del sets
+    torch.cuda.empty_cache()
+    return {"workload": gw.describe() + " with decays generated from eta [B,T] and nu_log [D]",
+            "launches_per_direction": iters,
+            "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                    "algorithmic_bytes": fb, "kernel": pf["name"]},
+            "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                    "algorithmic_bytes": bb, "kernel": pb["name"], "kernels": pb["kernels"]},
             "elements/s": 2 * E / ((fms + bms) * 1e-3)}
 
 
@@ -561,7 +611,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extensions", action="store_true",
-                    help="skip the timing of the state-carrying, complex and long-sequence scans")
+                    help="skip the timing of the state-carrying, complex, generated-decay and long-sequence scans")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=float, default=2e6)
     args = ap.parse_args()
