@@ -113,15 +113,26 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
             if (lane_ok) store_lanes<St, V>(out + o + static_cast<size_t>(j) * D, h);
         };
         if (n == L) {
+            // phases: the window's inputs to registers, every row's decay
+            // (independent of the state), then the dependent chain
             using Raw = typename RawOf<St, V>::T;
             Raw rb[L];
+            float av[L][V];
 #pragma unroll
             for (int j = 0; j < L; ++j) rb[j] = load_raw<St, V>(tb + j * DT);
 #pragma unroll
             for (int j = 0; j < L; ++j) {
+                const float e = __shfl_sync(0xffffffffu, e_lane, j);
+#pragma unroll
+                for (int v = 0; v < V; ++v) av[j][v] = __expf(-__fmul_rn(nu[v], e));
+            }
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
                 float y[V];
                 widen_raw(rb[j], y);
-                step(j, y);
+#pragma unroll
+                for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(av[j][v], h[v], y[v]);
+                if (lane_ok) store_lanes<St, V>(out + o + static_cast<size_t>(j) * D, h);
             }
         } else {
             for (int j = 0; j < n; ++j) {
@@ -137,6 +148,136 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
     if (!failed && lane_ok && last != nullptr) {
 #pragma unroll
         for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+    }
+}
+
+// Windowed forward (S > 1 sub-chunks of L rows per window, lane-scan prefix;
+// the window kernel's structure with the decay tile replaced by generated
+// decays): thread (s, g) loads its L rows of b, builds its L decays from the
+// rows' eta (loaded one window ahead) and its lanes' nu, summarizes its
+// sub-chunk as h -> P*h + Q, takes its entry state from the lane threads'
+// in-order walk over the S maps, and replays.  Splitting time inside the CTA
+// keeps several times more warps busy than the sequential form.
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ eta,
+                 const float *__restrict__ nu_log, typename C::St *__restrict__ out, float *__restrict__ last,
+                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 1, "generated-decay windowed forward: lane-scan shape, one plane");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[1] = {&tm_b};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
+        }
+        return;
+    }
+
+    const int s = threadIdx.x / G;
+    const int lg = threadIdx.x - s * G;
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + lg * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    const float *eta_row = eta + row0;
+    float nu[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+    float ev[L];  // eta of this thread's rows in the current window
+#pragma unroll
+    for (int j = 0; j < L; ++j) ev[j] = eta_at(eta_row, s * L + j, T);
+    float h[V];
+    float carry = 0.0f;  // window-to-window state of lane threadIdx.x (threads < DT)
+    int stage = 0, use = 0;
+    for (int k = 0; k < sm.nwin; ++k) {
+        const int rbase = k * sm.W + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float xa[L][V], xb[L][V], evn[L];
+#pragma unroll
+        for (int j = 0; j < L; ++j) evn[j] = eta_at(eta_row, rbase + sm.W + j, T);  // next window's rows
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            const float e = __expf(ev[j]);
+#pragma unroll
+            for (int v = 0; v < V; ++v) xa[j][v] = __expf(-__fmul_rn(nu[v], e));
+        }
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        const St *tb = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < L; ++j) unpack_lanes<St, V>(tb + j * DT, xb[j]);
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+        float P[V], Q[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+        if (n < L) {
+            // tail sub-chunk: steps past T become exact identity steps (a=1, b=0)
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    xa[j][v] = j < n ? xa[j][v] : 1.0f;
+                    xb[j][v] = j < n ? xb[j][v] : 0.0f;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                P[v] = __fmul_rn(xa[j][v], P[v]);
+                Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
+            }
+        }
+        float2 *pq = sm.sPQ<C>(0);
+#pragma unroll
+        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+        if (bar_sync_or(1, NT, !ok)) break;
+        // lane threads push the carried state through the sub-chunk maps in order
+        float *entry = sm.sEntry<C>();
+        if (static_cast<int>(threadIdx.x) < DT) {
+            float c = carry;
+#pragma unroll 4
+            for (int i = 0; i < S; ++i) {
+                const float2 m = pq[i * DT + threadIdx.x];
+                entry[i * DT + threadIdx.x] = c;
+                c = __fmaf_rn(m.x, c, m.y);
+            }
+            carry = c;
+        }
+        bar_sync_or(1, NT, false);
+#pragma unroll
+        for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
+        St *op = out + (row0 + rbase) * D + d;
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+            if (lane_ok && (n == L || j < n)) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
+        }
+        if (last != nullptr && lane_ok && n > 0 && rbase + n == T) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+        }
+#pragma unroll
+        for (int j = 0; j < L; ++j) ev[j] = evn[j];
     }
 }
 
@@ -207,19 +348,30 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
         const int n = min(T - wbase, L);
         const size_t o = (row0 + wbase) * D + d;
         float qrow[L];
-        // rows past T (only in the sequence's last window) are zero-filled:
-        // g stays 0 through them and their q is 0; nothing of theirs is stored
+        // phases: every row's log-decay and decay (independent of the state),
+        // then the dependent chain.  Rows past T (only in the sequence's last
+        // window) are zero-filled: g stays 0 through them and their q is 0;
+        // nothing of theirs is stored
+        float lav[L][V], av[L][V];
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            const float e = __shfl_sync(0xffffffffu, e_lane, j);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                lav[j][v] = -__fmul_rn(nu[v], e);
+                av[j][v] = __expf(lav[j][v]);
+            }
+        }
 #pragma unroll
         for (int j = L - 1; j >= 0; --j) {
             float hp[V], go[V], gav[V];
             unpack_lanes<St, V>(th + j * DT, hp);
             unpack_lanes<St, V>(tg + j * DT, go);
-            const float e = __shfl_sync(0xffffffffu, e_lane, j);
             float qs = 0.0f;
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float la = -__fmul_rn(nu[v], e);
-                const float a = __expf(la);
+                const float la = lav[j][v];
+                const float a = av[j][v];
                 g[v] = __fmaf_rn(a_next[v], g[v], go[v]);
                 gav[v] = __fmul_rn(g[v], hp[v]);
                 const float q = __fmul_rn(__fmul_rn(gav[v], a), la);

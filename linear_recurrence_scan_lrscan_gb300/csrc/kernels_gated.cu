@@ -1,6 +1,7 @@
 // Instantiations and launchers of the generated-decay scan kernels, and their
 // tile variant table.
 #include <algorithm>
+#include <cstdlib>
 
 #include "gated_kernels.cuh"
 #include "window_launch.cuh"
@@ -16,6 +17,21 @@ int launch_gwin_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     auto fn = gwin_fwd_kernel<C>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    using St = typename C::St;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], L.eta, L.nu_log, static_cast<St *>(L.out0), L.last, g,
+                                     L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C>
+int launch_gwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gwinw_fwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     using St = typename C::St;
     const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
@@ -58,6 +74,27 @@ WinDirCfg gdir_cfg(int nstage) {
     return d;
 }
 
+// Windowed generated-decay forward: S sub-chunks of L = 8 rows, lane scan.
+template <class C>
+WinDirCfg gwdir_cfg(int S, int nstage) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 1, "windowed generated-decay forward shape");
+    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
+    if (S > C::SMAX) std::abort();  // table error
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = S;
+    d.lane_scan = 1;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = S * C::G + 32;
+    d.smem = g.smem_bytes;
+    d.stage_bytes = g.stage_bytes;
+    d.launch = &launch_gwinw_fwd<C>;
+    return d;
+}
+
 // WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
 using GBF_64_1 = WinShape<bf16_t, 64, 1, 32, 1, 96, 1, true>;
 using GBB_64_1 = WinShape<bf16_t, 64, 1, 32, 2, 96, 1, true>;
@@ -68,16 +105,23 @@ using GFB_32_1 = WinShape<float, 32, 1, 32, 2, 64, 1, true>;
 using GFF_64_2 = WinShape<float, 64, 2, 32, 1, 64, 1, true>;
 using GFB_64_2 = WinShape<float, 64, 2, 32, 2, 64, 1, true>;
 
+using GWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 1, 160, 5, false>;
+using GWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 1, 288, 2, false>;
+
 #define F(SH, N) gdir_cfg<SH, true>(N)
 #define B(SH, N) gdir_cfg<SH, false>(N)
+#define FW(SH, S, N) gwdir_cfg<SH>(S, N)
 const WinVariant kGatedBF16[] = {
     {"gseq_bf16_d64_v1", F(GBF_64_1, 8), B(GBB_64_1, 6)},
     {"gseq_bf16_d64_v2", F(GBF_64_2, 8), B(GBB_64_2, 6)},
+    {"gwin_bf16_d32_s8", FW(GWF_BF_32_2_8, 8, 2), B(GBB_64_1, 6)},
 };
 const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
     {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
+    {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), B(GFB_32_1, 6)},
 };
+#undef FW
 #undef F
 #undef B
 

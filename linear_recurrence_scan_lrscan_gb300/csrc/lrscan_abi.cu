@@ -907,8 +907,8 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
         return LRSCAN_OK;
     }
     cudaStream_t st = pick_stream(stream);
+    if (T == 0) return copy_or_zero(grad_nu_log, nullptr, 1, D, st);  // no tokens: zero rate gradient
     if (!grad_eta || !grad_nu_log) return fail(LRSCAN_EINVAL, "NULL grad_eta or grad_nu_log");
-    if (T == 0) return copy_or_zero(grad_nu_log, nullptr, 1, D, st);
     if (!out || !grad_out || !grad_b) return fail(LRSCAN_EINVAL, "NULL out, grad_out or grad_b");
     if ((rc = check_params(eta, nu_log))) return rc;
     if (reinterpret_cast<uintptr_t>(grad_eta) % 4 || reinterpret_cast<uintptr_t>(grad_nu_log) % 4)

@@ -8,12 +8,17 @@ Tolerances (stated once, used by every parity test):
   * "exact": equal values (+0 == -0), used for the sequential paths, whose
     operation order is the oracle's own, and for identity-step padding.
 
+Sums over many terms (the generated-decay scan's grad_eta over lanes and
+grad_nu_log over tokens) are held to |got - ref| <= 1e-4 (1 + |ref|) +
+SUM_RTOL * sum|terms|: an fp32 sum of terms that are each within ~1e-6 of
+exact (fast exponential) can be off by a small multiple of 1e-6 of the sum of
+the terms' magnitudes, which is far larger than the result when they cancel.
+
 Paths that re-associate the recurrence through affine maps (window, chunk)
 make an fp32 error of a few ulps of the running state's magnitude.  Where a
 stored bf16 value is far smaller than that state (a near-cancellation), this
 can exceed 2 ulps of the tiny stored value; there the fp32 rule above is the
-bound, and such points must stay rare (REASSOC_MAX_FRACTION).  The named bf16
-workloads run on the sequential path, which is exact.
+bound, and such points must stay rare (REASSOC_MAX_FRACTION).
 """
 from __future__ import annotations
 
@@ -23,6 +28,7 @@ import torch
 F32_RTOL = 1e-4
 BF16_MAX_ULPS = 2
 REASSOC_MAX_FRACTION = 1e-3
+SUM_RTOL = 1e-5
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -80,3 +86,15 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", e
 def assert_last_close(got: np.ndarray, ref: np.ndarray, what: str = "last", exact: bool = False):
     """`last` is fp32 whatever the storage dtype: fp32 rule (or exact)."""
     assert_close(got.astype(np.float32), ref.astype(np.float32), "f32", what, exact)
+
+
+def assert_sum_close(got: np.ndarray, ref: np.ndarray, abs_sum: np.ndarray, what: str = "sum"):
+    """fp32 sums of many terms: |got - ref| <= 1e-4 (1 + |ref|) + SUM_RTOL * abs_sum,
+    where abs_sum is the sum of the absolute values of the summed terms."""
+    g, r, a = (np.asarray(x, dtype=np.float64) for x in (got, ref, abs_sum))
+    assert g.shape == r.shape == a.shape, (what, g.shape, r.shape, a.shape)
+    bad = ~(np.abs(g - r) <= F32_RTOL * (1.0 + np.abs(r)) + SUM_RTOL * a)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = [(tuple(i), float(g[tuple(i)]), float(r[tuple(i)]), float(a[tuple(i)])) for i in idx]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} sums out of tolerance; first: {detail}")
