@@ -823,6 +823,9 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
+    } else if (dir == 0 && (vi = find_one_wave(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8",
+                                                 dir, B, D, g)) >= 0) {
+        // the windowed forward: the measured fastest where all its CTAs fit one wave
     } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
         for (int i = 0; i < n; ++i) {
