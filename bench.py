@@ -572,15 +572,21 @@ def run_long_t(dev, peak) -> dict:
     return res
 
 
+# Sources of the time-tiled real-scan kernels the benchmark's step runs (their
+# code, shapes, stage counts and launch): DRAM counters recorded under another
+# hash of these files are stale.
+TILED_KERNEL_SOURCES = ("scan_common.cuh", "state_args.h", "window_kernels.cuh", "window_shapes.h",
+                        "window_launch.cuh", "kernels_window.cu")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; DRAM counters recorded for another hash are stale."""
+    """Hash of the tiled kernels' sources (TILED_KERNEL_SOURCES)."""
     import hashlib
     csrc = os.path.join(ROOT, "linear_recurrence_scan_lrscan_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in TILED_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
