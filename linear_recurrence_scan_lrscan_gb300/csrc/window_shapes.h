@@ -44,8 +44,6 @@ using BF_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 2, 160, 5, false>;
 using BB_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 3, 160, 5, false>;
 using BF_32_2_8_M8 = WinShape<bf16_t, 32, 2, 8, 2, 96, 8, false>;
 using BB_32_2_8_M8 = WinShape<bf16_t, 32, 2, 8, 3, 96, 8, false>;
-// 16 sub-chunks with a residency floor of 3 (640 lane tiles in 1.4 waves)
-using BB_32_2_8_M3 = WinShape<bf16_t, 32, 2, 8, 3, 288, 3, false>;
 // per-thread-prefix shapes (parallel fold, short critical path)
 using PF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, true>;
 using PFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, true>;
@@ -63,6 +61,6 @@ using WBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false>;
 #define LRSCAN_WIN_BWD_SHAPES(X)                                                                   \
     X(SBB_64_2_32) X(SBB_32_1_32) X(SBB_64_1_32) X(SBB_128_2_32) X(SBB_128_4_16) X(SFB_32_1_32) \
     X(SFB_64_2_16) X(SFB_64_1_32) X(SFB_128_4_8) X(BB_64_2_8) X(BB_32_2_8) X(FB_16_1_8)          \
-    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8) X(BB_32_2_8_M3)
+    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8)
 
 }  // namespace lrscan
