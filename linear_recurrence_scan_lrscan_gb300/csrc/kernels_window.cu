@@ -65,8 +65,6 @@ const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s8_m5_n2", F(BF_32_2_8_M5, 8, 2), B(BB_32_2_8_M5, 8, 2)},
     {"win_bf16_d32_s4_m8", F(BF_32_2_8_M8, 4, 4), B(BB_32_2_8_M8, 4, 3)},
     {"win_bf16_d32_s4_m8_n2", F(BF_32_2_8_M8, 4, 2), B(BB_32_2_8_M8, 4, 2)},
-    {"win_bf16_d32_s16_pt", F(PBF_32_2_8, 16, 3), B(PBB_32_2_8, 16, 4)},
-    {"win_bf16_d32_s16_pt_n2", F(PBF_32_2_8, 16, 2), B(PBB_32_2_8, 16, 2)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},

@@ -49,8 +49,6 @@ using PF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, true>;
 using PFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, true>;
 using PF_16_1_8 = WinShape<float, 16, 1, 8, 2, 544, 1, false, true>;
 using PFB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1, false, true>;
-using PBF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 2, 288, 2, false, true>;
-using PBB_32_2_8 = WinShape<bf16_t, 32, 2, 8, 3, 288, 2, false, true>;
 // L = 16: half the sub-chunks (and half the in-CTA prefix work) per window row
 using WBF_32_2_16 = WinShape<bf16_t, 32, 2, 16, 2, 288, 1, false>;
 using WBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false>;
@@ -58,11 +56,11 @@ using WBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false>;
 #define LRSCAN_WIN_FWD_SHAPES(X)                                                                   \
     X(SBF_64_2_32) X(SBF_128_2_32) X(SBF_128_4_32) X(SBF_32_1_32) X(SBF_64_1_32) X(SFF_32_1_32) \
     X(SFF_64_2_16) X(SFF_64_1_32) X(SFF_128_4_8) X(BF_64_2_8) X(BF_32_2_8) X(FF_16_1_8)          \
-    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8) X(PBF_32_2_8)
+    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8)
 
 #define LRSCAN_WIN_BWD_SHAPES(X)                                                                   \
     X(SBB_64_2_32) X(SBB_32_1_32) X(SBB_64_1_32) X(SBB_128_2_32) X(SBB_128_4_16) X(SFB_32_1_32) \
     X(SFB_64_2_16) X(SFB_64_1_32) X(SFB_128_4_8) X(BB_64_2_8) X(BB_32_2_8) X(FB_16_1_8)          \
-    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8) X(PBB_32_2_8)
+    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8)
 
 }  // namespace lrscan
