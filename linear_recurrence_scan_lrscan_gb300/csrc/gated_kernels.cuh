@@ -394,11 +394,190 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
     }
 }
 
+// Windowed backward (S sub-chunks of L = 8 rows, G = 16 threads per
+// sub-chunk row, lane-scan prefix).  Tiles: out one row early and grad_out.
+// Thread (s, g) builds the decays of rows rbase .. rbase + L (a_{t+1} for
+// its last row comes from the next sub-chunk's first row; 0 past T), takes
+// the adjoint entering its sub-chunk from the lane threads' walk over the S
+// reverse maps, replays, and sums q over its rows.  Row sums over the CTA's
+// lanes: the 16 threads of a sub-chunk exchange their 8 row sums (xor 8, then
+// a transpose-sum over 8 lanes): lane g < 8 ends with row g's sum.
+// part_eta: [B*T][gridDim.x]; part_nu: [B*S][D] (time sums per sub-chunk).
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_go,
+                 const float *__restrict__ eta, const float *__restrict__ nu_log,
+                 typename C::St *__restrict__ grad_b, float *__restrict__ part_eta, float *__restrict__ part_nu,
+                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 2 && C::L == 8 && C::G == 16,
+                  "windowed generated-decay backward: lane-scan shape, two planes, 8 rows x 16 threads");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+    const int nwin = sm.nwin;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[2] = {&tm_out, &tm_go};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow,
+                            [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i == 0 ? -1 : 0); }, wc);
+        }
+        return;
+    }
+
+    const int s = threadIdx.x / G;
+    const int lg = threadIdx.x - s * G;
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + lg * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    const float *eta_row = eta + row0;
+    const int ncol = gridDim.x;
+    float nu[V], acc_nu[V], g[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        acc_nu[v] = 0.0f;
+    }
+    float ev[L + 1];  // eta of rows rbase .. rbase + L of the window being processed
+    {
+        const int rb = (nwin - 1) * sm.W + s * L;
+#pragma unroll
+        for (int j = 0; j <= L; ++j) ev[j] = eta_at(eta_row, rb + j, T);
+    }
+    float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (threads < DT)
+    int stage = 0, use = 0;
+    for (int k = 0; k < nwin; ++k) {
+        const int wbase = (nwin - 1 - k) * sm.W;
+        const int rbase = wbase + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float evn[L + 1];
+#pragma unroll
+        for (int j = 0; j <= L; ++j) evn[j] = eta_at(eta_row, rbase - sm.W + j, T);  // next processed window
+        // decays a[j] of rows rbase + j (j = 0..L) and log-decays la[j] (j < L)
+        float a[L + 1][V], la[L][V];
+#pragma unroll
+        for (int j = 0; j <= L; ++j) {
+            const float e = __expf(ev[j]);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float l = -__fmul_rn(nu[v], e);
+                if (j < L) la[j][v] = l;
+                a[j][v] = __expf(l);
+            }
+        }
+        float xh[L][V], xg[L][V];
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        const St *th = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // h_{t-1}
+        const St *tg = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // grad_out_t
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                unpack_lanes<St, V>(th + j * DT, xh[j]);
+                unpack_lanes<St, V>(tg + j * DT, xg[j]);
+            }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+        // a'_{t+1} of row j is a[j + 1]: 0 for the row just before the end of
+        // the sequence (nothing enters after the last step), 1 for the
+        // identity steps past T in a tail sub-chunk.  Only rows j < n use
+        // a[j] and la[j] for their q, and j + 1 >= tl implies j + 1 >= n, so
+        // rewriting a[j + 1] there leaves every used a_t intact.
+        const int tl = T - rbase;  // rows of this sub-chunk before the sequence's end (may be <= 0)
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (j + 1 >= tl) a[j + 1][v] = (j < n) ? 0.0f : 1.0f;
+                if (j >= n) xg[j][v] = 0.0f;
+            }
+        }
+        float P[V], Q[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                P[v] = __fmul_rn(a[j + 1][v], P[v]);
+                Q[v] = __fmaf_rn(a[j + 1][v], Q[v], xg[j][v]);
+            }
+        }
+        float2 *pq = sm.sPQ<C>(0);
+#pragma unroll
+        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+        if (bar_sync_or(1, NT, !ok)) break;
+        float *entry = sm.sEntry<C>();
+        if (static_cast<int>(threadIdx.x) < DT) {
+            float c = carry;
+#pragma unroll 4
+            for (int i = S - 1; i >= 0; --i) {
+                const float2 m = pq[i * DT + threadIdx.x];
+                entry[i * DT + threadIdx.x] = c;
+                c = __fmaf_rn(m.x, c, m.y);
+            }
+            carry = c;
+        }
+        bar_sync_or(1, NT, false);
+#pragma unroll
+        for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
+        float qrow[L];
+        St *gbp = grad_b + (row0 + rbase) * D + d;
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+            float qs = 0.0f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                g[v] = __fmaf_rn(a[j + 1][v], g[v], xg[j][v]);
+                const float q = (j < n) ? __fmul_rn(__fmul_rn(__fmul_rn(g[v], xh[j][v]), a[j][v]), la[j][v]) : 0.0f;
+                acc_nu[v] += q;
+                qs += q;
+            }
+            qrow[j] = qs;
+            if (lane_ok && (n == L || j < n)) store_lanes<St, V>(gbp + static_cast<size_t>(j) * D, g);
+        }
+        // row sums over the sub-chunk's 16 threads (both half-warps do the same steps)
+#pragma unroll
+        for (int j = 0; j < L; ++j) qrow[j] += __shfl_xor_sync(0xffffffffu, qrow[j], 8);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1) {
+            const bool upper = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const float send = upper ? qrow[i] : qrow[i + w];
+                const float keep = upper ? qrow[i + w] : qrow[i];
+                qrow[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+        }
+        const int r = lg & 7;  // this thread now holds row r's sum
+        if (lg < 8 && r < n) part_eta[(row0 + rbase + r) * ncol + blockIdx.x] = qrow[0];
+#pragma unroll
+        for (int j = 0; j <= L; ++j) ev[j] = evn[j];
+    }
+    if (lane_ok) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) part_nu[(static_cast<size_t>(brow) * S + s) * D + d + v] = acc_nu[v];
+    }
+}
+
 // grad_eta[r] = sum over the ncol partials of row r (r < rows);
-// grad_nu_log[d] = sum over the B partials of lane d.
+// grad_nu_log[d] = sum over the nu_rows partials of lane d.
 __global__ void __launch_bounds__(256)
 gated_finish(const float *__restrict__ part_eta, const float *__restrict__ part_nu, float *__restrict__ grad_eta,
-             float *__restrict__ grad_nu_log, long long rows, int ncol, int B, int D) {
+             float *__restrict__ grad_nu_log, long long rows, int ncol, int nu_rows, int D) {
     const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (i < rows) {
         const float *p = part_eta + i * ncol;
@@ -408,7 +587,7 @@ gated_finish(const float *__restrict__ part_eta, const float *__restrict__ part_
     } else if (i < rows + D) {
         const int dd = static_cast<int>(i - rows);
         float s = 0.0f;
-        for (int b = 0; b < B; ++b) s += part_nu[static_cast<size_t>(b) * D + dd];
+        for (int b = 0; b < nu_rows; ++b) s += part_nu[static_cast<size_t>(b) * D + dd];
         grad_nu_log[dd] = s;
     }
 }

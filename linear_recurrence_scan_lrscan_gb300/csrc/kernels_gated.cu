@@ -41,6 +41,21 @@ int launch_gwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
 }
 
 template <class C>
+int launch_gwinw_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gwinw_bwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    using St = typename C::St;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, static_cast<St *>(L.out0),
+                                     L.part_eta, L.part_nu, g, L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C>
 int launch_gwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static unsigned long long mask = 0;
     static std::mutex mu;
@@ -74,10 +89,10 @@ WinDirCfg gdir_cfg(int nstage) {
     return d;
 }
 
-// Windowed generated-decay forward: S sub-chunks of L = 8 rows, lane scan.
-template <class C>
+// Windowed generated-decay tiles: S sub-chunks of L = 8 rows, lane scan.
+template <class C, bool FWD>
 WinDirCfg gwdir_cfg(int S, int nstage) {
-    static_assert(!C::SEQ && !C::PT && C::NIN == 1, "windowed generated-decay forward shape");
+    static_assert(!C::SEQ && !C::PT && C::NIN == (FWD ? 1 : 2), "windowed generated-decay shape");
     const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
     if (S > C::SMAX) std::abort();  // table error
     WinDirCfg d{};
@@ -91,7 +106,8 @@ WinDirCfg gwdir_cfg(int S, int nstage) {
     d.threads = S * C::G + 32;
     d.smem = g.smem_bytes;
     d.stage_bytes = g.stage_bytes;
-    d.launch = &launch_gwinw_fwd<C>;
+    if constexpr (FWD) d.launch = &launch_gwinw_fwd<C>;
+    else d.launch = &launch_gwinw_bwd<C>;
     return d;
 }
 
@@ -107,21 +123,26 @@ using GFB_64_2 = WinShape<float, 64, 2, 32, 2, 64, 1, true>;
 
 using GWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 1, 160, 5, false>;
 using GWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 1, 288, 2, false>;
+using GWB_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 2, 288, 2, false>;
+using GWB_FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 288, 2, false>;
 
 #define F(SH, N) gdir_cfg<SH, true>(N)
 #define B(SH, N) gdir_cfg<SH, false>(N)
-#define FW(SH, S, N) gwdir_cfg<SH>(S, N)
+#define FW(SH, S, N) gwdir_cfg<SH, true>(S, N)
+#define BW(SH, S, N) gwdir_cfg<SH, false>(S, N)
 const WinVariant kGatedBF16[] = {
     {"gseq_bf16_d64_v1", F(GBF_64_1, 8), B(GBB_64_1, 6)},
     {"gseq_bf16_d64_v2", F(GBF_64_2, 8), B(GBB_64_2, 6)},
-    {"gwin_bf16_d32_s8", FW(GWF_BF_32_2_8, 8, 2), B(GBB_64_1, 6)},
+    {"gwin_bf16_d32_s8", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8, 16, 2)},
+    {"gwin_bf16_d32_s8_n3", FW(GWF_BF_32_2_8, 8, 3), BW(GWB_BF_32_2_8, 16, 3)},
 };
 const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
     {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
-    {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), B(GFB_32_1, 6)},
+    {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), BW(GWB_FF_16_1_8, 16, 2)},
 };
 #undef FW
+#undef BW
 #undef F
 #undef B
 
@@ -137,11 +158,11 @@ const WinVariant *gwin_variants(int dtype, int *count) {
 }
 
 int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
-                        long long rows, int ncol, int B, int D, cudaStream_t stream) {
+                        long long rows, int ncol, int nu_rows, int D, cudaStream_t stream) {
     const long long n = rows + D;
     if (n == 0) return 0;
     gated_finish<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(part_eta, part_nu, grad_eta,
-                                                                           grad_nu_log, rows, ncol, B, D);
+                                                                           grad_nu_log, rows, ncol, nu_rows, D);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -91,7 +91,10 @@ const WinVariant *cwin_variants(int dtype, int *count);
 const WinVariant *gwin_variants(int dtype, int *count);
 int gplain_launch(const WinLaunch &L, int dtype, bool fwd);
 int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
-                        long long rows, int ncol, int B, int D, cudaStream_t stream);
+                        long long rows, int ncol, int nu_rows, int D, cudaStream_t stream);
+// Most sub-chunks a windowed generated-decay backward tile uses (rows of its
+// grad_nu_log partials per batch row).
+constexpr int kGatedMaxS = 16;
 
 // Three-phase chunked path and plain kernels (kernels_chunk.cu).
 struct ChunkLaunch {

@@ -792,9 +792,12 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
 // columns plus the ragged last CTA's extra warps.
 int64_t gated_ncol_bound(int64_t D) { return (D + 31) / 32 + 4; }
 
+// Backward scratch: grad_eta partials [B*T][ncol], then grad_nu_log partials
+// [B * kGatedMaxS][D] (one row per batch row and sub-chunk).
 size_t gated_workspace(int64_t B, int64_t T, int64_t D) {
     auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
-    return pad(static_cast<size_t>(B) * T * gated_ncol_bound(D) * 4) + pad(static_cast<size_t>(B) * D * 4);
+    return pad(static_cast<size_t>(B) * T * gated_ncol_bound(D) * 4) +
+           pad(static_cast<size_t>(B) * kGatedMaxS * D * 4);
 }
 
 // Tiled sequential kernels for 16-byte aligned rows, else plain kernels.
@@ -936,7 +939,7 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
     L.timeout_ns = g_timeout_ns.load();
     L.stream = st;
     L.device = dev;
-    int ncol;
+    int ncol, nu_rows = static_cast<int>(B);
     if (ch.path == kPathPlain) {
         ncol = static_cast<int>((D + 31) / 32);
         L.in0 = out; L.in1 = grad_out; L.out0 = grad_b;
@@ -945,7 +948,12 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
         if (gplain_launch(L, dtype, false)) return fail(LRSCAN_ECUDA, "generated-decay plain launch failed");
     } else {
         const WinDirCfg &v = ch.var->bwd;
-        ncol = static_cast<int>(((D + v.dt - 1) / v.dt) * (v.threads - 32) / 32);
+        // windowed tile: one partial per (row, CTA) and per (batch row,
+        // sub-chunk); sequential tile: one per (row, warp) and per batch row
+        const bool win = v.s > 1;
+        if (win && v.s > kGatedMaxS) return fail(LRSCAN_EINVAL, "internal: too many sub-chunks for the workspace");
+        ncol = static_cast<int>(win ? (D + v.dt - 1) / v.dt : ((D + v.dt - 1) / v.dt) * (v.threads - 32) / 32);
+        nu_rows = static_cast<int>(win ? B * v.s : B);
         const size_t es = esize(dtype);
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
@@ -959,15 +967,15 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
             L.eta = eta + b0 * T;
             L.out0 = static_cast<char *>(grad_b) + off;
             L.part_eta = part_eta + static_cast<size_t>(b0) * T * ncol;
-            L.part_nu = part_nu + static_cast<size_t>(b0) * D;
+            L.part_nu = part_nu + static_cast<size_t>(b0) * (win ? v.s : 1) * D;
             L.B = nb; L.T = T; L.D = D;
             if (v.launch(L, v))
                 return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
         }
     }
     if (ncol > gated_ncol_bound(D)) return fail(LRSCAN_EINVAL, "internal: partial columns exceed the workspace");
-    if (gated_finish_launch(part_eta, part_nu, grad_eta, grad_nu_log, B * T, ncol, static_cast<int>(B),
-                            static_cast<int>(D), st))
+    if (gated_finish_launch(part_eta, part_nu, grad_eta, grad_nu_log, B * T, ncol, nu_rows, static_cast<int>(D),
+                            st))
         return fail(LRSCAN_ECUDA, "generated-decay reduction launch failed");
     return LRSCAN_OK;
 }
