@@ -623,6 +623,17 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
 }
 
 // ---------------------------------------------------------------- complex --
+// Index of the named variant when it fits on an SM and gives at least 0.9
+// CTAs per SM, else -1.
+int find_variant(const WinVariant *tab, int n, const char *name, int dir, int64_t B, int64_t D, const Geometry &g) {
+    for (int i = 0; i < n; ++i) {
+        if (std::strcmp(tab[i].name, name) != 0) continue;
+        const Occ o = occupancy(tab[i], dir, B, D, g);
+        if (o.resident > 0 && static_cast<double>(o.ctas) >= 0.9 * g.sm_count) return i;
+    }
+    return -1;
+}
+
 // Index of the named variant when all its CTAs are resident at once (and
 // they are at least 0.9 per SM), else -1.
 int find_one_wave(const WinVariant *tab, int n, const char *name, int dir, int64_t B, int64_t D, const Geometry &g) {
@@ -788,9 +799,10 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
 }
 
 // ------------------------------------------------------- generated decay --
-// Partial-sum columns per row of the backward: at most ceil(D/32) warp
-// columns plus the ragged last CTA's extra warps.
-int64_t gated_ncol_bound(int64_t D) { return (D + 31) / 32 + 4; }
+// Partial-sum columns per row of the backward: one per CTA of a windowed
+// tile (at least 16 lanes each) or per warp of a sequential tile (32 lanes),
+// plus the ragged last CTA's extra warps.
+int64_t gated_ncol_bound(int64_t D) { return (D + 15) / 16 + 4; }
 
 // Backward scratch: grad_eta partials [B*T][ncol], then grad_nu_log partials
 // [B * kGatedMaxS][D] (one row per batch row and sub-chunk).
@@ -826,9 +838,10 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
-    } else if (dir == 0 && (vi = find_one_wave(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8",
-                                                 dir, B, D, g)) >= 0) {
-        // the windowed forward: the measured fastest where all its CTAs fit one wave
+    } else if ((vi = find_variant(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8", dir, B, D,
+                                  g)) >= 0) {
+        // the windowed tiles (time split inside the CTA): the measured fastest in both
+        // directions wherever the lanes give the GPU at least 0.9 CTAs per SM
     } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
         for (int i = 0; i < n; ++i) {
