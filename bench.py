@@ -162,8 +162,30 @@ def run_reference(args, w) -> dict:
     }
 
 
+def _oracle_slice_worker(args):
+    """One host process: the oracle's forward + backward on its own lanes of
+    the sample, `reps` times; returns (elements, seconds)."""
+    cid, lanes, lo, hi, reps = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS, make_inputs, to_numpy_storage
+    w = WORKLOADS[cid]
+    inp = make_inputs(cid, B=1, D=lanes)
+    a, b, g = (to_numpy_storage(inp[k])[:, :, lo:hi].copy() for k in ("a", "b", "grad_out"))
+    o = oracle.default()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        out, _ = o.fwd(a, b, w.dtype)
+        o.bwd(a, out, g, w.dtype)
+    return a.size * reps, time.perf_counter() - t0
+
+
 def cpu_baseline(w, seconds: float = 12.0) -> dict:
-    """The oracle as it stands, single-threaded, on a bounded sample."""
+    """The oracle as it stands on a bounded sample: single-threaded, and on
+    every host core (the sample's lanes split into disjoint slices, one
+    spawn-started process per core; lanes are independent)."""
+    import multiprocessing as mp
+
     import oracle
     from linear_recurrence_scan_lrscan_gb300.workloads import make_inputs, to_numpy_storage
 
@@ -180,8 +202,26 @@ def cpu_baseline(w, seconds: float = 12.0) -> dict:
         o.bwd(a, out, g, w.dtype)
         t_tot += time.perf_counter() - t0
         n += 1
-    return {"value": E * n / t_tot, "unit": "elements/s", "cores": 1, "kind": "oracle",
-            "sample": f"B=1 T={w.T} D={lanes} of {w.describe()}, fwd+bwd, {n} repetitions, single thread"}
+    single = E * n / t_tot
+    cores = max(1, min(os.cpu_count() or 1, lanes))
+    reps = max(1, n)
+    cuts = [lanes * i // cores for i in range(cores + 1)]
+    jobs = [(w.cid, lanes, cuts[i], cuts[i + 1], reps) for i in range(cores) if cuts[i + 1] > cuts[i]]
+    from concurrent.futures import ProcessPoolExecutor
+    # spawn-started workers (a fork after CUDA initialisation is unsafe); a
+    # worker that dies raises here instead of hanging the pool
+    with ProcessPoolExecutor(max_workers=len(jobs), mp_context=mp.get_context("spawn")) as pool:
+        t0 = time.perf_counter()
+        res = list(pool.map(_oracle_slice_worker, jobs))
+        wall = time.perf_counter() - t0
+    done = sum(r[0] for r in res)
+    slowest = max(r[1] for r in res)
+    multi = done / slowest
+    return {"value": multi, "unit": "elements/s", "cores": len(jobs), "kind": "oracle",
+            "sample": f"B=1 T={w.T} D={lanes} of {w.describe()}, fwd+bwd; {len(jobs)} spawn-started processes "
+                      f"on disjoint lane slices, {reps} repetitions each (slowest process's compute time; "
+                      f"{wall:.1f} s wall with start-up)",
+            "single_thread": {"value": single, "cores": 1, "repetitions": n}}
 
 
 def config_of(w, pf, pb) -> dict:
