@@ -53,19 +53,15 @@ WinDirCfg lb_cfg(int S) {
 
 // WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
 using LBF_F32 = WinShape<float, 32, 1, 8, 2, 288, 3, false>;
-using LBF_F32_L16 = WinShape<float, 32, 1, 16, 2, 288, 2, false>;
 using LBF_BF16 = WinShape<bf16_t, 32, 2, 8, 2, 160, 5, false>;
-using LBF_BF16_L16 = WinShape<bf16_t, 32, 2, 16, 2, 160, 3, false>;
 
 const WinVariant kLbF32[] = {
     {"lb_f32_d32_s8", lb_cfg<LBF_F32>(8), WinDirCfg{}},
     {"lb_f32_d32_s4", lb_cfg<LBF_F32>(4), WinDirCfg{}},
-    {"lb_f32_d32_l16_s8", lb_cfg<LBF_F32_L16>(8), WinDirCfg{}},
 };
 const WinVariant kLbBF16[] = {
     {"lb_bf16_d32_s8", lb_cfg<LBF_BF16>(8), WinDirCfg{}},
     {"lb_bf16_d32_s4", lb_cfg<LBF_BF16>(4), WinDirCfg{}},
-    {"lb_bf16_d32_l16_s8", lb_cfg<LBF_BF16_L16>(8), WinDirCfg{}},
 };
 
 }  // namespace

@@ -183,18 +183,13 @@ lb_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
         } else {
             if (ch < D) lb.maps[static_cast<size_t>(k) * nl + gl] = make_float2(wp, wq);
             publish(myflag, kLbMap);
-            // Warp-wide look back, 32 earlier windows per round: lane i
-            // inspects window j0 - i (acquire; every window publishes its map
-            // without waiting, so each flag appears); the nearest window with
-            // an inclusive state ends the walk, the windows before it have
-            // their maps composed in (acc = m_{j0} o m_{j0-1} o ...).
+            // look back: acc = (maps of windows j+1 .. k-1 composed)
             float ap = 1.0f, aq = 0.0f;
             bool timed_out = false;
-            for (int j0 = k - 1; j0 >= 0; j0 -= 32) {
-                const int jw = j0 - lane;
-                unsigned f = kLbIncl;  // nothing before window 0
-                if (jw >= 0) {
-                    const unsigned *fp = lb.flags + static_cast<size_t>(jw) * lb.nlt + tile;
+            for (int j = k - 1; j >= 0; --j) {
+                const unsigned *fp = lb.flags + static_cast<size_t>(j) * lb.nlt + tile;
+                unsigned f = 0;
+                if (lane == 0) {
                     const uint64_t start = global_timer_ns();
                     while ((f = ld_flag_acquire(fp)) == 0u) {
                         if (global_timer_ns() - start > timeout_ns) {
@@ -203,22 +198,18 @@ lb_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
                         }
                     }
                 }
-                if (__any_sync(0xffffffffu, f == 0u)) { timed_out = true; break; }
-                const unsigned pmask = __ballot_sync(0xffffffffu, f == kLbIncl);
-                __threadfence();  // the inspected flags were acquired by the warp: their data are visible
-                const int stop = pmask ? __ffs(pmask) - 1 : 32;  // windows j0 .. j0-stop+1 have maps only
-                for (int i = 0; i < stop; ++i) {
-                    const float2 m =
-                        ch < D ? __ldcg(lb.maps + static_cast<size_t>(j0 - i) * nl + gl) : make_float2(1.0f, 0.0f);
-                    aq = __fmaf_rn(ap, m.y, aq);
-                    ap = __fmul_rn(ap, m.x);
-                }
-                if (stop < 32) {
-                    const int jp = j0 - stop;
-                    const float h = (jp >= 0 && ch < D) ? __ldcg(lb.incl + static_cast<size_t>(jp) * nl + gl) : 0.0f;
+                f = __shfl_sync(0xffffffffu, f, 0);
+                if (f == 0u) { timed_out = true; break; }
+                __threadfence();  // lane 0 acquired the flag; its data are visible to the warp
+                if (f == kLbIncl) {
+                    const float h = ch < D ? __ldcg(lb.incl + static_cast<size_t>(j) * nl + gl) : 0.0f;
                     c = __fmaf_rn(ap, h, aq);
                     break;
                 }
+                const float2 m = ch < D ? __ldcg(lb.maps + static_cast<size_t>(j) * nl + gl) : make_float2(1.0f, 0.0f);
+                // acc <- acc o m_j  (m_j applies first)
+                aq = __fmaf_rn(ap, m.y, aq);
+                ap = __fmul_rn(ap, m.x);
             }
             if (!timed_out) {
                 if (ch < D) lb.incl[static_cast<size_t>(k) * nl + gl] = __fmaf_rn(wp, c, wq);
