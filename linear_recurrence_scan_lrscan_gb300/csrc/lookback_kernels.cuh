@@ -73,17 +73,16 @@ lb_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ unsigned s_ticket;
     const WinSmem sm = WinSmem::make(smem_raw, geom);
-    // the ticket lives next to the abort flag (the flag area has 16 bytes)
-    volatile unsigned *s_ticket = reinterpret_cast<volatile unsigned *>(smem_raw + geom.flag_off + 8);
     const int S = geom.S;
     const int NT = S * G;
     win_init<C>(sm, NT / 32, S);
     pdl_trigger();
     pdl_wait();
-    if (threadIdx.x == 0) *s_ticket = atomicAdd(lb.ticket, 1u);
+    if (threadIdx.x == 0) s_ticket = atomicAdd(lb.ticket, 1u);
     __syncthreads();
-    const unsigned id = *s_ticket;
+    const unsigned id = s_ticket;
     const int tile = static_cast<int>(id % static_cast<unsigned>(lb.nlt));  // (batch row, lane tile)
     const int k = static_cast<int>(id / static_cast<unsigned>(lb.nlt));      // time window
     const int brow = tile / lanes_per_row;
