@@ -73,8 +73,6 @@ extern "C" {
 #define LRSCAN_PATH_CHUNK   2  /* three phases: chunk summary -> warp-shuffle prefix -> replay */
 #define LRSCAN_PATH_WINDOW  3  /* single pass: time windows in shared memory, split in time inside the CTA */
 #define LRSCAN_PATH_PLAIN   4  /* sequential, plain loads; any alignment */
-#define LRSCAN_PATH_LOOKBACK 5 /* single pass over (lane tile, time window) CTAs with decoupled look-back
-                                  (forward); workspace lrscan_lookback_workspace_bytes() */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */
@@ -280,11 +278,6 @@ int lrscan_compose_maps(const float *maps, int64_t W, int64_t rank, const float 
 /* Sets the calling thread's stream (a cudaStream_t; NULL = legacy default
  * stream) used by lrscan_fwd / lrscan_bwd and by _ex calls given NULL. */
 int lrscan_set_stream(void *stream);
-
-/* Device bytes the look-back path needs: per-window flags, window maps and
- * states ([ceil(T/W)] x [B, D] fp32 x 3 plus flags), for the smallest window
- * any look-back tile uses (W = 32 rows); 0 for an empty problem. */
-size_t lrscan_lookback_workspace_bytes(int64_t B, int64_t T, int64_t D);
 
 /* Device bytes the chunked path needs for this shape: two fp32 [B, ceil(T/C), D]
  * buffers, plus two fp32 [B, ceil(T/C/512), D] buffers for the grouped prefix

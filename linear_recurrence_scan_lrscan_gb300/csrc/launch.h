@@ -34,7 +34,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 struct DevStatus;
 
-enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3, kPathPlain = 4, kPathLookback = 5 };
+enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3, kPathPlain = 4 };
 
 // Arguments of one time-tiled launch (forward: maps a,b / out0=out;
 // backward: maps a,out,grad_out / out0=grad_a, out1=grad_b).
@@ -56,10 +56,6 @@ struct WinLaunch {
     const float *eta, *nu_log;
     float *part_eta, *part_nu;
     const void *in0, *in1;
-    // single-pass look-back: per-launch scratch (zeroed flags and ticket)
-    unsigned int *lb_ticket, *lb_flags;
-    float2 *lb_maps;
-    float *lb_incl;
 };
 
 // One direction of a tile variant: compiled shape (DT, V, L) plus the
@@ -86,10 +82,6 @@ struct WinVariant {
 
 // path: kPathSeq or kPathWindow; dtype 0 = f32, 1 = bf16
 const WinVariant *win_variants(int path, int dtype, int *count);
-
-// Single-pass look-back tile variants (kernels_lookback.cu): forward only
-// (the backward entries have no launch function).
-const WinVariant *lb_variants(int dtype, int *count);
 
 // Complex scan tile variants (kernels_complex.cu); dtype 0 = f32, 1 = bf16.
 const WinVariant *cwin_variants(int dtype, int *count);

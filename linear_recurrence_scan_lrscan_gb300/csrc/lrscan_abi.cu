@@ -179,26 +179,6 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = tr
     return chunk_scratch(B, T, D, C, grouped).total();
 }
 
-// Look-back scratch: the ticket (256 bytes), flags [nwin][nlt] u32, window
-// maps [nwin][B*D] float2 and states [nwin][B*D] float; ticket and flags are
-// contiguous (one memset per launch).
-struct LbScratch {
-    size_t flags_off, flags_bytes, maps_off, incl_off, total;
-};
-LbScratch lookback_scratch(int64_t B, int64_t T, int64_t D, int W) {
-    auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
-    const int64_t nwin = (T + W - 1) / W;
-    const int64_t nlt = B * ((D + 31) / 32);
-    LbScratch s;
-    s.flags_off = 256;
-    s.flags_bytes = pad(static_cast<size_t>(nwin) * nlt * 4);
-    s.maps_off = s.flags_off + s.flags_bytes;
-    s.incl_off = s.maps_off + pad(static_cast<size_t>(nwin) * B * D * 8);
-    s.total = s.incl_off + pad(static_cast<size_t>(nwin) * B * D * 4);
-    return s;
-}
-size_t lookback_workspace(int64_t B, int64_t T, int64_t D, int W) { return lookback_scratch(B, T, D, W).total; }
-
 // The grouped prefix pays when every lane has many chunks and the lanes alone
 // give the GPU few warps to run the flat per-lane prefix.
 bool use_grouped_prefix(int64_t B, int64_t T, int64_t D, int C, const Geometry &g) {
@@ -301,8 +281,8 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
     ch->vec = (aligned16 && D % vmax == 0) ? vmax : 1;
 
     int path = want;
-    if (want < kPathAuto || want > kPathLookback) return fail(LRSCAN_EINVAL, "unknown path %d", want);
-    if ((path == kPathSeq || path == kPathWindow || path == kPathLookback) && !aligned16)
+    if (want < kPathAuto || want > kPathPlain) return fail(LRSCAN_EINVAL, "unknown path %d", want);
+    if ((path == kPathSeq || path == kPathWindow) && !aligned16)
         return fail(LRSCAN_EINVAL, "path %d needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)", path);
     int auto_vi = -1;
     if (path == kPathAuto) {
@@ -319,24 +299,6 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         }
     }
     ch->path = path;
-    if (path == kPathLookback) {
-        if (dir != 0) return fail(LRSCAN_EINVAL, "the look-back path is forward only");
-        int n = 0;
-        const WinVariant *tab = lb_variants(dtype, &n);
-        if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
-        const int vi = force_v > 0 ? force_v - 1 : 0;
-        const WinDirCfg &v = tab[vi].fwd;
-        ch->vidx = vi;
-        ch->var = &tab[vi];
-        ch->dir = 0;
-        ch->ctas = B * ((D + v.dt - 1) / v.dt) * ((T + v.w - 1) / v.w);
-        ch->threads = v.threads;
-        ch->smem = v.smem;
-        ch->stages = 1;
-        ch->kernels = 1;
-        ch->workspace = lookback_workspace(B, T, D, v.w);
-        return LRSCAN_OK;
-    }
     if (path == kPathSeq || path == kPathWindow) {
         int n = 0;
         const WinVariant *tab = win_variants(path, dtype, &n);
@@ -563,37 +525,6 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
     Choice ch;
     if ((rc = plan_call(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
     const size_t es = esize(dtype);
-    if (ch.path == kPathLookback) {
-        const WinDirCfg &v = ch.var->fwd;
-        void *ws = nullptr;
-        if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
-        const LbScratch sc = lookback_scratch(B, T, D, v.w);
-        char *base = static_cast<char *>(ws);
-        if (cudaMemsetAsync(base, 0, sc.flags_off + sc.flags_bytes, st) != cudaSuccess) {
-            cudaGetLastError();
-            return fail(LRSCAN_ECUDA, "look-back flag reset failed");
-        }
-        CUtensorMap ma, mb;
-        if (encode_map(&ma, a, dtype, B, T, D, v.dt, v.w) || encode_map(&mb, b, dtype, B, T, D, v.dt, v.w))
-            return LRSCAN_EINVAL;
-        WinLaunch L{};
-        L.maps[0] = &ma;
-        L.maps[1] = &mb;
-        L.out0 = out;
-        L.last = last;
-        L.B = B; L.T = T; L.D = D;
-        L.status = ctx->status;
-        L.timeout_ns = g_timeout_ns.load();
-        L.stream = st;
-        L.device = dev;
-        L.lb_ticket = reinterpret_cast<unsigned int *>(base);
-        L.lb_flags = reinterpret_cast<unsigned int *>(base + sc.flags_off);
-        L.lb_maps = reinterpret_cast<float2 *>(base + sc.maps_off);
-        L.lb_incl = reinterpret_cast<float *>(base + sc.incl_off);
-        if (v.launch(L, v))
-            return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
-        return LRSCAN_OK;
-    }
     if (ch.path == kPathSeq || ch.path == kPathWindow) {
         const WinDirCfg &v = ch.var->fwd;
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
@@ -1233,11 +1164,6 @@ int lrscan_set_stream(void *stream) {
     return LRSCAN_OK;
 }
 
-size_t lrscan_lookback_workspace_bytes(int64_t B, int64_t T, int64_t D) {
-    if (B <= 0 || T <= 0 || D <= 0) return 0;
-    return lookback_workspace(B, T, D, 32);
-}
-
 size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len) {
     const int C = chunk_len ? chunk_len : 64;
     if (B <= 0 || T <= 0 || D <= 0 || (C != 16 && C != 32 && C != 64)) return 0;
@@ -1262,11 +1188,6 @@ int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_alig
 int lrscan_num_variants(int path, int dtype, int dir) {
     (void)dir;
     if (dtype != LRSCAN_F32 && dtype != LRSCAN_BF16) return LRSCAN_EDTYPE;
-    if (path == kPathLookback) {
-        int n = 0;
-        lb_variants(dtype, &n);
-        return dir == 0 ? n : 0;
-    }
     if (path == kPathSeq || path == kPathWindow) {
         int n = 0;
         win_variants(path, dtype, &n);

@@ -27,7 +27,7 @@ LRSCAN_ETIMEOUT = -5
 LRSCAN_ENODEVICE = -6
 
 F32, BF16 = 0, 1
-PATHS = {"auto": 0, "seq": 1, "chunk": 2, "window": 3, "plain": 4, "lookback": 5}
+PATHS = {"auto": 0, "seq": 1, "chunk": 2, "window": 3, "plain": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -95,7 +95,6 @@ EXPORTS = {
     "lrscan_gated_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
     "lrscan_plan_gated": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
                            ctypes.POINTER(PlanInfo)], ctypes.c_int),
-    "lrscan_lookback_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
     "lrscan_set_stream": ([_P], ctypes.c_int),
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),

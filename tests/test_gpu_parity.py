@@ -378,24 +378,3 @@ def test_chunk_grouped_prefix(dt, shape, chunk):
     check_case(inp, path="chunk", chunk_len=chunk, tile_variant=1)
     auto = L.lrscan_plan(B, T, D, dt, "fwd", path="chunk", chunk_len=chunk)
     assert auto["name"].endswith("_grouped")
-
-
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("shape", [(3, 300, 200), (2, 513, 1000), (1, 20001, 64), (1, 1, 8), (4, 33, 40)])
-def test_lookback_forward(dt, shape):
-    """The single-pass look-back forward (one CTA per lane tile and time
-    window, decoupled look-back for the entry state) on every tile variant,
-    against the oracle (re-associating: tolerance)."""
-    B, T, D = shape
-    inp = random_inputs(B, T, D, dt, seed=800 + T, a_lo=0.6, a_hi=1.0)
-    ref_out, ref_last = orc().fwd(to_np(inp["a"]), to_np(inp["b"]), dt)
-    for v in range(1, L.lrscan_num_variants("lookback", dt) + 1):
-        out, last = gpu_fwd(inp["a"], inp["b"], path="lookback", tile_variant=v)
-        assert_close(out, ref_out, dt, f"lookback out v{v}", reassociated=True)
-        assert_last_close(last, ref_last, f"lookback last v{v}")
-
-
-def test_lookback_is_forward_only():
-    x = torch.zeros((1, 64, 32), device="cuda")
-    with pytest.raises(L.LrscanError):
-        L.lrscan_bwd(x, x, x, path="lookback")
