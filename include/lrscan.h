@@ -192,9 +192,13 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
  *   grad_ar = fma(Re g, Re p, Im g * Im p),  grad_ai = fma(Im g, Re p, -(Re g * Im p))
  * (a' = a_{t+1}, p = h_{t-1}); both paths use this order and agree bit for bit.
  * All planes are caller-owned device [B, T, D] tensors of one storage dtype;
- * paths: LRSCAN_PATH_SEQ (tiled, 16-byte aligned rows of every plane) or
- * LRSCAN_PATH_PLAIN (any alignment); auto picks seq when it can.  Moves 6
- * elements per (t, d) forward and 10 backward.  Other rules as lrscan_fwd_ex.
+ * paths: tiled (LRSCAN_PATH_SEQ or LRSCAN_PATH_WINDOW: one table of
+ * sequential and windowed tiles, 16-byte aligned rows of every plane) or
+ * LRSCAN_PATH_PLAIN (any alignment); auto picks a tiled variant when it can.
+ * The sequential tiles keep the order above and agree with it bit for bit;
+ * the windowed forward tiles (time split inside the CTA through complex
+ * affine maps) agree to rounding.  Moves 6 elements per (t, d) forward and 10
+ * backward.  Other rules as lrscan_fwd_ex.
  */
 int lrscan_cfwd(const void *ar, const void *ai, const void *br, const void *bi,
                 void *out_r, void *out_i, float *last_r, float *last_i,

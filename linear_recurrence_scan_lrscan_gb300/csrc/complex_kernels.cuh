@@ -254,6 +254,160 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
     }
 }
 
+// ---------------------------------------------------------------------------
+// Windowed complex forward (S > 1 sub-chunks of L rows per window, lane-scan
+// prefix): the window kernel's structure with complex maps.  Thread (s, g)
+// holds L rows of its lanes' four planes, summarizes its sub-chunk as the
+// complex affine map h -> P*h + Q (P = product of the decays, Q = the
+// sub-chunk's scan from zero, both with the recurrence's nested fmas), the
+// lane threads walk the S maps in order from the window's carried state, and
+// every thread replays its rows from its entry state.  Shared-memory scan
+// area per sub-chunk and lane: the map (Pr, Pi, Qr, Qi) and the entry state.
+template <class C>
+__host__ __device__ inline WinGeom make_cwin_geom(int S, int nstage, int T, int D) {
+    WinGeom g = make_win_geom<C>(S, nstage, T, D);
+    g.flag_off = g.scan_off + S * C::DT * 24;
+    g.smem_bytes = g.flag_off + 16;
+    return g;
+}
+
+__device__ __forceinline__ void cmul_add(float xr, float xi, float hr, float hi, float br, float bi, float &nr,
+                                         float &ni) {
+    // (xr + i xi) (hr + i hi) + (br + i bi), in the oracle's nested-fma order
+    nr = __fmaf_rn(xr, hr, __fmaf_rn(-xi, hi, br));
+    ni = __fmaf_rn(xi, hr, __fmaf_rn(xr, hi, bi));
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
+                 const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
+                 typename C::St *__restrict__ out_r, typename C::St *__restrict__ out_i,
+                 float *__restrict__ last_r, float *__restrict__ last_i, const __grid_constant__ WinGeom geom,
+                 DevStatus *status, uint64_t timeout_ns) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 4, "windowed complex forward: lane-scan shape, four planes");
+    using St = typename C::St;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T, D = geom.D;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[4] = {&tm_ar, &tm_ai, &tm_br, &tm_bi};
+            const int W = sm.W;
+            win_producer<C>(sm, maps, d0, brow, [W](int k, int) { return k * W; }, wc);
+        }
+        return;
+    }
+
+    const int s = threadIdx.x / G;
+    const int lg = threadIdx.x - s * G;
+    const int lane = threadIdx.x & 31;
+    const int d = d0 + lg * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    float4 *pq = reinterpret_cast<float4 *>(smem_raw + geom.scan_off);                          // [S][DT]
+    float2 *entry = reinterpret_cast<float2 *>(smem_raw + geom.scan_off + S * DT * 16);         // [S][DT]
+    float cr = 0.0f, ci = 0.0f;  // window-to-window state of lane threadIdx.x (threads < DT)
+    int stage = 0, use = 0;
+    for (int k = 0; k < sm.nwin; ++k) {
+        const int rbase = k * sm.W + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if (ok) {
+            const int off = (s * L) * DT + lg * V;
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                unpack_lanes<St, V>(sm.tile<C>(stage, 0) + off + j * DT, xr[j]);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 1) + off + j * DT, xi[j]);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 2) + off + j * DT, yr[j]);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 3) + off + j * DT, yi[j]);
+            }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+        if (n < L) {
+            // tail sub-chunk: steps past T become exact identity steps (a = 1, b = 0)
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    xr[j][v] = j < n ? xr[j][v] : 1.0f;
+                    xi[j][v] = j < n ? xi[j][v] : 0.0f;
+                    yr[j][v] = j < n ? yr[j][v] : 0.0f;
+                    yi[j][v] = j < n ? yi[j][v] : 0.0f;
+                }
+            }
+        }
+        // sub-chunk map: P = product of the decays, Q = the scan from zero
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float pr = 1.0f, pi = 0.0f, qr = 0.0f, qi = 0.0f;
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                float npr, npi, nqr, nqi;
+                cmul_add(xr[j][v], xi[j][v], pr, pi, 0.0f, 0.0f, npr, npi);
+                cmul_add(xr[j][v], xi[j][v], qr, qi, yr[j][v], yi[j][v], nqr, nqi);
+                pr = npr; pi = npi; qr = nqr; qi = nqi;
+            }
+            pq[s * DT + v * G + lg] = make_float4(pr, pi, qr, qi);
+        }
+        if (bar_sync_or(1, NT, !ok)) break;
+        if (static_cast<int>(threadIdx.x) < DT) {
+            float hr = cr, hi = ci;
+#pragma unroll 4
+            for (int i = 0; i < S; ++i) {
+                const float4 m = pq[i * DT + threadIdx.x];
+                entry[i * DT + threadIdx.x] = make_float2(hr, hi);
+                float nr, ni;
+                cmul_add(m.x, m.y, hr, hi, m.z, m.w, nr, ni);
+                hr = nr; hi = ni;
+            }
+            cr = hr; ci = hi;
+        }
+        bar_sync_or(1, NT, false);
+        float hr[V], hi[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const float2 e = entry[s * DT + v * G + lg];
+            hr[v] = e.x;
+            hi[v] = e.y;
+        }
+        const size_t o = (row0 + rbase) * D + d;
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                float nr, ni;
+                cmul_add(xr[j][v], xi[j][v], hr[v], hi[v], yr[j][v], yi[j][v], nr, ni);
+                hr[v] = nr; hi[v] = ni;
+            }
+            if (lane_ok && (n == L || j < n)) {
+                store_lanes<St, V>(out_r + o + static_cast<size_t>(j) * D, hr);
+                store_lanes<St, V>(out_i + o + static_cast<size_t>(j) * D, hi);
+            }
+        }
+        if (lane_ok && n > 0 && rbase + n == T) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (last_r) last_r[static_cast<size_t>(brow) * D + d + v] = hr[v];
+                if (last_i) last_i[static_cast<size_t>(brow) * D + d + v] = hi[v];
+            }
+        }
+    }
+}
+
 // Plain kernels: one lane per thread, plain loads, any alignment (same order
 // of operations, bit-identical to the tiled ones).
 template <typename St>

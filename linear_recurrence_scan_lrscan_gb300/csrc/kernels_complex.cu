@@ -30,6 +30,22 @@ int launch_cwin_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
 }
 
 template <class C>
+int launch_cwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = cwinw_fwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_cwin_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    using St = typename C::St;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
+                                     static_cast<St *>(L.out0), static_cast<St *>(L.out1), L.last, L.last_i, g,
+                                     L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C>
 int launch_cwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     static unsigned long long mask = 0;
     static std::mutex mu;
@@ -67,7 +83,31 @@ WinDirCfg cdir_cfg(int nstage) {
     return d;
 }
 
+// Windowed complex forward tile: S sub-chunks of L rows, lane scan.
+template <class C>
+WinDirCfg cwdir_cfg(int S, int nstage) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 4, "windowed complex forward shape");
+    if (S > C::SMAX) std::abort();  // table error
+    const WinGeom g = make_cwin_geom<C>(S, nstage, 1, 1);
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = S;
+    d.lane_scan = 1;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = S * C::G + 32;
+    d.smem = g.smem_bytes;
+    d.stage_bytes = g.stage_bytes;
+    d.launch = &launch_cwinw_fwd<C>;
+    return d;
+}
+
 // WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
+using CWF_BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 4, 288, 2, false>;
+using CWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 4, 288, 2, false>;
+using CWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 4, 288, 2, false>;
 using CBF_64_1_32 = WinShape<bf16_t, 64, 1, 32, 4, 96, 1, true>;
 using CBB_64_1_32 = WinShape<bf16_t, 64, 1, 32, 6, 96, 1, true>;
 using CBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 4, 64, 1, true>;
@@ -89,6 +129,8 @@ const WinVariant kCplxBF16[] = {
     {"cseq_bf16_d32_v1", F(CBF_32_1_32, 6), B(CBB_32_1_32, 4)},
     {"cseq_bf16_d64_v1_n4", F(CBF_64_1_32, 4), B(CBB_64_1_32, 3)},
     {"cseq_bf16_d64_v2_n4", F(CBF_64_2_32, 4), B(CBB_64_2_16, 5)},
+    {"cwin_bf16_d32_s8", cwdir_cfg<CWF_BF_32_1_8>(8, 3), B(CBB_64_1_32, 3)},
+    {"cwin_bf16_d32_s16_v2", cwdir_cfg<CWF_BF_32_2_8>(16, 2), B(CBB_64_1_32, 3)},
 };
 const WinVariant kCplxF32[] = {
     {"cseq_f32_d32_v1", F(CFF_32_1_32, 6), B(CFB_32_1_32, 4)},
@@ -96,6 +138,7 @@ const WinVariant kCplxF32[] = {
     {"cseq_f32_d64_v1", F(CFF_64_1_16, 8), B(CFB_64_1_16, 6)},
     {"cseq_f32_d32_v1_n4", F(CFF_32_1_32, 4), B(CFB_32_1_32, 3)},
     {"cseq_f32_d64_v1_n4", F(CFF_64_1_16, 4), B(CFB_64_1_16, 3)},
+    {"cwin_f32_d32_s8", cwdir_cfg<CWF_FF_32_1_8>(8, 3), B(CFB_32_1_32, 4)},
 };
 #undef F
 #undef B

@@ -654,11 +654,12 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     (void)T;
     const int want = opts ? opts->path : 0;
     const int force_v = opts ? opts->tile_variant : 0;
-    if (want != kPathAuto && want != kPathSeq && want != kPathPlain)
-        return fail(LRSCAN_EINVAL, "the complex scan has the seq and plain paths only (path %d)", want);
-    if (want == kPathSeq && !aligned16)
-        return fail(LRSCAN_EINVAL, "path seq needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
-    const int path = want == kPathAuto ? (aligned16 ? kPathSeq : kPathPlain) : want;
+    if (want != kPathAuto && want != kPathSeq && want != kPathWindow && want != kPathPlain)
+        return fail(LRSCAN_EINVAL, "the complex scan has the tiled (seq / window) and plain paths (path %d)", want);
+    if ((want == kPathSeq || want == kPathWindow) && !aligned16)
+        return fail(LRSCAN_EINVAL, "tiled paths need 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
+    // seq and window both name the tiled variant table (sequential and windowed tiles)
+    const int path = want == kPathAuto ? (aligned16 ? kPathSeq : kPathPlain) : (want == kPathPlain ? kPathPlain : kPathSeq);
     ch->path = path;
     ch->dir = dir;
     ch->kernels = 1;
@@ -689,6 +690,7 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     if (o.resident == 0) return fail(LRSCAN_EINVAL, "tile variant %s does not fit on an SM", tab[vi].name);
     ch->vidx = vi;
     ch->var = &tab[vi];
+    ch->path = dir_of(tab[vi], dir).s > 1 ? kPathWindow : kPathSeq;
     ch->ctas = o.ctas;
     ch->threads = dir_of(tab[vi], dir).threads;
     ch->smem = dir_of(tab[vi], dir).smem;

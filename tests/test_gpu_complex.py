@@ -1,6 +1,8 @@
-"""GPU parity of the complex diagonal scan (re/im planes) on both paths and
-every tile variant, against the oracle's complex scan.  Both paths keep the
-oracle's order of operations, so they are compared exactly."""
+"""GPU parity of the complex diagonal scan (re/im planes) on every path and
+tile variant, against the oracle's complex scan.  The sequential tiles and
+the plain kernels keep the oracle's order of operations and are compared
+exactly; the windowed forward tiles re-associate through complex affine maps
+and are held to the tolerances of parity_util."""
 import numpy as np
 import pytest
 import torch
@@ -40,18 +42,20 @@ def check_complex(inp, dt, **kw):
     assert L.lrscan_sync_check() == 0
     plan = L.lrscan_plan_complex(B, T, D, dt, "fwd", **kw)
     tag = plan["name"]
+    ex = plan["path"] != "window"  # windowed tiles re-associate through complex maps
     for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
-        assert_close(to_np(g), r, dt, f"{name}[{tag}]", exact=True)
+        assert_close(to_np(g), r, dt, f"{name}[{tag}]", exact=ex, reassociated=not ex)
     for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
-        assert_last_close(g.cpu().numpy(), r, f"{name}[{tag}]", exact=True)
+        assert_last_close(g.cpu().numpy(), r, f"{name}[{tag}]", exact=ex)
     # backward from the oracle's forward output
     out_r, out_i = from_np(ref[0], dt).cuda(), from_np(ref[1], dt).cuda()
     gref = o.cbwd(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt)
     ggot = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"], **kw)
     assert L.lrscan_sync_check() == 0
     planb = L.lrscan_plan_complex(B, T, D, dt, "bwd", **kw)
+    exb = planb["path"] != "window"
     for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot, gref):
-        assert_close(to_np(g), r, dt, f"{name}[{planb['name']}]", exact=True)
+        assert_close(to_np(g), r, dt, f"{name}[{planb['name']}]", exact=exb, reassociated=not exb)
     return plan, planb
 
 
@@ -74,7 +78,7 @@ def test_complex_every_variant(dt, shape):
     assert n > 3
     check_complex(inp, dt, path="plain")
     plan, _ = check_complex(inp, dt)
-    assert plan["path"] == "seq"
+    assert plan["path"] in ("seq", "window")
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -100,18 +104,25 @@ def test_complex_full_size_sampled_lanes():
     inp = make_complex_inputs()
     cu = {k: inp[k].cuda() for k in PLANES}
     out_r, out_i, last_r, last_i = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"])
-    grads = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"])
     assert L.lrscan_sync_check() == 0
-    r = np.random.default_rng(520)
     o = oracle.default()
+    # the backward reads the oracle's forward output, so both sides see the same h_{t-1}
+    full = o.cfwd(*(to_np(inp[k]) for k in ("ar", "ai", "br", "bi")), w.dtype)
+    grads = L.lrscan_cbwd(cu["ar"], cu["ai"], from_np(full[0], w.dtype).cuda(), from_np(full[1], w.dtype).cuda(),
+                          cu["go_r"], cu["go_i"])
+    assert L.lrscan_sync_check() == 0
+    del full
+    r = np.random.default_rng(520)
     for _ in range(6):
         b = int(r.integers(w.B))
         d = int(r.integers(w.D))
         sl = lambda t: np.ascontiguousarray(to_np(t[b:b + 1, :, d:d + 1]))  # noqa: E731
         ref = o.cfwd(sl(inp["ar"]), sl(inp["ai"]), sl(inp["br"]), sl(inp["bi"]), w.dtype)
-        assert_close(sl(out_r), ref[0], w.dtype, "out_r sampled", exact=True)
-        assert_close(sl(out_i), ref[1], w.dtype, "out_i sampled", exact=True)
-        assert last_r[b, d].item() == ref[2][0, 0] and last_i[b, d].item() == ref[3][0, 0]
+        ex = L.lrscan_plan_complex(w.B, w.T, w.D, w.dtype, "fwd")["path"] != "window"
+        assert_close(sl(out_r), ref[0], w.dtype, "out_r sampled", exact=ex, reassociated=not ex)
+        assert_close(sl(out_i), ref[1], w.dtype, "out_i sampled", exact=ex, reassociated=not ex)
+        assert_last_close(np.array([[last_r[b, d].item()]]), ref[2], "last_r sampled", exact=ex)
+        assert_last_close(np.array([[last_i[b, d].item()]]), ref[3], "last_i sampled", exact=ex)
         gref = o.cbwd(sl(inp["ar"]), sl(inp["ai"]), ref[0], ref[1], sl(inp["go_r"]), sl(inp["go_i"]), w.dtype)
         for g, gr_ in zip(grads, gref):
             assert_close(sl(g), gr_, w.dtype, "complex grads sampled", exact=True)
@@ -128,4 +139,4 @@ def test_complex_scan_autograd(dt):
     ref = o.cfwd(np_in["ar"], np_in["ai"], np_in["br"], np_in["bi"], dt)
     gref = o.cbwd(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt)
     for x, r in zip(xs, gref):
-        assert_close(to_np(x.grad), r, dt, "complex autograd", exact=True)
+        assert_close(to_np(x.grad), r, dt, "complex autograd", reassociated=True)
