@@ -676,8 +676,10 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
+    } else if (dtype == LRSCAN_BF16 && dir == 0 && (vi = find_variant(tab, n, "cwin_bf16_d32_s16_v2", dir, B, D, g)) >= 0) {
+        // measured best complex bf16 forward: the windowed tile (time split inside the CTA)
     } else if (dtype == LRSCAN_BF16 && (vi = find_one_wave(tab, n, "cseq_bf16_d64_v1_n4", dir, B, D, g)) >= 0) {
-        // measured best for both directions of the complex bf16 workload whenever it fits one wave
+        // measured best complex bf16 backward whenever all its CTAs fit one wave
     } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
         for (int i = 0; i < n; ++i) {
