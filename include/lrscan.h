@@ -227,8 +227,10 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
  *   grad_eta[b,t]  = sum_d q,   grad_nu_log[d] = sum_{b,t} q,
  *   q = grad_a * a * log a,  grad_a = g_t * out_{t-1},  log a = -exp(nu_log) exp(eta),
  * both fp32, summed in a fixed order (deterministic); it moves 3 elements per
- * (t, d).  Exponentials take the hardware's fast path (relative error of a few
- * 1e-7), so results agree with an exact evaluation to rounding, not bit for bit.
+ * (t, d).  Exponentials are fast approximations (e^x = 2^(x log2 e) with the
+ * ex2.approx instruction: relative error of a few 1e-7; a decay below 2^-126
+ * is taken as 0), so results agree with an exact evaluation to rounding, not
+ * bit for bit.
  * The backward needs lrscan_gated_workspace_bytes(B, T, D) bytes of scratch:
  * library-owned per (device, stream), or opts->workspace.  Paths:
  * LRSCAN_PATH_SEQ (tiled, 16-byte aligned rows) or LRSCAN_PATH_PLAIN; auto

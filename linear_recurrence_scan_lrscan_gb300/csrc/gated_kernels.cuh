@@ -10,7 +10,11 @@
 // instead of 5).  Backward, with grad_a = g * out_{t-1} and
 // q = grad_a * a * (-nu * E) (= dL / dlog a):
 //   grad_eta[b,t] = sum_d q,   grad_nu_log[d] = sum_{b,t} q.
-// Exponentials use the fast hardware path (__expf), as the page's tl.exp does.
+// Exponentials are fast approximations, as the page's tl.exp is: e^x is
+// taken as 2^(x log2 e) with 2^y on the multi-function unit.  The rate is kept
+// in base-2 units, nu2_d = nu_d log2 e, so each decay costs one multiply and
+// one ex2 (a = 2^(-nu2 E)), and the kernels accumulate
+// q2 = grad_a * a * log2(a) = q / ln 2; gated_finish scales the sums by ln 2.
 //
 // Tiled sequential kernels (S = 1, L = 32 rows per window): lane j of each
 // warp computes E for row j of the window (its eta loaded two windows ahead)
@@ -28,6 +32,26 @@ namespace lrscan {
 
 __device__ __forceinline__ float eta_at(const float *row, int t, int T) {
     return (t >= 0 && t < T) ? __ldg(row + t) : 0.0f;
+}
+
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// 2^y by the PTX ex2.approx.ftz.f32 instruction (relative error about 2^-22;
+// results below the normal range flush to zero, i.e. a decay under 2^-126
+// is taken as 0).
+__device__ __forceinline__ float ex2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+// e^x = 2^(x log2 e)
+__device__ __forceinline__ float exp_approx(float x) { return ex2_approx(__fmul_rn(x, kLog2e)); }
+
+// Rate of lane d in base-2 units: nu2 = exp(nu_log) log2 e, so a = 2^(-nu2 E).
+__device__ __forceinline__ float rate2(const float *nu_log, int d) {
+    return __fmul_rn(exp_approx(__ldg(nu_log + d)), kLog2e);
 }
 
 // After the call, lane l holds sum over the warp's lanes of v[l] (v has 32
@@ -82,10 +106,10 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
-    float nu[V], h[V];
+    float nu2[V], h[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
         h[v] = 0.0f;
     }
     float eta1 = eta_at(eta_row, lane, T), eta2 = eta_at(eta_row, L + lane, T);  // windows k, k+1
@@ -93,7 +117,7 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
     int stage = 0, use = 0;
     const int off = threadIdx.x * V;
     for (int k = 0; k < sm.nwin; ++k) {
-        const float e_lane = __expf(eta1);  // E of row k*L + lane
+        const float e_lane = exp_approx(eta1);  // E of row k*L + lane
         eta1 = eta2;
         eta2 = eta_at(eta_row, (k + 2) * L + lane, T);
         bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
@@ -107,7 +131,7 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
             const float e = __shfl_sync(0xffffffffu, e_lane, j);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float a = __expf(-__fmul_rn(nu[v], e));
+                const float a = ex2_approx(-__fmul_rn(nu2[v], e));
                 h[v] = __fmaf_rn(a, h[v], y[v]);
             }
             if (lane_ok) store_lanes<St, V>(out + o + static_cast<size_t>(j) * D, h);
@@ -124,7 +148,7 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
             for (int j = 0; j < L; ++j) {
                 const float e = __shfl_sync(0xffffffffu, e_lane, j);
 #pragma unroll
-                for (int v = 0; v < V; ++v) av[j][v] = __expf(-__fmul_rn(nu[v], e));
+                for (int v = 0; v < V; ++v) av[j][v] = ex2_approx(-__fmul_rn(nu2[v], e));
             }
 #pragma unroll
             for (int j = 0; j < L; ++j) {
@@ -163,7 +187,8 @@ __global__ void __launch_bounds__(C::MAXT, C::MINB)
 gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ eta,
                  const float *__restrict__ nu_log, typename C::St *__restrict__ out, float *__restrict__ last,
                  const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
-    static_assert(!C::SEQ && !C::PT && C::NIN == 1, "generated-decay windowed forward: lane-scan shape, one plane");
+    static_assert(!C::SEQ && !C::PT && C::NIN == 1 && C::G <= 32 && 32 % C::G == 0 && C::G >= C::L,
+                  "generated-decay windowed forward: lane-scan shape, one plane, row groups within a warp");
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -190,30 +215,32 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restri
     const int s = threadIdx.x / G;
     const int lg = threadIdx.x - s * G;
     const int lane = threadIdx.x & 31;
+    const int gbase = lane & ~(G - 1);  // first lane of this sub-chunk's thread group
+    const int myrow = lg < L ? lg : L - 1;  // row whose E this thread computes
     const int d = d0 + lg * V;
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
-    float nu[V];
+    float nu2[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
-    float ev[L];  // eta of this thread's rows in the current window
-#pragma unroll
-    for (int j = 0; j < L; ++j) ev[j] = eta_at(eta_row, s * L + j, T);
+    for (int v = 0; v < V; ++v) nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
+    float ev = eta_at(eta_row, s * L + myrow, T);  // eta of row myrow of the current window's sub-chunk
     float h[V];
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
     for (int k = 0; k < sm.nwin; ++k) {
         const int rbase = k * sm.W + s * L;
         const int n = min(max(T - rbase, 0), L);
-        float xa[L][V], xb[L][V], evn[L];
-#pragma unroll
-        for (int j = 0; j < L; ++j) evn[j] = eta_at(eta_row, rbase + sm.W + j, T);  // next window's rows
+        const float evn = eta_at(eta_row, rbase + sm.W + myrow, T);  // next window
+        // E of the sub-chunk's rows: one exponential per thread, then shuffles
+        // within the thread group
+        const float e_mine = exp_approx(ev);
+        float xa[L][V], xb[L][V];
 #pragma unroll
         for (int j = 0; j < L; ++j) {
-            const float e = __expf(ev[j]);
+            const float e = __shfl_sync(0xffffffffu, e_mine, gbase + j);
 #pragma unroll
-            for (int v = 0; v < V; ++v) xa[j][v] = __expf(-__fmul_rn(nu[v], e));
+            for (int v = 0; v < V; ++v) xa[j][v] = ex2_approx(-__fmul_rn(nu2[v], e));
         }
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *tb = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
@@ -276,20 +303,19 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restri
 #pragma unroll
             for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
         }
-#pragma unroll
-        for (int j = 0; j < L; ++j) ev[j] = evn[j];
+        ev = evn;
     }
 }
 
 // Backward.  Tiles: out one row early (h_{t-1}; zero fill before t = 0) and
-// grad_out.  part_eta: [B*T][ncol] with ncol = gridDim.x * (G / 32) warp
-// columns; part_nu: [B][D].
+// grad_out.  part_eta: [ncol][prow] with ncol = gridDim.x * (G / 32) warp
+// columns and prow = rows B*T of the whole call; part_nu: [B][D].
 template <class C>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_go,
                 const float *__restrict__ eta, const float *__restrict__ nu_log, typename C::St *__restrict__ grad_b,
-                float *__restrict__ part_eta, float *__restrict__ part_nu, const __grid_constant__ WinGeom geom,
-                DevStatus *status, uint64_t timeout_ns) {
+                float *__restrict__ part_eta, long long prow, float *__restrict__ part_nu,
+                const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
     static_assert(C::SEQ && C::NIN == 2 && C::L == 32 && C::G % 32 == 0,
                   "generated-decay backward: sequential, two planes, 32-row windows, whole warps");
     using St = typename C::St;
@@ -321,12 +347,11 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
-    const int ncol = gridDim.x * (G / 32);
     const int col = blockIdx.x * (G / 32) + static_cast<int>(threadIdx.x) / 32;
-    float nu[V], g[V], a_next[V], acc_nu[V];
+    float nu2[V], g[V], a_next[V], acc_nu[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
         g[v] = 0.0f;
         a_next[v] = 0.0f;  // a_T: nothing enters past the end
         acc_nu[v] = 0.0f;
@@ -336,7 +361,7 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
     int stage = 0, use = 0;
     const int off = threadIdx.x * V;
     for (int k = 0; k < nwin; ++k) {
-        const float e_lane = __expf(eta1);
+        const float e_lane = exp_approx(eta1);
         eta1 = eta2;
         eta2 = eta_at(eta_row, (nwin - 3 - k) * L + lane, T);
         bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
@@ -358,8 +383,8 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
             const float e = __shfl_sync(0xffffffffu, e_lane, j);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                lav[j][v] = -__fmul_rn(nu[v], e);
-                av[j][v] = __expf(lav[j][v]);
+                lav[j][v] = -__fmul_rn(nu2[v], e);  // log2 of the decay
+                av[j][v] = ex2_approx(lav[j][v]);
             }
         }
 #pragma unroll
@@ -383,7 +408,7 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
             if (lane_ok && (n == L || j < n)) store_lanes<St, V>(grad_b + o + static_cast<size_t>(j) * D, g);
         }
         const float rsum = warp_transpose_sum(qrow);  // row wbase + lane
-        if (lane < n) part_eta[(row0 + wbase + lane) * ncol + col] = rsum;
+        if (lane < n) part_eta[col * prow + row0 + wbase + lane] = rsum;
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty_bar(stage));
         if (++stage == sm.nstage) { stage = 0; ++use; }
@@ -399,16 +424,19 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
 // Thread (s, g) builds the decays of rows rbase .. rbase + L (a_{t+1} for
 // its last row comes from the next sub-chunk's first row; 0 past T), takes
 // the adjoint entering its sub-chunk from the lane threads' walk over the S
-// reverse maps, replays, and sums q over its rows.  Row sums over the CTA's
+// reverse maps, replays, and sums q2 over its rows.  Row sums over the CTA's
 // lanes: the 16 threads of a sub-chunk exchange their 8 row sums (xor 8, then
 // a transpose-sum over 8 lanes): lane g < 8 ends with row g's sum.
-// part_eta: [B*T][gridDim.x]; part_nu: [B*S][D] (time sums per sub-chunk).
+// part_eta: [gridDim.x][prow] (prow = rows B*T of the whole call, so the
+// eight rows of a sub-chunk land in 32 contiguous bytes); part_nu: [B*S][D]
+// (time sums per sub-chunk).
 template <class C>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_go,
                  const float *__restrict__ eta, const float *__restrict__ nu_log,
-                 typename C::St *__restrict__ grad_b, float *__restrict__ part_eta, float *__restrict__ part_nu,
-                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+                 typename C::St *__restrict__ grad_b, float *__restrict__ part_eta, long long prow,
+                 float *__restrict__ part_nu, const __grid_constant__ WinGeom geom, DevStatus *status,
+                 uint64_t timeout_ns) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 2 && C::L == 8 && C::G == 16,
                   "windowed generated-decay backward: lane-scan shape, two planes, 8 rows x 16 threads");
     using St = typename C::St;
@@ -439,53 +467,52 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     const int s = threadIdx.x / G;
     const int lg = threadIdx.x - s * G;
     const int lane = threadIdx.x & 31;
+    const int gbase = lane & ~(G - 1);  // first lane of this sub-chunk's thread group
+    const int myrow = lg <= L ? lg : L;  // row (of rbase .. rbase + L) whose E this thread computes
     const int d = d0 + lg * V;
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
-    const int ncol = gridDim.x;
-    float nu[V], acc_nu[V], g[V];
+    float nu2[V], acc_nu[V], g[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        nu[v] = lane_ok ? __expf(__ldg(nu_log + d + v)) : 0.0f;
+        nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
         acc_nu[v] = 0.0f;
     }
-    float ev[L + 1];  // eta of rows rbase .. rbase + L of the window being processed
-    {
-        const int rb = (nwin - 1) * sm.W + s * L;
-#pragma unroll
-        for (int j = 0; j <= L; ++j) ev[j] = eta_at(eta_row, rb + j, T);
-    }
+    float ev = eta_at(eta_row, (nwin - 1) * sm.W + s * L + myrow, T);  // current window
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
         const int rbase = wbase + s * L;
         const int n = min(max(T - rbase, 0), L);
-        float evn[L + 1];
-#pragma unroll
-        for (int j = 0; j <= L; ++j) evn[j] = eta_at(eta_row, rbase - sm.W + j, T);  // next processed window
-        // decays a[j] of rows rbase + j (j = 0..L) and log-decays la[j] (j < L)
-        float a[L + 1][V], la[L][V];
+        const float evn = eta_at(eta_row, rbase - sm.W + myrow, T);  // next processed window
+        // decays a[j] of rows rbase + j (j = 0..L), and a[j] * log2 a[j] (j < L)
+        const float e_mine = exp_approx(ev);
+        float a[L + 1][V], w[L][V];
 #pragma unroll
         for (int j = 0; j <= L; ++j) {
-            const float e = __expf(ev[j]);
+            const float e = __shfl_sync(0xffffffffu, e_mine, gbase + j);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const float l = -__fmul_rn(nu[v], e);
-                if (j < L) la[j][v] = l;
-                a[j][v] = __expf(l);
+                const float l = -__fmul_rn(nu2[v], e);
+                a[j][v] = ex2_approx(l);
+                if (j < L) w[j][v] = __fmul_rn(a[j][v], l);
             }
         }
-        float xh[L][V], xg[L][V];
+        float xg[L][V];
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *th = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // grad_out_t
         if (ok) {
 #pragma unroll
             for (int j = 0; j < L; ++j) {
-                unpack_lanes<St, V>(th + j * DT, xh[j]);
+                float xh[V];
+                unpack_lanes<St, V>(th + j * DT, xh);
                 unpack_lanes<St, V>(tg + j * DT, xg[j]);
+                // w = h_{t-1} a log2 a, so that q2 = g * w
+#pragma unroll
+                for (int v = 0; v < V; ++v) w[j][v] = __fmul_rn(xh[v], w[j][v]);
             }
         }
         __syncwarp();
@@ -494,15 +521,21 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         // a'_{t+1} of row j is a[j + 1]: 0 for the row just before the end of
         // the sequence (nothing enters after the last step), 1 for the
         // identity steps past T in a tail sub-chunk.  Only rows j < n use
-        // a[j] and la[j] for their q, and j + 1 >= tl implies j + 1 >= n, so
-        // rewriting a[j + 1] there leaves every used a_t intact.
+        // a[j] for their q, and j + 1 >= tl implies j + 1 >= n, so rewriting
+        // a[j + 1] there leaves every used a_t intact.  Rows past T get
+        // grad_out = 0 and w = 0.
         const int tl = T - rbase;  // rows of this sub-chunk before the sequence's end (may be <= 0)
+        if (tl <= L) {
 #pragma unroll
-        for (int j = 0; j < L; ++j) {
+            for (int j = 0; j < L; ++j) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                if (j + 1 >= tl) a[j + 1][v] = (j < n) ? 0.0f : 1.0f;
-                if (j >= n) xg[j][v] = 0.0f;
+                for (int v = 0; v < V; ++v) {
+                    if (j + 1 >= tl) a[j + 1][v] = (j < n) ? 0.0f : 1.0f;
+                    if (j >= n) {
+                        xg[j][v] = 0.0f;
+                        w[j][v] = 0.0f;
+                    }
+                }
             }
         }
         float P[V], Q[V];
@@ -542,7 +575,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 g[v] = __fmaf_rn(a[j + 1][v], g[v], xg[j][v]);
-                const float q = (j < n) ? __fmul_rn(__fmul_rn(__fmul_rn(g[v], xh[j][v]), a[j][v]), la[j][v]) : 0.0f;
+                const float q = __fmul_rn(g[v], w[j][v]);  // exactly 0 past T: g and w are 0 there
                 acc_nu[v] += q;
                 qs += q;
             }
@@ -563,9 +596,8 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
             }
         }
         const int r = lg & 7;  // this thread now holds row r's sum
-        if (lg < 8 && r < n) part_eta[(row0 + rbase + r) * ncol + blockIdx.x] = qrow[0];
-#pragma unroll
-        for (int j = 0; j <= L; ++j) ev[j] = evn[j];
+        if (lg < 8 && r < n) part_eta[blockIdx.x * prow + row0 + rbase + r] = qrow[0];
+        ev = evn;
     }
     if (lane_ok) {
 #pragma unroll
@@ -573,28 +605,46 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     }
 }
 
-// grad_eta[r] = sum over the ncol partials of row r (r < rows);
-// grad_nu_log[d] = sum over the nu_rows partials of lane d.
-__global__ void __launch_bounds__(256)
-gated_finish(const float *__restrict__ part_eta, const float *__restrict__ part_nu, float *__restrict__ grad_eta,
-             float *__restrict__ grad_nu_log, long long rows, int ncol, int nu_rows, int D) {
-    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    if (i < rows) {
-        const float *p = part_eta + i * ncol;
-        float s = 0.0f;
-        for (int c = 0; c < ncol; ++c) s += p[c];
-        grad_eta[i] = s;
-    } else if (i < rows + D) {
-        const int dd = static_cast<int>(i - rows);
-        float s = 0.0f;
-        for (int b = 0; b < nu_rows; ++b) s += part_nu[static_cast<size_t>(b) * D + dd];
-        grad_nu_log[dd] = s;
+// Both gradients are column sums of a row-major [K][N] matrix of partials,
+// scaled by ln 2 (the kernels sum q2 = q / ln 2): grad_eta[r] = ln 2 *
+// sum_c part_eta[c][r] (K = partial columns, N = rows B*T) and
+// grad_nu_log[d] = ln 2 * sum_b part_nu[b][d] (K = partial rows, N = D).
+// Blocks [0, blocks0) take the first, the rest the second.  A block covers 64
+// columns with 4 threads each; thread y sums the K range [K y / 4, K (y+1) / 4)
+// in order and thread y = 0 adds the four in order (deterministic).
+constexpr int kFinishCols = 64, kFinishSplit = 4;
+
+__global__ void __launch_bounds__(kFinishCols * kFinishSplit)
+gated_finish(const float *__restrict__ p0, int K0, long long N0, float *__restrict__ o0,
+             const float *__restrict__ p1, int K1, long long N1, float *__restrict__ o1, unsigned blocks0) {
+    const bool first = blockIdx.x < blocks0;
+    const float *p = first ? p0 : p1;
+    const int K = first ? K0 : K1;
+    const long long N = first ? N0 : N1;
+    float *o = first ? o0 : o1;
+    const long long n = static_cast<long long>(first ? blockIdx.x : blockIdx.x - blocks0) * kFinishCols + threadIdx.x;
+    const int y = threadIdx.y;
+    float sum = 0.0f;
+    if (n < N) {
+        const int k1 = static_cast<int>(static_cast<long long>(K) * (y + 1) / kFinishSplit);
+#pragma unroll 4
+        for (int k = static_cast<int>(static_cast<long long>(K) * y / kFinishSplit); k < k1; ++k)
+            sum += p[k * N + n];
+    }
+    __shared__ float part[kFinishSplit][kFinishCols];
+    part[y][threadIdx.x] = sum;
+    __syncthreads();
+    if (y == 0 && n < N) {
+        float t = part[0][threadIdx.x];
+#pragma unroll
+        for (int i = 1; i < kFinishSplit; ++i) t += part[i][threadIdx.x];
+        o[n] = __fmul_rn(t, kLn2);
     }
 }
 
 // Plain kernels (any alignment): thread per lane.  The backward's per-row
 // sums over lanes go through a warp shuffle reduction into the same
-// [B*T][ncol] partials (ncol = ceil(D / 32)).
+// [ncol][B*T] partials (ncol = ceil(D / 32)).
 template <typename St>
 __global__ void __launch_bounds__(128)
 gplain_fwd(const float *__restrict__ eta, const float *__restrict__ nu_log, const St *__restrict__ b,
@@ -602,13 +652,13 @@ gplain_fwd(const float *__restrict__ eta, const float *__restrict__ nu_log, cons
     const int brow = blockIdx.x / nlb;
     const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
     if (d >= D) return;
-    const float nu = __expf(__ldg(nu_log + d));
+    const float nu2 = rate2(nu_log, d);
     size_t i = static_cast<size_t>(brow) * T * D + d;
     float h = 0.0f;
     for (int t = 0; t < T; ++t) {
         float y[1];
         load_lanes_global<St, 1>(b + i, y);
-        const float a = __expf(-__fmul_rn(nu, __expf(__ldg(eta + static_cast<size_t>(brow) * T + t))));
+        const float a = ex2_approx(-__fmul_rn(nu2, exp_approx(__ldg(eta + static_cast<size_t>(brow) * T + t))));
         h = __fmaf_rn(a, h, y[0]);
         const float hv[1] = {h};
         store_lanes<St, 1>(out + i, hv);
@@ -625,9 +675,9 @@ gplain_bwd(const float *__restrict__ eta, const float *__restrict__ nu_log, cons
     const int brow = blockIdx.x / nlb;
     const int d = (blockIdx.x - brow * nlb) * 128 + threadIdx.x;
     const bool ok = d < D;  // every lane of a warp takes part in the row sums
-    const int ncol = (D + 31) / 32;
+    const size_t nrows = static_cast<size_t>(gridDim.x / nlb) * T;  // rows B*T: the partials' column stride
     const int col = d / 32;
-    const float nu = ok ? __expf(__ldg(nu_log + d)) : 0.0f;
+    const float nu2 = ok ? rate2(nu_log, d) : 0.0f;
     const size_t row = static_cast<size_t>(brow) * T * D + d;
     float g = 0.0f, a_next = 0.0f, acc = 0.0f;
     for (int t = T - 1; t >= 0; --t) {
@@ -637,8 +687,8 @@ gplain_bwd(const float *__restrict__ eta, const float *__restrict__ nu_log, cons
             load_lanes_global<St, 1>(grad_out + i, go);
             if (t > 0) load_lanes_global<St, 1>(out + i - D, hp);
         }
-        const float la = -__fmul_rn(nu, __expf(__ldg(eta + static_cast<size_t>(brow) * T + t)));
-        const float a = __expf(la);
+        const float la = -__fmul_rn(nu2, exp_approx(__ldg(eta + static_cast<size_t>(brow) * T + t)));
+        const float a = ex2_approx(la);
         g = __fmaf_rn(a_next, g, go[0]);
         const float q = ok ? __fmul_rn(__fmul_rn(__fmul_rn(g, hp[0]), a), la) : 0.0f;
         acc += q;
@@ -651,7 +701,7 @@ gplain_bwd(const float *__restrict__ eta, const float *__restrict__ nu_log, cons
 #pragma unroll
         for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
         if ((threadIdx.x & 31) == 0 && d < D)  // lane 0's lane is the warp's first: d < D iff the warp has lanes
-            part_eta[(static_cast<size_t>(brow) * T + t) * ncol + col] = s;
+            part_eta[static_cast<size_t>(col) * nrows + static_cast<size_t>(brow) * T + t] = s;
     }
     if (ok) part_nu[static_cast<size_t>(brow) * D + d] = acc;
 }

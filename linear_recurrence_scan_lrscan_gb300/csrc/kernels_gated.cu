@@ -51,7 +51,8 @@ int launch_gwinw_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     using St = typename C::St;
     const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
                                      L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, static_cast<St *>(L.out0),
-                                     L.part_eta, L.part_nu, g, L.status, L.timeout_ns);
+                                     L.part_eta, static_cast<long long>(L.part_rows), L.part_nu, g, L.status,
+                                     L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -66,7 +67,8 @@ int launch_gwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     using St = typename C::St;
     const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
                                      L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, static_cast<St *>(L.out0),
-                                     L.part_eta, L.part_nu, g, L.status, L.timeout_ns);
+                                     L.part_eta, static_cast<long long>(L.part_rows), L.part_nu, g, L.status,
+                                     L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -94,7 +96,7 @@ template <class C, bool FWD>
 WinDirCfg gwdir_cfg(int S, int nstage) {
     static_assert(!C::SEQ && !C::PT && C::NIN == (FWD ? 1 : 2), "windowed generated-decay shape");
     const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
-    if (S > C::SMAX) std::abort();  // table error
+    if (S > C::SMAX || (S * C::G) % 32 != 0) std::abort();  // table error: sub-chunk groups fill whole warps
     WinDirCfg d{};
     d.dt = C::DT;
     d.v = C::V;
@@ -124,6 +126,8 @@ using GFB_64_2 = WinShape<float, 64, 2, 32, 2, 64, 1, true>;
 using GWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 1, 160, 5, false>;
 using GWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 1, 288, 2, false>;
 using GWB_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 2, 288, 2, false>;
+using GWB_BF_32_2_8_M4 = WinShape<bf16_t, 32, 2, 8, 2, 160, 4, false>;
+using GWB_BF_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 2, 160, 5, false>;
 using GWB_FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 288, 2, false>;
 
 #define F(SH, N) gdir_cfg<SH, true>(N)
@@ -133,8 +137,10 @@ using GWB_FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 288, 2, false>;
 const WinVariant kGatedBF16[] = {
     {"gseq_bf16_d64_v1", F(GBF_64_1, 8), B(GBB_64_1, 6)},
     {"gseq_bf16_d64_v2", F(GBF_64_2, 8), B(GBB_64_2, 6)},
-    {"gwin_bf16_d32_s8", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8, 16, 2)},
-    {"gwin_bf16_d32_s8_n3", FW(GWF_BF_32_2_8, 8, 3), BW(GWB_BF_32_2_8, 16, 3)},
+    {"gwin_bf16_d32_s8", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8_M5, 8, 2)},
+    {"gwin_bf16_d32_s8_n3", FW(GWF_BF_32_2_8, 8, 3), BW(GWB_BF_32_2_8_M5, 8, 3)},
+    {"gwin_bf16_d32_s8_m4", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8_M4, 8, 2)},
+    {"gwin_bf16_d32_s16", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8, 16, 2)},
 };
 const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
@@ -157,12 +163,13 @@ const WinVariant *gwin_variants(int dtype, int *count) {
     return kGatedBF16;
 }
 
-int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
-                        long long rows, int ncol, int nu_rows, int D, cudaStream_t stream) {
-    const long long n = rows + D;
-    if (n == 0) return 0;
-    gated_finish<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(part_eta, part_nu, grad_eta,
-                                                                           grad_nu_log, rows, ncol, nu_rows, D);
+int gated_finish_launch(const float *part_eta, int ncol, long long rows, float *grad_eta, const float *part_nu,
+                        int nu_rows, int D, float *grad_nu_log, cudaStream_t stream) {
+    const unsigned b0 = static_cast<unsigned>((rows + kFinishCols - 1) / kFinishCols);
+    const unsigned b1 = static_cast<unsigned>((D + kFinishCols - 1) / kFinishCols);
+    if (b0 + b1 == 0) return 0;
+    gated_finish<<<b0 + b1, dim3(kFinishCols, kFinishSplit), 0, stream>>>(part_eta, ncol, rows, grad_eta, part_nu,
+                                                                         nu_rows, D, grad_nu_log, b0);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

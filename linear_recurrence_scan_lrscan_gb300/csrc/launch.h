@@ -55,6 +55,7 @@ struct WinLaunch {
     // sums, and the plain kernels' tensor inputs (in0 = b or out, in1 = grad_out)
     const float *eta, *nu_log;
     float *part_eta, *part_nu;
+    int64_t part_rows;            // column stride of part_eta: rows B*T of the whole call
     const void *in0, *in1;
 };
 
@@ -87,11 +88,12 @@ const WinVariant *win_variants(int path, int dtype, int *count);
 const WinVariant *cwin_variants(int dtype, int *count);
 
 // Generated-decay scan (kernels_gated.cu): tile variants, the plain
-// kernels, and the partial-sum reduction (part_eta [rows][ncol], part_nu [B][D]).
+// kernels, and the partial-sum reduction (part_eta [ncol][rows], part_nu
+// [nu_rows][D]; both column sums are scaled by ln 2).
 const WinVariant *gwin_variants(int dtype, int *count);
 int gplain_launch(const WinLaunch &L, int dtype, bool fwd);
-int gated_finish_launch(const float *part_eta, const float *part_nu, float *grad_eta, float *grad_nu_log,
-                        long long rows, int ncol, int nu_rows, int D, cudaStream_t stream);
+int gated_finish_launch(const float *part_eta, int ncol, long long rows, float *grad_eta, const float *part_nu,
+                        int nu_rows, int D, float *grad_nu_log, cudaStream_t stream);
 // Most sub-chunks a windowed generated-decay backward tile uses (rows of its
 // grad_nu_log partials per batch row).
 constexpr int kGatedMaxS = 16;

@@ -983,7 +983,8 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
             L.maps[1] = &mg;
             L.eta = eta + b0 * T;
             L.out0 = static_cast<char *>(grad_b) + off;
-            L.part_eta = part_eta + static_cast<size_t>(b0) * T * ncol;
+            L.part_eta = part_eta + static_cast<size_t>(b0) * T;  // [ncol][B*T]: row offset of this slice
+            L.part_rows = B * T;
             L.part_nu = part_nu + static_cast<size_t>(b0) * (win ? v.s : 1) * D;
             L.B = nb; L.T = T; L.D = D;
             if (v.launch(L, v))
@@ -991,7 +992,7 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
         }
     }
     if (ncol > gated_ncol_bound(D)) return fail(LRSCAN_EINVAL, "internal: partial columns exceed the workspace");
-    if (gated_finish_launch(part_eta, part_nu, grad_eta, grad_nu_log, B * T, ncol, nu_rows, static_cast<int>(D),
+    if (gated_finish_launch(part_eta, ncol, B * T, grad_eta, part_nu, nu_rows, static_cast<int>(D), grad_nu_log,
                             st))
         return fail(LRSCAN_ECUDA, "generated-decay reduction launch failed");
     return LRSCAN_OK;
