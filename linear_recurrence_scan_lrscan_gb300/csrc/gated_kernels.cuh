@@ -184,8 +184,8 @@ gwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restric
 // keeps several times more warps busy than the sequential form.
 template <class C>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
-gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ eta,
-                 const float *__restrict__ nu_log, typename C::St *__restrict__ out, float *__restrict__ last,
+gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
+                 const float *__restrict__ eta, const float *__restrict__ nu_log, float *__restrict__ last,
                  const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 1 && C::G <= 32 && 32 % C::G == 0 && C::G >= C::L,
                   "generated-decay windowed forward: lane-scan shape, one plane, row groups within a warp");
@@ -221,11 +221,18 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restri
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
+    // out tiles: staged in shared memory (two window buffers) and written by
+    // one thread outside the lane scan with a bulk tensor store, one window
+    // late; the tensor map clips rows past T and lanes past D
+    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));
+    const int obuf_elems = sm.W * DT;
+    const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     float nu2[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
     float ev = eta_at(eta_row, s * L + myrow, T);  // eta of row myrow of the current window's sub-chunk
     float h[V];
+    int replayed = 0;
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
     for (int k = 0; k < sm.nwin; ++k) {
@@ -277,6 +284,14 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restri
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) break;
+        if (issuer && k > 0) {
+            // every thread's rows of window k-1 are staged (fenced before the
+            // barrier above); once this store has been issued, the one before
+            // it must have finished reading the buffer window k is about to fill
+            tma_store_3d(&tm_out, smem_addr(obuf + ((k - 1) & 1) * obuf_elems), d0, (k - 1) * sm.W, brow);
+            bulk_commit();
+            bulk_wait_read<1>();
+        }
         // lane threads push the carried state through the sub-chunk maps in order
         float *entry = sm.sEntry<C>();
         if (static_cast<int>(threadIdx.x) < DT) {
@@ -292,18 +307,31 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const float *__restri
         bar_sync_or(1, NT, false);
 #pragma unroll
         for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
-        St *op = out + (row0 + rbase) * D + d;
+        St *op = obuf + (k & 1) * obuf_elems + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = 0; j < L; ++j) {
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
-            if (lane_ok && (n == L || j < n)) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
+            store_lanes<St, V>(op + j * DT, h);
         }
+        fence_proxy_async_smem();
+        replayed = k + 1;
         if (last != nullptr && lane_ok && n > 0 && rbase + n == T) {
 #pragma unroll
             for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
         }
         ev = evn;
+    }
+    // the last window's tile (not after an abort), then every store complete
+    // before the CTA's shared memory goes away
+    const bool aborted = bar_sync_or(1, NT, replayed != sm.nwin);
+    if (issuer) {
+        if (!aborted && replayed > 0) {
+            tma_store_3d(&tm_out, smem_addr(obuf + ((replayed - 1) & 1) * obuf_elems), d0, (replayed - 1) * sm.W,
+                         brow);
+            bulk_commit();
+        }
+        bulk_wait<0>();
     }
 }
 

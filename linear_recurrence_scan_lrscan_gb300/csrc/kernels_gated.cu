@@ -33,10 +33,9 @@ int launch_gwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    using St = typename C::St;
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], L.eta, L.nu_log, static_cast<St *>(L.out0), L.last, g,
-                                     L.status, L.timeout_ns);
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), win_out_smem(g),
+                                     L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, L.last, g, L.status,
+                                     L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -106,7 +105,7 @@ WinDirCfg gwdir_cfg(int S, int nstage) {
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
-    d.smem = g.smem_bytes;
+    d.smem = FWD ? win_out_smem(g) : g.smem_bytes;  // forward: plus the out staging buffers
     d.stage_bytes = g.stage_bytes;
     if constexpr (FWD) d.launch = &launch_gwinw_fwd<C>;
     else d.launch = &launch_gwinw_bwd<C>;

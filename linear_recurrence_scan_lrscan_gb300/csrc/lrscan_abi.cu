@@ -905,9 +905,12 @@ int run_gfwd(const float *eta, const float *nu_log, const void *b, void *out, fl
     for (int64_t b0 = 0; b0 < B; b0 += 65535) {
         const int64_t nb = std::min<int64_t>(65535, B - b0);
         const size_t off = static_cast<size_t>(b0) * T * D * es;
-        CUtensorMap mb;
-        if (encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+        CUtensorMap mb, mo;  // mo: the windowed tile writes out through a bulk tensor store
+        if (encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w) ||
+            encode_map(&mo, static_cast<char *>(out) + off, dtype, nb, T, D, v.dt, v.w))
+            return LRSCAN_EINVAL;
         L.maps[0] = &mb;
+        L.maps[1] = &mo;
         L.eta = eta + b0 * T;
         L.out0 = static_cast<char *>(out) + off;
         L.last = last ? last + b0 * D : nullptr;

@@ -109,6 +109,12 @@ __host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D
     return g;
 }
 
+// Output staging of kernels that write their result tiles back with bulk
+// tensor stores: two buffers of one window (W rows x DT lanes, storage type)
+// after the rest of the layout.
+__host__ __device__ inline int win_out_off(const WinGeom &g) { return (g.smem_bytes + 127) & ~127; }
+__host__ __device__ inline int win_out_smem(const WinGeom &g) { return win_out_off(g) + 2 * g.tile_bytes; }
+
 // Shared-memory layout of one CTA, with the launch geometry copied into
 // registers once (reading it through a pointer to the parameter would turn
 // every access into a generic load through L1).
