@@ -296,6 +296,11 @@ size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len);
  * 1 backward.  aligned16: whether the call's pointers are 16-byte aligned. */
 int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
                 const lrscan_opts *opts, lrscan_plan_info *info);
+/* lrscan_plan for a call with carried state or resets (lrscan_fwd_state,
+ * lrscan_bwd_state, the _ex calls given a state): the bf16 backward's
+ * automatic choice differs there. */
+int lrscan_plan_state(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
+                      const lrscan_opts *opts, lrscan_plan_info *info);
 
 /* Number of tile variants of a path (for sweeps); names via lrscan_plan. */
 int lrscan_num_variants(int path, int dtype, int dir);

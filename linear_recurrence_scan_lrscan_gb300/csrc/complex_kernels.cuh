@@ -282,7 +282,7 @@ template <class C>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                  const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
-                 typename C::St *__restrict__ out_r, typename C::St *__restrict__ out_i,
+                 const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
                  float *__restrict__ last_r, float *__restrict__ last_i, const __grid_constant__ WinGeom geom,
                  DevStatus *status, uint64_t timeout_ns) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 4, "windowed complex forward: lane-scan shape, four planes");
@@ -314,11 +314,16 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     const int lane = threadIdx.x & 31;
     const int d = d0 + lg * V;
     const bool lane_ok = d < D;
-    const size_t row0 = static_cast<size_t>(brow) * T;
     float4 *pq = reinterpret_cast<float4 *>(smem_raw + geom.scan_off);                          // [S][DT]
     float2 *entry = reinterpret_cast<float2 *>(smem_raw + geom.scan_off + S * DT * 16);         // [S][DT]
     float cr = 0.0f, ci = 0.0f;  // window-to-window state of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
+    // out_r / out_i tiles staged in shared memory, stored by one thread
+    // outside the lane scan a window late (rows past T, lanes past D clipped)
+    const OutStage<2, St> ost = make_out_stage<2, St>(smem_raw, geom);
+    const CUtensorMap *const omaps[2] = {&tm_or, &tm_oi};
+    const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
+    int replayed = 0;
     for (int k = 0; k < sm.nwin; ++k) {
         const int rbase = k * sm.W + s * L;
         const int n = min(max(T - rbase, 0), L);
@@ -364,6 +369,13 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
             pq[s * DT + v * G + lg] = make_float4(pr, pi, qr, qi);
         }
         if (bar_sync_or(1, NT, !ok)) break;
+        if (issuer && k > 0) {
+            // window k-1's rows are staged and fenced; once its stores are
+            // issued, the ones before must have finished reading the buffers
+            // window k is about to fill
+            ost.store(omaps, k - 1, d0, (k - 1) * sm.W, brow);
+            bulk_wait_read<1>();
+        }
         if (static_cast<int>(threadIdx.x) < DT) {
             float hr = cr, hi = ci;
 #pragma unroll 4
@@ -384,7 +396,8 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
             hr[v] = e.x;
             hi[v] = e.y;
         }
-        const size_t o = (row0 + rbase) * D + d;
+        St *const sor = ost.plane(k, 0) + (s * L) * DT + lg * V;
+        St *const soi = ost.plane(k, 1) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = 0; j < L; ++j) {
 #pragma unroll
@@ -393,11 +406,11 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
                 cmul_add(xr[j][v], xi[j][v], hr[v], hi[v], yr[j][v], yi[j][v], nr, ni);
                 hr[v] = nr; hi[v] = ni;
             }
-            if (lane_ok && (n == L || j < n)) {
-                store_lanes<St, V>(out_r + o + static_cast<size_t>(j) * D, hr);
-                store_lanes<St, V>(out_i + o + static_cast<size_t>(j) * D, hi);
-            }
+            store_lanes<St, V>(sor + j * DT, hr);
+            store_lanes<St, V>(soi + j * DT, hi);
         }
+        fence_proxy_async_smem();
+        replayed = k + 1;
         if (lane_ok && n > 0 && rbase + n == T) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
@@ -405,6 +418,13 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
                 if (last_i) last_i[static_cast<size_t>(brow) * D + d + v] = hi[v];
             }
         }
+    }
+    // the last window's tiles (not after an abort), then every store
+    // complete before the CTA's shared memory goes away
+    const bool aborted = bar_sync_or(1, NT, replayed != sm.nwin);
+    if (issuer) {
+        if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (replayed - 1) * sm.W, brow);
+        bulk_wait<0>();
     }
 }
 

@@ -461,8 +461,8 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
 template <class C>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_go,
-                 const float *__restrict__ eta, const float *__restrict__ nu_log,
-                 typename C::St *__restrict__ grad_b, float *__restrict__ part_eta, long long prow,
+                 const __grid_constant__ CUtensorMap tm_gb, const float *__restrict__ eta,
+                 const float *__restrict__ nu_log, float *__restrict__ part_eta, long long prow,
                  float *__restrict__ part_nu, const __grid_constant__ WinGeom geom, DevStatus *status,
                  uint64_t timeout_ns) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 2 && C::L == 8 && C::G == 16,
@@ -510,6 +510,12 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     float ev = eta_at(eta_row, (nwin - 1) * sm.W + s * L + myrow, T);  // current window
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
+    // grad_b tiles staged in shared memory, stored by one thread outside the
+    // lane scan a window late (rows past T and lanes past D are clipped)
+    const OutStage<1, St> ost = make_out_stage<1, St>(smem_raw, geom);
+    const CUtensorMap *const omaps[1] = {&tm_gb};
+    const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
+    int replayed = 0;
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
         const int rbase = wbase + s * L;
@@ -581,6 +587,13 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) break;
+        if (issuer && k > 0) {
+            // window k-1's rows are staged and fenced; once its store is
+            // issued, the one before must have finished reading the buffer
+            // window k is about to fill
+            ost.store(omaps, k - 1, d0, wbase + sm.W, brow);
+            bulk_wait_read<1>();
+        }
         float *entry = sm.sEntry<C>();
         if (static_cast<int>(threadIdx.x) < DT) {
             float c = carry;
@@ -596,7 +609,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
         for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
         float qrow[L];
-        St *gbp = grad_b + (row0 + rbase) * D + d;
+        St *gbp = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = L - 1; j >= 0; --j) {
             float qs = 0.0f;
@@ -608,8 +621,10 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
                 qs += q;
             }
             qrow[j] = qs;
-            if (lane_ok && (n == L || j < n)) store_lanes<St, V>(gbp + static_cast<size_t>(j) * D, g);
+            store_lanes<St, V>(gbp + j * DT, g);
         }
+        fence_proxy_async_smem();
+        replayed = k + 1;
         // row sums over the sub-chunk's 16 threads (both half-warps do the same steps)
 #pragma unroll
         for (int j = 0; j < L; ++j) qrow[j] += __shfl_xor_sync(0xffffffffu, qrow[j], 8);
@@ -630,6 +645,13 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     if (lane_ok) {
 #pragma unroll
         for (int v = 0; v < V; ++v) part_nu[(static_cast<size_t>(brow) * S + s) * D + d + v] = acc_nu[v];
+    }
+    // the last processed window's tile (not after an abort), then every store
+    // complete before the CTA's shared memory goes away
+    const bool aborted = bar_sync_or(1, NT, replayed != nwin);
+    if (issuer) {
+        if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (nwin - replayed) * sm.W, brow);
+        bulk_wait<0>();
     }
 }
 

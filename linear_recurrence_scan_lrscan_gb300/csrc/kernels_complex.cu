@@ -37,11 +37,9 @@ int launch_cwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_cwin_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    using St = typename C::St;
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
-                                     static_cast<St *>(L.out0), static_cast<St *>(L.out1), L.last, L.last_i, g,
-                                     L.status, L.timeout_ns);
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
+                                     win_out_smem(g, 2), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
+                                     *L.maps[4], *L.maps[5], L.last, L.last_i, g, L.status, L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -98,7 +96,7 @@ WinDirCfg cwdir_cfg(int S, int nstage) {
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
-    d.smem = g.smem_bytes;
+    d.smem = win_out_smem(g, 2);  // plus the out_r / out_i staging buffers
     d.stage_bytes = g.stage_bytes;
     d.launch = &launch_cwinw_fwd<C>;
     return d;

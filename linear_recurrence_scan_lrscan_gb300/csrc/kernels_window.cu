@@ -29,7 +29,7 @@ WinDirCfg dir_cfg(int S, int nstage) {
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
-    d.smem = g.smem_bytes;
+    d.smem = win_staged<C>() ? win_out_smem(g, FWD ? 1 : 2) : g.smem_bytes;  // plus the output staging buffers
     d.stage_bytes = g.stage_bytes;
     if constexpr (FWD) {
         static_assert(C::NIN == 2, "forward tiles: a, b");

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <iterator>
 #include <map>
 #include <mutex>
 
@@ -233,25 +234,33 @@ struct Pref {
     double max_ctas_per_sm;
 };
 constexpr double kAny = 1e30;
-const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s16_pt", 0.45, kAny}};
-const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny},
-                            {kPathWindow, "win_f32_d32_s16_pt", 0.45, kAny}};
+const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
+const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny}, {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
 const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
                              {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
-const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
-                             {kPathWindow, "win_bf16_d32_s16_n2", 0.9, kAny},
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, 5.0},
+                             {kPathWindow, "win_bf16_d32_l16_s8", 0.9, kAny},
                              {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
+// With carried state / resets the backward's extra per-row work (reset
+// masks, grad_last entry, grad_h0) no longer fits the five-CTA tile's
+// registers; the 16-sub-chunk tile measured fastest there.
+const Pref kPrefBF16BwdState[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
+                                  {kPathWindow, "win_bf16_d32_s16_n2", 0.9, kAny},
+                                  {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
 
-bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g, int *path, int *vidx) {
+bool auto_candidate(int dtype, int dir, bool ext, int64_t B, int64_t D, const Geometry &g, int *path, int *vidx) {
     const Pref *list;
     int n;
     if (dtype == LRSCAN_F32) {
         list = dir == 0 ? kPrefF32Fwd : kPrefF32Bwd;
-        n = 2;
+        n = dir == 0 ? static_cast<int>(std::size(kPrefF32Fwd)) : static_cast<int>(std::size(kPrefF32Bwd));
+    } else if (dir == 0) {
+        list = kPrefBF16Fwd;
+        n = static_cast<int>(std::size(kPrefBF16Fwd));
     } else {
-        list = dir == 0 ? kPrefBF16Fwd : kPrefBF16Bwd;
-        n = 3;
+        list = ext ? kPrefBF16BwdState : kPrefBF16Bwd;
+        n = ext ? static_cast<int>(std::size(kPrefBF16BwdState)) : static_cast<int>(std::size(kPrefBF16Bwd));
     }
     for (int i = 0; i < n; ++i) {
         int cnt = 0;
@@ -270,8 +279,9 @@ bool auto_candidate(int dtype, int dir, int64_t B, int64_t D, const Geometry &g,
     return false;
 }
 
+// ext: the call carries state or resets (lrscan_fwd_state / lrscan_bwd_state).
 int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
-              const Geometry &g, Choice *ch) {
+              const Geometry &g, Choice *ch, bool ext = false) {
     const int want = opts ? opts->path : 0;
     const int force_v = opts ? opts->tile_variant : 0;
     int chunk = opts && opts->chunk_len ? opts->chunk_len : 64;
@@ -288,7 +298,7 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
     if (path == kPathAuto) {
         if (!aligned16) {
             path = (B * D < 32LL * g.sm_count * 32 && T >= 16LL * chunk) ? kPathChunk : kPathPlain;
-        } else if (auto_candidate(dtype, dir, B, D, g, &path, &auto_vi)) {
+        } else if (auto_candidate(dtype, dir, ext, B, D, g, &path, &auto_vi)) {
             // measured preference list (see auto_candidate)
         } else if (T >= 16LL * chunk) {
             // too few lanes for a lane-tiled walk to fill the GPU: parallelize
@@ -523,20 +533,22 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
     cudaGetDevice(&dev);
     const bool al = aligned16({a, b, out}, D, dtype);
     Choice ch;
-    if ((rc = plan_call(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
+    if ((rc = plan_call(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     const size_t es = esize(dtype);
     if (ch.path == kPathSeq || ch.path == kPathWindow) {
         const WinDirCfg &v = ch.var->fwd;
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
             const size_t off = static_cast<size_t>(b0) * T * D * es;
-            CUtensorMap ma, mb;
+            CUtensorMap ma, mb, mo;  // mo: lane-scan tiles write out through bulk tensor stores
             if (encode_map(&ma, static_cast<const char *>(a) + off, dtype, nb, T, D, v.dt, v.w) ||
-                encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w))
+                encode_map(&mb, static_cast<const char *>(b) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mo, static_cast<char *>(out) + off, dtype, nb, T, D, v.dt, v.w))
                 return LRSCAN_EINVAL;
             WinLaunch L{};
             L.maps[0] = &ma;
             L.maps[1] = &mb;
+            L.maps[2] = &mo;
             L.out0 = static_cast<char *>(out) + off;
             L.last = last ? last + b0 * D : nullptr;
             L.B = nb; L.T = T; L.D = D;
@@ -580,22 +592,26 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
     cudaGetDevice(&dev);
     const bool al = aligned16({a, out, grad_out, grad_a, grad_b}, D, dtype);
     Choice ch;
-    if ((rc = plan_call(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
+    if ((rc = plan_call(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     const size_t es = esize(dtype);
     if (ch.path == kPathSeq || ch.path == kPathWindow) {
         const WinDirCfg &v = ch.var->bwd;
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
             const size_t off = static_cast<size_t>(b0) * T * D * es;
-            CUtensorMap ma, mo, mg;
+            CUtensorMap ma, mo, mg, mga, mgb;  // mga, mgb: lane-scan tiles write through bulk tensor stores
             if (encode_map(&ma, static_cast<const char *>(a) + off, dtype, nb, T, D, v.dt, v.w) ||
                 encode_map(&mo, static_cast<const char *>(out) + off, dtype, nb, T, D, v.dt, v.w) ||
-                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w))
+                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mga, static_cast<char *>(grad_a) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mgb, static_cast<char *>(grad_b) + off, dtype, nb, T, D, v.dt, v.w))
                 return LRSCAN_EINVAL;
             WinLaunch L{};
             L.maps[0] = &ma;
             L.maps[1] = &mo;
             L.maps[2] = &mg;
+            L.maps[3] = &mga;
+            L.maps[4] = &mgb;
             L.out0 = static_cast<char *>(grad_a) + off;
             L.out1 = static_cast<char *>(grad_b) + off;
             L.B = nb; L.T = T; L.D = D;
@@ -733,12 +749,13 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
     for (int64_t b0 = 0; b0 < B; b0 += 65535) {
         const int64_t nb = std::min<int64_t>(65535, B - b0);
         const size_t off = static_cast<size_t>(b0) * T * D * es;
-        CUtensorMap m[4];
-        for (int i = 0; i < 4; ++i)
-            if (encode_map(&m[i], static_cast<const char *>(in[i]) + off, dtype, nb, T, D, v.dt, v.w))
+        CUtensorMap m[6];  // ar, ai, br, bi; out_r, out_i (the windowed tiles write through bulk tensor stores)
+        const void *planes[6] = {in[0], in[1], in[2], in[3], out_r, out_i};
+        for (int i = 0; i < 6; ++i)
+            if (encode_map(&m[i], static_cast<const char *>(planes[i]) + off, dtype, nb, T, D, v.dt, v.w))
                 return LRSCAN_EINVAL;
         WinLaunch L{};
-        for (int i = 0; i < 4; ++i) L.maps[i] = &m[i];
+        for (int i = 0; i < 6; ++i) L.maps[i] = &m[i];
         L.out0 = static_cast<char *>(out_r) + off;
         L.out1 = static_cast<char *>(out_i) + off;
         L.last = last_r ? last_r + b0 * D : nullptr;
@@ -978,12 +995,14 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
         for (int64_t b0 = 0; b0 < B; b0 += 65535) {
             const int64_t nb = std::min<int64_t>(65535, B - b0);
             const size_t off = static_cast<size_t>(b0) * T * D * es;
-            CUtensorMap mo, mg;
+            CUtensorMap mo, mg, mgb;  // mgb: the windowed tile writes grad_b through bulk tensor stores
             if (encode_map(&mo, static_cast<const char *>(out) + off, dtype, nb, T, D, v.dt, v.w) ||
-                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w))
+                encode_map(&mg, static_cast<const char *>(grad_out) + off, dtype, nb, T, D, v.dt, v.w) ||
+                encode_map(&mgb, static_cast<char *>(grad_b) + off, dtype, nb, T, D, v.dt, v.w))
                 return LRSCAN_EINVAL;
             L.maps[0] = &mo;
             L.maps[1] = &mg;
+            L.maps[2] = &mgb;
             L.eta = eta + b0 * T;
             L.out0 = static_cast<char *>(grad_b) + off;
             L.part_eta = part_eta + static_cast<size_t>(b0) * T;  // [ncol][B*T]: row offset of this slice
@@ -1178,8 +1197,8 @@ size_t lrscan_workspace_bytes(int64_t B, int64_t T, int64_t D, int chunk_len) {
     return chunk_workspace(B, T, D, C);
 }
 
-int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16, const lrscan_opts *opts,
-                lrscan_plan_info *info) {
+static int plan_entry(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16, const lrscan_opts *opts,
+                      lrscan_plan_info *info, bool ext) {
     if (!info || (dir != 0 && dir != 1)) return LRSCAN_EINVAL;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
@@ -1187,10 +1206,21 @@ int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_alig
     if (device_ctx(&ctx) != LRSCAN_OK) ctx = nullptr;  // no device: plan for one GB300
     const bool al = is_aligned16 && (D * esize(dtype)) % 16 == 0;
     Choice ch;
-    if ((rc = plan_call(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch)))
+    if ((rc = plan_call(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch,
+                        ext)))
         return rc;
     fill_info(ch, info);
     return LRSCAN_OK;
+}
+
+int lrscan_plan(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16, const lrscan_opts *opts,
+                lrscan_plan_info *info) {
+    return plan_entry(B, T, D, dtype, dir, is_aligned16, opts, info, false);
+}
+
+int lrscan_plan_state(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
+                      const lrscan_opts *opts, lrscan_plan_info *info) {
+    return plan_entry(B, T, D, dtype, dir, is_aligned16, opts, info, true);
 }
 
 int lrscan_num_variants(int path, int dtype, int dir) {

@@ -113,7 +113,35 @@ __host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D
 // tensor stores: two buffers of one window (W rows x DT lanes, storage type)
 // after the rest of the layout.
 __host__ __device__ inline int win_out_off(const WinGeom &g) { return (g.smem_bytes + 127) & ~127; }
-__host__ __device__ inline int win_out_smem(const WinGeom &g) { return win_out_off(g) + 2 * g.tile_bytes; }
+__host__ __device__ inline int win_out_smem(const WinGeom &g, int planes = 1) {
+    return win_out_off(g) + 2 * planes * g.tile_bytes;
+}
+// Window tiles that stage their outputs this way: the lane-scan tiles (out
+// forward; grad_a and grad_b backward).
+template <class C> __host__ __device__ constexpr bool win_staged() { return !C::SEQ && !C::PT; }
+
+// NP output planes staged per processed window, double-buffered:
+// [2][NP][W][DT] storage elements at win_out_off.  Every consumer thread
+// writes its rows into plane(k, p) and fences them for the async proxy; after
+// the next window's first barrier one thread stores them (store), so the
+// buffers alternate and each store overlaps a window of compute.
+template <int NP, class St>
+struct OutStage {
+    St *buf;
+    int elems;  // W * DT
+    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((kw & 1) * NP + p) * elems; }
+    // bulk tensor stores of processed window kw's planes at (x, y, z), one group
+    __device__ __forceinline__ void store(const CUtensorMap *const (&maps)[NP], int kw, int x, int y, int z) const {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) tma_store_3d(maps[p], smem_addr(plane(kw, p)), x, y, z);
+        bulk_commit();
+    }
+};
+template <int NP, class St>
+__device__ __forceinline__ OutStage<NP, St> make_out_stage(unsigned char *smem, const WinGeom &g) {
+    return OutStage<NP, St>{reinterpret_cast<St *>(smem + win_out_off(g)),
+                            g.tile_bytes / static_cast<int>(sizeof(St))};
+}
 
 // Shared-memory layout of one CTA, with the launch geometry copied into
 // registers once (reading it through a pointer to the parameter would turn
@@ -243,10 +271,15 @@ __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, 
 template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-               typename C::St *__restrict__ out, float *__restrict__ last, const __grid_constant__ WinGeom geom,
-               DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StateArgs sx) {
+               const __grid_constant__ CUtensorMap tm_out, typename C::St *__restrict__ out, float *__restrict__ last,
+               const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns,
+               const __grid_constant__ StateArgs sx) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    // lane-scan tiles stage out in shared memory (two window buffers, written
+    // back by bulk tensor stores that clip rows past T and lanes past D);
+    // sequential and per-thread-prefix tiles store from registers
+    constexpr bool TS = win_staged<C>();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
@@ -280,6 +313,11 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (lane scan, threads < DT)
     bool failed = false;
     int stage = 0, use = 0;
+    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));
+    const int obuf_elems = sm.W * DT;
+    // one thread outside the lane scan issues each window's store one window late
+    const bool issuer = TS && static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
+    int replayed = 0;
     // EXT: this warp's rows start at window row wrow; bit j of rbits is a
     // reset at row s*L + j of the current window.  Positions are loaded two
     // windows ahead (pos_next: window k+1, pos_next2: window k+2).
@@ -418,6 +456,14 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
+        if (issuer && k > 0) {
+            // every thread's rows of window k-1 are staged (fenced before the
+            // barrier above); once this store has been issued, the one before
+            // it must have finished reading the buffer window k is about to fill
+            tma_store_3d(&tm_out, smem_addr(obuf + ((k - 1) & 1) * obuf_elems), d0, (k - 1) * sm.W, brow);
+            bulk_commit();
+            bulk_wait_read<1>();
+        }
         if constexpr (!C::PT) {
             // Threads 0..DT-1 each own one lane: push the carried state through
             // the sub-chunk maps in order, recording every sub-chunk's entry
@@ -451,8 +497,18 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        St *op = out + (row0 + rbase) * D + d;
-        if (n == L) {
+        if constexpr (TS) {
+            St *op = obuf + (k & 1) * obuf_elems + (s * L) * DT + lg * V;
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+                store_lanes<St, V>(op + j * DT, h);
+            }
+            fence_proxy_async_smem();
+            replayed = k + 1;
+        } else if (n == L) {
+            St *op = out + (row0 + rbase) * D + d;
 #pragma unroll
             for (int j = 0; j < L; ++j) {
 #pragma unroll
@@ -460,6 +516,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(j) * D, h);
             }
         } else {
+            St *op = out + (row0 + rbase) * D + d;
             // identity steps past T leave h unchanged; their rows are not stored
 #pragma unroll
             for (int j = 0; j < L; ++j) {
@@ -484,12 +541,27 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
         for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
     }
+    if constexpr (TS) {
+        // the last window's tile (not after an abort), then every store
+        // complete before the CTA's shared memory goes away
+        const bool aborted = bar_sync_or(1, NT, replayed != sm.nwin);
+        if (issuer) {
+            if (!aborted && replayed > 0) {
+                tma_store_3d(&tm_out, smem_addr(obuf + ((replayed - 1) & 1) * obuf_elems), d0,
+                             (replayed - 1) * sm.W, brow);
+                bulk_commit();
+            }
+            bulk_wait<0>();
+        }
+    }
 }
 
 // ============================================================================
 // Backward
 // ============================================================================
-template <class C, bool MASK>
+// STAGED: gb and ga point into the shared-memory staging tiles (row stride
+// DT, every row written; the bulk store clips rows past T and lanes past D).
+template <class C, bool MASK, bool STAGED>
 __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const float (&xh)[C::L][C::V],
                                          const float (&xg)[C::L][C::V], float (&g)[C::V], int n, bool lane_ok,
                                          typename C::St *gb, typename C::St *ga, int D, uint32_t rbits) {
@@ -506,7 +578,10 @@ __device__ __forceinline__ void bwd_rows(const float (&xa)[C::L][C::V], const fl
             gav[v] = __fmul_rn(g[v], xh[j][v]);
             if constexpr (MASK) gav[v] = ((rbits >> j) & 1u) ? 0.0f : gav[v];  // a_t unused at a reset
         }
-        if (lane_ok && (n == L || j < n)) {
+        if constexpr (STAGED) {
+            store_lanes<St, V>(gb + j * C::DT, g);
+            store_lanes<St, V>(ga + j * C::DT, gav);
+        } else if (lane_ok && (n == L || j < n)) {
             store_lanes<St, V>(gb + static_cast<size_t>(j) * D, g);
             store_lanes<St, V>(ga + static_cast<size_t>(j) * D, gav);
         }
@@ -529,11 +604,15 @@ __device__ __forceinline__ void store_grad_h0(const StateArgs &sx, const SegRow 
 template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_out,
-               const __grid_constant__ CUtensorMap tm_go, typename C::St *__restrict__ grad_a,
+               const __grid_constant__ CUtensorMap tm_go, const __grid_constant__ CUtensorMap tm_ga,
+               const __grid_constant__ CUtensorMap tm_gb, typename C::St *__restrict__ grad_a,
                typename C::St *__restrict__ grad_b, const __grid_constant__ WinGeom geom, DevStatus *status,
                uint64_t timeout_ns, const __grid_constant__ StateArgs sx) {
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    // lane-scan tiles stage grad_a and grad_b in shared memory (two window
+    // buffers of both planes) and write them back with bulk tensor stores
+    constexpr bool TS = win_staged<C>();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const WinSmem sm = WinSmem::make(smem_raw, geom);
     const int S = geom.S;
@@ -571,6 +650,18 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (lane scan, threads < DT)
     int stage = 0, use = 0;
     bool failed = false;
+    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));  // [buffer][grad_a, grad_b][W][DT]
+    const int obuf_elems = sm.W * DT;
+    const bool issuer = TS && static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
+    int replayed = 0;
+    // one thread outside the lane scan stores processed window kw from buffer kw & 1
+    auto store_window = [&](int kw) {
+        const uint32_t src = smem_addr(obuf + (kw & 1) * 2 * obuf_elems);
+        const int y = (nwin - 1 - kw) * sm.W;
+        tma_store_3d(&tm_ga, src, d0, y, brow);
+        tma_store_3d(&tm_gb, src + obuf_elems * static_cast<uint32_t>(sizeof(St)), d0, y, brow);
+        bulk_commit();
+    };
     // EXT: bit j of r0bits / r1bits is a reset at row s*L + j / s*L + j + 1
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
@@ -748,6 +839,13 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
         for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
+        if (issuer && k > 0) {
+            // rows of window k-1 are staged and fenced; after issuing its
+            // stores, the ones before must have finished reading the buffer
+            // window k is about to fill
+            store_window(k - 1);
+            bulk_wait_read<1>();
+        }
         if constexpr (!C::PT) {
             // lane threads push the carried adjoint through sub-chunks S-1 .. 0
             float *entry = sm.sEntry<C>();
@@ -778,9 +876,19 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-        const size_t gofs = (row0 + rbase) * D + d;
-        if (EXT && r0bits != 0) bwd_rows<C, true>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, r0bits);
-        else bwd_rows<C, false>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, 0u);
+        if constexpr (TS) {
+            St *sga = obuf + (k & 1) * 2 * obuf_elems + (s * L) * DT + lg * V;
+            St *sgb = sga + obuf_elems;
+            if (EXT && r0bits != 0) bwd_rows<C, true, true>(xa, xh, xg, g, n, lane_ok, sgb, sga, D, r0bits);
+            else bwd_rows<C, false, true>(xa, xh, xg, g, n, lane_ok, sgb, sga, D, 0u);
+            fence_proxy_async_smem();
+            replayed = k + 1;
+        } else {
+            const size_t gofs = (row0 + rbase) * D + d;
+            if (EXT && r0bits != 0)
+                bwd_rows<C, true, false>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, r0bits);
+            else bwd_rows<C, false, false>(xa, xh, xg, g, n, lane_ok, grad_b + gofs, grad_a + gofs, D, 0u);
+        }
         if (C::PT && s == 0) {
             float *nc = sm.sCarry<C>((k & 1) ^ 1);
 #pragma unroll
@@ -793,6 +901,15 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
     if constexpr (EXT && C::SEQ) {
         if (!failed && sx.grad_h0 != nullptr && lane_ok) store_grad_h0<C>(sx, seg, row0, brow, d, D, g);
+    }
+    if constexpr (TS) {
+        // the last window's tiles (not after an abort), then every store
+        // complete before the CTA's shared memory goes away
+        const bool aborted = bar_sync_or(1, NT, replayed != nwin);
+        if (issuer) {
+            if (!aborted && replayed > 0) store_window(replayed - 1);
+            bulk_wait<0>();
+        }
     }
     (void)failed;
 }

@@ -29,9 +29,10 @@ int launch_win_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], *L.maps[1], static_cast<typename C::St *>(L.out0), L.last,
-                                     g, L.status, L.timeout_ns, L.sx);
+    const int smem = win_staged<C>() ? win_out_smem(g) : g.smem_bytes;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), smem, L.stream,
+                                     *L.maps[0], *L.maps[1], *L.maps[2], static_cast<typename C::St *>(L.out0),
+                                     L.last, g, L.status, L.timeout_ns, L.sx);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -43,8 +44,9 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2],
+    const int smem = win_staged<C>() ? win_out_smem(g, 2) : g.smem_bytes;
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), smem, L.stream,
+                                     *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3], *L.maps[4],
                                      static_cast<typename C::St *>(L.out0), static_cast<typename C::St *>(L.out1), g,
                                      L.status, L.timeout_ns, L.sx);
     return e == cudaSuccess ? 0 : -1;

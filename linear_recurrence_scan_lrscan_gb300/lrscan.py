@@ -99,6 +99,8 @@ EXPORTS = {
     "lrscan_workspace_bytes": ([_I64, _I64, _I64, ctypes.c_int], ctypes.c_size_t),
     "lrscan_plan": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
                      ctypes.POINTER(PlanInfo)], ctypes.c_int),
+    "lrscan_plan_state": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
+                           ctypes.POINTER(PlanInfo)], ctypes.c_int),
     "lrscan_num_variants": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
     "lrscan_sync_check": ([], ctypes.c_int),
     "lrscan_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
@@ -484,16 +486,18 @@ def lrscan_gated_workspace_bytes(B: int, T: int, D: int) -> int:
 
 
 def lrscan_plan(B: int, T: int, D: int, dtype: torch.dtype | str = torch.float32, direction: str = "fwd",
-                aligned: bool = True, path=None, chunk_len=None, tile_variant=None) -> dict:
-    """What the dispatcher would run for this call (host only; no launch)."""
+                aligned: bool = True, path=None, chunk_len=None, tile_variant=None, state: bool = False) -> dict:
+    """What the dispatcher would run for this call (host only; no launch);
+    state=True plans a call with carried state or resets (lrscan_plan_state)."""
     code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
     if code is None:
         raise ValueError(f"unsupported dtype {dtype}")
     info = PlanInfo()
     o = _opts(path, chunk_len, tile_variant, None)
-    rc = lib().lrscan_plan(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
-                           ctypes.byref(o) if o is not None else None, ctypes.byref(info))
-    _check(rc, "lrscan_plan")
+    fn = lib().lrscan_plan_state if state else lib().lrscan_plan
+    rc = fn(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
+            ctypes.byref(o) if o is not None else None, ctypes.byref(info))
+    _check(rc, "lrscan_plan_state" if state else "lrscan_plan")
     return info.as_dict()
 
 

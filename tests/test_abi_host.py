@@ -87,9 +87,9 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s16_n4"),
-    3: ("win_f32_d32_s16_pt", "win_f32_d32_s16_pt"),
-    4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s16_n2"),
+    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s8_m5_n2"),
+    3: ("win_f32_d32_s16", "win_f32_d32_s16"),
+    4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l16_s8"),
     5: ("seq_f32_d32", "win_f32_d64_s8"),
 }
 
@@ -104,6 +104,17 @@ def test_occupancy_rule_on_the_named_workloads(lib, cid):
         assert p["kernels"] == 1
         # every lane tile of the GPU-filling variants gets a CTA of its own
         assert p["ctas"] == w.B * -(-w.D // p["lanes_per_cta"])
+
+
+def test_state_backward_takes_its_own_tile(lib):
+    """With carried state the bf16 backward takes the 16-sub-chunk tile (the
+    five-CTA tile's registers do not hold the extra per-row work); the forward
+    and the plain backward are unchanged."""
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
+    w = WORKLOADS[2]
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", state=True)["name"] == "win_bf16_d32_s16_n4"
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[2][1]
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", state=True)["name"] == EXPECTED_AUTO[2][0]
 
 
 def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
