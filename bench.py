@@ -293,7 +293,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     # step in SAMPLE_EVERY (an event between two kernels stops the next kernel's
     # launch from overlapping the previous one's tail, so the other steps run
     # without them); the step time is the region's end-to-end time.
-    sample_every = 8
+    sample_every = 32
     evs = {}
     clocks = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[dev.index]))

@@ -239,12 +239,15 @@ const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny}, {kPathWi
 const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
                              {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
-const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, 5.0},
+// bf16 backward up to 5 CTAs per SM: the 16-sub-chunk tile.  The five-CTA
+// tile is about 1 % faster launched alone, but the 16-sub-chunk tile's last
+// partial wave overlaps the next forward, which makes the forward + backward
+// step 1.5 % faster.
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
                              {kPathWindow, "win_bf16_d32_l16_s8", 0.9, kAny},
                              {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
-// With carried state / resets the backward's extra per-row work (reset
-// masks, grad_last entry, grad_h0) no longer fits the five-CTA tile's
-// registers; the 16-sub-chunk tile measured fastest there.
+// With carried state / resets: the 16-sub-chunk tiles (the extra per-row
+// work of resets, grad_last and grad_h0 spills in the five-CTA tile).
 const Pref kPrefBF16BwdState[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
                                   {kPathWindow, "win_bf16_d32_s16_n2", 0.9, kAny},
                                   {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};

@@ -87,7 +87,7 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s8_m5_n2"),
+    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_s16_n4"),
     3: ("win_f32_d32_s16", "win_f32_d32_s16"),
     4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l16_s8"),
     5: ("seq_f32_d32", "win_f32_d64_s8"),
@@ -106,15 +106,17 @@ def test_occupancy_rule_on_the_named_workloads(lib, cid):
         assert p["ctas"] == w.B * -(-w.D // p["lanes_per_cta"])
 
 
-def test_state_backward_takes_its_own_tile(lib):
-    """With carried state the bf16 backward takes the 16-sub-chunk tile (the
-    five-CTA tile's registers do not hold the extra per-row work); the forward
-    and the plain backward are unchanged."""
+def test_state_plans(lib):
+    """Calls with carried state plan with their own backward list: the
+    16-sub-chunk tiles at every lane count (the plain backward moves to the
+    16-row tile above five CTAs per SM); forwards are shared."""
     from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
-    w = WORKLOADS[2]
-    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", state=True)["name"] == "win_bf16_d32_s16_n4"
-    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[2][1]
-    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", state=True)["name"] == EXPECTED_AUTO[2][0]
+    for cid, want in ((2, "win_bf16_d32_s16_n4"), (4, "win_bf16_d32_s16_n2")):
+        w = WORKLOADS[cid]
+        assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", state=True)["name"] == want
+        assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", state=True)["name"] == EXPECTED_AUTO[cid][0]
+    w = WORKLOADS[4]
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[4][1] == "win_bf16_d32_l16_s8"
 
 
 def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
