@@ -129,6 +129,41 @@ int lrscan_bwd_ex(const void *a, const void *out, const void *grad_out,
                   void *stream, const lrscan_opts *opts);
 
 /*
+ * The same operations with host buffers: every [B,T,D] operand and `last`
+ * is a host pointer (page-locked memory moves at full link speed; pageable
+ * memory works through the driver's staging; device pointers are accepted
+ * too).  The call copies the inputs to device memory in chunks of
+ * ceil(B / 8) whole batch rows (fewer when one slot of a chunk's planes
+ * would pass 1 GiB, but at least one row), runs the device path on each chunk
+ * (lrscan_fwd_ex / lrscan_bwd_ex with `opts`), copies the results back, and
+ * returns when every host output is written.  Copies in, kernels and copies
+ * out run on three library-owned streams, so one chunk's kernels overlap the
+ * next chunk's copy in and the previous chunk's copy out.  Device staging is
+ * library-owned (up to three slots of one chunk's planes, kept for later
+ * calls).  Calls on one device run one at a time.
+ *
+ *   lrscan_fwd_host      a, b in; out, last out (last may be NULL).
+ *   lrscan_bwd_host      a, out, grad_out in; grad_a, grad_b out.
+ *   lrscan_fwd_bwd_host  a, b, grad_out in; out, last, grad_a, grad_b out:
+ *                        the forward then the backward of the same inputs,
+ *                        out staying on the device in between.
+ *
+ * Errors: as the device calls (a chunk's error stops the call after the
+ * copies already issued have drained), plus LRSCAN_ENOMEM when the staging
+ * cannot be allocated and LRSCAN_ECUDA for a failed copy.  A kernel's
+ * recorded error (LRSCAN_ETIMEOUT) is returned, and cleared, before the call
+ * returns.  T == 0 writes zeros to `last` and touches no device.
+ */
+int lrscan_fwd_host(const void *a, const void *b, void *out, float *last,
+                    int64_t B, int64_t T, int64_t D, int dtype, const lrscan_opts *opts);
+int lrscan_bwd_host(const void *a, const void *out, const void *grad_out,
+                    void *grad_a, void *grad_b,
+                    int64_t B, int64_t T, int64_t D, int dtype, const lrscan_opts *opts);
+int lrscan_fwd_bwd_host(const void *a, const void *b, const void *grad_out,
+                        void *out, float *last, void *grad_a, void *grad_b,
+                        int64_t B, int64_t T, int64_t D, int dtype, const lrscan_opts *opts);
+
+/*
  * Carried state and segment resets.  The state-carrying serial scans of
  * triton_training_scan.py (_samu_tiled_serial_forward and
  * _samu_tiled_serial_backward: initial state, per-token segment positions,

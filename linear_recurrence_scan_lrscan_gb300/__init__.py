@@ -7,7 +7,9 @@ its state-carrying form (initial state h0, segment resets, gradients of the
 final and initial states: ``scan_state``), the complex scan on re/im planes
 (``complex_scan``), the scan with decays generated in the kernel from
 per-token and per-lane parameters (``gated_scan``), and the pieces of a sequence split across devices
-(``lrscan_summary``, ``lrscan_compose_maps``, module ``tsplit``).
+(``lrscan_summary``, ``lrscan_compose_maps``, module ``tsplit``), and calls on
+host buffers that pipeline the copies with the kernels (``lrscan_fwd_host``,
+``lrscan_bwd_host``, ``lrscan_fwd_bwd_host``).
 
 The compute path is liblrscan.so (hand-written sm_103a CUDA kernels behind a C
 ABI, ``include/lrscan.h``); ``lrscan`` is its Python binding.  Importing this
@@ -28,9 +30,12 @@ from .lrscan import (  # noqa: F401
     lrscan_cfwd,
     lrscan_compose_maps,
     lrscan_bwd,
+    lrscan_bwd_host,
     lrscan_bwd_state,
     lrscan_fwd,
+    lrscan_fwd_bwd_host,
     lrscan_fwd_gated,
+    lrscan_fwd_host,
     lrscan_fwd_state,
     lrscan_gated_workspace_bytes,
     lrscan_num_variants,

@@ -224,8 +224,8 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
     // out tiles: staged in shared memory (two window buffers) and written by
     // one thread outside the lane scan with a bulk tensor store, one window
     // late; the tensor map clips rows past T and lanes past D
-    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));
-    const int obuf_elems = sm.W * DT;
+    const OutStage<1, St> ost = make_out_stage<1, St>(smem_raw, geom);
+    const CUtensorMap *const omaps[1] = {&tm_out};
     const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     float nu2[V];
 #pragma unroll
@@ -288,8 +288,7 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
             // every thread's rows of window k-1 are staged (fenced before the
             // barrier above); once this store has been issued, the one before
             // it must have finished reading the buffer window k is about to fill
-            tma_store_3d(&tm_out, smem_addr(obuf + ((k - 1) & 1) * obuf_elems), d0, (k - 1) * sm.W, brow);
-            bulk_commit();
+            ost.store(omaps, k - 1, d0, (k - 1) * sm.W, brow);
             bulk_wait_read<1>();
         }
         // lane threads push the carried state through the sub-chunk maps in order
@@ -307,7 +306,7 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
         bar_sync_or(1, NT, false);
 #pragma unroll
         for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
-        St *op = obuf + (k & 1) * obuf_elems + (s * L) * DT + lg * V;
+        St *op = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = 0; j < L; ++j) {
 #pragma unroll
@@ -326,11 +325,7 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
     // before the CTA's shared memory goes away
     const bool aborted = bar_sync_or(1, NT, replayed != sm.nwin);
     if (issuer) {
-        if (!aborted && replayed > 0) {
-            tma_store_3d(&tm_out, smem_addr(obuf + ((replayed - 1) & 1) * obuf_elems), d0, (replayed - 1) * sm.W,
-                         brow);
-            bulk_commit();
-        }
+        if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (replayed - 1) * sm.W, brow);
         bulk_wait<0>();
     }
 }

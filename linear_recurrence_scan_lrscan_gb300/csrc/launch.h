@@ -134,5 +134,7 @@ int selftest_wait_launch(DevStatus *status, uint64_t timeout_ns, cudaStream_t st
 
 // Records the detail text lrscan_last_error() returns and passes code through.
 int report_error(int code, const char *msg);
+// Reads and clears the device status word after `st` drains (lrscan_abi.cu).
+int take_device_status(cudaStream_t st);
 
 }  // namespace lrscan

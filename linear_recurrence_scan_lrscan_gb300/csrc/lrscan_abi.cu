@@ -1028,6 +1028,26 @@ int run_gbwd(const float *eta, const float *nu_log, const void *out, const void 
 // Lets other translation units of the library report why a call failed.
 int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
+// After `st` has drained: the first error a kernel recorded on the current
+// device since the last check (cleared), else LRSCAN_OK.
+int take_device_status(cudaStream_t st) {
+    DeviceCtx *ctx = nullptr;
+    int rc = device_ctx(&ctx);
+    if (rc) return rc;
+    DevStatus s{};
+    if (cudaMemcpyAsync(&s, ctx->status, sizeof s, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LRSCAN_ECUDA, "reading the device status failed");
+    }
+    if (s.code != 0) {
+        cudaMemsetAsync(ctx->status, 0, sizeof s, st);
+        cudaStreamSynchronize(st);
+        return fail(s.code, "a kernel reported error %d (wait site %d, block %u)", s.code, s.where, s.block);
+    }
+    return LRSCAN_OK;
+}
+
 }  // namespace lrscan
 
 using namespace lrscan;

@@ -313,8 +313,8 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float carry = 0.0f;  // window-to-window state of lane threadIdx.x (lane scan, threads < DT)
     bool failed = false;
     int stage = 0, use = 0;
-    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));
-    const int obuf_elems = sm.W * DT;
+    const OutStage<1, St> ost = make_out_stage<1, St>(smem_raw, geom);
+    const CUtensorMap *const omaps[1] = {&tm_out};
     // one thread outside the lane scan issues each window's store one window late
     const bool issuer = TS && static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     int replayed = 0;
@@ -460,8 +460,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             // every thread's rows of window k-1 are staged (fenced before the
             // barrier above); once this store has been issued, the one before
             // it must have finished reading the buffer window k is about to fill
-            tma_store_3d(&tm_out, smem_addr(obuf + ((k - 1) & 1) * obuf_elems), d0, (k - 1) * sm.W, brow);
-            bulk_commit();
+            ost.store(omaps, k - 1, d0, (k - 1) * sm.W, brow);
             bulk_wait_read<1>();
         }
         if constexpr (!C::PT) {
@@ -498,7 +497,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         if constexpr (TS) {
-            St *op = obuf + (k & 1) * obuf_elems + (s * L) * DT + lg * V;
+            St *op = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
             for (int j = 0; j < L; ++j) {
 #pragma unroll
@@ -546,11 +545,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // complete before the CTA's shared memory goes away
         const bool aborted = bar_sync_or(1, NT, replayed != sm.nwin);
         if (issuer) {
-            if (!aborted && replayed > 0) {
-                tma_store_3d(&tm_out, smem_addr(obuf + ((replayed - 1) & 1) * obuf_elems), d0,
-                             (replayed - 1) * sm.W, brow);
-                bulk_commit();
-            }
+            if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (replayed - 1) * sm.W, brow);
             bulk_wait<0>();
         }
     }
@@ -650,18 +645,12 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     float carry = 0.0f;  // window-to-window adjoint of lane threadIdx.x (lane scan, threads < DT)
     int stage = 0, use = 0;
     bool failed = false;
-    St *const obuf = reinterpret_cast<St *>(smem_raw + win_out_off(geom));  // [buffer][grad_a, grad_b][W][DT]
-    const int obuf_elems = sm.W * DT;
+    const OutStage<2, St> ost = make_out_stage<2, St>(smem_raw, geom);  // planes grad_a, grad_b
+    const CUtensorMap *const omaps[2] = {&tm_ga, &tm_gb};
+    // one thread outside the lane scan stores processed window kw (time rows
+    // from (nwin - 1 - kw) * W) one window late
     const bool issuer = TS && static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     int replayed = 0;
-    // one thread outside the lane scan stores processed window kw from buffer kw & 1
-    auto store_window = [&](int kw) {
-        const uint32_t src = smem_addr(obuf + (kw & 1) * 2 * obuf_elems);
-        const int y = (nwin - 1 - kw) * sm.W;
-        tma_store_3d(&tm_ga, src, d0, y, brow);
-        tma_store_3d(&tm_gb, src + obuf_elems * static_cast<uint32_t>(sizeof(St)), d0, y, brow);
-        bulk_commit();
-    };
     // EXT: bit j of r0bits / r1bits is a reset at row s*L + j / s*L + j + 1
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
@@ -843,7 +832,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             // rows of window k-1 are staged and fenced; after issuing its
             // stores, the ones before must have finished reading the buffer
             // window k is about to fill
-            store_window(k - 1);
+            ost.store(omaps, k - 1, d0, wbase + sm.W, brow);
             bulk_wait_read<1>();
         }
         if constexpr (!C::PT) {
@@ -877,8 +866,8 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
         }
         if constexpr (TS) {
-            St *sga = obuf + (k & 1) * 2 * obuf_elems + (s * L) * DT + lg * V;
-            St *sgb = sga + obuf_elems;
+            St *sga = ost.plane(k, 0) + (s * L) * DT + lg * V;
+            St *sgb = ost.plane(k, 1) + (s * L) * DT + lg * V;
             if (EXT && r0bits != 0) bwd_rows<C, true, true>(xa, xh, xg, g, n, lane_ok, sgb, sga, D, r0bits);
             else bwd_rows<C, false, true>(xa, xh, xg, g, n, lane_ok, sgb, sga, D, 0u);
             fence_proxy_async_smem();
@@ -907,7 +896,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // complete before the CTA's shared memory goes away
         const bool aborted = bar_sync_or(1, NT, replayed != nwin);
         if (issuer) {
-            if (!aborted && replayed > 0) store_window(replayed - 1);
+            if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (nwin - replayed) * sm.W, brow);
             bulk_wait<0>();
         }
     }

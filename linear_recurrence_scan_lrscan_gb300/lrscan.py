@@ -80,6 +80,11 @@ EXPORTS = {
     "lrscan_fwd_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_bwd_ex": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)],
                       ctypes.c_int),
+    "lrscan_fwd_host": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_bwd_host": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(Opts)],
+                        ctypes.c_int),
+    "lrscan_fwd_bwd_host": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(Opts)],
+                            ctypes.c_int),
     "lrscan_fwd_state": ([_P, _P, _P, _P, ctypes.POINTER(State), _I64, _I64, _I64, ctypes.c_int, _P,
                           ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_bwd_state": ([_P, _P, _P, _P, _P, ctypes.POINTER(State), _I64, _I64, _I64, ctypes.c_int, _P,
@@ -221,6 +226,86 @@ def lrscan_fwd(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None
                                  _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
     _check(rc, "lrscan_fwd")
     return out, last
+
+
+def _check_host(shape, dtype, **tensors):
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor; pin it for full copy speed")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if name == "last":
+            if t.dtype != torch.float32 or tuple(t.shape) != (shape[0], shape[2]):
+                raise ValueError("last must be fp32 [B, D]")
+            continue
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must be {dtype} {tuple(shape)}")
+
+
+def _host_like(t: torch.Tensor, shape=None, dtype=None) -> torch.Tensor:
+    return torch.empty(shape if shape is not None else t.shape, dtype=dtype or t.dtype, pin_memory=True)
+
+
+def lrscan_fwd_host(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+                    last: torch.Tensor | None = None, *, path=None, chunk_len=None, tile_variant=None):
+    """Forward scan of host (CPU) tensors through the device (lrscan_fwd_host):
+    copies in, kernels and copies out pipelined over batch-row chunks.  Outputs
+    not given are allocated in page-locked memory.  Returns (out, last)."""
+    if a.ndim != 3 or a.shape != b.shape:
+        raise ValueError("lrscan expects matching [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    out = _host_like(a) if out is None else out
+    last = _host_like(a, (B, D), torch.float32) if last is None else last
+    _check_host(a.shape, a.dtype, a=a, b=b, out=out, last=last)
+    o = _opts(path, chunk_len, tile_variant, None)
+    rc = lib().lrscan_fwd_host(a.data_ptr(), b.data_ptr(), out.data_ptr(), last.data_ptr(), B, T, D, code,
+                               ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_fwd_host")
+    return out, last
+
+
+def lrscan_bwd_host(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
+                    grad_a: torch.Tensor | None = None, grad_b: torch.Tensor | None = None, *,
+                    path=None, chunk_len=None, tile_variant=None):
+    """Backward scan of host tensors through the device (lrscan_bwd_host);
+    returns (grad_a, grad_b)."""
+    if a.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    grad_a = _host_like(a) if grad_a is None else grad_a
+    grad_b = _host_like(a) if grad_b is None else grad_b
+    _check_host(a.shape, a.dtype, a=a, out=out, grad_out=grad_out, grad_a=grad_a, grad_b=grad_b)
+    o = _opts(path, chunk_len, tile_variant, None)
+    rc = lib().lrscan_bwd_host(a.data_ptr(), out.data_ptr(), grad_out.data_ptr(), grad_a.data_ptr(),
+                               grad_b.data_ptr(), B, T, D, code, ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_bwd_host")
+    return grad_a, grad_b
+
+
+def lrscan_fwd_bwd_host(a: torch.Tensor, b: torch.Tensor, grad_out: torch.Tensor, out=None, last=None,
+                        grad_a=None, grad_b=None, *, path=None, chunk_len=None, tile_variant=None):
+    """Forward then backward of host tensors through the device
+    (lrscan_fwd_bwd_host; out stays on the device between them); returns
+    (out, last, grad_a, grad_b)."""
+    if a.ndim != 3 or a.shape != b.shape:
+        raise ValueError("lrscan expects matching [B, T, D] tensors")
+    code = _dtype_code(a)
+    B, T, D = a.shape
+    out = _host_like(a) if out is None else out
+    last = _host_like(a, (B, D), torch.float32) if last is None else last
+    grad_a = _host_like(a) if grad_a is None else grad_a
+    grad_b = _host_like(a) if grad_b is None else grad_b
+    _check_host(a.shape, a.dtype, a=a, b=b, grad_out=grad_out, out=out, last=last, grad_a=grad_a, grad_b=grad_b)
+    o = _opts(path, chunk_len, tile_variant, None)
+    rc = lib().lrscan_fwd_bwd_host(a.data_ptr(), b.data_ptr(), grad_out.data_ptr(), out.data_ptr(),
+                                   last.data_ptr(), grad_a.data_ptr(), grad_b.data_ptr(), B, T, D, code,
+                                   ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_fwd_bwd_host")
+    return out, last, grad_a, grad_b
 
 
 def lrscan_bwd(a: torch.Tensor, out: torch.Tensor, grad_out: torch.Tensor,
