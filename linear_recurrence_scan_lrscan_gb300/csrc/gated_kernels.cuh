@@ -293,16 +293,7 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
         }
         // lane threads push the carried state through the sub-chunk maps in order
         float *entry = sm.sEntry<C>();
-        if (static_cast<int>(threadIdx.x) < DT) {
-            float c = carry;
-#pragma unroll 4
-            for (int i = 0; i < S; ++i) {
-                const float2 m = pq[i * DT + threadIdx.x];
-                entry[i * DT + threadIdx.x] = c;
-                c = __fmaf_rn(m.x, c, m.y);
-            }
-            carry = c;
-        }
+        if (static_cast<int>(threadIdx.x) < DT) carry = lane_walk<false, DT>(pq, entry, S, threadIdx.x, carry);
         bar_sync_or(1, NT, false);
 #pragma unroll
         for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
@@ -590,16 +581,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
             bulk_wait_read<1>();
         }
         float *entry = sm.sEntry<C>();
-        if (static_cast<int>(threadIdx.x) < DT) {
-            float c = carry;
-#pragma unroll 4
-            for (int i = S - 1; i >= 0; --i) {
-                const float2 m = pq[i * DT + threadIdx.x];
-                entry[i * DT + threadIdx.x] = c;
-                c = __fmaf_rn(m.x, c, m.y);
-            }
-            carry = c;
-        }
+        if (static_cast<int>(threadIdx.x) < DT) carry = lane_walk<true, DT>(pq, entry, S, threadIdx.x, carry);
         bar_sync_or(1, NT, false);
 #pragma unroll
         for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];

@@ -245,6 +245,32 @@ __device__ __forceinline__ int lane_channel(int d0, int i) {
     return d0 + (i % C::G) * C::V + i / C::G;
 }
 
+// Lane scan of one window: lane thread i carries c through the S sub-chunk
+// maps pq[s * DT + i] in order (REVERSE: from S-1 down), recording each
+// sub-chunk's entry value first.  Maps are read four at a time ahead of their
+// fmas, so the loads do not queue behind the entry stores (same fmas, same
+// order as a one-map-at-a-time walk).
+template <bool REVERSE, int DT>
+__device__ __forceinline__ float lane_walk(const float2 *pq, float *entry, int S, int i, float c) {
+    for (int i0 = 0; i0 < S; i0 += 4) {
+        float2 m[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int s = REVERSE ? S - 1 - (i0 + j) : i0 + j;
+            m[j] = (i0 + j < S) ? pq[s * DT + i] : make_float2(1.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j < S) {
+                const int s = REVERSE ? S - 1 - (i0 + j) : i0 + j;
+                entry[s * DT + i] = c;
+                c = __fmaf_rn(m[j].x, c, m[j].y);
+            }
+        }
+    }
+    return c;
+}
+
 template <class C>
 __device__ __forceinline__ void win_init(const WinSmem &sm, int consumer_warps, int S) {
     constexpr int DT = C::DT;
@@ -468,16 +494,7 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             // the sub-chunk maps in order, recording every sub-chunk's entry
             // state (_real_chunk_prefix within the window; identity maps exact).
             float *entry = sm.sEntry<C>();
-            if (static_cast<int>(threadIdx.x) < DT) {
-                float c = carry;
-#pragma unroll 4
-                for (int i = 0; i < S; ++i) {
-                    const float2 m = pq[i * DT + threadIdx.x];
-                    entry[i * DT + threadIdx.x] = c;
-                    c = __fmaf_rn(m.x, c, m.y);
-                }
-                carry = c;
-            }
+            if (static_cast<int>(threadIdx.x) < DT) carry = lane_walk<false, DT>(pq, entry, S, threadIdx.x, carry);
             bar_sync_or(1, NT, false);
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
@@ -838,16 +855,7 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if constexpr (!C::PT) {
             // lane threads push the carried adjoint through sub-chunks S-1 .. 0
             float *entry = sm.sEntry<C>();
-            if (static_cast<int>(threadIdx.x) < DT) {
-                float c = carry;
-#pragma unroll 4
-                for (int i = S - 1; i >= 0; --i) {
-                    const float2 m = pq[i * DT + threadIdx.x];
-                    entry[i * DT + threadIdx.x] = c;
-                    c = __fmaf_rn(m.x, c, m.y);
-                }
-                carry = c;
-            }
+            if (static_cast<int>(threadIdx.x) < DT) carry = lane_walk<true, DT>(pq, entry, S, threadIdx.x, carry);
             bar_sync_or(1, NT, false);
 #pragma unroll
             for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
