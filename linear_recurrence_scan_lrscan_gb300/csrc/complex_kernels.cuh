@@ -377,14 +377,23 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
             bulk_wait_read<1>();
         }
         if (static_cast<int>(threadIdx.x) < DT) {
+            // maps read four at a time ahead of their complex fmas (the loads
+            // do not queue behind the entry stores)
             float hr = cr, hi = ci;
-#pragma unroll 4
-            for (int i = 0; i < S; ++i) {
-                const float4 m = pq[i * DT + threadIdx.x];
-                entry[i * DT + threadIdx.x] = make_float2(hr, hi);
-                float nr, ni;
-                cmul_add(m.x, m.y, hr, hi, m.z, m.w, nr, ni);
-                hr = nr; hi = ni;
+            for (int i0 = 0; i0 < S; i0 += 4) {
+                float4 m[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    m[j] = (i0 + j < S) ? pq[(i0 + j) * DT + threadIdx.x] : make_float4(1.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (i0 + j < S) {
+                        entry[(i0 + j) * DT + threadIdx.x] = make_float2(hr, hi);
+                        float nr, ni;
+                        cmul_add(m[j].x, m[j].y, hr, hi, m[j].z, m[j].w, nr, ni);
+                        hr = nr; hi = ni;
+                    }
+                }
             }
             cr = hr; ci = hi;
         }
