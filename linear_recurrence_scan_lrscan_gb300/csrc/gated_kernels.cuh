@@ -433,14 +433,18 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
     }
 }
 
+// Row-sum scratch of the windowed backward: per sub-chunk 8 rows x 17
+// floats, padded to 144 floats (144 mod 32 = 16).
+constexpr int kGatedQSub = 144;
+
 // Windowed backward (S sub-chunks of L = 8 rows, G = 16 threads per
 // sub-chunk row, lane-scan prefix).  Tiles: out one row early and grad_out.
 // Thread (s, g) builds the decays of rows rbase .. rbase + L (a_{t+1} for
 // its last row comes from the next sub-chunk's first row; 0 past T), takes
 // the adjoint entering its sub-chunk from the lane threads' walk over the S
 // reverse maps, replays, and sums q2 over its rows.  Row sums over the CTA's
-// lanes: the 16 threads of a sub-chunk exchange their 8 row sums (xor 8, then
-// a transpose-sum over 8 lanes): lane g < 8 ends with row g's sum.
+// lanes: each thread stores its 8 row sums in shared memory and thread g < 8
+// of the sub-chunk adds row g's 16 values.
 // part_eta: [gridDim.x][prow] (prow = rows B*T of the whole call, so the
 // eight rows of a sub-chunk land in 32 contiguous bytes); part_nu: [B*S][D]
 // (time sums per sub-chunk).
@@ -502,6 +506,10 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     const CUtensorMap *const omaps[1] = {&tm_gb};
     const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     int replayed = 0;
+    // per-row q2 sums of this thread's sub-chunk: [L][G + 1] floats (odd row
+    // pitch: the 8 summing threads read distinct banks), sub-chunks
+    // kGatedQSub floats apart (the two sub-chunks of a warp on opposite bank halves)
+    float *const qsub = reinterpret_cast<float *>(smem_raw + win_out_smem(geom)) + s * kGatedQSub;
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
         const int rbase = wbase + s * L;
@@ -520,7 +528,9 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
                 if (j < L) w[j][v] = __fmul_rn(a[j][v], l);
             }
         }
-        float xg[L][V];
+        // grad_out rows stay packed (storage words) until used: fewer registers
+        using Raw = typename RawOf<St, V>::T;
+        Raw xg[L];
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *th = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;  // h_{t-1}
         const St *tg = sm.tile<C>(stage, 1) + (s * L) * DT + lg * V;  // grad_out_t
@@ -529,7 +539,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
             for (int j = 0; j < L; ++j) {
                 float xh[V];
                 unpack_lanes<St, V>(th + j * DT, xh);
-                unpack_lanes<St, V>(tg + j * DT, xg[j]);
+                xg[j] = load_raw<St, V>(tg + j * DT);
                 // w = h_{t-1} a log2 a, so that q2 = g * w
 #pragma unroll
                 for (int v = 0; v < V; ++v) w[j][v] = __fmul_rn(xh[v], w[j][v]);
@@ -551,11 +561,9 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     if (j + 1 >= tl) a[j + 1][v] = (j < n) ? 0.0f : 1.0f;
-                    if (j >= n) {
-                        xg[j][v] = 0.0f;
-                        w[j][v] = 0.0f;
-                    }
+                    if (j >= n) w[j][v] = 0.0f;
                 }
+                if (j >= n) xg[j] = Raw{};  // zero bits: grad_out = +0
             }
         }
         float P[V], Q[V];
@@ -563,10 +571,12 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
 #pragma unroll
         for (int j = L - 1; j >= 0; --j) {
+            float gj[V];
+            widen_raw(xg[j], gj);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 P[v] = __fmul_rn(a[j + 1][v], P[v]);
-                Q[v] = __fmaf_rn(a[j + 1][v], Q[v], xg[j][v]);
+                Q[v] = __fmaf_rn(a[j + 1][v], Q[v], gj[v]);
             }
         }
         float2 *pq = sm.sPQ<C>(0);
@@ -585,38 +595,32 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         bar_sync_or(1, NT, false);
 #pragma unroll
         for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
-        float qrow[L];
         St *gbp = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = L - 1; j >= 0; --j) {
-            float qs = 0.0f;
+            float qs = 0.0f, gj[V];
+            widen_raw(xg[j], gj);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                g[v] = __fmaf_rn(a[j + 1][v], g[v], xg[j][v]);
+                g[v] = __fmaf_rn(a[j + 1][v], g[v], gj[v]);
                 const float q = __fmul_rn(g[v], w[j][v]);  // exactly 0 past T: g and w are 0 there
                 acc_nu[v] += q;
                 qs += q;
             }
-            qrow[j] = qs;
+            qsub[j * (G + 1) + lg] = qs;
             store_lanes<St, V>(gbp + j * DT, g);
         }
         fence_proxy_async_smem();
         replayed = k + 1;
-        // row sums over the sub-chunk's 16 threads (both half-warps do the same steps)
+        // row sums over the sub-chunk's 16 threads (its half-warp): thread
+        // lg < 8 adds row lg's 16 values in order
+        __syncwarp();
+        if (lg < L) {
+            float t = 0.0f;
 #pragma unroll
-        for (int j = 0; j < L; ++j) qrow[j] += __shfl_xor_sync(0xffffffffu, qrow[j], 8);
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1) {
-            const bool upper = (lane & w) != 0;
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-                const float send = upper ? qrow[i] : qrow[i + w];
-                const float keep = upper ? qrow[i + w] : qrow[i];
-                qrow[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-            }
+            for (int i = 0; i < G; ++i) t += qsub[lg * (G + 1) + i];
+            if (lg < n) part_eta[blockIdx.x * prow + row0 + rbase + lg] = t;
         }
-        const int r = lg & 7;  // this thread now holds row r's sum
-        if (lg < 8 && r < n) part_eta[blockIdx.x * prow + row0 + rbase + r] = qrow[0];
         ev = evn;
     }
     if (lane_ok) {
