@@ -65,6 +65,8 @@ const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s8_m5_n2", F(BF_32_2_8_M5, 8, 2), B(BB_32_2_8_M5, 8, 2)},
     {"win_bf16_d32_s4_m8", F(BF_32_2_8_M8, 4, 4), B(BB_32_2_8_M8, 4, 3)},
     {"win_bf16_d32_s4_m8_n2", F(BF_32_2_8_M8, 4, 2), B(BB_32_2_8_M8, 4, 2)},
+    {"win_bf16_d32_l4_s12_m5", F(BF_32_2_4_M5, 12, 2), B(BB_32_2_4_M5, 12, 2)},
+    {"win_bf16_d32_l4_s12_m5_n3", F(BF_32_2_4_M5, 12, 3), B(BB_32_2_4_M5, 12, 3)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},

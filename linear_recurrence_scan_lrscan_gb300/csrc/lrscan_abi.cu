@@ -239,15 +239,17 @@ const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny}, {kPathWi
 const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
                              {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
-// bf16 backward up to 5 CTAs per SM: the 16-sub-chunk tile.  The five-CTA
-// tile is about 1 % faster launched alone, but the 16-sub-chunk tile's last
-// partial wave overlaps the next forward, which makes the forward + backward
-// step 1.5 % faster.
-const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
+// bf16 backward up to 5 CTAs per SM: 12 sub-chunks of 4 rows, five CTAs per
+// SM (seven warps each, every CTA of a 640-tile launch resident): fastest
+// alone and in the forward + backward step (111.4 us against 114.0 us with
+// the 16-sub-chunk tile, whose partial last wave at least overlaps the next
+// forward, and 115.2 us with the five-CTA 8-row tile).
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_l4_s12_m5", 0.9, 5.0},
                              {kPathWindow, "win_bf16_d32_l16_s8", 0.9, kAny},
                              {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
-// With carried state / resets: the 16-sub-chunk tiles (the extra per-row
-// work of resets, grad_last and grad_h0 spills in the five-CTA tile).
+// With carried state / resets: the 16-sub-chunk tiles (80.7 us on the gated
+// workload against 81.3 us for the 12-sub-chunk tile and 93.5 us for the
+// five-CTA 8-row tile, whose reset masks and grad_last / grad_h0 work spill).
 const Pref kPrefBF16BwdState[] = {{kPathWindow, "win_bf16_d32_s16_n4", 0.9, 5.0},
                                   {kPathWindow, "win_bf16_d32_s16_n2", 0.9, kAny},
                                   {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
