@@ -106,6 +106,8 @@ WinDirCfg cwdir_cfg(int S, int nstage) {
 using CWF_BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 4, 288, 2, false>;
 using CWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 4, 288, 2, false>;
 using CWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 4, 288, 2, false>;
+// 4-row sub-chunks, five CTAs per SM: every CTA of a 640-tile launch resident
+using CWF_BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 4, 160, 5, false>;
 using CBF_64_1_32 = WinShape<bf16_t, 64, 1, 32, 4, 96, 1, true>;
 using CBB_64_1_32 = WinShape<bf16_t, 64, 1, 32, 6, 96, 1, true>;
 using CBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 4, 64, 1, true>;
@@ -129,6 +131,7 @@ const WinVariant kCplxBF16[] = {
     {"cseq_bf16_d64_v2_n4", F(CBF_64_2_32, 4), B(CBB_64_2_16, 5)},
     {"cwin_bf16_d32_s8", cwdir_cfg<CWF_BF_32_1_8>(8, 3), B(CBB_64_1_32, 3)},
     {"cwin_bf16_d32_s16_v2", cwdir_cfg<CWF_BF_32_2_8>(16, 2), B(CBB_64_1_32, 3)},
+    {"cwin_bf16_d32_l4_s8_m5", cwdir_cfg<CWF_BF_32_2_4_M5>(8, 2), B(CBB_64_1_32, 3)},
 };
 const WinVariant kCplxF32[] = {
     {"cseq_f32_d32_v1", F(CFF_32_1_32, 6), B(CFB_32_1_32, 4)},
