@@ -433,9 +433,13 @@ gwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constan
     }
 }
 
-// Row-sum scratch of the windowed backward: per sub-chunk 8 rows x 17
-// floats, padded to 144 floats (144 mod 32 = 16).
-constexpr int kGatedQSub = 144;
+// Row-sum scratch of the windowed backward: per sub-chunk L rows x (G + 1)
+// floats, padded so consecutive sub-chunks start 16 banks apart (the two
+// sub-chunks of a warp on opposite bank halves): 144 floats for 8 rows of 16.
+template <int L, int G>
+__host__ __device__ constexpr int gated_qsub_floats() {
+    return L * (G + 1) + (16 - (L * (G + 1)) % 32 + 32) % 32;
+}
 
 // Windowed backward (S sub-chunks of L = 8 rows, G = 16 threads per
 // sub-chunk row, lane-scan prefix).  Tiles: out one row early and grad_out.
@@ -455,8 +459,8 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
                  const float *__restrict__ nu_log, float *__restrict__ part_eta, long long prow,
                  float *__restrict__ part_nu, const __grid_constant__ WinGeom geom, DevStatus *status,
                  uint64_t timeout_ns) {
-    static_assert(!C::SEQ && !C::PT && C::NIN == 2 && C::L == 8 && C::G == 16,
-                  "windowed generated-decay backward: lane-scan shape, two planes, 8 rows x 16 threads");
+    static_assert(!C::SEQ && !C::PT && C::NIN == 2 && C::L <= 8 && C::G == 16,
+                  "windowed generated-decay backward: lane-scan shape, two planes, up to 8 rows x 16 threads");
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -508,8 +512,8 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     int replayed = 0;
     // per-row q2 sums of this thread's sub-chunk: [L][G + 1] floats (odd row
     // pitch: the 8 summing threads read distinct banks), sub-chunks
-    // kGatedQSub floats apart (the two sub-chunks of a warp on opposite bank halves)
-    float *const qsub = reinterpret_cast<float *>(smem_raw + win_out_smem(geom)) + s * kGatedQSub;
+    // gated_qsub_floats apart (the two sub-chunks of a warp on opposite bank halves)
+    float *const qsub = reinterpret_cast<float *>(smem_raw + win_out_smem(geom)) + s * gated_qsub_floats<L, G>();
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
         const int rbase = wbase + s * L;
@@ -613,7 +617,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         fence_proxy_async_smem();
         replayed = k + 1;
         // row sums over the sub-chunk's 16 threads (its half-warp): thread
-        // lg < 8 adds row lg's 16 values in order
+        // lg < L adds row lg's 16 values in order
         __syncwarp();
         if (lg < L) {
             float t = 0.0f;

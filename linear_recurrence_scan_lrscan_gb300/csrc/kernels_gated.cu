@@ -48,7 +48,8 @@ int launch_gwinw_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
     const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
     const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
-                                     win_out_smem(g) + cfg.s * kGatedQSub * 4, L.stream, *L.maps[0], *L.maps[1],
+                                     win_out_smem(g) + cfg.s * gated_qsub_floats<C::L, C::G>() * 4, L.stream,
+                                     *L.maps[0], *L.maps[1],
                                      *L.maps[2], L.eta, L.nu_log, L.part_eta,
                                      static_cast<long long>(L.part_rows), L.part_nu, g, L.status, L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
@@ -106,7 +107,7 @@ WinDirCfg gwdir_cfg(int S, int nstage) {
     d.threads = S * C::G + 32;
     // plus the staging buffers of out (forward) or grad_b (backward) and the
     // backward's row-sum scratch
-    d.smem = win_out_smem(g) + (FWD ? 0 : S * kGatedQSub * 4);
+    d.smem = win_out_smem(g) + (FWD ? 0 : S * gated_qsub_floats<C::L, C::G>() * 4);
     d.stage_bytes = g.stage_bytes;
     if constexpr (FWD) d.launch = &launch_gwinw_fwd<C>;
     else d.launch = &launch_gwinw_bwd<C>;
