@@ -437,6 +437,192 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     }
 }
 
+// conj(x) * h + b in the sequential backward's nested-fma order.
+__device__ __forceinline__ void cmulc_add(float xr, float xi, float hr, float hi, float br, float bi, float &nr,
+                                          float &ni) {
+    nr = __fmaf_rn(xr, hr, __fmaf_rn(xi, hi, br));
+    ni = __fmaf_rn(xr, hi, __fmaf_rn(-xi, hr, bi));
+}
+
+// ---------------------------------------------------------------------------
+// Windowed complex backward (S sub-chunks of L rows per window, processed in
+// reverse, lane-scan prefix): thread (s, g) reads its rows of a_{t+1},
+// out_{t-1} and grad_out, summarises its sub-chunk as the complex reverse map
+// g -> P g + Q (P the product of conj(a_{t+1}) over its rows), takes the
+// adjoint entering its last row from the lane threads' reverse walk over the
+// S maps, and replays g_t = conj(a_{t+1}) g_{t+1} + grad_out_t with
+// grad_a_t = g_t conj(out_{t-1}), grad_b_t = g_t.  out_{t-1} stays packed
+// until the replay.  The four gradient planes are staged in shared memory
+// (one buffer per plane) and written by bulk tensor stores, which clip rows
+// past T and lanes past D.  Rows past T are identity steps (a = 1,
+// grad_out = 0); a_T is the zero fill past the end.
+template <class C>
+__global__ void __launch_bounds__(C::MAXT, C::MINB)
+cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
+                 const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
+                 const __grid_constant__ CUtensorMap tm_gr, const __grid_constant__ CUtensorMap tm_gi,
+                 const __grid_constant__ CUtensorMap tm_gar, const __grid_constant__ CUtensorMap tm_gai,
+                 const __grid_constant__ CUtensorMap tm_gbr, const __grid_constant__ CUtensorMap tm_gbi,
+                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+    static_assert(!C::SEQ && !C::PT && C::NIN == 6, "windowed complex backward: lane-scan shape, six planes");
+    using St = typename C::St;
+    using Raw = typename RawOf<St, C::V>::T;
+    constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const WinSmem sm = WinSmem::make(smem_raw, geom);
+    const int S = geom.S;
+    const int NT = S * G;
+    win_init<C>(sm, NT / 32, S);
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, sm.abort_flag(), timeout_ns};
+    const int d0 = blockIdx.x * DT;
+    const int brow = blockIdx.y;
+    const int T = geom.T;
+    const int nwin = sm.nwin;
+
+    if (static_cast<int>(threadIdx.x) >= NT) {
+        if (static_cast<int>(threadIdx.x) == NT) {
+            const CUtensorMap *const maps[6] = {&tm_ar, &tm_ai, &tm_or, &tm_oi, &tm_gr, &tm_gi};
+            const int W = sm.W;
+            // planes 0, 1: a one step later; 2, 3: out one step earlier; 4, 5: grad_out
+            win_producer<C>(sm, maps, d0, brow,
+                            [W, nwin](int k, int i) { return (nwin - 1 - k) * W + (i < 2 ? 1 : (i < 4 ? -1 : 0)); },
+                            wc);
+        }
+        return;
+    }
+
+    const int s = threadIdx.x / G;
+    const int lg = threadIdx.x - s * G;
+    const int lane = threadIdx.x & 31;
+    float4 *pq = reinterpret_cast<float4 *>(smem_raw + geom.scan_off);                   // [S][DT]
+    float2 *entry = reinterpret_cast<float2 *>(smem_raw + geom.scan_off + S * DT * 16);  // [S][DT]
+    const OutStage<4, St, 1> ost = make_out_stage<4, St, 1>(smem_raw, geom);  // grad_ar, grad_ai, grad_br, grad_bi
+    const CUtensorMap *const omaps[4] = {&tm_gar, &tm_gai, &tm_gbr, &tm_gbi};
+    const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
+    int replayed = 0;
+    float cr = 0.0f, ci = 0.0f;  // window-to-window adjoint of lane threadIdx.x (threads < DT)
+    int stage = 0, use = 0;
+    const int off = (s * L) * DT + lg * V;
+    for (int k = 0; k < nwin; ++k) {
+        const int wbase = (nwin - 1 - k) * sm.W;
+        const int rbase = wbase + s * L;
+        const int n = min(max(T - rbase, 0), L);
+        float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
+        Raw pr[L], pi[L];
+        const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                unpack_lanes<St, V>(sm.tile<C>(stage, 0) + off + j * DT, xr[j]);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 1) + off + j * DT, xi[j]);
+                pr[j] = load_raw<St, V>(sm.tile<C>(stage, 2) + off + j * DT);
+                pi[j] = load_raw<St, V>(sm.tile<C>(stage, 3) + off + j * DT);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 4) + off + j * DT, yr[j]);
+                unpack_lanes<St, V>(sm.tile<C>(stage, 5) + off + j * DT, yi[j]);
+            }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        if (++stage == sm.nstage) { stage = 0; ++use; }
+        if (n < L) {
+            // rows past T: identity steps (a = 1, grad_out = 0)
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    xr[j][v] = j < n ? xr[j][v] : 1.0f;
+                    xi[j][v] = j < n ? xi[j][v] : 0.0f;
+                    yr[j][v] = j < n ? yr[j][v] : 0.0f;
+                    yi[j][v] = j < n ? yi[j][v] : 0.0f;
+                }
+            }
+        }
+        // reverse sub-chunk map: g at the first row = P g_after + Q
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float Pr = 1.0f, Pi = 0.0f, Qr = 0.0f, Qi = 0.0f;
+#pragma unroll
+            for (int j = L - 1; j >= 0; --j) {
+                float nPr, nPi, nQr, nQi;
+                cmulc_add(xr[j][v], xi[j][v], Pr, Pi, 0.0f, 0.0f, nPr, nPi);
+                cmulc_add(xr[j][v], xi[j][v], Qr, Qi, yr[j][v], yi[j][v], nQr, nQi);
+                Pr = nPr; Pi = nPi; Qr = nQr; Qi = nQi;
+            }
+            pq[s * DT + v * G + lg] = make_float4(Pr, Pi, Qr, Qi);
+        }
+        if (bar_sync_or(1, NT, !ok)) break;
+        if (issuer && k > 0) {
+            // window k-1's rows are staged and fenced: store them, and let the
+            // stores finish reading before this window's replay refills the buffers
+            ost.store(omaps, k - 1, d0, wbase + sm.W, brow);
+            bulk_wait_read<0>();
+        }
+        if (static_cast<int>(threadIdx.x) < DT) {
+            // lane threads walk the carried adjoint through sub-chunks S-1 .. 0,
+            // maps read four at a time ahead of their complex fmas
+            float hr = cr, hi = ci;
+            for (int i0 = 0; i0 < S; i0 += 4) {
+                float4 m[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    m[j] = (i0 + j < S) ? pq[(S - 1 - i0 - j) * DT + threadIdx.x] : make_float4(1.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (i0 + j < S) {
+                        entry[(S - 1 - i0 - j) * DT + threadIdx.x] = make_float2(hr, hi);
+                        float nr, ni;
+                        cmul_add(m[j].x, m[j].y, hr, hi, m[j].z, m[j].w, nr, ni);
+                        hr = nr; hi = ni;
+                    }
+                }
+            }
+            cr = hr; ci = hi;
+        }
+        bar_sync_or(1, NT, false);
+        float gr[V], gi[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const float2 e = entry[s * DT + v * G + lg];
+            gr[v] = e.x;
+            gi[v] = e.y;
+        }
+        St *const sar = ost.plane(k, 0) + off;
+        St *const sai = ost.plane(k, 1) + off;
+        St *const sbr = ost.plane(k, 2) + off;
+        St *const sbi = ost.plane(k, 3) + off;
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+            float hr[V], hi[V], far_[V], fai[V];
+            widen_raw(pr[j], hr);
+            widen_raw(pi[j], hi);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                float nr, ni;
+                cmulc_add(xr[j][v], xi[j][v], gr[v], gi[v], yr[j][v], yi[j][v], nr, ni);
+                gr[v] = nr;
+                gi[v] = ni;
+                far_[v] = __fmaf_rn(gr[v], hr[v], __fmul_rn(gi[v], hi[v]));
+                fai[v] = __fmaf_rn(gi[v], hr[v], -__fmul_rn(gr[v], hi[v]));
+            }
+            store_lanes<St, V>(sar + j * DT, far_);
+            store_lanes<St, V>(sai + j * DT, fai);
+            store_lanes<St, V>(sbr + j * DT, gr);
+            store_lanes<St, V>(sbi + j * DT, gi);
+        }
+        fence_proxy_async_smem();
+        replayed = k + 1;
+    }
+    // the last processed window's tiles (not after an abort), then every store
+    // complete before the CTA's shared memory goes away
+    const bool aborted = bar_sync_or(1, NT, replayed != nwin);
+    if (issuer) {
+        if (!aborted && replayed > 0) ost.store(omaps, replayed - 1, d0, (nwin - replayed) * sm.W, brow);
+        bulk_wait<0>();
+    }
+}
+
 // Plain kernels: one lane per thread, plain loads, any alignment (same order
 // of operations, bit-identical to the tiled ones).
 template <typename St>

@@ -81,10 +81,27 @@ WinDirCfg cdir_cfg(int nstage) {
     return d;
 }
 
-// Windowed complex forward tile: S sub-chunks of L rows, lane scan.
 template <class C>
+int launch_cwinw_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = cwinw_bwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const WinGeom g = make_cwin_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
+                                     win_out_smem(g, 4, 1), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
+                                     *L.maps[4], *L.maps[5], *L.maps[6], *L.maps[7], *L.maps[8], *L.maps[9], g,
+                                     L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+// Windowed complex tiles: S sub-chunks of L rows, lane scan.  Forward: a, b
+// in, out_r / out_i staged in two buffers; backward: a, out, grad_out in,
+// the four gradient planes staged in one buffer each.
+template <class C, bool FWD = true>
 WinDirCfg cwdir_cfg(int S, int nstage) {
-    static_assert(!C::SEQ && !C::PT && C::NIN == 4, "windowed complex forward shape");
+    static_assert(!C::SEQ && !C::PT && C::NIN == (FWD ? 4 : 6), "windowed complex shape");
     if (S > C::SMAX) std::abort();  // table error
     const WinGeom g = make_cwin_geom<C>(S, nstage, 1, 1);
     WinDirCfg d{};
@@ -96,9 +113,10 @@ WinDirCfg cwdir_cfg(int S, int nstage) {
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
-    d.smem = win_out_smem(g, 2);  // plus the out_r / out_i staging buffers
+    d.smem = FWD ? win_out_smem(g, 2) : win_out_smem(g, 4, 1);  // plus the output staging
     d.stage_bytes = g.stage_bytes;
-    d.launch = &launch_cwinw_fwd<C>;
+    if constexpr (FWD) d.launch = &launch_cwinw_fwd<C>;
+    else d.launch = &launch_cwinw_bwd<C>;
     return d;
 }
 
@@ -108,6 +126,7 @@ using CWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 4, 288, 2, false>;
 using CWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 4, 288, 2, false>;
 // 4-row sub-chunks, five CTAs per SM: every CTA of a 640-tile launch resident
 using CWF_BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 4, 160, 5, false>;
+using CWB_BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 6, 160, 5, false>;
 using CBF_64_1_32 = WinShape<bf16_t, 64, 1, 32, 4, 96, 1, true>;
 using CBB_64_1_32 = WinShape<bf16_t, 64, 1, 32, 6, 96, 1, true>;
 using CBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 4, 64, 1, true>;
@@ -131,7 +150,7 @@ const WinVariant kCplxBF16[] = {
     {"cseq_bf16_d64_v2_n4", F(CBF_64_2_32, 4), B(CBB_64_2_16, 5)},
     {"cwin_bf16_d32_s8", cwdir_cfg<CWF_BF_32_1_8>(8, 3), B(CBB_64_1_32, 3)},
     {"cwin_bf16_d32_s16_v2", cwdir_cfg<CWF_BF_32_2_8>(16, 2), B(CBB_64_1_32, 3)},
-    {"cwin_bf16_d32_l4_s8_m5", cwdir_cfg<CWF_BF_32_2_4_M5>(8, 2), B(CBB_64_1_32, 3)},
+    {"cwin_bf16_d32_l4_s8_m5", cwdir_cfg<CWF_BF_32_2_4_M5>(8, 2), (cwdir_cfg<CWB_BF_32_2_4_M5, false>(8, 2))},
 };
 const WinVariant kCplxF32[] = {
     {"cseq_f32_d32_v1", F(CFF_32_1_32, 6), B(CFB_32_1_32, 4)},

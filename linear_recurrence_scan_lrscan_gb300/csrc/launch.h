@@ -39,7 +39,7 @@ enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3
 // Arguments of one time-tiled launch (forward: maps a,b / out0=out;
 // backward: maps a,out,grad_out / out0=grad_a, out1=grad_b).
 struct WinLaunch {
-    const CUtensorMap *maps[6];   // input planes in kernel order (complex scan: up to 6)
+    const CUtensorMap *maps[10];  // planes in kernel order (complex backward: 6 in, 4 out)
     void *out0;
     void *out1;
     void *out2, *out3;            // complex backward: grad_br, grad_bi

@@ -703,8 +703,13 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         // measured best complex bf16 forward: the windowed tiles (time split
         // inside the CTA); 4-row sub-chunks with five CTAs per SM when all the
         // CTAs fit one wave (84.5 us on the complex workload against 93.1 us)
+    } else if (dtype == LRSCAN_BF16 && dir == 1 &&
+               (vi = find_one_wave(tab, n, "cwin_bf16_d32_l4_s8_m5", dir, B, D, g)) >= 0) {
+        // measured best complex bf16 backward: the windowed tile with 4-row
+        // sub-chunks, five CTAs per SM, when all its CTAs fit one wave (152.3 us
+        // on the complex workload against 157.4 us for the sequential tile)
     } else if (dtype == LRSCAN_BF16 && (vi = find_one_wave(tab, n, "cseq_bf16_d64_v1_n4", dir, B, D, g)) >= 0) {
-        // measured best complex bf16 backward whenever all its CTAs fit one wave
+        // else the sequential tile whenever all its CTAs fit one wave
     } else if (!pick_from_table(tab, n, dir, B, D, g, &vi)) {
         long long most = -1;
         for (int i = 0; i < n; ++i) {
@@ -807,12 +812,13 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
     for (int64_t b0 = 0; b0 < B; b0 += 65535) {
         const int64_t nb = std::min<int64_t>(65535, B - b0);
         const size_t off = static_cast<size_t>(b0) * T * D * es;
-        CUtensorMap m[6];
-        for (int i = 0; i < 6; ++i)
-            if (encode_map(&m[i], static_cast<const char *>(in[i]) + off, dtype, nb, T, D, v.dt, v.w))
-                return LRSCAN_EINVAL;
+        CUtensorMap m[10];  // 6 inputs, then the 4 gradients (windowed tiles store them with bulk copies)
+        for (int i = 0; i < 10; ++i) {
+            const char *base = i < 6 ? static_cast<const char *>(in[i]) : static_cast<const char *>(outp[i - 6]);
+            if (encode_map(&m[i], base + off, dtype, nb, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+        }
         WinLaunch L{};
-        for (int i = 0; i < 6; ++i) L.maps[i] = &m[i];
+        for (int i = 0; i < 10; ++i) L.maps[i] = &m[i];
         L.out0 = static_cast<char *>(outp[0]) + off;
         L.out1 = static_cast<char *>(outp[1]) + off;
         L.out2 = static_cast<char *>(outp[2]) + off;

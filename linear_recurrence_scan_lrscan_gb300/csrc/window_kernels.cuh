@@ -113,8 +113,8 @@ __host__ __device__ inline WinGeom make_win_geom(int S, int nstage, int T, int D
 // tensor stores: two buffers of one window (W rows x DT lanes, storage type)
 // after the rest of the layout.
 __host__ __device__ inline int win_out_off(const WinGeom &g) { return (g.smem_bytes + 127) & ~127; }
-__host__ __device__ inline int win_out_smem(const WinGeom &g, int planes = 1) {
-    return win_out_off(g) + 2 * planes * g.tile_bytes;
+__host__ __device__ inline int win_out_smem(const WinGeom &g, int planes = 1, int buffers = 2) {
+    return win_out_off(g) + buffers * planes * g.tile_bytes;
 }
 // Window tiles that stage their outputs this way: the lane-scan tiles (out
 // forward; grad_a and grad_b backward).
@@ -125,11 +125,13 @@ template <class C> __host__ __device__ constexpr bool win_staged() { return !C::
 // writes its rows into plane(k, p) and fences them for the async proxy; after
 // the next window's first barrier one thread stores them (store), so the
 // buffers alternate and each store overlaps a window of compute.
-template <int NP, class St>
+// NB = 1 keeps one buffer per plane: the thread that stores a window must
+// then wait for its reads (bulk_wait_read<0>) before the next replay writes.
+template <int NP, class St, int NB = 2>
 struct OutStage {
     St *buf;
     int elems;  // W * DT
-    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((kw & 1) * NP + p) * elems; }
+    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((NB == 1 ? 0 : kw & 1) * NP + p) * elems; }
     // bulk tensor stores of processed window kw's planes at (x, y, z), one group
     __device__ __forceinline__ void store(const CUtensorMap *const (&maps)[NP], int kw, int x, int y, int z) const {
 #pragma unroll
@@ -137,10 +139,10 @@ struct OutStage {
         bulk_commit();
     }
 };
-template <int NP, class St>
-__device__ __forceinline__ OutStage<NP, St> make_out_stage(unsigned char *smem, const WinGeom &g) {
-    return OutStage<NP, St>{reinterpret_cast<St *>(smem + win_out_off(g)),
-                            g.tile_bytes / static_cast<int>(sizeof(St))};
+template <int NP, class St, int NB = 2>
+__device__ __forceinline__ OutStage<NP, St, NB> make_out_stage(unsigned char *smem, const WinGeom &g) {
+    return OutStage<NP, St, NB>{reinterpret_cast<St *>(smem + win_out_off(g)),
+                                g.tile_bytes / static_cast<int>(sizeof(St))};
 }
 
 // Shared-memory layout of one CTA, with the launch geometry copied into
