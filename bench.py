@@ -593,10 +593,11 @@ def run_gated(iters: int, dev, peak) -> dict:
 
 
 def run_long_t(dev, peak) -> dict:
-    """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32, chunk 64 (65,536
-    chunk maps per lane, 64 lanes): the chunked path with the flat prefix (one
-    warp per lane walks all maps) and with the grouped prefix.  Inputs are
-    drawn on the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
+    """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32: the chunked path
+    with chunk 64 (65,536 chunk maps per lane, 64 lanes) with the flat prefix
+    (one warp per lane walks all maps) and with the grouped prefix, and the
+    automatic plan (grouped prefix over 128-step chunks).  Inputs are drawn on
+    the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
@@ -618,6 +619,12 @@ def run_long_t(dev, peak) -> dict:
                      "fwd_frac": 3 * E * 4 / (fms * 1e-3) / 1e9 / peak,
                      "bwd_frac": 5 * E * 4 / (bms * 1e-3) / 1e9 / peak,
                      "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+    fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last), 10, stream)
+    bms = time_launches(lambda i: L.lrscan_bwd(a, out, g, ga, gb), 10, stream)
+    res["auto_plan"] = {"fwd_ms": fms, "bwd_ms": bms,
+                        "fwd_frac": 3 * E * 4 / (fms * 1e-3) / 1e9 / peak,
+                        "bwd_frac": 5 * E * 4 / (bms * 1e-3) / 1e9 / peak,
+                        "elements/s": 2 * E / ((fms + bms) * 1e-3)}
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the long-sequence chunked path")
     res["auto"] = L.lrscan_plan(B, T, D, "f32", "fwd")["name"]

@@ -91,6 +91,8 @@ int chunk_dispatch(const ChunkLaunch &L, bool fwd) {
     LRSCAN_CHUNK_CASE(16)
     LRSCAN_CHUNK_CASE(32)
     LRSCAN_CHUNK_CASE(64)
+    LRSCAN_CHUNK_CASE(128)
+    LRSCAN_CHUNK_CASE(256)
 #undef LRSCAN_CHUNK_CASE
     return -2;
 }

@@ -135,9 +135,14 @@ def test_bf16_forward_takes_the_one_wave_window_tile(lib):
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
-    # 16,384 chunks per lane and only 64 lanes: the grouped prefix (5 kernels)
+    # 8,192 chunks of 128 steps per lane and only 64 lanes: the grouped prefix
+    # (5 kernels) with the longer chunks
     assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
-    assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
+    assert p["rows_per_window"] == 128 and p["name"].startswith("chunk128")
+    assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 128)
+    # an explicit chunk length is kept
+    p64 = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", chunk_len=64)
+    assert p64["rows_per_window"] == 64 and p64["name"].endswith("_grouped")
     flat = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", path="chunk", tile_variant=1)
     assert flat["kernels"] == 3 and flat["workspace_bytes"] == 2 * 16384 * 64 * 4
     # few chunks per lane: the flat prefix

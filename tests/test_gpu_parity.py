@@ -114,7 +114,7 @@ def test_tiled_paths_every_variant(dt, shape_i, path):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128, 256])
 def test_chunked_path(dt, chunk):
     for i, (B, T, D) in enumerate(SMALL_SHAPES[dt]):
         inp = random_inputs(B, T, D, dt, seed=200 + i, a_lo=0.6, a_hi=1.0)
