@@ -645,9 +645,9 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 // sum_c part_eta[c][r] (K = partial columns, N = rows B*T) and
 // grad_nu_log[d] = ln 2 * sum_b part_nu[b][d] (K = partial rows, N = D).
 // Blocks [0, blocks0) take the first, the rest the second.  A block covers 64
-// columns with 4 threads each; thread y sums the K range [K y / 4, K (y+1) / 4)
-// in order and thread y = 0 adds the four in order (deterministic).
-constexpr int kFinishCols = 64, kFinishSplit = 4;
+// columns with 8 threads each; thread y sums the K range [K y / 8, K (y+1) / 8)
+// in order and thread y = 0 adds the eight in order (deterministic).
+constexpr int kFinishCols = 64, kFinishSplit = 8;
 
 __global__ void __launch_bounds__(kFinishCols * kFinishSplit)
 gated_finish(const float *__restrict__ p0, int K0, long long N0, float *__restrict__ o0,
@@ -659,6 +659,7 @@ gated_finish(const float *__restrict__ p0, int K0, long long N0, float *__restri
     float *o = first ? o0 : o1;
     const long long n = static_cast<long long>(first ? blockIdx.x : blockIdx.x - blocks0) * kFinishCols + threadIdx.x;
     const int y = threadIdx.y;
+    pdl_wait();  // the partials come from the kernel before this one in the stream
     float sum = 0.0f;
     if (n < N) {
         const int k1 = static_cast<int>(static_cast<long long>(K) * (y + 1) / kFinishSplit);

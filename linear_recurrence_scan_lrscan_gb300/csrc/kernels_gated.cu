@@ -169,9 +169,11 @@ int gated_finish_launch(const float *part_eta, int ncol, long long rows, float *
     const unsigned b0 = static_cast<unsigned>((rows + kFinishCols - 1) / kFinishCols);
     const unsigned b1 = static_cast<unsigned>((D + kFinishCols - 1) / kFinishCols);
     if (b0 + b1 == 0) return 0;
-    gated_finish<<<b0 + b1, dim3(kFinishCols, kFinishSplit), 0, stream>>>(part_eta, ncol, rows, grad_eta, part_nu,
-                                                                         nu_rows, D, grad_nu_log, b0);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    // programmatic dependent launch: the blocks start while the backward
+    // drains and wait (griddepcontrol.wait) before reading its partials
+    const cudaError_t e = launch_pdl(gated_finish, dim3(b0 + b1), dim3(kFinishCols, kFinishSplit), 0, stream,
+                                     part_eta, ncol, rows, grad_eta, part_nu, nu_rows, D, grad_nu_log, b0);
+    return e == cudaSuccess ? 0 : -1;
 }
 
 int gplain_launch(const WinLaunch &L, int dtype, bool fwd) {
