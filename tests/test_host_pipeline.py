@@ -139,3 +139,16 @@ def test_host_full_size_workload_matches_device(_cuda):
     for name, h, d in (("out", out_h, out_d), ("grad_a", ga_h, ga_d), ("grad_b", gb_h, gb_d)):
         assert torch.equal(h.view(torch.int16), d.cpu().view(torch.int16)), name
     assert torch.equal(last_h, last_d.cpu())
+
+
+@gpu
+def test_host_call_reports_a_chunk_error_and_stays_usable(_cuda):
+    """A chunk whose device call fails (the tiled path forced on rows that are
+    not 16-byte multiples) stops the call with the error; the next call runs."""
+    inp = random_inputs(4, 40, 37, "bf16", seed=930)
+    a, b, g = (_pinned(inp[k]) for k in ("a", "b", "grad_out"))
+    with pytest.raises(L.LrscanError):
+        L.lrscan_fwd_bwd_host(a, b, g, path="seq")
+    out, last = L.lrscan_fwd_host(a, b)
+    ref_out, _ = oracle.default().fwd(to_np(a), to_np(b), "bf16")
+    assert_close(to_np(out), ref_out, "bf16", "out after a failed call", reassociated=True)
