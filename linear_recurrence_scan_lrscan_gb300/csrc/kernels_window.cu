@@ -81,6 +81,7 @@ const WinVariant kWinF32[] = {
     {"win_f32_d16_s16_pt", F(PF_16_1_8, 16, 4), B(PFB_16_1_8, 16, 4)},
     {"win_f32_d64_s8", F(FF_64_2_8, 8, 4), B(FB_64_2_8, 8, 3)},
     {"win_f32_d32_s8_pt", F(PF_32_1_8, 8, 8), B(PFB_32_1_8, 8, 6)},
+    {"win_f32_d32_s31", F(FF_32_1_8_X, 31, 2), B(FB_32_1_8, 16, 3)},
 };
 
 #undef F

@@ -234,7 +234,10 @@ struct Pref {
     double max_ctas_per_sm;
 };
 constexpr double kAny = 1e30;
-const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
+// fp32 forward with few lane tiles: one 32-warp CTA per tile (31 sub-chunks
+// of 8 rows): 333.6 us on the long fp32 workload against 372.5 us for 16
+// sub-chunks.
+const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s31", 0.45, kAny}};
 const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny}, {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
 const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},

@@ -48,6 +48,8 @@ using BB_32_2_8_M8 = WinShape<bf16_t, 32, 2, 8, 3, 96, 8, false>;
 // consumer warps on the same 640-tile launch
 using BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 2, 224, 5, false>;
 using BB_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 3, 224, 5, false>;
+// fp32, one CTA of 32 warps per lane tile (few lane tiles)
+using FF_32_1_8_X = WinShape<float, 32, 1, 8, 2, 1024, 1, false>;
 // per-thread-prefix shapes (parallel fold, short critical path)
 using PF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, true>;
 using PFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, true>;
@@ -60,7 +62,7 @@ using WBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false>;
 #define LRSCAN_WIN_FWD_SHAPES(X)                                                                   \
     X(SBF_64_2_32) X(SBF_128_2_32) X(SBF_128_4_32) X(SBF_32_1_32) X(SBF_64_1_32) X(SFF_32_1_32) \
     X(SFF_64_2_16) X(SFF_64_1_32) X(SFF_128_4_8) X(BF_64_2_8) X(BF_32_2_8) X(FF_16_1_8)          \
-    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8) X(BF_32_2_4_M5)
+    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8) X(BF_32_2_4_M5) X(FF_32_1_8_X)
 
 #define LRSCAN_WIN_BWD_SHAPES(X)                                                                   \
     X(SBB_64_2_32) X(SBB_32_1_32) X(SBB_64_1_32) X(SBB_128_2_32) X(SBB_128_4_16) X(SFB_32_1_32) \

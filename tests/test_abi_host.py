@@ -88,7 +88,7 @@ def test_workspace_bytes(lib):
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
     2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l4_s12_m5"),
-    3: ("win_f32_d32_s16", "win_f32_d32_s16"),
+    3: ("win_f32_d32_s31", "win_f32_d32_s16"),
     4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l16_s8"),
     5: ("seq_f32_d32", "win_f32_d64_s8"),
 }
