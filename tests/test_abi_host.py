@@ -193,3 +193,28 @@ def test_state_entry_points_validate_before_any_launch(lib):
         assert lib.lrscan_fwd_state(p, p, p, None, ctypes.byref(ok), B, T, D, 1, None, None) == L.LRSCAN_OK
         assert lib.lrscan_bwd_state(p, p, p, p, p, ctypes.byref(ok), B, T, D, 1, None, None) == L.LRSCAN_OK
     assert lib.lrscan_fwd_state(p, p, p, None, None, 1, 8, 8, 5, None, None) == L.LRSCAN_EDTYPE
+
+
+def test_missing_library_fails_loudly_with_no_fallback(tmp_path):
+    """Without liblrscan.so every entry point raises LrscanUnavailable: there
+    is no CPU path to fall back to."""
+    import subprocess
+    import sys
+    code = (
+        "import torch\n"
+        "from linear_recurrence_scan_lrscan_gb300 import lrscan as L\n"
+        "a = torch.zeros(1, 4, 8)\n"
+        "for call in (lambda: L.lrscan_plan(1, 4, 8, 'f32'),\n"
+        "             lambda: L.lrscan_fwd_host(a, a, out=torch.empty_like(a), last=torch.empty(1, 8))):\n"
+        "    try:\n"
+        "        call()\n"
+        "    except L.LrscanUnavailable:\n"
+        "        continue\n"
+        "    raise SystemExit('a call ran without the library')\n"
+        "try:\n"
+        "    L.lrscan_fwd(a, a)  # host tensors are refused: nothing computes on the CPU\n"
+        "except (L.LrscanUnavailable, ValueError):\n"
+        "    print('ok')\n")
+    env = dict(os.environ, LRSCAN_LIBRARY=str(tmp_path / "absent.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), (r.stdout, r.stderr)
