@@ -59,7 +59,7 @@ extern "C" {
 #define LRSCAN_EINVAL       (-1)  /* NULL required pointer, negative size, byte size overflow, bad option */
 #define LRSCAN_EDTYPE       (-2)  /* dtype is not LRSCAN_F32 or LRSCAN_BF16 */
 #define LRSCAN_ECUDA        (-3)  /* a CUDA runtime call or kernel launch failed */
-#define LRSCAN_ENOMEM       (-4)  /* the chunked path's workspace could not be allocated / is too small */
+#define LRSCAN_ENOMEM       (-4)  /* a workspace or staging buffer could not be allocated, or a caller workspace is too small */
 #define LRSCAN_ETIMEOUT     (-5)  /* a bounded device wait gave up (reported by lrscan_sync_check) */
 #define LRSCAN_ENODEVICE    (-6)  /* no usable sm_103 device is current */
 
