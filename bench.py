@@ -596,7 +596,8 @@ def run_long_t(dev, peak) -> dict:
     """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32: the chunked path
     with chunk 64 (65,536 chunk maps per lane, 64 lanes) with the flat prefix
     (one warp per lane walks all maps) and with the grouped prefix, and the
-    automatic plan (grouped prefix over 128-step chunks).  Inputs are drawn on
+    automatic plan (grouped prefix over 512-step chunks forward, 128-step
+    chunks backward).  Inputs are drawn on
     the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 

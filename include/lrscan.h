@@ -76,7 +76,7 @@ extern "C" {
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */
-    int chunk_len;          /* chunked path: 16, 32, 64, 128 or 256; 0 = 64, or 128 for long sequences on few lanes (grouped prefix) */
+    int chunk_len;          /* chunked path: 16, 32, 64, 128, 256 or 512; 0 = 64, or for long sequences on few lanes (grouped prefix) 512 forward and 128 backward */
     void *workspace;        /* chunked path: optional caller-owned device workspace ... */
     size_t workspace_bytes; /* ... of at least lrscan_workspace_bytes() bytes; NULL = library-owned */
     int tile_variant;       /* >= 1 forces one kernel tile variant of the path (lrscan_plan lists them); 0 = auto.

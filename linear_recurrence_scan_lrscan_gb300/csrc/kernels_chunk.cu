@@ -93,6 +93,7 @@ int chunk_dispatch(const ChunkLaunch &L, bool fwd) {
     LRSCAN_CHUNK_CASE(64)
     LRSCAN_CHUNK_CASE(128)
     LRSCAN_CHUNK_CASE(256)
+    LRSCAN_CHUNK_CASE(512)
 #undef LRSCAN_CHUNK_CASE
     return -2;
 }

@@ -134,12 +134,16 @@ def test_bf16_forward_takes_the_one_wave_window_tile(lib):
 
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
-    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
-    # 8,192 chunks of 128 steps per lane and only 64 lanes: the grouped prefix
-    # (5 kernels) with the longer chunks
-    assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
-    assert p["rows_per_window"] == 128 and p["name"].startswith("chunk128")
-    assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 128)
+    # 2^20 steps and only 64 lanes: the grouped prefix (5 kernels) with the
+    # longer chunks, 512 steps forward (2,048 chunks per lane) and 128 backward
+    for direction, c in (("fwd", 512), ("bwd", 128)):
+        p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction)
+        assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
+        assert p["rows_per_window"] == c and p["name"].startswith(f"chunk{c}")
+        assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, c)
+    # too short for 2,048 chunks of 512: the forward falls back to 256
+    p = L.lrscan_plan(1, (1 << 19) + 1000, 64, "f32", "fwd")
+    assert p["rows_per_window"] == 256 and p["name"].endswith("_grouped"), p
     # an explicit chunk length is kept
     p64 = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", chunk_len=64)
     assert p64["rows_per_window"] == 64 and p64["name"].endswith("_grouped")
@@ -176,6 +180,8 @@ def test_forced_paths_and_variants(lib):
     assert p["path"] == "chunk" and p["rows_per_window"] == 32
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(8, 1000, 512, "f32", "bwd", path="chunk", chunk_len=48)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(8, 1000, 512, "f32", "bwd", path="chunk", chunk_len=1024)
 
 
 def test_state_entry_points_validate_before_any_launch(lib):

@@ -114,7 +114,7 @@ def test_tiled_paths_every_variant(dt, shape_i, path):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("chunk", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128, 256, 512])
 def test_chunked_path(dt, chunk):
     for i, (B, T, D) in enumerate(SMALL_SHAPES[dt]):
         inp = random_inputs(B, T, D, dt, seed=200 + i, a_lo=0.6, a_hi=1.0)
@@ -366,7 +366,7 @@ def test_autograd_wrapper_matches_direct_calls():
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("shape,chunk", [((2, 40000, 8), 16), ((1, 70001, 16), 32)])
+@pytest.mark.parametrize("shape,chunk", [((2, 40000, 8), 16), ((1, 70001, 16), 32), ((1, 300001, 8), 512)])
 def test_chunk_grouped_prefix(dt, shape, chunk):
     """The grouped chunk prefix (group maps, their prefix, per-group rescan;
     several groups and a ragged last group) against the oracle, forced and
@@ -377,4 +377,5 @@ def test_chunk_grouped_prefix(dt, shape, chunk):
     assert plan["name"].endswith("_grouped") and plan["kernels"] == 5
     check_case(inp, path="chunk", chunk_len=chunk, tile_variant=1)
     auto = L.lrscan_plan(B, T, D, dt, "fwd", path="chunk", chunk_len=chunk)
-    assert auto["name"].endswith("_grouped")
+    # automatic from 2,048 chunks per lane (586 chunks of 512 stay flat)
+    assert auto["name"].endswith("_grouped") == (-(-T // chunk) >= 2048)
