@@ -54,6 +54,52 @@ __device__ __forceinline__ float rate2(const float *nu_log, int d) {
     return __fmul_rn(exp_approx(__ldg(nu_log + d)), kLog2e);
 }
 
+// Two fp32 lanes per instruction: the packed .f32x2 forms of PTX mul, fma
+// and add (Blackwell).  Each half is rounded as the scalar instruction
+// rounds it (round to nearest, subnormals kept), so the results are the
+// scalar code's bit for bit.
+__device__ __forceinline__ void mul_x2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add_x2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma_x2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                       float c1) {
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Element-wise d = a * b, d = a + b and d = a * b + c over V lanes, two per
+// packed instruction (an odd last lane takes the scalar form).  d may be one
+// of the operands.
+template <int V>
+__device__ __forceinline__ void vmul(float (&d)[V], const float (&a)[V], const float (&b)[V]) {
+#pragma unroll
+    for (int v = 0; v + 1 < V; v += 2) mul_x2(d[v], d[v + 1], a[v], a[v + 1], b[v], b[v + 1]);
+    if (V & 1) d[V - 1] = __fmul_rn(a[V - 1], b[V - 1]);
+}
+template <int V>
+__device__ __forceinline__ void vadd(float (&d)[V], const float (&a)[V], const float (&b)[V]) {
+#pragma unroll
+    for (int v = 0; v + 1 < V; v += 2) add_x2(d[v], d[v + 1], a[v], a[v + 1], b[v], b[v + 1]);
+    if (V & 1) d[V - 1] = __fadd_rn(a[V - 1], b[V - 1]);
+}
+template <int V>
+__device__ __forceinline__ void vfma(float (&d)[V], const float (&a)[V], const float (&b)[V], const float (&c)[V]) {
+#pragma unroll
+    for (int v = 0; v + 1 < V; v += 2) fma_x2(d[v], d[v + 1], a[v], a[v + 1], b[v], b[v + 1], c[v], c[v + 1]);
+    if (V & 1) d[V - 1] = __fmaf_rn(a[V - 1], b[V - 1], c[V - 1]);
+}
+
 // After the call, lane l holds sum over the warp's lanes of v[l] (v has 32
 // entries per lane): halves of the remaining entries are exchanged with the
 // partner lane at distance 16, 8, 4, 2, 1.
@@ -227,9 +273,9 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
     const OutStage<1, St> ost = make_out_stage<1, St>(smem_raw, geom);
     const CUtensorMap *const omaps[1] = {&tm_out};
     const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
-    float nu2[V];
+    float nnu2[V];  // -nu2: the decay exponent is (-nu2) * E
 #pragma unroll
-    for (int v = 0; v < V; ++v) nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
+    for (int v = 0; v < V; ++v) nnu2[v] = lane_ok ? -rate2(nu_log, d + v) : -0.0f;
     float ev = eta_at(eta_row, s * L + myrow, T);  // eta of row myrow of the current window's sub-chunk
     float h[V];
     int replayed = 0;
@@ -246,8 +292,12 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
 #pragma unroll
         for (int j = 0; j < L; ++j) {
             const float e = __shfl_sync(0xffffffffu, e_mine, gbase + j);
+            float ej[V];
 #pragma unroll
-            for (int v = 0; v < V; ++v) xa[j][v] = ex2_approx(-__fmul_rn(nu2[v], e));
+            for (int v = 0; v < V; ++v) ej[v] = e;
+            vmul(xa[j], nnu2, ej);
+#pragma unroll
+            for (int v = 0; v < V; ++v) xa[j][v] = ex2_approx(xa[j][v]);
         }
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         const St *tb = sm.tile<C>(stage, 0) + (s * L) * DT + lg * V;
@@ -274,11 +324,8 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
         }
 #pragma unroll
         for (int j = 0; j < L; ++j) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                P[v] = __fmul_rn(xa[j][v], P[v]);
-                Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
-            }
+            vmul(P, xa[j], P);
+            vfma(Q, xa[j], Q, xb[j]);
         }
         float2 *pq = sm.sPQ<C>(0);
 #pragma unroll
@@ -300,8 +347,7 @@ gwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
         St *op = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = 0; j < L; ++j) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+            vfma(h, xa[j], h, xb[j]);
             store_lanes<St, V>(op + j * DT, h);
         }
         fence_proxy_async_smem();
@@ -495,10 +541,10 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
     const bool lane_ok = d < D;
     const size_t row0 = static_cast<size_t>(brow) * T;
     const float *eta_row = eta + row0;
-    float nu2[V], acc_nu[V], g[V];
+    float nnu2[V], acc_nu[V], g[V];  // nnu2 = -nu2: the decay exponent is (-nu2) * E
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        nu2[v] = lane_ok ? rate2(nu_log, d + v) : 0.0f;
+        nnu2[v] = lane_ok ? -rate2(nu_log, d + v) : -0.0f;
         acc_nu[v] = 0.0f;
     }
     float ev = eta_at(eta_row, (nwin - 1) * sm.W + s * L + myrow, T);  // current window
@@ -525,12 +571,13 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
         for (int j = 0; j <= L; ++j) {
             const float e = __shfl_sync(0xffffffffu, e_mine, gbase + j);
+            float l[V];
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float l = -__fmul_rn(nu2[v], e);
-                a[j][v] = ex2_approx(l);
-                if (j < L) w[j][v] = __fmul_rn(a[j][v], l);
-            }
+            for (int v = 0; v < V; ++v) l[v] = e;
+            vmul(l, nnu2, l);
+#pragma unroll
+            for (int v = 0; v < V; ++v) a[j][v] = ex2_approx(l[v]);
+            if (j < L) vmul(w[j], a[j], l);
         }
         // grad_out rows stay packed (storage words) until used: fewer registers
         using Raw = typename RawOf<St, V>::T;
@@ -545,8 +592,7 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
                 unpack_lanes<St, V>(th + j * DT, xh);
                 xg[j] = load_raw<St, V>(tg + j * DT);
                 // w = h_{t-1} a log2 a, so that q2 = g * w
-#pragma unroll
-                for (int v = 0; v < V; ++v) w[j][v] = __fmul_rn(xh[v], w[j][v]);
+                vmul(w[j], xh, w[j]);
             }
         }
         __syncwarp();
@@ -577,11 +623,8 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         for (int j = L - 1; j >= 0; --j) {
             float gj[V];
             widen_raw(xg[j], gj);
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                P[v] = __fmul_rn(a[j + 1][v], P[v]);
-                Q[v] = __fmaf_rn(a[j + 1][v], Q[v], gj[v]);
-            }
+            vmul(P, a[j + 1], P);
+            vfma(Q, a[j + 1], Q, gj);
         }
         float2 *pq = sm.sPQ<C>(0);
 #pragma unroll
@@ -602,15 +645,13 @@ gwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
         St *gbp = ost.plane(k, 0) + (s * L) * DT + lg * V;
 #pragma unroll
         for (int j = L - 1; j >= 0; --j) {
-            float qs = 0.0f, gj[V];
+            float qs = 0.0f, gj[V], q[V];
             widen_raw(xg[j], gj);
+            vfma(g, a[j + 1], g, gj);
+            vmul(q, g, w[j]);  // exactly 0 past T: g and w are 0 there
+            vadd(acc_nu, acc_nu, q);
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                g[v] = __fmaf_rn(a[j + 1][v], g[v], gj[v]);
-                const float q = __fmul_rn(g[v], w[j][v]);  // exactly 0 past T: g and w are 0 there
-                acc_nu[v] += q;
-                qs += q;
-            }
+            for (int v = 0; v < V; ++v) qs += q[v];
             qsub[j * (G + 1) + lg] = qs;
             store_lanes<St, V>(gbp + j * DT, g);
         }
