@@ -119,7 +119,22 @@ int lrscan_bwd(const void *a, const void *out, const void *grad_out,
                int64_t B, int64_t T, int64_t D, int dtype);
 
 /* As above with an explicit stream (cudaStream_t; NULL = the thread's
- * current stream) and options (NULL = defaults). */
+ * current stream) and options (NULL = defaults).
+ *
+ * CUDA graphs: the device calls (lrscan_fwd / _bwd and their _ex, _state,
+ * complex and generated-decay forms, lrscan_summary, lrscan_compose_maps)
+ * enqueue kernels and stream-ordered copies only, so they can be captured
+ * into a graph and replayed, provided that
+ *   - one call has run on the device before the capture begins (it looks up
+ *     the device's properties and the tensor-map encoder), and
+ *   - the library-owned workspace of the stream (chunked path, generated-
+ *     decay backward) already has the size the captured call needs: a call
+ *     of that size has run on that stream outside capture, or opts->workspace
+ *     is passed.  A captured call that would have to grow it returns
+ *     LRSCAN_ENOMEM before it enqueues anything (the capture stays valid).
+ * The captured kernels read and write the pointers given at capture time.
+ * The host-buffer calls, lrscan_sync_check and lrscan_selftest_wait_timeout
+ * synchronize and cannot be captured. */
 int lrscan_fwd_ex(const void *a, const void *b, void *out, float *last,
                   int64_t B, int64_t T, int64_t D, int dtype,
                   void *stream, const lrscan_opts *opts);

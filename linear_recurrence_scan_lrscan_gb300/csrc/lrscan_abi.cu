@@ -466,6 +466,19 @@ int workspace_for(DeviceCtx *ctx, cudaStream_t st, size_t need, const lrscan_opt
     std::lock_guard<std::mutex> lk(g_mu);
     auto &slot = ctx->workspace[st];
     if (slot.second < need) {
+        // growing synchronizes the stream and allocates: neither may happen
+        // while the stream is being captured into a graph (nothing has been
+        // enqueued yet, so the capture stays valid)
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(LRSCAN_ECUDA, "cudaStreamIsCapturing failed");
+        }
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(LRSCAN_ENOMEM,
+                        "the library-owned workspace must grow to %zu bytes, which cannot happen during stream "
+                        "capture: make one call of this size before capturing, or pass opts->workspace",
+                        need);
         if (slot.first) {
             cudaStreamSynchronize(st);  // the old buffer may still be in use by this stream
             cudaFree(slot.first);
