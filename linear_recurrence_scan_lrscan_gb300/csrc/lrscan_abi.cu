@@ -149,8 +149,12 @@ Occ occupancy(const WinVariant &var, int dir, int64_t B, int64_t D, const Geomet
     const int smem = v.smem;
     const int nst = v.nstage;
     const int stage = v.stage_bytes;
-    Occ o;
+    Occ o{};
     o.ctas = B * ((D + v.dt - 1) / v.dt);
+    // the kernels' named barriers and mbarrier arrival counts take whole
+    // warps: a table entry whose threads are not (S * lanes-per-row + the
+    // producer warp) in whole warps never launches
+    if (v.threads < 64 || v.threads % 32 != 0) return o;
     int r_smem = smem > g.smem_optin ? 0 : g.smem_per_sm / (smem + 1024);
     int r_thr = g.max_threads_per_sm / v.threads;
     o.resident = std::min(std::min(r_smem, r_thr), 32);
@@ -917,6 +921,7 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     }
     if (vi < 0) return fail(LRSCAN_EINVAL, "no generated-decay tile variant fits this device");
     const Occ o = occupancy(tab[vi], dir, B, D, g);
+    if (o.resident == 0) return fail(LRSCAN_EINVAL, "tile variant %s does not fit on an SM", tab[vi].name);
     ch->vidx = vi;
     ch->var = &tab[vi];
     ch->ctas = o.ctas;

@@ -224,3 +224,40 @@ def test_missing_library_fails_loudly_with_no_fallback(tmp_path):
     env = dict(os.environ, LRSCAN_LIBRARY=str(tmp_path / "absent.so"))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), (r.stdout, r.stderr)
+
+
+def test_every_tile_variant_is_whole_warps(lib):
+    """The tiled kernels' named barriers and mbarrier arrival counts take whole
+    warps, so every variant of every table (real, carried-state, complex,
+    generated-decay; both directions) must plan with a thread count that is a
+    multiple of 32; the planner refuses an entry that is not."""
+    B, T, D = 8, 1000, 512
+    seen = 0
+    for dt in ("f32", "bf16"):
+        for direction in ("fwd", "bwd"):
+            planners = [("real", lambda v, path: L.lrscan_plan(B, T, D, dt, direction, path=path, tile_variant=v)),
+                        ("state", lambda v, path: L.lrscan_plan(B, T, D, dt, direction, path=path, tile_variant=v,
+                                                                state=True)),
+                        ("complex", lambda v, path: L.lrscan_plan_complex(B, T, D, dt, direction, path=path,
+                                                                          tile_variant=v))]
+            for what, plan in planners:
+                for path in ("seq", "window"):
+                    v = 1
+                    while True:
+                        try:
+                            p = plan(v, path)
+                        except L.LrscanError:
+                            break
+                        assert p["threads_per_cta"] % 32 == 0, (what, dt, direction, path, p)
+                        seen += 1
+                        v += 1
+            v = 1
+            while True:
+                try:
+                    p = L.lrscan_plan_gated(B, T, D, dt, direction, path="seq", tile_variant=v)
+                except L.LrscanError:
+                    break
+                assert p["threads_per_cta"] % 32 == 0, ("gated", dt, direction, p)
+                seen += 1
+                v += 1
+    assert seen > 40
