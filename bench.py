@@ -484,7 +484,8 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
     for f in sets:   # leave every set with the plain forward's output
         L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
     torch.cuda.synchronize()
-    return {"complex": run_complex(iters, dev, peak), "generated_decay": run_gated(iters, dev, peak),
+    return {"complex": run_complex(iters, dev, peak), "complex_long_t": run_complex_long_t(dev, peak),
+            "generated_decay": run_gated(iters, dev, peak),
             "long_t": run_long_t(dev, peak), "state": {
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
@@ -541,6 +542,45 @@ def run_complex(iters: int, dev, peak) -> dict:
             "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
                     "algorithmic_bytes": bb, "kernel": pb["name"]},
             "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+
+
+def run_complex_long_t(dev, peak) -> dict:
+    """The complex scan with few lanes and a long sequence: B=1 T=2^20 D=64
+    fp32 re/im planes, |a|~U(0.9,0.999) with phases ~U(-pi,pi), b and grad_out
+    ~N(0,1), drawn on the device from a seeded generator.  The automatic plan
+    takes the chunked path (complex chunk maps, grouped prefix); algorithmic
+    bytes are 6 (forward) and 10 (backward) elements per (t, d)."""
+    import math
+
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    B, T, D = 1, 1 << 20, 64
+    gen = torch.Generator(device=dev).manual_seed(20298)
+    rho = torch.empty(B, T, D, device=dev).uniform_(0.9, 0.999, generator=gen)
+    th = torch.empty(B, T, D, device=dev).uniform_(-math.pi, math.pi, generator=gen)
+    ar, ai = rho * torch.cos(th), rho * torch.sin(th)
+    del rho, th
+    br, bi, gr, gi = (torch.empty(B, T, D, device=dev).normal_(generator=gen) for _ in range(4))
+    outs = L.lrscan_cfwd(ar, ai, br, bi)
+    grads = L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi)
+    stream = torch.cuda.current_stream()
+    fms = time_launches(lambda i: L.lrscan_cfwd(ar, ai, br, bi, out_r=outs[0], out_i=outs[1], last_r=outs[2],
+                                                last_i=outs[3]), 10, stream)
+    bms = time_launches(lambda i: L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi, grads=grads), 10, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the long complex scan")
+    E = B * T * D
+    fb, bb = 6 * E * 4 + 8 * B * D, 10 * E * 4
+    res = {"workload": f"B={B} T={T} D={D} fp32 complex (few lanes, long sequence)",
+           "fwd": {"ms": fms, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                   "kernel": L.lrscan_plan_complex(B, T, D, "f32", "fwd")["name"]},
+           "bwd": {"ms": bms, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                   "kernel": L.lrscan_plan_complex(B, T, D, "f32", "bwd")["name"]},
+           "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+    del ar, ai, br, bi, gr, gi, outs, grads
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_gated(iters: int, dev, peak) -> dict:

@@ -243,12 +243,21 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
  * (a' = a_{t+1}, p = h_{t-1}); both paths use this order and agree bit for bit.
  * All planes are caller-owned device [B, T, D] tensors of one storage dtype;
  * paths: tiled (LRSCAN_PATH_SEQ or LRSCAN_PATH_WINDOW: one table of
- * sequential and windowed tiles, 16-byte aligned rows of every plane) or
- * LRSCAN_PATH_PLAIN (any alignment); auto picks a tiled variant when it can.
- * The sequential tiles keep the order above and agree with it bit for bit;
- * the windowed forward tiles (time split inside the CTA through complex
- * affine maps) agree to rounding.  Moves 6 elements per (t, d) forward and 10
- * backward.  Other rules as lrscan_fwd_ex.
+ * sequential and windowed tiles, 16-byte aligned rows of every plane),
+ * LRSCAN_PATH_CHUNK (three phases over time chunks of opts->chunk_len steps,
+ * 16 ... 512, default 64 fp32 / 128 bf16: complex chunk maps, their prefix -- flat, or grouped
+ * when a lane has many chunks; tile_variant 1 / 2 forces flat / grouped --
+ * and the replay; any alignment) or LRSCAN_PATH_PLAIN (any alignment).  Auto
+ * takes the chunked path when the lanes fill fewer than 0.45 lane tiles of
+ * 32 per SM (aligned rows; else 32 warps per SM) and T >= 16 chunks, else a
+ * tiled variant when the rows are aligned, else the plain kernels.
+ * The sequential tiles and the plain kernels keep the order above and agree
+ * with it bit for bit; the windowed tiles and the chunked path (complex
+ * affine maps) agree to rounding.  The chunked path needs
+ * lrscan_plan_complex(...).workspace_bytes of device scratch: library-owned
+ * per (device, stream), or opts->workspace.  Moves 6 elements per (t, d)
+ * forward and 10 backward (the chunked path re-reads its inputs: 10 and 16).
+ * Other rules as lrscan_fwd_ex.
  */
 int lrscan_cfwd(const void *ar, const void *ai, const void *br, const void *bi,
                 void *out_r, void *out_i, float *last_r, float *last_i,

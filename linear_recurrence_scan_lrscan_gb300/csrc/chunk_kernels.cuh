@@ -59,6 +59,34 @@ struct ChunkGeom {
     int Ncb;   // chunk blocks per row: ceil(Nc / cpb)
 };
 
+// Chunk geometry: 128-thread CTAs; when a chunk row needs at most 64 threads
+// (D / V <= 64), one CTA takes 128 / lt chunks so that no thread idles.
+inline ChunkGeom make_chunk_geom(int64_t T, int64_t D, int C, int V) {
+    ChunkGeom g;
+    g.T = static_cast<int>(T);
+    g.D = static_cast<int>(D);
+    g.Nc = static_cast<int>((T + C - 1) / C);
+    const int row_threads = static_cast<int>((D + V - 1) / V);
+    if (row_threads <= 64) {
+        int lt = 1;
+        while (lt < row_threads) lt <<= 1;
+        g.lt = lt;
+        g.cpb = 128 / lt;
+        g.nlb = 1;
+    } else {
+        g.lt = 128;
+        g.cpb = 1;
+        g.nlb = (row_threads + 127) / 128;
+    }
+    g.Ncb = (g.Nc + g.cpb - 1) / g.cpb;
+    return g;
+}
+
+// CTAs of a chunk-parallel launch over B rows.
+inline unsigned chunk_blocks(const ChunkGeom &g, int64_t B) {
+    return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Ncb * B);
+}
+
 // Linear CTA index -> (row, chunk block, lane block); consecutive CTAs take
 // neighbouring lanes of the same chunk block.  Within the CTA, thread t works
 // on chunk (block * cpb + t / lt) and lanes ((lane block * lt + t % lt) * V ...).

@@ -9,32 +9,9 @@ namespace lrscan {
 
 namespace {
 
-inline unsigned blocks_for(const ChunkGeom &g, int64_t B) {
-    return static_cast<unsigned>(static_cast<int64_t>(g.nlb) * g.Ncb * B);
-}
+inline unsigned blocks_for(const ChunkGeom &g, int64_t B) { return chunk_blocks(g, B); }
 
-// Chunk geometry: 128-thread CTAs; when a chunk row needs at most 64 threads
-// (D / V <= 64), one CTA takes 128 / lt chunks so that no thread idles.
-inline ChunkGeom chunk_geom(const ChunkLaunch &L, int C, int V) {
-    ChunkGeom g;
-    g.T = static_cast<int>(L.T);
-    g.D = static_cast<int>(L.D);
-    g.Nc = static_cast<int>((L.T + C - 1) / C);
-    const int row_threads = static_cast<int>((L.D + V - 1) / V);
-    if (row_threads <= 64) {
-        int lt = 1;
-        while (lt < row_threads) lt <<= 1;
-        g.lt = lt;
-        g.cpb = 128 / lt;
-        g.nlb = 1;
-    } else {
-        g.lt = 128;
-        g.cpb = 1;
-        g.nlb = (row_threads + 127) / 128;
-    }
-    g.Ncb = (g.Nc + g.cpb - 1) / g.cpb;
-    return g;
-}
+inline ChunkGeom chunk_geom(const ChunkLaunch &L, int C, int V) { return make_chunk_geom(L.T, L.D, C, V); }
 
 // Phase 2: the flat warp-per-lane prefix, or (when the launch carries group
 // scratch) the grouped form: group maps, their prefix, the per-group rescan.

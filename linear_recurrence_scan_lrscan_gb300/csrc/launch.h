@@ -123,6 +123,24 @@ int plain_bwd_launch(const ChunkLaunch &L, int dtype);
 int cplain_fwd_launch(const ChunkLaunch &L, const void *ai, const void *bi, void *out_i, float *last_i, int dtype);
 int cplain_bwd_launch(const void *const in[6], void *const out[4], int64_t B, int64_t T, int64_t D, int dtype,
                       cudaStream_t stream);
+// Complex chunked path.  Forward: in = {ar, ai, br, bi}, out = {out_r,
+// out_i}, last_r / last_i (may be null); backward: in = {ar, ai, out_r,
+// out_i, go_r, go_i}, out = {grad_ar, grad_ai, grad_br, grad_bi}.  maps: P re,
+// P im, Q re, Q im [B, Nc, D] each; gmaps: the grouped prefix's group maps
+// [B, ceil(Nc / kGroupChunks), D] each, or all null (flat prefix).
+struct CChunkLaunch {
+    const void *in[6];
+    void *out[4];
+    float *last_r, *last_i;
+    float *maps[4];
+    float *gmaps[4];
+    int64_t B, T, D;
+    int chunk;
+    int vec;  // lanes per thread: 2 when D is even and every plane 2-lane aligned, else 1
+    cudaStream_t stream;
+};
+int cchunk_fwd_launch(const CChunkLaunch &L, int dtype);
+int cchunk_bwd_launch(const CChunkLaunch &L, int dtype);
 // Whole-sequence affine summary per lane (dir 0: forward, 1: backward);
 // in0 = a, in1 = b or grad_out, P and Q = [B, D] outputs.
 int summary_launch(const ChunkLaunch &L, int dtype, int dir);

@@ -445,7 +445,7 @@ def lrscan_compose_maps(maps: torch.Tensor, rank: int, init: torch.Tensor | None
 
 
 def lrscan_cfwd(ar, ai, br, bi, *, out_r=None, out_i=None, last_r=None, last_i=None, want_last: bool = True,
-                path=None, tile_variant=None, stream=None):
+                path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
     """Complex forward scan on re/im planes [B, T, D]; returns
     (out_r, out_i, last_r, last_i) (last planes fp32 [B, D], or None)."""
     if ar.ndim != 3 or any(t.shape != ar.shape for t in (ai, br, bi)):
@@ -462,7 +462,7 @@ def lrscan_cfwd(ar, ai, br, bi, *, out_r=None, out_i=None, last_r=None, last_i=N
         if t is not None:
             _check_state_tensor(name, t, (B, D), torch.float32, ar.device)
     with torch.cuda.device(ar.device):
-        o = _opts(path, None, tile_variant, None)
+        o = _opts(path, chunk_len, tile_variant, workspace)
         rc = lib().lrscan_cfwd(ar.data_ptr(), ai.data_ptr(), br.data_ptr(), bi.data_ptr(), out_r.data_ptr(),
                                out_i.data_ptr(), last_r.data_ptr() if last_r is not None else None,
                                last_i.data_ptr() if last_i is not None else None, B, T, D, code,
@@ -471,8 +471,8 @@ def lrscan_cfwd(ar, ai, br, bi, *, out_r=None, out_i=None, last_r=None, last_i=N
     return out_r, out_i, last_r, last_i
 
 
-def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, path=None, tile_variant=None,
-                stream=None):
+def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, path=None, chunk_len=None,
+                tile_variant=None, workspace=None, stream=None):
     """Complex reverse scan; returns (grad_ar, grad_ai, grad_br, grad_bi) for the
     loss sum(grad_out_r * out_r + grad_out_i * out_i)."""
     if ar.ndim != 3:
@@ -483,7 +483,7 @@ def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, pat
     _check_tensors(ar.shape, ar.dtype, ar.device, ar=ar, ai=ai, out_r=out_r, out_i=out_i, grad_out_r=grad_out_r,
                    grad_out_i=grad_out_i, grad_ar=grads[0], grad_ai=grads[1], grad_br=grads[2], grad_bi=grads[3])
     with torch.cuda.device(ar.device):
-        o = _opts(path, None, tile_variant, None)
+        o = _opts(path, chunk_len, tile_variant, workspace)
         rc = lib().lrscan_cbwd(ar.data_ptr(), ai.data_ptr(), out_r.data_ptr(), out_i.data_ptr(),
                                grad_out_r.data_ptr(), grad_out_i.data_ptr(), *[g.data_ptr() for g in grads],
                                B, T, D, code, _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
@@ -492,12 +492,12 @@ def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, pat
 
 
 def lrscan_plan_complex(B: int, T: int, D: int, dtype="f32", direction: str = "fwd", aligned: bool = True,
-                        path=None, tile_variant=None) -> dict:
+                        path=None, tile_variant=None, chunk_len=None) -> dict:
     code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
     if code is None:
         raise ValueError(f"unsupported dtype {dtype}")
     info = PlanInfo()
-    o = _opts(path, None, tile_variant, None)
+    o = _opts(path, chunk_len, tile_variant, None)
     rc = lib().lrscan_plan_complex(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
                                    ctypes.byref(o) if o is not None else None, ctypes.byref(info))
     _check(rc, "lrscan_plan_complex")

@@ -42,7 +42,7 @@ def check_complex(inp, dt, **kw):
     assert L.lrscan_sync_check() == 0
     plan = L.lrscan_plan_complex(B, T, D, dt, "fwd", **kw)
     tag = plan["name"]
-    ex = plan["path"] != "window"  # windowed tiles re-associate through complex maps
+    ex = plan["path"] in ("seq", "plain")  # windowed tiles and chunks re-associate through complex maps
     for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
         assert_close(to_np(g), r, dt, f"{name}[{tag}]", exact=ex, reassociated=not ex)
     for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
@@ -53,7 +53,7 @@ def check_complex(inp, dt, **kw):
     ggot = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"], **kw)
     assert L.lrscan_sync_check() == 0
     planb = L.lrscan_plan_complex(B, T, D, dt, "bwd", **kw)
-    exb = planb["path"] != "window"
+    exb = planb["path"] in ("seq", "plain")
     for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot, gref):
         assert_close(to_np(g), r, dt, f"{name}[{planb['name']}]", exact=exb, reassociated=not exb)
     return plan, planb
@@ -94,7 +94,45 @@ def test_complex_empty_and_invalid():
     assert not lr.any() and not li.any()
     x = torch.zeros((1, 4, 16), device="cuda")
     with pytest.raises(L.LrscanError):
-        L.lrscan_cfwd(x, x, x, x, path="chunk")
+        L.lrscan_cfwd(x, x, x, x, path="chunk", chunk_len=48)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_cfwd(x, x, x, x, path="chunk", tile_variant=3)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [16, 64, 512])
+def test_complex_chunked_path(dt, chunk):
+    """Complex chunk maps, their prefix and the replay on the small shapes
+    (several chunks per lane, ragged tails, T shorter than a chunk)."""
+    for i, (B, T, D) in enumerate(SHAPES):
+        inp = make_complex_inputs(B, T, D, dt, seed=540 + i)
+        plan, planb = check_complex(inp, dt, path="chunk", chunk_len=chunk)
+        assert plan["path"] == "chunk" and planb["path"] == "chunk" and plan["name"] in (f"cchunk{chunk}_v1", f"cchunk{chunk}_v2")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_chunked_grouped_prefix_and_auto(dt):
+    """Few lanes, long sequence (2,500 chunks of 16 per lane: five groups of
+    512 maps, the last one ragged): the grouped prefix forced and as the
+    automatic choice, the flat prefix forced, and the automatic plan (64-step
+    chunks, flat) against the oracle."""
+    B, T, D = 1, 40000, 8
+    inp = make_complex_inputs(B, T, D, dt, seed=550)
+    plan, planb = check_complex(inp, dt, path="chunk", chunk_len=16, tile_variant=2)
+    assert plan["name"] == "cchunk16_v2_grouped" and planb["kernels"] == 5
+    assert L.lrscan_plan_complex(B, T, D, dt, "fwd", path="chunk", chunk_len=16)["name"] == "cchunk16_v2_grouped"
+    check_complex(inp, dt, path="chunk", chunk_len=16, tile_variant=1)
+    plan, planb = check_complex(inp, dt)
+    assert plan["path"] == "chunk" and planb["path"] == "chunk"
+
+
+def test_complex_chunked_unaligned_rows():
+    """The chunked kernels read one element per thread: any row alignment."""
+    inp = make_complex_inputs(2, 3000, 37, "bf16", seed=560)
+    plan, planb = check_complex(inp, "bf16", path="chunk", chunk_len=32)
+    assert plan["path"] == "chunk"
+    plan, _ = check_complex(inp, "bf16")
+    assert plan["path"] == "chunk"  # few lanes, long enough: chunks also without alignment
 
 
 def test_complex_full_size_sampled_lanes():
