@@ -3,8 +3,9 @@
 // grouped form _complex_affine_group_local / _outer / _correct), for complex
 // scans whose B*D lanes are too few to fill the GPU with a lane-tiled walk.
 // Time is cut into chunks of C steps; every (row, chunk, lane) is one thread
-// in phases 1 and 3 (V lanes per thread, 1 or 2: the re and im planes are
-// separate arrays, so a warp reads 32*V consecutive lanes of each plane).
+// in phases 1 and 3 (V lanes per thread, 4 on 16-byte aligned rows, else 1:
+// the re and im planes are separate arrays, so a warp reads 32*V consecutive
+// lanes of each plane).
 //
 //   phase 1  summary: chunk c of lane (b,d) as the complex affine map
 //            h -> P*h + Q (P = product of the decays, Q = the chunk's scan

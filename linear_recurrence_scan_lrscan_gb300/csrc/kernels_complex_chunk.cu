@@ -58,12 +58,12 @@ int cbwd_t(const CChunkLaunch &L) {
 }  // namespace
 
 int cchunk_fwd_launch(const CChunkLaunch &L, int dtype) {
-    if (L.vec == 2) return dtype == 0 ? cfwd_t<float, 2>(L) : cfwd_t<bf16_t, 2>(L);
+    if (L.vec == 4) return dtype == 0 ? cfwd_t<float, 4>(L) : cfwd_t<bf16_t, 4>(L);
     return dtype == 0 ? cfwd_t<float, 1>(L) : cfwd_t<bf16_t, 1>(L);
 }
 
 int cchunk_bwd_launch(const CChunkLaunch &L, int dtype) {
-    if (L.vec == 2) return dtype == 0 ? cbwd_t<float, 2>(L) : cbwd_t<bf16_t, 2>(L);
+    if (L.vec == 4) return dtype == 0 ? cbwd_t<float, 4>(L) : cbwd_t<bf16_t, 4>(L);
     return dtype == 0 ? cbwd_t<float, 1>(L) : cbwd_t<bf16_t, 1>(L);
 }
 

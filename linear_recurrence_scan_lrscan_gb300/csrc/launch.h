@@ -136,7 +136,7 @@ struct CChunkLaunch {
     float *gmaps[4];
     int64_t B, T, D;
     int chunk;
-    int vec;  // lanes per thread: 2 when D is even and every plane 2-lane aligned, else 1
+    int vec;  // lanes per thread: 4 on 16-byte aligned rows, else 1
     cudaStream_t stream;
 };
 int cchunk_fwd_launch(const CChunkLaunch &L, int dtype);

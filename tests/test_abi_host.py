@@ -268,12 +268,12 @@ def test_complex_chunked_plans(lib):
     sequences (fewer than 0.45 lane tiles of 32 per SM), twice the real
     path's scratch (re and im maps), flat or grouped prefix."""
     p = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "fwd")
-    assert p["path"] == "chunk" and p["name"] == "cchunk64_v2_grouped" and p["kernels"] == 5, p
+    assert p["path"] == "chunk" and p["name"] == "cchunk64_v4_grouped" and p["kernels"] == 5, p
     assert p["workspace_bytes"] == 2 * L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
     flat = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", path="chunk", tile_variant=1)
     assert flat["kernels"] == 3 and flat["workspace_bytes"] == 4 * 16384 * 64 * 4
     p = L.lrscan_plan_complex(1, 1 << 20, 64, "bf16", "fwd", path="chunk", chunk_len=256)
-    assert p["name"] == "cchunk256_v2_grouped" and p["rows_per_window"] == 256
+    assert p["name"] == "cchunk256_v4_grouped" and p["rows_per_window"] == 256
     # enough lanes, or a short sequence: the tiled kernels
     assert L.lrscan_plan_complex(8, 2048, 2560, "bf16", "fwd")["path"] in ("seq", "window")
     assert L.lrscan_plan_complex(1, 500, 64, "f32", "fwd")["path"] in ("seq", "window")
