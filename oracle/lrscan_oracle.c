@@ -606,6 +606,122 @@ int lro_cbwd_f64(const double *ar, const double *ai, const double *out_r,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Complex scan with carried state and segment resets.                     */
+/*                                                                         */
+/* triton_training_scan.py, _samu_tiled_serial_forward /                    */
+/* _samu_tiled_serial_backward: the page's state-carrying scan is complex  */
+/* (an initial state, RESET_FIRST restarts, the gradient arriving at the   */
+/* final state and the gradient of the initial state).  With the complex   */
+/* steps above and the state rules of the real state-carrying scan:        */
+/*   forward   h_{-1} = h0 (0 when absent); a'_t = 0 where segment_pos is 0 */
+/*             h_t = a'_t * h_{t-1} + b_t;  last = h_{T-1} (h0 when T = 0)   */
+/*   backward  g_T = grad_last (0 when absent) entering through a'_T = 1:   */
+/*             g_{T-1} = grad_out_{T-1} + grad_last (one rounding per part) */
+/*             g_t = grad_out_t + conj(a'_{t+1}) * g_{t+1}                  */
+/*             grad_b_t = g_t; grad_a_t = +0 where step t resets, else      */
+/*             g_t * conj(h_{t-1}) with h_{-1} = h0;                        */
+/*             grad_h0 = conj(a'_0) * g_0 (+0 at a reset; grad_last when    */
+/*             T = 0).                                                      */
+/* h0 / grad_last / grad_h0 are re and im [B,D] arrays in the state         */
+/* precision; every pointer of the extension may be NULL.                  */
+/* ---------------------------------------------------------------------- */
+
+#define CPLX_STATE_FWD_BODY(STATE, FMA, LOAD, STORE)                           \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE hr = h0_r ? h0_r[bb * D + d] : 0;                            \
+            STATE hi = h0_i ? h0_i[bb * D + d] : 0;                            \
+            for (int64_t t = 0; t < T; ++t) {                                  \
+                int64_t i = (bb * T + t) * D + d;                              \
+                int r = resets(seg, bb, T, t);                                 \
+                STATE xr = r ? 0 : LOAD(ar[i]), xi = r ? 0 : LOAD(ai[i]);      \
+                STATE nr = FMA(xr, hr, FMA(-xi, hi, LOAD(br[i])));             \
+                STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));              \
+                hr = nr;                                                       \
+                hi = ni;                                                       \
+                out_r[i] = STORE(hr);                                          \
+                out_i[i] = STORE(hi);                                          \
+            }                                                                  \
+            if (last_r) last_r[bb * D + d] = hr;                               \
+            if (last_i) last_i[bb * D + d] = hi;                               \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define CPLX_STATE_BWD_BODY(STATE, FMA, LOAD, STORE)                           \
+    if (bad_shape(B, T, D)) return LRO_EINVAL;                                 \
+    for (int64_t bb = 0; bb < B; ++bb) {                                       \
+        for (int64_t d = 0; d < D; ++d) {                                      \
+            STATE gr = gl_r ? gl_r[bb * D + d] : 0;                            \
+            STATE gi = gl_i ? gl_i[bb * D + d] : 0;                            \
+            for (int64_t t = T - 1; t >= 0; --t) {                             \
+                int64_t i = (bb * T + t) * D + d;                              \
+                /* conj(a'_{t+1}): 1 past the end (the grad_last entry), 0 at  \
+                 * a reset */                                                  \
+                STATE xr, xi;                                                  \
+                if (t == T - 1) {                                              \
+                    xr = 1;                                                    \
+                    xi = 0;                                                    \
+                } else if (resets(seg, bb, T, t + 1)) {                        \
+                    xr = 0;                                                    \
+                    xi = 0;                                                    \
+                } else {                                                       \
+                    xr = LOAD(ar[i + D]);                                      \
+                    xi = LOAD(ai[i + D]);                                      \
+                }                                                              \
+                STATE yr = LOAD(go_r[i]), yi = LOAD(go_i[i]);                  \
+                STATE nr = FMA(xr, gr, FMA(xi, gi, yr));                       \
+                STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));                      \
+                gr = nr;                                                       \
+                gi = ni;                                                       \
+                STATE pr = (t > 0) ? LOAD(out_r[i - D]) : (h0_r ? h0_r[bb * D + d] : 0); \
+                STATE pi = (t > 0) ? LOAD(out_i[i - D]) : (h0_i ? h0_i[bb * D + d] : 0); \
+                grad_br[i] = STORE(gr);                                        \
+                grad_bi[i] = STORE(gi);                                        \
+                if (resets(seg, bb, T, t)) {                                   \
+                    grad_ar[i] = STORE(0);                                     \
+                    grad_ai[i] = STORE(0);                                     \
+                } else {                                                       \
+                    grad_ar[i] = STORE(FMA(gr, pr, gi * pi));                  \
+                    grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));               \
+                }                                                              \
+            }                                                                  \
+            if (gh0_r || gh0_i) {                                              \
+                STATE hr = gr, hi = gi;                                        \
+                if (T > 0 && resets(seg, bb, T, 0)) {                          \
+                    hr = 0; /* a'_0 = 0: exactly +0 */                         \
+                    hi = 0;                                                    \
+                } else if (T > 0) {                                            \
+                    /* conj(a'_0) * g_0 */                                     \
+                    int64_t i0 = bb * T * D + d;                               \
+                    STATE xr = LOAD(ar[i0]), xi = LOAD(ai[i0]);                \
+                    hr = FMA(xr, gr, xi * gi);                                 \
+                    hi = FMA(xr, gi, -(xi * gr));                              \
+                }                                                              \
+                if (gh0_r) gh0_r[bb * D + d] = hr;                             \
+                if (gh0_i) gh0_i[bb * D + d] = hi;                             \
+            }                                                                  \
+        }                                                                      \
+    }                                                                          \
+    return LRO_OK;
+
+#define CFS_ARGS(ST, SS) const ST *ar, const ST *ai, const ST *br, const ST *bi, ST *out_r, ST *out_i,       \
+                         SS *last_r, SS *last_i, const SS *h0_r, const SS *h0_i, const int32_t *seg,       \
+                         int64_t B, int64_t T, int64_t D
+#define CBS_ARGS(ST, SS) const ST *ar, const ST *ai, const ST *out_r, const ST *out_i, const ST *go_r,     \
+                         const ST *go_i, const SS *h0_r, const SS *h0_i, const int32_t *seg,               \
+                         const SS *gl_r, const SS *gl_i, ST *grad_ar, ST *grad_ai, ST *grad_br,            \
+                         ST *grad_bi, SS *gh0_r, SS *gh0_i, int64_t B, int64_t T, int64_t D
+
+int lro_cfwd_state_f32(CFS_ARGS(float, float)) { CPLX_STATE_FWD_BODY(float, fmaf, LRO_SAME, LRO_SAME) }
+int lro_cfwd_state_bf16(CFS_ARGS(uint16_t, float)) { CPLX_STATE_FWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16) }
+int lro_cfwd_state_f64(CFS_ARGS(double, double)) { CPLX_STATE_FWD_BODY(double, fma, LRO_SAME, LRO_SAME) }
+int lro_cbwd_state_f32(CBS_ARGS(float, float)) { CPLX_STATE_BWD_BODY(float, fmaf, LRO_SAME, LRO_SAME) }
+int lro_cbwd_state_bf16(CBS_ARGS(uint16_t, float)) { CPLX_STATE_BWD_BODY(float, fmaf, lro_bf16_to_f32, lro_f32_to_bf16) }
+int lro_cbwd_state_f64(CBS_ARGS(double, double)) { CPLX_STATE_BWD_BODY(double, fma, LRO_SAME, LRO_SAME) }
+
+/* ---------------------------------------------------------------------- */
 /* Generated (factorized) decay.                                           */
 /*                                                                         */
 /* triton_training_scan.py, _samu_forward / _samu_precompute_decay: the   */

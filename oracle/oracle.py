@@ -77,6 +77,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lro_cbwd_f32", "lro_cbwd_bf16", "lro_cbwd_f64"):
         getattr(lib, name).argtypes = [_P] * 10 + [_I64, _I64, _I64]
         getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_cfwd_state_f32", "lro_cfwd_state_bf16", "lro_cfwd_state_f64"):
+        getattr(lib, name).argtypes = [_P] * 11 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("lro_cbwd_state_f32", "lro_cbwd_state_bf16", "lro_cbwd_state_f64"):
+        getattr(lib, name).argtypes = [_P] * 17 + [_I64, _I64, _I64]
+        getattr(lib, name).restype = ctypes.c_int
     for name in ("lro_gated_fwd_f32", "lro_gated_fwd_bf16", "lro_gated_fwd_f64"):
         getattr(lib, name).argtypes = [_P] * 5 + [_I64, _I64, _I64]
         getattr(lib, name).restype = ctypes.c_int
@@ -259,6 +265,50 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle complex backward failed ({rc})")
         return tuple(gs)
+
+    def cfwd_state(self, ar, ai, br, bi, dtype="f32", h0=None, segment_pos=None):
+        """Complex forward scan from the initial state h0 = (re, im) with segment
+        resets; ``(out_r, out_i, last_r, last_i)``."""
+        xs = [_c(x, dtype) for x in (ar, ai, br, bi)]
+        if any(x.shape != xs[0].shape for x in xs):
+            raise ValueError("ar, ai, br, bi must have the same [B, T, D] shape")
+        B, T, D = xs[0].shape
+        h0r, h0i = (None, None) if h0 is None else (self._state(h0[0], dtype, (B, D), "h0_r"),
+                                                    self._state(h0[1], dtype, (B, D), "h0_i"))
+        seg = self._seg(segment_pos, B, T)
+        out_r, out_i = np.empty_like(xs[0]), np.empty_like(xs[0])
+        last_r = np.empty((B, D), dtype=_LAST[dtype])
+        last_i = np.empty((B, D), dtype=_LAST[dtype])
+        opt = lambda x: None if x is None else _ptr(x)  # noqa: E731
+        rc = getattr(self.lib, f"lro_cfwd_state_{dtype}")(*[_ptr(x) for x in xs], _ptr(out_r), _ptr(out_i),
+                                                           _ptr(last_r), _ptr(last_i), opt(h0r), opt(h0i), opt(seg),
+                                                           B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle complex state forward failed ({rc})")
+        return out_r, out_i, last_r, last_i
+
+    def cbwd_state(self, ar, ai, out_r, out_i, go_r, go_i, dtype="f32", h0=None, segment_pos=None,
+                   grad_last=None):
+        """Reverse scan of :meth:`cfwd_state`; ``(grad_ar, grad_ai, grad_br,
+        grad_bi, grad_h0_r, grad_h0_i)``."""
+        xs = [_c(x, dtype) for x in (ar, ai, out_r, out_i, go_r, go_i)]
+        if any(x.shape != xs[0].shape for x in xs):
+            raise ValueError("complex backward inputs must have the same [B, T, D] shape")
+        B, T, D = xs[0].shape
+        h0r, h0i = (None, None) if h0 is None else (self._state(h0[0], dtype, (B, D), "h0_r"),
+                                                    self._state(h0[1], dtype, (B, D), "h0_i"))
+        glr, gli = (None, None) if grad_last is None else (self._state(grad_last[0], dtype, (B, D), "grad_last_r"),
+                                                           self._state(grad_last[1], dtype, (B, D), "grad_last_i"))
+        seg = self._seg(segment_pos, B, T)
+        gs = [np.empty_like(xs[0]) for _ in range(4)]
+        gh0 = [np.empty((B, D), dtype=_LAST[dtype]) for _ in range(2)]
+        opt = lambda x: None if x is None else _ptr(x)  # noqa: E731
+        rc = getattr(self.lib, f"lro_cbwd_state_{dtype}")(*[_ptr(x) for x in xs], opt(h0r), opt(h0i), opt(seg),
+                                                           opt(glr), opt(gli), *[_ptr(g) for g in gs],
+                                                           _ptr(gh0[0]), _ptr(gh0[1]), B, T, D)
+        if rc:
+            raise RuntimeError(f"oracle complex state backward failed ({rc})")
+        return (*gs, *gh0)
 
     def _gated_params(self, eta, nu_log, dtype, B, T, D):
         want = _LAST[dtype]

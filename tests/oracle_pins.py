@@ -924,4 +924,171 @@ def pin_gated_bf16_storage_is_fp32_state(o):
     assert np.array_equal(r16[1], r32[1]) and np.array_equal(r16[2], r32[2])
 
 
+# ------------------------------------------------ complex scan with state --
+def _cstate_case(seed, B, T, D, dtype=np.float64):
+    ar, ai, br, bi, gr, gi = _ccase(seed, B, T, D, dtype=dtype)
+    r = _rng(seed + 2000)
+    h0 = tuple(r.standard_normal((B, D)).astype(dtype) for _ in range(2))
+    gl = tuple(r.standard_normal((B, D)).astype(dtype) for _ in range(2))
+    return ar, ai, br, bi, gr, gi, h0, gl
+
+
+def pin_cstate_absent_is_plain_complex(o):
+    """No state, or a zero h0, no resets and a zero grad_last, gives the plain
+    complex scan bit for bit (every dtype); grad_h0 is then conj(a_0) * g_0."""
+    ar, ai, br, bi, gr, gi, _, _ = _cstate_case(60, 2, 33, 4, dtype=np.float32)
+    B, T, D = ar.shape
+    for dt in ("f32", "bf16", "f64"):
+        planes = _enc(o, dt, ar, ai, br, bi, gr, gi)
+        sdt = np.float64 if dt == "f64" else np.float32
+        ref = o.cfwd(*planes[:4], dt)
+        gref = o.cbwd(planes[0], planes[1], ref[0], ref[1], planes[4], planes[5], dt)
+        zero = (np.zeros((B, D), sdt), np.zeros((B, D), sdt))
+        noreset = np.arange(1, T + 1, dtype=np.int32)[None].repeat(B, 0)
+        for h0, seg, gl in ((None, None, None), (zero, noreset, zero)):
+            got = o.cfwd_state(*planes[:4], dt, h0=h0, segment_pos=seg)
+            for x, y in zip(got, ref):
+                assert np.array_equal(x, y), dt
+            g = o.cbwd_state(planes[0], planes[1], ref[0], ref[1], planes[4], planes[5], dt, h0=h0,
+                             segment_pos=seg, grad_last=gl)
+            for x, y in zip(g[:4], gref):
+                assert np.array_equal(x, y), dt
+            if dt == "f64":
+                a0 = planes[0][:, 0] + 1j * planes[1][:, 0]
+                g0 = g[2][:, 0] + 1j * g[3][:, 0]
+                want = np.conj(a0) * g0
+                np.testing.assert_allclose(g[4], want.real, rtol=1e-13, atol=1e-13)
+                np.testing.assert_allclose(g[5], want.imag, rtol=1e-13, atol=1e-13)
+
+
+def pin_cstate_reduces_to_real_state_scan(o):
+    """Zero imaginary parts everywhere (decays, inputs, h0, grad_last,
+    grad_out): the real planes are the real state-carrying scan bit for bit in
+    fp32, resets included, and every imaginary plane stays zero."""
+    ar, _, br, _, gr, _, h0, gl = _cstate_case(61, 3, 45, 5, dtype=np.float32)
+    ar = np.abs(ar)
+    z = np.zeros_like(ar)
+    zs = np.zeros_like(h0[0])
+    seg = _segments(62, 3, 45, p=0.1)
+    seg[0, 0] = 0
+    out_r, out_i, last_r, last_i = o.cfwd_state(ar, z, br, z, "f32", h0=(h0[0], zs), segment_pos=seg)
+    rr, lr = o.fwd_state(ar, br, "f32", h0=h0[0], segment_pos=seg)
+    assert np.array_equal(out_r, rr) and np.array_equal(last_r, lr)
+    assert not out_i.any() and not last_i.any()
+    g = o.cbwd_state(ar, z, out_r, out_i, gr, z, "f32", h0=(h0[0], zs), segment_pos=seg, grad_last=(gl[0], zs))
+    ga, gb, gh0 = o.bwd_state(ar, rr, gr, "f32", h0=h0[0], segment_pos=seg, grad_last=gl[0])
+    assert np.array_equal(g[2], gb) and np.array_equal(g[0], ga) and np.array_equal(g[4], gh0)
+    assert not g[1].any() and not g[3].any() and not g[5].any()
+
+
+def pin_cstate_matches_numpy_complex(o):
+    """fp64 against numpy complex128: the forward from h0 with a' = 0 at
+    segment starts, and the adjoint with grad_last entering after the last
+    step, conj(a'_{t+1}) transitions, grad_a = g conj(h_{t-1}) (0 at a reset)
+    and grad_h0 = conj(a'_0) g_0."""
+    B, T, D = 3, 57, 4
+    ar, ai, br, bi, gr, gi, h0, gl = _cstate_case(63, B, T, D)
+    seg = _segments(64, B, T, p=0.12)
+    seg[2, 0] = 0
+    a, b, go = ar + 1j * ai, br + 1j * bi, gr + 1j * gi
+    rs = seg == 0
+    ap = np.where(rs[..., None], 0, a)
+    h = h0[0] + 1j * h0[1]
+    hs = []
+    for t in range(T):
+        h = ap[:, t] * h + b[:, t]
+        hs.append(h)
+    hs = np.stack(hs, 1)
+    out_r, out_i, last_r, last_i = o.cfwd_state(ar, ai, br, bi, "f64", h0=h0, segment_pos=seg)
+    np.testing.assert_allclose(out_r + 1j * out_i, hs, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(last_r + 1j * last_i, hs[:, -1], rtol=1e-12, atol=1e-12)
+    g = gl[0] + 1j * gl[1]
+    gs = [None] * T
+    nxt = np.ones((B, D), complex)  # a'_T = 1: grad_last enters the last step
+    for t in range(T - 1, -1, -1):
+        g = go[:, t] + np.conj(nxt) * g
+        gs[t] = g
+        nxt = ap[:, t]
+    gs = np.stack(gs, 1)
+    prev = np.concatenate([(h0[0] + 1j * h0[1])[:, None], hs[:, :-1]], axis=1)
+    ga = np.where(rs[..., None], 0, gs * np.conj(prev))
+    gh0 = np.conj(ap[:, 0]) * gs[:, 0]
+    got = o.cbwd_state(ar, ai, out_r, out_i, gr, gi, "f64", h0=h0, segment_pos=seg, grad_last=gl)
+    np.testing.assert_allclose(got[2] + 1j * got[3], gs, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got[0] + 1j * got[1], ga, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got[4] + 1j * got[5], gh0, rtol=1e-12, atol=1e-12)
+    assert not got[0][rs].any() and not got[1][rs].any()
+
+
+def pin_cstate_finite_difference(o):
+    """Central differences of L = sum Re(conj(grad_out) h) + Re(conj(grad_last)
+    last) on a tiny fp64 case with one reset: dL/dRe(h0) + i dL/dIm(h0) is
+    grad_h0, and the same for a few decay and input entries."""
+    B, T, D = 1, 6, 2
+    ar, ai, br, bi, gr, gi, h0, gl = _cstate_case(65, B, T, D)
+    seg = np.array([[1, 2, 0, 1, 2, 3]], dtype=np.int32)
+
+    def loss(ar_, ai_, br_, bi_, h0_):
+        o_r, o_i, l_r, l_i = o.cfwd_state(ar_, ai_, br_, bi_, "f64", h0=h0_, segment_pos=seg)
+        return float((gr * o_r + gi * o_i).sum() + (gl[0] * l_r + gl[1] * l_i).sum())
+
+    o_r, o_i, _, _ = o.cfwd_state(ar, ai, br, bi, "f64", h0=h0, segment_pos=seg)
+    g_ar, g_ai, g_br, g_bi, gh_r, gh_i = o.cbwd_state(ar, ai, o_r, o_i, gr, gi, "f64", h0=h0, segment_pos=seg,
+                                                      grad_last=gl)
+    eps = 1e-6
+    for k in range(2):
+        for d in range(D):
+            hp = [h0[0].copy(), h0[1].copy()]
+            hm = [h0[0].copy(), h0[1].copy()]
+            hp[k][0, d] += eps
+            hm[k][0, d] -= eps
+            fd = (loss(ar, ai, br, bi, tuple(hp)) - loss(ar, ai, br, bi, tuple(hm))) / (2 * eps)
+            want = (gh_r if k == 0 else gh_i)[0, d]
+            assert abs(fd - want) <= 1e-6 * (1 + abs(want)), (k, d, fd, want)
+    for (t, d) in ((0, 0), (2, 1), (3, 0), (5, 1)):
+        for name, arr, grad in (("ar", 0, g_ar), ("ai", 1, g_ai), ("br", 2, g_br), ("bi", 3, g_bi)):
+            xs = [ar.copy(), ai.copy(), br.copy(), bi.copy()]
+            xp = [x.copy() for x in xs]
+            xm = [x.copy() for x in xs]
+            xp[arr][0, t, d] += eps
+            xm[arr][0, t, d] -= eps
+            fd = (loss(*xp, h0) - loss(*xm, h0)) / (2 * eps)
+            want = grad[0, t, d]
+            assert abs(fd - want) <= 1e-6 * (1 + abs(want)), (name, t, d, fd, want)
+
+
+def pin_cstate_prefill_continues_exactly(o):
+    """A prefix, then the rest from the prefix's final state, equals one
+    scan bit for bit (fp32 and fp64 forward, with resets); the split backward
+    (the suffix's grad_h0 as the prefix's grad_last) equals the whole one to
+    rounding (fp64)."""
+    B, T, D = 2, 40, 3
+    ar, ai, br, bi, gr, gi, h0, gl = _cstate_case(66, B, T, D)
+    seg = _segments(67, B, T)
+    c = np.ascontiguousarray
+    for dt, npdt in (("f32", np.float32), ("f64", np.float64)):
+        xs = [x.astype(npdt) for x in (ar, ai, br, bi)]
+        hh = tuple(x.astype(npdt) for x in h0)
+        ref = o.cfwd_state(*xs, dt, h0=hh, segment_pos=seg)
+        for T1 in (1, 13, 39):
+            p1 = o.cfwd_state(*[c(x[:, :T1]) for x in xs], dt, h0=hh, segment_pos=c(seg[:, :T1]))
+            p2 = o.cfwd_state(*[c(x[:, T1:]) for x in xs], dt, h0=(p1[2], p1[3]), segment_pos=c(seg[:, T1:]))
+            assert np.array_equal(np.concatenate([p1[0], p2[0]], 1), ref[0]), (dt, T1)
+            assert np.array_equal(np.concatenate([p1[1], p2[1]], 1), ref[1]), (dt, T1)
+            assert np.array_equal(p2[2], ref[2]) and np.array_equal(p2[3], ref[3]), (dt, T1)
+    ref = o.cfwd_state(ar, ai, br, bi, "f64", h0=h0, segment_pos=seg)
+    full = o.cbwd_state(ar, ai, ref[0], ref[1], gr, gi, "f64", h0=h0, segment_pos=seg, grad_last=gl)
+    for T1 in (1, 13, 39):
+        s1, s2 = (slice(None), slice(None, T1)), (slice(None), slice(T1, None))
+        p1 = o.cfwd_state(c(ar[s1]), c(ai[s1]), c(br[s1]), c(bi[s1]), "f64", h0=h0, segment_pos=c(seg[s1]))
+        b2 = o.cbwd_state(c(ar[s2]), c(ai[s2]), c(ref[0][s2]), c(ref[1][s2]), c(gr[s2]), c(gi[s2]), "f64",
+                          h0=(p1[2], p1[3]), segment_pos=c(seg[s2]), grad_last=gl)
+        b1 = o.cbwd_state(c(ar[s1]), c(ai[s1]), c(ref[0][s1]), c(ref[1][s1]), c(gr[s1]), c(gi[s1]), "f64",
+                          h0=h0, segment_pos=c(seg[s1]), grad_last=(b2[4], b2[5]))
+        for k in range(4):
+            np.testing.assert_allclose(np.concatenate([b1[k], b2[k]], 1), full[k], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b1[4], full[4], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b1[5], full[5], rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

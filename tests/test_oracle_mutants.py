@@ -59,6 +59,14 @@ MUTANTS = {
                                       "grad_ai[i] = STORE(FMA(gi, pr, gr * pi));"),
     "complex_grad_a_drops_cross_term": ("grad_ar[i] = STORE(FMA(gr, pr, gi * pi));",
                                         "grad_ar[i] = STORE(gr * pr);"),
+    "cstate_fwd_ignores_h0": ("STATE hr = h0_r ? h0_r[bb * D + d] : 0;", "STATE hr = 0;"),
+    "cstate_fwd_ignores_resets": ("STATE xr = r ? 0 : LOAD(ar[i]), xi = r ? 0 : LOAD(ai[i]);",
+                                  "STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);"),
+    "cstate_bwd_drops_grad_last": ("STATE gr = gl_r ? gl_r[bb * D + d] : 0;", "STATE gr = 0;"),
+    "cstate_bwd_reset_on_wrong_step": ("} else if (resets(seg, bb, T, t + 1)) {", "} else if (resets(seg, bb, T, t)) {"),
+    "cstate_bwd_prev_ignores_h0": ("LOAD(out_i[i - D]) : (h0_i ? h0_i[bb * D + d] : 0)", "LOAD(out_i[i - D]) : 0"),
+    "cstate_grad_a_not_masked": ("grad_ai[i] = STORE(0);", "grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));"),
+    "cstate_grad_h0_not_conjugated": ("hi = FMA(xr, gi, -(xi * gr));", "hi = FMA(xr, gi, xi * gr);"),
     "gated_rate_sign": ("STATE la = -(nu * e);                                          \\\n                h = FMA",
                         "STATE la = nu * e;                                             \\\n                h = FMA"),
     "gated_bwd_rate_not_exponentiated": ("STATE nu = EXP(nu_log[d]);                                         \\\n            STATE g = 0",
