@@ -273,6 +273,42 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
                         const lrscan_opts *opts, lrscan_plan_info *info);
 
 /*
+ * Complex scan with carried state and segment resets
+ * (triton_training_scan.py, _samu_tiled_serial_forward /
+ * _samu_tiled_serial_backward: the page's state-carrying scan is complex).
+ * The rules of lrscan_state, with complex states and conjugate transitions:
+ *   forward   h_{-1} = h0 (0 when absent); a'_t = 0 where segment_pos is 0;
+ *             h_t = a'_t * h_{t-1} + b_t; last = h_{T-1}
+ *   backward  grad_last enters step T-1 through a'_T = 1;
+ *             g_t = grad_out_t + conj(a'_{t+1}) * g_{t+1};  grad_b = g;
+ *             grad_a_t = +0 where step t starts a segment, else
+ *             g_t * conj(h_{t-1}) with h_{-1} = h0;
+ *             grad_h0 = conj(a'_0) * g_0 (+0 when step 0 starts a segment)
+ * Every member may be NULL (all NULL: the plain complex scan); fp32 / int32
+ * device pointers, 4-byte aligned.  These calls run on the chunked path
+ * (opts: LRSCAN_PATH_AUTO or LRSCAN_PATH_CHUNK, chunk_len, tile_variant
+ * 1 / 2 for the flat / grouped prefix, workspace as lrscan_plan_complex with
+ * path chunk reports); any row alignment.  With T == 0 the forward copies h0
+ * (or zeros) into last and the backward grad_last (or zeros) into grad_h0.
+ * The results agree with the sequential definition to rounding.
+ */
+typedef struct lrscan_cstate {
+    const float *h0_r, *h0_i;         /* [B, D] fp32 each: state before step 0 */
+    const int32_t *segment_pos;       /* [B, T] int32: 0 marks the first step of a segment */
+    const float *grad_last_r, *grad_last_i;  /* backward: [B, D] fp32 gradient arriving at last */
+    float *grad_h0_r, *grad_h0_i;     /* backward: [B, D] fp32 outputs, gradient of h0 */
+} lrscan_cstate;
+int lrscan_cfwd_state(const void *ar, const void *ai, const void *br, const void *bi,
+                      void *out_r, void *out_i, float *last_r, float *last_i,
+                      const lrscan_cstate *state, int64_t B, int64_t T, int64_t D, int dtype,
+                      void *stream, const lrscan_opts *opts);
+int lrscan_cbwd_state(const void *ar, const void *ai, const void *out_r, const void *out_i,
+                      const void *grad_out_r, const void *grad_out_i,
+                      void *grad_ar, void *grad_ai, void *grad_br, void *grad_bi,
+                      const lrscan_cstate *state, int64_t B, int64_t T, int64_t D, int dtype,
+                      void *stream, const lrscan_opts *opts);
+
+/*
  * Scan with a generated decay (triton_training_scan.py, _samu_forward and
  * _samu_precompute_decay, the radius part of the page's transition): the
  * decay of lane d at token t is rebuilt in the kernel instead of being read,

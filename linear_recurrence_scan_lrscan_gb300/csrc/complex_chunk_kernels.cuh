@@ -24,6 +24,14 @@
 // next chunk (0 past T), h_{t-1} at its first step from the previous chunk
 // (0 before 0), and grad_a = g * conj(h_{t-1}).  P and Q are fp32
 // [B, Nc, D] per component in a caller- or library-owned workspace.
+//
+// Carried state and segment resets (CStateArgs, every pointer may be null;
+// triton_training_scan.py, _samu_tiled_serial_forward / _backward): the
+// forward prefix starts from h0 and a_t is zeroed where segment_pos is 0; the
+// backward prefix starts from grad_last, which enters step T-1 through
+// a'_T = 1; conj(a'_{t+1}) is zeroed where step t+1 starts a segment, grad_a
+// is +0 where step t does, h_{-1} = h0 and chunk 0 writes
+// grad_h0 = conj(a'_0) * g_0 (+0 at a reset).
 #pragma once
 
 #include "chunk_kernels.cuh"
@@ -31,6 +39,25 @@
 #include "launch.h"
 
 namespace lrscan {
+
+// Segment start at step t (EXT instantiations only; the plain ones carry no
+// state and compile the state handling out).
+template <bool EXT>
+__device__ __forceinline__ bool cseg_reset(const CStateArgs &sx, int brow, int T, int t) {
+    return EXT && sx.seg != nullptr && __ldg(sx.seg + static_cast<size_t>(brow) * T + t) == 0;
+}
+
+// a'_t of V lanes (re, im): zero where step t starts a segment.
+template <typename St, int V, bool EXT>
+__device__ __forceinline__ void load_cdecay(const St *pr, const St *pi, const CStateArgs &sx, int brow, int T, int t,
+                                            float (&xr)[V], float (&xi)[V]) {
+    load_lanes_global<St, V>(pr, xr);
+    load_lanes_global<St, V>(pi, xi);
+    if (cseg_reset<EXT>(sx, brow, T, t)) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) { xr[v] = 0.0f; xi[v] = 0.0f; }
+    }
+}
 
 // Workspace views: P and Q, re and im, each [B, N, D] fp32.
 struct CMaps {
@@ -62,10 +89,10 @@ __device__ __forceinline__ CMap cshfl(const CMap &m, int src) {
 }
 
 // ---------------------------------------------------------------- phase 1 --
-template <typename St, int V>
+template <typename St, int V, bool EXT>
 __global__ void __launch_bounds__(128)
 cchunk_summary_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ br,
-                   const St *__restrict__ bi, CMaps m, ChunkGeom g, int C) {
+                   const St *__restrict__ bi, CMaps m, ChunkGeom g, int C, const CStateArgs sx) {
     int brow, c, d;
     if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
@@ -78,8 +105,7 @@ cchunk_summary_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const S
     for (int j = 0; j < n; ++j) {
         const size_t o = base + static_cast<size_t>(j) * g.D;
         float xr[V], xi[V], yr[V], yi[V];
-        load_lanes_global<St, V>(ar + o, xr);
-        load_lanes_global<St, V>(ai + o, xi);
+        load_cdecay<St, V, EXT>(ar + o, ai + o, sx, brow, g.T, t0 + j, xr, xi);
         load_lanes_global<St, V>(br + o, yr);
         load_lanes_global<St, V>(bi + o, yi);
 #pragma unroll
@@ -99,22 +125,23 @@ cchunk_summary_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const S
 
 // The map from the adjoint entering the chunk's last step (g at the next
 // chunk's first step) to g at the chunk's first step.
-template <typename St, int V>
+template <typename St, int V, bool EXT>
 __global__ void __launch_bounds__(128)
 cchunk_summary_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ gor,
-                   const St *__restrict__ goi, CMaps m, ChunkGeom g, int C) {
+                   const St *__restrict__ goi, CMaps m, ChunkGeom g, int C, const CStateArgs sx) {
     int brow, c, d;
     if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
-    float xr[V], xi[V];  // a_{t+1} of the last step: next chunk's first, 0 past T
+    // a'_{t+1} of the last step: the next chunk's first; past T, 1 when
+    // grad_last enters there, else 0
+    float xr[V], xi[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) { xr[v] = 0.0f; xi[v] = 0.0f; }
-    if (t0 + n < g.T) {
-        load_lanes_global<St, V>(ar + base + static_cast<size_t>(n) * g.D, xr);
-        load_lanes_global<St, V>(ai + base + static_cast<size_t>(n) * g.D, xi);
-    }
+    for (int v = 0; v < V; ++v) { xr[v] = EXT && sx.gl_r != nullptr ? 1.0f : 0.0f; xi[v] = 0.0f; }
+    if (t0 + n < g.T)
+        load_cdecay<St, V, EXT>(ar + base + static_cast<size_t>(n) * g.D, ai + base + static_cast<size_t>(n) * g.D, sx,
+                           brow, g.T, t0 + n, xr, xi);
     float pr[V], pi[V], qr[V], qi[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) { pr[v] = 1.0f; pi[v] = 0.0f; qr[v] = 0.0f; qi[v] = 0.0f; }
@@ -124,8 +151,7 @@ cchunk_summary_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const S
         float yr[V], yi[V], xnr[V], xni[V];
         load_lanes_global<St, V>(gor + o, yr);
         load_lanes_global<St, V>(goi + o, yi);
-        load_lanes_global<St, V>(ar + o, xnr);
-        load_lanes_global<St, V>(ai + o, xni);
+        load_cdecay<St, V, EXT>(ar + o, ai + o, sx, brow, g.T, t0 + j, xnr, xni);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float npr, npi, nqr, nqi;
@@ -185,13 +211,17 @@ __device__ __forceinline__ CMap cscan_maps(const CMaps m, size_t base, int D, in
 // the first processed chunk is 0.
 template <bool REVERSE>
 __global__ void __launch_bounds__(256)
-cchunk_prefix(CMaps m, int N, int D, long long lanes) {
+cchunk_prefix(CMaps m, int N, int D, long long lanes, const float *__restrict__ init_r,
+              const float *__restrict__ init_i) {
     const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (wid >= lanes) return;  // whole warps
     const long long brow = wid / D;
     const int d = static_cast<int>(wid - brow * D);
     const size_t base = static_cast<size_t>(brow) * N * D + d;
-    cscan_maps<REVERSE, true>(m, base, D, N, 0, N, CMap{0.0f, 0.0f, 0.0f, 0.0f});
+    // state entering the first processed chunk: h0 (forward) or grad_last (backward)
+    const CMap init{0.0f, 0.0f, init_r != nullptr ? __ldg(init_r + wid) : 0.0f,
+                    init_i != nullptr ? __ldg(init_i + wid) : 0.0f};
+    cscan_maps<REVERSE, true>(m, base, D, N, 0, N, init);
 }
 
 // Grouped prefix (a): one warp per (lane, group) composes the group's maps;
@@ -234,11 +264,12 @@ cchunk_group_rescan(CMaps m, const CMaps gm, int N, int D, int GC, int NG, long 
 }
 
 // ---------------------------------------------------------------- phase 3 --
-template <typename St, int V>
+template <typename St, int V, bool EXT>
 __global__ void __launch_bounds__(128)
 cchunk_replay_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ br,
                   const St *__restrict__ bi, const CMaps m, St *__restrict__ out_r, St *__restrict__ out_i,
-                  float *__restrict__ last_r, float *__restrict__ last_i, ChunkGeom g, int C) {
+                  float *__restrict__ last_r, float *__restrict__ last_i, ChunkGeom g, int C,
+                  const CStateArgs sx) {
     int brow, c, d;
     if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
@@ -252,8 +283,7 @@ cchunk_replay_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const St
     for (int j = 0; j < n; ++j) {
         const size_t o = base + static_cast<size_t>(j) * g.D;
         float xr[V], xi[V], yr[V], yi[V];
-        load_lanes_global<St, V>(ar + o, xr);
-        load_lanes_global<St, V>(ai + o, xi);
+        load_cdecay<St, V, EXT>(ar + o, ai + o, sx, brow, g.T, t0 + j, xr, xi);
         load_lanes_global<St, V>(br + o, yr);
         load_lanes_global<St, V>(bi + o, yi);
 #pragma unroll
@@ -276,45 +306,48 @@ cchunk_replay_fwd(const St *__restrict__ ar, const St *__restrict__ ai, const St
     }
 }
 
-template <typename St, int V>
+template <typename St, int V, bool EXT>
 __global__ void __launch_bounds__(128)
 cchunk_replay_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const St *__restrict__ out_r,
                   const St *__restrict__ out_i, const St *__restrict__ gor, const St *__restrict__ goi,
                   const CMaps m, St *__restrict__ gar, St *__restrict__ gai, St *__restrict__ gbr,
-                  St *__restrict__ gbi, ChunkGeom g, int C) {
+                  St *__restrict__ gbi, ChunkGeom g, int C, const CStateArgs sx) {
     int brow, c, d;
     if (!chunk_thread<V>(g, brow, c, d)) return;
     const int t0 = c * C;
     const int n = min(C, g.T - t0);
     const size_t base = (static_cast<size_t>(brow) * g.T + t0) * g.D + d;
     const size_t so = (static_cast<size_t>(brow) * g.Nc + c) * g.D + d;
-    float gr[V], gi[V], xr[V], xi[V];  // adjoint at the next chunk's first step; a_{t+1}
+    float gr[V], gi[V], xr[V], xi[V];  // adjoint at the next chunk's first step; a'_{t+1}
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         gr[v] = __ldcg(m.qr + so + v);
         gi[v] = __ldcg(m.qi + so + v);
-        xr[v] = 0.0f;
+        xr[v] = EXT && sx.gl_r != nullptr ? 1.0f : 0.0f;
         xi[v] = 0.0f;
     }
-    if (t0 + n < g.T) {
-        load_lanes_global<St, V>(ar + base + static_cast<size_t>(n) * g.D, xr);
-        load_lanes_global<St, V>(ai + base + static_cast<size_t>(n) * g.D, xi);
-    }
+    if (t0 + n < g.T)
+        load_cdecay<St, V, EXT>(ar + base + static_cast<size_t>(n) * g.D, ai + base + static_cast<size_t>(n) * g.D, sx,
+                           brow, g.T, t0 + n, xr, xi);
 #pragma unroll 4
     for (int j = n - 1; j >= 0; --j) {
         const size_t o = base + static_cast<size_t>(j) * g.D;
         float yr[V], yi[V], xnr[V], xni[V], pr[V], pi[V], far[V], fai[V];
         load_lanes_global<St, V>(gor + o, yr);
         load_lanes_global<St, V>(goi + o, yi);
-        load_lanes_global<St, V>(ar + o, xnr);
-        load_lanes_global<St, V>(ai + o, xni);
+        load_cdecay<St, V, EXT>(ar + o, ai + o, sx, brow, g.T, t0 + j, xnr, xni);
         if (t0 + j > 0) {
             load_lanes_global<St, V>(out_r + o - g.D, pr);
             load_lanes_global<St, V>(out_i + o - g.D, pi);
         } else {
+            const size_t hs = static_cast<size_t>(brow) * g.D + d;
 #pragma unroll
-            for (int v = 0; v < V; ++v) { pr[v] = 0.0f; pi[v] = 0.0f; }
+            for (int v = 0; v < V; ++v) {
+                pr[v] = EXT && sx.h0_r != nullptr ? sx.h0_r[hs + v] : 0.0f;
+                pi[v] = EXT && sx.h0_i != nullptr ? sx.h0_i[hs + v] : 0.0f;
+            }
         }
+        const bool rz = cseg_reset<EXT>(sx, brow, g.T, t0 + j);  // a_t unused: grad_a = +0
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float nr, ni;
@@ -322,8 +355,8 @@ cchunk_replay_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const St
             gr[v] = nr;
             gi[v] = ni;
             // grad_a = g * conj(h_{t-1})
-            far[v] = __fmaf_rn(gr[v], pr[v], __fmul_rn(gi[v], pi[v]));
-            fai[v] = __fmaf_rn(gi[v], pr[v], -__fmul_rn(gr[v], pi[v]));
+            far[v] = rz ? 0.0f : __fmaf_rn(gr[v], pr[v], __fmul_rn(gi[v], pi[v]));
+            fai[v] = rz ? 0.0f : __fmaf_rn(gi[v], pr[v], -__fmul_rn(gr[v], pi[v]));
             xr[v] = xnr[v];
             xi[v] = xni[v];
         }
@@ -331,6 +364,18 @@ cchunk_replay_bwd(const St *__restrict__ ar, const St *__restrict__ ai, const St
         store_lanes<St, V>(gbi + o, gi);
         store_lanes<St, V>(gar + o, far);
         store_lanes<St, V>(gai + o, fai);
+    }
+    if (EXT && c == 0 && (sx.gh0_r != nullptr || sx.gh0_i != nullptr)) {
+        // x holds a'_0: grad_h0 = conj(a'_0) * g_0, exactly +0 at a reset
+        const bool r0 = cseg_reset<EXT>(sx, brow, g.T, 0);
+        const size_t hs = static_cast<size_t>(brow) * g.D + d;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const float hr = r0 ? 0.0f : __fmaf_rn(xr[v], gr[v], __fmul_rn(xi[v], gi[v]));
+            const float hi = r0 ? 0.0f : __fmaf_rn(xr[v], gi[v], -__fmul_rn(xi[v], gr[v]));
+            if (sx.gh0_r != nullptr) sx.gh0_r[hs + v] = hr;
+            if (sx.gh0_i != nullptr) sx.gh0_i[hs + v] = hi;
+        }
     }
 }
 

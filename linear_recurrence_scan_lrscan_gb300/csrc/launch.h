@@ -128,6 +128,14 @@ int cplain_bwd_launch(const void *const in[6], void *const out[4], int64_t B, in
 // out_i, go_r, go_i}, out = {grad_ar, grad_ai, grad_br, grad_bi}.  maps: P re,
 // P im, Q re, Q im [B, Nc, D] each; gmaps: the grouped prefix's group maps
 // [B, ceil(Nc / kGroupChunks), D] each, or all null (flat prefix).
+// Carried state of a complex scan: h0 and grad_last in, grad_h0 out (re and
+// im fp32 [B, D] each), segment positions int32 [B, T]; all null: none.
+struct CStateArgs {
+    const float *h0_r, *h0_i;
+    const int32_t *seg;
+    const float *gl_r, *gl_i;
+    float *gh0_r, *gh0_i;
+};
 struct CChunkLaunch {
     const void *in[6];
     void *out[4];
@@ -138,6 +146,7 @@ struct CChunkLaunch {
     int chunk;
     int vec;  // lanes per thread: 4 on 16-byte aligned rows, else 1
     cudaStream_t stream;
+    CStateArgs sx;
 };
 int cchunk_fwd_launch(const CChunkLaunch &L, int dtype);
 int cchunk_bwd_launch(const CChunkLaunch &L, int dtype);

@@ -721,9 +721,12 @@ size_t cchunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped) {
     return 2 * chunk_workspace(B, T, D, C, grouped);
 }
 
+// ext: the call carries state or resets (chunked path only).
 int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
-                 const Geometry &g, Choice *ch) {
+                 const Geometry &g, Choice *ch, bool ext = false) {
     const int want = opts ? opts->path : 0;
+    if (ext && want != kPathAuto && want != kPathChunk)
+        return fail(LRSCAN_EINVAL, "the complex scan with carried state runs on the chunked path (path %d)", want);
     const int force_v = opts ? opts->tile_variant : 0;
     if (want != kPathAuto && want != kPathSeq && want != kPathWindow && want != kPathPlain && want != kPathChunk)
         return fail(LRSCAN_EINVAL, "unknown complex scan path %d", want);
@@ -740,7 +743,7 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         // 0.45 tiles per SM; the plain kernels' bound without alignment) and
         // a long sequence: parallelize over time chunks
         const long long few = aligned16 ? static_cast<long long>(0.45 * g.sm_count * 32) : 32LL * g.sm_count * 32;
-        if (B * D < few && T >= 16LL * chunk) path = kPathChunk;
+        if (ext || (B * D < few && T >= 16LL * chunk)) path = kPathChunk;
         else path = aligned16 ? kPathSeq : kPathPlain;
     } else {
         // seq and window both name the tiled variant table (sequential and windowed tiles)
@@ -816,15 +819,43 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     return LRSCAN_OK;
 }
 
+// Complex carried state, checked (fp32 / int32 pointers 4-byte aligned);
+// *any is set when the call carries state.
+int check_cstate(const lrscan_cstate *s, bool bwd, CStateArgs *sx, bool *any) {
+    *sx = CStateArgs{};
+    *any = false;
+    if (!s) return LRSCAN_OK;
+    sx->h0_r = s->h0_r;
+    sx->h0_i = s->h0_i;
+    sx->seg = s->segment_pos;
+    if (bwd) {
+        sx->gl_r = s->grad_last_r;
+        sx->gl_i = s->grad_last_i;
+        sx->gh0_r = s->grad_h0_r;
+        sx->gh0_i = s->grad_h0_i;
+    }
+    const void *ps[7] = {sx->h0_r, sx->h0_i, sx->seg, sx->gl_r, sx->gl_i, sx->gh0_r, sx->gh0_i};
+    for (const void *p : ps) {
+        if (!p) continue;
+        if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return fail(LRSCAN_EINVAL, "state pointer %p is not 4-byte aligned", p);
+        *any = true;
+    }
+    return LRSCAN_OK;
+}
+
 int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, float *last_i, int64_t B, int64_t T,
-             int64_t D, int dtype, void *stream, const lrscan_opts *opts) {
+             int64_t D, int dtype, void *stream, const lrscan_opts *opts, const lrscan_cstate *state = nullptr) {
     t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
+    CStateArgs sx;
+    bool ext = false;
+    if ((rc = check_cstate(state, false, &sx, &ext))) return rc;
     if (B == 0 || D == 0) return LRSCAN_OK;
     cudaStream_t st = pick_stream(stream);
     if (T == 0) {
-        if ((rc = copy_or_zero(last_r, nullptr, B, D, st)) || (rc = copy_or_zero(last_i, nullptr, B, D, st))) return rc;
+        if ((rc = copy_or_zero(last_r, sx.h0_r, B, D, st)) || (rc = copy_or_zero(last_i, sx.h0_i, B, D, st)))
+            return rc;
         return LRSCAN_OK;
     }
     if (!in[0] || !in[1] || !in[2] || !in[3] || !out_r || !out_i)
@@ -835,7 +866,7 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
     cudaGetDevice(&dev);
     const bool al = aligned16({in[0], in[1], in[2], in[3], out_r, out_i}, D, dtype);
     Choice ch;
-    if ((rc = plan_complex(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch))) return rc;
+    if ((rc = plan_complex(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     const size_t es = esize(dtype);
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
@@ -846,6 +877,7 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
         L.out[1] = out_i;
         L.last_r = last_r;
         L.last_i = last_i;
+        L.sx = sx;
         set_cchunk_scratch(&L, ws, B, T, D, ch);
         L.B = B; L.T = T; L.D = D; L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
         return cchunk_fwd_launch(L, dtype)
@@ -887,11 +919,20 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
 }
 
 int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T, int64_t D, int dtype, void *stream,
-             const lrscan_opts *opts) {
+             const lrscan_opts *opts, const lrscan_cstate *state = nullptr) {
     t_detail[0] = 0;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
-    if (B == 0 || D == 0 || T == 0) return LRSCAN_OK;
+    CStateArgs sx;
+    bool ext = false;
+    if ((rc = check_cstate(state, true, &sx, &ext))) return rc;
+    if (B == 0 || D == 0) return LRSCAN_OK;
+    if (T == 0) {
+        cudaStream_t st0 = pick_stream(stream);
+        if ((rc = copy_or_zero(sx.gh0_r, sx.gl_r, B, D, st0)) || (rc = copy_or_zero(sx.gh0_i, sx.gl_i, B, D, st0)))
+            return rc;
+        return LRSCAN_OK;
+    }
     for (int i = 0; i < 6; ++i)
         if (!in[i]) return fail(LRSCAN_EINVAL, "NULL complex backward input %d", i);
     for (int i = 0; i < 4; ++i)
@@ -903,13 +944,14 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
     cudaGetDevice(&dev);
     const bool al = aligned16({in[0], in[1], in[2], in[3], in[4], in[5], outp[0], outp[1], outp[2], outp[3]}, D, dtype);
     Choice ch;
-    if ((rc = plan_complex(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch))) return rc;
+    if ((rc = plan_complex(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
         if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
         CChunkLaunch L{};
         for (int i = 0; i < 6; ++i) L.in[i] = in[i];
         for (int i = 0; i < 4; ++i) L.out[i] = outp[i];
+        L.sx = sx;
         set_cchunk_scratch(&L, ws, B, T, D, ch);
         L.B = B; L.T = T; L.D = D; L.chunk = ch.chunk; L.vec = ch.vec; L.stream = st;
         return cchunk_bwd_launch(L, dtype)
@@ -1287,6 +1329,22 @@ int lrscan_cbwd(const void *ar, const void *ai, const void *out_r, const void *o
     const void *in[6] = {ar, ai, out_r, out_i, grad_out_r, grad_out_i};
     void *const outp[4] = {grad_ar, grad_ai, grad_br, grad_bi};
     return run_cbwd(in, outp, B, T, D, dtype, stream, opts);
+}
+
+int lrscan_cfwd_state(const void *ar, const void *ai, const void *br, const void *bi, void *out_r, void *out_i,
+                      float *last_r, float *last_i, const lrscan_cstate *state, int64_t B, int64_t T, int64_t D,
+                      int dtype, void *stream, const lrscan_opts *opts) {
+    const void *in[4] = {ar, ai, br, bi};
+    return run_cfwd(in, out_r, out_i, last_r, last_i, B, T, D, dtype, stream, opts, state);
+}
+
+int lrscan_cbwd_state(const void *ar, const void *ai, const void *out_r, const void *out_i, const void *grad_out_r,
+                      const void *grad_out_i, void *grad_ar, void *grad_ai, void *grad_br, void *grad_bi,
+                      const lrscan_cstate *state, int64_t B, int64_t T, int64_t D, int dtype, void *stream,
+                      const lrscan_opts *opts) {
+    const void *in[6] = {ar, ai, out_r, out_i, grad_out_r, grad_out_i};
+    void *const outp[4] = {grad_ar, grad_ai, grad_br, grad_bi};
+    return run_cbwd(in, outp, B, T, D, dtype, stream, opts, state);
 }
 
 int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,

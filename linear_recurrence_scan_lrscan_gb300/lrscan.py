@@ -74,6 +74,12 @@ class State(ctypes.Structure):
                 ("grad_h0", ctypes.c_void_p)]
 
 
+class CState(ctypes.Structure):
+    _fields_ = [("h0_r", ctypes.c_void_p), ("h0_i", ctypes.c_void_p), ("segment_pos", ctypes.c_void_p),
+                ("grad_last_r", ctypes.c_void_p), ("grad_last_i", ctypes.c_void_p), ("grad_h0_r", ctypes.c_void_p),
+                ("grad_h0_i", ctypes.c_void_p)]
+
+
 EXPORTS = {
     "lrscan_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
     "lrscan_bwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int], ctypes.c_int),
@@ -93,6 +99,10 @@ EXPORTS = {
     "lrscan_compose_maps": ([_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
     "lrscan_cfwd": ([_P] * 8 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_cbwd": ([_P] * 10 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_cfwd_state": ([_P] * 8 + [ctypes.POINTER(CState), _I64, _I64, _I64, ctypes.c_int, _P,
+                                     ctypes.POINTER(Opts)], ctypes.c_int),
+    "lrscan_cbwd_state": ([_P] * 10 + [ctypes.POINTER(CState), _I64, _I64, _I64, ctypes.c_int, _P,
+                                      ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_plan_complex": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
                              ctypes.POINTER(PlanInfo)], ctypes.c_int),
     "lrscan_fwd_gated": ([_P] * 5 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
@@ -489,6 +499,74 @@ def lrscan_cbwd(ar, ai, out_r, out_i, grad_out_r, grad_out_i, *, grads=None, pat
                                B, T, D, code, _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
     _check(rc, "lrscan_cbwd")
     return grads
+
+
+def _cstate(ar, h0=None, segment_pos=None, grad_last=None, grad_h0=None) -> CState:
+    B, T, D = ar.shape
+    st = CState()
+    pairs = (("h0", h0, ("h0_r", "h0_i")), ("grad_last", grad_last, ("grad_last_r", "grad_last_i")),
+             ("grad_h0", grad_h0, ("grad_h0_r", "grad_h0_i")))
+    for name, pair, fields in pairs:
+        if pair is None:
+            continue
+        if len(pair) != 2:
+            raise ValueError(f"{name} must be a (re, im) pair of tensors")
+        for f, t in zip(fields, pair):
+            setattr(st, f, _check_state_tensor(f, t, (B, D), torch.float32, ar.device))
+    st.segment_pos = _check_state_tensor("segment_pos", segment_pos, (B, T), torch.int32, ar.device)
+    return st
+
+
+def lrscan_cfwd_state(ar, ai, br, bi, h0=None, segment_pos=None, *, out_r=None, out_i=None, last_r=None,
+                      last_i=None, path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
+    """Complex forward scan from the fp32 (re, im) [B, D] state h0, restarting
+    where the int32 [B, T] segment_pos is 0; returns (out_r, out_i, last_r,
+    last_i).  Runs on the chunked path."""
+    if ar.ndim != 3 or any(t.shape != ar.shape for t in (ai, br, bi)):
+        raise ValueError("lrscan expects matching [B, T, D] planes")
+    code = _dtype_code(ar)
+    B, T, D = ar.shape
+    out_r = torch.empty_like(ar) if out_r is None else out_r
+    out_i = torch.empty_like(ar) if out_i is None else out_i
+    last_r = torch.empty((B, D), device=ar.device, dtype=torch.float32) if last_r is None else last_r
+    last_i = torch.empty((B, D), device=ar.device, dtype=torch.float32) if last_i is None else last_i
+    _check_tensors(ar.shape, ar.dtype, ar.device, ar=ar, ai=ai, br=br, bi=bi, out_r=out_r, out_i=out_i)
+    for name, t in (("last_r", last_r), ("last_i", last_i)):
+        _check_state_tensor(name, t, (B, D), torch.float32, ar.device)
+    st = _cstate(ar, h0=h0, segment_pos=segment_pos)
+    with torch.cuda.device(ar.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_cfwd_state(ar.data_ptr(), ai.data_ptr(), br.data_ptr(), bi.data_ptr(), out_r.data_ptr(),
+                                     out_i.data_ptr(), last_r.data_ptr(), last_i.data_ptr(), ctypes.byref(st),
+                                     B, T, D, code, _stream_ptr(stream), ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_cfwd_state")
+    return out_r, out_i, last_r, last_i
+
+
+def lrscan_cbwd_state(ar, ai, out_r, out_i, grad_out_r, grad_out_i, h0=None, segment_pos=None, grad_last=None, *,
+                      grads=None, grad_h0=None, path=None, chunk_len=None, tile_variant=None, workspace=None,
+                      stream=None):
+    """Reverse scan of :func:`lrscan_cfwd_state` for the loss
+    sum(Re(conj(grad_out) h)) + Re(conj(grad_last) last); returns
+    (grad_ar, grad_ai, grad_br, grad_bi, grad_h0_r, grad_h0_i)."""
+    if ar.ndim != 3:
+        raise ValueError("lrscan expects [B, T, D] planes")
+    code = _dtype_code(ar)
+    B, T, D = ar.shape
+    grads = tuple(torch.empty_like(ar) for _ in range(4)) if grads is None else tuple(grads)
+    if grad_h0 is None:
+        grad_h0 = tuple(torch.empty((B, D), device=ar.device, dtype=torch.float32) for _ in range(2))
+    _check_tensors(ar.shape, ar.dtype, ar.device, ar=ar, ai=ai, out_r=out_r, out_i=out_i, grad_out_r=grad_out_r,
+                   grad_out_i=grad_out_i, grad_ar=grads[0], grad_ai=grads[1], grad_br=grads[2], grad_bi=grads[3])
+    st = _cstate(ar, h0=h0, segment_pos=segment_pos, grad_last=grad_last, grad_h0=grad_h0)
+    with torch.cuda.device(ar.device):
+        o = _opts(path, chunk_len, tile_variant, workspace)
+        rc = lib().lrscan_cbwd_state(ar.data_ptr(), ai.data_ptr(), out_r.data_ptr(), out_i.data_ptr(),
+                                     grad_out_r.data_ptr(), grad_out_i.data_ptr(), *[g.data_ptr() for g in grads],
+                                     ctypes.byref(st), B, T, D, code, _stream_ptr(stream),
+                                     ctypes.byref(o) if o is not None else None)
+    _check(rc, "lrscan_cbwd_state")
+    return (*grads, *grad_h0)
 
 
 def lrscan_plan_complex(B: int, T: int, D: int, dtype="f32", direction: str = "fwd", aligned: bool = True,

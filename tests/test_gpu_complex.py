@@ -179,3 +179,95 @@ def test_complex_scan_autograd(dt):
     gref = o.cbwd(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt)
     for x, r in zip(xs, gref):
         assert_close(to_np(x.grad), r, dt, "complex autograd", reassociated=True)
+
+
+# ------------------------------------------------ carried state and resets --
+def _cstate_inputs(B, T, D, dt, seed):
+    inp = make_complex_inputs(B, T, D, dt, seed=seed)
+    r = np.random.default_rng(seed)
+    h0 = [r.standard_normal((B, D)).astype(np.float32) for _ in range(2)]
+    gl = [r.standard_normal((B, D)).astype(np.float32) for _ in range(2)]
+    starts = r.random((B, T)) < 0.03
+    seg = np.zeros((B, T), dtype=np.int32)
+    for bb in range(B):
+        pos = 0
+        for t in range(T):
+            pos = 0 if starts[bb, t] else (pos + 1 if t > 0 else 1)
+            seg[bb, t] = pos
+    return inp, h0, gl, seg
+
+
+def check_cstate(inp, dt, h0, gl, seg, **kw):
+    """Forward and backward with carried state against the oracle; the
+    backward reads the oracle's forward output (both sides see the same
+    h_{t-1})."""
+    np_in = {k: to_np(inp[k]) for k in PLANES}
+    o = oracle.default()
+    ref = o.cfwd_state(np_in["ar"], np_in["ai"], np_in["br"], np_in["bi"], dt, h0=tuple(h0), segment_pos=seg)
+    cu = {k: inp[k].cuda() for k in PLANES}
+    th0 = tuple(torch.from_numpy(x).cuda() for x in h0)
+    tgl = tuple(torch.from_numpy(x).cuda() for x in gl)
+    tseg = torch.from_numpy(seg).cuda()
+    got = L.lrscan_cfwd_state(cu["ar"], cu["ai"], cu["br"], cu["bi"], h0=th0, segment_pos=tseg, **kw)
+    assert L.lrscan_sync_check() == 0
+    for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
+        assert_close(to_np(g), r, dt, f"{name} (state)", reassociated=True)
+    for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
+        assert_last_close(g.cpu().numpy(), r, f"{name} (state)")
+    out_r, out_i = from_np(ref[0], dt).cuda(), from_np(ref[1], dt).cuda()
+    gref = o.cbwd_state(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt, h0=tuple(h0),
+                        segment_pos=seg, grad_last=tuple(gl))
+    ggot = L.lrscan_cbwd_state(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"], h0=th0, segment_pos=tseg,
+                               grad_last=tgl, **kw)
+    assert L.lrscan_sync_check() == 0
+    for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot[:4], gref[:4]):
+        assert_close(to_np(g), r, dt, f"{name} (state)", reassociated=True)
+    for name, g, r in zip(("grad_h0_r", "grad_h0_i"), ggot[4:], gref[4:]):
+        assert_last_close(g.cpu().numpy(), r, f"{name} (state)")
+    # grad_a is exactly +0 at every segment start
+    rs = np.broadcast_to((seg == 0)[..., None], ref[0].shape)
+    for g in ggot[:2]:
+        assert not to_np(g).view(np.uint16 if dt == "bf16" else np.uint32)[rs].any()
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [None, 16])
+def test_complex_state_every_shape(dt, chunk):
+    for i, (B, T, D) in enumerate(SHAPES):
+        inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=570 + i)
+        check_cstate(inp, dt, h0, gl, seg, chunk_len=chunk)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_state_grouped_prefix_and_unaligned(dt):
+    inp, h0, gl, seg = _cstate_inputs(1, 40000, 8, dt, seed=580)
+    check_cstate(inp, dt, h0, gl, seg, chunk_len=16, tile_variant=2)  # five groups of 512 chunk maps
+    check_cstate(inp, dt, h0, gl, seg, chunk_len=16, tile_variant=1)
+    inp, h0, gl, seg = _cstate_inputs(2, 500, 37, dt, seed=581)      # rows not 16-byte aligned
+    check_cstate(inp, dt, h0, gl, seg, chunk_len=32)
+
+
+def test_complex_state_absent_equals_plain_and_empty():
+    inp = make_complex_inputs(2, 300, 64, "f32", seed=590)
+    cu = {k: inp[k].cuda() for k in PLANES}
+    a = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"], path="chunk")
+    b = L.lrscan_cfwd_state(cu["ar"], cu["ai"], cu["br"], cu["bi"], path="chunk")
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    ga = L.lrscan_cbwd(cu["ar"], cu["ai"], a[0], a[1], cu["go_r"], cu["go_i"], path="chunk")
+    gb = L.lrscan_cbwd_state(cu["ar"], cu["ai"], a[0], a[1], cu["go_r"], cu["go_i"], path="chunk")
+    for x, y in zip(ga, gb[:4]):
+        assert torch.equal(x, y)
+    # T == 0: last = h0, grad_h0 = grad_last
+    e = torch.empty((2, 0, 16), device="cuda")
+    h0 = (torch.randn(2, 16, device="cuda"), torch.randn(2, 16, device="cuda"))
+    gl = (torch.randn(2, 16, device="cuda"), torch.randn(2, 16, device="cuda"))
+    _, _, lr, li = L.lrscan_cfwd_state(e, e, e, e, h0=h0)
+    assert torch.equal(lr, h0[0]) and torch.equal(li, h0[1])
+    g = L.lrscan_cbwd_state(e, e, e, e, e, e, grad_last=gl)
+    assert torch.equal(g[4], gl[0]) and torch.equal(g[5], gl[1])
+    # the state-carrying complex scan runs on the chunked path only
+    x = torch.zeros((1, 64, 16), device="cuda")
+    with pytest.raises(L.LrscanError):
+        L.lrscan_cfwd_state(x, x, x, x, h0=(x[:, 0], x[:, 0]), path="seq")
+    assert L.lrscan_sync_check() == 0
