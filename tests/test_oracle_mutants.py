@@ -51,8 +51,8 @@ MUTANTS = {
                          "STATE nr = FMA(xr, hr, FMA(xi, hi, LOAD(br[i])));"),
     "complex_fwd_swapped_parts": ("STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));",
                                   "STATE ni = FMA(xi, hi, FMA(xr, hr, LOAD(bi[i])));"),
-    "complex_bwd_no_conjugate": ("STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));",
-                                 "STATE ni = FMA(xr, gi, FMA(xi, gr, yi));"),
+    "complex_bwd_no_conjugate": ("                    STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));",
+                                 "                    STATE ni = FMA(xr, gi, FMA(xi, gr, yi));"),
     "complex_bwd_uses_a_t": ("STATE xr = LOAD(ar[i + D]), xi = LOAD(ai[i + D]);",
                              "STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);"),
     "complex_grad_a_not_conjugated": ("grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));",
