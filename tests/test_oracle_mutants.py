@@ -13,6 +13,8 @@ import oracle_pins
 from oracle import Oracle, load
 from oracle.oracle import _SRC, compile_library
 
+CPLX_FWD_STEP = 'STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);                      \\\n                STATE nr = FMA(xr, hr, FMA(-xi, hi, LOAD(br[i])));             \\\n                STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));'
+
 MUTANTS = {
     "fwd_f64_drops_b": ("h[d] = fma(a[i], h[d], b[i]);", "h[d] = a[i] * h[d];"),
     "fwd_f64_no_row_reset": ("for (int64_t d = 0; d < D; ++d) h[d] = 0.0;\n", "\n"),
@@ -47,18 +49,19 @@ MUTANTS = {
     "state_grad_h0_ignores_first_reset": ("grad_h0[bb * D + d] = resets(seg, bb, T, 0)",
                                           "grad_h0[bb * D + d] = 0"),
     "state_empty_grad_h0_zero": ("grad_h0[bb * D + d] = g;", "grad_h0[bb * D + d] = 0;"),
-    "complex_fwd_sign": ("STATE nr = FMA(xr, hr, FMA(-xi, hi, LOAD(br[i])));",
-                         "STATE nr = FMA(xr, hr, FMA(xi, hi, LOAD(br[i])));"),
-    "complex_fwd_swapped_parts": ("STATE ni = FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])));",
-                                  "STATE ni = FMA(xi, hi, FMA(xr, hr, LOAD(bi[i])));"),
+    # anchors include the plain complex body's own loads (the state-carrying
+    # complex body repeats these statements)
+    "complex_fwd_sign": (CPLX_FWD_STEP, CPLX_FWD_STEP.replace("FMA(-xi, hi, LOAD(br[i]))", "FMA(xi, hi, LOAD(br[i]))")),
+    "complex_fwd_swapped_parts": (CPLX_FWD_STEP, CPLX_FWD_STEP.replace("FMA(xi, hr, FMA(xr, hi, LOAD(bi[i])))",
+                                                                       "FMA(xi, hi, FMA(xr, hr, LOAD(bi[i])))")),
     "complex_bwd_no_conjugate": ("                    STATE ni = FMA(xr, gi, FMA(-xi, gr, yi));",
                                  "                    STATE ni = FMA(xr, gi, FMA(xi, gr, yi));"),
     "complex_bwd_uses_a_t": ("STATE xr = LOAD(ar[i + D]), xi = LOAD(ai[i + D]);",
                              "STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);"),
-    "complex_grad_a_not_conjugated": ("grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));",
-                                      "grad_ai[i] = STORE(FMA(gi, pr, gr * pi));"),
-    "complex_grad_a_drops_cross_term": ("grad_ar[i] = STORE(FMA(gr, pr, gi * pi));",
-                                        "grad_ar[i] = STORE(gr * pr);"),
+    "complex_grad_a_not_conjugated": ("\n                grad_ai[i] = STORE(FMA(gi, pr, -(gr * pi)));",
+                                      "\n                grad_ai[i] = STORE(FMA(gi, pr, gr * pi));"),
+    "complex_grad_a_drops_cross_term": ("\n                grad_ar[i] = STORE(FMA(gr, pr, gi * pi));",
+                                        "\n                grad_ar[i] = STORE(gr * pr);"),
     "cstate_fwd_ignores_h0": ("STATE hr = h0_r ? h0_r[bb * D + d] : 0;", "STATE hr = 0;"),
     "cstate_fwd_ignores_resets": ("STATE xr = r ? 0 : LOAD(ar[i]), xi = r ? 0 : LOAD(ai[i]);",
                                   "STATE xr = LOAD(ar[i]), xi = LOAD(ai[i]);"),
