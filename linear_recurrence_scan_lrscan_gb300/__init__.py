@@ -5,7 +5,7 @@
 
 its state-carrying form (initial state h0, segment resets, gradients of the
 final and initial states: ``scan_state``), the complex scan on re/im planes
-(``complex_scan``), the scan with decays generated in the kernel from
+(``complex_scan``; with carried complex state ``complex_scan_state``), the scan with decays generated in the kernel from
 per-token and per-lane parameters (``gated_scan``), and the pieces of a sequence split across devices
 (``lrscan_summary``, ``lrscan_compose_maps``, module ``tsplit``), and calls on
 host buffers that pipeline the copies with the kernels (``lrscan_fwd_host``,
@@ -18,16 +18,20 @@ it has not been built.
 """
 from .lrscan import (  # noqa: F401
     ComplexScan,
+    ComplexScanState,
     GatedScan,
     LinearRecurrenceScan,
     LinearRecurrenceScanState,
     LrscanError,
     LrscanUnavailable,
     complex_scan,
+    complex_scan_state,
     gated_scan,
     lrscan_bwd_gated,
     lrscan_cbwd,
+    lrscan_cbwd_state,
     lrscan_cfwd,
+    lrscan_cfwd_state,
     lrscan_compose_maps,
     lrscan_bwd,
     lrscan_bwd_host,

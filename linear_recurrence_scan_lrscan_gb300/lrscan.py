@@ -769,6 +769,51 @@ def complex_scan(ar, ai, br, bi, path=None):
     return ComplexScan.apply(ar, ai, br, bi, path)
 
 
+class ComplexScanState(torch.autograd.Function):
+    """Autograd wrapper of the state-carrying complex scan: (out_r, out_i,
+    last_r, last_i) = scan(ar, ai, br, bi, h0 = (h0_r, h0_i), segment_pos);
+    gradients flow to the decays, the inputs and h0 from every output."""
+
+    @staticmethod
+    def forward(ctx, ar, ai, br, bi, h0_r, h0_i, segment_pos, chunk_len=None):
+        ar, ai, br, bi = (t.contiguous() for t in (ar, ai, br, bi))
+        B, _, D = ar.shape
+        if (h0_r is None) != (h0_i is None):
+            zero = torch.zeros((B, D), device=ar.device, dtype=torch.float32)
+            h0_r = zero if h0_r is None else h0_r
+            h0_i = zero if h0_i is None else h0_i
+        h0 = None if h0_r is None else (h0_r.contiguous(), h0_i.contiguous())
+        seg = segment_pos.contiguous() if segment_pos is not None else None
+        out_r, out_i, last_r, last_i = lrscan_cfwd_state(ar, ai, br, bi, h0=h0, segment_pos=seg, chunk_len=chunk_len)
+        ctx.save_for_backward(ar, ai, out_r, out_i, *(h0 if h0 is not None else (None, None)), seg)
+        ctx.chunk_len = chunk_len
+        ctx.has_h0 = h0 is not None
+        ctx.mark_non_differentiable(*(() if seg is None else (seg,)))
+        return out_r, out_i, last_r, last_i
+
+    @staticmethod
+    def backward(ctx, g_out_r, g_out_i, g_last_r, g_last_i):
+        ar, ai, out_r, out_i, h0_r, h0_i, seg = ctx.saved_tensors
+        gr = torch.zeros_like(out_r) if g_out_r is None else g_out_r.contiguous()
+        gi = torch.zeros_like(out_i) if g_out_i is None else g_out_i.contiguous()
+        gl = None
+        if g_last_r is not None or g_last_i is not None:
+            z = torch.zeros((ar.shape[0], ar.shape[2]), device=ar.device, dtype=torch.float32)
+            gl = ((z if g_last_r is None else g_last_r).contiguous(), (z if g_last_i is None else g_last_i).contiguous())
+        h0 = (h0_r, h0_i) if ctx.has_h0 else None
+        g = lrscan_cbwd_state(ar, ai, out_r, out_i, gr, gi, h0=h0, segment_pos=seg, grad_last=gl,
+                              chunk_len=ctx.chunk_len)
+        gh0 = (g[4], g[5]) if ctx.has_h0 else (None, None)
+        return (*g[:4], *gh0, None, None)
+
+
+def complex_scan_state(ar, ai, br, bi, h0=None, segment_pos=None, chunk_len=None):
+    """Differentiable state-carrying complex scan; h0 is an fp32 (re, im) pair
+    of [B, D] tensors or None; returns (out_r, out_i, last_r, last_i)."""
+    h0_r, h0_i = (None, None) if h0 is None else h0
+    return ComplexScanState.apply(ar, ai, br, bi, h0_r, h0_i, segment_pos, chunk_len)
+
+
 class GatedScan(torch.autograd.Function):
     """Autograd wrapper of the generated-decay scan: out = scan(eta, nu_log, b)."""
 

@@ -271,3 +271,28 @@ def test_complex_state_absent_equals_plain_and_empty():
     with pytest.raises(L.LrscanError):
         L.lrscan_cfwd_state(x, x, x, x, h0=(x[:, 0], x[:, 0]), path="seq")
     assert L.lrscan_sync_check() == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_scan_state_autograd(dt):
+    """The autograd wrapper: gradients of Re(conj(go) h) + Re(conj(gl) last)
+    to the decays, the inputs and h0 against the oracle."""
+    B, T, D = 2, 300, 64
+    inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=595)
+    xs = [inp[k].cuda().requires_grad_() for k in ("ar", "ai", "br", "bi")]
+    th0 = [torch.from_numpy(x).cuda().requires_grad_() for x in h0]
+    tseg = torch.from_numpy(seg).cuda()
+    out_r, out_i, last_r, last_i = L.complex_scan_state(*xs, h0=tuple(th0), segment_pos=tseg)
+    go_r, go_i = inp["go_r"].cuda().float(), inp["go_i"].cuda().float()
+    glr, gli = (torch.from_numpy(x).cuda() for x in gl)
+    loss = (out_r.float() * go_r + out_i.float() * go_i).sum() + (last_r * glr + last_i * gli).sum()
+    loss.backward()
+    o = oracle.default()
+    np_in = {k: to_np(inp[k]) for k in PLANES}
+    ref = o.cfwd_state(np_in["ar"], np_in["ai"], np_in["br"], np_in["bi"], dt, h0=tuple(h0), segment_pos=seg)
+    gref = o.cbwd_state(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt, h0=tuple(h0),
+                        segment_pos=seg, grad_last=tuple(gl))
+    for x, r in zip(xs, gref[:4]):
+        assert_close(to_np(x.grad), r, dt, "complex state autograd", reassociated=True)
+    for x, r in zip(th0, gref[4:]):
+        assert_last_close(x.grad.cpu().numpy(), r, "grad h0 (autograd)")
