@@ -139,6 +139,29 @@ def test_complex_step_replays():
     _graph_replay_matches_eager(case(1020), run, case(1021))
 
 
+def test_complex_state_step_replays():
+    """The state-carrying complex scan (chunked path, library-owned workspace)."""
+    B, T, D, dt = 2, 300, 64, "bf16"
+    planes = ("ar", "ai", "br", "bi", "go_r", "go_i")
+
+    def case(seed):
+        inp = make_complex_inputs(B, T, D, dt, seed=seed)
+        x = {k: inp[k].cuda() for k in planes}
+        g = torch.Generator("cpu").manual_seed(seed)
+        for k in ("h0_r", "h0_i", "gl_r", "gl_i"):
+            x[k] = torch.randn(B, D, generator=g).cuda()
+        x["seg"] = _segments(B, T, seed)
+        return x
+
+    def run(x):
+        out = L.lrscan_cfwd_state(x["ar"], x["ai"], x["br"], x["bi"], h0=(x["h0_r"], x["h0_i"]), segment_pos=x["seg"])
+        g = L.lrscan_cbwd_state(x["ar"], x["ai"], out[0], out[1], x["go_r"], x["go_i"], h0=(x["h0_r"], x["h0_i"]),
+                                segment_pos=x["seg"], grad_last=(x["gl_r"], x["gl_i"]))
+        return (*out, *g)
+
+    _graph_replay_matches_eager(case(1040), run, case(1041))
+
+
 def test_generated_decay_step_replays():
     B, T, D, dt = 2, 300, 128, "bf16"
 
