@@ -1,8 +1,10 @@
 """GPU parity of the complex diagonal scan (re/im planes) on every path and
-tile variant, against the oracle's complex scan.  The sequential tiles and
-the plain kernels keep the oracle's order of operations and are compared
-exactly; the windowed forward tiles re-associate through complex affine maps
-and are held to the tolerances of parity_util."""
+tile variant, against the oracle's complex scan, and of the state-carrying
+complex scan (h0, segment resets, grad_last, grad_h0) against the oracle's
+complex state functions.  The sequential tiles and the plain kernels keep the
+oracle's order of operations and are compared exactly; the windowed tiles and
+the chunked path re-associate through complex affine maps and are held to the
+tolerances of parity_util."""
 import numpy as np
 import pytest
 import torch
