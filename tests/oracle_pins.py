@@ -1057,6 +1057,33 @@ def pin_cstate_finite_difference(o):
             assert abs(fd - want) <= 1e-6 * (1 + abs(want)), (name, t, d, fd, want)
 
 
+def pin_cstate_empty_sequence_and_first_step_reset(o):
+    """T == 0: the final state is h0 and the initial-state gradient is
+    grad_last (zeros without them).  A reset at step 0 ignores h0 entirely:
+    the outputs equal the scan without state and grad_h0 is exactly +0."""
+    e = np.zeros((2, 0, 3))
+    h0 = (np.arange(6.0).reshape(2, 3), -np.arange(6.0).reshape(2, 3) - 1)
+    gl = (np.full((2, 3), 0.5), np.full((2, 3), -2.0))
+    _, _, lr, li = o.cfwd_state(e, e, e, e, "f64", h0=h0)
+    assert np.array_equal(lr, h0[0]) and np.array_equal(li, h0[1])
+    g = o.cbwd_state(e, e, e, e, e, e, "f64", h0=h0, grad_last=gl)
+    assert np.array_equal(g[4], gl[0]) and np.array_equal(g[5], gl[1])
+    g = o.cbwd_state(e, e, e, e, e, e, "f64")
+    assert not g[4].any() and not g[5].any()
+    ar, ai, br, bi, gr, gi, h0, _ = _cstate_case(68, 2, 20, 3)
+    seg = np.arange(20, dtype=np.int32)[None].repeat(2, 0)  # position 0 at step 0: a reset
+    ref = o.cfwd(ar, ai, br, bi, "f64")
+    got = o.cfwd_state(ar, ai, br, bi, "f64", h0=h0, segment_pos=seg)
+    for x, y in zip(got, ref):
+        assert np.array_equal(x, y)
+    g = o.cbwd_state(ar, ai, ref[0], ref[1], gr, gi, "f64", h0=h0, segment_pos=seg)
+    gref = o.cbwd(ar, ai, ref[0], ref[1], gr, gi, "f64")
+    for x, y in zip(g[2:4], gref[2:4]):
+        assert np.array_equal(x, y)
+    assert not g[0][:, 0].any() and not g[1][:, 0].any()
+    assert not g[4].any() and not g[5].any() and not np.signbit(g[4]).any()
+
+
 def pin_cstate_prefill_continues_exactly(o):
     """A prefix, then the rest from the prefix's final state, equals one
     scan bit for bit (fp32 and fp64 forward, with resets); the split backward
