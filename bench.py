@@ -1,13 +1,21 @@
 """Benchmark of the diagonal linear-recurrence scan (forward + backward).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4] [--sets 3]
+                    [--impl reference]
 
 One step = one forward scan and one backward scan over one batch of the
-workload (default: the gated bf16 workload, B=8 T=2048 D=2560, bf16 storage,
-fp32 state).  Inputs are resident in HBM before the timed region.  Three
-independent buffer sets rotate so that no kernel reads what the previous
-kernels left in L2 (each set is larger than a third of the 126 MB L2 and
-the rotation touches 3x that between reuses).
+workload: by default the largest named workload (near-unit bf16, B=16 T=4096
+D=4096, bf16 storage, fp32 state; 268 M elements per tensor, 512 MiB, larger
+than L2).  Inputs are resident in HBM before the timed region, and three
+independent buffer sets rotate (each kernel reads the set that was written or
+read two steps earlier).
+
+The JSON line carries the step throughput (`value`), each direction timed
+alone over back-to-back launches (`fwd`, `bwd`, `roofline` for the slower
+one), the same figures for every other named workload (`per_config`), the
+end-to-end figure through the host-buffer C ABI call (`e2e`), the next rows
+on their own workloads (`extensions`) and the oracle on the host cores
+(`cpu_baseline`).
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas: the scan's lanes shard with
@@ -224,20 +232,111 @@ def cpu_baseline(w, seconds: float = 12.0) -> dict:
             "single_thread": {"value": single, "cores": 1, "repetitions": n}}
 
 
-def config_of(w, pf, pb) -> dict:
+def config_of(w, pf, pb, nsets: int = 3) -> dict:
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
     c = {"workload": w.describe(), "B": w.B, "T": w.T, "D": w.D, "storage": w.dtype, "state": "f32",
-         "elements_per_step": w.elements,
-         "l2": "three rotating buffer sets; every kernel's inputs were last touched >= 2 kernels "
-               "(> 126 MB of traffic) earlier"}
+         "elements_per_step": w.elements}
+    big = w.elements * w.storage_bytes > L2_BYTES
+    c["l2"] = (f"inputs larger than L2 ({w.elements * w.storage_bytes / 2**20:.0f} MiB per tensor) and "
+               if big else "") + (f"{nsets} rotating buffer sets; each kernel reads the set written or read "
+                                  f"{nsets - 1} steps earlier" if nsets > 1 else "one buffer set")
     if w.chunk:
         c["chunk"] = w.chunk
     if pf is not None:
         c["fwd_kernel"] = pf["name"]
         c["bwd_kernel"] = pb["name"]
+    c["why_this_workload"] = ("the metric names no workload: the largest of the five named workloads "
+                              "that fits one GPU (by elements per step)"
+                              if w.elements == max(x.elements for x in WORKLOADS.values()) else
+                              "chosen with --config")
     return c
 
 
 # ------------------------------------------------------------------ ours ----
+def device_sets(w, host: dict, dev, nsets: int, opts: dict) -> list[dict]:
+    """`nsets` independent device copies of the workload's inputs with their
+    output buffers; each set's `out` holds that set's forward result."""
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    sets = []
+    for _ in range(nsets):
+        a, b, g = host["a"].to(dev), host["b"].to(dev), host["grad_out"].to(dev)
+        sets.append({"a": a, "b": b, "g": g, "out": torch.empty_like(a), "ga": torch.empty_like(a),
+                     "gb": torch.empty_like(a),
+                     "last": torch.empty(w.B, w.D, device=dev, dtype=torch.float32)})
+    for s in sets:
+        L.lrscan_fwd(s["a"], s["b"], s["out"], s["last"], **opts)
+    torch.cuda.synchronize()
+    return sets
+
+
+def fwd_call(sets, opts):
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    n = len(sets)
+
+    def fn(i):
+        s = sets[i % n]
+        L.lrscan_fwd(s["a"], s["b"], s["out"], s["last"], **opts)
+    return fn
+
+
+def bwd_call(sets, opts):
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    n = len(sets)
+
+    def fn(i):
+        s = sets[i % n]
+        L.lrscan_bwd(s["a"], s["out"], s["g"], s["ga"], s["gb"], **opts)
+    return fn
+
+
+def kernel_timing(w, sets, opts, iters: int, stream, peak: float) -> dict:
+    """Forward alone and backward alone, each over `iters` back-to-back
+    launches rotating the buffer sets (CUDA events on the launching stream):
+    mean device time per launch, algorithmic GB/s and its fraction of the
+    measured copy peak, with the kernel the dispatcher ran."""
+    from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    fms = time_launches(fwd_call(sets, opts), iters, stream)
+    bms = time_launches(bwd_call(sets, opts), iters, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError(f"device error while timing {w.describe()}")
+    pf = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", **opts)
+    pb = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", **opts)
+    bf, bb = algorithmic_bytes(w)
+    res = {"workload": w.describe(), "launches_per_direction": iters, "buffer_sets": len(sets)}
+    for key, ms, by, p in (("fwd", fms, bf, pf), ("bwd", bms, bb, pb)):
+        gbs = by / (ms * 1e-3) / 1e9
+        res[key] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak, "algorithmic_bytes": by,
+                    "elements/s": w.elements / (ms * 1e-3), "kernel": p["name"], "path": p["path"],
+                    "kernels": p["kernels"], "traffic": load_traffic(w, key, p["name"])}
+    res["elements/s"] = 2 * w.elements / ((fms + bms) * 1e-3)
+    return res
+
+
+def run_per_config(args, dev, stream, peak, headline: dict) -> dict:
+    """Every named workload (1-5) at full size on its automatic plan, timed
+    like the headline (back-to-back launches per direction, rotating buffer
+    sets).  The headline workload's entry is the one measured above."""
+    import torch
+
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS, make_inputs
+    out = {}
+    for cid, w in WORKLOADS.items():
+        if cid == args.config:
+            out[str(cid)] = headline
+            continue
+        host = make_inputs(cid)
+        # tiny workloads are launch-latency bound: more launches per sample
+        iters = max(20, min(args.steps, 200)) if w.elements > (1 << 20) else 200
+        sets = device_sets(w, host, dev, min(3, args.sets), {})
+        del host
+        out[str(cid)] = kernel_timing(w, sets, {}, iters, stream, peak)
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     import torch
 
@@ -259,42 +358,21 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     pf = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", **opts)
     pb = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", **opts)
 
-    nsets = 3
-    sets = []
-    for i in range(nsets):
-        a = a_h.to(dev)
-        b = b_h.to(dev)
-        g = g_h.to(dev)
-        sets.append({"a": a, "b": b, "g": g, "out": torch.empty_like(a), "ga": torch.empty_like(a),
-                     "gb": torch.empty_like(a),
-                     "last": torch.empty(w.B, w.D, device=dev, dtype=torch.float32)})
-    for s in sets:   # every set holds a valid forward output before the loop
-        L.lrscan_fwd(s["a"], s["b"], s["out"], s["last"], **opts)
-    torch.cuda.synchronize()
+    sets = device_sets(w, inp, dev, args.sets, opts)
+    nsets = len(sets)
+    fwd, bwd = fwd_call(sets, opts), bwd_call(sets, opts)
 
-    def step(i, ev=None):
-        f = sets[i % nsets]
-        bset = sets[(i + nsets - 1) % nsets]
-        if ev is not None:
-            ev[0].record(stream)
-        L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
-        if ev is not None:
-            ev[1].record(stream)
-        L.lrscan_bwd(bset["a"], bset["out"], bset["g"], bset["ga"], bset["gb"], **opts)
-        if ev is not None:
-            ev[2].record(stream)
+    def step(i):
+        # the backward reads the set the previous step's forward wrote
+        fwd(i)
+        bwd(i + nsets - 1)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     assert L.lrscan_sync_check() == 0
 
-    # Device-timed region.  Per-kernel durations are sampled with events on one
-    # step in SAMPLE_EVERY (an event between two kernels stops the next kernel's
-    # launch from overlapping the previous one's tail, so the other steps run
-    # without them); the step time is the region's end-to-end time.
-    sample_every = 32
-    evs = {}
+    peaks = load_peaks()
     clocks = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[dev.index]))
     if rank == 0:
@@ -303,26 +381,27 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    # Device-timed region: K steps of forward + backward, nothing else on the stream.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        ev = None
-        if i % sample_every == min(sample_every // 2, args.steps - 1):
-            ev = evs[i] = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        step(args.warmup + i, ev)
+        step(args.warmup + i)
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop() if rank == 0 else None
     rc = L.lrscan_sync_check()
     if rc != 0:
         raise RuntimeError(f"device error during the timed region: {rc}")
     total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
-    total_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms], dist, dev)
+    # Per-kernel durations, right after the step loop and still under the clock
+    # sampler: each direction alone over back-to-back launches.
+    iters = max(20, min(args.steps, 200))
+    kt = kernel_timing(w, sets, opts, iters, stream, peaks["hbm_gbs"])
+    clk = clocks.stop() if rank == 0 else None
+    total_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, kt["fwd"]["us"] * 1e-3, kt["bwd"]["us"] * 1e-3], dist,
+                                              dev)
     ms_per_step = total_ms / args.steps
 
     # end to end through the host-buffer entry point: pinned host inputs ->
@@ -379,16 +458,16 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
                "path": "lrscan_fwd_bwd_host (C ABI, pinned host buffers): batch-row chunks, copies in / kernels / "
                        "copies out on three streams",
                "unpipelined_ms_per_step": serial_ms}
+        del pa, pbuf, pg, ho, hga, hgb, hl
         assert L.lrscan_sync_check() == 0
+    del inp, a_h, b_h, g_h
 
     if rank != 0:
         return None
-    peaks = load_peaks()
     bf, bb = algorithmic_bytes(w)
     gbs_f = bf / (fwd_ms * 1e-3) / 1e9
     gbs_b = bb / (bwd_ms * 1e-3) / 1e9
-    dominant = ("bwd", bb, bwd_ms, gbs_b) if bwd_ms >= fwd_ms else ("fwd", bf, fwd_ms, gbs_f)
-    traffic = load_traffic(w, dominant[0], pb["name"] if dominant[0] == "bwd" else pf["name"])
+    dominant = ("bwd", bb, bwd_ms, gbs_b, pb) if bwd_ms >= fwd_ms else ("fwd", bf, fwd_ms, gbs_f, pf)
     line = {
         "metric": METRIC,
         "value": job_throughput(world, w.elements, ms_per_step),
@@ -402,25 +481,29 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w, pf, pb),
-        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]}:{(pb if dominant[0] == 'bwd' else pf)['name']}",
+        "config": config_of(w, pf, pb, nsets),
+        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]}:{dominant[4]['name']}",
                      "achieved": dominant[3], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dominant[3] / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": dominant[1], "traffic": traffic},
-        "fwd": {"ms": fwd_ms, "GB/s": gbs_f, "frac": gbs_f / peaks["hbm_gbs"],
-                "elements/s": w.elements / (fwd_ms * 1e-3), "kernel": pf["name"], "path": pf["path"]},
-        "bwd": {"ms": bwd_ms, "GB/s": gbs_b, "frac": gbs_b / peaks["hbm_gbs"],
-                "elements/s": w.elements / (bwd_ms * 1e-3), "kernel": pb["name"], "path": pb["path"]},
+                     "algorithmic_bytes_per_launch": dominant[1], "launch_us": dominant[2] * 1e3,
+                     "launches_timed": iters, "traffic": kt[dominant[0]]["traffic"]},
+        "fwd": kt["fwd"],
+        "bwd": kt["bwd"],
         "step_GB/s": (bf + bb) / (ms_per_step * 1e-3) / 1e9,
-        "kernel_timing": f"CUDA events around each kernel on {len(evs)} sampled steps of the timed region "
-                         f"(one in {sample_every}); the other steps run without per-kernel events",
+        "kernel_timing": f"each direction alone over {iters} back-to-back launches rotating {nsets} buffer "
+                         "sets, CUDA events on the launching stream, right after the step loop (clocks "
+                         "sampled over both)",
         "gpu_launches": args.steps * (pf["kernels"] + pb["kernels"]),
         "clocks": clk,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_per_config:
+        line["per_config"] = run_per_config(args, dev, stream, peaks["hbm_gbs"], kt)
     if not args.no_extensions:
-        line["extensions"] = run_extensions(args, w, dev, sets, opts, peaks["hbm_gbs"])
+        line["extensions"] = run_extensions(args, dev, peaks["hbm_gbs"])
+    del sets
+    torch.cuda.empty_cache()
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
@@ -444,17 +527,22 @@ def time_launches(fn, iters: int, stream) -> float:
     return e0.elapsed_time(e1) / iters
 
 
-def run_extensions(args, w, dev, sets, opts, peak) -> dict:
-    """The state-carrying scan on the same workload and buffer sets: initial
-    state h0, a segment start every 512 tokens on average, grad_last in and
-    grad_h0 out.  Each direction is timed over back-to-back launches rotating
-    the three buffer sets; GB/s counts the bytes the operation must move."""
+def run_extensions(args, dev, peak) -> dict:
+    """The next rows on their own workloads.  Here: the state-carrying scan
+    on the gated workload (2): initial state h0, a segment start every 512
+    tokens on average, grad_last in and grad_h0 out.  Each direction is timed
+    over back-to-back launches rotating three buffer sets; GB/s counts the
+    bytes the operation must move."""
     import numpy as np
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+    from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS, make_inputs
     stream = torch.cuda.current_stream()
-    iters = max(10, min(args.steps, 200))
+    iters = max(20, min(args.steps, 200))
+    w = WORKLOADS[2]
+    opts = {}
+    sets = device_sets(w, make_inputs(2), dev, 3, opts)
     B, T, D, E, s = w.B, w.T, w.D, w.elements, w.storage_bytes
     r = np.random.default_rng(7)
     pos = np.zeros((B, T), dtype=np.int32)
@@ -481,12 +569,12 @@ def run_extensions(args, w, dev, sets, opts, peak) -> dict:
         raise RuntimeError("device error while timing the state-carrying scan")
     fb = 3 * E * s + 4 * B * T + 2 * 4 * B * D
     bb = 5 * E * s + 4 * B * T + 3 * 4 * B * D
-    for f in sets:   # leave every set with the plain forward's output
-        L.lrscan_fwd(f["a"], f["b"], f["out"], f["last"], **opts)
-    torch.cuda.synchronize()
+    del sets
+    torch.cuda.empty_cache()
     return {"complex": run_complex(iters, dev, peak), "complex_long_t": run_complex_long_t(dev, peak),
             "generated_decay": run_gated(iters, dev, peak),
             "long_t": run_long_t(dev, peak), "state": {
+        "workload": w.describe(),
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
         "launches_per_direction": iters,
@@ -502,6 +590,7 @@ def run_complex(iters: int, dev, peak) -> dict:
     shape and decay magnitudes with random phases), three rotating buffer
     sets; forward moves 6 elements per (t, d) (+ the fp32 final state),
     backward 10."""
+    import numpy as np
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
@@ -531,17 +620,57 @@ def run_complex(iters: int, dev, peak) -> dict:
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the complex scan")
     E, s = cw.elements, cw.storage_bytes
-    fb, bb = 6 * E * s + 8 * cw.B * cw.D, 10 * E * s
-    pf = L.lrscan_plan_complex(cw.B, cw.T, cw.D, cw.dtype, "fwd")
-    pb = L.lrscan_plan_complex(cw.B, cw.T, cw.D, cw.dtype, "bwd")
+    B, T, D = cw.B, cw.T, cw.D
+    fb, bb = 6 * E * s + 8 * B * D, 10 * E * s
+    pf = L.lrscan_plan_complex(B, T, D, cw.dtype, "fwd")
+    pb = L.lrscan_plan_complex(B, T, D, cw.dtype, "bwd")
+    res = {"workload": cw.describe() + " complex (re/im planes)", "launches_per_direction": iters,
+           "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                   "algorithmic_bytes": fb, "kernel": pf["name"]},
+           "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                   "algorithmic_bytes": bb, "kernel": pb["name"]},
+           "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+
+    # the same workload with carried state: complex h0 in, a segment start
+    # every 512 tokens on average, complex grad_last in, grad_h0 out
+    r = np.random.default_rng(8)
+    pos = np.zeros((B, T), dtype=np.int32)
+    starts = r.random((B, T)) < 1.0 / 512
+    for t in range(1, T):
+        pos[:, t] = np.where(starts[:, t], 0, pos[:, t - 1] + 1)
+    seg = torch.from_numpy(pos).to(dev)
+    h0 = (torch.randn(B, D, device=dev), torch.randn(B, D, device=dev))
+    gl = (torch.randn(B, D, device=dev), torch.randn(B, D, device=dev))
+    gh0 = [torch.empty(B, D, device=dev) for _ in range(2)]
+
+    def sfwd(i):
+        st = sets[i % 3]
+        L.lrscan_cfwd_state(st["ar"], st["ai"], st["br"], st["bi"], h0=h0, segment_pos=seg, out_r=st["out"][0],
+                            out_i=st["out"][1], last_r=st["last"][0], last_i=st["last"][1])
+
+    def sbwd(i):
+        st = sets[i % 3]
+        L.lrscan_cbwd_state(st["ar"], st["ai"], st["out"][0], st["out"][1], st["go_r"], st["go_i"], h0=h0,
+                            segment_pos=seg, grad_last=gl, grads=st["grads"], grad_h0=gh0)
+    sfms = time_launches(sfwd, iters, stream)
+    sbms = time_launches(sbwd, iters, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the state-carrying complex scan")
+    sfb = fb + 4 * B * T + 8 * B * D
+    sbb = bb + 4 * B * T + 3 * 8 * B * D
+    psf = L.lrscan_plan_complex(B, T, D, cw.dtype, "fwd", state=True)
+    psb = L.lrscan_plan_complex(B, T, D, cw.dtype, "bwd", state=True)
+    res["state"] = {
+        "what": "carried state: complex h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
+                "complex grad_last in, grad_h0 out",
+        "fwd": {"ms": sfms, "GB/s": sfb / (sfms * 1e-3) / 1e9, "frac": sfb / (sfms * 1e-3) / 1e9 / peak,
+                "algorithmic_bytes": sfb, "kernel": psf["name"]},
+        "bwd": {"ms": sbms, "GB/s": sbb / (sbms * 1e-3) / 1e9, "frac": sbb / (sbms * 1e-3) / 1e9 / peak,
+                "algorithmic_bytes": sbb, "kernel": psb["name"]},
+        "elements/s": 2 * E / ((sfms + sbms) * 1e-3)}
     del sets
     torch.cuda.empty_cache()
-    return {"workload": cw.describe() + " complex (re/im planes)", "launches_per_direction": iters,
-            "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
-                    "algorithmic_bytes": fb, "kernel": pf["name"]},
-            "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
-                    "algorithmic_bytes": bb, "kernel": pb["name"]},
-            "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+    return res
 
 
 def run_complex_long_t(dev, peak) -> dict:
@@ -711,7 +840,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, help="workload id 1..5 (default 2)")
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload id 1..5 (default 4, the largest: B=16 T=4096 D=4096 bf16)")
+    ap.add_argument("--sets", type=int, default=3,
+                    help="rotating device buffer sets (1 keeps the footprint small, e.g. for a profiler)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the timing of the other named workloads")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default=None, choices=[None, "auto", "seq", "window", "chunk", "plain"])
     ap.add_argument("--variant", type=int, default=0)
@@ -725,6 +859,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.sets < 1:
+        ap.error("--sets must be >= 1")
 
     from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.config]

@@ -98,6 +98,10 @@ typedef struct lrscan_plan_info {
     int kernels;            /* kernel launches per call */
     size_t workspace_bytes; /* device workspace the call needs */
     char name[64];          /* variant name */
+    int exact;              /* 1: every result is bit-identical to the sequential
+                               definition (its fused multiply-add order); 0: the
+                               path re-associates through affine maps (agrees to
+                               rounding) or uses a fast exponential */
 } lrscan_plan_info;
 
 /*
@@ -271,6 +275,12 @@ int lrscan_cbwd(const void *ar, const void *ai, const void *out_r, const void *o
 /* lrscan_plan for the complex scan (tile variants listed by tile_variant 1..) */
 int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
                         const lrscan_opts *opts, lrscan_plan_info *info);
+/* The plan of a complex call with carried state or resets
+ * (lrscan_cfwd_state / lrscan_cbwd_state): the same choice as
+ * lrscan_plan_complex, except that unaligned rows take the chunked path (the
+ * plain kernels carry no state). */
+int lrscan_plan_complex_state(int64_t B, int64_t T, int64_t D, int dtype, int dir, int aligned16,
+                              const lrscan_opts *opts, lrscan_plan_info *info);
 
 /*
  * Complex scan with carried state and segment resets
@@ -285,12 +295,17 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
  *             g_t * conj(h_{t-1}) with h_{-1} = h0;
  *             grad_h0 = conj(a'_0) * g_0 (+0 when step 0 starts a segment)
  * Every member may be NULL (all NULL: the plain complex scan); fp32 / int32
- * device pointers, 4-byte aligned.  These calls run on the chunked path
- * (opts: LRSCAN_PATH_AUTO or LRSCAN_PATH_CHUNK, chunk_len, tile_variant
- * 1 / 2 for the flat / grouped prefix, workspace as lrscan_plan_complex with
- * path chunk reports); any row alignment.  With T == 0 the forward copies h0
- * (or zeros) into last and the backward grad_last (or zeros) into grad_h0.
- * The results agree with the sequential definition to rounding.
+ * device pointers, 4-byte aligned.  These calls run on the tiled kernels
+ * (opts: LRSCAN_PATH_AUTO, or LRSCAN_PATH_SEQ / LRSCAN_PATH_WINDOW with
+ * tile_variant as lrscan_plan_complex_state reports) when every plane's rows
+ * are 16-byte aligned and the lanes fill the GPU, else on the chunked path
+ * (LRSCAN_PATH_CHUNK: chunk_len, tile_variant 1 / 2 for the flat / grouped
+ * prefix, workspace as lrscan_plan_complex_state reports; any row
+ * alignment).  LRSCAN_PATH_PLAIN is refused (LRSCAN_EINVAL).  With T == 0
+ * the forward copies h0 (or zeros) into last and the backward grad_last (or
+ * zeros) into grad_h0.  The sequential tiles reproduce the sequential
+ * definition bit for bit (lrscan_plan_info.exact); the windowed tiles and
+ * the chunked path agree with it to rounding.
  */
 typedef struct lrscan_cstate {
     const float *h0_r, *h0_i;         /* [B, D] fp32 each: state before step 0 */
@@ -435,10 +450,16 @@ int lrscan_version(void);
  * memory-pool callback, where a nested allocation would re-enter the
  * allocator; latency-critical loops that ban allocation because cudaMalloc
  * may synchronize the device; hosts that only hand the library pre-sized
- * buffers).  It runs the same three chunked phases as LRSCAN_PATH_CHUNK with
- * the same arguments and results as lrscan_fwd_ex(..., path = chunk,
- * chunk_len), but its scratch (the chunk summaries P and Q) lives in one
- * fixed device array of LRSCAN_NOALLOC_SCRATCH_BYTES that the library owns.
+ * buffers).  It runs the three chunked phases of LRSCAN_PATH_CHUNK with the
+ * arguments of lrscan_fwd_ex(..., path = chunk, chunk_len), but its scratch
+ * (the chunk summaries P and Q) lives in one fixed device array of
+ * LRSCAN_NOALLOC_SCRATCH_BYTES that the library owns.
+ *   - It always uses the flat chunk prefix (one warp per lane walks all the
+ *     lane's chunk maps).  Where the regular chunked call picks the grouped
+ *     prefix (many chunks per lane, few lanes) the two compose the maps in a
+ *     different order, so their results can differ by rounding (both stay
+ *     within the scan's tolerances of the sequential definition), and long
+ *     sequences on few lanes run slower here.
  *   - Every GPU that loads the library holds that array until the process
  *     exits.
  *   - A problem needs 2 * B * ceil(T / chunk_len) * D * 4 bytes of it (each
@@ -449,8 +470,10 @@ int lrscan_version(void);
  *     wrong results.  Calls on one stream are safe.  Nothing has to be cleared
  *     between calls: each call writes all the scratch it reads.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture begins.
+ *     per device, with that device current).  With CUDA's lazy module
+ *     loading that lookup may load the library's device code and reserve the
+ *     array's memory at that moment.  So make one warm-up call on each device
+ *     outside any allocator callback, before any stream capture begins.
  *   - a, b, out, last, sizes and dtype as in lrscan_fwd; chunk_len 16, 32 or
  *     64 (0 means 64); stream is a cudaStream_t (NULL = legacy default stream).
  */

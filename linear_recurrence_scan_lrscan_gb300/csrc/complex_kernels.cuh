@@ -20,19 +20,29 @@
 // memory into registers first, so all those loads issue before the dependent
 // chain (and before the chunk's global stores, which the compiler cannot
 // reorder them across).
+//
+// EXT instantiations add the carried state and segment resets (CStateArgs,
+// triton_training_scan.py, _samu_tiled_serial_forward / _backward): the
+// forward starts from h0 and zeroes a_t where a segment starts; the backward
+// starts from grad_last (entering step T-1 through a'_T = 1), zeroes
+// conj(a'_{t+1}) where step t+1 starts a segment, writes grad_a = +0 where
+// step t starts one, reads h0 as h_{-1} and writes grad_h0 = conj(a'_0) g_0.
+// Each warp turns the segment positions of its rows into bit masks with one
+// ballot per window (loaded one window ahead).  EXT = false compiles all of
+// it out.
 #pragma once
 
 #include "window_kernels.cuh"
 
 namespace lrscan {
 
-template <class C, int CH>
+template <class C, int CH, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                 const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
                 typename C::St *__restrict__ out_r, typename C::St *__restrict__ out_i,
                 float *__restrict__ last_r, float *__restrict__ last_i, const __grid_constant__ WinGeom geom,
-                DevStatus *status, uint64_t timeout_ns) {
+                DevStatus *status, uint64_t timeout_ns, const __grid_constant__ CStateArgs sx) {
     static_assert(C::SEQ && C::NIN == 4, "complex forward: sequential shape, four input planes");
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
@@ -66,8 +76,31 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
     bool failed = false;
     int stage = 0, use = 0;
     const int off = threadIdx.x * V;
+    // EXT: bit j of rbits is a reset at row j of the current window (lane l
+    // holds the position of row l, one window ahead)
+    static_assert(!EXT || L <= 32, "one ballot covers a window's rows");
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
+    int32_t pos_next = 1;
+    if constexpr (EXT) {
+        if (lane_ok) {
+            const size_t hs = static_cast<size_t>(brow) * D + d;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                hr[v] = sx.h0_r != nullptr ? sx.h0_r[hs + v] : 0.0f;
+                hi[v] = sx.h0_i != nullptr ? sx.h0_i[hs + v] : 0.0f;
+            }
+        }
+        pos_next = seg.at(lane < L ? lane : -1);
+    }
     for (int k = 0; k < sm.nwin; ++k) {
-        if (!mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull)) { failed = true; break; }
+        uint32_t rbits = 0;
+        if constexpr (EXT) {
+            rbits = __ballot_sync(0xffffffffu, pos_next == 0);
+            pos_next = seg.at(lane < L ? (k + 1) * sm.W + lane : -1);
+        }
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if constexpr (EXT) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
+        if (!ok) { failed = true; break; }
         const St *tar = sm.tile<C>(stage, 0) + off;
         const St *tai = sm.tile<C>(stage, 1) + off;
         const St *tbr = sm.tile<C>(stage, 2) + off;
@@ -75,8 +108,15 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
         const int rbase = k * sm.W;
         const int n = min(T - rbase, L);
         const size_t o = (row0 + rbase) * D + d;
-        auto compute = [&](int j, const float (&xr)[V], const float (&xi)[V], const float (&yr)[V],
-                           const float (&yi)[V]) {
+        // MASK: a'_t = 0 on the window's reset rows (warp-uniform choice)
+        auto compute = [&](int j, float (&xr)[V], float (&xi)[V], const float (&yr)[V], const float (&yi)[V],
+                           bool masked) {
+            if (EXT && masked) {
+                if ((rbits >> j) & 1u) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) xr[v] = xi[v] = 0.0f;
+                }
+            }
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const float nr = __fmaf_rn(xr[v], hr[v], __fmaf_rn(-xi[v], hi[v], yr[v]));
@@ -89,38 +129,42 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
                 store_lanes<St, V>(out_i + o + static_cast<size_t>(j) * D, hi);
             }
         };
-        if (n == L) {
-            using Raw = typename RawOf<St, V>::T;
+        auto rows = [&](bool masked) {
+            if (n == L) {
+                using Raw = typename RawOf<St, V>::T;
 #pragma unroll
-            for (int j0 = 0; j0 < L; j0 += CH) {
-                Raw r0[CH], r1[CH], r2[CH], r3[CH];
+                for (int j0 = 0; j0 < L; j0 += CH) {
+                    Raw r0[CH], r1[CH], r2[CH], r3[CH];
 #pragma unroll
-                for (int j = 0; j < CH; ++j) {
-                    r0[j] = load_raw<St, V>(tar + (j0 + j) * DT);
-                    r1[j] = load_raw<St, V>(tai + (j0 + j) * DT);
-                    r2[j] = load_raw<St, V>(tbr + (j0 + j) * DT);
-                    r3[j] = load_raw<St, V>(tbi + (j0 + j) * DT);
+                    for (int j = 0; j < CH; ++j) {
+                        r0[j] = load_raw<St, V>(tar + (j0 + j) * DT);
+                        r1[j] = load_raw<St, V>(tai + (j0 + j) * DT);
+                        r2[j] = load_raw<St, V>(tbr + (j0 + j) * DT);
+                        r3[j] = load_raw<St, V>(tbi + (j0 + j) * DT);
+                    }
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        float xr[V], xi[V], yr[V], yi[V];
+                        widen_raw(r0[j], xr);
+                        widen_raw(r1[j], xi);
+                        widen_raw(r2[j], yr);
+                        widen_raw(r3[j], yi);
+                        compute(j0 + j, xr, xi, yr, yi, masked);
+                    }
                 }
-#pragma unroll
-                for (int j = 0; j < CH; ++j) {
+            } else {
+                for (int j = 0; j < n; ++j) {
                     float xr[V], xi[V], yr[V], yi[V];
-                    widen_raw(r0[j], xr);
-                    widen_raw(r1[j], xi);
-                    widen_raw(r2[j], yr);
-                    widen_raw(r3[j], yi);
-                    compute(j0 + j, xr, xi, yr, yi);
+                    unpack_lanes<St, V>(tar + j * DT, xr);
+                    unpack_lanes<St, V>(tai + j * DT, xi);
+                    unpack_lanes<St, V>(tbr + j * DT, yr);
+                    unpack_lanes<St, V>(tbi + j * DT, yi);
+                    compute(j, xr, xi, yr, yi, masked);
                 }
             }
-        } else {
-            for (int j = 0; j < n; ++j) {
-                float xr[V], xi[V], yr[V], yi[V];
-                unpack_lanes<St, V>(tar + j * DT, xr);
-                unpack_lanes<St, V>(tai + j * DT, xi);
-                unpack_lanes<St, V>(tbr + j * DT, yr);
-                unpack_lanes<St, V>(tbi + j * DT, yi);
-                compute(j, xr, xi, yr, yi);
-            }
-        }
+        };
+        if (EXT && rbits != 0) rows(true);
+        else rows(false);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty_bar(stage));
         if (++stage == sm.nstage) { stage = 0; ++use; }
@@ -134,14 +178,32 @@ cwin_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
     }
 }
 
-template <class C, int CH>
+// grad_h0 = conj(a'_0) * g_0 for V lanes (+0 where step 0 starts a segment),
+// in the oracle's order: (fma(ar, gr, ai*gi), fma(ar, gi, -(ai*gr))).
+template <typename St, int V>
+__device__ __forceinline__ void store_cgrad_h0(const CStateArgs &sx, bool reset0, size_t a_off, size_t hs,
+                                               const float (&gr)[V], const float (&gi)[V]) {
+    float ar[V], ai[V];
+    load_lanes_global<St, V>(static_cast<const St *>(sx.ar) + a_off, ar);
+    load_lanes_global<St, V>(static_cast<const St *>(sx.ai) + a_off, ai);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const float hr = reset0 ? 0.0f : __fmaf_rn(ar[v], gr[v], __fmul_rn(ai[v], gi[v]));
+        const float hi = reset0 ? 0.0f : __fmaf_rn(ar[v], gi[v], -__fmul_rn(ai[v], gr[v]));
+        if (sx.gh0_r != nullptr) sx.gh0_r[hs + v] = hr;
+        if (sx.gh0_i != nullptr) sx.gh0_i[hs + v] = hi;
+    }
+}
+
+template <class C, int CH, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                 const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
                 const __grid_constant__ CUtensorMap tm_gr, const __grid_constant__ CUtensorMap tm_gi,
                 typename C::St *__restrict__ grad_ar, typename C::St *__restrict__ grad_ai,
                 typename C::St *__restrict__ grad_br, typename C::St *__restrict__ grad_bi,
-                const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+                const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns,
+                const __grid_constant__ CStateArgs sx) {
     static_assert(C::SEQ && C::NIN == 6, "complex backward: sequential shape, six input planes");
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
@@ -178,8 +240,42 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
     for (int v = 0; v < V; ++v) gr[v] = gi[v] = 0.0f;
     int stage = 0, use = 0;
     const int off = threadIdx.x * V;
+    // EXT: bit j of r0bits / r1bits is a reset at row j / j + 1 of the current
+    // window (positions loaded one window ahead); h_{-1} = h0
+    static_assert(!EXT || L <= 32, "one ballot covers a window's rows");
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
+    const size_t hs = static_cast<size_t>(brow) * D + d;
+    int32_t pos0_next = 1, pos1_next = 1;
+    float h0r[V], h0i[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) h0r[v] = h0i[v] = 0.0f;
+    bool failed = false;
+    if constexpr (EXT) {
+        if (lane_ok) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                gr[v] = sx.gl_r != nullptr ? sx.gl_r[hs + v] : 0.0f;
+                gi[v] = sx.gl_i != nullptr ? sx.gl_i[hs + v] : 0.0f;
+                h0r[v] = sx.h0_r != nullptr ? sx.h0_r[hs + v] : 0.0f;
+                h0i[v] = sx.h0_i != nullptr ? sx.h0_i[hs + v] : 0.0f;
+            }
+        }
+        const int wb0 = (nwin - 1) * sm.W + lane;
+        pos0_next = seg.at(lane < L ? wb0 : -1);
+        pos1_next = seg.at(lane < L ? wb0 + 1 : -1);
+    }
     for (int k = 0; k < nwin; ++k) {
-        if (!mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull)) break;
+        uint32_t r0bits = 0, r1bits = 0;
+        if constexpr (EXT) {
+            r0bits = __ballot_sync(0xffffffffu, pos0_next == 0);
+            r1bits = __ballot_sync(0xffffffffu, pos1_next == 0);
+            const int wb = (nwin - 2 - k) * sm.W + lane;
+            pos0_next = seg.at(lane < L ? wb : -1);
+            pos1_next = seg.at(lane < L ? wb + 1 : -1);
+        }
+        bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
+        if constexpr (EXT) ok = __all_sync(0xffffffffu, ok);  // keep the warp's ballots converged
+        if (!ok) { failed = true; break; }
         const St *tar = sm.tile<C>(stage, 0) + off;  // a_{t+1}
         const St *tai = sm.tile<C>(stage, 1) + off;
         const St *tpr = sm.tile<C>(stage, 2) + off;  // h_{t-1}
@@ -189,8 +285,22 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
         const int wbase = (nwin - 1 - k) * sm.W;
         const int n = min(T - wbase, L);
         const size_t o = (row0 + wbase) * D + d;
-        auto compute = [&](int j, const float (&xr)[V], const float (&xi)[V], const float (&pr)[V],
-                           const float (&pi)[V], const float (&yr)[V], const float (&yi)[V]) {
+        // SPECIAL (EXT, warp-uniform): this window holds a reset, step T-1 or step 0
+        auto compute = [&](int j, float (&xr)[V], float (&xi)[V], float (&pr)[V], float (&pi)[V],
+                           const float (&yr)[V], const float (&yi)[V], bool special) {
+            if (EXT && special) {
+                // conj(a'_{t+1}): 1 at step T-1 (grad_last enters), 0 where step t+1 starts a segment
+                const bool one = k == 0 && j == n - 1;
+                const bool zero = (r1bits >> j) & 1u;
+                const bool first = wbase + j == 0;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    xr[v] = one ? 1.0f : (zero ? 0.0f : xr[v]);
+                    xi[v] = one ? 0.0f : (zero ? 0.0f : xi[v]);
+                    pr[v] = first ? h0r[v] : pr[v];
+                    pi[v] = first ? h0i[v] : pi[v];
+                }
+            }
             float far_[V], fai[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) {
@@ -201,6 +311,12 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
                 far_[v] = __fmaf_rn(gr[v], pr[v], __fmul_rn(gi[v], pi[v]));
                 fai[v] = __fmaf_rn(gi[v], pr[v], -__fmul_rn(gr[v], pi[v]));
             }
+            if (EXT && special) {
+                if ((r0bits >> j) & 1u) {  // a_t unused at a segment start
+#pragma unroll
+                    for (int v = 0; v < V; ++v) far_[v] = fai[v] = 0.0f;
+                }
+            }
             if (lane_ok) {
                 const size_t oj = o + static_cast<size_t>(j) * D;
                 store_lanes<St, V>(grad_br + oj, gr);
@@ -209,49 +325,58 @@ cwin_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant
                 store_lanes<St, V>(grad_ai + oj, fai);
             }
         };
-        if (n == L) {
-            using Raw = typename RawOf<St, V>::T;
+        auto rows = [&](bool special) {
+            if (n == L) {
+                using Raw = typename RawOf<St, V>::T;
 #pragma unroll
-            for (int j1 = L; j1 > 0; j1 -= CH) {  // rows j1-CH .. j1-1, last first
-                Raw r[6][CH];
+                for (int j1 = L; j1 > 0; j1 -= CH) {  // rows j1-CH .. j1-1, last first
+                    Raw r[6][CH];
 #pragma unroll
-                for (int j = 0; j < CH; ++j) {
-                    const int row = (j1 - CH + j) * DT;
-                    r[0][j] = load_raw<St, V>(tar + row);
-                    r[1][j] = load_raw<St, V>(tai + row);
-                    r[2][j] = load_raw<St, V>(tpr + row);
-                    r[3][j] = load_raw<St, V>(tpi + row);
-                    r[4][j] = load_raw<St, V>(tgr + row);
-                    r[5][j] = load_raw<St, V>(tgi + row);
+                    for (int j = 0; j < CH; ++j) {
+                        const int row = (j1 - CH + j) * DT;
+                        r[0][j] = load_raw<St, V>(tar + row);
+                        r[1][j] = load_raw<St, V>(tai + row);
+                        r[2][j] = load_raw<St, V>(tpr + row);
+                        r[3][j] = load_raw<St, V>(tpi + row);
+                        r[4][j] = load_raw<St, V>(tgr + row);
+                        r[5][j] = load_raw<St, V>(tgi + row);
+                    }
+#pragma unroll
+                    for (int j = CH - 1; j >= 0; --j) {
+                        float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V];
+                        widen_raw(r[0][j], xr);
+                        widen_raw(r[1][j], xi);
+                        widen_raw(r[2][j], pr);
+                        widen_raw(r[3][j], pi);
+                        widen_raw(r[4][j], yr);
+                        widen_raw(r[5][j], yi);
+                        compute(j1 - CH + j, xr, xi, pr, pi, yr, yi, special);
+                    }
                 }
-#pragma unroll
-                for (int j = CH - 1; j >= 0; --j) {
+            } else {
+                for (int j = n - 1; j >= 0; --j) {
                     float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V];
-                    widen_raw(r[0][j], xr);
-                    widen_raw(r[1][j], xi);
-                    widen_raw(r[2][j], pr);
-                    widen_raw(r[3][j], pi);
-                    widen_raw(r[4][j], yr);
-                    widen_raw(r[5][j], yi);
-                    compute(j1 - CH + j, xr, xi, pr, pi, yr, yi);
+                    unpack_lanes<St, V>(tar + j * DT, xr);
+                    unpack_lanes<St, V>(tai + j * DT, xi);
+                    unpack_lanes<St, V>(tpr + j * DT, pr);
+                    unpack_lanes<St, V>(tpi + j * DT, pi);
+                    unpack_lanes<St, V>(tgr + j * DT, yr);
+                    unpack_lanes<St, V>(tgi + j * DT, yi);
+                    compute(j, xr, xi, pr, pi, yr, yi, special);
                 }
             }
-        } else {
-            for (int j = n - 1; j >= 0; --j) {
-                float xr[V], xi[V], pr[V], pi[V], yr[V], yi[V];
-                unpack_lanes<St, V>(tar + j * DT, xr);
-                unpack_lanes<St, V>(tai + j * DT, xi);
-                unpack_lanes<St, V>(tpr + j * DT, pr);
-                unpack_lanes<St, V>(tpi + j * DT, pi);
-                unpack_lanes<St, V>(tgr + j * DT, yr);
-                unpack_lanes<St, V>(tgi + j * DT, yi);
-                compute(j, xr, xi, pr, pi, yr, yi);
-            }
-        }
+        };
+        if (EXT && ((r0bits | r1bits) != 0 || k == 0 || wbase == 0)) rows(true);
+        else rows(false);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty_bar(stage));
         if (++stage == sm.nstage) { stage = 0; ++use; }
     }
+    if constexpr (EXT) {
+        if (!failed && lane_ok && (sx.gh0_r != nullptr || sx.gh0_i != nullptr))
+            store_cgrad_h0<St, V>(sx, seg.at(0) == 0, row0 * D + d, hs, gr, gi);
+    }
+    (void)failed;
 }
 
 // ---------------------------------------------------------------------------
@@ -278,13 +403,13 @@ __device__ __forceinline__ void cmul_add(float xr, float xi, float hr, float hi,
     ni = __fmaf_rn(xi, hr, __fmaf_rn(xr, hi, bi));
 }
 
-template <class C>
+template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                  const __grid_constant__ CUtensorMap tm_br, const __grid_constant__ CUtensorMap tm_bi,
                  const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
                  float *__restrict__ last_r, float *__restrict__ last_i, const __grid_constant__ WinGeom geom,
-                 DevStatus *status, uint64_t timeout_ns) {
+                 DevStatus *status, uint64_t timeout_ns, const __grid_constant__ CStateArgs sx) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 4, "windowed complex forward: lane-scan shape, four planes");
     using St = typename C::St;
     constexpr int V = C::V, L = C::L, DT = C::DT, G = C::G;
@@ -324,9 +449,29 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     const CUtensorMap *const omaps[2] = {&tm_or, &tm_oi};
     const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     int replayed = 0;
+    // EXT: this warp's rows start at window row wrow; bit j of rbits is a
+    // reset at row s*L + j of the current window (positions one window ahead)
+    static_assert(!EXT || (G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + static_cast<size_t>(brow) * T : nullptr) : nullptr, T};
+    const int wrow = ((threadIdx.x & ~31u) / G) * L;
+    int32_t pos_next = 1;
+    if constexpr (EXT) {
+        if (static_cast<int>(threadIdx.x) < DT) {
+            const int ch = lane_channel<C>(d0, threadIdx.x);
+            const size_t hs = static_cast<size_t>(brow) * D + ch;
+            cr = (ch < D && sx.h0_r != nullptr) ? sx.h0_r[hs] : 0.0f;
+            ci = (ch < D && sx.h0_i != nullptr) ? sx.h0_i[hs] : 0.0f;
+        }
+        pos_next = seg.at(wrow + lane);
+    }
     for (int k = 0; k < sm.nwin; ++k) {
         const int rbase = k * sm.W + s * L;
         const int n = min(max(T - rbase, 0), L);
+        uint32_t rbits = 0;
+        if constexpr (EXT) {
+            rbits = __ballot_sync(0xffffffffu, pos_next == 0) >> (s * L - wrow);
+            pos_next = seg.at((k + 1) * sm.W + wrow + lane);
+        }
         float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
         if (ok) {
@@ -342,6 +487,20 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
         if (++stage == sm.nstage) { stage = 0; ++use; }
+        if constexpr (EXT) {
+            if (rbits != 0) {
+                // a'_t = 0 where step t starts a segment
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    const bool z = (rbits >> j) & 1u;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        xr[j][v] = z ? 0.0f : xr[j][v];
+                        xi[j][v] = z ? 0.0f : xi[j][v];
+                    }
+                }
+            }
+        }
         if (n < L) {
             // tail sub-chunk: steps past T become exact identity steps (a = 1, b = 0)
 #pragma unroll
@@ -456,14 +615,15 @@ __device__ __forceinline__ void cmulc_add(float xr, float xi, float hr, float hi
 // (one buffer per plane) and written by bulk tensor stores, which clip rows
 // past T and lanes past D.  Rows past T are identity steps (a = 1,
 // grad_out = 0); a_T is the zero fill past the end.
-template <class C>
+template <class C, bool EXT>
 __global__ void __launch_bounds__(C::MAXT, C::MINB)
 cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constant__ CUtensorMap tm_ai,
                  const __grid_constant__ CUtensorMap tm_or, const __grid_constant__ CUtensorMap tm_oi,
                  const __grid_constant__ CUtensorMap tm_gr, const __grid_constant__ CUtensorMap tm_gi,
                  const __grid_constant__ CUtensorMap tm_gar, const __grid_constant__ CUtensorMap tm_gai,
                  const __grid_constant__ CUtensorMap tm_gbr, const __grid_constant__ CUtensorMap tm_gbi,
-                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns) {
+                 const __grid_constant__ WinGeom geom, DevStatus *status, uint64_t timeout_ns,
+                 const __grid_constant__ CStateArgs sx) {
     static_assert(!C::SEQ && !C::PT && C::NIN == 6, "windowed complex backward: lane-scan shape, six planes");
     using St = typename C::St;
     using Raw = typename RawOf<St, C::V>::T;
@@ -505,10 +665,50 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     float cr = 0.0f, ci = 0.0f;  // window-to-window adjoint of lane threadIdx.x (threads < DT)
     int stage = 0, use = 0;
     const int off = (s * L) * DT + lg * V;
+    // EXT: bit j of r0bits / r1bits is a reset at row s*L + j / s*L + j + 1 of
+    // the current window (positions one window ahead); h_{-1} = h0
+    static_assert(!EXT || (G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
+    const int D = geom.D;
+    const int d = d0 + lg * V;
+    const bool lane_ok = d < D;
+    const size_t row0 = static_cast<size_t>(brow) * T;
+    const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
+    const int wrow = ((threadIdx.x & ~31u) / G) * L;
+    int32_t pos0_next = 1, pos1_next = 1;
+    float h0r[V], h0i[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) h0r[v] = h0i[v] = 0.0f;
+    if constexpr (EXT) {
+        if (lane_ok) {
+            const size_t hs = static_cast<size_t>(brow) * D + d;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                h0r[v] = sx.h0_r != nullptr ? sx.h0_r[hs + v] : 0.0f;
+                h0i[v] = sx.h0_i != nullptr ? sx.h0_i[hs + v] : 0.0f;
+            }
+        }
+        if (static_cast<int>(threadIdx.x) < DT) {
+            const int ch = lane_channel<C>(d0, threadIdx.x);
+            const size_t hs = static_cast<size_t>(brow) * D + ch;
+            cr = (ch < D && sx.gl_r != nullptr) ? sx.gl_r[hs] : 0.0f;
+            ci = (ch < D && sx.gl_i != nullptr) ? sx.gl_i[hs] : 0.0f;
+        }
+        const int wb0 = (nwin - 1) * sm.W + wrow + lane;
+        pos0_next = seg.at(wb0);
+        pos1_next = seg.at(wb0 + 1);
+    }
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
         const int rbase = wbase + s * L;
         const int n = min(max(T - rbase, 0), L);
+        uint32_t r0bits = 0, r1bits = 0;
+        if constexpr (EXT) {
+            r0bits = __ballot_sync(0xffffffffu, pos0_next == 0) >> (s * L - wrow);
+            r1bits = __ballot_sync(0xffffffffu, pos1_next == 0) >> (s * L - wrow);
+            const int wb = (nwin - 2 - k) * sm.W + wrow + lane;
+            pos0_next = seg.at(wb);
+            pos1_next = seg.at(wb + 1);
+        }
         float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
         Raw pr[L], pi[L];
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
@@ -526,14 +726,32 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
         if (++stage == sm.nstage) { stage = 0; ++use; }
-        if (n < L) {
+        // rows from na on take conj(a') = 1: steps past T (identity steps)
+        // and, with the carried state, step T-1 (grad_last enters through a'_T = 1)
+        int na = n;
+        if constexpr (EXT) {
+            if (n > 0 && rbase + n == T) na = n - 1;
+            if (r1bits != 0) {
+                // conj(a'_{t+1}) = 0 where step t+1 starts a segment
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    const bool z = (r1bits >> j) & 1u;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        xr[j][v] = z ? 0.0f : xr[j][v];
+                        xi[j][v] = z ? 0.0f : xi[j][v];
+                    }
+                }
+            }
+        }
+        if (na < L) {
             // rows past T: identity steps (a = 1, grad_out = 0)
 #pragma unroll
             for (int j = 0; j < L; ++j) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    xr[j][v] = j < n ? xr[j][v] : 1.0f;
-                    xi[j][v] = j < n ? xi[j][v] : 0.0f;
+                    xr[j][v] = j < na ? xr[j][v] : 1.0f;
+                    xi[j][v] = j < na ? xi[j][v] : 0.0f;
                     yr[j][v] = j < n ? yr[j][v] : 0.0f;
                     yi[j][v] = j < n ? yi[j][v] : 0.0f;
                 }
@@ -597,6 +815,12 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
             float hr[V], hi[V], far_[V], fai[V];
             widen_raw(pr[j], hr);
             widen_raw(pi[j], hi);
+            if constexpr (EXT) {
+                if (j == 0 && rbase == 0) {  // h_{-1} = h0 (fp32)
+#pragma unroll
+                    for (int v = 0; v < V; ++v) { hr[v] = h0r[v]; hi[v] = h0i[v]; }
+                }
+            }
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 float nr, ni;
@@ -606,6 +830,12 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
                 far_[v] = __fmaf_rn(gr[v], hr[v], __fmul_rn(gi[v], hi[v]));
                 fai[v] = __fmaf_rn(gi[v], hr[v], -__fmul_rn(gr[v], hi[v]));
             }
+            if constexpr (EXT) {
+                if ((r0bits >> j) & 1u) {  // a_t unused at a segment start
+#pragma unroll
+                    for (int v = 0; v < V; ++v) far_[v] = fai[v] = 0.0f;
+                }
+            }
             store_lanes<St, V>(sar + j * DT, far_);
             store_lanes<St, V>(sai + j * DT, fai);
             store_lanes<St, V>(sbr + j * DT, gr);
@@ -613,6 +843,10 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         }
         fence_proxy_async_smem();
         replayed = k + 1;
+        if constexpr (EXT) {
+            if (rbase == 0 && lane_ok && (sx.gh0_r != nullptr || sx.gh0_i != nullptr))
+                store_cgrad_h0<St, V>(sx, seg.at(0) == 0, row0 * D + d, static_cast<size_t>(brow) * D + d, gr, gi);
+        }
     }
     // the last processed window's tiles (not after an abort), then every store
     // complete before the CTA's shared memory goes away

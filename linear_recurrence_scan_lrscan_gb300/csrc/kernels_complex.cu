@@ -1,64 +1,25 @@
-// Instantiations and launchers of the complex scan kernels, and their tile
-// variant table.
+// Instantiations of the complex scan kernels (the EXT ones are in
+// kernels_complex_state.cu), and their tile variant table.
 #include <cstdlib>
 
-#include "complex_kernels.cuh"
-#include "window_launch.cuh"
+#include "complex_launch.cuh"
 
 namespace lrscan {
 
+#define LRSCAN_EXTERN_CSF(SH) extern template int launch_cwin_fwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+#define LRSCAN_EXTERN_CSB(SH) extern template int launch_cwin_bwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+#define LRSCAN_EXTERN_CWF(SH) extern template int launch_cwinw_fwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+#define LRSCAN_EXTERN_CWB(SH) extern template int launch_cwinw_bwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+LRSCAN_CSEQ_FWD_SHAPES(LRSCAN_EXTERN_CSF)
+LRSCAN_CSEQ_BWD_SHAPES(LRSCAN_EXTERN_CSB)
+LRSCAN_CWIN_FWD_SHAPES(LRSCAN_EXTERN_CWF)
+LRSCAN_CWIN_BWD_SHAPES(LRSCAN_EXTERN_CWB)
+#undef LRSCAN_EXTERN_CSF
+#undef LRSCAN_EXTERN_CSB
+#undef LRSCAN_EXTERN_CWF
+#undef LRSCAN_EXTERN_CWB
+
 namespace {
-
-// rows staged in registers per step of a full window
-template <class C> constexpr int kStageRowsFwd = C::L < 16 ? C::L : 16;
-template <class C> constexpr int kStageRowsBwd = C::L < 8 ? C::L : 8;
-
-template <class C>
-int launch_cwin_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = cwin_fwd_kernel<C, kStageRowsFwd<C>>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    using St = typename C::St;
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
-                                     static_cast<St *>(L.out0), static_cast<St *>(L.out1), L.last, L.last_i, g,
-                                     L.status, L.timeout_ns);
-    return e == cudaSuccess ? 0 : -1;
-}
-
-template <class C>
-int launch_cwinw_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = cwinw_fwd_kernel<C>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_cwin_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
-                                     win_out_smem(g, 2), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
-                                     *L.maps[4], *L.maps[5], L.last, L.last_i, g, L.status, L.timeout_ns);
-    return e == cudaSuccess ? 0 : -1;
-}
-
-template <class C>
-int launch_cwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = cwin_bwd_kernel<C, kStageRowsBwd<C>>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(1, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    using St = typename C::St;
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads), g.smem_bytes,
-                                     L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3], *L.maps[4],
-                                     *L.maps[5], static_cast<St *>(L.out0), static_cast<St *>(L.out1),
-                                     static_cast<St *>(L.out2), static_cast<St *>(L.out3), g, L.status,
-                                     L.timeout_ns);
-    return e == cudaSuccess ? 0 : -1;
-}
 
 template <class C, bool FWD>
 WinDirCfg cdir_cfg(int nstage) {
@@ -70,30 +31,20 @@ WinDirCfg cdir_cfg(int nstage) {
     d.v = C::V;
     d.l = C::L;
     d.s = 1;
+    d.exact = 1;  // the sequential nested-fma order
     d.w = g.W;
     d.nstage = nstage;
     d.threads = C::G + 32;
     d.smem = g.smem_bytes;
     d.stage_bytes = g.stage_bytes;
-    if constexpr (FWD) d.launch = &launch_cwin_fwd<C>;
-    else d.launch = &launch_cwin_bwd<C>;
-    d.launch_state = nullptr;
+    if constexpr (FWD) {
+        d.launch = &launch_cwin_fwd<C, false>;
+        d.launch_state = &launch_cwin_fwd<C, true>;
+    } else {
+        d.launch = &launch_cwin_bwd<C, false>;
+        d.launch_state = &launch_cwin_bwd<C, true>;
+    }
     return d;
-}
-
-template <class C>
-int launch_cwinw_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = cwinw_bwd_kernel<C>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_cwin_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
-                                     win_out_smem(g, 4, 1), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
-                                     *L.maps[4], *L.maps[5], *L.maps[6], *L.maps[7], *L.maps[8], *L.maps[9], g,
-                                     L.status, L.timeout_ns);
-    return e == cudaSuccess ? 0 : -1;
 }
 
 // Windowed complex tiles: S sub-chunks of L rows, lane scan.  Forward: a, b
@@ -115,30 +66,15 @@ WinDirCfg cwdir_cfg(int S, int nstage) {
     d.threads = S * C::G + 32;
     d.smem = FWD ? win_out_smem(g, 2) : win_out_smem(g, 4, 1);  // plus the output staging
     d.stage_bytes = g.stage_bytes;
-    if constexpr (FWD) d.launch = &launch_cwinw_fwd<C>;
-    else d.launch = &launch_cwinw_bwd<C>;
+    if constexpr (FWD) {
+        d.launch = &launch_cwinw_fwd<C, false>;
+        d.launch_state = &launch_cwinw_fwd<C, true>;
+    } else {
+        d.launch = &launch_cwinw_bwd<C, false>;
+        d.launch_state = &launch_cwinw_bwd<C, true>;
+    }
     return d;
 }
-
-// WinShape<St, DT, V, L, NIN, MAXT, MINB, SEQ>
-using CWF_BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 4, 288, 2, false>;
-using CWF_BF_32_2_8 = WinShape<bf16_t, 32, 2, 8, 4, 288, 2, false>;
-using CWF_FF_32_1_8 = WinShape<float, 32, 1, 8, 4, 288, 2, false>;
-// 4-row sub-chunks, five CTAs per SM: every CTA of a 640-tile launch resident
-using CWF_BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 4, 160, 5, false>;
-using CWB_BF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 6, 160, 5, false>;
-using CBF_64_1_32 = WinShape<bf16_t, 64, 1, 32, 4, 96, 1, true>;
-using CBB_64_1_32 = WinShape<bf16_t, 64, 1, 32, 6, 96, 1, true>;
-using CBF_64_2_32 = WinShape<bf16_t, 64, 2, 32, 4, 64, 1, true>;
-using CBB_64_2_16 = WinShape<bf16_t, 64, 2, 16, 6, 64, 1, true>;
-using CBF_32_1_32 = WinShape<bf16_t, 32, 1, 32, 4, 64, 1, true>;
-using CBB_32_1_32 = WinShape<bf16_t, 32, 1, 32, 6, 64, 1, true>;
-using CFF_32_1_32 = WinShape<float, 32, 1, 32, 4, 64, 1, true>;
-using CFB_32_1_32 = WinShape<float, 32, 1, 32, 6, 64, 1, true>;
-using CFF_64_2_16 = WinShape<float, 64, 2, 16, 4, 64, 1, true>;
-using CFB_64_2_16 = WinShape<float, 64, 2, 16, 6, 64, 1, true>;
-using CFF_64_1_16 = WinShape<float, 64, 1, 16, 4, 96, 1, true>;
-using CFB_64_1_16 = WinShape<float, 64, 1, 16, 6, 96, 1, true>;
 
 #define F(SH, N) cdir_cfg<SH, true>(N)
 #define B(SH, N) cdir_cfg<SH, false>(N)

@@ -13,6 +13,12 @@ LRSCAN_WIN_FWD_SHAPES(LRSCAN_EXTERN_FWD)
 LRSCAN_WIN_BWD_SHAPES(LRSCAN_EXTERN_BWD)
 #undef LRSCAN_EXTERN_FWD
 #undef LRSCAN_EXTERN_BWD
+#define LRSCAN_EXTERN_XF(SH) extern template int launch_xwp_fwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+#define LRSCAN_EXTERN_XB(SH) extern template int launch_xwp_bwd<SH, true>(const WinLaunch &, const WinDirCfg &);
+LRSCAN_XWP_FWD_SHAPES(LRSCAN_EXTERN_XF)
+LRSCAN_XWP_BWD_SHAPES(LRSCAN_EXTERN_XB)
+#undef LRSCAN_EXTERN_XF
+#undef LRSCAN_EXTERN_XB
 
 namespace {
 
@@ -26,6 +32,7 @@ WinDirCfg dir_cfg(int S, int nstage) {
     d.l = C::L;
     d.s = S;
     d.lane_scan = (!C::SEQ && !C::PT) ? 1 : 0;
+    d.exact = (C::SEQ || C::EX) ? 1 : 0;
     d.w = g.W;
     d.nstage = nstage;
     d.threads = S * C::G + 32;
@@ -43,8 +50,39 @@ WinDirCfg dir_cfg(int S, int nstage) {
     return d;
 }
 
+// Pipelined exact tiles: S * G replay threads plus DT walker threads.
+template <class C, bool FWD>
+WinDirCfg xdir_cfg(int S, int nstage) {
+    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
+    if (!C::EX || S > C::SMAX || S * C::G + C::DT > C::MAXT) std::abort();  // table error
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = S;
+    d.lane_scan = 1;
+    d.exact = 1;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = S * C::G + C::DT;
+    d.smem = win_out_smem(g, FWD ? 1 : 2, 3);  // plus three output staging buffers
+    d.stage_bytes = g.stage_bytes;
+    if constexpr (FWD) {
+        static_assert(C::NIN == 2, "forward tiles: a, b");
+        d.launch = &launch_xwp_fwd<C, false>;
+        d.launch_state = &launch_xwp_fwd<C, true>;
+    } else {
+        static_assert(C::NIN == 3, "backward tiles: a, out, grad_out");
+        d.launch = &launch_xwp_bwd<C, false>;
+        d.launch_state = &launch_xwp_bwd<C, true>;
+    }
+    return d;
+}
+
 #define F(SH, S, N) dir_cfg<SH, true>(S, N)
 #define B(SH, S, N) dir_cfg<SH, false>(S, N)
+#define XF(SH, S, N) xdir_cfg<SH, true>(S, N)
+#define XB(SH, S, N) xdir_cfg<SH, false>(S, N)
 
 
 const WinVariant kSeqBF16[] = {
@@ -54,6 +92,10 @@ const WinVariant kSeqBF16[] = {
     {"seq_bf16_d128_v4", F(SBF_128_4_32, 1, 6), B(SBB_128_4_16, 1, 6)},
     {"seq_bf16_d32_v1", F(SBF_32_1_32, 1, 8), B(SBB_32_1_32, 1, 6)},
     {"seq_bf16_d64_v1", F(SBF_64_1_32, 1, 8), B(SBB_64_1_32, 1, 6)},
+    // shallower rings: four 128-lane CTAs resident per SM
+    {"seq_bf16_d128_v4_n3", F(SBF_128_4_32, 1, 3), B(SBB_128_4_16, 1, 3)},
+    {"seq_bf16_d128_n2", F(SBF_128_2_32, 1, 2), B(SBB_128_2_32, 1, 2)},
+    {"seq_bf16_d128_n3", F(SBF_128_2_32, 1, 3), B(SBB_128_2_32, 1, 3)},
 };
 const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s16", F(BF_32_2_8, 16, 3), B(BB_32_2_8, 16, 4)},
@@ -67,6 +109,15 @@ const WinVariant kWinBF16[] = {
     {"win_bf16_d32_s4_m8_n2", F(BF_32_2_8_M8, 4, 2), B(BB_32_2_8_M8, 4, 2)},
     {"win_bf16_d32_l4_s12_m5", F(BF_32_2_4_M5, 12, 2), B(BB_32_2_4_M5, 12, 2)},
     {"win_bf16_d32_l4_s12_m5_n3", F(BF_32_2_4_M5, 12, 3), B(BB_32_2_4_M5, 12, 3)},
+    // exact walk (bit-identical to the sequential scan)
+    {"xwin_bf16_d32_s8_m5_n2", F(XBF_32_2_8_M5, 8, 2), B(XBB_32_2_8_M5, 8, 2)},
+    {"xwin_bf16_d32_l4_s12_m5", F(XBF_32_2_4_M5, 12, 2), B(XBB_32_2_4_M5, 12, 2)},
+    {"xwin_bf16_d32_l16_s8", F(XWBF_32_2_16, 8, 4), B(XWBB_32_2_16, 8, 4)},
+    {"xwin_bf16_d32_s8_m5_n3", F(XBF_32_2_8_M5, 8, 3), B(XBB_32_2_8_M5, 8, 3)},
+    // pipelined exact walk (walker warps beside the replay threads)
+    {"xwp_bf16_d32_s8_m5_n2", XF(XBF_32_2_8_M5, 8, 2), XB(XBB_32_2_4_M5, 12, 2)},
+    {"xwp_bf16_d32_s8_m5_n3", XF(XBF_32_2_8_M5, 8, 3), XB(XBB_32_2_8_M5, 8, 2)},
+    {"xwp_bf16_d32_l16_s8", XF(XWBF_32_2_16, 8, 4), XB(XWBB_32_2_16, 8, 4)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},
@@ -82,10 +133,18 @@ const WinVariant kWinF32[] = {
     {"win_f32_d64_s8", F(FF_64_2_8, 8, 4), B(FB_64_2_8, 8, 3)},
     {"win_f32_d32_s8_pt", F(PF_32_1_8, 8, 8), B(PFB_32_1_8, 8, 6)},
     {"win_f32_d32_s31", F(FF_32_1_8_X, 31, 2), B(FB_32_1_8, 16, 3)},
+    // exact walk (bit-identical to the sequential scan)
+    {"xwin_f32_d64_s8", F(XFF_64_2_8, 8, 4), B(XFB_64_2_8, 8, 3)},
+    {"xwin_f32_d32_s16", F(XFF_32_1_8, 16, 4), B(XFB_32_1_8, 16, 3)},
+    // pipelined exact walk
+    {"xwp_f32_d64_s8", XF(XPFF_64_2_8, 8, 3), XB(XPFB_64_2_8, 8, 2)},
+    {"xwp_f32_d32_s16", XF(XFF_32_1_8, 16, 4), XB(XFB_32_1_8, 16, 3)},
 };
 
 #undef F
 #undef B
+#undef XF
+#undef XB
 
 
 }  // namespace

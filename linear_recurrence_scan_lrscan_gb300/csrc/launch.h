@@ -51,6 +51,7 @@ struct WinLaunch {
     cudaStream_t stream;
     int device;
     StateArgs sx;  // carried state and resets (used by the EXT launchers only)
+    CStateArgs csx;  // the complex scan's carried state (complex EXT launchers)
     // generated-decay scan: per-token / per-lane parameters, backward partial
     // sums, and the plain kernels' tensor inputs (in0 = b or out, in1 = grad_out)
     const float *eta, *nu_log;
@@ -67,6 +68,7 @@ struct WinDirCfg {
     int l;           // steps per sub-chunk (registers)
     int s;           // sub-chunks per window
     int lane_scan;   // windowed prefix by lane threads (1) or per thread (0)
+    int exact;       // results bit-identical to the sequential definition (1)
     int w;           // rows per window = s*l
     int nstage;      // pipeline depth
     int threads;     // s*(dt/v) + 32
@@ -128,14 +130,6 @@ int cplain_bwd_launch(const void *const in[6], void *const out[4], int64_t B, in
 // out_i, go_r, go_i}, out = {grad_ar, grad_ai, grad_br, grad_bi}.  maps: P re,
 // P im, Q re, Q im [B, Nc, D] each; gmaps: the grouped prefix's group maps
 // [B, ceil(Nc / kGroupChunks), D] each, or all null (flat prefix).
-// Carried state of a complex scan: h0 and grad_last in, grad_h0 out (re and
-// im fp32 [B, D] each), segment positions int32 [B, T]; all null: none.
-struct CStateArgs {
-    const float *h0_r, *h0_i;
-    const int32_t *seg;
-    const float *gl_r, *gl_i;
-    float *gh0_r, *gh0_i;
-};
 struct CChunkLaunch {
     const void *in[6];
     void *out[4];

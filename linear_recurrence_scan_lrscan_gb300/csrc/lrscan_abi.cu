@@ -238,20 +238,39 @@ struct Pref {
     double max_ctas_per_sm;
 };
 constexpr double kAny = 1e30;
+// Exact tiles come first wherever they hold the rate: the sequential tiles,
+// and the windowed tiles whose lane threads walk the window's rows with the
+// sequential step (xwin_*), reproduce the sequential definition bit for bit.
 // fp32 forward with few lane tiles: one 32-warp CTA per tile (31 sub-chunks
 // of 8 rows): 333.6 us on the long fp32 workload against 372.5 us for 16
 // sub-chunks.
 const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s31", 0.45, kAny}};
-const Pref kPrefF32Bwd[] = {{kPathWindow, "win_f32_d64_s8", 3.0, kAny}, {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
-const Pref kPrefBF16Fwd[] = {{kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
+// fp32 backward with many lane tiles: the exact 64-lane window tile (102.1 us
+// on the padded workload against 100.0 us for the re-associating one and
+// 105.7 us for the fastest sequential tile)
+const Pref kPrefF32Bwd[] = {{kPathWindow, "xwin_f32_d64_s8", 3.0, kAny},
+                            {kPathWindow, "win_f32_d64_s8", 3.0, kAny},
+                            {kPathWindow, "win_f32_d32_s16", 0.45, kAny}};
+// bf16 forward: the sequential 128-lane tile with a three-stage ring (four
+// CTAs resident per SM, so 512 tiles run in one wave) from two CTAs per SM
+// (245.9 us on the near-unit workload, exact, against 241.0 us for the
+// re-associating window tile and 259.2 us for the six-stage four-lane tile,
+// 1.68 waves); fewer lanes: the one-wave window tile (42.1 us on the gated
+// workload against 49.3 us for the fastest sequential tile and 56.0 us for the
+// exact window tile).
+const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d128_n3", 2.0, kAny},
+                             {kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
                              {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
-// bf16 backward up to 5 CTAs per SM: 12 sub-chunks of 4 rows, five CTAs per
-// SM (seven warps each, every CTA of a 640-tile launch resident): fastest
-// alone and in the forward + backward step (111.4 us against 114.0 us with
-// the 16-sub-chunk tile, whose partial last wave at least overlaps the next
-// forward, and 115.2 us with the five-CTA 8-row tile).
-const Pref kPrefBF16Bwd[] = {{kPathWindow, "win_bf16_d32_l4_s12_m5", 0.9, 5.0},
+// bf16 backward: the sequential 128-lane tile with a two-stage ring (four
+// CTAs per SM, one wave) from two CTAs per SM (417.1 us on the near-unit
+// workload, exact, against 404.0 us re-associating and 432.2 us for the
+// four-stage tile); up to 5 CTAs per SM the exact window tile with 8
+// sub-chunks of 8 rows, five CTAs per SM (73.7 us on the gated workload, as
+// fast as the re-associating 12-sub-chunk tile's 73.4 us).
+const Pref kPrefBF16Bwd[] = {{kPathSeq, "seq_bf16_d128_n2", 2.0, kAny},
+                             {kPathWindow, "xwin_bf16_d32_s8_m5_n2", 0.9, 5.0},
+                             {kPathWindow, "win_bf16_d32_l4_s12_m5", 0.9, 5.0},
                              {kPathWindow, "win_bf16_d32_l16_s8", 0.9, kAny},
                              {kPathWindow, "win_bf16_d64_s8", 0.45, kAny}};
 // With carried state / resets: the 16-sub-chunk tiles (80.7 us on the gated
@@ -403,6 +422,7 @@ void fill_info(const Choice &c, lrscan_plan_info *info) {
     info->kernels = c.kernels;
     info->workspace_bytes = c.workspace;
     info->subchunks = 1;
+    info->exact = c.var ? dir_of(*c.var, c.dir).exact : (c.path == kPathPlain ? 1 : 0);
     if (c.var) {
         const WinDirCfg &d = dir_of(*c.var, c.dir);
         info->lanes_per_cta = d.dt;
@@ -725,8 +745,8 @@ size_t cchunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped) {
 int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned16, const lrscan_opts *opts,
                  const Geometry &g, Choice *ch, bool ext = false) {
     const int want = opts ? opts->path : 0;
-    if (ext && want != kPathAuto && want != kPathChunk)
-        return fail(LRSCAN_EINVAL, "the complex scan with carried state runs on the chunked path (path %d)", want);
+    if (ext && want == kPathPlain)
+        return fail(LRSCAN_EINVAL, "the plain complex kernels carry no state (path %d)", want);
     const int force_v = opts ? opts->tile_variant : 0;
     if (want != kPathAuto && want != kPathSeq && want != kPathWindow && want != kPathPlain && want != kPathChunk)
         return fail(LRSCAN_EINVAL, "unknown complex scan path %d", want);
@@ -742,9 +762,12 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         // too few lanes for lane tiles of 32 to give the SMs work (fewer than
         // 0.45 tiles per SM; the plain kernels' bound without alignment) and
         // a long sequence: parallelize over time chunks
+        // With carried state the tiled kernels (EXT instantiations) run as
+        // they would without it; unaligned rows take the chunked kernels,
+        // which carry state at any alignment.
         const long long few = aligned16 ? static_cast<long long>(0.45 * g.sm_count * 32) : 32LL * g.sm_count * 32;
-        if (ext || (B * D < few && T >= 16LL * chunk)) path = kPathChunk;
-        else path = aligned16 ? kPathSeq : kPathPlain;
+        if (B * D < few && T >= 16LL * chunk) path = kPathChunk;
+        else path = aligned16 ? kPathSeq : (ext ? kPathChunk : kPathPlain);
     } else {
         // seq and window both name the tiled variant table (sequential and windowed tiles)
         path = (want == kPathPlain || want == kPathChunk) ? want : kPathSeq;
@@ -843,6 +866,26 @@ int check_cstate(const lrscan_cstate *s, bool bwd, CStateArgs *sx, bool *any) {
     return LRSCAN_OK;
 }
 
+// The complex state of batch rows b0.. of a tiled launch (planes ar / ai:
+// the backward's decays, for grad_h0).
+CStateArgs cstate_slice(const CStateArgs &s, const void *ar, const void *ai, int64_t b0, int64_t T, int64_t D,
+                        size_t es) {
+    CStateArgs x = s;
+    const size_t sd = static_cast<size_t>(b0) * D;
+    auto f = [sd](const float *p) { return p ? p + sd : nullptr; };
+    x.h0_r = f(s.h0_r);
+    x.h0_i = f(s.h0_i);
+    x.gl_r = f(s.gl_r);
+    x.gl_i = f(s.gl_i);
+    x.gh0_r = s.gh0_r ? s.gh0_r + sd : nullptr;
+    x.gh0_i = s.gh0_i ? s.gh0_i + sd : nullptr;
+    x.seg = s.seg ? s.seg + static_cast<size_t>(b0) * T : nullptr;
+    const size_t po = static_cast<size_t>(b0) * T * D * es;
+    x.ar = ar ? static_cast<const char *>(ar) + po : nullptr;
+    x.ai = ai ? static_cast<const char *>(ai) + po : nullptr;
+    return x;
+}
+
 int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, float *last_i, int64_t B, int64_t T,
              int64_t D, int dtype, void *stream, const lrscan_opts *opts, const lrscan_cstate *state = nullptr) {
     t_detail[0] = 0;
@@ -912,7 +955,8 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
         L.timeout_ns = g_timeout_ns.load();
         L.stream = st;
         L.device = dev;
-        if (v.launch(L, v))
+        if (ext) L.csx = cstate_slice(sx, nullptr, nullptr, b0, T, D, es);
+        if ((ext ? v.launch_state : v.launch)(L, v))
             return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
     }
     return LRSCAN_OK;
@@ -983,7 +1027,8 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
         L.timeout_ns = g_timeout_ns.load();
         L.stream = st;
         L.device = dev;
-        if (v.launch(L, v))
+        if (ext) L.csx = cstate_slice(sx, in[0], in[1], b0, T, D, es);
+        if ((ext ? v.launch_state : v.launch)(L, v))
             return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
     }
     return LRSCAN_OK;
@@ -1347,8 +1392,8 @@ int lrscan_cbwd_state(const void *ar, const void *ai, const void *out_r, const v
     return run_cbwd(in, outp, B, T, D, dtype, stream, opts, state);
 }
 
-int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
-                        const lrscan_opts *opts, lrscan_plan_info *info) {
+static int plan_complex_entry(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
+                              const lrscan_opts *opts, lrscan_plan_info *info, bool ext) {
     if (!info || (dir != 0 && dir != 1)) return LRSCAN_EINVAL;
     int rc = check_shape(B, T, D, dtype);
     if (rc) return rc;
@@ -1356,7 +1401,8 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
     if (device_ctx(&ctx) != LRSCAN_OK) ctx = nullptr;
     const bool al = is_aligned16 && (D * esize(dtype)) % 16 == 0;
     Choice ch;
-    if ((rc = plan_complex(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch)))
+    if ((rc = plan_complex(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch,
+                           ext)))
         return rc;
     fill_info(ch, info);
     if (ch.path == kPathChunk) {
@@ -1364,6 +1410,16 @@ int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int
         std::snprintf(info->name, sizeof info->name, "cchunk%d_v%d%s", ch.chunk, ch.vec, ch.vidx == 1 ? "_grouped" : "");
     }
     return LRSCAN_OK;
+}
+
+int lrscan_plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
+                        const lrscan_opts *opts, lrscan_plan_info *info) {
+    return plan_complex_entry(B, T, D, dtype, dir, is_aligned16, opts, info, false);
+}
+
+int lrscan_plan_complex_state(int64_t B, int64_t T, int64_t D, int dtype, int dir, int is_aligned16,
+                              const lrscan_opts *opts, lrscan_plan_info *info) {
+    return plan_complex_entry(B, T, D, dtype, dir, is_aligned16, opts, info, true);
 }
 
 int lrscan_fwd_gated(const float *eta, const float *nu_log, const void *b, void *out, float *last, int64_t B,
@@ -1394,6 +1450,7 @@ int lrscan_plan_gated(int64_t B, int64_t T, int64_t D, int dtype, int dir, int i
     if ((rc = plan_gated(B > 0 ? B : 1, D > 0 ? D : 1, dtype, dir, al, opts, geometry_of(ctx), &ch))) return rc;
     if (dir == 1) ch.workspace = gated_workspace(B > 0 ? B : 1, T > 0 ? T : 1, D > 0 ? D : 1);
     fill_info(ch, info);
+    info->exact = 0;  // generated decays use a fast exponential
     return LRSCAN_OK;
 }
 

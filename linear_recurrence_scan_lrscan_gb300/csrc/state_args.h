@@ -17,4 +17,16 @@ struct StateArgs {
     const void *a;           // the decays [B, T, D] (backward: grad_h0 = a'_0 * g_0)
 };
 
+// Carried state of a complex scan: h0 and grad_last in, grad_h0 out (re and
+// im fp32 [B, D] each), segment positions int32 [B, T]; all null: none.  The
+// tiled backward also reads the decay planes ar / ai [B, T, D] for
+// grad_h0 = conj(a'_0) * g_0.
+struct CStateArgs {
+    const float *h0_r, *h0_i;
+    const int32_t *seg;
+    const float *gl_r, *gl_i;
+    float *gh0_r, *gh0_i;
+    const void *ar, *ai;
+};
+
 }  // namespace lrscan

@@ -51,13 +51,19 @@ namespace lrscan {
 // Compile-time shape.  MAXT / MINB feed __launch_bounds__.  A shape is either
 // sequential (launched with S == 1, rows streamed from shared memory) or
 // windowed (S > 1, each thread's L rows held in registers).
-template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_, bool SEQ_, bool PT_ = false>
+template <typename St_, int DT_, int V_, int L_, int NIN_, int MAXT_, int MINB_, bool SEQ_, bool PT_ = false,
+          bool EX_ = false>
 struct WinShape {
     using St = St_;
     static constexpr bool SEQ = SEQ_;
     // windowed prefix: false = lane threads scan the maps, true = every thread
     // folds the maps before its own sub-chunk
     static constexpr bool PT = PT_;
+    // exact windowed tile: the lane threads walk the window's rows one step at
+    // a time (no sub-chunk maps), so the entry states and every replayed value
+    // are the sequential definition's own
+    static constexpr bool EX = EX_;
+    static_assert(!EX_ || (!SEQ_ && !PT_), "exact walk: a lane-scan windowed shape");
     static constexpr int DT = DT_;    // lanes per CTA
     static constexpr int V = V_;      // lanes per thread
     static constexpr int L = L_;      // steps per sub-chunk (held in registers)
@@ -127,11 +133,17 @@ template <class C> __host__ __device__ constexpr bool win_staged() { return !C::
 // buffers alternate and each store overlaps a window of compute.
 // NB = 1 keeps one buffer per plane: the thread that stores a window must
 // then wait for its reads (bulk_wait_read<0>) before the next replay writes.
+// NB = 3 lets the replay of window k start right after the barrier that
+// issues window k-1's store: the store of k-2, whose buffer window k+1 takes,
+// only has to finish reading before the next barrier.
 template <int NP, class St, int NB = 2>
 struct OutStage {
     St *buf;
     int elems;  // W * DT
-    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((NB == 1 ? 0 : kw & 1) * NP + p) * elems; }
+    __device__ __forceinline__ St *plane(int kw, int p) const {
+        const int b = NB == 1 ? 0 : (NB == 2 ? (kw & 1) : kw % NB);
+        return buf + (b * NP + p) * elems;
+    }
     // bulk tensor stores of processed window kw's planes at (x, y, z), one group
     __device__ __forceinline__ void store(const CUtensorMap *const (&maps)[NP], int kw, int x, int y, int z) const {
 #pragma unroll
@@ -268,6 +280,50 @@ __device__ __forceinline__ float lane_walk(const float2 *pq, float *entry, int S
                 entry[s * DT + i] = c;
                 c = __fmaf_rn(m[j].x, c, m[j].y);
             }
+        }
+    }
+    return c;
+}
+
+// Exact walk of one window (EX tiles).  Lane thread i carries c through the
+// window's rows with the sequential step itself, in order (REVERSE: last row
+// first), and records the value entering each sub-chunk at entry[s * DT + i];
+// the sub-chunk replays then repeat exactly these steps, so every stored
+// value is bit-identical to the sequential scan.  ta / tb are the window's
+// decay and addend tiles (backward: a_{t+1} and grad_out_t), row stride DT;
+// lane thread i reads column (i % G) * V + i / G, the lane its scan index
+// stands for.  Rows from `real` on lie past the sequence end and are identity
+// steps (a = 1, addend 0); rmask[s] holds the sub-chunk's reset rows (EXT:
+// a = 0 there); with ONE_AT (EXT backward) row real - 1, step T-1, takes
+// a = 1 (grad_last enters through a'_T = 1).  Every override is the one the
+// replay applies to its register copy of the same row.
+template <class C, bool REVERSE, bool EXT, bool ONE_AT>
+__device__ __forceinline__ float exact_walk(const typename C::St *ta, const typename C::St *tb, float *entry,
+                                           const uint32_t *rmask, int S, int i, int real, float c) {
+    constexpr int L = C::L, DT = C::DT, G = C::G, V = C::V;
+    const int col = (i % G) * V + i / G;
+    for (int ii = 0; ii < S; ++ii) {
+        const int s = REVERSE ? S - 1 - ii : ii;
+        entry[s * DT + i] = c;
+        float x[L], y[L];
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            float t1[1], t2[1];
+            unpack_lanes<typename C::St, 1>(ta + (s * L + j) * DT + col, t1);
+            unpack_lanes<typename C::St, 1>(tb + (s * L + j) * DT + col, t2);
+            x[j] = t1[0];
+            y[j] = t2[0];
+        }
+        const uint32_t rb = EXT ? rmask[s] : 0u;
+#pragma unroll
+        for (int jj = 0; jj < L; ++jj) {
+            const int j = REVERSE ? L - 1 - jj : jj;
+            const int r = s * L + j;
+            float xv = ((rb >> j) & 1u) ? 0.0f : x[j];
+            float yv = y[j];
+            if (r >= real) { xv = 1.0f; yv = 0.0f; }
+            else if (ONE_AT && r == real - 1) xv = 1.0f;
+            c = __fmaf_rn(xv, c, yv);
         }
     }
     return c;
@@ -444,9 +500,17 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 unpack_lanes<St, V>(tb + j * DT, xb[j]);
             }
         }
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        // exact tiles release the stage only after the walk has read it
+        const int cur = stage;
+        if constexpr (!C::EX) {
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        }
         if (++stage == sm.nstage) { stage = 0; ++use; }
+        if constexpr (C::EX && EXT) {
+            // the walk takes the reset rows of every sub-chunk from here
+            if (lg == 0) reinterpret_cast<uint32_t *>(sm.sPQ<C>(0))[s] = rbits & ((1u << L) - 1u);
+        }
         // sub-chunk summary h -> P*h + Q (an empty tail sub-chunk is the identity)
         float P[V], Q[V];
 #pragma unroll
@@ -471,18 +535,20 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-#pragma unroll
-        for (int j = 0; j < L; ++j) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                P[v] = __fmul_rn(xa[j][v], P[v]);
-                Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
-            }
-        }
         const int par = C::PT ? (k & 1) : 0;
         float2 *pq = sm.sPQ<C>(par);
+        if constexpr (!C::EX) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    P[v] = __fmul_rn(xa[j][v], P[v]);
+                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xb[j][v]);
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+        }
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
         if (issuer && k > 0) {
             // every thread's rows of window k-1 are staged (fenced before the
@@ -491,7 +557,19 @@ win_fwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             ost.store(omaps, k - 1, d0, (k - 1) * sm.W, brow);
             bulk_wait_read<1>();
         }
-        if constexpr (!C::PT) {
+        if constexpr (C::EX) {
+            // lane threads walk the window's rows exactly (sequential steps),
+            // recording every sub-chunk's entry state; then the stage is free
+            float *entry = sm.sEntry<C>();
+            if (static_cast<int>(threadIdx.x) < DT)
+                carry = exact_walk<C, false, EXT, false>(sm.tile<C>(cur, 0), sm.tile<C>(cur, 1), entry,
+                                                         reinterpret_cast<const uint32_t *>(pq), S, threadIdx.x,
+                                                         T - k * sm.W, carry);
+            bar_sync_or(1, NT, false);
+            if (lane == 0) mbar_arrive(sm.empty_bar(cur));
+#pragma unroll
+            for (int v = 0; v < V; ++v) h[v] = entry[s * DT + v * G + lg];
+        } else if constexpr (!C::PT) {
             // Threads 0..DT-1 each own one lane: push the carried state through
             // the sub-chunk maps in order, recording every sub-chunk's entry
             // state (_real_chunk_prefix within the window; identity maps exact).
@@ -798,9 +876,17 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 unpack_lanes<St, V>(tg + j * DT, xg[j]);
             }
         }
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        // exact tiles release the stage only after the walk has read it
+        const int cur = stage;
+        if constexpr (!C::EX) {
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(sm.empty_bar(stage));
+        }
         if (++stage == sm.nstage) { stage = 0; ++use; }
+        if constexpr (C::EX && EXT) {
+            // the walk takes the rows whose next step starts a segment from here
+            if (lg == 0) reinterpret_cast<uint32_t *>(sm.sPQ<C>(0))[s] = r1bits & ((1u << L) - 1u);
+        }
         // reverse sub-chunk summary: g at the sub-chunk's first step as
         // P * (g just after the sub-chunk) + Q
         float P[V], Q[V];
@@ -834,18 +920,20 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
-#pragma unroll
-        for (int j = L - 1; j >= 0; --j) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                P[v] = __fmul_rn(xa[j][v], P[v]);
-                Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
-            }
-        }
         const int par = C::PT ? (k & 1) : 0;
         float2 *pq = sm.sPQ<C>(par);
+        if constexpr (!C::EX) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+            for (int j = L - 1; j >= 0; --j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    P[v] = __fmul_rn(xa[j][v], P[v]);
+                    Q[v] = __fmaf_rn(xa[j][v], Q[v], xg[j][v]);
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < V; ++v) pq[s * DT + v * G + lg] = make_float2(P[v], Q[v]);
+        }
         if (bar_sync_or(1, NT, !ok)) { failed = true; break; }
         if (issuer && k > 0) {
             // rows of window k-1 are staged and fenced; after issuing its
@@ -854,7 +942,20 @@ win_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             ost.store(omaps, k - 1, d0, wbase + sm.W, brow);
             bulk_wait_read<1>();
         }
-        if constexpr (!C::PT) {
+        if constexpr (C::EX) {
+            // lane threads walk the window's rows exactly, last row first,
+            // recording the adjoint entering every sub-chunk from above; then
+            // the stage is free
+            float *entry = sm.sEntry<C>();
+            if (static_cast<int>(threadIdx.x) < DT)
+                carry = exact_walk<C, true, EXT, EXT>(sm.tile<C>(cur, 0), sm.tile<C>(cur, 2), entry,
+                                                      reinterpret_cast<const uint32_t *>(pq), S, threadIdx.x,
+                                                      T - wbase, carry);
+            bar_sync_or(1, NT, false);
+            if (lane == 0) mbar_arrive(sm.empty_bar(cur));
+#pragma unroll
+            for (int v = 0; v < V; ++v) g[v] = entry[s * DT + v * G + lg];
+        } else if constexpr (!C::PT) {
             // lane threads push the carried adjoint through sub-chunks S-1 .. 0
             float *entry = sm.sEntry<C>();
             if (static_cast<int>(threadIdx.x) < DT) carry = lane_walk<true, DT>(pq, entry, S, threadIdx.x, carry);

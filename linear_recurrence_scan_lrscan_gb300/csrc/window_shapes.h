@@ -59,14 +59,38 @@ using PFB_16_1_8 = WinShape<float, 16, 1, 8, 3, 544, 1, false, true>;
 using WBF_32_2_16 = WinShape<bf16_t, 32, 2, 16, 2, 288, 1, false>;
 using WBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false>;
 
+// Exact windowed shapes: the lane threads walk the window's rows with the
+// sequential step (no sub-chunk maps), so every result is bit-identical to
+// the sequential scan.
+using XBF_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 2, 160, 5, false, false, true>;
+using XBB_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 3, 160, 5, false, false, true>;
+using XBF_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 2, 224, 5, false, false, true>;
+using XBB_32_2_4_M5 = WinShape<bf16_t, 32, 2, 4, 3, 224, 5, false, false, true>;
+using XWBF_32_2_16 = WinShape<bf16_t, 32, 2, 16, 2, 288, 1, false, false, true>;
+using XWBB_32_2_16 = WinShape<bf16_t, 32, 2, 16, 3, 288, 1, false, false, true>;
+using XFF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 2, false, false, true>;
+using XFB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1, false, false, true>;
+using XFF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, false, true>;
+using XFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, false, true>;
+
+// 64-lane exact shapes for the pipelined tiles (8 sub-chunks of 32 replay
+// threads plus 64 walker threads)
+using XPFF_64_2_8 = WinShape<float, 64, 2, 8, 2, 320, 1, false, false, true>;
+using XPFB_64_2_8 = WinShape<float, 64, 2, 8, 3, 320, 1, false, false, true>;
+
+#define LRSCAN_XWP_FWD_SHAPES(X) X(XBF_32_2_8_M5) X(XWBF_32_2_16) X(XPFF_64_2_8) X(XFF_32_1_8)
+#define LRSCAN_XWP_BWD_SHAPES(X) X(XBB_32_2_4_M5) X(XBB_32_2_8_M5) X(XWBB_32_2_16) X(XPFB_64_2_8) X(XFB_32_1_8)
+
 #define LRSCAN_WIN_FWD_SHAPES(X)                                                                   \
     X(SBF_64_2_32) X(SBF_128_2_32) X(SBF_128_4_32) X(SBF_32_1_32) X(SBF_64_1_32) X(SFF_32_1_32) \
     X(SFF_64_2_16) X(SFF_64_1_32) X(SFF_128_4_8) X(BF_64_2_8) X(BF_32_2_8) X(FF_16_1_8)          \
-    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8) X(BF_32_2_4_M5) X(FF_32_1_8_X)
+    X(FF_32_1_8) X(FF_64_2_8) X(PF_32_1_8) X(PF_16_1_8) X(WBF_32_2_16) X(BF_32_2_8_M5) X(BF_32_2_8_M8) X(BF_32_2_4_M5) X(FF_32_1_8_X)   \
+    X(XBF_32_2_8_M5) X(XBF_32_2_4_M5) X(XWBF_32_2_16) X(XFF_64_2_8) X(XFF_32_1_8)
 
 #define LRSCAN_WIN_BWD_SHAPES(X)                                                                   \
     X(SBB_64_2_32) X(SBB_32_1_32) X(SBB_64_1_32) X(SBB_128_2_32) X(SBB_128_4_16) X(SFB_32_1_32) \
     X(SFB_64_2_16) X(SFB_64_1_32) X(SFB_128_4_8) X(BB_64_2_8) X(BB_32_2_8) X(FB_16_1_8)          \
-    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8) X(BB_32_2_4_M5)
+    X(FB_32_1_8) X(FB_64_2_8) X(PFB_32_1_8) X(PFB_16_1_8) X(WBB_32_2_16) X(BB_32_2_8_M5) X(BB_32_2_8_M8) X(BB_32_2_4_M5)                  \
+    X(XBB_32_2_8_M5) X(XBB_32_2_4_M5) X(XWBB_32_2_16) X(XFB_64_2_8) X(XFB_32_1_8)
 
 }  // namespace lrscan

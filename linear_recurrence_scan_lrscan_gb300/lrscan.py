@@ -60,7 +60,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_variant", ctypes.c_int), ("lanes_per_cta", ctypes.c_int),
                 ("rows_per_window", ctypes.c_int), ("subchunks", ctypes.c_int), ("stages", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("threads_per_cta", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t), ("name", ctypes.c_char * 64)]
+                ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t), ("name", ctypes.c_char * 64),
+                ("exact", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {k: getattr(self, k) for k, _ in self._fields_ if k != "name"}
@@ -105,6 +106,8 @@ EXPORTS = {
                                       ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_plan_complex": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts),
                              ctypes.POINTER(PlanInfo)], ctypes.c_int),
+    "lrscan_plan_complex_state": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.POINTER(Opts), ctypes.POINTER(PlanInfo)], ctypes.c_int),
     "lrscan_fwd_gated": ([_P] * 5 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_bwd_gated": ([_P] * 7 + [_I64, _I64, _I64, ctypes.c_int, _P, ctypes.POINTER(Opts)], ctypes.c_int),
     "lrscan_gated_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
@@ -570,15 +573,19 @@ def lrscan_cbwd_state(ar, ai, out_r, out_i, grad_out_r, grad_out_i, h0=None, seg
 
 
 def lrscan_plan_complex(B: int, T: int, D: int, dtype="f32", direction: str = "fwd", aligned: bool = True,
-                        path=None, tile_variant=None, chunk_len=None) -> dict:
+                        path=None, tile_variant=None, chunk_len=None, state: bool = False) -> dict:
+    """What the dispatcher would run for a complex scan (host only);
+    state=True plans a call with carried state or resets
+    (lrscan_plan_complex_state)."""
     code = {"f32": F32, "bf16": BF16}.get(dtype) if isinstance(dtype, str) else _DTYPES.get(dtype)
     if code is None:
         raise ValueError(f"unsupported dtype {dtype}")
     info = PlanInfo()
     o = _opts(path, chunk_len, tile_variant, None)
-    rc = lib().lrscan_plan_complex(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
-                                   ctypes.byref(o) if o is not None else None, ctypes.byref(info))
-    _check(rc, "lrscan_plan_complex")
+    fn = lib().lrscan_plan_complex_state if state else lib().lrscan_plan_complex
+    rc = fn(B, T, D, code, 0 if direction == "fwd" else 1, int(aligned),
+            ctypes.byref(o) if o is not None else None, ctypes.byref(info))
+    _check(rc, "lrscan_plan_complex_state" if state else "lrscan_plan_complex")
     return info.as_dict()
 
 

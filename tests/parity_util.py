@@ -18,7 +18,10 @@ Paths that re-associate the recurrence through affine maps (window, chunk)
 make an fp32 error of a few ulps of the running state's magnitude.  Where a
 stored bf16 value is far smaller than that state (a near-cancellation), this
 can exceed 2 ulps of the tiny stored value; there the fp32 rule above is the
-bound, and such points must stay rare (REASSOC_MAX_FRACTION).
+bound, and such points must stay rare (REASSOC_MAX_FRACTION).  That
+allowance (reassociated=True) is for small cases on every path and for the
+extension workloads (complex, generated decay); the named workloads at full
+size (test_gpu_fullsize.py) are held to the stated tolerances without it.
 """
 from __future__ import annotations
 
@@ -48,6 +51,17 @@ def bf16_ulp_distance(x: np.ndarray, y: np.ndarray) -> np.ndarray:
         mag = b & 0x7FFF
         return np.where(b & 0x8000, -mag, mag)
     return np.abs(key(x) - key(y))
+
+
+def bf16_beyond_ulps(got: np.ndarray, ref: np.ndarray) -> tuple[int, int]:
+    """(points more than 2 bf16 ulps from ref, of which how many still meet
+    the fp32 rule |err| <= 1e-4 (1 + |ref|)), over bf16 bit-pattern arrays."""
+    bad = (bf16_ulp_distance(got, ref) > BF16_MAX_ULPS) & ~np.isnan(bf16_bits_to_f32(ref))
+    if not bad.any():
+        return 0, 0
+    gd = bf16_bits_to_f32(got[bad]).astype(np.float64)
+    rd = bf16_bits_to_f32(ref[bad]).astype(np.float64)
+    return int(bad.sum()), int((np.abs(gd - rd) <= F32_RTOL * (1.0 + np.abs(rd))).sum())
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", exact: bool = False,

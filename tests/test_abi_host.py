@@ -87,20 +87,23 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l4_s12_m5"),
+    2: ("win_bf16_d32_s8_m5_n2", "xwin_bf16_d32_s8_m5_n2"),
     3: ("win_f32_d32_s31", "win_f32_d32_s16"),
-    4: ("win_bf16_d32_s8_m5_n2", "win_bf16_d32_l16_s8"),
-    5: ("seq_f32_d32", "win_f32_d64_s8"),
+    4: ("seq_bf16_d128_n3", "seq_bf16_d128_n2"),
+    5: ("seq_f32_d32", "xwin_f32_d64_s8"),
 }
+# which of those reproduce the sequential definition bit for bit
+EXPECTED_EXACT = {2: (False, True), 3: (False, False), 4: (True, True), 5: (True, True)}
 
 
 @pytest.mark.parametrize("cid", sorted(EXPECTED_AUTO))
 def test_occupancy_rule_on_the_named_workloads(lib, cid):
     from linear_recurrence_scan_lrscan_gb300.workloads import WORKLOADS
     w = WORKLOADS[cid]
-    for direction, want in zip(("fwd", "bwd"), EXPECTED_AUTO[cid]):
+    for direction, want, exact in zip(("fwd", "bwd"), EXPECTED_AUTO[cid], EXPECTED_EXACT[cid]):
         p = L.lrscan_plan(w.B, w.T, w.D, w.dtype, direction)
         assert p["name"] == want, (cid, direction, p)
+        assert p["exact"] == int(exact), (cid, direction, p)
         assert p["kernels"] == 1
         # every lane tile of the GPU-filling variants gets a CTA of its own
         assert p["ctas"] == w.B * -(-w.D // p["lanes_per_cta"])
@@ -116,7 +119,7 @@ def test_state_plans(lib):
         assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", state=True)["name"] == want
         assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", state=True)["name"] == EXPECTED_AUTO[cid][0]
     w = WORKLOADS[4]
-    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[4][1] == "win_bf16_d32_l16_s8"
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[4][1] == "seq_bf16_d128_n2"
 
 
 def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
@@ -124,13 +127,29 @@ def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(
         assert L.lrscan_plan(B, T, D, dt, "fwd")["path"] == "seq"
 
 
-def test_bf16_forward_takes_the_one_wave_window_tile(lib):
-    """The high-residency window tile puts every CTA of the lane tiling on
-    the GPU at once (5 per SM); it is the measured fastest bf16 forward."""
-    for (B, T, D) in [(8, 2048, 2560), (16, 4096, 4096)]:
-        p = L.lrscan_plan(B, T, D, "bf16", "fwd")
-        assert p["name"] == "win_bf16_d32_s8_m5_n2" and p["path"] == "window", p
-        assert p["threads_per_cta"] == 8 * 16 + 32
+def test_bf16_forward_tiles(lib):
+    """Few lanes: the high-residency window tile puts every CTA of the lane
+    tiling on the GPU at once (5 per SM), the measured fastest bf16 forward
+    there.  From two 128-lane tiles per SM: the exact sequential tile."""
+    p = L.lrscan_plan(8, 2048, 2560, "bf16", "fwd")
+    assert p["name"] == "win_bf16_d32_s8_m5_n2" and p["path"] == "window", p
+    assert p["threads_per_cta"] == 8 * 16 + 32
+    p = L.lrscan_plan(16, 4096, 4096, "bf16", "fwd")
+    assert p["name"] == "seq_bf16_d128_n3" and p["path"] == "seq" and p["exact"] == 1, p
+
+
+def test_exact_flag_of_every_tile_variant(lib):
+    """Sequential tiles and the exact-walk window tiles report exact results;
+    re-associating window tiles and the chunked path do not; plain kernels do."""
+    for dt in ("f32", "bf16"):
+        for path in ("seq", "window"):
+            for v in range(1, L.lrscan_num_variants(path, dt) + 1):
+                p = L.lrscan_plan(4, 512, 1024, dt, "fwd", path=path, tile_variant=v)
+                want = path == "seq" or p["name"].startswith(("xwin_", "xwp_"))
+                assert p["exact"] == int(want), p
+        assert L.lrscan_plan(1, 1 << 16, 64, dt, "fwd", path="chunk")["exact"] == 0
+        assert L.lrscan_plan(4, 512, 1024, dt, "fwd", path="plain")["exact"] == 1
+        assert L.lrscan_plan_gated(4, 512, 1024, dt, "fwd", path="plain")["exact"] == 0
 
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):

@@ -12,7 +12,7 @@ import torch
 import oracle
 from linear_recurrence_scan_lrscan_gb300 import lrscan as L
 from linear_recurrence_scan_lrscan_gb300.workloads import COMPLEX_WORKLOAD, make_complex_inputs
-from parity_util import assert_close, assert_last_close, to_np
+from parity_util import assert_close, assert_last_close, bf16_beyond_ulps, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def check_complex(inp, dt, **kw):
     assert L.lrscan_sync_check() == 0
     plan = L.lrscan_plan_complex(B, T, D, dt, "fwd", **kw)
     tag = plan["name"]
-    ex = plan["path"] in ("seq", "plain")  # windowed tiles and chunks re-associate through complex maps
+    ex = bool(plan["exact"])  # windowed tiles and chunks re-associate through complex maps
     for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
         assert_close(to_np(g), r, dt, f"{name}[{tag}]", exact=ex, reassociated=not ex)
     for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
@@ -55,7 +55,7 @@ def check_complex(inp, dt, **kw):
     ggot = L.lrscan_cbwd(cu["ar"], cu["ai"], out_r, out_i, cu["go_r"], cu["go_i"], **kw)
     assert L.lrscan_sync_check() == 0
     planb = L.lrscan_plan_complex(B, T, D, dt, "bwd", **kw)
-    exb = planb["path"] in ("seq", "plain")
+    exb = bool(planb["exact"])
     for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot, gref):
         assert_close(to_np(g), r, dt, f"{name}[{planb['name']}]", exact=exb, reassociated=not exb)
     return plan, planb
@@ -137,36 +137,37 @@ def test_complex_chunked_unaligned_rows():
     assert plan["path"] == "chunk"  # few lanes, long enough: chunks also without alignment
 
 
-def test_complex_full_size_sampled_lanes():
+def test_complex_full_size_every_element():
     """The complex workload at full size in the benchmark's launch
-    configuration, checked on sampled lanes the oracle computes one by one."""
+    configuration, every element of every plane against the oracle (the
+    windowed tiles re-associate: near-cancellation points allowed under the
+    fp32 rule, and counted); the backward reads the oracle's forward output,
+    so both sides see the same h_{t-1}."""
     w = COMPLEX_WORKLOAD
     inp = make_complex_inputs()
     cu = {k: inp[k].cuda() for k in PLANES}
-    out_r, out_i, last_r, last_i = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"])
+    got = L.lrscan_cfwd(cu["ar"], cu["ai"], cu["br"], cu["bi"])
     assert L.lrscan_sync_check() == 0
     o = oracle.default()
-    # the backward reads the oracle's forward output, so both sides see the same h_{t-1}
-    full = o.cfwd(*(to_np(inp[k]) for k in ("ar", "ai", "br", "bi")), w.dtype)
-    grads = L.lrscan_cbwd(cu["ar"], cu["ai"], from_np(full[0], w.dtype).cuda(), from_np(full[1], w.dtype).cuda(),
+    ref = o.cfwd(*(to_np(inp[k]) for k in ("ar", "ai", "br", "bi")), w.dtype)
+    ex = bool(L.lrscan_plan_complex(w.B, w.T, w.D, w.dtype, "fwd")["exact"])
+    for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
+        gn = to_np(g)
+        print(f"[fullsize] complex {name}: beyond 2 bf16 ulps {bf16_beyond_ulps(gn, r)}", flush=True)
+        assert_close(gn, r, w.dtype, f"complex {name}, full size", exact=ex, reassociated=not ex)
+    for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
+        assert_last_close(g.cpu().numpy(), r, f"complex {name}, full size", exact=ex)
+    del got
+    grads = L.lrscan_cbwd(cu["ar"], cu["ai"], from_np(ref[0], w.dtype).cuda(), from_np(ref[1], w.dtype).cuda(),
                           cu["go_r"], cu["go_i"])
     assert L.lrscan_sync_check() == 0
-    del full
-    r = np.random.default_rng(520)
-    for _ in range(6):
-        b = int(r.integers(w.B))
-        d = int(r.integers(w.D))
-        sl = lambda t: np.ascontiguousarray(to_np(t[b:b + 1, :, d:d + 1]))  # noqa: E731
-        ref = o.cfwd(sl(inp["ar"]), sl(inp["ai"]), sl(inp["br"]), sl(inp["bi"]), w.dtype)
-        ex = L.lrscan_plan_complex(w.B, w.T, w.D, w.dtype, "fwd")["path"] != "window"
-        assert_close(sl(out_r), ref[0], w.dtype, "out_r sampled", exact=ex, reassociated=not ex)
-        assert_close(sl(out_i), ref[1], w.dtype, "out_i sampled", exact=ex, reassociated=not ex)
-        assert_last_close(np.array([[last_r[b, d].item()]]), ref[2], "last_r sampled", exact=ex)
-        assert_last_close(np.array([[last_i[b, d].item()]]), ref[3], "last_i sampled", exact=ex)
-        gref = o.cbwd(sl(inp["ar"]), sl(inp["ai"]), ref[0], ref[1], sl(inp["go_r"]), sl(inp["go_i"]), w.dtype)
-        exb = L.lrscan_plan_complex(w.B, w.T, w.D, w.dtype, "bwd")["path"] != "window"
-        for g, gr_ in zip(grads, gref):
-            assert_close(sl(g), gr_, w.dtype, "complex grads sampled", exact=exb, reassociated=not exb)
+    gref = o.cbwd(*(to_np(inp[k]) for k in ("ar", "ai")), ref[0], ref[1],
+                  *(to_np(inp[k]) for k in ("go_r", "go_i")), w.dtype)
+    exb = bool(L.lrscan_plan_complex(w.B, w.T, w.D, w.dtype, "bwd")["exact"])
+    for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), grads, gref):
+        gn = to_np(g)
+        print(f"[fullsize] complex {name}: beyond 2 bf16 ulps {bf16_beyond_ulps(gn, r)}", flush=True)
+        assert_close(gn, r, w.dtype, f"complex {name}, full size", exact=exb, reassociated=not exb)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -212,10 +213,14 @@ def check_cstate(inp, dt, h0, gl, seg, **kw):
     tseg = torch.from_numpy(seg).cuda()
     got = L.lrscan_cfwd_state(cu["ar"], cu["ai"], cu["br"], cu["bi"], h0=th0, segment_pos=tseg, **kw)
     assert L.lrscan_sync_check() == 0
+    B, T, D = inp["shape"]
+    plan = L.lrscan_plan_complex(B, T, D, dt, "fwd", state=True, **kw)
+    planb = L.lrscan_plan_complex(B, T, D, dt, "bwd", state=True, **kw)
+    ex, exb = bool(plan["exact"]), bool(planb["exact"])
     for name, g, r in zip(("out_r", "out_i"), got[:2], ref[:2]):
-        assert_close(to_np(g), r, dt, f"{name} (state)", reassociated=True)
+        assert_close(to_np(g), r, dt, f"{name} (state) [{plan['name']}]", exact=ex, reassociated=not ex)
     for name, g, r in zip(("last_r", "last_i"), got[2:], ref[2:]):
-        assert_last_close(g.cpu().numpy(), r, f"{name} (state)")
+        assert_last_close(g.cpu().numpy(), r, f"{name} (state) [{plan['name']}]", exact=ex)
     out_r, out_i = from_np(ref[0], dt).cuda(), from_np(ref[1], dt).cuda()
     gref = o.cbwd_state(np_in["ar"], np_in["ai"], ref[0], ref[1], np_in["go_r"], np_in["go_i"], dt, h0=tuple(h0),
                         segment_pos=seg, grad_last=tuple(gl))
@@ -223,13 +228,14 @@ def check_cstate(inp, dt, h0, gl, seg, **kw):
                                grad_last=tgl, **kw)
     assert L.lrscan_sync_check() == 0
     for name, g, r in zip(("grad_ar", "grad_ai", "grad_br", "grad_bi"), ggot[:4], gref[:4]):
-        assert_close(to_np(g), r, dt, f"{name} (state)", reassociated=True)
+        assert_close(to_np(g), r, dt, f"{name} (state) [{planb['name']}]", exact=exb, reassociated=not exb)
     for name, g, r in zip(("grad_h0_r", "grad_h0_i"), ggot[4:], gref[4:]):
-        assert_last_close(g.cpu().numpy(), r, f"{name} (state)")
+        assert_last_close(g.cpu().numpy(), r, f"{name} (state) [{planb['name']}]", exact=exb)
     # grad_a is exactly +0 at every segment start
     rs = np.broadcast_to((seg == 0)[..., None], ref[0].shape)
     for g in ggot[:2]:
         assert not to_np(g).view(np.uint16 if dt == "bf16" else np.uint32)[rs].any()
+    return plan, planb
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -237,7 +243,28 @@ def check_cstate(inp, dt, h0, gl, seg, **kw):
 def test_complex_state_every_shape(dt, chunk):
     for i, (B, T, D) in enumerate(SHAPES):
         inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=570 + i)
-        check_cstate(inp, dt, h0, gl, seg, chunk_len=chunk)
+        check_cstate(inp, dt, h0, gl, seg, path="chunk", chunk_len=chunk)
+        check_cstate(inp, dt, h0, gl, seg)  # the automatic plan
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_state_every_tile_variant(dt):
+    """Every tiled complex variant (sequential tiles bit for bit, windowed
+    tiles to rounding) with h0, resets, grad_last and grad_h0, on shapes with
+    ragged lane tiles and ragged last windows, against the oracle."""
+    for i, (B, T, D) in enumerate([(3, 300, 200), (2, 77, 48), (1, 1, 16), (2, 1030, 96)]):
+        inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=600 + i)
+        if i % 2:
+            seg[:, 0] = 0   # a reset at step 0
+        n = 1
+        while True:
+            try:
+                L.lrscan_plan_complex(B, T, D, dt, path="seq", tile_variant=n, state=True)
+            except L.LrscanError:
+                break
+            check_cstate(inp, dt, h0, gl, seg, path="seq", tile_variant=n)
+            n += 1
+        assert n > 5
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -268,10 +295,10 @@ def test_complex_state_absent_equals_plain_and_empty():
     assert torch.equal(lr, h0[0]) and torch.equal(li, h0[1])
     g = L.lrscan_cbwd_state(e, e, e, e, e, e, grad_last=gl)
     assert torch.equal(g[4], gl[0]) and torch.equal(g[5], gl[1])
-    # the state-carrying complex scan runs on the chunked path only
+    # the plain complex kernels carry no state
     x = torch.zeros((1, 64, 16), device="cuda")
     with pytest.raises(L.LrscanError):
-        L.lrscan_cfwd_state(x, x, x, x, h0=(x[:, 0], x[:, 0]), path="seq")
+        L.lrscan_cfwd_state(x, x, x, x, h0=(x[:, 0], x[:, 0]), path="plain")
     assert L.lrscan_sync_check() == 0
 
 

@@ -10,7 +10,7 @@ import torch
 import oracle
 from linear_recurrence_scan_lrscan_gb300 import lrscan as L
 from linear_recurrence_scan_lrscan_gb300.workloads import GATED_WORKLOAD, make_gated_inputs
-from parity_util import assert_close, assert_last_close, assert_sum_close, bf16_bits_to_f32, to_np
+from parity_util import bf16_beyond_ulps, assert_close, assert_last_close, assert_sum_close, bf16_bits_to_f32, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -105,34 +105,32 @@ def test_gated_empty_sequence():
 
 def test_gated_full_size():
     """The generated-decay workload at full size in the benchmark's launch
-    configuration.  The forward is checked on sampled lanes the oracle
-    computes one by one; the backward runs on the oracle's forward output (so
-    both sides read the same h_{t-1}) and grad_b is checked on sampled lanes,
-    grad_eta on every token and grad_nu_log on every lane."""
+    configuration, every element: out and last of the forward; the backward
+    runs on the oracle's forward output (so both sides read the same
+    h_{t-1}): grad_b on every element, grad_eta on every token and
+    grad_nu_log on every lane.  The decays come from a fast exponential, so
+    this path agrees with the oracle to rounding (near-cancellation points
+    allowed under the fp32 rule, and counted)."""
     w = GATED_WORKLOAD
     inp = make_gated_inputs()
     etad, nud = inp["eta"].cuda(), inp["nu_log"].cuda()
     out, last = L.lrscan_fwd_gated(etad, nud, inp["b"].cuda())
     assert L.lrscan_sync_check() == 0
     o = oracle.default()
-    r = np.random.default_rng(720)
     eta, nu = inp["eta"].numpy(), inp["nu_log"].numpy()
-    for _ in range(4):
-        bb, d = int(r.integers(w.B)), int(r.integers(w.D))
-        sl = lambda t: np.ascontiguousarray(to_np(t[bb:bb + 1, :, d:d + 1]))  # noqa: E731
-        ref_out, ref_last = o.gated_fwd(eta[bb:bb + 1], nu[d:d + 1], sl(inp["b"]), w.dtype)
-        assert_close(sl(out), ref_out, w.dtype, "gated out sampled", reassociated=True)
-        assert_last_close(last[bb:bb + 1, d:d + 1].cpu().numpy(), ref_last, "gated last sampled")
+    ref_out, ref_last = o.gated_fwd(eta, nu, to_np(inp["b"]), w.dtype)
+    out_n = to_np(out)
     del out
-    ref_out, _ = o.gated_fwd(eta, nu, to_np(inp["b"]), w.dtype)
+    print(f"[fullsize] gated out: beyond 2 bf16 ulps {bf16_beyond_ulps(out_n, ref_out)}", flush=True)
+    assert_close(out_n, ref_out, w.dtype, "gated out, full size", reassociated=True)
+    assert_last_close(last.cpu().numpy(), ref_last, "gated last, full size")
     g = to_np(inp["grad_out"])
     ref_gb, ref_geta, ref_gnu = o.gated_bwd(eta, nu, ref_out, g, w.dtype)
     gb, geta, gnu = L.lrscan_bwd_gated(etad, nud, from_np(ref_out, w.dtype).cuda(), inp["grad_out"].cuda())
     assert L.lrscan_sync_check() == 0
-    for _ in range(4):
-        bb, d = int(r.integers(w.B)), int(r.integers(w.D))
-        assert_close(to_np(gb[bb:bb + 1, :, d:d + 1]), np.ascontiguousarray(ref_gb[bb:bb + 1, :, d:d + 1]), w.dtype,
-                     "gated grad_b sampled", reassociated=True)
+    gb_n = to_np(gb)
+    print(f"[fullsize] gated grad_b: beyond 2 bf16 ulps {bf16_beyond_ulps(gb_n, ref_gb)}", flush=True)
+    assert_close(gb_n, ref_gb, w.dtype, "gated grad_b, full size", reassociated=True)
     s_eta, s_nu = abs_terms(eta, nu, ref_out, g, w.dtype)
     assert_sum_close(geta.cpu().numpy(), ref_geta, s_eta, "gated grad_eta, full size")
     assert_sum_close(gnu.cpu().numpy(), ref_gnu, s_nu, "gated grad_nu_log, full size")

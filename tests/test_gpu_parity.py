@@ -2,9 +2,8 @@
 same seeded inputs, element by element (tolerances in parity_util).
 
 Small cases span several lane tiles, windows and chunks with ragged tails on
-both axes; the named workloads run at full size in the launch configuration
-the benchmark times (auto path) and are checked on sampled lanes, which the
-oracle computes one by one.
+both axes, on every path and tile variant.  The named workloads at full size
+(every element) are in test_gpu_fullsize.py.
 """
 import numpy as np
 import pytest
@@ -41,8 +40,10 @@ def _dt(t):
     return "bf16" if t.dtype == torch.bfloat16 else "f32"
 
 
-def exact_path(path, plan_path):
-    return (plan_path if path in (None, "auto") else path) in ("seq", "plain")
+def exact_plan(plan) -> bool:
+    """Paths whose every result is the sequential definition's own (the
+    sequential and plain kernels, and the exact-walk windowed tiles)."""
+    return bool(plan["exact"])
 
 
 def gpu_fwd(a, b, **kw):
@@ -72,7 +73,7 @@ def check_case(inp, path=None, **kw):
     o = orc()
     ref_out, ref_last = o.fwd(to_np(a), to_np(b), dt)
     plan = L.lrscan_plan(B, T, D, dt, "fwd", path=path, **kw)
-    ex = exact_path(path, plan["path"])
+    ex = exact_plan(plan)
     out, last = gpu_fwd(a, b, path=path, **kw)
     assert_close(out, ref_out, dt, f"out[{plan['name']}]", exact=ex, reassociated=not ex)
     assert_last_close(last, ref_last, f"last[{plan['name']}]", exact=ex)
@@ -83,7 +84,7 @@ def check_case(inp, path=None, **kw):
     out_t = from_np(ref_out, dt)
     ref_ga, ref_gb = o.bwd(to_np(a), ref_out, to_np(g), dt)
     planb = L.lrscan_plan(B, T, D, dt, "bwd", path=path, **kw)
-    exb = exact_path(path, planb["path"])
+    exb = exact_plan(planb)
     ga, gb = gpu_bwd(a, out_t, g, path=path, **kw)
     assert_close(gb, ref_gb, dt, f"grad_b[{planb['name']}]", exact=exb, reassociated=not exb)
     assert_close(ga, ref_ga, dt, f"grad_a[{planb['name']}]", exact=exb, reassociated=not exb)
@@ -202,58 +203,6 @@ def test_named_workloads_reduced_size_all_paths(cid):
     check_case(inp, path="chunk", chunk_len=w.chunk or 64)
 
 
-def _sample_lanes(B, D, n, seed):
-    r = np.random.default_rng(seed)
-    lanes = {(0, 0), (B - 1, D - 1), (B // 2, D // 2)}
-    while len(lanes) < n:
-        lanes.add((int(r.integers(B)), int(r.integers(D))))
-    return sorted(lanes)
-
-
-@pytest.mark.parametrize("cid", [2, 3, 4, 5])
-def test_named_workloads_full_size_sampled(cid):
-    """Full size, auto path (what the benchmark times); oracle on sampled lanes.
-
-    Lanes (b, d) are independent, so the backward's `out` input is all zeros
-    except the sampled lanes, which hold the oracle's forward values: every
-    compared number depends on oracle-side inputs only."""
-    w = WORKLOADS[cid]
-    inp = make_inputs(cid)
-    dt = w.dtype
-    a, b, g = inp["a"], inp["b"], inp["grad_out"]
-    plan = L.lrscan_plan(w.B, w.T, w.D, dt, "fwd")
-    planb = L.lrscan_plan(w.B, w.T, w.D, dt, "bwd")
-    ad, bd, gd = a.cuda(), b.cuda(), g.cuda()
-    out, last = L.lrscan_fwd(ad, bd)
-    assert L.lrscan_sync_check() == 0
-    lanes = _sample_lanes(w.B, w.D, 24, cid)
-    o = orc()
-    an, bn, gn = to_np(a), to_np(b), to_np(g)
-    out_n, last_n = to_np(out), last.cpu().numpy()
-    exf = exact_path(None, plan["path"])
-    exb = exact_path(None, planb["path"])
-    out_for_bwd = torch.zeros_like(ad)
-    ref = {}
-    for (bb, d) in lanes:
-        sl = np.s_[bb:bb + 1, :, d:d + 1]
-        ro, rl = o.fwd(np.ascontiguousarray(an[sl]), np.ascontiguousarray(bn[sl]), dt)
-        assert_close(out_n[sl], ro, dt, f"cfg{cid} out lane {(bb, d)}", exact=exf, reassociated=not exf)
-        assert_last_close(last_n[bb:bb + 1, d:d + 1], rl, f"cfg{cid} last lane {(bb, d)}", exact=exf)
-        out_for_bwd[bb, :, d] = from_np(ro, dt).reshape(-1).cuda()
-        ref[(bb, d)] = o.bwd(np.ascontiguousarray(an[sl]), ro, np.ascontiguousarray(gn[sl]), dt)
-    ga, gb = L.lrscan_bwd(ad, out_for_bwd, gd)
-    assert L.lrscan_sync_check() == 0
-    ga_n, gb_n = to_np(ga), to_np(gb)
-    for (bb, d), (rga, rgb) in ref.items():
-        sl = np.s_[bb:bb + 1, :, d:d + 1]
-        assert_close(gb_n[sl], rgb, dt, f"cfg{cid} grad_b lane {(bb, d)}", exact=exb, reassociated=not exb)
-        assert_close(ga_n[sl], rga, dt, f"cfg{cid} grad_a lane {(bb, d)}", exact=exb, reassociated=not exb)
-    if w.padded:
-        ga2, gb2 = L.lrscan_bwd(ad, out, gd)
-        assert L.lrscan_sync_check() == 0
-        _check_padding(inp["lengths"].numpy(), out_n, last_n, to_np(ga2), to_np(gb2), exact_carry=exf)
-
-
 def _check_padding(lengths, out, last, ga, gb, exact_carry):
     B = out.shape[0]
     for bb in range(B):
@@ -279,7 +228,7 @@ def test_padding_identity_steps(path):
     out, last = gpu_fwd(inp["a"], inp["b"], path=path)
     ga, gb = gpu_bwd(inp["a"], torch.from_numpy(out), inp["grad_out"], path=path)
     plan = L.lrscan_plan(16, 512, 256, "f32", "fwd", path=path)
-    _check_padding(lengths, out, last, ga, gb, exact_carry=exact_path(path, plan["path"]))
+    _check_padding(lengths, out, last, ga, gb, exact_carry=exact_plan(plan))
 
 
 def test_empty_and_degenerate_shapes():

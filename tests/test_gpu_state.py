@@ -63,8 +63,8 @@ def state_inputs(B, T, D, dt, seed):
     return inp
 
 
-def exact_path(path, plan_path):
-    return (plan_path if path in (None, "auto") else path) in ("seq", "plain")
+def exact_plan(plan) -> bool:
+    return bool(plan["exact"])
 
 
 def check_state_case(inp, path=None, use=("h0", "seg", "grad_last"), want_grad_h0=True, **kw):
@@ -77,7 +77,7 @@ def check_state_case(inp, path=None, use=("h0", "seg", "grad_last"), want_grad_h
     o = oracle.default()
     ref_out, ref_last = o.fwd_state(to_np(a), to_np(b), dt, h0=h0, segment_pos=seg)
     plan = L.lrscan_plan(B, T, D, dt, "fwd", path=path, **kw)
-    ex = exact_path(path, plan["path"])
+    ex = exact_plan(plan)
     cu = lambda x: None if x is None else torch.from_numpy(x).cuda()  # noqa: E731
     out, last = L.lrscan_fwd_state(a.cuda(), b.cuda(), h0=cu(h0), segment_pos=cu(seg), path=path, **kw)
     assert L.lrscan_sync_check() == 0
@@ -88,7 +88,7 @@ def check_state_case(inp, path=None, use=("h0", "seg", "grad_last"), want_grad_h
     ref_ga, ref_gb, ref_gh0 = o.bwd_state(to_np(a), ref_out, to_np(g), dt, h0=h0, segment_pos=seg,
                                           grad_last=gl)
     planb = L.lrscan_plan(B, T, D, dt, "bwd", path=path, **kw)
-    exb = exact_path(path, planb["path"])
+    exb = exact_plan(planb)
     gh0 = torch.full((B, D), float("nan"), device="cuda") if want_grad_h0 else None
     ga, gb, gh0_out = L.lrscan_bwd_state(a.cuda(), from_np(ref_out, dt).cuda(), g.cuda(), h0=cu(h0),
                                          segment_pos=cu(seg), grad_last=cu(gl), grad_h0=gh0,

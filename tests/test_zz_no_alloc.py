@@ -4,10 +4,12 @@ Some callers cannot call cudaMalloc while they run -- code inside an
 allocator or memory-pool callback, loops that ban allocation because it can
 synchronize the device, hosts that give the library only pre-sized buffers.
 For them the library keeps the chunked path's scratch in a fixed device
-array.  This test calls that entry point through the C ABI and checks it
-against the regular (allocating) entry point on the same inputs, on two
-calls in a row with different shapes and dtypes, and checks that a problem
-too large for the fixed scratch is refused before anything runs.
+array.  These tests call that entry point through the C ABI and check it
+against the CPU oracle (the sequential definition) element by element, and
+against the regular (allocating) entry point, on calls in a row with
+different shapes, dtypes and chunk lengths, ragged sequence ends, without a
+final-state output, with an empty sequence, and check that a problem too
+large for the fixed scratch is refused before anything runs.
 
 The file name puts it last in collection order; it depends on no other test.
 """
@@ -15,9 +17,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from linear_recurrence_scan_lrscan_gb300 import lrscan as L
 from linear_recurrence_scan_lrscan_gb300.workloads import random_inputs
-from parity_util import assert_close, to_np
+from parity_util import assert_close, assert_last_close, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -31,28 +34,65 @@ def lib():
     return L.lib()
 
 
-def _noalloc(lib, a, b, chunk, stream):
+def _noalloc(lib, a, b, chunk, stream, want_last=True):
     B, T, D = a.shape
-    out = torch.empty_like(a)
-    last = torch.empty((B, D), device=a.device, dtype=torch.float32)
+    out = torch.full_like(a, 7.0)
+    last = torch.full((B, D), 7.0, device=a.device, dtype=torch.float32) if want_last else None
     code = L.F32 if a.dtype == torch.float32 else L.BF16
-    rc = lib.lrscan_fwd_chunk_noalloc(a.data_ptr(), b.data_ptr(), out.data_ptr(), last.data_ptr(),
-                                      B, T, D, code, chunk, stream.cuda_stream)
+    rc = lib.lrscan_fwd_chunk_noalloc(a.data_ptr(), b.data_ptr(), out.data_ptr(),
+                                      last.data_ptr() if want_last else None, B, T, D, code, chunk,
+                                      stream.cuda_stream)
     assert rc == L.LRSCAN_OK, (rc, lib.lrscan_last_error())
     return out, last
 
 
-def test_noalloc_matches_the_allocating_chunked_forward_on_two_calls_in_a_row(lib):
+# (B, T, D, dtype, chunk_len): T not a multiple of the chunk length in most
+# cases (a ragged last chunk); chunk_len 0 means the default 64
+CASES = [(2, 3000, 256, "f32", 64), (3, 777, 136, "bf16", 32), (2, 1001, 64, "f32", 16),
+         (1, 4099, 40, "bf16", 0), (4, 129, 24, "f32", 32), (2, 2050, 512, "bf16", 16)]
+
+
+@pytest.mark.parametrize("want_last", [True, False])
+def test_noalloc_matches_the_oracle_on_calls_in_a_row(lib, want_last):
     stream = torch.cuda.current_stream()
-    cases = [(2, 3000, 256, "f32", 64), (3, 777, 136, "bf16", 32)]
-    for (B, T, D, dt, chunk) in cases:
+    o = oracle.default()
+    for (B, T, D, dt, chunk) in CASES:
         inp = random_inputs(B, T, D, dt, seed=B * 1000 + T, a_lo=0.7, a_hi=1.0)
         a, b = inp["a"].cuda(), inp["b"].cuda()
-        out_ref, last_ref = L.lrscan_fwd(a, b, path="chunk", chunk_len=chunk)
+        ref_out, ref_last = o.fwd(to_np(inp["a"]), to_np(inp["b"]), dt)
+        out, last = _noalloc(lib, a, b, chunk, stream, want_last)
+        assert L.lrscan_sync_check() == 0
+        what = f"no-alloc {dt} B={B} T={T} D={D} C={chunk}"
+        # the chunked forward re-associates: held to the scan's tolerances
+        assert_close(to_np(out), ref_out, dt, f"{what} out", reassociated=True)
+        if want_last:
+            assert_last_close(last.cpu().numpy(), ref_last, f"{what} last")
+            if dt == "f32":
+                assert np.array_equal(last.cpu().numpy(), to_np(out)[:, -1, :])
+
+
+def test_noalloc_matches_the_allocating_chunked_forward_on_two_calls_in_a_row(lib):
+    stream = torch.cuda.current_stream()
+    for (B, T, D, dt, chunk) in CASES[:2]:
+        inp = random_inputs(B, T, D, dt, seed=B * 1000 + T, a_lo=0.7, a_hi=1.0)
+        a, b = inp["a"].cuda(), inp["b"].cuda()
+        out_ref, last_ref = L.lrscan_fwd(a, b, path="chunk", chunk_len=chunk or 64)
         out, last = _noalloc(lib, a, b, chunk, stream)
         assert L.lrscan_sync_check() == 0
-        assert_close(to_np(out), to_np(out_ref), dt, f"no-alloc out {dt}", reassociated=True)
-        assert_close(last.cpu().numpy(), last_ref.cpu().numpy(), "f32", f"no-alloc last {dt}")
+        # both take the flat chunk prefix at these sizes: the same operations
+        assert torch.equal(out, out_ref) and torch.equal(last, last_ref)
+
+
+def test_noalloc_empty_sequence_zeroes_last(lib):
+    for dt in (torch.float32, torch.bfloat16):
+        a = torch.empty(3, 0, 16, dtype=dt, device="cuda")
+        last = torch.full((3, 16), 7.0, device="cuda")
+        code = L.F32 if dt == torch.float32 else L.BF16
+        rc = lib.lrscan_fwd_chunk_noalloc(a.data_ptr(), a.data_ptr(), a.data_ptr(), last.data_ptr(), 3, 0, 16,
+                                          code, 0, None)
+        assert rc == L.LRSCAN_OK
+        assert L.lrscan_sync_check() == 0
+        assert not last.any()
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lib):
