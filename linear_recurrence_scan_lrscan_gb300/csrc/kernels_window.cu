@@ -13,12 +13,6 @@ LRSCAN_WIN_FWD_SHAPES(LRSCAN_EXTERN_FWD)
 LRSCAN_WIN_BWD_SHAPES(LRSCAN_EXTERN_BWD)
 #undef LRSCAN_EXTERN_FWD
 #undef LRSCAN_EXTERN_BWD
-#define LRSCAN_EXTERN_XF(SH) extern template int launch_xwp_fwd<SH, true>(const WinLaunch &, const WinDirCfg &);
-#define LRSCAN_EXTERN_XB(SH) extern template int launch_xwp_bwd<SH, true>(const WinLaunch &, const WinDirCfg &);
-LRSCAN_XWP_FWD_SHAPES(LRSCAN_EXTERN_XF)
-LRSCAN_XWP_BWD_SHAPES(LRSCAN_EXTERN_XB)
-#undef LRSCAN_EXTERN_XF
-#undef LRSCAN_EXTERN_XB
 
 namespace {
 
@@ -50,39 +44,8 @@ WinDirCfg dir_cfg(int S, int nstage) {
     return d;
 }
 
-// Pipelined exact tiles: S * G replay threads plus DT walker threads.
-template <class C, bool FWD>
-WinDirCfg xdir_cfg(int S, int nstage) {
-    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
-    if (!C::EX || S > C::SMAX || S * C::G + C::DT > C::MAXT) std::abort();  // table error
-    WinDirCfg d{};
-    d.dt = C::DT;
-    d.v = C::V;
-    d.l = C::L;
-    d.s = S;
-    d.lane_scan = 1;
-    d.exact = 1;
-    d.w = g.W;
-    d.nstage = nstage;
-    d.threads = S * C::G + C::DT;
-    d.smem = win_out_smem(g, FWD ? 1 : 2, 3);  // plus three output staging buffers
-    d.stage_bytes = g.stage_bytes;
-    if constexpr (FWD) {
-        static_assert(C::NIN == 2, "forward tiles: a, b");
-        d.launch = &launch_xwp_fwd<C, false>;
-        d.launch_state = &launch_xwp_fwd<C, true>;
-    } else {
-        static_assert(C::NIN == 3, "backward tiles: a, out, grad_out");
-        d.launch = &launch_xwp_bwd<C, false>;
-        d.launch_state = &launch_xwp_bwd<C, true>;
-    }
-    return d;
-}
-
 #define F(SH, S, N) dir_cfg<SH, true>(S, N)
 #define B(SH, S, N) dir_cfg<SH, false>(S, N)
-#define XF(SH, S, N) xdir_cfg<SH, true>(S, N)
-#define XB(SH, S, N) xdir_cfg<SH, false>(S, N)
 
 
 const WinVariant kSeqBF16[] = {
@@ -114,10 +77,6 @@ const WinVariant kWinBF16[] = {
     {"xwin_bf16_d32_l4_s12_m5", F(XBF_32_2_4_M5, 12, 2), B(XBB_32_2_4_M5, 12, 2)},
     {"xwin_bf16_d32_l16_s8", F(XWBF_32_2_16, 8, 4), B(XWBB_32_2_16, 8, 4)},
     {"xwin_bf16_d32_s8_m5_n3", F(XBF_32_2_8_M5, 8, 3), B(XBB_32_2_8_M5, 8, 3)},
-    // pipelined exact walk (walker warps beside the replay threads)
-    {"xwp_bf16_d32_s8_m5_n2", XF(XBF_32_2_8_M5, 8, 2), XB(XBB_32_2_4_M5, 12, 2)},
-    {"xwp_bf16_d32_s8_m5_n3", XF(XBF_32_2_8_M5, 8, 3), XB(XBB_32_2_8_M5, 8, 2)},
-    {"xwp_bf16_d32_l16_s8", XF(XWBF_32_2_16, 8, 4), XB(XWBB_32_2_16, 8, 4)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},
@@ -136,15 +95,10 @@ const WinVariant kWinF32[] = {
     // exact walk (bit-identical to the sequential scan)
     {"xwin_f32_d64_s8", F(XFF_64_2_8, 8, 4), B(XFB_64_2_8, 8, 3)},
     {"xwin_f32_d32_s16", F(XFF_32_1_8, 16, 4), B(XFB_32_1_8, 16, 3)},
-    // pipelined exact walk
-    {"xwp_f32_d64_s8", XF(XPFF_64_2_8, 8, 3), XB(XPFB_64_2_8, 8, 2)},
-    {"xwp_f32_d32_s16", XF(XFF_32_1_8, 16, 4), XB(XFB_32_1_8, 16, 3)},
 };
 
 #undef F
 #undef B
-#undef XF
-#undef XB
 
 
 }  // namespace

@@ -12,11 +12,5 @@ LRSCAN_WIN_FWD_SHAPES(LRSCAN_INST_FWD)
 LRSCAN_WIN_BWD_SHAPES(LRSCAN_INST_BWD)
 #undef LRSCAN_INST_FWD
 #undef LRSCAN_INST_BWD
-#define LRSCAN_INST_XF(SH) template int launch_xwp_fwd<SH, true>(const WinLaunch &, const WinDirCfg &);
-#define LRSCAN_INST_XB(SH) template int launch_xwp_bwd<SH, true>(const WinLaunch &, const WinDirCfg &);
-LRSCAN_XWP_FWD_SHAPES(LRSCAN_INST_XF)
-LRSCAN_XWP_BWD_SHAPES(LRSCAN_INST_XB)
-#undef LRSCAN_INST_XF
-#undef LRSCAN_INST_XB
 
 }  // namespace lrscan

@@ -133,17 +133,11 @@ template <class C> __host__ __device__ constexpr bool win_staged() { return !C::
 // buffers alternate and each store overlaps a window of compute.
 // NB = 1 keeps one buffer per plane: the thread that stores a window must
 // then wait for its reads (bulk_wait_read<0>) before the next replay writes.
-// NB = 3 lets the replay of window k start right after the barrier that
-// issues window k-1's store: the store of k-2, whose buffer window k+1 takes,
-// only has to finish reading before the next barrier.
 template <int NP, class St, int NB = 2>
 struct OutStage {
     St *buf;
     int elems;  // W * DT
-    __device__ __forceinline__ St *plane(int kw, int p) const {
-        const int b = NB == 1 ? 0 : (NB == 2 ? (kw & 1) : kw % NB);
-        return buf + (b * NP + p) * elems;
-    }
+    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((NB == 1 ? 0 : kw & 1) * NP + p) * elems; }
     // bulk tensor stores of processed window kw's planes at (x, y, z), one group
     __device__ __forceinline__ void store(const CUtensorMap *const (&maps)[NP], int kw, int x, int y, int z) const {
 #pragma unroll

@@ -5,7 +5,6 @@
 
 #include <mutex>
 
-#include "exact_kernels.cuh"
 #include "launch.h"
 #include "window_kernels.cuh"
 
@@ -50,36 +49,6 @@ int launch_win_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
                                      *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3], *L.maps[4],
                                      static_cast<typename C::St *>(L.out0), static_cast<typename C::St *>(L.out1), g,
                                      L.status, L.timeout_ns, L.sx);
-    return e == cudaSuccess ? 0 : -1;
-}
-
-// Pipelined exact tiles: S * G replay threads and DT walker threads (the
-// first walker thread also produces), output staging in three buffers.
-template <class C, bool EXT>
-int launch_xwp_fwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = xwp_fwd_kernel<C, EXT>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
-                                     win_out_smem(g, 1, 3), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], L.last, g,
-                                     L.status, L.timeout_ns, L.sx);
-    return e == cudaSuccess ? 0 : -1;
-}
-
-template <class C, bool EXT>
-int launch_xwp_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
-    static unsigned long long mask = 0;
-    static std::mutex mu;
-    auto fn = xwp_bwd_kernel<C, EXT>;
-    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
-    const WinGeom g = make_win_geom<C>(cfg.s, cfg.nstage, static_cast<int>(L.T), static_cast<int>(L.D));
-    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
-    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(cfg.threads),
-                                     win_out_smem(g, 2, 3), L.stream, *L.maps[0], *L.maps[1], *L.maps[2], *L.maps[3],
-                                     *L.maps[4], g, L.status, L.timeout_ns, L.sx);
     return e == cudaSuccess ? 0 : -1;
 }
 

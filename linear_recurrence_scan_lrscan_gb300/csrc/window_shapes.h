@@ -73,14 +73,6 @@ using XFB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1, false, false, true>;
 using XFF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, false, true>;
 using XFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, false, true>;
 
-// 64-lane exact shapes for the pipelined tiles (8 sub-chunks of 32 replay
-// threads plus 64 walker threads)
-using XPFF_64_2_8 = WinShape<float, 64, 2, 8, 2, 320, 1, false, false, true>;
-using XPFB_64_2_8 = WinShape<float, 64, 2, 8, 3, 320, 1, false, false, true>;
-
-#define LRSCAN_XWP_FWD_SHAPES(X) X(XBF_32_2_8_M5) X(XWBF_32_2_16) X(XPFF_64_2_8) X(XFF_32_1_8)
-#define LRSCAN_XWP_BWD_SHAPES(X) X(XBB_32_2_4_M5) X(XBB_32_2_8_M5) X(XWBB_32_2_16) X(XPFB_64_2_8) X(XFB_32_1_8)
-
 #define LRSCAN_WIN_FWD_SHAPES(X)                                                                   \
     X(SBF_64_2_32) X(SBF_128_2_32) X(SBF_128_4_32) X(SBF_32_1_32) X(SBF_64_1_32) X(SFF_32_1_32) \
     X(SFF_64_2_16) X(SFF_64_1_32) X(SFF_128_4_8) X(BF_64_2_8) X(BF_32_2_8) X(FF_16_1_8)          \

@@ -145,7 +145,7 @@ def test_exact_flag_of_every_tile_variant(lib):
         for path in ("seq", "window"):
             for v in range(1, L.lrscan_num_variants(path, dt) + 1):
                 p = L.lrscan_plan(4, 512, 1024, dt, "fwd", path=path, tile_variant=v)
-                want = path == "seq" or p["name"].startswith(("xwin_", "xwp_"))
+                want = path == "seq" or p["name"].startswith("xwin_")
                 assert p["exact"] == int(want), p
         assert L.lrscan_plan(1, 1 << 16, 64, dt, "fwd", path="chunk")["exact"] == 0
         assert L.lrscan_plan(4, 512, 1024, dt, "fwd", path="plain")["exact"] == 1
