@@ -450,11 +450,12 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     const bool issuer = static_cast<int>(threadIdx.x) == (NT > DT ? DT : 0);
     int replayed = 0;
     // EXT: this warp's rows start at window row wrow; bit j of rbits is a
-    // reset at row s*L + j of the current window (positions one window ahead)
+    // reset at row s*L + j of the current window (positions loaded two
+    // windows ahead)
     static_assert(!EXT || (G >= 32 ? 1 : 32 / G) * L <= 32, "one ballot covers a warp's rows");
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + static_cast<size_t>(brow) * T : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
-    int32_t pos_next = 1;
+    int32_t pos_next = 1, pos_next2 = 1;
     if constexpr (EXT) {
         if (static_cast<int>(threadIdx.x) < DT) {
             const int ch = lane_channel<C>(d0, threadIdx.x);
@@ -463,6 +464,7 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
             ci = (ch < D && sx.h0_i != nullptr) ? sx.h0_i[hs] : 0.0f;
         }
         pos_next = seg.at(wrow + lane);
+        pos_next2 = seg.at(sm.W + wrow + lane);
     }
     for (int k = 0; k < sm.nwin; ++k) {
         const int rbase = k * sm.W + s * L;
@@ -470,7 +472,8 @@ cwinw_fwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         uint32_t rbits = 0;
         if constexpr (EXT) {
             rbits = __ballot_sync(0xffffffffu, pos_next == 0) >> (s * L - wrow);
-            pos_next = seg.at((k + 1) * sm.W + wrow + lane);
+            pos_next = pos_next2;
+            pos_next2 = seg.at((k + 2) * sm.W + wrow + lane);
         }
         float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
         const bool ok = mbar_wait(sm.full_bar(stage), use & 1, wc, kSiteConsumerFull);
@@ -674,7 +677,7 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
     const size_t row0 = static_cast<size_t>(brow) * T;
     const SegRow seg{EXT ? (sx.seg != nullptr ? sx.seg + row0 : nullptr) : nullptr, T};
     const int wrow = ((threadIdx.x & ~31u) / G) * L;
-    int32_t pos0_next = 1, pos1_next = 1;
+    int32_t pos0_next = 1, pos1_next = 1, pos0_next2 = 1, pos1_next2 = 1;  // windows k+1, k+2
     float h0r[V], h0i[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) h0r[v] = h0i[v] = 0.0f;
@@ -696,6 +699,8 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         const int wb0 = (nwin - 1) * sm.W + wrow + lane;
         pos0_next = seg.at(wb0);
         pos1_next = seg.at(wb0 + 1);
+        pos0_next2 = seg.at(wb0 - sm.W);
+        pos1_next2 = seg.at(wb0 - sm.W + 1);
     }
     for (int k = 0; k < nwin; ++k) {
         const int wbase = (nwin - 1 - k) * sm.W;
@@ -705,9 +710,11 @@ cwinw_bwd_kernel(const __grid_constant__ CUtensorMap tm_ar, const __grid_constan
         if constexpr (EXT) {
             r0bits = __ballot_sync(0xffffffffu, pos0_next == 0) >> (s * L - wrow);
             r1bits = __ballot_sync(0xffffffffu, pos1_next == 0) >> (s * L - wrow);
-            const int wb = (nwin - 2 - k) * sm.W + wrow + lane;
-            pos0_next = seg.at(wb);
-            pos1_next = seg.at(wb + 1);
+            pos0_next = pos0_next2;
+            pos1_next = pos1_next2;
+            const int wb = (nwin - 3 - k) * sm.W + wrow + lane;
+            pos0_next2 = seg.at(wb);
+            pos1_next2 = seg.at(wb + 1);
         }
         float xr[L][V], xi[L][V], yr[L][V], yi[L][V];
         Raw pr[L], pi[L];

@@ -13,6 +13,12 @@ LRSCAN_WIN_FWD_SHAPES(LRSCAN_EXTERN_FWD)
 LRSCAN_WIN_BWD_SHAPES(LRSCAN_EXTERN_BWD)
 #undef LRSCAN_EXTERN_FWD
 #undef LRSCAN_EXTERN_BWD
+#define LRSCAN_EXTERN_WF(SH) extern template int launch_wfx<SH, false, true>(const WinLaunch &, const WinDirCfg &);
+#define LRSCAN_EXTERN_WB(SH) extern template int launch_wfx<SH, true, true>(const WinLaunch &, const WinDirCfg &);
+LRSCAN_WFX_FWD_SHAPES(LRSCAN_EXTERN_WF)
+LRSCAN_WFX_BWD_SHAPES(LRSCAN_EXTERN_WB)
+#undef LRSCAN_EXTERN_WF
+#undef LRSCAN_EXTERN_WB
 
 namespace {
 
@@ -44,8 +50,32 @@ WinDirCfg dir_cfg(int S, int nstage) {
     return d;
 }
 
+// Wavefront exact tiles: S consumer warps (one per sub-chunk) plus the producer.
+template <class C, bool FWD>
+WinDirCfg wdir_cfg(int S, int nstage) {
+    static_assert(C::EX && C::G == 32, "wavefront shape: one warp per sub-chunk");
+    const WinGeom g = make_win_geom<C>(S, nstage, 1, 1);
+    if (S < 2 || S * 32 + 32 > C::MAXT) std::abort();  // table error
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = S;
+    d.exact = 1;
+    d.w = g.W;
+    d.nstage = nstage;
+    d.threads = S * 32 + 32;
+    d.smem = win_out_smem(g, FWD ? 1 : 2, 3);
+    d.stage_bytes = g.stage_bytes;
+    d.launch = &launch_wfx<C, !FWD, false>;
+    d.launch_state = &launch_wfx<C, !FWD, true>;
+    return d;
+}
+
 #define F(SH, S, N) dir_cfg<SH, true>(S, N)
 #define B(SH, S, N) dir_cfg<SH, false>(S, N)
+#define WF(SH, S, N) wdir_cfg<SH, true>(S, N)
+#define WB(SH, S, N) wdir_cfg<SH, false>(S, N)
 
 
 const WinVariant kSeqBF16[] = {
@@ -77,6 +107,14 @@ const WinVariant kWinBF16[] = {
     {"xwin_bf16_d32_l4_s12_m5", F(XBF_32_2_4_M5, 12, 2), B(XBB_32_2_4_M5, 12, 2)},
     {"xwin_bf16_d32_l16_s8", F(XWBF_32_2_16, 8, 4), B(XWBB_32_2_16, 8, 4)},
     {"xwin_bf16_d32_s8_m5_n3", F(XBF_32_2_8_M5, 8, 3), B(XBB_32_2_8_M5, 8, 3)},
+    // wavefront exact tiles (the chain runs through one warp per sub-chunk)
+    {"wfx_bf16_d32_s4_l16", WF(WFF_BF_32_1_16, 4, 2), WB(WFB_BF_32_1_16, 4, 2)},
+    {"wfx_bf16_d32_s4_l16_n3", WF(WFF_BF_32_1_16, 4, 3), WB(WFB_BF_32_1_16, 4, 3)},
+    {"wfx_bf16_d32_s8_l8", WF(WFF_BF_32_1_8, 8, 2), WB(WFB_BF_32_1_8, 8, 2)},
+    {"wfx_bf16_d64_s4_l16_v2", WF(WFF_BF_64_2_16, 4, 2), WB(WFB_BF_64_2_16, 4, 2)},
+    {"wfx_bf16_d32_s2_l32", WF(WFF_BF_32_1_32, 2, 3), WB(WFB_BF_32_1_32, 2, 3)},
+    {"wfx_bf16_d32_s2_l16", WF(WFF_BF_32_1_16, 2, 3), WB(WFB_BF_32_1_16, 2, 3)},
+    {"wfx_bf16_d32_s3_l16", WF(WFF_BF_32_1_16, 3, 2), WB(WFB_BF_32_1_16, 3, 2)},
 };
 const WinVariant kSeqF32[] = {
     {"seq_f32_d32", F(SFF_32_1_32, 1, 8), B(SFB_32_1_32, 1, 6)},
@@ -95,10 +133,15 @@ const WinVariant kWinF32[] = {
     // exact walk (bit-identical to the sequential scan)
     {"xwin_f32_d64_s8", F(XFF_64_2_8, 8, 4), B(XFB_64_2_8, 8, 3)},
     {"xwin_f32_d32_s16", F(XFF_32_1_8, 16, 4), B(XFB_32_1_8, 16, 3)},
+    // wavefront exact tiles
+    {"wfx_f32_d32_s4_l16", WF(WFF_FF_32_1_16, 4, 2), WB(WFB_FF_32_1_16, 4, 2)},
+    {"wfx_f32_d64_s8_l8_v2", WF(WFF_FF_64_2_8, 8, 2), WB(WFB_FF_64_2_8, 8, 2)},
 };
 
 #undef F
 #undef B
+#undef WF
+#undef WB
 
 
 }  // namespace

@@ -262,13 +262,17 @@ const Pref kPrefBF16Fwd[] = {{kPathSeq, "seq_bf16_d128_n3", 2.0, kAny},
                              {kPathWindow, "win_bf16_d32_s8_m5_n2", 0.9, kAny},
                              {kPathSeq, "seq_bf16_d64_v1", 1.5, kAny},
                              {kPathWindow, "win_bf16_d32_s16", 0.9, kAny}};
-// bf16 backward: the sequential 128-lane tile with a two-stage ring (four
-// CTAs per SM, one wave) from two CTAs per SM (417.1 us on the near-unit
-// workload, exact, against 404.0 us re-associating and 432.2 us for the
-// four-stage tile); up to 5 CTAs per SM the exact window tile with 8
-// sub-chunks of 8 rows, five CTAs per SM (73.7 us on the gated workload, as
-// fast as the re-associating 12-sub-chunk tile's 73.4 us).
-const Pref kPrefBF16Bwd[] = {{kPathSeq, "seq_bf16_d128_n2", 2.0, kAny},
+// bf16 backward: from five 64-lane tiles per SM the wavefront exact tile (one
+// warp per 16-row sub-chunk, the chain handed from warp to warp: 407.9 us on
+// the near-unit workload, exact, against 404.0 us re-associating); from two
+// 128-lane tiles per SM the sequential tile with a two-stage ring (417.1 us
+// there, exact, four CTAs per SM, one wave); up to 5 CTAs per SM the
+// wavefront tile with three 16-row sub-chunks of 32 lanes, five CTAs per SM
+// (70.7 us on the gated workload, exact, against 73.4 us for the fastest
+// re-associating tile and 73.7 us for the exact walk-and-replay tile).
+const Pref kPrefBF16Bwd[] = {{kPathWindow, "wfx_bf16_d64_s4_l16_v2", 5.0, kAny},
+                             {kPathSeq, "seq_bf16_d128_n2", 2.0, kAny},
+                             {kPathWindow, "wfx_bf16_d32_s3_l16", 0.9, 5.0},
                              {kPathWindow, "xwin_bf16_d32_s8_m5_n2", 0.9, 5.0},
                              {kPathWindow, "win_bf16_d32_l4_s12_m5", 0.9, 5.0},
                              {kPathWindow, "win_bf16_d32_l16_s8", 0.9, kAny},

@@ -77,7 +77,7 @@ struct WinShape {
     static_assert(ROW_BYTES % 16 == 0, "tensor-copy rows are multiples of 16 bytes");
     static_assert(DT <= 256, "tensor-copy box limit");
     static_assert(L >= 1 && L <= 64, "rows per window (sequential) or per sub-chunk");
-    static_assert(SEQ || L <= 16, "windowed sub-chunks are held in registers");
+    static_assert(SEQ || L <= 16 || (EX_ && L <= 32), "windowed sub-chunks are held in registers");
 };
 
 // Launch-time geometry (filled by the host from S and the stage count).
@@ -137,7 +137,10 @@ template <int NP, class St, int NB = 2>
 struct OutStage {
     St *buf;
     int elems;  // W * DT
-    __device__ __forceinline__ St *plane(int kw, int p) const { return buf + ((NB == 1 ? 0 : kw & 1) * NP + p) * elems; }
+    __device__ __forceinline__ St *plane(int kw, int p) const {
+        const int b = NB == 1 ? 0 : (NB == 2 ? (kw & 1) : kw % NB);
+        return buf + (b * NP + p) * elems;
+    }
     // bulk tensor stores of processed window kw's planes at (x, y, z), one group
     __device__ __forceinline__ void store(const CUtensorMap *const (&maps)[NP], int kw, int x, int y, int z) const {
 #pragma unroll

@@ -73,6 +73,26 @@ using XFB_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 1, false, false, true>;
 using XFF_32_1_8 = WinShape<float, 32, 1, 8, 2, 544, 1, false, false, true>;
 using XFB_32_1_8 = WinShape<float, 32, 1, 8, 3, 544, 1, false, false, true>;
 
+// Wavefront exact shapes: one warp per sub-chunk (32 lane groups of V lanes).
+using WFF_BF_32_1_16 = WinShape<bf16_t, 32, 1, 16, 2, 160, 5, false, false, true>;
+using WFB_BF_32_1_16 = WinShape<bf16_t, 32, 1, 16, 3, 160, 5, false, false, true>;
+using WFF_BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 2, 288, 3, false, false, true>;
+using WFB_BF_32_1_8 = WinShape<bf16_t, 32, 1, 8, 3, 288, 3, false, false, true>;
+using WFF_BF_64_2_16 = WinShape<bf16_t, 64, 2, 16, 2, 160, 4, false, false, true>;
+using WFB_BF_64_2_16 = WinShape<bf16_t, 64, 2, 16, 3, 160, 4, false, false, true>;
+using WFF_FF_32_1_16 = WinShape<float, 32, 1, 16, 2, 160, 4, false, false, true>;
+using WFB_FF_32_1_16 = WinShape<float, 32, 1, 16, 3, 160, 4, false, false, true>;
+using WFF_FF_64_2_8 = WinShape<float, 64, 2, 8, 2, 288, 2, false, false, true>;
+using WFB_FF_64_2_8 = WinShape<float, 64, 2, 8, 3, 288, 2, false, false, true>;
+
+using WFF_BF_32_1_32 = WinShape<bf16_t, 32, 1, 32, 2, 96, 6, false, false, true>;
+using WFB_BF_32_1_32 = WinShape<bf16_t, 32, 1, 32, 3, 96, 6, false, false, true>;
+
+#define LRSCAN_WFX_FWD_SHAPES(X) \
+    X(WFF_BF_32_1_16) X(WFF_BF_32_1_8) X(WFF_BF_64_2_16) X(WFF_FF_32_1_16) X(WFF_FF_64_2_8) X(WFF_BF_32_1_32)
+#define LRSCAN_WFX_BWD_SHAPES(X) \
+    X(WFB_BF_32_1_16) X(WFB_BF_32_1_8) X(WFB_BF_64_2_16) X(WFB_FF_32_1_16) X(WFB_FF_64_2_8) X(WFB_BF_32_1_32)
+
 #define LRSCAN_WIN_FWD_SHAPES(X)                                                                   \
     X(SBF_64_2_32) X(SBF_128_2_32) X(SBF_128_4_32) X(SBF_32_1_32) X(SBF_64_1_32) X(SFF_32_1_32) \
     X(SFF_64_2_16) X(SFF_64_1_32) X(SFF_128_4_8) X(BF_64_2_8) X(BF_32_2_8) X(FF_16_1_8)          \

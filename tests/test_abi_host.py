@@ -87,9 +87,9 @@ def test_workspace_bytes(lib):
 
 EXPECTED_AUTO = {
     # workload: (forward tile, backward tile) the occupancy rule must pick
-    2: ("win_bf16_d32_s8_m5_n2", "xwin_bf16_d32_s8_m5_n2"),
+    2: ("win_bf16_d32_s8_m5_n2", "wfx_bf16_d32_s3_l16"),
     3: ("win_f32_d32_s31", "win_f32_d32_s16"),
-    4: ("seq_bf16_d128_n3", "seq_bf16_d128_n2"),
+    4: ("seq_bf16_d128_n3", "wfx_bf16_d64_s4_l16_v2"),
     5: ("seq_f32_d32", "xwin_f32_d64_s8"),
 }
 # which of those reproduce the sequential definition bit for bit
@@ -119,7 +119,7 @@ def test_state_plans(lib):
         assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", state=True)["name"] == want
         assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", state=True)["name"] == EXPECTED_AUTO[cid][0]
     w = WORKLOADS[4]
-    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[4][1] == "seq_bf16_d128_n2"
+    assert L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd")["name"] == EXPECTED_AUTO[4][1] == "wfx_bf16_d64_s4_l16_v2"
 
 
 def test_fp32_forward_prefers_the_exact_sequential_path_when_lanes_fill_the_gpu(lib):
@@ -145,7 +145,7 @@ def test_exact_flag_of_every_tile_variant(lib):
         for path in ("seq", "window"):
             for v in range(1, L.lrscan_num_variants(path, dt) + 1):
                 p = L.lrscan_plan(4, 512, 1024, dt, "fwd", path=path, tile_variant=v)
-                want = path == "seq" or p["name"].startswith("xwin_")
+                want = path == "seq" or p["name"].startswith(("xwin_", "wfx_"))
                 assert p["exact"] == int(want), p
         assert L.lrscan_plan(1, 1 << 16, 64, dt, "fwd", path="chunk")["exact"] == 0
         assert L.lrscan_plan(4, 512, 1024, dt, "fwd", path="plain")["exact"] == 1
