@@ -806,8 +806,8 @@ def run_long_t(dev, peak) -> dict:
 # Sources of the time-tiled real-scan kernels the benchmark's step runs (their
 # code, shapes, stage counts and launch): DRAM counters recorded under another
 # hash of these files are stale.
-TILED_KERNEL_SOURCES = ("scan_common.cuh", "state_args.h", "window_kernels.cuh", "window_shapes.h",
-                        "window_launch.cuh", "kernels_window.cu")
+TILED_KERNEL_SOURCES = ("scan_common.cuh", "state_args.h", "window_kernels.cuh", "wavefront_kernels.cuh",
+                        "window_shapes.h", "window_launch.cuh", "kernels_window.cu")
 
 
 def kernel_source_hash() -> str:

@@ -121,6 +121,8 @@ const WinVariant kSeqF32[] = {
     {"seq_f32_d64", F(SFF_64_2_16, 1, 8), B(SFB_64_2_16, 1, 6)},
     {"seq_f32_d64_v1", F(SFF_64_1_32, 1, 4), B(SFB_64_1_32, 1, 4)},
     {"seq_f32_d128", F(SFF_128_4_8, 1, 8), B(SFB_128_4_8, 1, 6)},
+    // a shallower ring: more CTAs resident per SM
+    {"seq_f32_d64_v1_n3", F(SFF_64_1_32, 1, 3), B(SFB_64_1_32, 1, 2)},
 };
 const WinVariant kWinF32[] = {
     {"win_f32_d32_s16_pt", F(PF_32_1_8, 16, 4), B(PFB_32_1_8, 16, 3)},

@@ -244,7 +244,11 @@ constexpr double kAny = 1e30;
 // fp32 forward with few lane tiles: one 32-warp CTA per tile (31 sub-chunks
 // of 8 rows): 333.6 us on the long fp32 workload against 372.5 us for 16
 // sub-chunks.
-const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d32", 1.5, kAny}, {kPathWindow, "win_f32_d32_s31", 0.45, kAny}};
+// With many lane tiles, the 64-lane one-lane-per-thread tile with a three-stage
+// ring (61.4 us on the padded workload against 63.4 us for the 32-lane tile).
+const Pref kPrefF32Fwd[] = {{kPathSeq, "seq_f32_d64_v1_n3", 3.0, kAny},
+                            {kPathSeq, "seq_f32_d32", 1.5, kAny},
+                            {kPathWindow, "win_f32_d32_s31", 0.45, kAny}};
 // fp32 backward with many lane tiles: the exact 64-lane window tile (102.1 us
 // on the padded workload against 100.0 us for the re-associating one and
 // 105.7 us for the fastest sequential tile)

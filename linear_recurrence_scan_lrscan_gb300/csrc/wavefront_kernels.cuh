@@ -46,8 +46,11 @@ wfx_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUt
     const int NT = S * 32;
     float *xfer = reinterpret_cast<float *>(smem_raw + geom.scan_off);  // [S][DT] state handed to warp s
     auto hb = [&](int q) { return smem_addr(smem_raw + geom.scan_off + S * DT * 4 + q * 8); };
+    // staged[k & 1]: the other warps' output rows of window k are written
+    auto staged = [&](int q) { return smem_addr(smem_raw + geom.scan_off + S * DT * 4 + S * 8 + q * 8); };
     if (threadIdx.x == 0) {
         for (int q = 0; q < S; ++q) mbar_init(hb(q), 32);
+        for (int q = 0; q < 2; ++q) mbar_init(staged(q), (S - 1) * 32);
     }
     win_init<C>(sm, S, S);  // full / empty barriers, abort flag; syncs the CTA
     pdl_trigger();
@@ -190,25 +193,47 @@ wfx_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUt
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = xfer[s * DT + lane * V + v];
         }
-        // the chain through this sub-chunk's rows
-        St *o0 = ost.plane(k, 0) + (s * L) * DT + lane * V;
+        // the chain through this sub-chunk's rows: the fused multiply-adds
+        // alone, so that the state moves on before the conversions and stores
+        float hr[L][V];
 #pragma unroll
         for (int q = 0; q < L; ++q) {
             const int j = BWD ? L - 1 - q : q;
 #pragma unroll
-            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+            for (int v = 0; v < V; ++v) {
+                h[v] = __fmaf_rn(xa[j][v], h[v], xb[j][v]);
+                hr[j][v] = h[v];
+            }
+        }
+        if (closer) {
+            // the store of window k-2 has finished reading the buffer window
+            // k+1 takes (the latest store, of k-1, may still be reading)
+            __syncwarp();
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+        }
+        // hand the state to the next sub-chunk in chain order
+        if (!(closer && k + 1 == nwin)) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) xfer[succ * DT + lane * V + v] = h[v];
+            mbar_arrive(hb(succ));
+        }
+        // this sub-chunk's outputs into the window's stage
+        St *o0 = ost.plane(k, 0) + (s * L) * DT + lane * V;
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
             if constexpr (BWD) {
                 float ga[V];
                 const bool z = EXT && ((r0bits >> j) & 1u);  // a_t unused at a segment start
 #pragma unroll
-                for (int v = 0; v < V; ++v) ga[v] = z ? 0.0f : __fmul_rn(h[v], xh[j][v]);
+                for (int v = 0; v < V; ++v) ga[v] = z ? 0.0f : __fmul_rn(hr[j][v], xh[j][v]);
                 store_lanes<St, V>(o0 + j * DT, ga);
-                store_lanes<St, V>(ost.plane(k, 1) + (s * L + j) * DT + lane * V, h);
+                store_lanes<St, V>(ost.plane(k, 1) + (s * L + j) * DT + lane * V, hr[j]);
             } else {
-                store_lanes<St, V>(o0 + j * DT, h);
+                store_lanes<St, V>(o0 + j * DT, hr[j]);
                 if (last != nullptr && lane_ok && j == n - 1 && rbase + n == T) {
 #pragma unroll
-                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = hr[j][v];
                 }
             }
         }
@@ -216,19 +241,16 @@ wfx_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUt
             if (rbase == 0 && sx.grad_h0 != nullptr && lane_ok) store_grad_h0<C>(sx, seg, row0, brow, d, D, h);
         }
         fence_proxy_async_smem();  // the staged rows, for the closing warp's bulk store
-        if (closer) {
+        if (!closer) {
+            mbar_arrive(staged(k & 1));
+        } else {
+            ok = mbar_wait(staged(k & 1), (k >> 1) & 1, wc, kSiteHandoff);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { failed = true; break; }
             __syncwarp();
-            if (lane == 0) {
-                ost.store(omaps, k, d0, wbase, brow);
-                bulk_wait_read<2>();  // the store of window k-2 is done with the buffer k+1 takes
-            }
+            if (lane == 0) ost.store(omaps, k, d0, wbase, brow);
             __syncwarp();
-            if (k + 1 == nwin) break;
         }
-        // hand the state to the next sub-chunk in chain order
-#pragma unroll
-        for (int v = 0; v < V; ++v) xfer[succ * DT + lane * V + v] = h[v];
-        mbar_arrive(hb(succ));
     }
     if (closer && lane == 0) bulk_wait<0>();
     (void)failed;

@@ -90,7 +90,7 @@ EXPECTED_AUTO = {
     2: ("win_bf16_d32_s8_m5_n2", "wfx_bf16_d32_s3_l16"),
     3: ("win_f32_d32_s31", "win_f32_d32_s16"),
     4: ("seq_bf16_d128_n3", "wfx_bf16_d64_s4_l16_v2"),
-    5: ("seq_f32_d32", "xwin_f32_d64_s8"),
+    5: ("seq_f32_d64_v1_n3", "xwin_f32_d64_s8"),
 }
 # which of those reproduce the sequential definition bit for bit
 EXPECTED_EXACT = {2: (False, True), 3: (False, False), 4: (True, True), 5: (True, True)}
