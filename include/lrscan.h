@@ -73,11 +73,19 @@ extern "C" {
 #define LRSCAN_PATH_CHUNK   2  /* three phases: chunk summary -> warp-shuffle prefix -> replay */
 #define LRSCAN_PATH_WINDOW  3  /* single pass: time windows in shared memory, split in time inside the CTA */
 #define LRSCAN_PATH_PLAIN   4  /* sequential, plain loads; any alignment */
+#define LRSCAN_PATH_STREAM  5  /* single pass over time chunks (triton_training_scan.py, _real_chunk_summary /
+                                  _real_chunk_prefix / _real_chunk_replay fused): persistent CTAs take chunks of
+                                  512 steps in ticket order, publish each chunk's map, find its entering state by
+                                  looking back over the published maps and leaving states, and replay it while its
+                                  tiles are still in L2.  Bulk-copy path (16-byte aligned rows); plain scan only
+                                  (no carried state); needs workspace_bytes of device scratch like the chunked
+                                  path; agrees with the sequential definition to rounding.  tile_variant:
+                                  1 = 32-lane tiles, 2 = 64-lane tiles */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */
     int chunk_len;          /* chunked path: 16, 32, 64, 128, 256 or 512; 0 = 64, or for long sequences on few lanes (grouped prefix) 512 forward and 128 backward */
-    void *workspace;        /* chunked path: optional caller-owned device workspace ... */
+    void *workspace;        /* chunked and streaming paths: optional caller-owned device workspace ... */
     size_t workspace_bytes; /* ... of at least lrscan_workspace_bytes() bytes; NULL = library-owned */
     int tile_variant;       /* >= 1 forces one kernel tile variant of the path (lrscan_plan lists them); 0 = auto.
                                Chunked path: 1 = flat prefix (one warp per lane walks all chunk maps),
@@ -89,7 +97,7 @@ typedef struct lrscan_plan_info {
     int path;               /* LRSCAN_PATH_* actually taken */
     int tile_variant;       /* variant id within the path */
     int lanes_per_cta;      /* channel lanes one CTA owns */
-    int rows_per_window;    /* time steps per shared-memory window (SEQ/WINDOW) or chunk length (CHUNK) */
+    int rows_per_window;    /* time steps per shared-memory window (SEQ/WINDOW/STREAM) or chunk length (CHUNK) */
     int subchunks;          /* time splits inside a window (WINDOW), 1 otherwise */
     int stages;             /* shared-memory pipeline depth */
     int ctas;               /* CTAs of the main kernel */

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liblrscan.so")
-SOURCES = ["lrscan_abi.cu", "kernels_window.cu", "kernels_window_state.cu", "kernels_chunk.cu", "kernels_complex.cu", "kernels_complex_state.cu", "kernels_complex_chunk.cu", "kernels_gated.cu", "noalloc_chunk.cu", "host_pipeline.cu"]
+SOURCES = ["lrscan_abi.cu", "kernels_window.cu", "kernels_window_state.cu", "kernels_chunk.cu", "kernels_complex.cu", "kernels_complex_state.cu", "kernels_complex_chunk.cu", "kernels_stream.cu", "kernels_gated.cu", "noalloc_chunk.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -34,7 +34,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 struct DevStatus;
 
-enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3, kPathPlain = 4 };
+enum PathId : int { kPathAuto = 0, kPathSeq = 1, kPathChunk = 2, kPathWindow = 3, kPathPlain = 4, kPathStream = 5 };
 
 // Arguments of one time-tiled launch (forward: maps a,b / out0=out;
 // backward: maps a,out,grad_out / out0=grad_a, out1=grad_b).
@@ -58,6 +58,8 @@ struct WinLaunch {
     float *part_eta, *part_nu;
     int64_t part_rows;            // column stride of part_eta: rows B*T of the whole call
     const void *in0, *in1;
+    StreamArgs sa;                // persistent chunk-streaming kernels: publication workspace
+    int grid;                     // persistent chunk-streaming kernels: CTAs to launch
 };
 
 // One direction of a tile variant: compiled shape (DT, V, L) plus the
@@ -74,6 +76,7 @@ struct WinDirCfg {
     int threads;     // s*(dt/v) + 32
     int smem;        // dynamic shared memory bytes
     int stage_bytes;
+    int max_resident;  // CTAs per SM the registers allow (0: not limited beyond threads and shared memory)
     int (*launch)(const WinLaunch &, const WinDirCfg &);        // plain scan
     int (*launch_state)(const WinLaunch &, const WinDirCfg &);  // with carried state / resets
 };
@@ -85,6 +88,10 @@ struct WinVariant {
 
 // path: kPathSeq or kPathWindow; dtype 0 = f32, 1 = bf16
 const WinVariant *win_variants(int path, int dtype, int *count);
+
+// Persistent chunk-streaming variants (kernels_stream.cu); dtype 0 = f32,
+// 1 = bf16.
+const WinVariant *stream_variants(int dtype, int *count);
 
 // Complex scan tile variants (kernels_complex.cu); dtype 0 = f32, 1 = bf16.
 const WinVariant *cwin_variants(int dtype, int *count);

@@ -184,6 +184,24 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = tr
     return chunk_scratch(B, T, D, C, grouped).total();
 }
 
+// Chunk-streaming workspace: the ticket word (first 256 bytes), one flag per
+// chunk, then the chunk maps (float2 per lane) and leaving states (float per
+// lane); the ticket and flags are zeroed before every launch.
+constexpr int kStreamWindowsPerChunk = 8;
+struct StreamScratch {
+    size_t head;  // ticket + flags
+    size_t agg, incl;
+    size_t total() const { return head + agg + incl; }
+};
+StreamScratch stream_scratch(int64_t ng, int64_t nc, int dt) {
+    auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
+    StreamScratch s;
+    s.head = 256 + pad(static_cast<size_t>(ng) * nc * 4);
+    s.agg = pad(static_cast<size_t>(ng) * nc * dt * 8);
+    s.incl = pad(static_cast<size_t>(ng) * nc * dt * 4);
+    return s;
+}
+
 // The grouped prefix pays when every lane has many chunks and the lanes alone
 // give the GPU few warps to run the flat per-lane prefix.
 bool use_grouped_prefix(int64_t B, int64_t T, int64_t D, int C, const Geometry &g) {
@@ -331,8 +349,10 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
     ch->vec = (aligned16 && D % vmax == 0) ? vmax : 1;
 
     int path = want;
-    if (want < kPathAuto || want > kPathPlain) return fail(LRSCAN_EINVAL, "unknown path %d", want);
-    if ((path == kPathSeq || path == kPathWindow) && !aligned16)
+    if (want < kPathAuto || want > kPathStream) return fail(LRSCAN_EINVAL, "unknown path %d", want);
+    if (path == kPathStream && ext)
+        return fail(LRSCAN_EINVAL, "the chunk-streaming path carries no state or resets");
+    if ((path == kPathSeq || path == kPathWindow || path == kPathStream) && !aligned16)
         return fail(LRSCAN_EINVAL, "path %d needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)", path);
     int auto_vi = -1;
     if (path == kPathAuto) {
@@ -380,6 +400,29 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         ch->dir = dir;
         ch->kernels = 1;
         ch->workspace = 0;
+    } else if (path == kPathStream) {
+        int n = 0;
+        const WinVariant *tab = stream_variants(dtype, &n);
+        if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
+        const int vi = force_v > 0 ? force_v - 1 : 0;
+        const WinDirCfg &v = dir_of(tab[vi], dir);
+        const Occ o = occupancy(tab[vi], dir, B, D, g);
+        if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);
+        const int64_t ng = B * ((D + v.dt - 1) / v.dt);
+        const int64_t rows = static_cast<int64_t>(kStreamWindowsPerChunk) * v.w;
+        const int64_t nc = (T + rows - 1) / rows;
+        if (ng * nc > 0x7fffffffLL) return fail(LRSCAN_EINVAL, "too many chunks for the streaming path");
+        ch->vidx = vi;
+        ch->var = &tab[vi];
+        ch->chunk = static_cast<int>(rows);
+        const int resident = v.max_resident > 0 ? std::min(o.resident, v.max_resident) : o.resident;
+        ch->ctas = std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count);
+        ch->threads = v.threads;
+        ch->smem = v.smem;
+        ch->stages = v.nstage;
+        ch->dir = dir;
+        ch->kernels = 1;
+        ch->workspace = stream_scratch(ng, nc, v.dt).total();
     } else if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix
         if (force_v > 2) return fail(LRSCAN_EINVAL, "the chunked path has two variants (1 flat, 2 grouped prefix)");
@@ -594,6 +637,54 @@ int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_
     return LRSCAN_OK;
 }
 
+// The persistent chunk-streaming path: tensor maps of the inputs (forward a,
+// b; backward a, out, grad_out) and outputs (forward out; backward grad_a,
+// grad_b), the publication workspace zeroed where the kernel expects it, one
+// launch.
+int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::initializer_list<void *> outs,
+               float *last, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev, DeviceCtx *ctx,
+               const lrscan_opts *opts, bool bwd) {
+    const WinDirCfg &v = dir_of(*ch.var, bwd ? 1 : 0);
+    const int64_t ndt = (D + v.dt - 1) / v.dt;
+    const int64_t ng = B * ndt;
+    const int64_t nc = (T + ch.chunk - 1) / ch.chunk;
+    const StreamScratch sc = stream_scratch(ng, nc, v.dt);
+    void *ws = nullptr;
+    int rc = workspace_for(ctx, st, ch.workspace, opts, &ws);
+    if (rc) return rc;
+    CUtensorMap maps[5];
+    int k = 0;
+    for (const void *p : ins)
+        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+    for (void *p : outs)
+        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+    WinLaunch L{};
+    for (int i = 0; i < k; ++i) L.maps[i] = &maps[i];
+    L.last = last;
+    L.B = B; L.T = T; L.D = D;
+    L.status = ctx->status;
+    L.timeout_ns = g_timeout_ns.load();
+    L.stream = st;
+    L.device = dev;
+    char *base = static_cast<char *>(ws);
+    L.sa.ticket = reinterpret_cast<unsigned int *>(base);
+    L.sa.flag = reinterpret_cast<uint32_t *>(base + 256);
+    L.sa.agg = reinterpret_cast<float2 *>(base + sc.head);
+    L.sa.incl = reinterpret_cast<float *>(base + sc.head + sc.agg);
+    L.sa.nc = static_cast<int>(nc);
+    L.sa.nwc = ch.chunk / v.w;
+    L.sa.ndt = static_cast<int>(ndt);
+    L.sa.ng = static_cast<int>(ng);
+    L.grid = static_cast<int>(ch.ctas);
+    if (cudaMemsetAsync(ws, 0, sc.head, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
+    }
+    if (v.launch(L, v))
+        return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
+    return LRSCAN_OK;
+}
+
 int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int64_t T, int64_t D, int dtype,
             void *stream, const lrscan_opts *opts, const lrscan_state *state = nullptr) {
     t_detail[0] = 0;
@@ -640,6 +731,7 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
         }
         return LRSCAN_OK;
     }
+    if (ch.path == kPathStream) return run_stream(ch, {a, b}, {out}, last, B, T, D, dtype, st, dev, ctx, opts, false);
     ChunkLaunch L{};
     L.in0 = a; L.in1 = b; L.out0 = out; L.last = last;
     L.B = B; L.T = T; L.D = D;
@@ -703,6 +795,8 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
         }
         return LRSCAN_OK;
     }
+    if (ch.path == kPathStream)
+        return run_stream(ch, {a, out, grad_out}, {grad_a, grad_b}, nullptr, B, T, D, dtype, st, dev, ctx, opts, true);
     ChunkLaunch L{};
     L.in0 = a; L.in1 = out; L.in2 = grad_out; L.out0 = grad_a; L.out1 = grad_b;
     L.B = B; L.T = T; L.D = D;
@@ -1507,6 +1601,11 @@ int lrscan_num_variants(int path, int dtype, int dir) {
     if (path == kPathSeq || path == kPathWindow) {
         int n = 0;
         win_variants(path, dtype, &n);
+        return n;
+    }
+    if (path == kPathStream) {
+        int n = 0;
+        stream_variants(dtype, &n);
         return n;
     }
     if (path == kPathChunk || path == kPathPlain) return 1;

@@ -27,7 +27,7 @@ LRSCAN_ETIMEOUT = -5
 LRSCAN_ENODEVICE = -6
 
 F32, BF16 = 0, 1
-PATHS = {"auto": 0, "seq": 1, "chunk": 2, "window": 3, "plain": 4}
+PATHS = {"auto": 0, "seq": 1, "chunk": 2, "window": 3, "plain": 4, "stream": 5}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 

@@ -299,3 +299,33 @@ def test_complex_chunked_plans(lib):
     for bad in (dict(chunk_len=48), dict(tile_variant=3)):
         with pytest.raises(L.LrscanError):
             L.lrscan_plan_complex(1, 4096, 64, "f32", "fwd", path="chunk", **bad)
+
+
+def test_stream_plans(lib):
+    """The persistent chunk-streaming path: 512-step chunks (eight 64-row
+    windows), at most the resident CTAs of the GPU, its publication workspace
+    (ticket, one flag per chunk, a map and a state per chunk and lane), and
+    refusals where it cannot run."""
+    pad = lambda x: (x + 255) // 256 * 256
+    for dt, names in (("f32", ("stream_f32_d32_s8", "stream_f32_d64_s8")),
+                      ("bf16", ("stream_bf16_d32_s8", "stream_bf16_d64_s8"))):
+        assert L.lrscan_num_variants("stream", dt) == 2
+        for v, name in enumerate(names, 1):
+            for direction in ("fwd", "bwd"):
+                B, T, D = 1, 1 << 22, 64
+                p = L.lrscan_plan(B, T, D, dt, direction, path="stream", tile_variant=v)
+                assert p["path"] == "stream" and p["name"] == name and p["exact"] == 0, p
+                assert p["rows_per_window"] == 64 and p["subchunks"] == 8 and p["kernels"] == 1
+                dtl = p["lanes_per_cta"]
+                ng, nc = B * -(-D // dtl), -(-T // 512)
+                assert p["workspace_bytes"] == 256 + pad(ng * nc * 4) + pad(ng * nc * dtl * 8) + pad(ng * nc * dtl * 4)
+                assert 0 < p["ctas"] <= min(ng * nc, 2 * 152) and p["ctas"] % 152 == 0, p
+                assert p["threads_per_cta"] == 8 * 32 + 32
+    # a short sequence: no more CTAs than chunk tickets
+    assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 2
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=3)

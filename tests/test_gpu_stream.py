@@ -1,0 +1,90 @@
+"""GPU parity of the persistent chunk-streaming path (path "stream") against
+the CPU oracle: forward and backward, both storage dtypes, every variant, on
+shapes with ragged lane tiles, partial chunks, one-step sequences, and more
+chunks than CTAs (so every CTA takes several tickets and looks back over
+chunks published by others)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_scan_lrscan_gb300 import lrscan as L
+from linear_recurrence_scan_lrscan_gb300.workloads import random_inputs
+from parity_util import assert_close, assert_last_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L.lib()
+    yield
+    assert L.lrscan_sync_check() == 0
+
+
+ORC = None
+
+
+def orc():
+    global ORC
+    if ORC is None:
+        ORC = oracle.default()
+    return ORC
+
+
+def from_np(x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x))
+
+
+SHAPES = [(1, 1, 32), (1, 511, 32), (1, 512, 64), (1, 513, 64), (3, 700, 32), (2, 3001, 96), (1, 5000, 64),
+          (2, 40000, 32)]
+
+
+def check(B, T, D, dt, variant, seed, a_lo=0.6):
+    inp = random_inputs(B, T, D, dt, seed=seed, a_lo=a_lo, a_hi=1.0)
+    a, b, g = inp["a"], inp["b"], inp["grad_out"]
+    o = orc()
+    ref_out, ref_last = o.fwd(to_np(a), to_np(b), dt)
+    kw = dict(path="stream", tile_variant=variant)
+    plan = L.lrscan_plan(B, T, D, dt, "fwd", **kw)
+    assert plan["path"] == "stream" and not plan["exact"]
+    out, last = L.lrscan_fwd(a.cuda(), b.cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    name = f"{plan['name']} B={B} T={T} D={D}"
+    assert_close(to_np(out), ref_out, dt, f"out[{name}]", reassociated=True)
+    assert_last_close(last.cpu().numpy(), ref_last, f"last[{name}]")
+    if dt == "f32":
+        assert np.array_equal(last.cpu().numpy(), to_np(out)[:, -1, :])
+    ref_ga, ref_gb = o.bwd(to_np(a), ref_out, to_np(g), dt)
+    ga, gb = L.lrscan_bwd(a.cuda(), from_np(ref_out, dt).cuda(), g.cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    assert_close(to_np(gb), ref_gb, dt, f"grad_b[{name}]", reassociated=True)
+    assert_close(to_np(ga), ref_ga, dt, f"grad_a[{name}]", reassociated=True)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("shape_i", range(len(SHAPES)))
+def test_stream_parity(dt, variant, shape_i):
+    B, T, D = SHAPES[shape_i]
+    check(B, T, D, dt, variant, seed=900 + shape_i)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_stream_many_chunks_per_cta(dt):
+    """1,024 chunk tickets (two 32-lane groups x 512 chunks): several per CTA."""
+    B, T, D = 1, 1 << 18, 64
+    plan = L.lrscan_plan(B, T, D, dt, "fwd", path="stream", tile_variant=1)
+    assert plan["ctas"] < 2 * ((T + plan["rows_per_window"] * 8 - 1) // (plan["rows_per_window"] * 8))
+    check(B, T, D, dt, 1, seed=950, a_lo=0.9)
+
+
+def test_stream_refuses_state():
+    a = torch.rand(1, 64, 32, device="cuda")
+    h0 = torch.zeros(1, 32, device="cuda")
+    with pytest.raises(RuntimeError):
+        L.lrscan_fwd_state(a, a, h0=h0, path="stream")
