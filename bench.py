@@ -764,9 +764,10 @@ def run_gated(iters: int, dev, peak) -> dict:
 def run_long_t(dev, peak) -> dict:
     """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32: the chunked path
     with chunk 64 (65,536 chunk maps per lane, 64 lanes) with the flat prefix
-    (one warp per lane walks all maps) and with the grouped prefix, and the
-    automatic plan (grouped prefix over 512-step chunks forward, 128-step
-    chunks backward).  Inputs are drawn on
+    (one warp per lane walks all maps) and with the grouped prefix, the
+    single-pass chunk-streaming path on 32- and 64-lane tiles, and the
+    automatic plan (grouped prefix over 512-step chunks forward, streaming
+    backward).  Inputs are drawn on
     the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 
@@ -781,8 +782,10 @@ def run_long_t(dev, peak) -> dict:
     stream = torch.cuda.current_stream()
     E = B * T * D
     res = {"workload": f"B={B} T={T} D={D} fp32 chunk {C} (few lanes, long sequence)"}
-    for variant, name in ((1, "flat_prefix"), (2, "grouped_prefix")):
-        kw = dict(path="chunk", chunk_len=C, tile_variant=variant)
+    for kw, name in ((dict(path="chunk", chunk_len=C, tile_variant=1), "flat_prefix"),
+                     (dict(path="chunk", chunk_len=C, tile_variant=2), "grouped_prefix"),
+                     (dict(path="stream", tile_variant=1), "stream_d32"),
+                     (dict(path="stream", tile_variant=2), "stream_d64")):
         fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last, **kw), 10, stream)
         bms = time_launches(lambda i: L.lrscan_bwd(a, out, g, ga, gb, **kw), 10, stream)
         res[name] = {"fwd_ms": fms, "bwd_ms": bms,
@@ -797,7 +800,7 @@ def run_long_t(dev, peak) -> dict:
                         "elements/s": 2 * E / ((fms + bms) * 1e-3)}
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the long-sequence chunked path")
-    res["auto"] = L.lrscan_plan(B, T, D, "f32", "fwd")["name"]
+    res["auto"] = {d: L.lrscan_plan(B, T, D, "f32", d)["name"] for d in ("fwd", "bwd")}
     del a, b, g, out, ga, gb
     torch.cuda.empty_cache()
     return res

@@ -186,17 +186,17 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = tr
 
 // Chunk-streaming workspace: the ticket word (first 256 bytes), one flag per
 // chunk, then the chunk maps (float2 per lane) and leaving states (float per
-// lane); the ticket and flags are zeroed before every launch.
-constexpr int kStreamWindowsPerChunk = 8;
+// lane); the ticket and the flags are zeroed before every launch.
 struct StreamScratch {
-    size_t head;  // ticket + flags
+    size_t flags;  // byte size, padded to 256
     size_t agg, incl;
-    size_t total() const { return head + agg + incl; }
+    size_t head() const { return 256 + flags; }
+    size_t total() const { return head() + agg + incl; }
 };
 StreamScratch stream_scratch(int64_t ng, int64_t nc, int dt) {
     auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
     StreamScratch s;
-    s.head = 256 + pad(static_cast<size_t>(ng) * nc * 4);
+    s.flags = pad(static_cast<size_t>(ng) * nc * 4);
     s.agg = pad(static_cast<size_t>(ng) * nc * dt * 8);
     s.incl = pad(static_cast<size_t>(ng) * nc * dt * 4);
     return s;
@@ -362,8 +362,15 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
             // measured preference list (see auto_candidate)
         } else if (T >= 16LL * chunk) {
             // too few lanes for a lane-tiled walk to fill the GPU: parallelize
-            // over time chunks instead
+            // over time chunks instead -- in one pass (chunk streaming) where
+            // that measured faster than the three chunked phases: bf16, the
+            // fp32 backward, and the fp32 forward from 256 lanes (B=1 T=2^22
+            // D=64 fp32 forward: 0.87 ms chunked against 0.98 ms streamed;
+            // backward 1.27 against 1.24 ms; bf16 0.72 / 0.81 against 0.58 /
+            // 0.70 ms; B=8 T=2^18 D=64 fp32 0.50 / 0.74 against 0.42 / 0.56 ms)
             path = kPathChunk;
+            const bool long_seq = T >= 64LL * 256;  // 64 chunks of 256 steps per lane group
+            if (!ext && long_seq && (dtype == LRSCAN_BF16 || dir == 1 || B * D >= 256)) path = kPathStream;
         } else {
             path = kPathSeq;  // small problem: latency-bound whatever runs it
         }
@@ -404,19 +411,30 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         int n = 0;
         const WinVariant *tab = stream_variants(dtype, &n);
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
-        const int vi = force_v > 0 ? force_v - 1 : 0;
+        // 64-lane tiles where they give four lane groups (fp32) or wherever
+        // a row holds 64 lanes (bf16); else 32-lane tiles
+        int vi = force_v > 0 ? force_v - 1 : 0;
+        if (force_v == 0 && n > 1)
+            vi = (dtype == LRSCAN_BF16 ? D >= 64 : B * ((D + 63) / 64) >= 4) ? 1 : 0;
         const WinDirCfg &v = dir_of(tab[vi], dir);
         const Occ o = occupancy(tab[vi], dir, B, D, g);
         if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);
         const int64_t ng = B * ((D + v.dt - 1) / v.dt);
-        const int64_t rows = static_cast<int64_t>(kStreamWindowsPerChunk) * v.w;
+        const int64_t rows = static_cast<int64_t>(v.s) * v.w;  // window warps x rows each
         const int64_t nc = (T + rows - 1) / rows;
         if (ng * nc > 0x7fffffffLL) return fail(LRSCAN_EINVAL, "too many chunks for the streaming path");
         ch->vidx = vi;
         ch->var = &tab[vi];
         ch->chunk = static_cast<int>(rows);
         const int resident = v.max_resident > 0 ? std::min(o.resident, v.max_resident) : o.resident;
-        ch->ctas = std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count);
+        // A chunk's tiles must still be in L2 when its replay reads them: a CTA
+        // brings about 3.5 chunks' worth of input planes into L2 between a
+        // chunk's summary and its replay (the replay trails by two chunks), so
+        // the grid keeps that under 48 MB.
+        const long long chunk_in = rows * v.dt * esize(dtype) * 2;
+        const long long l2_ctas = std::max<long long>(g.sm_count, (48LL << 20) * 2 / (7 * chunk_in));
+        ch->ctas = std::min<long long>(std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count),
+                                       l2_ctas);
         ch->threads = v.threads;
         ch->smem = v.smem;
         ch->stages = v.nstage;
@@ -652,14 +670,15 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
     void *ws = nullptr;
     int rc = workspace_for(ctx, st, ch.workspace, opts, &ws);
     if (rc) return rc;
-    CUtensorMap maps[5];
+    CUtensorMap maps[3];
     int k = 0;
     for (const void *p : ins)
         if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
-    for (void *p : outs)
-        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
     WinLaunch L{};
     for (int i = 0; i < k; ++i) L.maps[i] = &maps[i];
+    auto o = outs.begin();
+    L.out0 = *o;
+    L.out1 = outs.size() > 1 ? *(o + 1) : nullptr;
     L.last = last;
     L.B = B; L.T = T; L.D = D;
     L.status = ctx->status;
@@ -669,14 +688,14 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
     char *base = static_cast<char *>(ws);
     L.sa.ticket = reinterpret_cast<unsigned int *>(base);
     L.sa.flag = reinterpret_cast<uint32_t *>(base + 256);
-    L.sa.agg = reinterpret_cast<float2 *>(base + sc.head);
-    L.sa.incl = reinterpret_cast<float *>(base + sc.head + sc.agg);
+    L.sa.agg = reinterpret_cast<float2 *>(base + sc.head());
+    L.sa.incl = reinterpret_cast<float *>(base + sc.head() + sc.agg);
     L.sa.nc = static_cast<int>(nc);
-    L.sa.nwc = ch.chunk / v.w;
+    L.sa.nwc = v.s;
     L.sa.ndt = static_cast<int>(ndt);
     L.sa.ng = static_cast<int>(ng);
     L.grid = static_cast<int>(ch.ctas);
-    if (cudaMemsetAsync(ws, 0, sc.head, st) != cudaSuccess) {
+    if (cudaMemsetAsync(ws, 0, sc.head(), st) != cudaSuccess) {
         cudaGetLastError();
         return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
     }

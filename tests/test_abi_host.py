@@ -153,13 +153,24 @@ def test_exact_flag_of_every_tile_variant(lib):
 
 
 def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
-    # 2^20 steps and only 64 lanes: the grouped prefix (5 kernels) with the
-    # longer chunks, 512 steps forward (2,048 chunks per lane) and 128 backward
-    for direction, c in (("fwd", 512), ("bwd", 128)):
-        p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction)
-        assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
-        assert p["rows_per_window"] == c and p["name"].startswith(f"chunk{c}")
-        assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, c)
+    # 2^20 steps and only 64 fp32 lanes: the forward takes the grouped prefix
+    # (5 kernels) with 512-step chunks (2,048 chunks per lane); the backward
+    # streams the chunks in one pass (with state it keeps the chunked path:
+    # 128-step chunks)
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
+    assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
+    assert p["rows_per_window"] == 512 and p["name"].startswith("chunk512")
+    assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
+    assert L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd")["name"] == "stream_f32_d32"
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", state=True)
+    assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
+    # bf16, or 256 fp32 lanes and more: both directions streamed, on 64-lane tiles
+    for (B, D, dt) in ((1, 64, "bf16"), (8, 64, "f32"), (1, 256, "bf16")):
+        for direction in ("fwd", "bwd"):
+            p = L.lrscan_plan(B, 1 << 18, D, dt, direction)
+            assert p["path"] == "stream" and p["lanes_per_cta"] == 64, p
+    # too short for 64 stream chunks per lane group: chunked
+    assert L.lrscan_plan(1, 8192, 64, "bf16", "fwd")["path"] == "chunk"
     # too short for 2,048 chunks of 512: the forward falls back to 256
     p = L.lrscan_plan(1, (1 << 19) + 1000, 64, "f32", "fwd")
     assert p["rows_per_window"] == 256 and p["name"].endswith("_grouped"), p
@@ -302,27 +313,33 @@ def test_complex_chunked_plans(lib):
 
 
 def test_stream_plans(lib):
-    """The persistent chunk-streaming path: 512-step chunks (eight 64-row
-    windows), at most the resident CTAs of the GPU, its publication workspace
-    (ticket, one flag per chunk, a map and a state per chunk and lane), and
-    refusals where it cannot run."""
+    """The persistent chunk-streaming path: eight window warps per chunk (256
+    steps of 32-row windows; 128 steps for 64-lane fp32 tiles), at most the
+    resident CTAs of the GPU and no more than keep the chunks in flight inside
+    L2, its publication workspace (ticket, one flag per chunk, a map and a
+    state per chunk and lane), and refusals where it cannot run."""
     pad = lambda x: (x + 255) // 256 * 256
-    for dt, names in (("f32", ("stream_f32_d32_s8", "stream_f32_d64_s8")),
-                      ("bf16", ("stream_bf16_d32_s8", "stream_bf16_d64_s8"))):
+    for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d64")),
+                      ("bf16", ("stream_bf16_d32", "stream_bf16_d64"))):
+        es = 4 if dt == "f32" else 2
         assert L.lrscan_num_variants("stream", dt) == 2
         for v, name in enumerate(names, 1):
             for direction in ("fwd", "bwd"):
                 B, T, D = 1, 1 << 22, 64
                 p = L.lrscan_plan(B, T, D, dt, direction, path="stream", tile_variant=v)
                 assert p["path"] == "stream" and p["name"] == name and p["exact"] == 0, p
-                assert p["rows_per_window"] == 64 and p["subchunks"] == 8 and p["kernels"] == 1
+                rows = 16 if name == "stream_f32_d64" else 32
+                assert p["rows_per_window"] == rows and p["subchunks"] == 8 and p["kernels"] == 1
+                assert p["threads_per_cta"] == 11 * 32 and p["stages"] == 16
                 dtl = p["lanes_per_cta"]
-                ng, nc = B * -(-D // dtl), -(-T // 512)
+                chunk = 8 * rows
+                ng, nc = B * -(-D // dtl), -(-T // chunk)
                 assert p["workspace_bytes"] == 256 + pad(ng * nc * 4) + pad(ng * nc * dtl * 8) + pad(ng * nc * dtl * 4)
-                assert 0 < p["ctas"] <= min(ng * nc, 2 * 152) and p["ctas"] % 152 == 0, p
-                assert p["threads_per_cta"] == 8 * 32 + 32
+                l2_ctas = max(152, (48 << 20) * 2 // (7 * chunk * dtl * es * 2))
+                resident = min(2 if name == "stream_bf16_d32" else 1, 233472 // (p["smem_bytes"] + 1024))
+                assert p["ctas"] == min(ng * nc, resident * 152, l2_ctas), p
     # a short sequence: no more CTAs than chunk tickets
-    assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 2
+    assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 4
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
     with pytest.raises(L.LrscanError):

@@ -40,8 +40,8 @@ def from_np(x, dtype):
     return torch.from_numpy(np.ascontiguousarray(x))
 
 
-SHAPES = [(1, 1, 32), (1, 511, 32), (1, 512, 64), (1, 513, 64), (3, 700, 32), (2, 3001, 96), (1, 5000, 64),
-          (2, 40000, 32)]
+SHAPES = [(1, 1, 32), (1, 255, 32), (1, 256, 64), (1, 257, 64), (3, 700, 32), (2, 3001, 96), (1, 5000, 64),
+          (2, 40000, 32), (1, 9, 8)]
 
 
 def check(B, T, D, dt, variant, seed, a_lo=0.6):
@@ -76,10 +76,11 @@ def test_stream_parity(dt, variant, shape_i):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_stream_many_chunks_per_cta(dt):
-    """1,024 chunk tickets (two 32-lane groups x 512 chunks): several per CTA."""
+    """2,048 chunk tickets (two 32-lane groups x 1,024 chunks): several per CTA."""
     B, T, D = 1, 1 << 18, 64
     plan = L.lrscan_plan(B, T, D, dt, "fwd", path="stream", tile_variant=1)
-    assert plan["ctas"] < 2 * ((T + plan["rows_per_window"] * 8 - 1) // (plan["rows_per_window"] * 8))
+    chunk = plan["rows_per_window"] * plan["subchunks"]
+    assert plan["ctas"] < 2 * (T // chunk)
     check(B, T, D, dt, 1, seed=950, a_lo=0.9)
 
 
@@ -88,3 +89,42 @@ def test_stream_refuses_state():
     h0 = torch.zeros(1, 32, device="cuda")
     with pytest.raises(RuntimeError):
         L.lrscan_fwd_state(a, a, h0=h0, path="stream")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_stream_in_cuda_graph(dt):
+    """Captured into a graph (the workspace's ticket and flags are cleared by a
+    captured memset each call), replayed twice with new inputs: each replay
+    against the oracle.  The captured backward reads its own static input
+    (filled with the oracle's forward output before each replay)."""
+    B, T, D = 1, 20000, 64
+    kw = dict(path="stream")
+    o = orc()
+    static = {k: v.cuda() for k, v in random_inputs(B, T, D, dt, seed=970, a_lo=0.8, a_hi=1.0).items()
+              if k in ("a", "b", "grad_out")}
+    static["out_in"] = torch.empty_like(static["a"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        L.lrscan_fwd(static["a"], static["b"], **kw)  # outside capture: sizes the workspace
+        L.lrscan_bwd(static["a"], static["out_in"], static["grad_out"], **kw)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        out, last = L.lrscan_fwd(static["a"], static["b"], **kw)
+        ga, gb = L.lrscan_bwd(static["a"], static["out_in"], static["grad_out"], **kw)
+    for seed in (971, 972):
+        fresh = random_inputs(B, T, D, dt, seed=seed, a_lo=0.8, a_hi=1.0)
+        a_np = to_np(fresh["a"])
+        ref_out, ref_last = o.fwd(a_np, to_np(fresh["b"]), dt)
+        ref_ga, ref_gb = o.bwd(a_np, ref_out, to_np(fresh["grad_out"]), dt)
+        for k in ("a", "b", "grad_out"):
+            static[k].copy_(fresh[k].cuda())
+        static["out_in"].copy_(from_np(ref_out, dt).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert L.lrscan_sync_check() == 0
+        assert_close(to_np(out), ref_out, dt, f"out replay {seed}", reassociated=True)
+        assert_last_close(last.cpu().numpy(), ref_last, f"last replay {seed}")
+        assert_close(to_np(gb), ref_gb, dt, f"grad_b replay {seed}", reassociated=True)
+        assert_close(to_np(ga), ref_ga, dt, f"grad_a replay {seed}", reassociated=True)
