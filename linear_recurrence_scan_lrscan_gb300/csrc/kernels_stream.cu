@@ -29,12 +29,12 @@ int launch_stream(const WinLaunch &L, const WinDirCfg &cfg) {
 
 // rows_per_window (w) = rows of one window warp, subchunks (s) = window warps
 // per chunk: a chunk is s * w steps.
-// nstage must be a multiple of NWC: window w then always lands in stages
-// w, w + NWC, ..., which its own warp alone waits on and releases, so each of
-// its parity waits is at most one phase ahead of the last one it saw complete.
+// nstage is 2 * NWC: window warp w owns stages w (summary tiles) and
+// NWC + w (replay tiles), issues their copies itself and alone waits on them,
+// so each of its parity waits is one phase past the last one it saw complete.
 template <class C, bool FWD>
 WinDirCfg sdir_cfg(int nstage) {
-    if (nstage <= 0 || nstage % C::NWC != 0) std::abort();  // table error
+    if (nstage != 2 * C::NWC) std::abort();  // table error
     const StreamGeom g = make_stream_geom<C, FWD ? 2 : 3>(nstage);
     WinDirCfg d{};
     d.dt = C::DT;

@@ -9,39 +9,40 @@
 // ticket counter, chunk-major over the groups (forward: earliest chunk first;
 // backward: latest first).  A CTA has NWC window warps (warp w owns window w
 // of every chunk, all DT lanes, V lanes per thread), two scan warps (chunks
-// alternate between them) and a producer warp, and passes over each chunk
+// alternate between them) and a ticket warp, and passes over each chunk
 // twice:
-//   summary  the producer streams the chunk's window tiles in (bulk tensor
-//            copies, from HBM); each window warp reduces its window to the
-//            affine map h -> P h + Q of its rows, one lane per thread;
+//   summary  each window warp copies its window's tiles in (bulk tensor
+//            copies, from HBM) and reduces them to the affine map
+//            h -> P h + Q of its rows, one lane per thread;
 //   prefix   the last window warp to finish composes the window maps into
 //            the chunk's map and publishes it; a scan warp looks back over
-//            the chunks before it (the nearest
-//            one whose leaving state is published, composed with the maps of
-//            the chunks in between, gives the entering state), publishes the
-//            chunk's leaving state, and hands every window warp the state
-//            entering its window;
-//   replay   the producer streams the same tiles in again, now from L2, and
-//            each window warp runs its rows with the sequential step from its
-//            entering state, storing every output row straight to global
-//            memory (a warp writes whole rows of its DT lanes).
+//            the chunks before it (the nearest one whose leaving state is
+//            published, composed with the maps of the chunks in between,
+//            gives the entering state), publishes the chunk's leaving state,
+//            and hands every window warp the state entering its window;
+//   replay   each window warp copies the same tiles in again, now from L2,
+//            runs its rows with the sequential step from its entering state
+//            and stores every output row straight to global memory (a warp
+//            writes whole rows of its DT lanes).
 // The replay of chunk k follows the summaries of chunks k+1 and k+2, and two
-// scan warps publish and look back for consecutive chunks at once, so the
-// look-back's latency (a few L2 round trips) hides behind two chunks of work;
-// the three chunks between a summary and its replay are what L2 holds.  Each
-// window warp owns two ring stages, so one tile loads while it works on the
-// other.
+// scan warps look back for consecutive chunks at once, so the look-back's
+// latency (a few L2 round trips) hides behind two chunks of work; the three
+// chunks between a summary and its replay are what L2 holds.  Each window
+// warp owns two ring stages (summary and replay tiles), so one tile loads
+// while it works on the other.
 // HBM carries the scan's own traffic: forward a, b in, out out; backward a,
-// out, grad_out in, grad_a, grad_b out.
+// out, grad_out in, grad_a, grad_b out.  Results agree with the sequential
+// definition to rounding; which published states a look-back composes depends
+// on timing, so two calls can differ in the last bits.
 //
 // Publication: one flag word per chunk (0 before the call, kChunkAgg once the
 // map is out, kChunkIncl once the leaving state is out): the warp's lanes
 // write their lanes' values, a warp barrier, then lane 0 stores the flag with
 // release semantics; readers acquire the flags, pass a warp barrier, and read
-// the values past L1.  The
-// look-back waits only on chunks with earlier tickets, which running CTAs
-// hold, so it always ends; still every wait is bounded (timeout:
-// LRSCAN_ETIMEOUT in the status word, and the kernel returns).
+// the values past L1.  The look-back waits only on chunks with earlier
+// tickets, which running CTAs hold, so it always ends; still every wait is
+// bounded (timeout: LRSCAN_ETIMEOUT in the status word, and the kernel
+// returns).
 #pragma once
 
 #include "scan_common.cuh"
@@ -53,13 +54,13 @@ constexpr uint32_t kChunkAgg = 1, kChunkIncl = 2;
 
 enum StreamSite : int { kSiteLookback = 8, kSiteStreamStep = 9 };
 
-// Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
-// window (per window warp), windows per chunk, CTAs per SM the registers must
-// allow.  One warp spans the DT lanes of a window row.
 // Chunks a replay trails its summary by, scan warps, and map / entering-state
 // buffers (one per chunk between a summary and its replay, plus one).
 constexpr int kStreamLag = 2, kStreamScanWarps = 2, kStreamBufs = kStreamLag + 1;
 
+// Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
+// window (per window warp), windows per chunk, CTAs per SM the registers must
+// allow.  One warp spans the DT lanes of a window row.
 template <class St_, int DT_, int V_, int W_, int NWC_, int MINB_>
 struct StreamShape {
     using St = St_;
@@ -74,10 +75,10 @@ constexpr int kStreamStepSlots = 8;
 
 // Shared-memory layout (bytes from the 1024-aligned base), host and device.
 struct StreamGeom {
-    int nstage;      // ring depth (window tiles), a multiple of NWC
+    int nstage;      // ring stages (window tiles): 2 * NWC, two per window warp
     int tile_bytes;  // one plane of one window: W * DT * elem
     int stage_bytes; // NIN planes
-    int bar_off;     // full[nstage], empty[nstage], step_full[slots], maps_ready[bufs], entries_ready[bufs]
+    int bar_off;     // full[nstage], step_free[nstage], step_full[slots], maps_ready[bufs], entries_ready[bufs]
     int ticket_off;  // step tickets [slots]
     int map_off;     // window maps [bufs][NWC][DT] float2
     int entry_off;   // window entering states [bufs][NWC][DT] float
