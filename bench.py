@@ -297,17 +297,20 @@ def kernel_timing(w, sets, opts, iters: int, stream, peak: float) -> dict:
     mean device time per launch, algorithmic GB/s and its fraction of the
     measured copy peak, with the kernel the dispatcher ran."""
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
-    fms = time_launches(fwd_call(sets, opts), iters, stream)
-    bms = time_launches(bwd_call(sets, opts), iters, stream)
+    fs = time_launch_samples(fwd_call(sets, opts), iters, stream)
+    bs = time_launch_samples(bwd_call(sets, opts), iters, stream)
+    fms, bms = sorted(fs)[1], sorted(bs)[1]  # medians of three samples
     if L.lrscan_sync_check() != 0:
         raise RuntimeError(f"device error while timing {w.describe()}")
     pf = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "fwd", **opts)
     pb = L.lrscan_plan(w.B, w.T, w.D, w.dtype, "bwd", **opts)
     bf, bb = algorithmic_bytes(w)
-    res = {"workload": w.describe(), "launches_per_direction": iters, "buffer_sets": len(sets)}
-    for key, ms, by, p in (("fwd", fms, bf, pf), ("bwd", bms, bb, pb)):
+    res = {"workload": w.describe(), "launches_per_direction": 3 * iters, "buffer_sets": len(sets),
+           "timing": f"median of 3 samples of {iters} back-to-back launches"}
+    for key, ms, smp, by, p in (("fwd", fms, fs, bf, pf), ("bwd", bms, bs, bb, pb)):
         gbs = by / (ms * 1e-3) / 1e9
-        res[key] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak, "algorithmic_bytes": by,
+        res[key] = {"us": ms * 1e3, "samples_us": [round(x * 1e3, 2) for x in smp], "GB/s": gbs,
+                    "frac": gbs / peak, "algorithmic_bytes": by,
                     "elements/s": w.elements / (ms * 1e-3), "kernel": p["name"], "path": p["path"],
                     "kernels": p["kernels"], "traffic": load_traffic(w, key, p["name"])}
     res["elements/s"] = 2 * w.elements / ((fms + bms) * 1e-3)
@@ -486,7 +489,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
                      "achieved": dominant[3], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dominant[3] / peaks["hbm_gbs"], "peak_source": peaks["source"],
                      "algorithmic_bytes_per_launch": dominant[1], "launch_us": dominant[2] * 1e3,
-                     "launches_timed": iters, "traffic": kt[dominant[0]]["traffic"]},
+                     "launches_timed": 3 * iters, "timing": kt["timing"],
+                     "traffic": kt[dominant[0]]["traffic"]},
         "fwd": kt["fwd"],
         "bwd": kt["bwd"],
         "step_GB/s": (bf + bb) / (ms_per_step * 1e-3) / 1e9,
@@ -510,21 +514,32 @@ def run_ours(args, w, rank: int, world: int, dist) -> dict | None:
 
 
 # ------------------------------------------------------------ extensions ----
-def time_launches(fn, iters: int, stream) -> float:
-    """Mean device time of one call of fn(i) over `iters` back-to-back calls
-    (after 3 untimed ones), CUDA events on the launching stream."""
+def time_launch_samples(fn, iters: int, stream, samples: int = 3) -> list[float]:
+    """Mean device time (ms) of one call of fn(i) over `iters` back-to-back
+    calls, `samples` times (after 3 untimed calls); CUDA events on the
+    launching stream around each sample."""
     import torch
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(iters):
-        fn(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / iters
+    out = []
+    for _ in range(samples):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(iters):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / iters)
+    return out
+
+
+def time_launches(fn, iters: int, stream) -> float:
+    """Median over three samples of the mean device time of one call of fn(i)
+    over `iters` back-to-back calls (a host stall that starves the device in
+    one sample does not set the figure)."""
+    return float(sorted(time_launch_samples(fn, iters, stream))[1])
 
 
 def run_extensions(args, dev, peak) -> dict:
@@ -577,7 +592,7 @@ def run_extensions(args, dev, peak) -> dict:
         "workload": w.describe(),
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
                 "grad_last in, grad_h0 out",
-        "launches_per_direction": iters,
+        "launches_per_direction": 3 * iters, "timing": "median of 3 samples",
         "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
                 "algorithmic_bytes": fb},
         "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
@@ -624,7 +639,7 @@ def run_complex(iters: int, dev, peak) -> dict:
     fb, bb = 6 * E * s + 8 * B * D, 10 * E * s
     pf = L.lrscan_plan_complex(B, T, D, cw.dtype, "fwd")
     pb = L.lrscan_plan_complex(B, T, D, cw.dtype, "bwd")
-    res = {"workload": cw.describe() + " complex (re/im planes)", "launches_per_direction": iters,
+    res = {"workload": cw.describe() + " complex (re/im planes)", "launches_per_direction": 3 * iters, "timing": "median of 3 samples",
            "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
                    "algorithmic_bytes": fb, "kernel": pf["name"]},
            "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,
@@ -753,7 +768,7 @@ def run_gated(iters: int, dev, peak) -> dict:
     del sets
     torch.cuda.empty_cache()
     return {"workload": gw.describe() + " with decays generated from eta [B,T] and nu_log [D]",
-            "launches_per_direction": iters,
+            "launches_per_direction": 3 * iters, "timing": "median of 3 samples",
             "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
                     "algorithmic_bytes": fb, "kernel": pf["name"]},
             "bwd": {"ms": bms, "GB/s": bb / (bms * 1e-3) / 1e9, "frac": bb / (bms * 1e-3) / 1e9 / peak,

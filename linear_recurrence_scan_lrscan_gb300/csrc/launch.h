@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "state_args.h"
+#include "stream_args.h"
 
 namespace lrscan {
 

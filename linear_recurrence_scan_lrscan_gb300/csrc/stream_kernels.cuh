@@ -46,7 +46,7 @@
 #pragma once
 
 #include "scan_common.cuh"
-#include "state_args.h"
+#include "stream_args.h"
 
 namespace lrscan {
 
