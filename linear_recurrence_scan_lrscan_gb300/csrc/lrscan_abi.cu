@@ -670,9 +670,12 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
     void *ws = nullptr;
     int rc = workspace_for(ctx, st, ch.workspace, opts, &ws);
     if (rc) return rc;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];  // inputs in kernel order, then the outputs at 3 and 4
     int k = 0;
     for (const void *p : ins)
+        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+    k = 3;
+    for (void *p : outs)
         if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
     WinLaunch L{};
     for (int i = 0; i < k; ++i) L.maps[i] = &maps[i];

@@ -1,0 +1,583 @@
+// Chunk streaming with summary and replay in separate warps.
+//
+// The same single pass as stream_kernel (chunk maps published, entering
+// states by look-back, the replay re-reading its tiles from L2), with the
+// roles of a window warp split: NW summary warps, NW replay warps, NSCAN scan
+// warps (chunk k goes to scan warp k mod NSCAN) and a ticket warp.  A chunk is
+// NWIN = NW * R windows of W rows; summary warp w reduces windows w, w + NW,
+// ... of every chunk to their maps and replay warp w replays the same
+// windows.  A summary never waits behind a replay: the summary warps run
+// ahead of the replay warps by up to NB - 1 chunks (the map / entering-state
+// buffers are the only link), so every chunk's map is published as soon as
+// its tiles have landed.  Each summary warp streams its tiles through S
+// stages of its own (S - 1 tiles in flight ahead of the one it reduces), each
+// replay warp through two.
+//
+// Per chunk k (buffer b = k mod NB):
+//   summary warps   reduce their windows, wait until the replay warps have
+//                   finished chunk k - NB (buffer free), write their window
+//                   maps; the last one to finish composes the chunk's map,
+//                   publishes it (flag kChunkAgg) and signals maps_ready[b];
+//   scan warp       looks back for the entering state, publishes the leaving
+//                   state (kChunkIncl), writes each window's entering state and
+//                   signals entries_ready[b];
+//   replay warps    replay their windows, store the outputs and signal
+//                   buf_free[b].
+// The first invalid ticket ends the sequence: summary warp 0 writes an end
+// mark into the next NSCAN buffers, one for each scan warp.
+#pragma once
+
+#include "stream_kernels.cuh"
+
+namespace lrscan {
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// L2 eviction priorities: a summary's tiles are read again by the replay
+// (evict last), a replay's tiles and the outputs are not (evict first).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *m, int x, int y, int z, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// tma_store_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *m, uint32_t src, int x, int y, int z,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::
+                     "l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+                 : "memory");
+}
+
+// Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
+// window, summary (= replay) warps, windows per warp and chunk, summary and
+// replay stages per warp, scan warps, chunk buffers.
+template <class St_, int DT_, int V_, int W_, int NW_, int R_, int S_, int SR_, int NSCAN_, int NB_>
+struct SplitShape {
+    using St = St_;
+    static constexpr int DT = DT_, V = V_, W = W_, NW = NW_, R = R_, S = S_, SR = SR_, NSCAN = NSCAN_, NB = NB_;
+    static constexpr int NWIN = NW * R;  // windows per chunk
+    static constexpr int THREADS = (2 * NW + NSCAN + 1) * 32;
+    static constexpr int MINB = 1;
+    static_assert(DT == 32 * V, "one warp spans a tile row");
+    static_assert(W % 8 == 0, "rows are taken eight at a time");
+    static_assert(NB % NSCAN == 0, "a scan warp sees every use of its buffers");
+    static_assert(S >= 2 && S - 1 <= R, "tiles in flight stay within the next chunk");
+    static_assert(SR == 2 || SR == 3, "a replay tile is prefetched one window ahead");
+};
+
+constexpr int kSplitSlots = 8;  // step ring of the ticket warp
+constexpr int kSplitAhead = 2;  // ticket k is fetched once the summaries of chunk k - 2 have started
+
+// Shared-memory layout, host and device.  Summary warp w owns stages
+// w*S .. w*S+S-1 of the summary ring (two planes each), replay warp w owns
+// stages w*SR .. w*SR+SR-1 of the replay ring (NIN planes each; the outputs
+// overwrite their inputs there and leave by bulk tensor stores).
+struct SplitGeom {
+    int tile_bytes;    // one plane of one window: W * DT * elem
+    int sstage_bytes;  // summary stage: forward a, b; backward a, grad_out
+    int rstage_bytes;  // replay stage: forward a, b; backward a, out, grad_out
+    int rring_off;     // replay ring after the summary ring
+    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_free[slots], maps[NB], entries[NB], buf_free[NB]
+    int ticket_off;    // step tickets [slots]
+    int tick_off;      // chunk tickets per buffer [NB] (-1: end mark)
+    int map_off;       // window maps [NB][NWIN][DT] float2
+    int cmap_off;      // chunk maps [NB][DT] float2
+    int entry_off;     // window entering states [NB][NWIN][DT] float
+    int count_off;     // summary warps done per buffer [NB]
+    int flag_off;      // abort flag
+    int smem_bytes;
+};
+
+template <class C, bool BWD>
+__host__ __device__ inline SplitGeom make_split_geom() {
+    SplitGeom g{};
+    g.tile_bytes = C::W * C::DT * static_cast<int>(sizeof(typename C::St));
+    g.sstage_bytes = 2 * g.tile_bytes;
+    g.rstage_bytes = (BWD ? 3 : 2) * g.tile_bytes;
+    g.rring_off = C::NW * C::S * g.sstage_bytes;
+    g.bar_off = g.rring_off + C::NW * C::SR * g.rstage_bytes;
+    const int nbar = C::NW * C::S + C::NW * C::SR + 2 * kSplitSlots + 3 * C::NB;
+    g.ticket_off = g.bar_off + nbar * 8;
+    g.tick_off = g.ticket_off + kSplitSlots * 4;
+    g.map_off = (g.tick_off + C::NB * 4 + 15) / 16 * 16;
+    g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8;
+    g.entry_off = g.cmap_off + C::NB * C::DT * 8;
+    g.count_off = g.entry_off + C::NB * C::NWIN * C::DT * 4;
+    g.flag_off = g.count_off + C::NB * 4;
+    g.smem_bytes = g.flag_off + 16;
+    return g;
+}
+
+// Forward tiles: a, b (row t); output out (tm_o0), staged over b.  Backward
+// tiles: a one row late (a_{t+1}), out one row early (h_{t-1}), grad_out;
+// outputs grad_a (tm_o0, staged over h_{t-1}) and grad_b (tm_o1, staged over
+// grad_out).
+template <class C, bool BWD>
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+stream_split_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUtensorMap tm_1,
+                    const __grid_constant__ CUtensorMap tm_2, const __grid_constant__ CUtensorMap tm_o0,
+                    const __grid_constant__ CUtensorMap tm_o1, float *__restrict__ last, int T, int D,
+                    DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
+    using St = typename C::St;
+    constexpr int DT = C::DT, V = C::V, W = C::W, NW = C::NW, R = C::R, S = C::S, SR = C::SR, NSCAN = C::NSCAN;
+    constexpr int NB = C::NB;
+    constexpr int NWIN = C::NWIN;
+    constexpr int NIN = BWD ? 3 : 2;
+    constexpr int SLOTS = kSplitSlots;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const SplitGeom geo = make_split_geom<C, BWD>();
+    auto stile = [&](int st, int plane) {  // summary ring: plane 0 = a, 1 = b / grad_out
+        return reinterpret_cast<St *>(smem_raw + st * geo.sstage_bytes + plane * geo.tile_bytes);
+    };
+    auto rtile = [&](int st, int plane) {  // replay ring: planes in tensor-map order
+        return reinterpret_cast<St *>(smem_raw + geo.rring_off + st * geo.rstage_bytes + plane * geo.tile_bytes);
+    };
+    auto bar = [&](int i) { return smem_addr(smem_raw + geo.bar_off + 8 * i); };
+    constexpr int BS = NW * S;  // summary-ring barriers first
+    auto sfull = [&](int st) { return bar(st); };
+    auto rfull = [&](int st) { return bar(BS + st); };
+    constexpr int BR = BS + NW * SR;  // then the replay ring's
+    auto step_full = [&](int q) { return bar(BR + q); };
+    auto step_free = [&](int q) { return bar(BR + SLOTS + q); };
+    auto maps_bar = [&](int b) { return bar(BR + 2 * SLOTS + b); };
+    auto entries_bar = [&](int b) { return bar(BR + 2 * SLOTS + NB + b); };
+    auto buf_free = [&](int b) { return bar(BR + 2 * SLOTS + 2 * NB + b); };
+    int *step_ticket = reinterpret_cast<int *>(smem_raw + geo.ticket_off);
+    volatile int *tick_of = reinterpret_cast<volatile int *>(smem_raw + geo.tick_off);
+    float2 *wmap = reinterpret_cast<float2 *>(smem_raw + geo.map_off);
+    float2 *cmap = reinterpret_cast<float2 *>(smem_raw + geo.cmap_off);
+    float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off);
+    unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < BS; ++st) mbar_init(sfull(st), 1);
+        for (int st = 0; st < NW * SR; ++st) mbar_init(rfull(st), 1);
+        for (int q = 0; q < SLOTS; ++q) {
+            mbar_init(step_full(q), 1);
+            mbar_init(step_free(q), NW);
+        }
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(maps_bar(b), 1);  // the last summary warp (or the end mark)
+            mbar_init(entries_bar(b), 1);
+            mbar_init(buf_free(b), NW);
+            wcount[b] = 0;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx wc{status, abort_flag, timeout_ns};
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int CH = NWIN * W;
+    const long long total = static_cast<long long>(sa.ng) * sa.nc;
+    const CUtensorMap *const maps[3] = {&tm_0, &tm_1, &tm_2};
+    // chunk coordinates of ticket t
+    struct Chunk {
+        int cc, gi, c, brow, x0;
+    };
+    auto decode = [&](int t) {
+        Chunk ch;
+        ch.cc = t / sa.ng;
+        ch.gi = t - ch.cc * sa.ng;
+        ch.c = BWD ? sa.nc - 1 - ch.cc : ch.cc;
+        ch.brow = ch.gi / sa.ndt;
+        ch.x0 = (ch.gi - ch.brow * sa.ndt) * DT;
+        return ch;
+    };
+    // bounded wait, blind to the abort flag, for a copy this warp issued
+    auto drain_one = [&](uint32_t fb, uint32_t par) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(fb, par)) {
+            if (global_timer_ns() - t0 > wc.timeout_ns) {
+                record_error(wc, kErrTimeout, kSiteDrain);
+                break;
+            }
+        }
+    };
+
+    if (warp == 2 * NW + NSCAN) {
+        // ------------------------------------------------------------ tickets
+        if (lane == 0) {
+            for (int j = 0;; ++j) {
+                if (j >= kSplitAhead) {
+                    const int jf = j - kSplitAhead;
+                    if (!mbar_wait(step_free(jf % SLOTS), static_cast<uint32_t>((jf / SLOTS) & 1), wc,
+                                   kSiteProducerEmpty))
+                        return;
+                }
+                const long long tj = static_cast<long long>(atomicAdd(sa.ticket, 1u));
+                const int tk = tj < total ? static_cast<int>(tj) : -1;
+                step_ticket[j % SLOTS] = tk;
+                mbar_arrive(step_full(j % SLOTS));
+                if (tk < 0) return;
+            }
+        }
+        return;
+    }
+
+    if (warp < NW) {
+        // ------------------------------------------------------ summary warps
+        const int w = warp;
+        int u_iss = 0, u_done = 0;  // tiles issued / reduced, counted over this warp's chunks (R per chunk)
+        auto sissue = [&](int u, int t) {  // lane 0: tile u (window (u % R) * NW + w of ticket t)
+            const Chunk ch = decode(t);
+            const int st = w * S + u % S;
+            const uint32_t fb = sfull(st);
+            mbar_arrive_expect_tx(fb, 2 * geo.tile_bytes);
+            const int y = ch.c * CH + ((u % R) * NW + w) * W;
+            const uint64_t keep = l2_evict_last_policy();
+            tma_load_3d_hint(smem_addr(stile(st, 0)), maps[0], ch.x0, y + (BWD ? 1 : 0), ch.brow, fb, keep);
+            tma_load_3d_hint(smem_addr(stile(st, 1)), maps[BWD ? 2 : 1], ch.x0, y, ch.brow, fb, keep);
+        };
+        auto drain = [&]() {
+            if (lane != 0) return;
+            for (int u = u_done; u < u_iss; ++u) drain_one(sfull(w * S + u % S), static_cast<uint32_t>((u / S) & 1));
+        };
+        if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
+        int tk = step_ticket[0];
+        for (int k = 0;; ++k) {
+            const int b = k % NB;
+            if (tk < 0) {
+                // no more chunks: summary warp 0 marks the end in the next NSCAN
+                // buffers (each once the replays of its previous chunk are done),
+                // so that every scan warp and the replay warps see it
+                if (w == 0) {
+                    for (int i = 0; i < NSCAN; ++i) {
+                        const int ke = k + i, be = ke % NB;
+                        if (ke >= NB && !warp_wait(buf_free(be), static_cast<uint32_t>(((ke / NB) - 1) & 1), wc,
+                                                   kSiteStreamStep)) {
+                            drain();
+                            return;
+                        }
+                        if (lane == 0) {
+                            tick_of[be] = -1;
+                            mbar_arrive(maps_bar(be));
+                        }
+                        __syncwarp();
+                    }
+                }
+                drain();
+                return;
+            }
+            // the next ticket (its first tiles go out while this chunk is reduced)
+            const int q1 = (k + 1) % SLOTS;
+            if (!warp_wait(step_full(q1), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc, kSiteStreamStep)) {
+                drain();
+                return;
+            }
+            const int tn = step_ticket[q1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(step_free(k % SLOTS));
+            const Chunk ch = decode(tk);
+            float P[R][V], Q[R][V];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int u = k * R + r;
+                // keep S - 1 tiles in flight ahead of this one (chunks k and k + 1)
+                while (u_iss <= u + S - 1) {
+                    const int t = u_iss / R == k ? tk : tn;
+                    if (t < 0) break;
+                    if (lane == 0) sissue(u_iss, t);
+                    ++u_iss;
+                }
+                const int wbase = ch.c * CH + (r * NW + w) * W;
+                const int nrows = min(max(T - wbase, 0), W);
+                const int st = w * S + u % S;
+                if (!warp_wait(sfull(st), static_cast<uint32_t>((u / S) & 1), wc, kSiteConsumerFull)) {
+                    drain();
+                    return;
+                }
+                const St *ta = stile(st, 0);
+                const St *tb = stile(st, 1);
+                // the window's map (rows past T are identity steps)
+#pragma unroll
+                for (int v = 0; v < V; ++v) { P[r][v] = 1.0f; Q[r][v] = 0.0f; }
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
+                    float xa[8][V], xb[8][V];
+                    load8<St, V, DT>(ta, r0, lane, xa);
+                    load8<St, V, DT>(tb, r0, lane, xb);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int row = BWD ? 7 - rr : rr;
+                        if (r0 + row < nrows) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                P[r][v] = __fmul_rn(xa[row][v], P[r][v]);
+                                Q[r][v] = __fmaf_rn(xa[row][v], Q[r][v], xb[row][v]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();  // every lane done with the stage before it is refilled
+                ++u_done;
+            }
+            // buffer b is free once the replays of chunk k - NB are done
+            if (k >= NB && !warp_wait(buf_free(b), static_cast<uint32_t>(((k / NB) - 1) & 1), wc, kSiteStreamStep)) {
+                drain();
+                return;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 *mp = wmap + (b * NWIN + r * NW + w) * DT + lane * V;
+#pragma unroll
+                for (int v = 0; v < V; ++v) mp[v] = make_float2(P[r][v], Q[r][v]);
+            }
+            __syncwarp();
+            unsigned int before = 0;
+            if (lane == 0) before = atom_add_acq_rel_cta(wcount + b, 1u);
+            before = __shfl_sync(0xffffffffu, before, 0);
+            if (before == NW - 1) {
+                // the last summary warp of this chunk: compose the window maps in
+                // chain order and publish the chunk's map at once
+                __syncwarp();
+                const float2 *cm = wmap + b * NWIN * DT;
+                float Pc[V], Qc[V];
+#pragma unroll
+                for (int v = 0; v < V; ++v) { Pc[v] = 1.0f; Qc[v] = 0.0f; }
+                for (int jw = 0; jw < NWIN; ++jw) {
+                    const int ww = BWD ? NWIN - 1 - jw : jw;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const float2 m = cm[ww * DT + lane * V + v];
+                        Qc[v] = __fmaf_rn(m.x, Qc[v], m.y);
+                        Pc[v] = __fmul_rn(m.x, Pc[v]);
+                    }
+                }
+                const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    cmap[b * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
+                    sa.agg[slot_g * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
+                }
+                __syncwarp();  // every lane's map written before lane 0's release
+                if (lane == 0) {
+                    st_release_gpu(sa.flag + slot_g, kChunkAgg);
+                    tick_of[b] = tk;
+                    wcount[b] = 0;  // next used NB chunks on, after this buffer's replays
+                    mbar_arrive(maps_bar(b));
+                }
+            }
+            tk = tn;
+        }
+    }
+
+    if (warp >= 2 * NW) {
+        // --------------------------------------------------------- scan warps
+        // scan warp j takes chunks j, j + NSCAN, ... until an end mark
+        const int i0 = lane * V;
+        for (int k = warp - 2 * NW;; k += NSCAN) {
+            const int b = k % NB;
+            if (!warp_wait(maps_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) return;
+            const int t = tick_of[b];
+            if (t < 0) return;
+            const Chunk ch = decode(t);
+            float Pc[V], Qc[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float2 m = cmap[b * DT + i0 + v];
+                Pc[v] = m.x;
+                Qc[v] = m.y;
+            }
+            float h[V];
+            if (!stream_lookback<DT, V, 32 / V>(sa, ch.gi, ch.cc, i0, h, wc)) return;
+            const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
+#pragma unroll
+            for (int v = 0; v < V; ++v) sa.incl[slot_g * DT + i0 + v] = __fmaf_rn(Pc[v], h[v], Qc[v]);
+            __syncwarp();  // every lane's state written before lane 0's release
+            if (lane == 0) st_release_gpu(sa.flag + slot_g, kChunkIncl);
+            // the state entering every window, in chain order
+            const float2 *mp = wmap + b * NWIN * DT;
+            float *ep = wentry + b * NWIN * DT;
+            for (int jw = 0; jw < NWIN; ++jw) {
+                const int ww = BWD ? NWIN - 1 - jw : jw;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    ep[ww * DT + i0 + v] = h[v];
+                    const float2 m = mp[ww * DT + i0 + v];
+                    h[v] = __fmaf_rn(m.x, h[v], m.y);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(entries_bar(b));
+        }
+    }
+
+    // ------------------------------------------------------------ replay warps
+    const int w = warp - NW;
+    const uint64_t drop = l2_evict_first_policy();  // replay tiles and outputs: not read again here
+    int u_iss = 0, u_done = 0;  // tiles issued / replayed, counted over this warp's chunks (R per chunk)
+    auto rissue = [&](int u, int t) {  // lane 0: tile u (window (u % R) * NW + w of ticket t)
+        // the stage last held tile u - SR, whose outputs were committed SR - 2
+        // bulk groups before the newest: wait until they have left it
+        bulk_wait_read<SR - 2>();
+        const Chunk ch = decode(t);
+        const int st = w * SR + u % SR;
+        const uint32_t fb = rfull(st);
+        mbar_arrive_expect_tx(fb, NIN * geo.tile_bytes);
+        const int y = ch.c * CH + ((u % R) * NW + w) * W;
+#pragma unroll
+        for (int i = 0; i < NIN; ++i) {
+            const int dy = BWD ? (i == 0 ? 1 : (i == 1 ? -1 : 0)) : 0;
+            tma_load_3d_hint(smem_addr(rtile(st, i)), maps[i], ch.x0, y + dy, ch.brow, fb, drop);
+        }
+    };
+    auto drain = [&]() {
+        if (lane != 0) return;
+        for (int u = u_done; u < u_iss; ++u) drain_one(rfull(w * SR + u % SR), static_cast<uint32_t>((u / SR) & 1));
+        bulk_wait<0>();  // the outputs in flight have left shared memory and landed
+    };
+    for (int k = 0;; ++k) {
+        const int b = k % NB;
+        if (!warp_wait(maps_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) {
+            drain();
+            return;
+        }
+        const int t = tick_of[b];
+        if (t < 0) {
+            drain();
+            return;
+        }
+        const Chunk ch = decode(t);
+        const int d = ch.x0 + lane * V;
+        for (int r = 0; r < R; ++r) {
+            const int u = k * R + r;
+            if (u_iss == u) {  // not prefetched
+                if (lane == 0) rissue(u, t);
+                ++u_iss;
+            }
+            // the next tile into the next stage; past this chunk only if the
+            // next chunk's map is already out
+            if (u_iss == u + 1) {
+                if (r + 1 < R) {
+                    if (lane == 0) rissue(u + 1, t);
+                    ++u_iss;
+                } else {
+                    int did = 0;
+                    if (lane == 0) {
+                        const int b1 = (k + 1) % NB;
+                        if (mbar_test_wait(maps_bar(b1), static_cast<uint32_t>(((k + 1) / NB) & 1))) {
+                            const int t1 = tick_of[b1];
+                            if (t1 >= 0) {
+                                rissue(u + 1, t1);
+                                did = 1;
+                            }
+                        }
+                    }
+                    u_iss += __shfl_sync(0xffffffffu, did, 0);
+                }
+            }
+            if (r == 0 && !warp_wait(entries_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) {
+                drain();
+                return;
+            }
+            const int st = w * SR + u % SR;
+            if (!warp_wait(rfull(st), static_cast<uint32_t>((u / SR) & 1), wc, kSiteConsumerFull)) {
+                drain();
+                return;
+            }
+            const int wi = r * NW + w;
+            const int wbase = ch.c * CH + wi * W;
+            const int nrows = min(max(T - wbase, 0), W);
+            St *ta = rtile(st, 0);
+            St *tb = rtile(st, NIN - 1);
+            float h[V];
+            const float *ep = wentry + (b * NWIN + wi) * DT + lane * V;
+#pragma unroll
+            for (int v = 0; v < V; ++v) h[v] = ep[v];
+            if constexpr (!BWD) {
+                // out_t over b_t in the tile (each lane rewrites what it read)
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    float xa[8][V], xb[8][V];
+                    load8<St, V, DT>(ta, g8, lane, xa);
+                    load8<St, V, DT>(tb, g8, lane, xb);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        if (g8 + rr < nrows) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[rr][v], h[v], xb[rr][v]);
+                            store_lanes<St, V>(tb + (g8 + rr) * DT + lane * V, h);
+                        }
+                    }
+                }
+                if (last != nullptr && d < D && nrows > 0 && wbase + nrows == T) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(ch.brow) * D + d + v] = h[v];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d_hint(&tm_o0, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
+                    bulk_commit();
+                }
+            } else {
+                // grad_b_t over grad_out_t, grad_a_t over h_{t-1}
+                St *th = rtile(st, 1);
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    const int r0 = (nrows - 1 - g8) & ~7;
+                    float xa[8][V], xh[8][V], xg[8][V];
+                    load8<St, V, DT>(ta, r0, lane, xa);
+                    load8<St, V, DT>(th, r0, lane, xh);
+                    load8<St, V, DT>(tb, r0, lane, xg);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int row = 7 - rr;
+                        if (r0 + row < nrows) {
+                            float gav[V];
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                h[v] = __fmaf_rn(xa[row][v], h[v], xg[row][v]);
+                                gav[v] = __fmul_rn(h[v], xh[row][v]);
+                            }
+                            store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, h);
+                            store_lanes<St, V>(th + (r0 + row) * DT + lane * V, gav);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d_hint(&tm_o0, smem_addr(th), ch.x0, wbase, ch.brow, drop);
+                    tma_store_3d_hint(&tm_o1, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
+                    bulk_commit();
+                }
+            }
+            __syncwarp();  // every lane done with the stage before it is refilled
+            ++u_done;
+        }
+        if (lane == 0) mbar_arrive(buf_free(b));  // the buffer's entering states are read
+    }
+}
+
+}  // namespace lrscan

@@ -314,29 +314,38 @@ def test_complex_chunked_plans(lib):
 
 def test_stream_plans(lib):
     """The persistent chunk-streaming path: eight window warps per chunk (256
-    steps of 32-row windows; 128 steps for 64-lane fp32 tiles), at most the
-    resident CTAs of the GPU and no more than keep the chunks in flight inside
-    L2, its publication workspace (ticket, one flag per chunk, a map and a
-    state per chunk and lane), and refusals where it cannot run."""
+    steps of 32-row windows; 128 steps for 64-lane fp32 tiles), or, split
+    into summary and replay warps, 128-step chunks; at most the resident CTAs
+    of the GPU and no more than keep the chunks in flight inside L2, its
+    publication workspace (ticket, one flag per chunk, a map and a state per
+    chunk and lane), and refusals where it cannot run."""
     pad = lambda x: (x + 255) // 256 * 256
-    for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d64")),
-                      ("bf16", ("stream_bf16_d32", "stream_bf16_d64"))):
+    # name: (rows per window, windows per chunk, threads, stages, CTAs per SM)
+    shapes = {"stream_f32_d32": (32, 8, 11 * 32, 16, 1), "stream_f32_d64": (16, 8, 11 * 32, 16, 1),
+              "stream_bf16_d32": (32, 8, 11 * 32, 16, 2), "stream_bf16_d64": (32, 8, 11 * 32, 16, 1),
+              "stream_split_f32_d32": (32, 16, 11 * 32, (24, 20), 1),
+              "stream_split_f32_d32_b": (32, 16, 11 * 32, (20, 20), 1),
+              "stream_split_bf16_d64": (32, 16, 11 * 32, (24, 20), 1)}
+    for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d64", "stream_split_f32_d32",
+                               "stream_split_f32_d32_b")),
+                      ("bf16", ("stream_bf16_d32", "stream_bf16_d64", "stream_split_bf16_d64"))):
         es = 4 if dt == "f32" else 2
-        assert L.lrscan_num_variants("stream", dt) == 2
+        assert L.lrscan_num_variants("stream", dt) == len(names)
         for v, name in enumerate(names, 1):
+            rows, nwin, threads, stages, per_sm = shapes[name]
             for direction in ("fwd", "bwd"):
                 B, T, D = 1, 1 << 22, 64
                 p = L.lrscan_plan(B, T, D, dt, direction, path="stream", tile_variant=v)
                 assert p["path"] == "stream" and p["name"] == name and p["exact"] == 0, p
-                rows = 16 if name == "stream_f32_d64" else 32
-                assert p["rows_per_window"] == rows and p["subchunks"] == 8 and p["kernels"] == 1
-                assert p["threads_per_cta"] == 11 * 32 and p["stages"] == 16
+                assert p["rows_per_window"] == rows and p["subchunks"] == nwin and p["kernels"] == 1
+                nst = stages if isinstance(stages, int) else stages[direction == "bwd"]
+                assert p["threads_per_cta"] == threads and p["stages"] == nst
                 dtl = p["lanes_per_cta"]
-                chunk = 8 * rows
+                chunk = nwin * rows
                 ng, nc = B * -(-D // dtl), -(-T // chunk)
                 assert p["workspace_bytes"] == 256 + pad(ng * nc * 4) + pad(ng * nc * dtl * 8) + pad(ng * nc * dtl * 4)
                 l2_ctas = max(152, (48 << 20) * 2 // (7 * chunk * dtl * es * 2))
-                resident = min(2 if name == "stream_bf16_d32" else 1, 233472 // (p["smem_bytes"] + 1024))
+                resident = min(per_sm, 233472 // (p["smem_bytes"] + 1024))
                 assert p["ctas"] == min(ng * nc, resident * 152, l2_ctas), p
     # a short sequence: no more CTAs than chunk tickets
     assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 4
@@ -345,4 +354,4 @@ def test_stream_plans(lib):
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
     with pytest.raises(L.LrscanError):
-        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=3)
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=5)
