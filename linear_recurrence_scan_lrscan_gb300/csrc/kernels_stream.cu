@@ -89,6 +89,7 @@ WinDirCfg split_cfg() {
     d.smem = g.smem_bytes;
     d.stage_bytes = g.rstage_bytes;
     d.max_resident = 1;
+    d.ws_unset = 1;
     d.launch = &launch_split<C, !FWD>;
     d.launch_state = nullptr;
     return d;

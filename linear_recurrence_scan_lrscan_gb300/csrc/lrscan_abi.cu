@@ -186,7 +186,9 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = tr
 
 // Chunk-streaming workspace: the ticket word (first 256 bytes), one flag per
 // chunk, then the chunk maps (float2 per lane) and leaving states (float per
-// lane); the ticket and the flags are zeroed before every launch.
+// lane); the ticket and the flags are zeroed before every launch, and for
+// kernels that publish without flags the maps and states are filled with
+// all-ones words.
 struct StreamScratch {
     size_t flags;  // byte size, padded to 256
     size_t agg, incl;
@@ -698,7 +700,8 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
     L.sa.ndt = static_cast<int>(ndt);
     L.sa.ng = static_cast<int>(ng);
     L.grid = static_cast<int>(ch.ctas);
-    if (cudaMemsetAsync(ws, 0, sc.head(), st) != cudaSuccess) {
+    if (cudaMemsetAsync(ws, 0, sc.head(), st) != cudaSuccess ||
+        (v.ws_unset && cudaMemsetAsync(base + sc.head(), 0xff, sc.agg + sc.incl, st) != cudaSuccess)) {
         cudaGetLastError();
         return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
     }

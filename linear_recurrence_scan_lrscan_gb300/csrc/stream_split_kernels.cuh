@@ -17,10 +17,10 @@
 //   summary warps   reduce their windows, wait until the replay warps have
 //                   finished chunk k - NB (buffer free), write their window
 //                   maps; the last one to finish composes the chunk's map,
-//                   publishes it (flag kChunkAgg) and signals maps_ready[b];
+//                   publishes it and signals maps_ready[b];
 //   scan warp       looks back for the entering state, publishes the leaving
-//                   state (kChunkIncl), writes each window's entering state and
-//                   signals entries_ready[b];
+//                   state, writes each window's entering state and signals
+//                   entries_ready[b];
 //   replay warps    replay their windows, store the outputs and signal
 //                   buf_free[b].
 // The first invalid ticket ends the sequence: summary warp 0 writes an end
@@ -74,6 +74,124 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *m, uint32_t
                      "l"(reinterpret_cast<uint64_t>(m)),
                  "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
                  : "memory");
+}
+
+// Publication without flags or fences.  The workspace's chunk maps and
+// leaving states start filled with kUnset words; a lane publishes its map as
+// one 64-bit word (P low, Q high) and its leaving state as one 32-bit word,
+// each a single-copy-atomic relaxed store at GPU scope, so a reader that sees
+// a word other than kUnset sees the whole value.  A value whose bits are
+// kUnset (a NaN) is published as another NaN.
+constexpr uint32_t kUnset = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t unset_safe_bits(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return u == kUnset ? 0x7fffffffu : u;
+}
+__device__ __forceinline__ void publish_map(float2 *p, float P, float Q) {
+    const uint64_t word = (static_cast<uint64_t>(unset_safe_bits(Q)) << 32) | unset_safe_bits(P);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(word) : "memory");
+}
+__device__ __forceinline__ void publish_state(float *p, float h) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(unset_safe_bits(h)) : "memory");
+}
+__device__ __forceinline__ uint64_t peek_map(const float2 *p) {
+    uint64_t word;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(word) : "l"(p) : "memory");
+    return word;
+}
+__device__ __forceinline__ uint32_t peek_state(const float *p) {
+    uint32_t word;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(word) : "l"(p) : "memory");
+    return word;
+}
+
+// Entering state of chunk `cc` (ticket order within group gi) for lanes
+// i0 .. i0+V-1; the whole warp calls it.  Each lane walks back on its own:
+// per round it reads the leaving states and maps of its next BATCH chunks (one
+// L2 round trip), folds maps in until it meets a published leaving state
+// (done) or a chunk with nothing out yet (read again next round).  Maps are
+// composed outermost first: h_in = M_cc-1 o M_cc-2 o ... (h_state); chunk -1
+// leaves the zero state.  Returns false when the wait expired or the CTA is
+// aborting.
+template <int DT, int V, int BATCH>
+__device__ bool split_lookback(const StreamArgs &sa, int gi, int cc, int i0, float (&h_in)[V], const WaitCtx &wc) {
+    const int lane = threadIdx.x & 31;
+    const size_t g0 = static_cast<size_t>(gi) * sa.nc;
+    float aP[V], aQ[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { aP[v] = 1.0f; aQ[v] = 0.0f; }
+    int j = cc - 1;  // the next chunk this lane folds
+    bool done = false;
+    uint64_t start = 0;
+    bool timed = false;
+    for (uint32_t spin = 0;; ++spin) {
+        if (!done) {
+            uint32_t st[BATCH][V];
+            uint64_t mw[BATCH][V];
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (j - t >= 0) {
+                    const size_t row = (g0 + j - t) * DT + i0;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        st[t][v] = peek_state(sa.incl + row + v);
+                        mw[t][v] = peek_map(sa.agg + row + v);
+                    }
+                }
+            }
+            bool go = true;
+            int folded = 0;
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (go) {
+                    if (j - t < 0) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) h_in[v] = aQ[v];  // aP * 0 + aQ
+                        done = true;
+                        go = false;
+                    } else {
+                        bool has_state = true, has_map = true;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            has_state = has_state && st[t][v] != kUnset;
+                            has_map = has_map && static_cast<uint32_t>(mw[t][v]) != kUnset;
+                        }
+                        if (has_state) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) h_in[v] = __fmaf_rn(aP[v], __uint_as_float(st[t][v]), aQ[v]);
+                            done = true;
+                            go = false;
+                        } else if (has_map) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                const float P = __uint_as_float(static_cast<uint32_t>(mw[t][v]));
+                                const float Q = __uint_as_float(static_cast<uint32_t>(mw[t][v] >> 32));
+                                aQ[v] = __fmaf_rn(aP[v], Q, aQ[v]);
+                                aP[v] = __fmul_rn(aP[v], P);
+                            }
+                            ++folded;
+                        } else {
+                            go = false;  // not out yet: read it again next round
+                        }
+                    }
+                }
+            }
+            j -= folded;
+        }
+        if (__all_sync(0xffffffffu, done)) return true;
+        if ((spin & 7u) == 7u) {
+            bool stop = *wc.abort_flag != 0;
+            if (!timed) {
+                start = global_timer_ns();
+                timed = true;
+            } else if (global_timer_ns() - start > wc.timeout_ns) {
+                stop = true;
+                if (lane == 0) record_error(wc, kErrTimeout, kSiteLookback);
+            }
+            if (__any_sync(0xffffffffu, stop)) return false;
+        }
+    }
 }
 
 // Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
@@ -379,11 +497,10 @@ stream_split_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_const
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     cmap[b * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
-                    sa.agg[slot_g * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
+                    publish_map(sa.agg + slot_g * DT + lane * V + v, Pc[v], Qc[v]);
                 }
-                __syncwarp();  // every lane's map written before lane 0's release
+                __syncwarp();  // every lane's cmap entries written before the maps_ready arrive
                 if (lane == 0) {
-                    st_release_gpu(sa.flag + slot_g, kChunkAgg);
                     tick_of[b] = tk;
                     wcount[b] = 0;  // next used NB chunks on, after this buffer's replays
                     mbar_arrive(maps_bar(b));
@@ -411,12 +528,10 @@ stream_split_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_const
                 Qc[v] = m.y;
             }
             float h[V];
-            if (!stream_lookback<DT, V, 32 / V>(sa, ch.gi, ch.cc, i0, h, wc)) return;
+            if (!split_lookback<DT, V, 16 / V>(sa, ch.gi, ch.cc, i0, h, wc)) return;
             const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
 #pragma unroll
-            for (int v = 0; v < V; ++v) sa.incl[slot_g * DT + i0 + v] = __fmaf_rn(Pc[v], h[v], Qc[v]);
-            __syncwarp();  // every lane's state written before lane 0's release
-            if (lane == 0) st_release_gpu(sa.flag + slot_g, kChunkIncl);
+            for (int v = 0; v < V; ++v) publish_state(sa.incl + slot_g * DT + i0 + v, __fmaf_rn(Pc[v], h[v], Qc[v]));
             // the state entering every window, in chain order
             const float2 *mp = wmap + b * NWIN * DT;
             float *ep = wentry + b * NWIN * DT;
