@@ -780,10 +780,10 @@ def run_long_t(dev, peak) -> dict:
     """Few lanes, very long sequence: B=1 T=2^22 D=64 fp32: the chunked path
     with chunk 64 (65,536 chunk maps per lane, 64 lanes) with the flat prefix
     (one warp per lane walks all maps) and with the grouped prefix, the
-    single-pass chunk-streaming path on 32- and 64-lane tiles, and the
-    automatic plan (grouped prefix over 512-step chunks forward, streaming
-    backward).  Inputs are drawn on
-    the device from a seeded generator (a~U(0.9,0.9999), b,g~N(0,1))."""
+    chunked path at its own chunk lengths (grouped prefix over 512-step chunks
+    forward, 128 backward), the single-pass chunk-streaming path, and the
+    automatic plan (streaming).  Inputs are drawn on the device from a seeded
+    generator (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
@@ -799,8 +799,8 @@ def run_long_t(dev, peak) -> dict:
     res = {"workload": f"B={B} T={T} D={D} fp32 chunk {C} (few lanes, long sequence)"}
     for kw, name in ((dict(path="chunk", chunk_len=C, tile_variant=1), "flat_prefix"),
                      (dict(path="chunk", chunk_len=C, tile_variant=2), "grouped_prefix"),
-                     (dict(path="stream", tile_variant=1), "stream_d32"),
-                     (dict(path="stream", tile_variant=2), "stream_d64")):
+                     (dict(path="chunk"), "chunked_own_length"),
+                     (dict(path="stream"), "stream")):
         fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last, **kw), 10, stream)
         bms = time_launches(lambda i: L.lrscan_bwd(a, out, g, ga, gb, **kw), 10, stream)
         res[name] = {"fwd_ms": fms, "bwd_ms": bms,

@@ -74,16 +74,18 @@ extern "C" {
 #define LRSCAN_PATH_WINDOW  3  /* single pass: time windows in shared memory, split in time inside the CTA */
 #define LRSCAN_PATH_PLAIN   4  /* sequential, plain loads; any alignment */
 #define LRSCAN_PATH_STREAM  5  /* single pass over time chunks (triton_training_scan.py, _real_chunk_summary /
-                                  _real_chunk_prefix / _real_chunk_replay fused): persistent CTAs take chunks of
-                                  256 steps (128 for 64-lane fp32 tiles) in ticket order, publish each chunk's map,
-                                  find its entering state by looking back over the published maps and leaving
-                                  states, and replay it while its tiles are still in L2.  Bulk-copy path (16-byte
+                                  _real_chunk_prefix / _real_chunk_replay fused): one persistent CTA per SM takes
+                                  chunks of 512 steps (bf16 forward on 32-lane tiles: 1024) in ticket order; its
+                                  summary warps publish each chunk's map, a scan warp finds the entering state by
+                                  looking back over the published maps and leaving states, and its replay warps
+                                  run the chunk again while its tiles are still in L2.  Bulk-copy path (16-byte
                                   aligned rows); plain scan only (no carried state); needs workspace_bytes of device
                                   scratch like the chunked path; agrees with the sequential definition to rounding,
                                   and two calls may differ in the last bits (which published states a look-back
-                                  composes depends on timing).  tile_variant: 1 = 32-lane tiles, 2 = 64-lane tiles.
-                                  Auto takes it for few lanes and at least 64 chunks per lane group when it measured
-                                  faster than the chunked path: bf16, the fp32 backward, fp32 from 256 lanes */
+                                  composes depends on timing).  tile_variant: fp32 1 = 32-lane tiles; bf16 1 =
+                                  32-lane tiles, 2 = 64-lane tiles.  Auto takes it for few lanes and at least 32
+                                  chunks of 512 steps per lane group (bf16: the 64-lane tile for a backward on at
+                                  most 128 lanes) */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */

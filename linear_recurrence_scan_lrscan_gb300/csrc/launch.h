@@ -78,7 +78,6 @@ struct WinDirCfg {
     int smem;        // dynamic shared memory bytes
     int stage_bytes;
     int max_resident;  // CTAs per SM the registers allow (0: not limited beyond threads and shared memory)
-    int ws_unset;      // chunk streaming: maps and states start as all-ones words (1), or flags start at zero (0)
     int (*launch)(const WinLaunch &, const WinDirCfg &);        // plain scan
     int (*launch_state)(const WinLaunch &, const WinDirCfg &);  // with carried state / resets
 };

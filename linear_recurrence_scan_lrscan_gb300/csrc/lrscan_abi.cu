@@ -184,21 +184,18 @@ size_t chunk_workspace(int64_t B, int64_t T, int64_t D, int C, bool grouped = tr
     return chunk_scratch(B, T, D, C, grouped).total();
 }
 
-// Chunk-streaming workspace: the ticket word (first 256 bytes), one flag per
-// chunk, then the chunk maps (float2 per lane) and leaving states (float per
-// lane); the ticket and the flags are zeroed before every launch, and for
-// kernels that publish without flags the maps and states are filled with
-// all-ones words.
+// Chunk-streaming workspace: the ticket word (first 256 bytes), then the
+// chunk maps (float2 per lane) and leaving states (float per lane); before
+// every launch the ticket is zeroed and the maps and states are filled with
+// all-ones words (nothing published).
 struct StreamScratch {
-    size_t flags;  // byte size, padded to 256
-    size_t agg, incl;
-    size_t head() const { return 256 + flags; }
+    size_t agg, incl;  // byte sizes, padded to 256
+    size_t head() const { return 256; }
     size_t total() const { return head() + agg + incl; }
 };
 StreamScratch stream_scratch(int64_t ng, int64_t nc, int dt) {
     auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
     StreamScratch s;
-    s.flags = pad(static_cast<size_t>(ng) * nc * 4);
     s.agg = pad(static_cast<size_t>(ng) * nc * dt * 8);
     s.incl = pad(static_cast<size_t>(ng) * nc * dt * 4);
     return s;
@@ -364,15 +361,15 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
             // measured preference list (see auto_candidate)
         } else if (T >= 16LL * chunk) {
             // too few lanes for a lane-tiled walk to fill the GPU: parallelize
-            // over time chunks instead -- in one pass (chunk streaming) where
-            // that measured faster than the three chunked phases: bf16, the
-            // fp32 backward, and the fp32 forward from 256 lanes (B=1 T=2^22
-            // D=64 fp32 forward: 0.87 ms chunked against 0.98 ms streamed;
-            // backward 1.27 against 1.24 ms; bf16 0.72 / 0.81 against 0.58 /
-            // 0.70 ms; B=8 T=2^18 D=64 fp32 0.50 / 0.74 against 0.42 / 0.56 ms)
+            // over time chunks instead, in one pass (chunk streaming) from 32
+            // chunks of 512 steps per lane group (measured against the three
+            // chunked phases, fp32 forward / backward: B=1 T=2^22 D=64 0.52 /
+            // 0.97 against 0.87 / 1.25 ms; B=1 T=2^14 D=64 26 / 23 against
+            // 33 / 54 us; B=4 T=2^16 D=256 0.16 / 0.26 against 0.27 / 0.39 ms),
+            // else (or with a chunk length asked for) in three chunked phases
             path = kPathChunk;
-            const bool long_seq = T >= 64LL * 256;  // 64 chunks of 256 steps per lane group
-            if (!ext && long_seq && (dtype == LRSCAN_BF16 || dir == 1 || B * D >= 256)) path = kPathStream;
+            const bool long_seq = T >= 32LL * 512;
+            if (!ext && long_seq && !(opts && opts->chunk_len)) path = kPathStream;
         } else {
             path = kPathSeq;  // small problem: latency-bound whatever runs it
         }
@@ -413,11 +410,12 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         int n = 0;
         const WinVariant *tab = stream_variants(dtype, &n);
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
-        // 64-lane tiles where they give four lane groups (fp32) or wherever
-        // a row holds 64 lanes (bf16); else 32-lane tiles
+        // fp32: one variant.  bf16: 32-lane tiles, except the backward on at
+        // most 128 lanes, where the 64-lane tile measured faster (B=1 T=2^22
+        // D=64 backward: 0.49 against 0.54 ms; B=8 T=2^18 D=64: 0.25 against
+        // 0.25 ms, D=256 T=2^20: 0.51 against 0.47 ms)
         int vi = force_v > 0 ? force_v - 1 : 0;
-        if (force_v == 0 && n > 1)
-            vi = (dtype == LRSCAN_BF16 ? D >= 64 : B * ((D + 63) / 64) >= 4) ? 1 : 0;
+        if (force_v == 0 && dtype == LRSCAN_BF16 && dir == 1 && B * D <= 128) vi = 1;
         const WinDirCfg &v = dir_of(tab[vi], dir);
         const Occ o = occupancy(tab[vi], dir, B, D, g);
         if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);
@@ -428,15 +426,13 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         ch->vidx = vi;
         ch->var = &tab[vi];
         ch->chunk = static_cast<int>(rows);
+        // One CTA per SM (no more than there are chunk tickets).  A chunk's
+        // tiles must still be in L2 when its replay reads them: with two chunk
+        // buffers a CTA holds at most about two and a half chunks of input
+        // planes between summaries and replays (512-step fp32 chunks: 40 MB
+        // over 152 SMs).
         const int resident = v.max_resident > 0 ? std::min(o.resident, v.max_resident) : o.resident;
-        // A chunk's tiles must still be in L2 when its replay reads them: a CTA
-        // brings about 3.5 chunks' worth of input planes into L2 between a
-        // chunk's summary and its replay (the replay trails by two chunks), so
-        // the grid keeps that under 48 MB.
-        const long long chunk_in = rows * v.dt * esize(dtype) * 2;
-        const long long l2_ctas = std::max<long long>(g.sm_count, (48LL << 20) * 2 / (7 * chunk_in));
-        ch->ctas = std::min<long long>(std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count),
-                                       l2_ctas);
+        ch->ctas = std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count);
         ch->threads = v.threads;
         ch->smem = v.smem;
         ch->stages = v.nstage;
@@ -659,8 +655,8 @@ int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_
 
 // The persistent chunk-streaming path: tensor maps of the inputs (forward a,
 // b; backward a, out, grad_out) and outputs (forward out; backward grad_a,
-// grad_b), the publication workspace zeroed where the kernel expects it, one
-// launch.
+// grad_b), the publication workspace reset (ticket zeroed, maps and states
+// all-ones), one launch.
 int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::initializer_list<void *> outs,
                float *last, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev, DeviceCtx *ctx,
                const lrscan_opts *opts, bool bwd) {
@@ -692,16 +688,14 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
     L.device = dev;
     char *base = static_cast<char *>(ws);
     L.sa.ticket = reinterpret_cast<unsigned int *>(base);
-    L.sa.flag = reinterpret_cast<uint32_t *>(base + 256);
     L.sa.agg = reinterpret_cast<float2 *>(base + sc.head());
     L.sa.incl = reinterpret_cast<float *>(base + sc.head() + sc.agg);
     L.sa.nc = static_cast<int>(nc);
-    L.sa.nwc = v.s;
     L.sa.ndt = static_cast<int>(ndt);
     L.sa.ng = static_cast<int>(ng);
     L.grid = static_cast<int>(ch.ctas);
     if (cudaMemsetAsync(ws, 0, sc.head(), st) != cudaSuccess ||
-        (v.ws_unset && cudaMemsetAsync(base + sc.head(), 0xff, sc.agg + sc.incl, st) != cudaSuccess)) {
+        cudaMemsetAsync(base + sc.head(), 0xff, sc.agg + sc.incl, st) != cudaSuccess) {
         cudaGetLastError();
         return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
     }

@@ -9,16 +9,15 @@
 namespace lrscan {
 
 // Publication workspace of one call of the persistent chunk-streaming kernels
-// (ticket counter and per-chunk flags zeroed before the launch; maps and
-// leaving states written by the kernel).  Chunks are indexed in ticket order
-// within each lane group (the backward takes the latest chunk first).
+// (ticket counter zeroed, maps and leaving states filled with all-ones words
+// before the launch; maps and leaving states then written by the kernel).
+// Chunks are indexed in ticket order within each lane group (the backward
+// takes the latest chunk first).
 struct StreamArgs {
     unsigned int *ticket;  // next chunk ticket
-    uint32_t *flag;        // [ng * nc] publication states
     float2 *agg;           // [ng * nc][DT] chunk maps (P, Q), lane-thread order
     float *incl;           // [ng * nc][DT] state leaving the chunk, lane-thread order
     int nc;                // chunks per lane group
-    int nwc;               // windows per chunk
     int ndt;               // lane tiles per batch row
     int ng;                // lane groups: B * ndt
 };

@@ -5,44 +5,39 @@
 // own).
 //
 // Every lane group (batch row x lane tile of DT lanes) is cut in time into
-// chunks of NWC windows of W rows.  A fixed grid of CTAs takes chunks from a
-// ticket counter, chunk-major over the groups (forward: earliest chunk first;
-// backward: latest first).  A CTA has NWC window warps (warp w owns window w
-// of every chunk, all DT lanes, V lanes per thread), two scan warps (chunks
-// alternate between them) and a ticket warp, and passes over each chunk
-// twice:
-//   summary  each window warp copies its window's tiles in (bulk tensor
-//            copies, from HBM) and reduces them to the affine map
-//            h -> P h + Q of its rows, one lane per thread;
-//   prefix   the last window warp to finish composes the window maps into
-//            the chunk's map and publishes it; a scan warp looks back over
-//            the chunks before it (the nearest one whose leaving state is
-//            published, composed with the maps of the chunks in between,
-//            gives the entering state), publishes the chunk's leaving state,
-//            and hands every window warp the state entering its window;
-//   replay   each window warp copies the same tiles in again, now from L2,
-//            runs its rows with the sequential step from its entering state
-//            and stores every output row straight to global memory (a warp
-//            writes whole rows of its DT lanes).
-// The replay of chunk k follows the summaries of chunks k+1 and k+2, and two
-// scan warps look back for consecutive chunks at once, so the look-back's
-// latency (a few L2 round trips) hides behind two chunks of work; the three
-// chunks between a summary and its replay are what L2 holds.  Each window
-// warp owns two ring stages (summary and replay tiles), so one tile loads
-// while it works on the other.
+// chunks of NWIN windows of W rows.  A fixed grid of CTAs (one per SM) takes
+// chunks from a ticket counter, chunk-major over the groups (forward: earliest
+// chunk first; backward: latest first), and passes over each chunk twice:
+// once to reduce it to its affine map h -> P h + Q (tiles from HBM), once to
+// replay it from its entering state (the same tiles again, from L2).  A CTA's
+// warps have one role each:
+//   ticket warp     fetches chunk tickets two chunks ahead of the summaries;
+//   NW summary      warp w reduces windows w, w + NW, ... of every chunk,
+//   warps           streaming its tiles through S stages of its own (S - 1
+//                   copies in flight ahead of the tile it reduces); the last
+//                   to finish a chunk composes the window maps and publishes
+//                   the chunk's map;
+//   NSCAN scan      chunk k goes to scan warp k mod NSCAN: it looks back over
+//   warps           the chunks before it for the entering state, publishes
+//                   the leaving state and hands out each window's entering
+//                   state;
+//   NW replay       warp w replays the windows its summary twin reduced,
+//   warps           through SR stages of its own: each row's result
+//                   overwrites the input it consumed in shared memory, and
+//                   the window leaves by bulk tensor stores.
+// Summaries run ahead of replays by up to NB - 1 chunks (the map and
+// entering-state buffers are the only link), so a chunk's map is out as soon
+// as its tiles have landed, whatever the replays wait for; NB is kept small
+// so that a chunk's tiles are still in L2 when its replay reads them (loads
+// for the replay carry an evict-first hint, the summaries' an evict-last one).
+//
 // HBM carries the scan's own traffic: forward a, b in, out out; backward a,
 // out, grad_out in, grad_a, grad_b out.  Results agree with the sequential
 // definition to rounding; which published states a look-back composes depends
-// on timing, so two calls can differ in the last bits.
-//
-// Publication: one flag word per chunk (0 before the call, kChunkAgg once the
-// map is out, kChunkIncl once the leaving state is out): the warp's lanes
-// write their lanes' values, a warp barrier, then lane 0 stores the flag with
-// release semantics; readers acquire the flags, pass a warp barrier, and read
-// the values past L1.  The look-back waits only on chunks with earlier
-// tickets, which running CTAs hold, so it always ends; still every wait is
-// bounded (timeout: LRSCAN_ETIMEOUT in the status word, and the kernel
-// returns).
+// on timing, so two calls can differ in the last bits.  The look-back waits
+// only on chunks with earlier tickets, which running CTAs hold, so it always
+// ends; still every wait is bounded (timeout: LRSCAN_ETIMEOUT in the status
+// word, and the kernel returns).
 #pragma once
 
 #include "scan_common.cuh"
@@ -50,165 +45,13 @@
 
 namespace lrscan {
 
-constexpr uint32_t kChunkAgg = 1, kChunkIncl = 2;
-
 enum StreamSite : int { kSiteLookback = 8, kSiteStreamStep = 9 };
-
-// Chunks a replay trails its summary by, scan warps, and map / entering-state
-// buffers (one per chunk between a summary and its replay, plus one).
-constexpr int kStreamLag = 2, kStreamScanWarps = 2, kStreamBufs = kStreamLag + 1;
-
-// Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
-// window (per window warp), windows per chunk, CTAs per SM the registers must
-// allow.  One warp spans the DT lanes of a window row.
-template <class St_, int DT_, int V_, int W_, int NWC_, int MINB_>
-struct StreamShape {
-    using St = St_;
-    static constexpr int DT = DT_, V = V_, W = W_, NWC = NWC_, MINB = MINB_;
-    static constexpr int THREADS = (NWC + kStreamScanWarps + 1) * 32;
-    static_assert(DT == 32 * V, "one warp spans a tile row");
-    static_assert(W % 8 == 0, "rows are taken eight at a time");
-};
-
-// Steps a CTA keeps tickets for (ring of step slots).
-constexpr int kStreamStepSlots = 8;
-
-// Shared-memory layout (bytes from the 1024-aligned base), host and device.
-struct StreamGeom {
-    int nstage;      // ring stages (window tiles): 2 * NWC, two per window warp
-    int tile_bytes;  // one plane of one window: W * DT * elem
-    int stage_bytes; // NIN planes
-    int bar_off;     // full[nstage], step_free[nstage], step_full[slots], maps_ready[bufs], entries_ready[bufs]
-    int ticket_off;  // step tickets [slots]
-    int map_off;     // window maps [bufs][NWC][DT] float2
-    int entry_off;   // window entering states [bufs][NWC][DT] float
-    int cmap_off;    // chunk maps [bufs][DT] float2, composed by the last window warp
-    int count_off;   // window warps done with a chunk's summary [bufs]
-    int flag_off;    // abort flag
-    int smem_bytes;
-};
-
-template <class C, int NIN>
-__host__ __device__ inline StreamGeom make_stream_geom(int nstage) {
-    StreamGeom g{};
-    g.nstage = nstage;
-    g.tile_bytes = C::W * C::DT * static_cast<int>(sizeof(typename C::St));
-    g.stage_bytes = NIN * g.tile_bytes;
-    g.bar_off = nstage * g.stage_bytes;
-    const int nbar = 2 * nstage + kStreamStepSlots + 2 * kStreamBufs;
-    g.ticket_off = g.bar_off + nbar * 8;
-    g.map_off = (g.ticket_off + kStreamStepSlots * 4 + 15) / 16 * 16;
-    g.entry_off = g.map_off + kStreamBufs * C::NWC * C::DT * 8;
-    g.cmap_off = g.entry_off + kStreamBufs * C::NWC * C::DT * 4;
-    g.count_off = g.cmap_off + kStreamBufs * C::DT * 8;
-    g.flag_off = g.count_off + kStreamBufs * 4;
-    g.smem_bytes = g.flag_off + 16;
-    return g;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ unsigned int atom_add_acq_rel_cta(unsigned int *p, unsigned int v) {
     unsigned int old;
     asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v)
                  : "memory");
     return old;
-}
-
-// Entering state of chunk `cc` (ticket order within group gi) for lanes
-// i0 .. i0+V-1, from the chunk maps and leaving states other CTAs published;
-// the whole warp calls it.  Lane l of the warp inspects chunk base - l: the
-// nearest chunk whose leaving state is out bounds the walk, and every chunk
-// between (in ticket order) must have its map out.  Maps are composed
-// outermost first: h_in = M_base o M_base-1 o ... (h_state); chunk -1 leaves
-// the zero state.  Returns false when the wait expired or the CTA is aborting.
-template <int DT, int V, int BATCH>
-__device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, float (&h_in)[V], const WaitCtx &wc) {
-    static_assert(32 % BATCH == 0, "whole batches per round");
-    const int lane = threadIdx.x & 31;
-    const size_t g0 = static_cast<size_t>(gi) * sa.nc;
-    float aP[V], aQ[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) { aP[v] = 1.0f; aQ[v] = 0.0f; }
-    int base = cc - 1;
-    uint64_t start = 0;
-    bool timed = false;
-    for (;;) {
-        if (base < 0) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) h_in[v] = aQ[v];  // aP * 0 + aQ
-            return true;
-        }
-        const int ci = base - lane;
-        int tstar = 32;
-        for (uint32_t spin = 0;; ++spin) {
-            const uint32_t f = ci >= 0 ? ld_acquire_gpu(sa.flag + g0 + ci) : kChunkIncl;
-            const uint32_t ready = __ballot_sync(0xffffffffu, f != 0u);
-            const uint32_t inclm = __ballot_sync(0xffffffffu, f == kChunkIncl);
-            tstar = inclm ? __ffs(inclm) - 1 : 32;
-            const uint32_t need = tstar >= 31 ? 0xffffffffu : ((2u << tstar) - 1u);
-            if ((ready & need) == need) break;
-            if ((spin & 31u) == 31u) {
-                bool stop = *wc.abort_flag != 0;
-                if (!timed) {
-                    start = global_timer_ns();
-                    timed = true;
-                } else if (global_timer_ns() - start > wc.timeout_ns) {
-                    stop = true;
-                    if (lane == 0) record_error(wc, kErrTimeout, kSiteLookback);
-                }
-                if (__any_sync(0xffffffffu, stop)) return false;
-            }
-        }
-        // the maps and states read below were published before flags that
-        // other lanes of this warp acquired: the warp barrier orders those
-        // acquires before every lane's reads (loads bypass L1)
-        __syncwarp();
-        const int nagg = tstar < 32 ? tstar : 32;
-        // the maps of up to 32 chunks: every load of a batch issued before
-        // any is used (one L2 round trip per batch), then folded in order
-#pragma unroll
-        for (int t0 = 0; t0 < 32; t0 += BATCH) {
-            if (t0 >= nagg) break;
-            float2 m[BATCH][V];
-#pragma unroll
-            for (int t = 0; t < BATCH; ++t) {
-                if (t0 + t < nagg) {
-                    const float2 *row = sa.agg + (g0 + base - t0 - t) * DT + i0;
-#pragma unroll
-                    for (int v = 0; v < V; ++v) m[t][v] = __ldcg(row + v);
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < BATCH; ++t) {
-                if (t0 + t < nagg) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        aQ[v] = __fmaf_rn(aP[v], m[t][v].y, aQ[v]);
-                        aP[v] = __fmul_rn(aP[v], m[t][v].x);
-                    }
-                }
-            }
-        }
-        if (tstar < 32) {
-            const int cb = base - tstar;
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float hb = cb >= 0 ? __ldcg(sa.incl + (g0 + cb) * DT + i0 + v) : 0.0f;
-                h_in[v] = __fmaf_rn(aP[v], hb, aQ[v]);
-            }
-            return true;
-        }
-        base -= 32;
-    }
 }
 
 // Bounded wait on an mbarrier by a whole warp, the outcome agreed.
@@ -224,57 +67,282 @@ __device__ __forceinline__ void load8(const St *tile, int r0, int lane, float (&
     for (int r = 0; r < 8; ++r) unpack_lanes<St, V>(tile + (r0 + r) * DT + lane * V, x[r]);
 }
 
-// One kernel for both directions.  Forward tiles: a, b (row t); output out.
-// Backward tiles: a one row late (a_{t+1}), out one row early (h_{t-1}),
-// grad_out; outputs grad_a (out0), grad_b (out1).  Outputs are written
-// directly to global memory.
-//
-// Steps: step k takes ticket k (-1 once the chunks are gone) and runs the
-// summary of ticket k, then the replay of ticket k - kStreamLag.  Window warp w
-// keeps its summary tiles in stage w and its replay tiles in stage NWC + w and
-// issues their bulk copies itself, each as soon as the stage's previous tile
-// is done (the next summary's before this step's replay, the next replay's
-// after it).  A ticket warp fetches ticket k once the window warps have
-// finished step k - 3 and publishes it in a ring of step slots.
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// L2 eviction priorities: a summary's tiles are read again by the replay
+// (evict last), a replay's tiles and the outputs are not (evict first).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *m, int x, int y, int z, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// tma_store_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *m, uint32_t src, int x, int y, int z,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::
+                     "l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+                 : "memory");
+}
+
+// Publication without flags or fences.  The workspace's chunk maps and
+// leaving states start filled with kUnset words; a lane publishes its map as
+// one 64-bit word (P low, Q high) and its leaving state as one 32-bit word,
+// each a single-copy-atomic relaxed store at GPU scope, so a reader that sees
+// a word other than kUnset sees the whole value.  A value whose bits are
+// kUnset (a NaN) is published as another NaN.
+constexpr uint32_t kUnset = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t unset_safe_bits(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return u == kUnset ? 0x7fffffffu : u;
+}
+__device__ __forceinline__ void publish_map(float2 *p, float P, float Q) {
+    const uint64_t word = (static_cast<uint64_t>(unset_safe_bits(Q)) << 32) | unset_safe_bits(P);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(word) : "memory");
+}
+__device__ __forceinline__ void publish_state(float *p, float h) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(unset_safe_bits(h)) : "memory");
+}
+__device__ __forceinline__ uint64_t peek_map(const float2 *p) {
+    uint64_t word;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(word) : "l"(p) : "memory");
+    return word;
+}
+__device__ __forceinline__ uint32_t peek_state(const float *p) {
+    uint32_t word;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(word) : "l"(p) : "memory");
+    return word;
+}
+
+// Entering state of chunk `cc` (ticket order within group gi) for lanes
+// i0 .. i0+V-1; the whole warp calls it.  Each lane walks back on its own:
+// per round it reads the leaving states and maps of its next BATCH chunks (one
+// L2 round trip), folds maps in until it meets a published leaving state
+// (done) or a chunk with nothing out yet (read again next round).  Maps are
+// composed outermost first: h_in = M_cc-1 o M_cc-2 o ... (h_state); chunk -1
+// leaves the zero state.  Returns false when the wait expired or the CTA is
+// aborting.
+template <int DT, int V, int BATCH>
+__device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, float (&h_in)[V], const WaitCtx &wc) {
+    const int lane = threadIdx.x & 31;
+    const size_t g0 = static_cast<size_t>(gi) * sa.nc;
+    float aP[V], aQ[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { aP[v] = 1.0f; aQ[v] = 0.0f; }
+    int j = cc - 1;  // the next chunk this lane folds
+    bool done = false;
+    uint64_t start = 0;
+    bool timed = false;
+    for (uint32_t spin = 0;; ++spin) {
+        if (!done) {
+            uint32_t st[BATCH][V];
+            uint64_t mw[BATCH][V];
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (j - t >= 0) {
+                    const size_t row = (g0 + j - t) * DT + i0;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        st[t][v] = peek_state(sa.incl + row + v);
+                        mw[t][v] = peek_map(sa.agg + row + v);
+                    }
+                }
+            }
+            bool go = true;
+            int folded = 0;
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (go) {
+                    if (j - t < 0) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) h_in[v] = aQ[v];  // aP * 0 + aQ
+                        done = true;
+                        go = false;
+                    } else {
+                        bool has_state = true, has_map = true;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            has_state = has_state && st[t][v] != kUnset;
+                            has_map = has_map && static_cast<uint32_t>(mw[t][v]) != kUnset;
+                        }
+                        if (has_state) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) h_in[v] = __fmaf_rn(aP[v], __uint_as_float(st[t][v]), aQ[v]);
+                            done = true;
+                            go = false;
+                        } else if (has_map) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                const float P = __uint_as_float(static_cast<uint32_t>(mw[t][v]));
+                                const float Q = __uint_as_float(static_cast<uint32_t>(mw[t][v] >> 32));
+                                aQ[v] = __fmaf_rn(aP[v], Q, aQ[v]);
+                                aP[v] = __fmul_rn(aP[v], P);
+                            }
+                            ++folded;
+                        } else {
+                            go = false;  // not out yet: read it again next round
+                        }
+                    }
+                }
+            }
+            j -= folded;
+        }
+        if (__all_sync(0xffffffffu, done)) return true;
+        if ((spin & 7u) == 7u) {
+            bool stop = *wc.abort_flag != 0;
+            if (!timed) {
+                start = global_timer_ns();
+                timed = true;
+            } else if (global_timer_ns() - start > wc.timeout_ns) {
+                stop = true;
+                if (lane == 0) record_error(wc, kErrTimeout, kSiteLookback);
+            }
+            if (__any_sync(0xffffffffu, stop)) return false;
+        }
+    }
+}
+
+// Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
+// window, summary (= replay) warps, windows per warp and chunk, summary and
+// replay stages per warp, scan warps, chunk buffers.
+template <class St_, int DT_, int V_, int W_, int NW_, int R_, int S_, int SR_, int NSCAN_, int NB_>
+struct StreamShape {
+    using St = St_;
+    static constexpr int DT = DT_, V = V_, W = W_, NW = NW_, R = R_, S = S_, SR = SR_, NSCAN = NSCAN_, NB = NB_;
+    static constexpr int NWIN = NW * R;  // windows per chunk
+    static constexpr int THREADS = (2 * NW + NSCAN + 1) * 32;
+    static constexpr int MINB = 1;
+    static_assert(DT == 32 * V, "one warp spans a tile row");
+    static_assert(W % 8 == 0, "rows are taken eight at a time");
+    static_assert(NB % NSCAN == 0, "a scan warp sees every use of its buffers");
+    static_assert(S >= 2 && S - 1 <= R, "tiles in flight stay within the next chunk");
+    static_assert(SR == 2 || SR == 3, "a replay tile is prefetched one window ahead");
+};
+
+constexpr int kStreamSlots = 8;  // step ring of the ticket warp
+constexpr int kStreamAhead = 2;  // ticket k is fetched once the summaries of chunk k - 2 have started
+
+// Shared-memory layout, host and device.  Summary warp w owns stages
+// w*S .. w*S+S-1 of the summary ring (two planes each), replay warp w owns
+// stages w*SR .. w*SR+SR-1 of the replay ring (NIN planes each; the outputs
+// overwrite their inputs there and leave by bulk tensor stores).
+struct StreamGeom {
+    int tile_bytes;    // one plane of one window: W * DT * elem
+    int sstage_bytes;  // summary stage: forward a, b; backward a, grad_out
+    int rstage_bytes;  // replay stage: forward a, b; backward a, out, grad_out
+    int rring_off;     // replay ring after the summary ring
+    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_free[slots], maps[NB], entries[NB], buf_free[NB]
+    int ticket_off;    // step tickets [slots]
+    int tick_off;      // chunk tickets per buffer [NB] (-1: end mark)
+    int map_off;       // window maps [NB][NWIN][DT] float2
+    int cmap_off;      // chunk maps [NB][DT] float2
+    int entry_off;     // window entering states [NB][NWIN][DT] float
+    int count_off;     // summary warps done per buffer [NB]
+    int flag_off;      // abort flag
+    int smem_bytes;
+};
+
+template <class C, bool BWD>
+__host__ __device__ inline StreamGeom make_stream_geom() {
+    StreamGeom g{};
+    g.tile_bytes = C::W * C::DT * static_cast<int>(sizeof(typename C::St));
+    g.sstage_bytes = 2 * g.tile_bytes;
+    g.rstage_bytes = (BWD ? 3 : 2) * g.tile_bytes;
+    g.rring_off = C::NW * C::S * g.sstage_bytes;
+    g.bar_off = g.rring_off + C::NW * C::SR * g.rstage_bytes;
+    const int nbar = C::NW * C::S + C::NW * C::SR + 2 * kStreamSlots + 3 * C::NB;
+    g.ticket_off = g.bar_off + nbar * 8;
+    g.tick_off = g.ticket_off + kStreamSlots * 4;
+    g.map_off = (g.tick_off + C::NB * 4 + 15) / 16 * 16;
+    g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8;
+    g.entry_off = g.cmap_off + C::NB * C::DT * 8;
+    g.count_off = g.entry_off + C::NB * C::NWIN * C::DT * 4;
+    g.flag_off = g.count_off + C::NB * 4;
+    g.smem_bytes = g.flag_off + 16;
+    return g;
+}
+
+// Forward tiles: a, b (row t); output out (tm_o0), staged over b.  Backward
+// tiles: a one row late (a_{t+1}), out one row early (h_{t-1}), grad_out;
+// outputs grad_a (tm_o0, staged over h_{t-1}) and grad_b (tm_o1, staged over
+// grad_out).
 template <class C, bool BWD>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUtensorMap tm_1,
-              const __grid_constant__ CUtensorMap tm_2, typename C::St *__restrict__ out0,
-              typename C::St *__restrict__ out1, float *__restrict__ last, int T, int D, int nstage,
-              DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
+                    const __grid_constant__ CUtensorMap tm_2, const __grid_constant__ CUtensorMap tm_o0,
+                    const __grid_constant__ CUtensorMap tm_o1, float *__restrict__ last, int T, int D,
+                    DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
     using St = typename C::St;
-    constexpr int DT = C::DT, V = C::V, W = C::W, NWC = C::NWC;
+    constexpr int DT = C::DT, V = C::V, W = C::W, NW = C::NW, R = C::R, S = C::S, SR = C::SR, NSCAN = C::NSCAN;
+    constexpr int NB = C::NB;
+    constexpr int NWIN = C::NWIN;
     constexpr int NIN = BWD ? 3 : 2;
-    constexpr int LAG = kStreamLag, NB = kStreamBufs, SLOTS = kStreamStepSlots;
-    constexpr int AHEAD = 3;  // the ticket warp fetches ticket k after the window warps finish step k - AHEAD
-    static_assert(SLOTS % kStreamScanWarps == 0, "a scan warp sees every use of its step slots");
-    static_assert(SLOTS >= AHEAD + 2 * LAG + 1, "a step slot is rewritten only after every reader is done");
+    constexpr int SLOTS = kStreamSlots;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const StreamGeom geo = make_stream_geom<C, NIN>(nstage);
-    auto tile = [&](int stage, int plane) {
-        return reinterpret_cast<St *>(smem_raw + stage * geo.stage_bytes + plane * geo.tile_bytes);
+    const StreamGeom geo = make_stream_geom<C, BWD>();
+    auto stile = [&](int st, int plane) {  // summary ring: plane 0 = a, 1 = b / grad_out
+        return reinterpret_cast<St *>(smem_raw + st * geo.sstage_bytes + plane * geo.tile_bytes);
+    };
+    auto rtile = [&](int st, int plane) {  // replay ring: planes in tensor-map order
+        return reinterpret_cast<St *>(smem_raw + geo.rring_off + st * geo.rstage_bytes + plane * geo.tile_bytes);
     };
     auto bar = [&](int i) { return smem_addr(smem_raw + geo.bar_off + 8 * i); };
-    auto full_bar = [&](int s) { return bar(s); };
-    auto free_bar = [&](int q) { return bar(nstage + q); };  // window warps done with step slot q's step
-    auto step_bar = [&](int q) { return bar(2 * nstage + q); };
-    auto maps_bar = [&](int b) { return bar(2 * nstage + SLOTS + b); };
-    auto entries_bar = [&](int b) { return bar(2 * nstage + SLOTS + NB + b); };
+    constexpr int BS = NW * S;  // summary-ring barriers first
+    auto sfull = [&](int st) { return bar(st); };
+    auto rfull = [&](int st) { return bar(BS + st); };
+    constexpr int BR = BS + NW * SR;  // then the replay ring's
+    auto step_full = [&](int q) { return bar(BR + q); };
+    auto step_free = [&](int q) { return bar(BR + SLOTS + q); };
+    auto maps_bar = [&](int b) { return bar(BR + 2 * SLOTS + b); };
+    auto entries_bar = [&](int b) { return bar(BR + 2 * SLOTS + NB + b); };
+    auto buf_free = [&](int b) { return bar(BR + 2 * SLOTS + 2 * NB + b); };
     int *step_ticket = reinterpret_cast<int *>(smem_raw + geo.ticket_off);
-    float2 *wmap = reinterpret_cast<float2 *>(smem_raw + geo.map_off);    // [NB][NWC][DT]
-    float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off);  // [NB][NWC][DT]
-    float2 *cmap = reinterpret_cast<float2 *>(smem_raw + geo.cmap_off);   // [NB][DT]
-    unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);  // [NB]
+    volatile int *tick_of = reinterpret_cast<volatile int *>(smem_raw + geo.tick_off);
+    float2 *wmap = reinterpret_cast<float2 *>(smem_raw + geo.map_off);
+    float2 *cmap = reinterpret_cast<float2 *>(smem_raw + geo.cmap_off);
+    float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off);
+    unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < nstage; ++s) mbar_init(full_bar(s), 1);
+        for (int st = 0; st < BS; ++st) mbar_init(sfull(st), 1);
+        for (int st = 0; st < NW * SR; ++st) mbar_init(rfull(st), 1);
         for (int q = 0; q < SLOTS; ++q) {
-            mbar_init(free_bar(q), NWC);
-            mbar_init(step_bar(q), 1);
+            mbar_init(step_full(q), 1);
+            mbar_init(step_free(q), NW);
         }
         for (int b = 0; b < NB; ++b) {
-            mbar_init(maps_bar(b), 1);  // the last window warp, once the chunk's map is out
+            mbar_init(maps_bar(b), 1);  // the last summary warp (or the end mark)
             mbar_init(entries_bar(b), 1);
+            mbar_init(buf_free(b), NW);
             wcount[b] = 0;
         }
         *abort_flag = 0;
@@ -286,62 +354,209 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
     const WaitCtx wc{status, abort_flag, timeout_ns};
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    const int CH = NWC * W;
+    const int CH = NWIN * W;
     const long long total = static_cast<long long>(sa.ng) * sa.nc;
-    // step tickets of the last LAG + 1 steps, newest at hist[0]
-    auto push = [](int (&hist)[LAG + 1], int tk) {
-#pragma unroll
-        for (int i = LAG; i > 0; --i) hist[i] = hist[i - 1];
-        hist[0] = tk;
+    const CUtensorMap *const maps[3] = {&tm_0, &tm_1, &tm_2};
+    // chunk coordinates of ticket t
+    struct Chunk {
+        int cc, gi, c, brow, x0;
     };
-    auto pending = [](const int (&hist)[LAG + 1]) {  // a replay is still to come
-        bool any = false;
-#pragma unroll
-        for (int i = 0; i < LAG; ++i) any = any || hist[i] >= 0;
-        return any;
+    auto decode = [&](int t) {
+        Chunk ch;
+        ch.cc = t / sa.ng;
+        ch.gi = t - ch.cc * sa.ng;
+        ch.c = BWD ? sa.nc - 1 - ch.cc : ch.cc;
+        ch.brow = ch.gi / sa.ndt;
+        ch.x0 = (ch.gi - ch.brow * sa.ndt) * DT;
+        return ch;
+    };
+    // bounded wait, blind to the abort flag, for a copy this warp issued
+    auto drain_one = [&](uint32_t fb, uint32_t par) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(fb, par)) {
+            if (global_timer_ns() - t0 > wc.timeout_ns) {
+                record_error(wc, kErrTimeout, kSiteDrain);
+                break;
+            }
+        }
     };
 
-    if (warp == NWC + kStreamScanWarps) {
-        // --------------------------------------------------------- ticket warp
-        // publishes tickets until every scan warp has seen an invalid one
+    if (warp == 2 * NW + NSCAN) {
+        // ------------------------------------------------------------ tickets
         if (lane == 0) {
-            int invalid = 0;
-            for (int j = 0; invalid < kStreamScanWarps; ++j) {
-                if (j >= AHEAD) {
-                    const int jf = j - AHEAD;
-                    if (!mbar_wait(free_bar(jf % SLOTS), static_cast<uint32_t>((jf / SLOTS) & 1), wc,
+            for (int j = 0;; ++j) {
+                if (j >= kStreamAhead) {
+                    const int jf = j - kStreamAhead;
+                    if (!mbar_wait(step_free(jf % SLOTS), static_cast<uint32_t>((jf / SLOTS) & 1), wc,
                                    kSiteProducerEmpty))
                         return;
                 }
-                int tk = -1;
-                if (invalid == 0) {
-                    const long long tj = static_cast<long long>(atomicAdd(sa.ticket, 1u));
-                    tk = tj < total ? static_cast<int>(tj) : -1;
-                }
-                if (tk < 0) ++invalid;
+                const long long tj = static_cast<long long>(atomicAdd(sa.ticket, 1u));
+                const int tk = tj < total ? static_cast<int>(tj) : -1;
                 step_ticket[j % SLOTS] = tk;
-                mbar_arrive(step_bar(j % SLOTS));
+                mbar_arrive(step_full(j % SLOTS));
+                if (tk < 0) return;
             }
         }
         return;
     }
 
-    if (warp >= NWC) {
-        // ---------------------------------------------------------- scan warps
-        // scan warp j handles the chunks of steps j, j + 2, j + 4, ...; once a
-        // ticket is invalid every later one is too
-        const int i0 = lane * V;  // first of this thread's lanes in the tile
-        for (int k = warp - NWC;; k += kStreamScanWarps) {
-            const int q = k % SLOTS;
-            if (!warp_wait(step_bar(q), static_cast<uint32_t>((k / SLOTS) & 1), wc, kSiteStreamStep)) return;
-            const int tk = step_ticket[q];
-            if (tk < 0) return;
-            const int cc = tk / sa.ng;
-            const int gi = tk - cc * sa.ng;
-            const size_t g0 = static_cast<size_t>(gi) * sa.nc;
+    if (warp < NW) {
+        // ------------------------------------------------------ summary warps
+        const int w = warp;
+        int u_iss = 0, u_done = 0;  // tiles issued / reduced, counted over this warp's chunks (R per chunk)
+        auto sissue = [&](int u, int t) {  // lane 0: tile u (window (u % R) * NW + w of ticket t)
+            const Chunk ch = decode(t);
+            const int st = w * S + u % S;
+            const uint32_t fb = sfull(st);
+            mbar_arrive_expect_tx(fb, 2 * geo.tile_bytes);
+            const int y = ch.c * CH + ((u % R) * NW + w) * W;
+            const uint64_t keep = l2_evict_last_policy();
+            tma_load_3d_hint(smem_addr(stile(st, 0)), maps[0], ch.x0, y + (BWD ? 1 : 0), ch.brow, fb, keep);
+            tma_load_3d_hint(smem_addr(stile(st, 1)), maps[BWD ? 2 : 1], ch.x0, y, ch.brow, fb, keep);
+        };
+        auto drain = [&]() {
+            if (lane != 0) return;
+            for (int u = u_done; u < u_iss; ++u) drain_one(sfull(w * S + u % S), static_cast<uint32_t>((u / S) & 1));
+        };
+        if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
+        int tk = step_ticket[0];
+        for (int k = 0;; ++k) {
+            const int b = k % NB;
+            if (tk < 0) {
+                // no more chunks: summary warp 0 marks the end in the next NSCAN
+                // buffers (each once the replays of its previous chunk are done),
+                // so that every scan warp and the replay warps see it
+                if (w == 0) {
+                    for (int i = 0; i < NSCAN; ++i) {
+                        const int ke = k + i, be = ke % NB;
+                        if (ke >= NB && !warp_wait(buf_free(be), static_cast<uint32_t>(((ke / NB) - 1) & 1), wc,
+                                                   kSiteStreamStep)) {
+                            drain();
+                            return;
+                        }
+                        if (lane == 0) {
+                            tick_of[be] = -1;
+                            mbar_arrive(maps_bar(be));
+                        }
+                        __syncwarp();
+                    }
+                }
+                drain();
+                return;
+            }
+            // the next ticket (its first tiles go out while this chunk is reduced)
+            const int q1 = (k + 1) % SLOTS;
+            if (!warp_wait(step_full(q1), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc, kSiteStreamStep)) {
+                drain();
+                return;
+            }
+            const int tn = step_ticket[q1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(step_free(k % SLOTS));
+            const Chunk ch = decode(tk);
+            float P[R][V], Q[R][V];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int u = k * R + r;
+                // keep S - 1 tiles in flight ahead of this one (chunks k and k + 1)
+                while (u_iss <= u + S - 1) {
+                    const int t = u_iss / R == k ? tk : tn;
+                    if (t < 0) break;
+                    if (lane == 0) sissue(u_iss, t);
+                    ++u_iss;
+                }
+                const int wbase = ch.c * CH + (r * NW + w) * W;
+                const int nrows = min(max(T - wbase, 0), W);
+                const int st = w * S + u % S;
+                if (!warp_wait(sfull(st), static_cast<uint32_t>((u / S) & 1), wc, kSiteConsumerFull)) {
+                    drain();
+                    return;
+                }
+                const St *ta = stile(st, 0);
+                const St *tb = stile(st, 1);
+                // the window's map (rows past T are identity steps)
+#pragma unroll
+                for (int v = 0; v < V; ++v) { P[r][v] = 1.0f; Q[r][v] = 0.0f; }
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
+                    float xa[8][V], xb[8][V];
+                    load8<St, V, DT>(ta, r0, lane, xa);
+                    load8<St, V, DT>(tb, r0, lane, xb);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int row = BWD ? 7 - rr : rr;
+                        if (r0 + row < nrows) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                P[r][v] = __fmul_rn(xa[row][v], P[r][v]);
+                                Q[r][v] = __fmaf_rn(xa[row][v], Q[r][v], xb[row][v]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();  // every lane done with the stage before it is refilled
+                ++u_done;
+            }
+            // buffer b is free once the replays of chunk k - NB are done
+            if (k >= NB && !warp_wait(buf_free(b), static_cast<uint32_t>(((k / NB) - 1) & 1), wc, kSiteStreamStep)) {
+                drain();
+                return;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 *mp = wmap + (b * NWIN + r * NW + w) * DT + lane * V;
+#pragma unroll
+                for (int v = 0; v < V; ++v) mp[v] = make_float2(P[r][v], Q[r][v]);
+            }
+            __syncwarp();
+            unsigned int before = 0;
+            if (lane == 0) before = atom_add_acq_rel_cta(wcount + b, 1u);
+            before = __shfl_sync(0xffffffffu, before, 0);
+            if (before == NW - 1) {
+                // the last summary warp of this chunk: compose the window maps in
+                // chain order and publish the chunk's map at once
+                __syncwarp();
+                const float2 *cm = wmap + b * NWIN * DT;
+                float Pc[V], Qc[V];
+#pragma unroll
+                for (int v = 0; v < V; ++v) { Pc[v] = 1.0f; Qc[v] = 0.0f; }
+                for (int jw = 0; jw < NWIN; ++jw) {
+                    const int ww = BWD ? NWIN - 1 - jw : jw;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const float2 m = cm[ww * DT + lane * V + v];
+                        Qc[v] = __fmaf_rn(m.x, Qc[v], m.y);
+                        Pc[v] = __fmul_rn(m.x, Pc[v]);
+                    }
+                }
+                const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    cmap[b * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
+                    publish_map(sa.agg + slot_g * DT + lane * V + v, Pc[v], Qc[v]);
+                }
+                __syncwarp();  // every lane's cmap entries written before the maps_ready arrive
+                if (lane == 0) {
+                    tick_of[b] = tk;
+                    wcount[b] = 0;  // next used NB chunks on, after this buffer's replays
+                    mbar_arrive(maps_bar(b));
+                }
+            }
+            tk = tn;
+        }
+    }
+
+    if (warp >= 2 * NW) {
+        // --------------------------------------------------------- scan warps
+        // scan warp j takes chunks j, j + NSCAN, ... until an end mark
+        const int i0 = lane * V;
+        for (int k = warp - 2 * NW;; k += NSCAN) {
             const int b = k % NB;
             if (!warp_wait(maps_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) return;
-            const float2 *mp = wmap + b * NWC * DT;
+            const int t = tick_of[b];
+            if (t < 0) return;
+            const Chunk ch = decode(t);
             float Pc[V], Qc[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) {
@@ -349,23 +564,20 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                 Pc[v] = m.x;
                 Qc[v] = m.y;
             }
-            const size_t slot = g0 + cc;
             float h[V];
-            // batches of maps in flight: as many as the registers hold
-            constexpr int BATCH = C::MINB > 1 ? 16 / V : 32 / V;
-            if (!stream_lookback<DT, V, BATCH>(sa, gi, cc, i0, h, wc)) return;
+            if (!stream_lookback<DT, V, 16 / V>(sa, ch.gi, ch.cc, i0, h, wc)) return;
+            const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
 #pragma unroll
-            for (int v = 0; v < V; ++v) sa.incl[slot * DT + i0 + v] = __fmaf_rn(Pc[v], h[v], Qc[v]);
-            __syncwarp();  // every lane's state written before lane 0's release
-            if (lane == 0) st_release_gpu(sa.flag + slot, kChunkIncl);
+            for (int v = 0; v < V; ++v) publish_state(sa.incl + slot_g * DT + i0 + v, __fmaf_rn(Pc[v], h[v], Qc[v]));
             // the state entering every window, in chain order
-            float *ep = wentry + b * NWC * DT;
-            for (int j = 0; j < NWC; ++j) {
-                const int w = BWD ? NWC - 1 - j : j;
+            const float2 *mp = wmap + b * NWIN * DT;
+            float *ep = wentry + b * NWIN * DT;
+            for (int jw = 0; jw < NWIN; ++jw) {
+                const int ww = BWD ? NWIN - 1 - jw : jw;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    ep[w * DT + i0 + v] = h[v];
-                    const float2 m = mp[w * DT + i0 + v];
+                    ep[ww * DT + i0 + v] = h[v];
+                    const float2 m = mp[ww * DT + i0 + v];
                     h[v] = __fmaf_rn(m.x, h[v], m.y);
                 }
             }
@@ -374,204 +586,116 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
         }
     }
 
-    // --------------------------------------------------------- window warps
-    const int w = warp;  // window of every chunk this warp owns
-    const int sA = w, sB = NWC + w;  // summary and replay stages
-    const CUtensorMap *const maps[3] = {&tm_0, &tm_1, &tm_2};
-    if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < NIN; ++i) prefetch_tensormap(maps[i]);
-    }
-    // bulk copies of window w of ticket t into stage st (lane 0)
-    auto issue = [&](int st, int t, bool replay) {
-        const int cc = t / sa.ng;
-        const int gi = t - cc * sa.ng;
-        const int c = BWD ? sa.nc - 1 - cc : cc;
-        const int brow = gi / sa.ndt;
-        const int x0 = (gi - brow * sa.ndt) * DT;
-        const bool skip_out = BWD && !replay;  // the backward summary needs a and grad_out only
-        const uint32_t fb = full_bar(st);
-        mbar_arrive_expect_tx(fb, (skip_out ? NIN - 1 : NIN) * geo.tile_bytes);
-        const int y = c * CH + w * W;
+    // ------------------------------------------------------------ replay warps
+    const int w = warp - NW;
+    const uint64_t drop = l2_evict_first_policy();  // replay tiles and outputs: not read again here
+    int u_iss = 0, u_done = 0;  // tiles issued / replayed, counted over this warp's chunks (R per chunk)
+    auto rissue = [&](int u, int t) {  // lane 0: tile u (window (u % R) * NW + w of ticket t)
+        // the stage last held tile u - SR, whose outputs were committed SR - 2
+        // bulk groups before the newest: wait until they have left it
+        bulk_wait_read<SR - 2>();
+        const Chunk ch = decode(t);
+        const int st = w * SR + u % SR;
+        const uint32_t fb = rfull(st);
+        mbar_arrive_expect_tx(fb, NIN * geo.tile_bytes);
+        const int y = ch.c * CH + ((u % R) * NW + w) * W;
 #pragma unroll
         for (int i = 0; i < NIN; ++i) {
-            if (skip_out && i == 1) continue;
             const int dy = BWD ? (i == 0 ? 1 : (i == 1 ? -1 : 0)) : 0;
-            tma_load_3d(smem_addr(tile(st, i)), maps[i], x0, y + dy, brow, fb);
+            tma_load_3d_hint(smem_addr(rtile(st, i)), maps[i], ch.x0, y + dy, ch.brow, fb, drop);
         }
     };
-    int uA = 0, uB = 0;  // copies waited on per stage (phase parity)
-    int iA = 0, iB = 0;  // copies issued per stage
-    // before leaving early: every copy this warp issued has landed (bounded,
-    // blind to the abort flag: copies in flight always land)
     auto drain = [&]() {
         if (lane != 0) return;
-        const int st[2] = {sA, sB};
-        const int issued[2] = {iA, iB};
-        const int waited[2] = {uA, uB};
-        for (int i = 0; i < 2; ++i) {
-            if (issued[i] == waited[i]) continue;
-            const uint32_t fb = full_bar(st[i]);
-            const uint32_t par = static_cast<uint32_t>(waited[i] & 1);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(fb, par)) {
-                if (global_timer_ns() - t0 > wc.timeout_ns) {
-                    record_error(wc, kErrTimeout, kSiteDrain);
-                    break;
-                }
-            }
-        }
+        for (int u = u_done; u < u_iss; ++u) drain_one(rfull(w * SR + u % SR), static_cast<uint32_t>((u / SR) & 1));
+        bulk_wait<0>();  // the outputs in flight have left shared memory and landed
     };
-    int hist[LAG + 1];
-#pragma unroll
-    for (int i = 0; i <= LAG; ++i) hist[i] = -1;
-    if (!warp_wait(step_bar(0), 0u, wc, kSiteStreamStep)) return;
-    int tk = step_ticket[0];
-    if (tk >= 0) {
-        if (lane == 0) issue(sA, tk, false);
-        ++iA;
-    }
     for (int k = 0;; ++k) {
-        push(hist, tk);
-        // ------------------------------------------------ summary of ticket k
-        if (tk >= 0) {
-            const int t = tk;
-            const int cc = t / sa.ng;
-            const int gi = t - cc * sa.ng;
-            const int c = BWD ? sa.nc - 1 - cc : cc;
-            const int wbase = c * CH + w * W;
-            const int nrows = min(max(T - wbase, 0), W);
-            if (!warp_wait(full_bar(sA), static_cast<uint32_t>(uA & 1), wc, kSiteConsumerFull)) { drain(); return; }
-            ++uA;
-            const St *ta = tile(sA, 0);
-            const St *tb = tile(sA, NIN - 1);
-            const int b = k % NB;
-            // the window's map (rows past T are identity steps)
-            float P[V], Q[V];
-#pragma unroll
-            for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
-            for (int g8 = 0; g8 < nrows; g8 += 8) {
-                const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
-                float xa[8][V], xb[8][V];
-                load8<St, V, DT>(ta, r0, lane, xa);
-                load8<St, V, DT>(tb, r0, lane, xb);
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int r = BWD ? 7 - rr : rr;
-                    if (r0 + r < nrows) {
-#pragma unroll
-                        for (int v = 0; v < V; ++v) {
-                            P[v] = __fmul_rn(xa[r][v], P[v]);
-                            Q[v] = __fmaf_rn(xa[r][v], Q[v], xb[r][v]);
+        const int b = k % NB;
+        if (!warp_wait(maps_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) {
+            drain();
+            return;
+        }
+        const int t = tick_of[b];
+        if (t < 0) {
+            drain();
+            return;
+        }
+        const Chunk ch = decode(t);
+        const int d = ch.x0 + lane * V;
+        for (int r = 0; r < R; ++r) {
+            const int u = k * R + r;
+            if (u_iss == u) {  // not prefetched
+                if (lane == 0) rissue(u, t);
+                ++u_iss;
+            }
+            // the next tile into the next stage; past this chunk only if the
+            // next chunk's map is already out
+            if (u_iss == u + 1) {
+                if (r + 1 < R) {
+                    if (lane == 0) rissue(u + 1, t);
+                    ++u_iss;
+                } else {
+                    int did = 0;
+                    if (lane == 0) {
+                        const int b1 = (k + 1) % NB;
+                        if (mbar_test_wait(maps_bar(b1), static_cast<uint32_t>(((k + 1) / NB) & 1))) {
+                            const int t1 = tick_of[b1];
+                            if (t1 >= 0) {
+                                rissue(u + 1, t1);
+                                did = 1;
+                            }
                         }
                     }
+                    u_iss += __shfl_sync(0xffffffffu, did, 0);
                 }
             }
-            float2 *mp = wmap + b * NWC * DT + w * DT + lane * V;
-#pragma unroll
-            for (int v = 0; v < V; ++v) mp[v] = make_float2(P[v], Q[v]);
-            __syncwarp();
-            unsigned int before = 0;
-            if (lane == 0) before = atom_add_acq_rel_cta(wcount + b, 1u);
-            before = __shfl_sync(0xffffffffu, before, 0);
-            if (before == NWC - 1) {
-                // the last window warp of this chunk: compose the window maps
-                // in chain order and publish the chunk's map at once, so that
-                // look-backs elsewhere find it without waiting for this CTA's
-                // scan warps
-                __syncwarp();
-                const float2 *cm = wmap + b * NWC * DT;
-                float Pc[V], Qc[V];
-#pragma unroll
-                for (int v = 0; v < V; ++v) { Pc[v] = 1.0f; Qc[v] = 0.0f; }
-                for (int j = 0; j < NWC; ++j) {
-                    const int ww = BWD ? NWC - 1 - j : j;
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        const float2 m = cm[ww * DT + lane * V + v];
-                        Qc[v] = __fmaf_rn(m.x, Qc[v], m.y);
-                        Pc[v] = __fmul_rn(m.x, Pc[v]);
-                    }
-                }
-                const size_t slot = static_cast<size_t>(gi) * sa.nc + cc;
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    cmap[b * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
-                    sa.agg[slot * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
-                }
-                __syncwarp();  // every lane's map written before lane 0's release
-                if (lane == 0) {
-                    st_release_gpu(sa.flag + slot, kChunkAgg);
-                    wcount[b] = 0;  // next used NB steps on, after the scan warp has taken this chunk
-                    mbar_arrive(maps_bar(b));
-                }
-            }
-        }
-        // ------------------- next ticket; its summary tile into the free stage
-        int tn = -1;
-        if (tk >= 0) {
-            const int q = (k + 1) % SLOTS;
-            if (!warp_wait(step_bar(q), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc, kSiteStreamStep)) {
+            if (r == 0 && !warp_wait(entries_bar(b), static_cast<uint32_t>((k / NB) & 1), wc, kSiteStreamStep)) {
                 drain();
                 return;
             }
-            tn = step_ticket[q];
-            __syncwarp();  // the stage's tile read by every lane before it is overwritten
-            if (tn >= 0) {
-                if (lane == 0) issue(sA, tn, false);
-                ++iA;
+            const int st = w * SR + u % SR;
+            if (!warp_wait(rfull(st), static_cast<uint32_t>((u / SR) & 1), wc, kSiteConsumerFull)) {
+                drain();
+                return;
             }
-        }
-        // ------------------------------------------- replay of ticket k - LAG
-        if (hist[LAG] >= 0) {
-            const int t = hist[LAG];
-            const int kc = k - LAG;  // the step whose chunk this is
-            const int cc = t / sa.ng;
-            const int gi = t - cc * sa.ng;
-            const int c = BWD ? sa.nc - 1 - cc : cc;
-            const int brow = gi / sa.ndt;
-            const int x0 = (gi - brow * sa.ndt) * DT;
-            const int d = x0 + lane * V;
-            const bool lane_ok = d < D;
-            const int wbase = c * CH + w * W;
+            const int wi = r * NW + w;
+            const int wbase = ch.c * CH + wi * W;
             const int nrows = min(max(T - wbase, 0), W);
-            const int b = kc % NB;
-            if (!warp_wait(full_bar(sB), static_cast<uint32_t>(uB & 1), wc, kSiteConsumerFull)) { drain(); return; }
-            ++uB;
-            if (!warp_wait(entries_bar(b), static_cast<uint32_t>((kc / NB) & 1), wc, kSiteStreamStep)) {
-                drain();
-                return;
-            }
-            const St *ta = tile(sB, 0);
-            const St *tb = tile(sB, NIN - 1);
+            St *ta = rtile(st, 0);
+            St *tb = rtile(st, NIN - 1);
             float h[V];
-            const float *ep = wentry + b * NWC * DT + w * DT + lane * V;
+            const float *ep = wentry + (b * NWIN + wi) * DT + lane * V;
 #pragma unroll
             for (int v = 0; v < V; ++v) h[v] = ep[v];
-            const size_t rowb = static_cast<size_t>(brow) * T;
             if constexpr (!BWD) {
-                St *op = out0 + (rowb + wbase) * D + d;
+                // out_t over b_t in the tile (each lane rewrites what it read)
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     float xa[8][V], xb[8][V];
                     load8<St, V, DT>(ta, g8, lane, xa);
                     load8<St, V, DT>(tb, g8, lane, xb);
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        if (g8 + r < nrows) {
+                    for (int rr = 0; rr < 8; ++rr) {
+                        if (g8 + rr < nrows) {
 #pragma unroll
-                            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[r][v], h[v], xb[r][v]);
-                            if (lane_ok) store_lanes<St, V>(op + static_cast<size_t>(g8 + r) * D, h);
+                            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[rr][v], h[v], xb[rr][v]);
+                            store_lanes<St, V>(tb + (g8 + rr) * DT + lane * V, h);
                         }
                     }
                 }
-                if (last != nullptr && lane_ok && nrows > 0 && wbase + nrows == T) {
+                if (last != nullptr && d < D && nrows > 0 && wbase + nrows == T) {
 #pragma unroll
-                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(ch.brow) * D + d + v] = h[v];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d_hint(&tm_o0, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
+                    bulk_commit();
                 }
             } else {
-                const St *th = tile(sB, 1);
-                St *gap = out0 + (rowb + wbase) * D + d;
-                St *gbp = out1 + (rowb + wbase) * D + d;
+                // grad_b_t over grad_out_t, grad_a_t over h_{t-1}
+                St *th = rtile(st, 1);
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     const int r0 = (nrows - 1 - g8) & ~7;
                     float xa[8][V], xh[8][V], xg[8][V];
@@ -580,33 +704,31 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                     load8<St, V, DT>(tb, r0, lane, xg);
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
-                        const int r = 7 - rr;
-                        if (r0 + r < nrows) {
+                        const int row = 7 - rr;
+                        if (r0 + row < nrows) {
                             float gav[V];
 #pragma unroll
                             for (int v = 0; v < V; ++v) {
-                                h[v] = __fmaf_rn(xa[r][v], h[v], xg[r][v]);
-                                gav[v] = __fmul_rn(h[v], xh[r][v]);
+                                h[v] = __fmaf_rn(xa[row][v], h[v], xg[row][v]);
+                                gav[v] = __fmul_rn(h[v], xh[row][v]);
                             }
-                            if (lane_ok) {
-                                store_lanes<St, V>(gbp + static_cast<size_t>(r0 + r) * D, h);
-                                store_lanes<St, V>(gap + static_cast<size_t>(r0 + r) * D, gav);
-                            }
+                            store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, h);
+                            store_lanes<St, V>(th + (r0 + row) * DT + lane * V, gav);
                         }
                     }
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d_hint(&tm_o0, smem_addr(th), ch.x0, wbase, ch.brow, drop);
+                    tma_store_3d_hint(&tm_o1, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
+                    bulk_commit();
+                }
             }
-            __syncwarp();  // the stage's tile read by every lane before it is overwritten
+            __syncwarp();  // every lane done with the stage before it is refilled
+            ++u_done;
         }
-        // ------------------------- the next replay's tile into the free stage
-        if (hist[LAG - 1] >= 0) {
-            if (lane == 0) issue(sB, hist[LAG - 1], true);
-            ++iB;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(free_bar(k % SLOTS));
-        if (tk < 0 && !pending(hist)) return;
-        tk = tn;
+        if (lane == 0) mbar_arrive(buf_free(b));  // the buffer's entering states are read
     }
 }
 

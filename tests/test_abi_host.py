@@ -152,27 +152,32 @@ def test_exact_flag_of_every_tile_variant(lib):
         assert L.lrscan_plan_gated(4, 512, 1024, dt, "fwd", path="plain")["exact"] == 0
 
 
-def test_occupancy_rule_few_lanes_long_sequence_takes_chunks(lib):
-    # 2^20 steps and only 64 fp32 lanes: the forward takes the grouped prefix
-    # (5 kernels) with 512-step chunks (2,048 chunks per lane); the backward
-    # streams the chunks in one pass (with state it keeps the chunked path:
-    # 128-step chunks)
-    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd")
-    assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].endswith("_grouped"), p
-    assert p["rows_per_window"] == 512 and p["name"].startswith("chunk512")
+def test_occupancy_rule_few_lanes_long_sequence(lib):
+    # 2^20 steps and only 64 fp32 lanes: both directions stream the chunks in
+    # one pass (1,024 chunks of 512 steps per lane group); with state they keep
+    # the chunked path's grouped prefix (512-step chunks forward, 128 backward)
+    for direction in ("fwd", "bwd"):
+        p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction)
+        assert p["path"] == "stream" and p["name"] == "stream_f32_d32" and p["kernels"] == 1, p
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", state=True)
+    assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].startswith("chunk512"), p
+    assert p["name"].endswith("_grouped") and p["rows_per_window"] == 512
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
-    assert L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd")["name"] == "stream_f32_d32"
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", state=True)
     assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
-    # bf16, or 256 fp32 lanes and more: both directions streamed, on 64-lane tiles
-    for (B, D, dt) in ((1, 64, "bf16"), (8, 64, "f32"), (1, 256, "bf16")):
+    # fp32 on 32-lane tiles; bf16 on 32-lane tiles, but 64-lane tiles for a
+    # backward on at most 128 lanes
+    for (B, D, dt) in ((1, 64, "bf16"), (8, 64, "f32"), (1, 256, "bf16"), (8, 64, "bf16")):
         for direction in ("fwd", "bwd"):
             p = L.lrscan_plan(B, 1 << 18, D, dt, direction)
-            assert p["path"] == "stream" and p["lanes_per_cta"] == 64, p
-    # too short for 64 stream chunks per lane group: chunked
+            lanes = 64 if (dt == "bf16" and direction == "bwd" and B * D <= 128) else 32
+            assert p["path"] == "stream" and p["lanes_per_cta"] == lanes, (B, D, dt, direction, p)
+    # 32 chunks of 512 steps per lane group stream; fewer take the chunked path
+    assert L.lrscan_plan(1, 16384, 64, "bf16", "fwd")["path"] == "stream"
     assert L.lrscan_plan(1, 8192, 64, "bf16", "fwd")["path"] == "chunk"
-    # too short for 2,048 chunks of 512: the forward falls back to 256
-    p = L.lrscan_plan(1, (1 << 19) + 1000, 64, "f32", "fwd")
+    # the chunked path's grouped prefix: too short for 2,048 chunks of 512, the
+    # forward falls back to 256
+    p = L.lrscan_plan(1, (1 << 19) + 1000, 64, "f32", "fwd", path="chunk")
     assert p["rows_per_window"] == 256 and p["name"].endswith("_grouped"), p
     # an explicit chunk length is kept
     p64 = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", chunk_len=64)
@@ -313,45 +318,36 @@ def test_complex_chunked_plans(lib):
 
 
 def test_stream_plans(lib):
-    """The persistent chunk-streaming path: eight window warps per chunk (256
-    steps of 32-row windows; 128 steps for 64-lane fp32 tiles), or, split
-    into summary and replay warps, 128-step chunks; at most the resident CTAs
-    of the GPU and no more than keep the chunks in flight inside L2, its
-    publication workspace (ticket, one flag per chunk, a map and a state per
-    chunk and lane), and refusals where it cannot run."""
+    """The persistent chunk-streaming path: four summary, four replay, two scan
+    warps and a ticket warp per CTA, one CTA per SM (no more than there are
+    chunk tickets), 512-step chunks (bf16 forward on 32-lane tiles: 1024), its
+    publication workspace (ticket, a map and a state per chunk and lane), and
+    refusals where it cannot run."""
     pad = lambda x: (x + 255) // 256 * 256
-    # name: (rows per window, windows per chunk, threads, stages, CTAs per SM)
-    shapes = {"stream_f32_d32": (32, 8, 11 * 32, 16, 1), "stream_f32_d64": (16, 8, 11 * 32, 16, 1),
-              "stream_bf16_d32": (32, 8, 11 * 32, 16, 2), "stream_bf16_d64": (32, 8, 11 * 32, 16, 1),
-              "stream_split_f32_d32": (32, 16, 11 * 32, (24, 20), 1),
-              "stream_split_f32_d32_b": (32, 16, 11 * 32, (20, 20), 1),
-              "stream_split_bf16_d64": (32, 16, 11 * 32, (24, 20), 1)}
-    for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d64", "stream_split_f32_d32",
-                               "stream_split_f32_d32_b")),
-                      ("bf16", ("stream_bf16_d32", "stream_bf16_d64", "stream_split_bf16_d64"))):
-        es = 4 if dt == "f32" else 2
+    # name: {direction: (rows per window, windows per chunk, ring stages)}
+    shapes = {"stream_f32_d32": {"fwd": (32, 16, 20), "bwd": (32, 16, 20)},
+              "stream_bf16_d32": {"fwd": (64, 16, 24), "bwd": (64, 8, 20)},
+              "stream_bf16_d64": {"fwd": (32, 16, 24), "bwd": (32, 16, 20)}}
+    for dt, names in (("f32", ("stream_f32_d32",)), ("bf16", ("stream_bf16_d32", "stream_bf16_d64"))):
         assert L.lrscan_num_variants("stream", dt) == len(names)
         for v, name in enumerate(names, 1):
-            rows, nwin, threads, stages, per_sm = shapes[name]
             for direction in ("fwd", "bwd"):
+                rows, nwin, stages = shapes[name][direction]
                 B, T, D = 1, 1 << 22, 64
                 p = L.lrscan_plan(B, T, D, dt, direction, path="stream", tile_variant=v)
                 assert p["path"] == "stream" and p["name"] == name and p["exact"] == 0, p
                 assert p["rows_per_window"] == rows and p["subchunks"] == nwin and p["kernels"] == 1
-                nst = stages if isinstance(stages, int) else stages[direction == "bwd"]
-                assert p["threads_per_cta"] == threads and p["stages"] == nst
+                assert p["threads_per_cta"] == 11 * 32 and p["stages"] == stages
+                assert p["smem_bytes"] <= 227 * 1024
                 dtl = p["lanes_per_cta"]
-                chunk = nwin * rows
-                ng, nc = B * -(-D // dtl), -(-T // chunk)
-                assert p["workspace_bytes"] == 256 + pad(ng * nc * 4) + pad(ng * nc * dtl * 8) + pad(ng * nc * dtl * 4)
-                l2_ctas = max(152, (48 << 20) * 2 // (7 * chunk * dtl * es * 2))
-                resident = min(per_sm, 233472 // (p["smem_bytes"] + 1024))
-                assert p["ctas"] == min(ng * nc, resident * 152, l2_ctas), p
-    # a short sequence: no more CTAs than chunk tickets
-    assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 4
+                ng, nc = B * -(-D // dtl), -(-T // (nwin * rows))
+                assert p["workspace_bytes"] == 256 + pad(ng * nc * dtl * 8) + pad(ng * nc * dtl * 4)
+                assert p["ctas"] == min(ng * nc, 152), p
+    # a short sequence: no more CTAs than chunk tickets (2 rows x 2 lane tiles x 2 chunks)
+    assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 2
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
     with pytest.raises(L.LrscanError):
-        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=5)
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=2)

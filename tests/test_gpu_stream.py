@@ -10,7 +10,7 @@ import torch
 import oracle
 from linear_recurrence_scan_lrscan_gb300 import lrscan as L
 from linear_recurrence_scan_lrscan_gb300.workloads import random_inputs
-from parity_util import assert_close, assert_last_close, to_np
+from parity_util import assert_close, assert_last_close, bf16_bits_to_f32, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ def check(B, T, D, dt, variant, seed, a_lo=0.6):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("shape_i", range(len(SHAPES)))
 def test_stream_parity(dt, variant, shape_i):
     if variant > L.lrscan_num_variants("stream", dt):
@@ -78,7 +78,8 @@ def test_stream_parity(dt, variant, shape_i):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_stream_many_chunks_per_cta(dt):
-    """2,048 chunk tickets (two 32-lane groups x 1,024 chunks): several per CTA."""
+    """More chunk tickets than CTAs (two 32-lane groups x 512 chunks of 512
+    steps; bf16 forward: chunks of 1024): several per CTA."""
     B, T, D = 1, 1 << 18, 64
     plan = L.lrscan_plan(B, T, D, dt, "fwd", path="stream", tile_variant=1)
     chunk = plan["rows_per_window"] * plan["subchunks"]
@@ -95,9 +96,9 @@ def test_stream_refuses_state():
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_stream_in_cuda_graph(dt):
-    """Captured into a graph (the workspace's ticket and flags are cleared by a
-    captured memset each call), replayed twice with new inputs: each replay
-    against the oracle.  The captured backward reads its own static input
+    """Captured into a graph (the workspace's ticket is zeroed and its maps and
+    states refilled by captured memsets each call), replayed twice with new
+    inputs: each replay against the oracle.  The captured backward reads its own static input
     (filled with the oracle's forward output before each replay)."""
     B, T, D = 1, 20000, 64
     kw = dict(path="stream")
@@ -130,3 +131,31 @@ def test_stream_in_cuda_graph(dt):
         assert_last_close(last.cpu().numpy(), ref_last, f"last replay {seed}")
         assert_close(to_np(gb), ref_gb, dt, f"grad_b replay {seed}", reassociated=True)
         assert_close(to_np(ga), ref_ga, dt, f"grad_a replay {seed}", reassociated=True)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_stream_nan_inputs(dt):
+    """NaNs whose bits are all ones (the workspace's "nothing published" word)
+    in b, a and grad_out: the call ends without a timeout, the NaNs spread as
+    in the oracle (from their step on, along their lane), and every other
+    output agrees with it."""
+    B, T, D = 1, 20000, 64
+    inp = random_inputs(B, T, D, dt, seed=990, a_lo=0.8, a_hi=1.0)
+    a_np, b_np, g_np = (np.array(to_np(inp[k])) for k in ("a", "b", "grad_out"))
+    ones = np.array([0xFFFFFFFF], dtype=np.uint32).view(np.float32)[0] if dt == "f32" else np.uint16(0xFFFF)
+    b_np[0, 7000, 5] = ones
+    a_np[0, 12000, 40] = ones
+    g_np[0, 15000, 20] = ones
+    o = orc()
+    ref_out, ref_last = o.fwd(a_np, b_np, dt)
+    ref_ga, ref_gb = o.bwd(a_np, ref_out, g_np, dt)
+    kw = dict(path="stream")
+    out, last = L.lrscan_fwd(from_np(a_np, dt).cuda(), from_np(b_np, dt).cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    ga, gb = L.lrscan_bwd(from_np(a_np, dt).cuda(), from_np(ref_out, dt).cuda(), from_np(g_np, dt).cuda(), **kw)
+    assert L.lrscan_sync_check() == 0
+    as_f32 = (lambda x: bf16_bits_to_f32(x)) if dt == "bf16" else (lambda x: x)
+    for name, got, ref in (("out", to_np(out), ref_out), ("grad_b", to_np(gb), ref_gb), ("grad_a", to_np(ga), ref_ga)):
+        assert np.isnan(as_f32(ref)).any(), name
+        assert_close(got, ref, dt, name, reassociated=True)  # NaN pattern equal, the rest within tolerance
+    assert np.array_equal(np.isnan(last.cpu().numpy()), np.isnan(ref_last))
