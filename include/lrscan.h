@@ -75,17 +75,19 @@ extern "C" {
 #define LRSCAN_PATH_PLAIN   4  /* sequential, plain loads; any alignment */
 #define LRSCAN_PATH_STREAM  5  /* single pass over time chunks (triton_training_scan.py, _real_chunk_summary /
                                   _real_chunk_prefix / _real_chunk_replay fused): one persistent CTA per SM takes
-                                  chunks of 512 steps (bf16 forward on 32-lane tiles: 1024) in ticket order; its
-                                  summary warps publish each chunk's map, a scan warp finds the entering state by
-                                  looking back over the published maps and leaving states, and its replay warps
-                                  run the chunk again while its tiles are still in L2.  Bulk-copy path (16-byte
-                                  aligned rows); plain scan only (no carried state); needs workspace_bytes of device
-                                  scratch like the chunked path; agrees with the sequential definition to rounding,
-                                  and two calls may differ in the last bits (which published states a look-back
-                                  composes depends on timing).  tile_variant: fp32 1 = 32-lane tiles; bf16 1 =
-                                  32-lane tiles, 2 = 64-lane tiles.  Auto takes it for few lanes and at least 32
-                                  chunks of 512 steps per lane group (bf16: the 64-lane tile for a backward on at
-                                  most 128 lanes) */
+                                  chunks of 256 to 1024 steps in ticket order; its summary warps publish each
+                                  chunk's map, a scan warp finds the entering state by looking back over the
+                                  published maps and leaving states, and its replay warps run the chunk again
+                                  while its tiles are still in L2.  Bulk-copy path (16-byte aligned rows); plain
+                                  scan only (no carried state); needs workspace_bytes of device scratch like the
+                                  chunked path; agrees with the sequential definition to rounding, and two calls
+                                  may differ in the last bits (which published states a look-back composes depends
+                                  on timing).  tile_variant: fp32 1 = 32-lane tiles (forward 512-step chunks,
+                                  backward 256), 2 = 32-lane tiles, 256-step chunks; bf16 1 = 32-lane tiles
+                                  (forward 1024, backward 512), 2 = 64-lane tiles (512), 3 = 64-lane tiles (256).
+                                  Auto takes it for few lanes and at least 32 chunks of 512 steps per lane group:
+                                  fp32 variant 2 for a forward from eight lane groups, else 1; bf16 variant 1
+                                  forward, 2 (one 64-lane group) or 3 backward */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */

@@ -51,23 +51,30 @@ WinDirCfg stream_cfg() {
 
 // StreamShape<St, DT, V, W, NW, R, S, SR, NSCAN, NB>: four summary and four
 // replay warps, two scan warps, two chunk buffers, one CTA per SM.  fp32:
-// 32-lane tiles of 32-row windows in 512-step chunks (forward three summary /
-// two replay stages, backward two / three).  bf16: 32-lane tiles of 64-row
-// windows (forward 1024-step chunks, backward 512), or 64-lane tiles of
-// 32-row windows in 512-step chunks.
-using SF32_D32_F = StreamShape<float, 32, 1, 32, 4, 4, 3, 2, 2, 2>;
-using SF32_D32_B = StreamShape<float, 32, 1, 32, 4, 4, 2, 3, 2, 2>;
+// 32-lane tiles of 32-row windows; forward 512-step chunks (three summary /
+// two replay stages) or 256-step ones (more lane groups), backward 256-step
+// chunks (two / three stages: its replays trail their summaries by less time,
+// so more of their tiles are still in L2).  bf16: 32-lane tiles of 64-row
+// windows (forward 1024-step chunks, backward 512), or 64-lane tiles of 32-row
+// windows in 512- or 256-step chunks.
+using SF32_C512_F = StreamShape<float, 32, 1, 32, 4, 4, 3, 2, 2, 2>;
+using SF32_C256_F = StreamShape<float, 32, 1, 32, 4, 2, 3, 2, 2, 2>;
+using SF32_C256_B = StreamShape<float, 32, 1, 32, 4, 2, 2, 3, 2, 2>;
 using SBF_D32_F = StreamShape<bf16_t, 32, 1, 64, 4, 4, 3, 3, 2, 2>;
 using SBF_D32_B = StreamShape<bf16_t, 32, 1, 64, 4, 2, 2, 3, 2, 2>;
 using SBF_D64_F = StreamShape<bf16_t, 64, 2, 32, 4, 4, 3, 3, 2, 2>;
 using SBF_D64_B = StreamShape<bf16_t, 64, 2, 32, 4, 4, 3, 2, 2, 2>;
+using SBF_D64_C256_F = StreamShape<bf16_t, 64, 2, 32, 4, 2, 3, 3, 2, 2>;
+using SBF_D64_C256_B = StreamShape<bf16_t, 64, 2, 32, 4, 2, 3, 2, 2, 2>;
 
 const WinVariant kStreamF32[] = {
-    {"stream_f32_d32", stream_cfg<SF32_D32_F, true>(), stream_cfg<SF32_D32_B, false>()},
+    {"stream_f32_d32", stream_cfg<SF32_C512_F, true>(), stream_cfg<SF32_C256_B, false>()},
+    {"stream_f32_d32_c256", stream_cfg<SF32_C256_F, true>(), stream_cfg<SF32_C256_B, false>()},
 };
 const WinVariant kStreamBF16[] = {
     {"stream_bf16_d32", stream_cfg<SBF_D32_F, true>(), stream_cfg<SBF_D32_B, false>()},
     {"stream_bf16_d64", stream_cfg<SBF_D64_F, true>(), stream_cfg<SBF_D64_B, false>()},
+    {"stream_bf16_d64_c256", stream_cfg<SBF_D64_C256_F, true>(), stream_cfg<SBF_D64_C256_B, false>()},
 };
 
 }  // namespace

@@ -410,12 +410,22 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         int n = 0;
         const WinVariant *tab = stream_variants(dtype, &n);
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
-        // fp32: one variant.  bf16: 32-lane tiles, except the backward on at
-        // most 128 lanes, where the 64-lane tile measured faster (B=1 T=2^22
-        // D=64 backward: 0.49 against 0.54 ms; B=8 T=2^18 D=64: 0.25 against
-        // 0.25 ms, D=256 T=2^20: 0.51 against 0.47 ms)
+        // Measured on few-lane long sequences (fraction of the copy rate):
+        // fp32 forward, 512- against 256-step chunks: 0.92 / 0.73 at two 32-lane
+        // groups (B=1 D=64), 0.89 / 0.81 at four, 0.89 / 0.89 and 0.80 / 0.88 at
+        // eight (B=1 D=256, B=4 D=64), 0.77 / 0.89 at sixteen; the fp32 backward
+        // takes 256-step chunks in both variants.  bf16 forward: 32-lane tiles;
+        // bf16 backward: the 64-lane tile in 512-step chunks for one 64-lane
+        // group (0.83 against 0.74), in 256-step chunks from four (0.86-0.88
+        // against 0.78-0.80; two and three groups are not measured)
         int vi = force_v > 0 ? force_v - 1 : 0;
-        if (force_v == 0 && dtype == LRSCAN_BF16 && dir == 1 && B * D <= 128) vi = 1;
+        if (force_v == 0) {
+            if (dtype == LRSCAN_F32) {
+                vi = dir == 0 && B * ((D + 31) / 32) >= 8 ? 1 : 0;
+            } else if (dir == 1) {
+                vi = B * ((D + 63) / 64) >= 2 ? 2 : 1;
+            }
+        }
         const WinDirCfg &v = dir_of(tab[vi], dir);
         const Occ o = occupancy(tab[vi], dir, B, D, g);
         if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);

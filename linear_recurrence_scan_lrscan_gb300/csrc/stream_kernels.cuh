@@ -11,7 +11,7 @@
 // once to reduce it to its affine map h -> P h + Q (tiles from HBM), once to
 // replay it from its entering state (the same tiles again, from L2).  A CTA's
 // warps have one role each:
-//   ticket warp     fetches chunk tickets two chunks ahead of the summaries;
+//   ticket warp     fetches chunk tickets one chunk ahead of the summaries;
 //   NW summary      warp w reduces windows w, w + NW, ... of every chunk,
 //   warps           streaming its tiles through S stages of its own (S - 1
 //                   copies in flight ahead of the tile it reduces); the last
@@ -248,8 +248,7 @@ struct StreamShape {
     static_assert(SR == 2 || SR == 3, "a replay tile is prefetched one window ahead");
 };
 
-constexpr int kStreamSlots = 8;  // step ring of the ticket warp
-constexpr int kStreamAhead = 2;  // ticket k is fetched once the summaries of chunk k - 2 have started
+constexpr int kStreamSlots = 8;  // ticket ring of the ticket warp
 
 // Shared-memory layout, host and device.  Summary warp w owns stages
 // w*S .. w*S+S-1 of the summary ring (two planes each), replay warp w owns
@@ -260,7 +259,7 @@ struct StreamGeom {
     int sstage_bytes;  // summary stage: forward a, b; backward a, grad_out
     int rstage_bytes;  // replay stage: forward a, b; backward a, out, grad_out
     int rring_off;     // replay ring after the summary ring
-    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_free[slots], maps[NB], entries[NB], buf_free[NB]
+    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_req[slots], maps[NB], entries[NB], buf_free[NB]
     int ticket_off;    // step tickets [slots]
     int tick_off;      // chunk tickets per buffer [NB] (-1: end mark)
     int map_off;       // window maps [NB][NWIN][DT] float2
@@ -321,7 +320,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
     auto rfull = [&](int st) { return bar(BS + st); };
     constexpr int BR = BS + NW * SR;  // then the replay ring's
     auto step_full = [&](int q) { return bar(BR + q); };
-    auto step_free = [&](int q) { return bar(BR + SLOTS + q); };
+    auto step_req = [&](int q) { return bar(BR + SLOTS + q); };
     auto maps_bar = [&](int b) { return bar(BR + 2 * SLOTS + b); };
     auto entries_bar = [&](int b) { return bar(BR + 2 * SLOTS + NB + b); };
     auto buf_free = [&](int b) { return bar(BR + 2 * SLOTS + 2 * NB + b); };
@@ -337,7 +336,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
         for (int st = 0; st < NW * SR; ++st) mbar_init(rfull(st), 1);
         for (int q = 0; q < SLOTS; ++q) {
             mbar_init(step_full(q), 1);
-            mbar_init(step_free(q), NW);
+            mbar_init(step_req(q), NW);
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(maps_bar(b), 1);  // the last summary warp (or the end mark)
@@ -384,10 +383,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
     if (warp == 2 * NW + NSCAN) {
         // ------------------------------------------------------------ tickets
         if (lane == 0) {
+            // ticket 0 at once; ticket j >= 1 once every summary warp has asked
+            // for it (at the start of its chunk j - 1, request slot (j-1) mod SLOTS)
             for (int j = 0;; ++j) {
-                if (j >= kStreamAhead) {
-                    const int jf = j - kStreamAhead;
-                    if (!mbar_wait(step_free(jf % SLOTS), static_cast<uint32_t>((jf / SLOTS) & 1), wc,
+                if (j >= 1) {
+                    const int m = j - 1;
+                    if (!mbar_wait(step_req(m % SLOTS), static_cast<uint32_t>((m / SLOTS) & 1), wc,
                                    kSiteProducerEmpty))
                         return;
                 }
@@ -445,15 +446,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                 drain();
                 return;
             }
-            // the next ticket (its first tiles go out while this chunk is reduced)
+            // ask for the next ticket now and read it when its first tile is due
+            // (a ticket is taken about one chunk before its summary starts, so
+            // look-backs rarely wait on a chunk whose CTA has not begun it)
+            if (lane == 0) mbar_arrive(step_req(k % SLOTS));
             const int q1 = (k + 1) % SLOTS;
-            if (!warp_wait(step_full(q1), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc, kSiteStreamStep)) {
-                drain();
-                return;
-            }
-            const int tn = step_ticket[q1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(step_free(k % SLOTS));
+            int tn = -2;  // not read yet
             const Chunk ch = decode(tk);
             float P[R][V], Q[R][V];
 #pragma unroll
@@ -461,6 +459,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                 const int u = k * R + r;
                 // keep S - 1 tiles in flight ahead of this one (chunks k and k + 1)
                 while (u_iss <= u + S - 1) {
+                    if (u_iss / R != k && tn == -2) {
+                        if (!warp_wait(step_full(q1), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc,
+                                       kSiteStreamStep)) {
+                            drain();
+                            return;
+                        }
+                        tn = step_ticket[q1];
+                    }
                     const int t = u_iss / R == k ? tk : tn;
                     if (t < 0) break;
                     if (lane == 0) sissue(u_iss, t);
@@ -542,6 +548,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                     wcount[b] = 0;  // next used NB chunks on, after this buffer's replays
                     mbar_arrive(maps_bar(b));
                 }
+            }
+            if (tn == -2) {
+                if (!warp_wait(step_full(q1), static_cast<uint32_t>(((k + 1) / SLOTS) & 1), wc, kSiteStreamStep)) {
+                    drain();
+                    return;
+                }
+                tn = step_ticket[q1];
             }
             tk = tn;
         }

@@ -165,13 +165,19 @@ def test_occupancy_rule_few_lanes_long_sequence(lib):
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", state=True)
     assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
-    # fp32 on 32-lane tiles; bf16 on 32-lane tiles, but 64-lane tiles for a
-    # backward on at most 128 lanes
-    for (B, D, dt) in ((1, 64, "bf16"), (8, 64, "f32"), (1, 256, "bf16"), (8, 64, "bf16")):
-        for direction in ("fwd", "bwd"):
+    # fp32 on 32-lane tiles (forward: 256-step chunks from eight lane groups);
+    # bf16 forward on 32-lane tiles, bf16 backward on 64-lane tiles (256-step
+    # chunks from two lane groups)
+    want = {(1, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d64"),
+            (8, 64, "f32"): ("stream_f32_d32_c256", "stream_f32_d32"),
+            (1, 128, "f32"): ("stream_f32_d32", "stream_f32_d32"),
+            (1, 256, "bf16"): ("stream_bf16_d32", "stream_bf16_d64_c256"),
+            (8, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d64_c256")}
+    for (B, D, dt), names in want.items():
+        for direction, name in zip(("fwd", "bwd"), names):
             p = L.lrscan_plan(B, 1 << 18, D, dt, direction)
-            lanes = 64 if (dt == "bf16" and direction == "bwd" and B * D <= 128) else 32
-            assert p["path"] == "stream" and p["lanes_per_cta"] == lanes, (B, D, dt, direction, p)
+            lanes = 64 if (dt == "bf16" and direction == "bwd") else 32
+            assert p["path"] == "stream" and p["name"] == name and p["lanes_per_cta"] == lanes, (B, D, dt, p)
     # 32 chunks of 512 steps per lane group stream; fewer take the chunked path
     assert L.lrscan_plan(1, 16384, 64, "bf16", "fwd")["path"] == "stream"
     assert L.lrscan_plan(1, 8192, 64, "bf16", "fwd")["path"] == "chunk"
@@ -320,15 +326,18 @@ def test_complex_chunked_plans(lib):
 def test_stream_plans(lib):
     """The persistent chunk-streaming path: four summary, four replay, two scan
     warps and a ticket warp per CTA, one CTA per SM (no more than there are
-    chunk tickets), 512-step chunks (bf16 forward on 32-lane tiles: 1024), its
-    publication workspace (ticket, a map and a state per chunk and lane), and
-    refusals where it cannot run."""
+    chunk tickets), 256- to 1024-step chunks, its publication workspace
+    (ticket, a map and a state per chunk and lane), and refusals where it
+    cannot run."""
     pad = lambda x: (x + 255) // 256 * 256
     # name: {direction: (rows per window, windows per chunk, ring stages)}
-    shapes = {"stream_f32_d32": {"fwd": (32, 16, 20), "bwd": (32, 16, 20)},
+    shapes = {"stream_f32_d32": {"fwd": (32, 16, 20), "bwd": (32, 8, 20)},
+              "stream_f32_d32_c256": {"fwd": (32, 8, 20), "bwd": (32, 8, 20)},
               "stream_bf16_d32": {"fwd": (64, 16, 24), "bwd": (64, 8, 20)},
-              "stream_bf16_d64": {"fwd": (32, 16, 24), "bwd": (32, 16, 20)}}
-    for dt, names in (("f32", ("stream_f32_d32",)), ("bf16", ("stream_bf16_d32", "stream_bf16_d64"))):
+              "stream_bf16_d64": {"fwd": (32, 16, 24), "bwd": (32, 16, 20)},
+              "stream_bf16_d64_c256": {"fwd": (32, 8, 24), "bwd": (32, 8, 20)}}
+    for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d32_c256")),
+                      ("bf16", ("stream_bf16_d32", "stream_bf16_d64", "stream_bf16_d64_c256"))):
         assert L.lrscan_num_variants("stream", dt) == len(names)
         for v, name in enumerate(names, 1):
             for direction in ("fwd", "bwd"):
@@ -350,4 +359,4 @@ def test_stream_plans(lib):
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
     with pytest.raises(L.LrscanError):
-        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=2)
+        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=3)

@@ -67,7 +67,7 @@ def check(B, T, D, dt, variant, seed, a_lo=0.6):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 @pytest.mark.parametrize("shape_i", range(len(SHAPES)))
 def test_stream_parity(dt, variant, shape_i):
     if variant > L.lrscan_num_variants("stream", dt):
