@@ -692,8 +692,9 @@ def run_complex_long_t(dev, peak) -> dict:
     """The complex scan with few lanes and a long sequence: B=1 T=2^20 D=64
     fp32 re/im planes, |a|~U(0.9,0.999) with phases ~U(-pi,pi), b and grad_out
     ~N(0,1), drawn on the device from a seeded generator.  The automatic plan
-    takes the chunked path (complex chunk maps, grouped prefix); algorithmic
-    bytes are 6 (forward) and 10 (backward) elements per (t, d)."""
+    (chunk streaming) beside the chunked path (complex chunk maps, grouped
+    prefix); algorithmic bytes are 6 (forward) and 10 (backward) elements per
+    (t, d)."""
     import math
 
     import torch
@@ -709,19 +710,24 @@ def run_complex_long_t(dev, peak) -> dict:
     outs = L.lrscan_cfwd(ar, ai, br, bi)
     grads = L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi)
     stream = torch.cuda.current_stream()
-    fms = time_launches(lambda i: L.lrscan_cfwd(ar, ai, br, bi, out_r=outs[0], out_i=outs[1], last_r=outs[2],
-                                                last_i=outs[3]), 10, stream)
-    bms = time_launches(lambda i: L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi, grads=grads), 10, stream)
-    if L.lrscan_sync_check() != 0:
-        raise RuntimeError("device error while timing the long complex scan")
     E = B * T * D
     fb, bb = 6 * E * 4 + 8 * B * D, 10 * E * 4
-    res = {"workload": f"B={B} T={T} D={D} fp32 complex (few lanes, long sequence)",
-           "fwd": {"ms": fms, "frac": fb / (fms * 1e-3) / 1e9 / peak,
-                   "kernel": L.lrscan_plan_complex(B, T, D, "f32", "fwd")["name"]},
-           "bwd": {"ms": bms, "frac": bb / (bms * 1e-3) / 1e9 / peak,
-                   "kernel": L.lrscan_plan_complex(B, T, D, "f32", "bwd")["name"]},
-           "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+    res = {"workload": f"B={B} T={T} D={D} fp32 complex (few lanes, long sequence)"}
+    for kw, name in ((dict(), "auto"), (dict(path="chunk"), "chunked")):
+        fms = time_launches(lambda i: L.lrscan_cfwd(ar, ai, br, bi, out_r=outs[0], out_i=outs[1], last_r=outs[2],
+                                                    last_i=outs[3], **kw), 10, stream)
+        bms = time_launches(lambda i: L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi, grads=grads, **kw), 10, stream)
+        if L.lrscan_sync_check() != 0:
+            raise RuntimeError("device error while timing the long complex scan")
+        part = {"fwd": {"ms": fms, "frac": fb / (fms * 1e-3) / 1e9 / peak,
+                        "kernel": L.lrscan_plan_complex(B, T, D, "f32", "fwd", **kw)["name"]},
+                "bwd": {"ms": bms, "frac": bb / (bms * 1e-3) / 1e9 / peak,
+                        "kernel": L.lrscan_plan_complex(B, T, D, "f32", "bwd", **kw)["name"]},
+                "elements/s": 2 * E / ((fms + bms) * 1e-3)}
+        if name == "auto":
+            res.update(part)
+        else:
+            res[name] = part
     del ar, ai, br, bi, gr, gi, outs, grads
     torch.cuda.empty_cache()
     return res

@@ -266,16 +266,23 @@ int lrscan_bwd_state(const void *a, const void *out, const void *grad_out,
  * LRSCAN_PATH_CHUNK (three phases over time chunks of opts->chunk_len steps,
  * 16 ... 512, default 64 fp32 / 128 bf16: complex chunk maps, their prefix -- flat, or grouped
  * when a lane has many chunks; tile_variant 1 / 2 forces flat / grouped --
- * and the replay; any alignment) or LRSCAN_PATH_PLAIN (any alignment).  Auto
- * takes the chunked path when the lanes fill fewer than 0.45 lane tiles of
- * 32 per SM (aligned rows; else 32 warps per SM) and T >= 16 chunks, else a
- * tiled variant when the rows are aligned, else the plain kernels.
+ * and the replay; any alignment), LRSCAN_PATH_STREAM (the persistent
+ * chunk-streaming kernels of the real scan on the re / im planes: complex
+ * chunk maps and states published as self-validating words; fp32 forward
+ * 256-step chunks, backward 128; bf16 512 and 256; aligned rows, no carried
+ * state; one tile variant) or LRSCAN_PATH_PLAIN (any alignment).  Auto takes,
+ * when the lanes fill fewer than 0.45 lane tiles of 32 per SM (aligned rows;
+ * else 32 warps per SM) and T >= 16 chunks, the streaming path (aligned rows,
+ * no carried state, no chunk_len asked for, T >= 32 * 512), else the chunked
+ * path; with more lanes a tiled variant when the rows are aligned, else the
+ * plain kernels.
  * The sequential tiles and the plain kernels keep the order above and agree
- * with it bit for bit; the windowed tiles and the chunked path (complex
- * affine maps) agree to rounding.  The chunked path needs
- * lrscan_plan_complex(...).workspace_bytes of device scratch: library-owned
- * per (device, stream), or opts->workspace.  Moves 6 elements per (t, d)
- * forward and 10 backward (the chunked path re-reads its inputs: 10 and 16).
+ * with it bit for bit; the windowed tiles, the chunked and the streaming
+ * paths (complex affine maps) agree to rounding.  The chunked and streaming
+ * paths need lrscan_plan_complex(...).workspace_bytes of device scratch:
+ * library-owned per (device, stream), or opts->workspace.  Moves 6 elements
+ * per (t, d) forward and 10 backward (the chunked path re-reads its inputs:
+ * 10 and 16).
  * Other rules as lrscan_fwd_ex.
  */
 int lrscan_cfwd(const void *ar, const void *ai, const void *br, const void *bi,

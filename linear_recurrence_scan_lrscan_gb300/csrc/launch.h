@@ -93,6 +93,8 @@ const WinVariant *win_variants(int path, int dtype, int *count);
 // Persistent chunk-streaming variants (kernels_stream.cu); dtype 0 = f32,
 // 1 = bf16.
 const WinVariant *stream_variants(int dtype, int *count);
+// The same kernels on the complex scan's re / im planes.
+const WinVariant *cstream_variants(int dtype, int *count);
 
 // Complex scan tile variants (kernels_complex.cu); dtype 0 = f32, 1 = bf16.
 const WinVariant *cwin_variants(int dtype, int *count);

@@ -193,12 +193,41 @@ struct StreamScratch {
     size_t head() const { return 256; }
     size_t total() const { return head() + agg + incl; }
 };
-StreamScratch stream_scratch(int64_t ng, int64_t nc, int dt) {
+StreamScratch stream_scratch(int64_t ng, int64_t nc, int dt, int k = 1) {  // k = 2: complex maps and states
     auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
     StreamScratch s;
-    s.agg = pad(static_cast<size_t>(ng) * nc * dt * 8);
-    s.incl = pad(static_cast<size_t>(ng) * nc * dt * 4);
+    s.agg = pad(static_cast<size_t>(ng) * nc * dt * 8 * k);
+    s.incl = pad(static_cast<size_t>(ng) * nc * dt * 4 * k);
     return s;
+}
+
+// The plan of a chunk-streaming call on variant vi of tab (k = 2: the
+// complex scan's maps and states).
+int plan_stream_variant(const WinVariant *tab, int vi, int dir, int64_t B, int64_t T, int64_t D, int k,
+                        const Geometry &g, Choice *ch) {
+    const WinDirCfg &v = dir_of(tab[vi], dir);
+    const Occ o = occupancy(tab[vi], dir, B, D, g);
+    if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);
+    const int64_t ng = B * ((D + v.dt - 1) / v.dt);
+    const int64_t rows = static_cast<int64_t>(v.s) * v.w;  // windows x rows each
+    const int64_t nc = (T + rows - 1) / rows;
+    if (ng * nc > 0x7fffffffLL) return fail(LRSCAN_EINVAL, "too many chunks for the streaming path");
+    ch->vidx = vi;
+    ch->var = &tab[vi];
+    ch->chunk = static_cast<int>(rows);
+    // One CTA per SM (no more than there are chunk tickets).  A chunk's tiles
+    // must still be in L2 when its replay reads them: with two chunk buffers a
+    // CTA holds at most about two and a half chunks of input planes between
+    // summaries and replays (512-step fp32 chunks: 40 MB over 152 SMs).
+    const int resident = v.max_resident > 0 ? std::min(o.resident, v.max_resident) : o.resident;
+    ch->ctas = std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count);
+    ch->threads = v.threads;
+    ch->smem = v.smem;
+    ch->stages = v.nstage;
+    ch->dir = dir;
+    ch->kernels = 1;
+    ch->workspace = stream_scratch(ng, nc, v.dt, k).total();
+    return LRSCAN_OK;
 }
 
 // The grouped prefix pays when every lane has many chunks and the lanes alone
@@ -426,29 +455,7 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
                 vi = B * ((D + 63) / 64) >= 2 ? 2 : 1;
             }
         }
-        const WinDirCfg &v = dir_of(tab[vi], dir);
-        const Occ o = occupancy(tab[vi], dir, B, D, g);
-        if (o.resident == 0) return fail(LRSCAN_EINVAL, "stream variant %s does not fit on an SM", tab[vi].name);
-        const int64_t ng = B * ((D + v.dt - 1) / v.dt);
-        const int64_t rows = static_cast<int64_t>(v.s) * v.w;  // window warps x rows each
-        const int64_t nc = (T + rows - 1) / rows;
-        if (ng * nc > 0x7fffffffLL) return fail(LRSCAN_EINVAL, "too many chunks for the streaming path");
-        ch->vidx = vi;
-        ch->var = &tab[vi];
-        ch->chunk = static_cast<int>(rows);
-        // One CTA per SM (no more than there are chunk tickets).  A chunk's
-        // tiles must still be in L2 when its replay reads them: with two chunk
-        // buffers a CTA holds at most about two and a half chunks of input
-        // planes between summaries and replays (512-step fp32 chunks: 40 MB
-        // over 152 SMs).
-        const int resident = v.max_resident > 0 ? std::min(o.resident, v.max_resident) : o.resident;
-        ch->ctas = std::min<long long>(ng * nc, static_cast<long long>(resident) * g.sm_count);
-        ch->threads = v.threads;
-        ch->smem = v.smem;
-        ch->stages = v.nstage;
-        ch->dir = dir;
-        ch->kernels = 1;
-        ch->workspace = stream_scratch(ng, nc, v.dt).total();
+        return plan_stream_variant(tab, vi, dir, B, T, D, 1, g, ch);
     } else if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix
         if (force_v > 2) return fail(LRSCAN_EINVAL, "the chunked path has two variants (1 flat, 2 grouped prefix)");
@@ -668,29 +675,32 @@ int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_
 // grad_b), the publication workspace reset (ticket zeroed, maps and states
 // all-ones), one launch.
 int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::initializer_list<void *> outs,
-               float *last, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev, DeviceCtx *ctx,
-               const lrscan_opts *opts, bool bwd) {
+               float *last, float *last_i, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev,
+               DeviceCtx *ctx, const lrscan_opts *opts, bool bwd, bool cplx) {
     const WinDirCfg &v = dir_of(*ch.var, bwd ? 1 : 0);
     const int64_t ndt = (D + v.dt - 1) / v.dt;
     const int64_t ng = B * ndt;
     const int64_t nc = (T + ch.chunk - 1) / ch.chunk;
-    const StreamScratch sc = stream_scratch(ng, nc, v.dt);
+    const StreamScratch sc = stream_scratch(ng, nc, v.dt, cplx ? 2 : 1);
     void *ws = nullptr;
     int rc = workspace_for(ctx, st, ch.workspace, opts, &ws);
     if (rc) return rc;
-    CUtensorMap maps[5];  // inputs in kernel order, then the outputs at 3 and 4
-    int k = 0;
-    for (const void *p : ins)
-        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
-    k = 3;
-    for (void *p : outs)
-        if (encode_map(&maps[k++], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+    CUtensorMap maps[10];  // inputs in kernel order from 0, outputs from 6
     WinLaunch L{};
-    for (int i = 0; i < k; ++i) L.maps[i] = &maps[i];
-    auto o = outs.begin();
-    L.out0 = *o;
-    L.out1 = outs.size() > 1 ? *(o + 1) : nullptr;
+    int k = 0;
+    for (const void *p : ins) {
+        if (encode_map(&maps[k], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+        L.maps[k] = &maps[k];
+        ++k;
+    }
+    k = 6;
+    for (void *p : outs) {
+        if (encode_map(&maps[k], p, dtype, B, T, D, v.dt, v.w)) return LRSCAN_EINVAL;
+        L.maps[k] = &maps[k];
+        ++k;
+    }
     L.last = last;
+    L.last_i = last_i;
     L.B = B; L.T = T; L.D = D;
     L.status = ctx->status;
     L.timeout_ns = g_timeout_ns.load();
@@ -760,7 +770,8 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
         }
         return LRSCAN_OK;
     }
-    if (ch.path == kPathStream) return run_stream(ch, {a, b}, {out}, last, B, T, D, dtype, st, dev, ctx, opts, false);
+    if (ch.path == kPathStream)
+        return run_stream(ch, {a, b}, {out}, last, nullptr, B, T, D, dtype, st, dev, ctx, opts, false, false);
     ChunkLaunch L{};
     L.in0 = a; L.in1 = b; L.out0 = out; L.last = last;
     L.B = B; L.T = T; L.D = D;
@@ -825,7 +836,8 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
         return LRSCAN_OK;
     }
     if (ch.path == kPathStream)
-        return run_stream(ch, {a, out, grad_out}, {grad_a, grad_b}, nullptr, B, T, D, dtype, st, dev, ctx, opts, true);
+        return run_stream(ch, {a, out, grad_out}, {grad_a, grad_b}, nullptr, nullptr, B, T, D, dtype, st, dev, ctx, opts,
+                          true, false);
     ChunkLaunch L{};
     L.in0 = a; L.in1 = out; L.in2 = grad_out; L.out0 = grad_a; L.out1 = grad_b;
     L.B = B; L.T = T; L.D = D;
@@ -879,10 +891,13 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
     if (ext && want == kPathPlain)
         return fail(LRSCAN_EINVAL, "the plain complex kernels carry no state (path %d)", want);
     const int force_v = opts ? opts->tile_variant : 0;
-    if (want != kPathAuto && want != kPathSeq && want != kPathWindow && want != kPathPlain && want != kPathChunk)
+    if (want != kPathAuto && want != kPathSeq && want != kPathWindow && want != kPathPlain && want != kPathChunk &&
+        want != kPathStream)
         return fail(LRSCAN_EINVAL, "unknown complex scan path %d", want);
-    if ((want == kPathSeq || want == kPathWindow) && !aligned16)
+    if ((want == kPathSeq || want == kPathWindow || want == kPathStream) && !aligned16)
         return fail(LRSCAN_EINVAL, "tiled paths need 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
+    if (want == kPathStream && ext)
+        return fail(LRSCAN_EINVAL, "the chunk-streaming path carries no state or resets");
     // default chunk: 64 steps fp32, 128 bf16 (the same bytes per chunk row;
     // measured on few-lane complex scans: bf16 10-13 % faster than at 64)
     const int chunk = opts && opts->chunk_len ? opts->chunk_len : (dtype == LRSCAN_BF16 ? 128 : 64);
@@ -896,17 +911,26 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         // With carried state the tiled kernels (EXT instantiations) run as
         // they would without it; unaligned rows take the chunked kernels,
         // which carry state at any alignment.
+        // In one pass (chunk streaming) from 32 chunks of 512 steps per lane
+        // group, without carried state or an asked-for chunk length.
         const long long few = aligned16 ? static_cast<long long>(0.45 * g.sm_count * 32) : 32LL * g.sm_count * 32;
-        if (B * D < few && T >= 16LL * chunk) path = kPathChunk;
+        if (B * D < few && T >= 16LL * chunk)
+            path = (aligned16 && !ext && T >= 32LL * 512 && !(opts && opts->chunk_len)) ? kPathStream : kPathChunk;
         else path = aligned16 ? kPathSeq : (ext ? kPathChunk : kPathPlain);
     } else {
         // seq and window both name the tiled variant table (sequential and windowed tiles)
-        path = (want == kPathPlain || want == kPathChunk) ? want : kPathSeq;
+        path = (want == kPathPlain || want == kPathChunk || want == kPathStream) ? want : kPathSeq;
     }
     ch->path = path;
     ch->dir = dir;
     ch->kernels = 1;
     ch->vec = 1;
+    if (path == kPathStream) {
+        int n = 0;
+        const WinVariant *tab = cstream_variants(dtype, &n);
+        if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
+        return plan_stream_variant(tab, force_v > 0 ? force_v - 1 : 0, dir, B, T, D, 2, g, ch);
+    }
     if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix
         if (force_v > 2) return fail(LRSCAN_EINVAL, "the chunked path has two variants (1 flat, 2 grouped prefix)");
@@ -1042,6 +1066,9 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
     Choice ch;
     if ((rc = plan_complex(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     const size_t es = esize(dtype);
+    if (ch.path == kPathStream)
+        return run_stream(ch, {in[0], in[1], in[2], in[3]}, {out_r, out_i}, last_r, last_i, B, T, D, dtype, st, dev,
+                          ctx, opts, false, true);
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
         if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
@@ -1120,6 +1147,9 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
     const bool al = aligned16({in[0], in[1], in[2], in[3], in[4], in[5], outp[0], outp[1], outp[2], outp[3]}, D, dtype);
     Choice ch;
     if ((rc = plan_complex(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch, ext))) return rc;
+    if (ch.path == kPathStream)
+        return run_stream(ch, {in[0], in[1], in[2], in[3], in[4], in[5]}, {outp[0], outp[1], outp[2], outp[3]},
+                          nullptr, nullptr, B, T, D, dtype, st, dev, ctx, opts, true, true);
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
         if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;

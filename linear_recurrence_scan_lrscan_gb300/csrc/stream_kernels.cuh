@@ -231,14 +231,123 @@ __device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, fl
     }
 }
 
+// Complex steps in the nested fused multiply-add order of the sequential
+// complex scan: x * h + b, and conj(x) * h + b.
+__device__ __forceinline__ void cx_step(float xr, float xi, float hr, float hi, float br, float bi, float &nr,
+                                        float &ni) {
+    nr = __fmaf_rn(xr, hr, __fmaf_rn(-xi, hi, br));
+    ni = __fmaf_rn(xi, hr, __fmaf_rn(xr, hi, bi));
+}
+__device__ __forceinline__ void cxc_step(float xr, float xi, float hr, float hi, float br, float bi, float &nr,
+                                         float &ni) {
+    nr = __fmaf_rn(xr, hr, __fmaf_rn(xi, hi, br));
+    ni = __fmaf_rn(xr, hi, __fmaf_rn(-xi, hr, bi));
+}
+
+// Complex look-back: as stream_lookback, for complex maps (two words per lane
+// and chunk: P = (re, im), Q = (re, im)) and leaving states (one word).
+template <int DT, int V, int BATCH>
+__device__ bool stream_lookback_cx(const StreamArgs &sa, int gi, int cc, int i0, float (&hr_in)[V],
+                                   float (&hi_in)[V], const WaitCtx &wc) {
+    const int lane = threadIdx.x & 31;
+    const size_t g0 = static_cast<size_t>(gi) * sa.nc;
+    const float2 *states = reinterpret_cast<const float2 *>(sa.incl);
+    float aPr[V], aPi[V], aQr[V], aQi[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { aPr[v] = 1.0f; aPi[v] = 0.0f; aQr[v] = 0.0f; aQi[v] = 0.0f; }
+    int j = cc - 1;
+    bool done = false;
+    uint64_t start = 0;
+    bool timed = false;
+    for (uint32_t spin = 0;; ++spin) {
+        if (!done) {
+            uint64_t sw[BATCH][V], pw[BATCH][V], qw[BATCH][V];
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (j - t >= 0) {
+                    const size_t row = (g0 + j - t) * DT + i0;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        sw[t][v] = peek_map(states + row + v);
+                        pw[t][v] = peek_map(sa.agg + 2 * (row + v));
+                        qw[t][v] = peek_map(sa.agg + 2 * (row + v) + 1);
+                    }
+                }
+            }
+            bool go = true;
+            int folded = 0;
+#pragma unroll
+            for (int t = 0; t < BATCH; ++t) {
+                if (go) {
+                    if (j - t < 0) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) { hr_in[v] = aQr[v]; hi_in[v] = aQi[v]; }
+                        done = true;
+                        go = false;
+                    } else {
+                        bool has_state = true, has_map = true;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            has_state = has_state && static_cast<uint32_t>(sw[t][v]) != kUnset;
+                            has_map = has_map && static_cast<uint32_t>(pw[t][v]) != kUnset &&
+                                      static_cast<uint32_t>(qw[t][v]) != kUnset;
+                        }
+                        if (has_state) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v)
+                                cx_step(aPr[v], aPi[v], __uint_as_float(static_cast<uint32_t>(sw[t][v])),
+                                        __uint_as_float(static_cast<uint32_t>(sw[t][v] >> 32)), aQr[v], aQi[v],
+                                        hr_in[v], hi_in[v]);
+                            done = true;
+                            go = false;
+                        } else if (has_map) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                const float Pr = __uint_as_float(static_cast<uint32_t>(pw[t][v]));
+                                const float Pi = __uint_as_float(static_cast<uint32_t>(pw[t][v] >> 32));
+                                const float Qr = __uint_as_float(static_cast<uint32_t>(qw[t][v]));
+                                const float Qi = __uint_as_float(static_cast<uint32_t>(qw[t][v] >> 32));
+                                float nQr, nQi, nPr, nPi;
+                                cx_step(aPr[v], aPi[v], Qr, Qi, aQr[v], aQi[v], nQr, nQi);
+                                cx_step(aPr[v], aPi[v], Pr, Pi, 0.0f, 0.0f, nPr, nPi);
+                                aQr[v] = nQr; aQi[v] = nQi; aPr[v] = nPr; aPi[v] = nPi;
+                            }
+                            ++folded;
+                        } else {
+                            go = false;
+                        }
+                    }
+                }
+            }
+            j -= folded;
+        }
+        if (__all_sync(0xffffffffu, done)) return true;
+        if ((spin & 7u) == 7u) {
+            bool stop = *wc.abort_flag != 0;
+            if (!timed) {
+                start = global_timer_ns();
+                timed = true;
+            } else if (global_timer_ns() - start > wc.timeout_ns) {
+                stop = true;
+                if (lane == 0) record_error(wc, kErrTimeout, kSiteLookback);
+            }
+            if (__any_sync(0xffffffffu, stop)) return false;
+        }
+    }
+}
+
 // Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
 // window, summary (= replay) warps, windows per warp and chunk, summary and
-// replay stages per warp, scan warps, chunk buffers.
-template <class St_, int DT_, int V_, int W_, int NW_, int R_, int S_, int SR_, int NSCAN_, int NB_>
+// replay stages per warp, scan warps, chunk buffers, complex scan (re / im
+// planes).
+template <class St_, int DT_, int V_, int W_, int NW_, int R_, int S_, int SR_, int NSCAN_, int NB_,
+          bool CPLX_ = false>
 struct StreamShape {
     using St = St_;
     static constexpr int DT = DT_, V = V_, W = W_, NW = NW_, R = R_, S = S_, SR = SR_, NSCAN = NSCAN_, NB = NB_;
-    static constexpr int NWIN = NW * R;  // windows per chunk
+    static constexpr bool CPLX = CPLX_;
+    static constexpr int K = CPLX ? 2 : 1;  // floats per value (re, im)
+    static constexpr int NWIN = NW * R;     // windows per chunk
     static constexpr int THREADS = (2 * NW + NSCAN + 1) * 32;
     static constexpr int MINB = 1;
     static_assert(DT == 32 * V, "one warp spans a tile row");
@@ -250,21 +359,47 @@ struct StreamShape {
 
 constexpr int kStreamSlots = 8;  // ticket ring of the ticket warp
 
+// Tensor maps of one call: inputs in kernel order (real forward a, b;
+// backward a, out, grad_out; complex forward ar, ai, br, bi; backward ar, ai,
+// out_r, out_i, grad_out_r, grad_out_i), outputs (real forward out; backward
+// grad_a, grad_b; complex forward out_r, out_i; backward grad_ar, grad_ai,
+// grad_br, grad_bi).
+struct StreamMaps {
+    CUtensorMap in[6];
+    CUtensorMap out[4];
+};
+
+// Planes of a direction.  Summary planes: the decay's K parts (backward: one
+// row late), then the drive's K parts (forward b, backward grad_out).  Replay
+// planes: every input, the decay one row late and out one row early in the
+// backward.  Output o is staged over replay plane K + o (forward: over b;
+// backward: grad_a over out, grad_b over grad_out).
+template <class C, bool BWD>
+struct StreamPlanes {
+    static constexpr int K = C::K;
+    static constexpr int NS = 2 * K;
+    static constexpr int NIN = K * (BWD ? 3 : 2);
+    static constexpr int NOUT = BWD ? 2 * K : K;
+    __device__ static int sum_map(int p) { return p < K ? p : (BWD ? 2 * K + (p - K) : p); }
+    __device__ static int sum_dy(int p) { return p < K && BWD ? 1 : 0; }
+    __device__ static int rep_dy(int p) { return BWD ? (p < K ? 1 : (p < 2 * K ? -1 : 0)) : 0; }
+};
+
 // Shared-memory layout, host and device.  Summary warp w owns stages
-// w*S .. w*S+S-1 of the summary ring (two planes each), replay warp w owns
+// w*S .. w*S+S-1 of the summary ring (NS planes each), replay warp w owns
 // stages w*SR .. w*SR+SR-1 of the replay ring (NIN planes each; the outputs
 // overwrite their inputs there and leave by bulk tensor stores).
 struct StreamGeom {
     int tile_bytes;    // one plane of one window: W * DT * elem
-    int sstage_bytes;  // summary stage: forward a, b; backward a, grad_out
-    int rstage_bytes;  // replay stage: forward a, b; backward a, out, grad_out
+    int sstage_bytes;  // summary stage
+    int rstage_bytes;  // replay stage
     int rring_off;     // replay ring after the summary ring
     int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_req[slots], maps[NB], entries[NB], buf_free[NB]
     int ticket_off;    // step tickets [slots]
     int tick_off;      // chunk tickets per buffer [NB] (-1: end mark)
-    int map_off;       // window maps [NB][NWIN][DT] float2
-    int cmap_off;      // chunk maps [NB][DT] float2
-    int entry_off;     // window entering states [NB][NWIN][DT] float
+    int map_off;       // window maps [NB][NWIN][DT][2K] floats (P, Q)
+    int cmap_off;      // chunk maps [NB][DT][2K] floats
+    int entry_off;     // window entering states [NB][NWIN][DT][K] floats
     int count_off;     // summary warps done per buffer [NB]
     int flag_off;      // abort flag
     int smem_bytes;
@@ -272,43 +407,43 @@ struct StreamGeom {
 
 template <class C, bool BWD>
 __host__ __device__ inline StreamGeom make_stream_geom() {
+    constexpr int K = C::K;
     StreamGeom g{};
     g.tile_bytes = C::W * C::DT * static_cast<int>(sizeof(typename C::St));
-    g.sstage_bytes = 2 * g.tile_bytes;
-    g.rstage_bytes = (BWD ? 3 : 2) * g.tile_bytes;
+    g.sstage_bytes = 2 * K * g.tile_bytes;
+    g.rstage_bytes = K * (BWD ? 3 : 2) * g.tile_bytes;
     g.rring_off = C::NW * C::S * g.sstage_bytes;
     g.bar_off = g.rring_off + C::NW * C::SR * g.rstage_bytes;
     const int nbar = C::NW * C::S + C::NW * C::SR + 2 * kStreamSlots + 3 * C::NB;
     g.ticket_off = g.bar_off + nbar * 8;
     g.tick_off = g.ticket_off + kStreamSlots * 4;
     g.map_off = (g.tick_off + C::NB * 4 + 15) / 16 * 16;
-    g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8;
-    g.entry_off = g.cmap_off + C::NB * C::DT * 8;
-    g.count_off = g.entry_off + C::NB * C::NWIN * C::DT * 4;
+    g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8 * K;
+    g.entry_off = g.cmap_off + C::NB * C::DT * 8 * K;
+    g.count_off = g.entry_off + C::NB * C::NWIN * C::DT * 4 * K;
     g.flag_off = g.count_off + C::NB * 4;
     g.smem_bytes = g.flag_off + 16;
     return g;
 }
 
-// Forward tiles: a, b (row t); output out (tm_o0), staged over b.  Backward
-// tiles: a one row late (a_{t+1}), out one row early (h_{t-1}), grad_out;
-// outputs grad_a (tm_o0, staged over h_{t-1}) and grad_b (tm_o1, staged over
-// grad_out).
+// One kernel for both directions and both element kinds (StreamPlanes lists
+// the planes).  Outputs overwrite the replay tile planes they were computed
+// from and leave by bulk tensor stores; `last` / `last_i` (forward, may be
+// NULL) receive the state after the final step.
 template <class C, bool BWD>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
-stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ CUtensorMap tm_1,
-                    const __grid_constant__ CUtensorMap tm_2, const __grid_constant__ CUtensorMap tm_o0,
-                    const __grid_constant__ CUtensorMap tm_o1, float *__restrict__ last, int T, int D,
-                    DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
+stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, float *__restrict__ last_i, int T,
+              int D, DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
     using St = typename C::St;
+    using PL = StreamPlanes<C, BWD>;
     constexpr int DT = C::DT, V = C::V, W = C::W, NW = C::NW, R = C::R, S = C::S, SR = C::SR, NSCAN = C::NSCAN;
-    constexpr int NB = C::NB;
+    constexpr int NB = C::NB, K = C::K;
     constexpr int NWIN = C::NWIN;
-    constexpr int NIN = BWD ? 3 : 2;
+    constexpr int NS = PL::NS, NIN = PL::NIN, NOUT = PL::NOUT;
     constexpr int SLOTS = kStreamSlots;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const StreamGeom geo = make_stream_geom<C, BWD>();
-    auto stile = [&](int st, int plane) {  // summary ring: plane 0 = a, 1 = b / grad_out
+    auto stile = [&](int st, int plane) {  // summary ring
         return reinterpret_cast<St *>(smem_raw + st * geo.sstage_bytes + plane * geo.tile_bytes);
     };
     auto rtile = [&](int st, int plane) {  // replay ring: planes in tensor-map order
@@ -326,9 +461,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
     auto buf_free = [&](int b) { return bar(BR + 2 * SLOTS + 2 * NB + b); };
     int *step_ticket = reinterpret_cast<int *>(smem_raw + geo.ticket_off);
     volatile int *tick_of = reinterpret_cast<volatile int *>(smem_raw + geo.tick_off);
-    float2 *wmap = reinterpret_cast<float2 *>(smem_raw + geo.map_off);
-    float2 *cmap = reinterpret_cast<float2 *>(smem_raw + geo.cmap_off);
-    float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off);
+    float *wmap = reinterpret_cast<float *>(smem_raw + geo.map_off);     // [NB][NWIN][DT][2K]
+    float *cmap = reinterpret_cast<float *>(smem_raw + geo.cmap_off);    // [NB][DT][2K]
+    float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off); // [NB][NWIN][DT][K]
     unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
     if (threadIdx.x == 0) {
@@ -355,7 +490,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     const int CH = NWIN * W;
     const long long total = static_cast<long long>(sa.ng) * sa.nc;
-    const CUtensorMap *const maps[3] = {&tm_0, &tm_1, &tm_2};
     // chunk coordinates of ticket t
     struct Chunk {
         int cc, gi, c, brow, x0;
@@ -410,11 +544,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
             const Chunk ch = decode(t);
             const int st = w * S + u % S;
             const uint32_t fb = sfull(st);
-            mbar_arrive_expect_tx(fb, 2 * geo.tile_bytes);
+            mbar_arrive_expect_tx(fb, NS * geo.tile_bytes);
             const int y = ch.c * CH + ((u % R) * NW + w) * W;
             const uint64_t keep = l2_evict_last_policy();
-            tma_load_3d_hint(smem_addr(stile(st, 0)), maps[0], ch.x0, y + (BWD ? 1 : 0), ch.brow, fb, keep);
-            tma_load_3d_hint(smem_addr(stile(st, 1)), maps[BWD ? 2 : 1], ch.x0, y, ch.brow, fb, keep);
+#pragma unroll
+            for (int p = 0; p < NS; ++p)
+                tma_load_3d_hint(smem_addr(stile(st, p)), &tm.in[PL::sum_map(p)], ch.x0, y + PL::sum_dy(p), ch.brow,
+                                 fb, keep);
         };
         auto drain = [&]() {
             if (lane != 0) return;
@@ -453,7 +589,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
             const int q1 = (k + 1) % SLOTS;
             int tn = -2;  // not read yet
             const Chunk ch = decode(tk);
-            float P[R][V], Q[R][V];
+            // window maps h -> P h + Q: P[r][v][0..K-1], Q[r][v][0..K-1]
+            float P[R][V][K], Q[R][V][K];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int u = k * R + r;
@@ -479,24 +616,59 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                     drain();
                     return;
                 }
-                const St *ta = stile(st, 0);
-                const St *tb = stile(st, 1);
                 // the window's map (rows past T are identity steps)
 #pragma unroll
-                for (int v = 0; v < V; ++v) { P[r][v] = 1.0f; Q[r][v] = 0.0f; }
-                for (int g8 = 0; g8 < nrows; g8 += 8) {
-                    const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
-                    float xa[8][V], xb[8][V];
-                    load8<St, V, DT>(ta, r0, lane, xa);
-                    load8<St, V, DT>(tb, r0, lane, xb);
+                for (int v = 0; v < V; ++v) {
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) {
-                        const int row = BWD ? 7 - rr : rr;
-                        if (r0 + row < nrows) {
+                    for (int q = 0; q < K; ++q) { P[r][v][q] = q == 0 ? 1.0f : 0.0f; Q[r][v][q] = 0.0f; }
+                }
+                if constexpr (!C::CPLX) {
+                    const St *ta = stile(st, 0);
+                    const St *tb = stile(st, 1);
+                    for (int g8 = 0; g8 < nrows; g8 += 8) {
+                        const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
+                        float xa[8][V], xb[8][V];
+                        load8<St, V, DT>(ta, r0, lane, xa);
+                        load8<St, V, DT>(tb, r0, lane, xb);
 #pragma unroll
-                            for (int v = 0; v < V; ++v) {
-                                P[r][v] = __fmul_rn(xa[row][v], P[r][v]);
-                                Q[r][v] = __fmaf_rn(xa[row][v], Q[r][v], xb[row][v]);
+                        for (int rr = 0; rr < 8; ++rr) {
+                            const int row = BWD ? 7 - rr : rr;
+                            if (r0 + row < nrows) {
+#pragma unroll
+                                for (int v = 0; v < V; ++v) {
+                                    P[r][v][0] = __fmul_rn(xa[row][v], P[r][v][0]);
+                                    Q[r][v][0] = __fmaf_rn(xa[row][v], Q[r][v][0], xb[row][v]);
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    // complex: planes a_r, a_i, b_r, b_i (backward: conj of a_{t+1}, grad_out)
+                    for (int g8 = 0; g8 < nrows; g8 += 8) {
+                        const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;
+                        float xr[8][V], xi[8][V], br[8][V], bi[8][V];
+                        load8<St, V, DT>(stile(st, 0), r0, lane, xr);
+                        load8<St, V, DT>(stile(st, 1), r0, lane, xi);
+                        load8<St, V, DT>(stile(st, 2), r0, lane, br);
+                        load8<St, V, DT>(stile(st, 3), r0, lane, bi);
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) {
+                            const int row = BWD ? 7 - rr : rr;
+                            if (r0 + row < nrows) {
+#pragma unroll
+                                for (int v = 0; v < V; ++v) {
+                                    float nPr, nPi, nQr, nQi;
+                                    if constexpr (BWD) {
+                                        cxc_step(xr[row][v], xi[row][v], P[r][v][0], P[r][v][1], 0.0f, 0.0f, nPr, nPi);
+                                        cxc_step(xr[row][v], xi[row][v], Q[r][v][0], Q[r][v][1], br[row][v],
+                                                 bi[row][v], nQr, nQi);
+                                    } else {
+                                        cx_step(xr[row][v], xi[row][v], P[r][v][0], P[r][v][1], 0.0f, 0.0f, nPr, nPi);
+                                        cx_step(xr[row][v], xi[row][v], Q[r][v][0], Q[r][v][1], br[row][v],
+                                                bi[row][v], nQr, nQi);
+                                    }
+                                    P[r][v][0] = nPr; P[r][v][1] = nPi; Q[r][v][0] = nQr; Q[r][v][1] = nQi;
+                                }
                             }
                         }
                     }
@@ -511,9 +683,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                float2 *mp = wmap + (b * NWIN + r * NW + w) * DT + lane * V;
+                float *mp = wmap + ((b * NWIN + r * NW + w) * DT + lane * V) * 2 * K;
 #pragma unroll
-                for (int v = 0; v < V; ++v) mp[v] = make_float2(P[r][v], Q[r][v]);
+                for (int v = 0; v < V; ++v) {
+#pragma unroll
+                    for (int q = 0; q < K; ++q) {
+                        mp[v * 2 * K + q] = P[r][v][q];
+                        mp[v * 2 * K + K + q] = Q[r][v][q];
+                    }
+                }
             }
             __syncwarp();
             unsigned int before = 0;
@@ -523,24 +701,42 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                 // the last summary warp of this chunk: compose the window maps in
                 // chain order and publish the chunk's map at once
                 __syncwarp();
-                const float2 *cm = wmap + b * NWIN * DT;
-                float Pc[V], Qc[V];
+                const float *cm = wmap + b * NWIN * DT * 2 * K;
+                float Pc[V][K], Qc[V][K];
 #pragma unroll
-                for (int v = 0; v < V; ++v) { Pc[v] = 1.0f; Qc[v] = 0.0f; }
+                for (int v = 0; v < V; ++v) {
+#pragma unroll
+                    for (int q = 0; q < K; ++q) { Pc[v][q] = q == 0 ? 1.0f : 0.0f; Qc[v][q] = 0.0f; }
+                }
                 for (int jw = 0; jw < NWIN; ++jw) {
                     const int ww = BWD ? NWIN - 1 - jw : jw;
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const float2 m = cm[ww * DT + lane * V + v];
-                        Qc[v] = __fmaf_rn(m.x, Qc[v], m.y);
-                        Pc[v] = __fmul_rn(m.x, Pc[v]);
+                        const float *m = cm + (ww * DT + lane * V + v) * 2 * K;
+                        if constexpr (!C::CPLX) {
+                            Qc[v][0] = __fmaf_rn(m[0], Qc[v][0], m[1]);
+                            Pc[v][0] = __fmul_rn(m[0], Pc[v][0]);
+                        } else {
+                            float nQr, nQi, nPr, nPi;
+                            cx_step(m[0], m[1], Qc[v][0], Qc[v][1], m[2], m[3], nQr, nQi);
+                            cx_step(m[0], m[1], Pc[v][0], Pc[v][1], 0.0f, 0.0f, nPr, nPi);
+                            Qc[v][0] = nQr; Qc[v][1] = nQi; Pc[v][0] = nPr; Pc[v][1] = nPi;
+                        }
                     }
                 }
                 const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    cmap[b * DT + lane * V + v] = make_float2(Pc[v], Qc[v]);
-                    publish_map(sa.agg + slot_g * DT + lane * V + v, Pc[v], Qc[v]);
+                    float *cp = cmap + (b * DT + lane * V + v) * 2 * K;
+#pragma unroll
+                    for (int q = 0; q < K; ++q) { cp[q] = Pc[v][q]; cp[K + q] = Qc[v][q]; }
+                    const size_t gidx = slot_g * DT + lane * V + v;
+                    if constexpr (!C::CPLX) {
+                        publish_map(sa.agg + gidx, Pc[v][0], Qc[v][0]);
+                    } else {
+                        publish_map(sa.agg + 2 * gidx, Pc[v][0], Pc[v][1]);
+                        publish_map(sa.agg + 2 * gidx + 1, Qc[v][0], Qc[v][1]);
+                    }
                 }
                 __syncwarp();  // every lane's cmap entries written before the maps_ready arrive
                 if (lane == 0) {
@@ -570,28 +766,49 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
             const int t = tick_of[b];
             if (t < 0) return;
             const Chunk ch = decode(t);
-            float Pc[V], Qc[V];
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float2 m = cmap[b * DT + i0 + v];
-                Pc[v] = m.x;
-                Qc[v] = m.y;
-            }
-            float h[V];
-            if (!stream_lookback<DT, V, 16 / V>(sa, ch.gi, ch.cc, i0, h, wc)) return;
+            float h[V][K];
             const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
+            if constexpr (!C::CPLX) {
+                float hin[V];
+                if (!stream_lookback<DT, V, 16 / V>(sa, ch.gi, ch.cc, i0, hin, wc)) return;
 #pragma unroll
-            for (int v = 0; v < V; ++v) publish_state(sa.incl + slot_g * DT + i0 + v, __fmaf_rn(Pc[v], h[v], Qc[v]));
+                for (int v = 0; v < V; ++v) {
+                    const float *cp = cmap + (b * DT + i0 + v) * 2;
+                    h[v][0] = hin[v];
+                    publish_state(sa.incl + slot_g * DT + i0 + v, __fmaf_rn(cp[0], hin[v], cp[1]));
+                }
+            } else {
+                float hr[V], hi[V];
+                if (!stream_lookback_cx<DT, V, 8 / V>(sa, ch.gi, ch.cc, i0, hr, hi, wc)) return;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float *cp = cmap + (b * DT + i0 + v) * 4;
+                    float lr, li;
+                    cx_step(cp[0], cp[1], hr[v], hi[v], cp[2], cp[3], lr, li);
+                    publish_map(reinterpret_cast<float2 *>(sa.incl) + slot_g * DT + i0 + v, lr, li);
+                    h[v][0] = hr[v];
+                    h[v][1] = hi[v];
+                }
+            }
             // the state entering every window, in chain order
-            const float2 *mp = wmap + b * NWIN * DT;
-            float *ep = wentry + b * NWIN * DT;
+            const float *mp = wmap + b * NWIN * DT * 2 * K;
+            float *ep = wentry + b * NWIN * DT * K;
             for (int jw = 0; jw < NWIN; ++jw) {
                 const int ww = BWD ? NWIN - 1 - jw : jw;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    ep[ww * DT + i0 + v] = h[v];
-                    const float2 m = mp[ww * DT + i0 + v];
-                    h[v] = __fmaf_rn(m.x, h[v], m.y);
+                    const float *m = mp + (ww * DT + i0 + v) * 2 * K;
+                    float *e = ep + (ww * DT + i0 + v) * K;
+#pragma unroll
+                    for (int q = 0; q < K; ++q) e[q] = h[v][q];
+                    if constexpr (!C::CPLX) {
+                        h[v][0] = __fmaf_rn(m[0], h[v][0], m[1]);
+                    } else {
+                        float nr, ni;
+                        cx_step(m[0], m[1], h[v][0], h[v][1], m[2], m[3], nr, ni);
+                        h[v][0] = nr;
+                        h[v][1] = ni;
+                    }
                 }
             }
             __syncwarp();
@@ -613,10 +830,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
         mbar_arrive_expect_tx(fb, NIN * geo.tile_bytes);
         const int y = ch.c * CH + ((u % R) * NW + w) * W;
 #pragma unroll
-        for (int i = 0; i < NIN; ++i) {
-            const int dy = BWD ? (i == 0 ? 1 : (i == 1 ? -1 : 0)) : 0;
-            tma_load_3d_hint(smem_addr(rtile(st, i)), maps[i], ch.x0, y + dy, ch.brow, fb, drop);
-        }
+        for (int p = 0; p < NIN; ++p)
+            tma_load_3d_hint(smem_addr(rtile(st, p)), &tm.in[p], ch.x0, y + PL::rep_dy(p), ch.brow, fb, drop);
     };
     auto drain = [&]() {
         if (lane != 0) return;
@@ -675,14 +890,17 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
             const int wi = r * NW + w;
             const int wbase = ch.c * CH + wi * W;
             const int nrows = min(max(T - wbase, 0), W);
-            St *ta = rtile(st, 0);
-            St *tb = rtile(st, NIN - 1);
-            float h[V];
-            const float *ep = wentry + (b * NWIN + wi) * DT + lane * V;
+            float h[V][K];
+            const float *ep = wentry + ((b * NWIN + wi) * DT + lane * V) * K;
 #pragma unroll
-            for (int v = 0; v < V; ++v) h[v] = ep[v];
-            if constexpr (!BWD) {
+            for (int v = 0; v < V; ++v) {
+#pragma unroll
+                for (int q = 0; q < K; ++q) h[v][q] = ep[v * K + q];
+            }
+            if constexpr (!C::CPLX && !BWD) {
                 // out_t over b_t in the tile (each lane rewrites what it read)
+                St *ta = rtile(st, 0);
+                St *tb = rtile(st, 1);
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     float xa[8][V], xb[8][V];
                     load8<St, V, DT>(ta, g8, lane, xa);
@@ -690,25 +908,18 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
                         if (g8 + rr < nrows) {
+                            float hv[V];
 #pragma unroll
-                            for (int v = 0; v < V; ++v) h[v] = __fmaf_rn(xa[rr][v], h[v], xb[rr][v]);
-                            store_lanes<St, V>(tb + (g8 + rr) * DT + lane * V, h);
+                            for (int v = 0; v < V; ++v) hv[v] = h[v][0] = __fmaf_rn(xa[rr][v], h[v][0], xb[rr][v]);
+                            store_lanes<St, V>(tb + (g8 + rr) * DT + lane * V, hv);
                         }
                     }
                 }
-                if (last != nullptr && d < D && nrows > 0 && wbase + nrows == T) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) last[static_cast<size_t>(ch.brow) * D + d + v] = h[v];
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d_hint(&tm_o0, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
-                    bulk_commit();
-                }
-            } else {
+            } else if constexpr (!C::CPLX) {
                 // grad_b_t over grad_out_t, grad_a_t over h_{t-1}
+                St *ta = rtile(st, 0);
                 St *th = rtile(st, 1);
+                St *tb = rtile(st, 2);
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     const int r0 = (nrows - 1 - g8) & ~7;
                     float xa[8][V], xh[8][V], xg[8][V];
@@ -719,24 +930,92 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_0, const __grid_constant__ 
                     for (int rr = 0; rr < 8; ++rr) {
                         const int row = 7 - rr;
                         if (r0 + row < nrows) {
-                            float gav[V];
+                            float gv[V], gav[V];
 #pragma unroll
                             for (int v = 0; v < V; ++v) {
-                                h[v] = __fmaf_rn(xa[row][v], h[v], xg[row][v]);
-                                gav[v] = __fmul_rn(h[v], xh[row][v]);
+                                gv[v] = h[v][0] = __fmaf_rn(xa[row][v], h[v][0], xg[row][v]);
+                                gav[v] = __fmul_rn(h[v][0], xh[row][v]);
                             }
-                            store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, h);
+                            store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, gv);
                             store_lanes<St, V>(th + (r0 + row) * DT + lane * V, gav);
                         }
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d_hint(&tm_o0, smem_addr(th), ch.x0, wbase, ch.brow, drop);
-                    tma_store_3d_hint(&tm_o1, smem_addr(tb), ch.x0, wbase, ch.brow, drop);
-                    bulk_commit();
+            } else if constexpr (!BWD) {
+                // complex: out_t over b_t (planes 2, 3)
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    float xr[8][V], xi[8][V], br[8][V], bi[8][V];
+                    load8<St, V, DT>(rtile(st, 0), g8, lane, xr);
+                    load8<St, V, DT>(rtile(st, 1), g8, lane, xi);
+                    load8<St, V, DT>(rtile(st, 2), g8, lane, br);
+                    load8<St, V, DT>(rtile(st, 3), g8, lane, bi);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        if (g8 + rr < nrows) {
+                            float or_[V], oi[V];
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                cx_step(xr[rr][v], xi[rr][v], h[v][0], h[v][1], br[rr][v], bi[rr][v], or_[v], oi[v]);
+                                h[v][0] = or_[v];
+                                h[v][1] = oi[v];
+                            }
+                            store_lanes<St, V>(rtile(st, 2) + (g8 + rr) * DT + lane * V, or_);
+                            store_lanes<St, V>(rtile(st, 3) + (g8 + rr) * DT + lane * V, oi);
+                        }
+                    }
                 }
+            } else {
+                // complex backward: g = conj(a_{t+1}) g + grad_out; grad_b = g over
+                // grad_out (planes 4, 5), grad_a = g conj(h_{t-1}) over out (2, 3)
+                for (int g8 = 0; g8 < nrows; g8 += 8) {
+                    const int r0 = (nrows - 1 - g8) & ~7;
+                    float xr[8][V], xi[8][V], hr[8][V], hi[8][V], gr[8][V], gi[8][V];
+                    load8<St, V, DT>(rtile(st, 0), r0, lane, xr);
+                    load8<St, V, DT>(rtile(st, 1), r0, lane, xi);
+                    load8<St, V, DT>(rtile(st, 2), r0, lane, hr);
+                    load8<St, V, DT>(rtile(st, 3), r0, lane, hi);
+                    load8<St, V, DT>(rtile(st, 4), r0, lane, gr);
+                    load8<St, V, DT>(rtile(st, 5), r0, lane, gi);
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int row = 7 - rr;
+                        if (r0 + row < nrows) {
+                            float ngr[V], ngi[V], gar[V], gai[V];
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                cxc_step(xr[row][v], xi[row][v], h[v][0], h[v][1], gr[row][v], gi[row][v], ngr[v],
+                                         ngi[v]);
+                                h[v][0] = ngr[v];
+                                h[v][1] = ngi[v];
+                                // g * conj(h_{t-1})
+                                gar[v] = __fmaf_rn(ngr[v], hr[row][v], __fmul_rn(ngi[v], hi[row][v]));
+                                gai[v] = __fmaf_rn(ngi[v], hr[row][v], -__fmul_rn(ngr[v], hi[row][v]));
+                            }
+                            const int o = (r0 + row) * DT + lane * V;
+                            store_lanes<St, V>(rtile(st, 4) + o, ngr);
+                            store_lanes<St, V>(rtile(st, 5) + o, ngi);
+                            store_lanes<St, V>(rtile(st, 2) + o, gar);
+                            store_lanes<St, V>(rtile(st, 3) + o, gai);
+                        }
+                    }
+                }
+            }
+            if constexpr (!BWD) {
+                if (last != nullptr && d < D && nrows > 0 && wbase + nrows == T) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        last[static_cast<size_t>(ch.brow) * D + d + v] = h[v][0];
+                        if constexpr (C::CPLX) last_i[static_cast<size_t>(ch.brow) * D + d + v] = h[v][1];
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o)
+                    tma_store_3d_hint(&tm.out[o], smem_addr(rtile(st, K + o)), ch.x0, wbase, ch.brow, drop);
+                bulk_commit();
             }
             __syncwarp();  // every lane done with the stage before it is refilled
             ++u_done;

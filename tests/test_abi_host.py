@@ -305,11 +305,14 @@ def test_every_tile_variant_is_whole_warps(lib):
 
 
 def test_complex_chunked_plans(lib):
-    """The complex scan's chunked path: automatic for few lanes and long
-    sequences (fewer than 0.45 lane tiles of 32 per SM), twice the real
-    path's scratch (re and im maps), flat or grouped prefix."""
-    p = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "fwd")
+    """The complex scan's chunked path: automatic for few lanes (fewer than
+    0.45 lane tiles of 32 per SM) and sequences too short to stream, or with
+    state or an asked-for chunk length; twice the real path's scratch (re and
+    im maps), flat or grouped prefix."""
+    p = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "fwd", chunk_len=64)
     assert p["path"] == "chunk" and p["name"] == "cchunk64_v4_grouped" and p["kernels"] == 5, p
+    assert L.lrscan_plan_complex(1, 8192, 64, "f32", "fwd")["path"] == "chunk"
+    assert L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", state=True)["path"] == "chunk"
     assert p["workspace_bytes"] == 2 * L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
     flat = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", path="chunk", tile_variant=1)
     assert flat["kernels"] == 3 and flat["workspace_bytes"] == 4 * 16384 * 64 * 4
@@ -321,6 +324,32 @@ def test_complex_chunked_plans(lib):
     for bad in (dict(chunk_len=48), dict(tile_variant=3)):
         with pytest.raises(L.LrscanError):
             L.lrscan_plan_complex(1, 4096, 64, "f32", "fwd", path="chunk", **bad)
+
+
+def test_complex_stream_plans(lib):
+    """The complex scan streams few-lane long sequences: 32-lane tiles (fp32
+    16-row windows, forward 256-step chunks, backward 128; bf16 32-row
+    windows, 512 and 256), and twice the real path's publication words (a
+    complex map is two 64-bit words, a state one)."""
+    pad = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for dt, rows, chunks in (("f32", 16, (256, 128)), ("bf16", 32, (512, 256))):
+        for direction, chunk in zip(("fwd", "bwd"), chunks):
+            B, T, D = 1, 1 << 20, 64
+            p = L.lrscan_plan_complex(B, T, D, dt, direction)
+            assert p["path"] == "stream" and p["name"] == f"cstream_{dt}_d32" and p["exact"] == 0, p
+            assert p["rows_per_window"] == rows and p["subchunks"] * rows == chunk and p["kernels"] == 1
+            assert p["threads_per_cta"] == 11 * 32 and p["smem_bytes"] <= 227 * 1024
+            ng, nc = 2, T // chunk
+            assert p["workspace_bytes"] == 256 + pad(ng * nc * 32 * 16) + pad(ng * nc * 32 * 8), p
+            assert p["ctas"] == min(ng * nc, 152)
+            q = L.lrscan_plan_complex(B, T, D, dt, direction, path="stream")
+            assert q["name"] == p["name"]
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=2)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
+    with pytest.raises(L.LrscanError):
+        L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
 
 
 def test_stream_plans(lib):

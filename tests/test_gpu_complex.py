@@ -83,6 +83,32 @@ def test_complex_every_variant(dt, shape):
     assert plan["path"] in ("seq", "window")
 
 
+STREAM_SHAPES = [(1, 1, 32), (1, 255, 32), (1, 257, 64), (3, 700, 32), (2, 3001, 96), (1, 5000, 64),
+                 (2, 40000, 32), (1, 9, 8)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", STREAM_SHAPES)
+def test_complex_stream_path(dt, shape):
+    """The persistent chunk-streaming kernel on the complex planes: ragged lane
+    tiles, partial chunks, one-step sequences, several chunks per lane group,
+    forward and backward against the oracle."""
+    B, T, D = shape
+    inp = make_complex_inputs(B, T, D, dt, seed=560 + T % 97)
+    plan, planb = check_complex(inp, dt, path="stream")
+    assert plan["path"] == "stream" and planb["path"] == "stream" and plan["name"].startswith("cstream_")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_stream_many_chunks_per_cta(dt):
+    """More chunk tickets than CTAs (two lane groups x 512 forward chunks of
+    512 steps), the automatic plan."""
+    B, T, D = 1, 1 << 18, 64
+    inp = make_complex_inputs(B, T, D, dt, seed=575)
+    plan, planb = check_complex(inp, dt)
+    assert plan["path"] == "stream" and planb["path"] == "stream" and plan["ctas"] < 2 * (T // 512)
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_complex_unaligned_takes_plain(dt):
     inp = make_complex_inputs(2, 90, 37, dt, seed=510)
@@ -116,8 +142,8 @@ def test_complex_chunked_path(dt, chunk):
 def test_complex_chunked_grouped_prefix_and_auto(dt):
     """Few lanes, long sequence (2,500 chunks of 16 per lane: five groups of
     512 maps, the last one ragged): the grouped prefix forced and as the
-    automatic choice, the flat prefix forced, and the automatic plan (64-step
-    chunks, flat) against the oracle."""
+    automatic choice of the chunked path, the flat prefix forced, and the
+    automatic plan (chunk streaming) against the oracle."""
     B, T, D = 1, 40000, 8
     inp = make_complex_inputs(B, T, D, dt, seed=550)
     plan, planb = check_complex(inp, dt, path="chunk", chunk_len=16, tile_variant=2)
@@ -125,7 +151,7 @@ def test_complex_chunked_grouped_prefix_and_auto(dt):
     assert L.lrscan_plan_complex(B, T, D, dt, "fwd", path="chunk", chunk_len=16)["name"].endswith("_grouped")
     check_complex(inp, dt, path="chunk", chunk_len=16, tile_variant=1)
     plan, planb = check_complex(inp, dt)
-    assert plan["path"] == "chunk" and planb["path"] == "chunk"
+    assert plan["path"] == "stream" and planb["path"] == "stream"
 
 
 def test_complex_chunked_unaligned_rows():
