@@ -4,6 +4,7 @@
 #include <cstdlib>
 
 #include "gated_kernels.cuh"
+#include "gated_pipe_kernels.cuh"
 #include "window_launch.cuh"
 
 namespace lrscan {
@@ -71,6 +72,42 @@ int launch_gwin_bwd(const WinLaunch &L, const WinDirCfg &cfg) {
     return e == cudaSuccess ? 0 : -1;
 }
 
+template <class C>
+int launch_gpipe_fwd(const WinLaunch &L, const WinDirCfg &) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gpipe_fwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const GPipeGeom g = make_gpipe_geom<C>();
+    const int ndt = static_cast<int>((L.D + C::DT - 1) / C::DT);
+    const cudaError_t e = launch_pdl(fn, dim3(ndt, static_cast<unsigned>(L.B)), dim3(C::THREADS), g.smem_bytes,
+                                     L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, L.last, static_cast<int>(L.T),
+                                     static_cast<int>(L.D), L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+// Forward with warp roles (gated_pipe_kernels.cuh): W-row windows, one lane per
+// thread, a ring of NST b tiles.
+template <class C>
+WinDirCfg gpdir_cfg() {
+    const GPipeGeom g = make_gpipe_geom<C>();
+    WinDirCfg d{};
+    d.dt = C::DT;
+    d.v = 1;
+    d.l = C::W;
+    d.s = 1;
+    d.lane_scan = 1;
+    d.exact = 0;
+    d.w = C::W;
+    d.nstage = C::NST;
+    d.threads = C::THREADS;
+    d.smem = g.smem_bytes;
+    d.stage_bytes = g.tile_bytes;
+    d.max_resident = C::MINB;
+    d.launch = &launch_gpipe_fwd<C>;
+    return d;
+}
+
 template <class C, bool FWD>
 WinDirCfg gdir_cfg(int nstage) {
     static_assert(C::NIN == (FWD ? 1 : 2), "generated-decay planes: b forward; out and grad_out backward");
@@ -131,6 +168,12 @@ using GWB_BF_32_2_8_M4 = WinShape<bf16_t, 32, 2, 8, 2, 160, 4, false>;
 using GWB_BF_32_2_8_M5 = WinShape<bf16_t, 32, 2, 8, 2, 160, 5, false>;
 using GWB_FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 288, 2, false>;
 
+// GPipeShape<St, W, NS, NR, NST, NM, MINB>: two summary and three replay warps
+// on 16-row windows, twelve ring stages, eight window slots, five CTAs per SM
+// (fp32 only: with bf16 rows the warp handoffs per window, not the bytes, set
+// the time).
+using GP_FF_16 = GPipeShape<float, 16, 2, 3, 12, 8, 5>;
+
 #define F(SH, N) gdir_cfg<SH, true>(N)
 #define B(SH, N) gdir_cfg<SH, false>(N)
 #define FW(SH, S, N) gwdir_cfg<SH, true>(S, N)
@@ -147,6 +190,7 @@ const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
     {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
     {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), BW(GWB_FF_16_1_8, 16, 2)},
+    {"gpipe_f32_w16", gpdir_cfg<GP_FF_16>(), BW(GWB_FF_16_1_8, 16, 2)},
 };
 #undef FW
 #undef BW

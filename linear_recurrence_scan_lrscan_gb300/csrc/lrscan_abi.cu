@@ -1235,6 +1235,10 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
+    } else if (dtype == LRSCAN_F32 && dir == 0 && B * ((D + 31) / 32) >= 4LL * g.sm_count &&
+               (vi = find_variant(tab, n, "gpipe_f32_w16", dir, B, D, g)) >= 0) {
+        // fp32 forward from four 32-lane tiles per SM: the tile with warp roles
+        // (61.9 us on B=8 T=2048 D=2560 fp32 against 65.9 us for the windowed tile)
     } else if ((vi = find_variant(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8", dir, B, D,
                                   g)) >= 0) {
         // the windowed tiles (time split inside the CTA): the measured fastest in both
