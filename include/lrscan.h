@@ -443,8 +443,10 @@ int lrscan_num_variants(int path, int dtype, int dir);
  * CUDA error as LRSCAN_ECUDA, else LRSCAN_OK. */
 int lrscan_sync_check(void);
 
-/* Limit on every bounded device-side wait, in nanoseconds (default 1e9).
- * Applies to launches made after the call, on every device. */
+/* Limit on every bounded device-side wait, in nanoseconds (default 1e9; at
+ * least 1e6, else LRSCAN_EINVAL: the kernels also bound their drains of their
+ * own bulk copies with it).  Applies to launches made after the call, on every
+ * device. */
 int lrscan_set_wait_timeout_ns(uint64_t ns);
 
 /* Self-test of the bounded wait: launches one CTA that waits, with the given

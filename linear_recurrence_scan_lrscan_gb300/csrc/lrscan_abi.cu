@@ -1699,7 +1699,11 @@ int lrscan_sync_check(void) {
 }
 
 int lrscan_set_wait_timeout_ns(uint64_t ns) {
-    if (ns == 0) return LRSCAN_EINVAL;
+    // The same limit bounds the waits with which a kernel drains its own bulk
+    // copies before it exits: those land within microseconds, and a limit that
+    // gave up before they did would let a CTA leave with copies still writing
+    // into its shared memory.
+    if (ns < 1000000ull) return fail(LRSCAN_EINVAL, "wait limit %llu ns is under 1 ms", static_cast<unsigned long long>(ns));
     g_timeout_ns.store(ns);
     return LRSCAN_OK;
 }

@@ -67,6 +67,15 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert lib.lrscan_bwd(p, p, p, p, p, 1, 8, 8, 3) == L.LRSCAN_EDTYPE
 
 
+def test_wait_limit_has_a_floor(lib):
+    """The device wait limit also bounds the kernels' drains of their own bulk
+    copies, so limits under 1 ms are refused; the default (1 s) is restored."""
+    assert lib.lrscan_set_wait_timeout_ns(0) == L.LRSCAN_EINVAL
+    assert lib.lrscan_set_wait_timeout_ns(999_999) == L.LRSCAN_EINVAL
+    assert lib.lrscan_set_wait_timeout_ns(1_000_000) == L.LRSCAN_OK
+    assert lib.lrscan_set_wait_timeout_ns(1_000_000_000) == L.LRSCAN_OK
+
+
 def test_empty_problems_are_noops(lib):
     # B == 0 or D == 0: nothing to do, NULL pointers allowed, no device needed
     assert _fwd(lib, None, None, None, None, 0, 8, 8, 0) == L.LRSCAN_OK
