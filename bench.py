@@ -588,6 +588,7 @@ def run_extensions(args, dev, peak) -> dict:
     torch.cuda.empty_cache()
     return {"complex": run_complex(iters, dev, peak), "complex_long_t": run_complex_long_t(dev, peak),
             "generated_decay": run_gated(iters, dev, peak),
+            "generated_decay_fp32": run_gated(iters, dev, peak, "f32"),
             "long_t": run_long_t(dev, peak), "state": {
         "workload": w.describe(),
         "what": "carried state: h0 in, segment resets (int32 positions, ~1 start per 512 tokens), "
@@ -733,19 +734,20 @@ def run_complex_long_t(dev, peak) -> dict:
     return res
 
 
-def run_gated(iters: int, dev, peak) -> dict:
+def run_gated(iters: int, dev, peak, dtype=None) -> dict:
     """The scan with decays generated in the kernel (exp(-exp(nu_log_d) exp(eta_t)))
-    on the gated workload's shape, three rotating buffer sets.  Forward moves b
-    in and out out (2 elements per (t, d)) plus eta, nu_log and the fp32 final
-    state; backward moves out, grad_out in and grad_b out (3 elements) plus
-    eta, nu_log in and grad_eta, grad_nu_log out."""
+    on the gated workload's shape (its bf16 storage, or `dtype`), three rotating
+    buffer sets.  Forward moves b in and out out (2 elements per (t, d)) plus
+    eta, nu_log and the fp32 final state; backward moves out, grad_out in and
+    grad_b out (3 elements) plus eta, nu_log in and grad_eta, grad_nu_log out."""
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
     from linear_recurrence_scan_lrscan_gb300.workloads import GATED_WORKLOAD as gw
     from linear_recurrence_scan_lrscan_gb300.workloads import make_gated_inputs
     stream = torch.cuda.current_stream()
-    host = make_gated_inputs()
+    dtype = dtype or gw.dtype
+    host = make_gated_inputs(dtype=dtype)
     sets = []
     for _ in range(3):
         st = {k: host[k].to(dev) for k in ("eta", "nu_log", "b", "grad_out")}
@@ -766,14 +768,16 @@ def run_gated(iters: int, dev, peak) -> dict:
     bms = time_launches(bwd, iters, stream)
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the generated-decay scan")
-    B, T, D, E, s = gw.B, gw.T, gw.D, gw.elements, gw.storage_bytes
+    B, T, D, E = gw.B, gw.T, gw.D, gw.elements
+    s = 4 if dtype == "f32" else 2
     fb = 2 * E * s + 4 * B * T + 4 * D + 4 * B * D
     bb = 3 * E * s + 2 * (4 * B * T + 4 * D)
-    pf = L.lrscan_plan_gated(B, T, D, gw.dtype, "fwd")
-    pb = L.lrscan_plan_gated(B, T, D, gw.dtype, "bwd")
+    pf = L.lrscan_plan_gated(B, T, D, dtype, "fwd")
+    pb = L.lrscan_plan_gated(B, T, D, dtype, "bwd")
     del sets
     torch.cuda.empty_cache()
-    return {"workload": gw.describe() + " with decays generated from eta [B,T] and nu_log [D]",
+    desc = gw.describe() if dtype == gw.dtype else f"B={B} T={T} D={D} {dtype}"
+    return {"workload": desc + " with decays generated from eta [B,T] and nu_log [D]",
             "launches_per_direction": 3 * iters, "timing": "median of 3 samples",
             "fwd": {"ms": fms, "GB/s": fb / (fms * 1e-3) / 1e9, "frac": fb / (fms * 1e-3) / 1e9 / peak,
                     "algorithmic_bytes": fb, "kernel": pf["name"]},
