@@ -78,8 +78,9 @@ extern "C" {
                                   chunks of 256 to 1024 steps in ticket order; its summary warps publish each
                                   chunk's map, a scan warp finds the entering state by looking back over the
                                   published maps and leaving states, and its replay warps run the chunk again
-                                  while its tiles are still in L2.  Bulk-copy path (16-byte aligned rows); plain
-                                  scan only (no carried state); needs workspace_bytes of device scratch like the
+                                  while its tiles are still in L2.  Bulk-copy path (16-byte aligned rows); carries
+                                  state and resets (lrscan_fwd_state / lrscan_bwd_state; the complex scan: none); needs
+                                  workspace_bytes of device scratch like the
                                   chunked path; agrees with the sequential definition to rounding, and two calls
                                   may differ in the last bits (which published states a look-back composes depends
                                   on timing).  tile_variant: fp32 1 = 32-lane tiles (forward 512-step chunks,

@@ -10,11 +10,11 @@ namespace lrscan {
 
 namespace {
 
-template <class C, bool BWD>
+template <class C, bool BWD, bool EXT>
 int launch_stream(const WinLaunch &L, const WinDirCfg &) {
     static unsigned long long mask = 0;
     static std::mutex mu;
-    auto fn = stream_kernel<C, BWD>;
+    auto fn = stream_kernel<C, BWD, EXT>;
     if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
     if (L.grid <= 0) return -1;
     const StreamGeom g = make_stream_geom<C, BWD>();
@@ -25,7 +25,7 @@ int launch_stream(const WinLaunch &L, const WinDirCfg &) {
     for (int i = 0; i < PL::NOUT; ++i) m.out[i] = *L.maps[6 + i];
     const cudaError_t e = launch_pdl(fn, dim3(static_cast<unsigned>(L.grid)), dim3(C::THREADS), g.smem_bytes,
                                      L.stream, m, L.last, L.last_i, static_cast<int>(L.T), static_cast<int>(L.D),
-                                     L.status, L.timeout_ns, L.sa);
+                                     L.status, L.timeout_ns, L.sa, L.sx);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -47,8 +47,10 @@ WinDirCfg stream_cfg() {
     d.smem = g.smem_bytes;
     d.stage_bytes = g.rstage_bytes;
     d.max_resident = 1;
-    d.launch = &launch_stream<C, !FWD>;
-    d.launch_state = nullptr;
+    d.launch = &launch_stream<C, !FWD, false>;
+    // carried state and resets: the real scan's kernels
+    if constexpr (C::CPLX) d.launch_state = nullptr;
+    else d.launch_state = &launch_stream<C, !FWD, true>;
     return d;
 }
 

@@ -378,8 +378,7 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
 
     int path = want;
     if (want < kPathAuto || want > kPathStream) return fail(LRSCAN_EINVAL, "unknown path %d", want);
-    if (path == kPathStream && ext)
-        return fail(LRSCAN_EINVAL, "the chunk-streaming path carries no state or resets");
+
     if ((path == kPathSeq || path == kPathWindow || path == kPathStream) && !aligned16)
         return fail(LRSCAN_EINVAL, "path %d needs 16-byte aligned pointers and rows (D*elem %% 16 == 0)", path);
     int auto_vi = -1;
@@ -398,7 +397,7 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
             // else (or with a chunk length asked for) in three chunked phases
             path = kPathChunk;
             const bool long_seq = T >= 32LL * 512;
-            if (!ext && long_seq && !(opts && opts->chunk_len)) path = kPathStream;
+            if (long_seq && !(opts && opts->chunk_len)) path = kPathStream;
         } else {
             path = kPathSeq;  // small problem: latency-bound whatever runs it
         }
@@ -676,7 +675,7 @@ int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_
 // all-ones), one launch.
 int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::initializer_list<void *> outs,
                float *last, float *last_i, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev,
-               DeviceCtx *ctx, const lrscan_opts *opts, bool bwd, bool cplx) {
+               DeviceCtx *ctx, const lrscan_opts *opts, bool bwd, bool cplx, const StateArgs *sx = nullptr) {
     const WinDirCfg &v = dir_of(*ch.var, bwd ? 1 : 0);
     const int64_t ndt = (D + v.dt - 1) / v.dt;
     const int64_t ng = B * ndt;
@@ -719,7 +718,8 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
         cudaGetLastError();
         return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
     }
-    if (v.launch(L, v))
+    if (sx) L.sx = *sx;
+    if ((sx ? v.launch_state : v.launch)(L, v))
         return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
     return LRSCAN_OK;
 }
@@ -770,8 +770,11 @@ int run_fwd(const void *a, const void *b, void *out, float *last, int64_t B, int
         }
         return LRSCAN_OK;
     }
-    if (ch.path == kPathStream)
-        return run_stream(ch, {a, b}, {out}, last, nullptr, B, T, D, dtype, st, dev, ctx, opts, false, false);
+    if (ch.path == kPathStream) {
+        const StateArgs sx = state_slice(ext ? state : nullptr, false, a, 0, T, D, es);
+        return run_stream(ch, {a, b}, {out}, last, nullptr, B, T, D, dtype, st, dev, ctx, opts, false, false,
+                          ext ? &sx : nullptr);
+    }
     ChunkLaunch L{};
     L.in0 = a; L.in1 = b; L.out0 = out; L.last = last;
     L.B = B; L.T = T; L.D = D;
@@ -835,9 +838,11 @@ int run_bwd(const void *a, const void *out, const void *grad_out, void *grad_a, 
         }
         return LRSCAN_OK;
     }
-    if (ch.path == kPathStream)
+    if (ch.path == kPathStream) {
+        const StateArgs sx = state_slice(ext ? state : nullptr, true, a, 0, T, D, es);
         return run_stream(ch, {a, out, grad_out}, {grad_a, grad_b}, nullptr, nullptr, B, T, D, dtype, st, dev, ctx, opts,
-                          true, false);
+                          true, false, ext ? &sx : nullptr);
+    }
     ChunkLaunch L{};
     L.in0 = a; L.in1 = out; L.in2 = grad_out; L.out0 = grad_a; L.out1 = grad_b;
     L.B = B; L.T = T; L.D = D;

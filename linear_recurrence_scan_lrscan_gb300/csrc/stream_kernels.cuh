@@ -41,6 +41,7 @@
 #pragma once
 
 #include "scan_common.cuh"
+#include "state_args.h"
 #include "stream_args.h"
 
 namespace lrscan {
@@ -149,10 +150,13 @@ __device__ __forceinline__ uint32_t peek_state(const float *p) {
 // L2 round trip), folds maps in until it meets a published leaving state
 // (done) or a chunk with nothing out yet (read again next round).  Maps are
 // composed outermost first: h_in = M_cc-1 o M_cc-2 o ... (h_state); chunk -1
-// leaves the zero state.  Returns false when the wait expired or the CTA is
+// leaves the zero state, or with START the state at h_start[0 .. V-1]
+// (carried state: h0 forward, grad_last backward; null: zeros), read only by a
+// walk that gets there.  Returns false when the wait expired or the CTA is
 // aborting.
-template <int DT, int V, int BATCH>
-__device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, float (&h_in)[V], const WaitCtx &wc) {
+template <int DT, int V, int BATCH, bool START = false>
+__device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, float (&h_in)[V], const WaitCtx &wc,
+                                const float *h_start = nullptr) {
     const int lane = threadIdx.x & 31;
     const size_t g0 = static_cast<size_t>(gi) * sa.nc;
     float aP[V], aQ[V];
@@ -184,7 +188,12 @@ __device__ bool stream_lookback(const StreamArgs &sa, int gi, int cc, int i0, fl
                 if (go) {
                     if (j - t < 0) {
 #pragma unroll
-                        for (int v = 0; v < V; ++v) h_in[v] = aQ[v];  // aP * 0 + aQ
+                        for (int v = 0; v < V; ++v) {
+                            if constexpr (START)
+                                h_in[v] = h_start != nullptr ? __fmaf_rn(aP[v], h_start[v], aQ[v]) : aQ[v];
+                            else
+                                h_in[v] = aQ[v];  // aP * 0 + aQ
+                        }
                         done = true;
                         go = false;
                     } else {
@@ -336,6 +345,34 @@ __device__ bool stream_lookback_cx(const StreamArgs &sa, int gi, int cc, int i0,
     }
 }
 
+// Segment positions of rows t0 .. t0+NR-1 of batch row brow, lane l holding
+// rows l, 32 + l, ...: loaded ahead of their use (rows outside [0, T) read as
+// 1, no reset).
+template <int NR>
+struct SegRows {
+    static constexpr int N = (NR + 31) / 32;
+    int v[N];
+    __device__ __forceinline__ void load(const int32_t *seg, int brow, int T, int t0, int lane) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int r = i * 32 + lane;
+            const int t = t0 + r;
+            v[i] = (r < NR && t >= 0 && t < T) ? __ldg(seg + static_cast<size_t>(brow) * T + t) : 1;
+        }
+    }
+    // bit r of the result for row r < 64 (the whole warp calls it); row 64, if
+    // any, in *row64
+    __device__ __forceinline__ uint64_t bits(bool *row64) const {
+        uint64_t m = 0;
+#pragma unroll
+        for (int i = 0; i < N && i < 2; ++i)
+            m |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, v[i] == 0)) << (32 * i);
+        if constexpr (N > 2) *row64 = __ballot_sync(0xffffffffu, v[2] == 0) & 1u;
+        else *row64 = false;
+        return m;
+    }
+};
+
 // Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
 // window, summary (= replay) warps, windows per warp and chunk, summary and
 // replay stages per warp, scan warps, chunk buffers, complex scan (re / im
@@ -400,6 +437,7 @@ struct StreamGeom {
     int map_off;       // window maps [NB][NWIN][DT][2K] floats (P, Q)
     int cmap_off;      // chunk maps [NB][DT][2K] floats
     int entry_off;     // window entering states [NB][NWIN][DT][K] floats
+    int mask_off;      // carried-state calls: window reset masks [NB][NWIN][2] (step t, step t+1)
     int count_off;     // summary warps done per buffer [NB]
     int flag_off;      // abort flag
     int smem_bytes;
@@ -420,7 +458,8 @@ __host__ __device__ inline StreamGeom make_stream_geom() {
     g.map_off = (g.tick_off + C::NB * 4 + 15) / 16 * 16;
     g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8 * K;
     g.entry_off = g.cmap_off + C::NB * C::DT * 8 * K;
-    g.count_off = g.entry_off + C::NB * C::NWIN * C::DT * 4 * K;
+    g.mask_off = g.entry_off + C::NB * C::NWIN * C::DT * 4 * K;
+    g.count_off = g.mask_off + C::NB * C::NWIN * 16;
     g.flag_off = g.count_off + C::NB * 4;
     g.smem_bytes = g.flag_off + 16;
     return g;
@@ -429,11 +468,18 @@ __host__ __device__ inline StreamGeom make_stream_geom() {
 // One kernel for both directions and both element kinds (StreamPlanes lists
 // the planes).  Outputs overwrite the replay tile planes they were computed
 // from and leave by bulk tensor stores; `last` / `last_i` (forward, may be
-// NULL) receive the state after the final step.
-template <class C, bool BWD>
+// NULL) receive the state after the final step.  EXT (real scan): carried
+// state and segment resets as in the tiled kernels -- a_t = 0 where
+// segment_pos is 0 (backward: a_{t+1} = 0 where step t+1 resets, 1 past the
+// end, where grad_last enters), the chain started from h0 (forward) or
+// grad_last (backward), out_{-1} = h0 in grad_a, grad_a = +0 at a reset, and
+// grad_h0 = a'_0 * g_0 from the window holding step 0.
+template <class C, bool BWD, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, float *__restrict__ last_i, int T,
-              int D, DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa) {
+              int D, DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa,
+              const __grid_constant__ StateArgs sx) {
+    static_assert(!EXT || !C::CPLX, "carried state on the real scan");
     using St = typename C::St;
     using PL = StreamPlanes<C, BWD>;
     constexpr int DT = C::DT, V = C::V, W = C::W, NW = C::NW, R = C::R, S = C::S, SR = C::SR, NSCAN = C::NSCAN;
@@ -464,6 +510,7 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
     float *wmap = reinterpret_cast<float *>(smem_raw + geo.map_off);     // [NB][NWIN][DT][2K]
     float *cmap = reinterpret_cast<float *>(smem_raw + geo.cmap_off);    // [NB][DT][2K]
     float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off); // [NB][NWIN][DT][K]
+    [[maybe_unused]] uint64_t *wmask = reinterpret_cast<uint64_t *>(smem_raw + geo.mask_off);  // [NB][NWIN][2]
     unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
     if (threadIdx.x == 0) {
@@ -558,6 +605,10 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
         };
         if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
         int tk = step_ticket[0];
+        // carried-state calls: segment positions of the current tile's rows and,
+        // loaded one tile ahead, of the next (backward: one row more, for a_{t+1})
+        [[maybe_unused]] SegRows<W + (BWD ? 1 : 0)> segc, segn;
+        [[maybe_unused]] bool seg_next = false;
         for (int k = 0;; ++k) {
             const int b = k % NB;
             if (tk < 0) {
@@ -591,6 +642,8 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
             const Chunk ch = decode(tk);
             // window maps h -> P h + Q: P[r][v][0..K-1], Q[r][v][0..K-1]
             float P[R][V][K], Q[R][V][K];
+            // carried-state calls: each window's resets at step t and at step t+1
+            [[maybe_unused]] uint64_t mcur[R], mnext[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int u = k * R + r;
@@ -612,6 +665,18 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 const int wbase = ch.c * CH + (r * NW + w) * W;
                 const int nrows = min(max(T - wbase, 0), W);
                 const int st = w * S + u % S;
+                if constexpr (EXT) {
+                    if (sx.seg != nullptr) {
+                        if (seg_next) segc = segn;
+                        else segc.load(sx.seg, ch.brow, T, wbase, lane);
+                        seg_next = false;
+                        if (u + 1 < u_iss) {  // the next tile is out: its ticket is known and valid
+                            const Chunk c1 = decode((u + 1) / R == k ? tk : tn);
+                            segn.load(sx.seg, c1.brow, T, c1.c * CH + (((u + 1) % R) * NW + w) * W, lane);
+                            seg_next = true;
+                        }
+                    }
+                }
                 if (!warp_wait(sfull(st), static_cast<uint32_t>((u / S) & 1), wc, kSiteConsumerFull)) {
                     drain();
                     return;
@@ -625,11 +690,41 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 if constexpr (!C::CPLX) {
                     const St *ta = stile(st, 0);
                     const St *tb = stile(st, 1);
+                    // resets of the decays this window uses (backward: a_{t+1})
+                    [[maybe_unused]] uint64_t rbits = 0;
+                    if constexpr (EXT) {
+                        uint64_t rc = 0, rn = 0;
+                        if (sx.seg != nullptr) {
+                            bool row64 = false;
+                            const uint64_t full = segc.bits(&row64);
+                            if constexpr (BWD) {
+                                rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
+                                rn = (full >> 1) | (static_cast<uint64_t>(row64) << 63);
+                            } else {
+                                rc = full;
+                            }
+                        }
+                        mcur[r] = rc;
+                        mnext[r] = rn;
+                        rbits = BWD ? rn : rc;
+                    }
                     for (int g8 = 0; g8 < nrows; g8 += 8) {
                         const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
                         float xa[8][V], xb[8][V];
                         load8<St, V, DT>(ta, r0, lane, xa);
                         load8<St, V, DT>(tb, r0, lane, xb);
+                        if constexpr (EXT) {
+                            // the group's resets (0) and, backward, its row past
+                            // the end (a'_T = 1), as selects ahead of the chain
+                            const uint32_t m8 = static_cast<uint32_t>(rbits >> r0) & 0xffu;
+                            const int pe = BWD ? T - 1 - (wbase + r0) : -1;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                                for (int v = 0; v < V; ++v)
+                                    xa[q][v] = q == pe ? 1.0f : (((m8 >> q) & 1u) ? 0.0f : xa[q][v]);
+                            }
+                        }
 #pragma unroll
                         for (int rr = 0; rr < 8; ++rr) {
                             const int row = BWD ? 7 - rr : rr;
@@ -680,6 +775,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
             if (k >= NB && !warp_wait(buf_free(b), static_cast<uint32_t>(((k / NB) - 1) & 1), wc, kSiteStreamStep)) {
                 drain();
                 return;
+            }
+            if constexpr (EXT) {
+                if (lane == 0) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        wmask[(b * NWIN + r * NW + w) * 2] = mcur[r];
+                        wmask[(b * NWIN + r * NW + w) * 2 + 1] = mnext[r];
+                    }
+                }
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -770,7 +874,14 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
             const size_t slot_g = static_cast<size_t>(ch.gi) * sa.nc + ch.cc;
             if constexpr (!C::CPLX) {
                 float hin[V];
-                if (!stream_lookback<DT, V, 16 / V>(sa, ch.gi, ch.cc, i0, hin, wc)) return;
+                // the chain's start: h0 forward, grad_last backward (lanes past D
+                // read none: their results are clipped)
+                const float *st0 = nullptr;
+                if constexpr (EXT) {
+                    const float *s0 = BWD ? sx.grad_last : sx.h0;
+                    if (s0 != nullptr && ch.x0 + i0 < D) st0 = s0 + static_cast<size_t>(ch.brow) * D + ch.x0 + i0;
+                }
+                if (!stream_lookback<DT, V, 16 / V, EXT>(sa, ch.gi, ch.cc, i0, hin, wc, st0)) return;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const float *cp = cmap + (b * DT + i0 + v) * 2;
@@ -901,10 +1012,20 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 // out_t over b_t in the tile (each lane rewrites what it read)
                 St *ta = rtile(st, 0);
                 St *tb = rtile(st, 1);
+                [[maybe_unused]] uint64_t rbits = 0;
+                if constexpr (EXT) rbits = wmask[(b * NWIN + wi) * 2];
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     float xa[8][V], xb[8][V];
                     load8<St, V, DT>(ta, g8, lane, xa);
                     load8<St, V, DT>(tb, g8, lane, xb);
+                    if constexpr (EXT) {
+                        const uint32_t m8 = static_cast<uint32_t>(rbits >> g8) & 0xffu;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) xa[q][v] = ((m8 >> q) & 1u) ? 0.0f : xa[q][v];
+                        }
+                    }
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
                         if (g8 + rr < nrows) {
@@ -920,12 +1041,44 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 St *ta = rtile(st, 0);
                 St *th = rtile(st, 1);
                 St *tb = rtile(st, 2);
+                // EXT: resets of a_{t+1} (rnext) and of step t itself (rcur), and
+                // out_{-1} = h0
+                [[maybe_unused]] uint64_t rnext = 0, rcur = 0;
+                [[maybe_unused]] float h0v[V];
+                if constexpr (EXT) {
+                    rcur = wmask[(b * NWIN + wi) * 2];
+                    rnext = wmask[(b * NWIN + wi) * 2 + 1];
+#pragma unroll
+                    for (int v = 0; v < V; ++v)  // out_{-1} = h0: read by the window holding step 0 only
+                        h0v[v] = (wbase == 0 && sx.h0 != nullptr && d + v < D)
+                                     ? sx.h0[static_cast<size_t>(ch.brow) * D + d + v]
+                                     : 0.0f;
+                }
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     const int r0 = (nrows - 1 - g8) & ~7;
                     float xa[8][V], xh[8][V], xg[8][V];
                     load8<St, V, DT>(ta, r0, lane, xa);
                     load8<St, V, DT>(th, r0, lane, xh);
                     load8<St, V, DT>(tb, r0, lane, xg);
+                    [[maybe_unused]] uint32_t zmask = 0;  // rows whose grad_a is +0 (resets)
+                    if constexpr (EXT) {
+                        // the group's resets of a_{t+1} (0), the row past the end
+                        // (a'_T = 1: grad_last enters there), out_{-1} = h0, as
+                        // selects ahead of the chain
+                        const uint32_t mn = static_cast<uint32_t>(rnext >> r0) & 0xffu;
+                        zmask = static_cast<uint32_t>(rcur >> r0) & 0xffu;
+                        const int pe = T - 1 - (wbase + r0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v)
+                                xa[q][v] = q == pe ? 1.0f : (((mn >> q) & 1u) ? 0.0f : xa[q][v]);
+                        }
+                        if (wbase + r0 == 0) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) xh[0][v] = h0v[v];
+                        }
+                    }
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
                         const int row = 7 - rr;
@@ -935,10 +1088,23 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                             for (int v = 0; v < V; ++v) {
                                 gv[v] = h[v][0] = __fmaf_rn(xa[row][v], h[v][0], xg[row][v]);
                                 gav[v] = __fmul_rn(h[v][0], xh[row][v]);
+                                if constexpr (EXT) gav[v] = ((zmask >> row) & 1u) ? 0.0f : gav[v];
                             }
                             store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, gv);
                             store_lanes<St, V>(th + (r0 + row) * DT + lane * V, gav);
                         }
+                    }
+                }
+                if constexpr (EXT) {
+                    // grad_h0 = a'_0 * g_0 from the window holding step 0 (h holds g_0)
+                    if (sx.grad_h0 != nullptr && wbase == 0 && d < D) {
+                        float a0[V];
+                        unpack_lanes<St, V>(static_cast<const St *>(sx.a) + static_cast<size_t>(ch.brow) * T * D + d,
+                                            a0);
+#pragma unroll
+                        for (int v = 0; v < V; ++v)
+                            sx.grad_h0[static_cast<size_t>(ch.brow) * D + d + v] =
+                                (rcur & 1) ? 0.0f : __fmul_rn(a0[v], h[v][0]);
                     }
                 }
             } else if constexpr (!BWD) {

@@ -163,16 +163,18 @@ def test_exact_flag_of_every_tile_variant(lib):
 
 def test_occupancy_rule_few_lanes_long_sequence(lib):
     # 2^20 steps and only 64 fp32 lanes: both directions stream the chunks in
-    # one pass (1,024 chunks of 512 steps per lane group); with state they keep
-    # the chunked path's grouped prefix (512-step chunks forward, 128 backward)
+    # one pass (1,024 chunks of 512 steps per lane group), with or without
+    # carried state; the chunked path's grouped prefix (512-step chunks
+    # forward, 128 backward) when it is asked for
     for direction in ("fwd", "bwd"):
-        p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction)
-        assert p["path"] == "stream" and p["name"] == "stream_f32_d32" and p["kernels"] == 1, p
-    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", state=True)
+        for state in (False, True):
+            p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction, state=state)
+            assert p["path"] == "stream" and p["name"] == "stream_f32_d32" and p["kernels"] == 1, p
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", path="chunk", state=True)
     assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].startswith("chunk512"), p
     assert p["name"].endswith("_grouped") and p["rows_per_window"] == 512
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
-    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", state=True)
+    p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", path="chunk", state=True)
     assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
     # fp32 on 32-lane tiles (forward: 256-step chunks from eight lane groups);
     # bf16 forward on 32-lane tiles, bf16 backward on 64-lane tiles (256-step
@@ -394,7 +396,6 @@ def test_stream_plans(lib):
     assert L.lrscan_plan(2, 1000, 64, "f32", "fwd", path="stream")["ctas"] == 2 * 2 * 2
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
-    with pytest.raises(L.LrscanError):
-        L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
+    assert L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)["path"] == "stream"
     with pytest.raises(L.LrscanError):
         L.lrscan_plan(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=3)

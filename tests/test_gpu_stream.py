@@ -87,11 +87,37 @@ def test_stream_many_chunks_per_cta(dt):
     check(B, T, D, dt, 1, seed=950, a_lo=0.9)
 
 
-def test_stream_refuses_state():
+STATE_SHAPES = [(1, 1, 32), (2, 3001, 96), (3, 700, 32), (1, 40000, 32), (1, 9, 8)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape_i", range(len(STATE_SHAPES)))
+def test_stream_carried_state(dt, shape_i):
+    """h0, segment resets (about one token in twenty starts a segment; batch
+    row 0 starts one at t=0, row 1 continues h0), grad_last and grad_h0 on
+    every stream variant, forward and backward against the oracle's state
+    functions; grad_a is +0 at every reset."""
+    from test_gpu_state import check_state_case, state_inputs
+    B, T, D = STATE_SHAPES[shape_i]
+    inp = state_inputs(B, T, D, dt, seed=960 + shape_i)
+    for v in range(1, L.lrscan_num_variants("stream", dt) + 1):
+        plan, planb = check_state_case(inp, path="stream", tile_variant=v)
+        assert plan["path"] == "stream" and planb["path"] == "stream"
+
+
+@pytest.mark.parametrize("use", [("h0",), ("seg",), ("grad_last",)])
+def test_stream_state_members_one_at_a_time(use):
+    from test_gpu_state import check_state_case, state_inputs
+    inp = state_inputs(2, 5000, 64, "f32", seed=975)
+    check_state_case(inp, path="stream", use=use)
+    check_state_case(inp, path="stream", use=use, want_grad_h0=False)
+
+
+def test_complex_stream_refuses_state():
     a = torch.rand(1, 64, 32, device="cuda")
     h0 = torch.zeros(1, 32, device="cuda")
-    with pytest.raises(RuntimeError):
-        L.lrscan_fwd_state(a, a, h0=h0, path="stream")
+    with pytest.raises(L.LrscanError):
+        L.lrscan_cfwd_state(a, a, a, a, h0=(h0, h0), path="stream")
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
