@@ -587,6 +587,7 @@ def run_extensions(args, dev, peak) -> dict:
     del sets
     torch.cuda.empty_cache()
     return {"complex": run_complex(iters, dev, peak), "complex_long_t": run_complex_long_t(dev, peak),
+            "complex_long_t_bf16": run_complex_long_t(dev, peak, "bf16"),
             "generated_decay": run_gated(iters, dev, peak),
             "generated_decay_fp32": run_gated(iters, dev, peak, "f32"),
             "long_t": run_long_t(dev, peak), "state": {
@@ -689,13 +690,13 @@ def run_complex(iters: int, dev, peak) -> dict:
     return res
 
 
-def run_complex_long_t(dev, peak) -> dict:
+def run_complex_long_t(dev, peak, dtype="f32") -> dict:
     """The complex scan with few lanes and a long sequence: B=1 T=2^20 D=64
-    fp32 re/im planes, |a|~U(0.9,0.999) with phases ~U(-pi,pi), b and grad_out
-    ~N(0,1), drawn on the device from a seeded generator.  The automatic plan
-    (chunk streaming) beside the chunked path (complex chunk maps, grouped
-    prefix); algorithmic bytes are 6 (forward) and 10 (backward) elements per
-    (t, d)."""
+    re/im planes (fp32, or bf16 storage of the same draws), |a|~U(0.9,0.999)
+    with phases ~U(-pi,pi), b and grad_out ~N(0,1), drawn on the device from a
+    seeded generator.  The automatic plan (chunk streaming) beside the chunked
+    path (complex chunk maps, grouped prefix); algorithmic bytes are 6
+    (forward) and 10 (backward) elements per (t, d)."""
     import math
 
     import torch
@@ -705,15 +706,17 @@ def run_complex_long_t(dev, peak) -> dict:
     gen = torch.Generator(device=dev).manual_seed(20298)
     rho = torch.empty(B, T, D, device=dev).uniform_(0.9, 0.999, generator=gen)
     th = torch.empty(B, T, D, device=dev).uniform_(-math.pi, math.pi, generator=gen)
-    ar, ai = rho * torch.cos(th), rho * torch.sin(th)
+    cv = (lambda x: x.bfloat16()) if dtype == "bf16" else (lambda x: x)
+    ar, ai = cv(rho * torch.cos(th)), cv(rho * torch.sin(th))
     del rho, th
-    br, bi, gr, gi = (torch.empty(B, T, D, device=dev).normal_(generator=gen) for _ in range(4))
+    br, bi, gr, gi = (cv(torch.empty(B, T, D, device=dev).normal_(generator=gen)) for _ in range(4))
     outs = L.lrscan_cfwd(ar, ai, br, bi)
     grads = L.lrscan_cbwd(ar, ai, outs[0], outs[1], gr, gi)
     stream = torch.cuda.current_stream()
     E = B * T * D
-    fb, bb = 6 * E * 4 + 8 * B * D, 10 * E * 4
-    res = {"workload": f"B={B} T={T} D={D} fp32 complex (few lanes, long sequence)"}
+    es = 2 if dtype == "bf16" else 4
+    fb, bb = 6 * E * es + 8 * B * D, 10 * E * es
+    res = {"workload": f"B={B} T={T} D={D} {'bf16' if dtype == 'bf16' else 'fp32'} complex (few lanes, long sequence)"}
     for kw, name in ((dict(), "auto"), (dict(path="chunk"), "chunked")):
         fms = time_launches(lambda i: L.lrscan_cfwd(ar, ai, br, bi, out_r=outs[0], out_i=outs[1], last_r=outs[2],
                                                     last_i=outs[3], **kw), 10, stream)
@@ -721,9 +724,9 @@ def run_complex_long_t(dev, peak) -> dict:
         if L.lrscan_sync_check() != 0:
             raise RuntimeError("device error while timing the long complex scan")
         part = {"fwd": {"ms": fms, "frac": fb / (fms * 1e-3) / 1e9 / peak,
-                        "kernel": L.lrscan_plan_complex(B, T, D, "f32", "fwd", **kw)["name"]},
+                        "kernel": L.lrscan_plan_complex(B, T, D, dtype, "fwd", **kw)["name"]},
                 "bwd": {"ms": bms, "frac": bb / (bms * 1e-3) / 1e9 / peak,
-                        "kernel": L.lrscan_plan_complex(B, T, D, "f32", "bwd", **kw)["name"]},
+                        "kernel": L.lrscan_plan_complex(B, T, D, dtype, "bwd", **kw)["name"]},
                 "elements/s": 2 * E / ((fms + bms) * 1e-3)}
         if name == "auto":
             res.update(part)
@@ -792,8 +795,9 @@ def run_long_t(dev, peak) -> dict:
     (one warp per lane walks all maps) and with the grouped prefix, the
     chunked path at its own chunk lengths (grouped prefix over 512-step chunks
     forward, 128 backward), the single-pass chunk-streaming path, and the
-    automatic plan (streaming).  Inputs are drawn on the device from a seeded
-    generator (a~U(0.9,0.9999), b,g~N(0,1))."""
+    automatic plan (streaming); then the automatic plan on bf16 storage of the
+    same draws.  Inputs are drawn on the device from a seeded generator
+    (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 
     from linear_recurrence_scan_lrscan_gb300 import lrscan as L
@@ -826,6 +830,17 @@ def run_long_t(dev, peak) -> dict:
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the long-sequence chunked path")
     res["auto"] = {d: L.lrscan_plan(B, T, D, "f32", d)["name"] for d in ("fwd", "bwd")}
+    a, b, g = a.bfloat16(), b.bfloat16(), g.bfloat16()
+    out, ga, gb = torch.empty_like(a), torch.empty_like(a), torch.empty_like(a)
+    fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last), 10, stream)
+    bms = time_launches(lambda i: L.lrscan_bwd(a, out, g, ga, gb), 10, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the long bf16 scan")
+    res["auto_plan_bf16"] = {"fwd_ms": fms, "bwd_ms": bms,
+                             "fwd_frac": 3 * E * 2 / (fms * 1e-3) / 1e9 / peak,
+                             "bwd_frac": 5 * E * 2 / (bms * 1e-3) / 1e9 / peak,
+                             "elements/s": 2 * E / ((fms + bms) * 1e-3),
+                             "kernels": {d: L.lrscan_plan(B, T, D, "bf16", d)["name"] for d in ("fwd", "bwd")}}
     del a, b, g, out, ga, gb
     torch.cuda.empty_cache()
     return res

@@ -84,11 +84,11 @@ extern "C" {
                                   chunked path; agrees with the sequential definition to rounding, and two calls
                                   may differ in the last bits (which published states a look-back composes depends
                                   on timing).  tile_variant: fp32 1 = 32-lane tiles (forward 512-step chunks,
-                                  backward 256), 2 = 32-lane tiles, 256-step chunks; bf16 1 = 32-lane tiles
-                                  (forward 1024, backward 512), 2 = 64-lane tiles (512), 3 = 64-lane tiles (256).
-                                  Auto takes it for few lanes and at least 32 chunks of 512 steps per lane group:
-                                  fp32 variant 2 for a forward from eight lane groups, else 1; bf16 variant 1
-                                  forward, 2 (one 64-lane group) or 3 backward */
+                                  backward 256), 2 = 32-lane tiles, 256-step chunks; bf16 1 = 32-lane tiles,
+                                  eight summary and eight replay warps (forward 1024, backward 512), 2 = 64-lane
+                                  tiles (512), 3 = 64-lane tiles (256).  Auto takes it for few lanes and at least
+                                  32 chunks of 512 steps per lane group: fp32 variant 2 for a forward from eight
+                                  lane groups, else 1; bf16 variant 1 */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */

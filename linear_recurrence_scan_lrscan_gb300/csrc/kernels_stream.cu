@@ -54,32 +54,40 @@ WinDirCfg stream_cfg() {
     return d;
 }
 
-// StreamShape<St, DT, V, W, NW, R, S, SR, NSCAN, NB>: four summary and four
-// replay warps, two scan warps, two chunk buffers, one CTA per SM.  fp32:
+// StreamShape<St, DT, V, W, NW, R, S, SR, NSCAN, NB>: two scan warps, two
+// chunk buffers, one CTA per SM.  fp32: four summary and four replay warps on
 // 32-lane tiles of 32-row windows; forward 512-step chunks (three summary /
 // two replay stages) or 256-step ones (more lane groups), backward 256-step
 // chunks (two / three stages: its replays trail their summaries by less time,
-// so more of their tiles are still in L2).  bf16: 32-lane tiles of 64-row
-// windows (forward 1024-step chunks, backward 512), or 64-lane tiles of 32-row
-// windows in 512- or 256-step chunks.
+// so more of their tiles are still in L2).  bf16: eight summary and eight
+// replay warps on 32-lane tiles of 32-row windows, forward 1024-step chunks
+// (three / two stages), backward 512 (two / three); at B=1 T=2^22 D=64 that
+// is 0.30 against 0.32 ms forward and 0.47 against 0.48 ms backward of four
+// warps of each kind on 64-row windows, at B=1 T=2^20 D=256 0.29 against 0.32
+// and 0.43 against 0.46 ms.  The other bf16 variants keep four of each on
+// 64-lane tiles of 32-row windows in 512- or 256-step chunks.
 using SF32_C512_F = StreamShape<float, 32, 1, 32, 4, 4, 3, 2, 2, 2>;
 using SF32_C256_F = StreamShape<float, 32, 1, 32, 4, 2, 3, 2, 2, 2>;
 using SF32_C256_B = StreamShape<float, 32, 1, 32, 4, 2, 2, 3, 2, 2>;
-using SBF_D32_F = StreamShape<bf16_t, 32, 1, 64, 4, 4, 3, 3, 2, 2>;
-using SBF_D32_B = StreamShape<bf16_t, 32, 1, 64, 4, 2, 2, 3, 2, 2>;
+using SBF_D32_F = StreamShape<bf16_t, 32, 1, 32, 8, 4, 3, 2, 2, 2>;
+using SBF_D32_B = StreamShape<bf16_t, 32, 1, 32, 8, 2, 2, 3, 2, 2>;
 using SBF_D64_F = StreamShape<bf16_t, 64, 2, 32, 4, 4, 3, 3, 2, 2>;
 using SBF_D64_B = StreamShape<bf16_t, 64, 2, 32, 4, 4, 3, 2, 2, 2>;
 using SBF_D64_C256_F = StreamShape<bf16_t, 64, 2, 32, 4, 2, 3, 3, 2, 2>;
 using SBF_D64_C256_B = StreamShape<bf16_t, 64, 2, 32, 4, 2, 3, 2, 2, 2>;
 
-// Complex: four (forward) or six (backward) planes per tile, so 16-row fp32
-// windows (32-row bf16).  fp32 forward 256-step chunks, backward 128 (at B=1
-// T=2^20 D=64 against 512 / 256: 0.30 against 0.41 ms forward, 0.47 against
-// 0.50 ms backward); bf16 forward 512, backward 256.
+// Complex: four (forward) or six (backward) planes per tile.  The forward
+// keeps four summary and four replay warps on 16-row fp32 windows (32-row
+// bf16) in 256-step (512) chunks: at B=1 T=2^20 D=64, 256 against 512 steps
+// is 0.30 against 0.41 ms, and eight warps of each kind on 8-row windows take
+// 0.33 ms.  The backward takes eight of each on 8-row fp32 windows (16-row
+// bf16), two summary and two replay stages, in 128-step (256) chunks: at B=1
+// T=2^18 D=256, 0.43 against 0.48 ms fp32 and 0.27 against 0.30 ms bf16 of
+// four warps of each kind on the forward's windows.
 using SC_F32_F = StreamShape<float, 32, 1, 16, 4, 4, 3, 2, 2, 2, true>;
-using SC_F32_B = StreamShape<float, 32, 1, 16, 4, 2, 3, 2, 2, 2, true>;
+using SC_F32_B = StreamShape<float, 32, 1, 8, 8, 2, 2, 2, 2, 2, true>;
 using SC_BF_F = StreamShape<bf16_t, 32, 1, 32, 4, 4, 3, 2, 2, 2, true>;
-using SC_BF_B = StreamShape<bf16_t, 32, 1, 32, 4, 2, 3, 2, 2, 2, true>;
+using SC_BF_B = StreamShape<bf16_t, 32, 1, 16, 8, 2, 2, 2, 2, 2, true>;
 
 const WinVariant kCStreamF32[] = {
     {"cstream_f32_d32", stream_cfg<SC_F32_F, true>(), stream_cfg<SC_F32_B, false>()},

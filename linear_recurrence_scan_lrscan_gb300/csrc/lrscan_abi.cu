@@ -442,18 +442,13 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         // fp32 forward, 512- against 256-step chunks: 0.92 / 0.73 at two 32-lane
         // groups (B=1 D=64), 0.89 / 0.81 at four, 0.89 / 0.89 and 0.80 / 0.88 at
         // eight (B=1 D=256, B=4 D=64), 0.77 / 0.89 at sixteen; the fp32 backward
-        // takes 256-step chunks in both variants.  bf16 forward: 32-lane tiles;
-        // bf16 backward: the 64-lane tile in 512-step chunks for one 64-lane
-        // group (0.83 against 0.74), in 256-step chunks from four (0.86-0.88
-        // against 0.78-0.80; two and three groups are not measured)
+        // takes 256-step chunks in both variants.  bf16: the first variant
+        // (eight summary and eight replay warps on 32-lane tiles) in both
+        // directions, 0.78-0.81 forward and 0.84-0.93 backward at B=1 D=64,
+        // B=1 D=256 and B=8 D=64 against at most 0.75 and 0.88 for the 64-lane
+        // variants
         int vi = force_v > 0 ? force_v - 1 : 0;
-        if (force_v == 0) {
-            if (dtype == LRSCAN_F32) {
-                vi = dir == 0 && B * ((D + 31) / 32) >= 8 ? 1 : 0;
-            } else if (dir == 1) {
-                vi = B * ((D + 63) / 64) >= 2 ? 2 : 1;
-            }
-        }
+        if (force_v == 0 && dtype == LRSCAN_F32) vi = dir == 0 && B * ((D + 31) / 32) >= 8 ? 1 : 0;
         return plan_stream_variant(tab, vi, dir, B, T, D, 1, g, ch);
     } else if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix

@@ -176,19 +176,17 @@ def test_occupancy_rule_few_lanes_long_sequence(lib):
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", path="chunk", state=True)
     assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
-    # fp32 on 32-lane tiles (forward: 256-step chunks from eight lane groups);
-    # bf16 forward on 32-lane tiles, bf16 backward on 64-lane tiles (256-step
-    # chunks from two lane groups)
-    want = {(1, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d64"),
+    # 32-lane tiles throughout; the fp32 forward takes 256-step chunks from
+    # eight lane groups, bf16 the eight-warp variant in both directions
+    want = {(1, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d32"),
             (8, 64, "f32"): ("stream_f32_d32_c256", "stream_f32_d32"),
             (1, 128, "f32"): ("stream_f32_d32", "stream_f32_d32"),
-            (1, 256, "bf16"): ("stream_bf16_d32", "stream_bf16_d64_c256"),
-            (8, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d64_c256")}
+            (1, 256, "bf16"): ("stream_bf16_d32", "stream_bf16_d32"),
+            (8, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d32")}
     for (B, D, dt), names in want.items():
         for direction, name in zip(("fwd", "bwd"), names):
             p = L.lrscan_plan(B, 1 << 18, D, dt, direction)
-            lanes = 64 if (dt == "bf16" and direction == "bwd") else 32
-            assert p["path"] == "stream" and p["name"] == name and p["lanes_per_cta"] == lanes, (B, D, dt, p)
+            assert p["path"] == "stream" and p["name"] == name and p["lanes_per_cta"] == 32, (B, D, dt, p)
     # 32 chunks of 512 steps per lane group stream; fewer take the chunked path
     assert L.lrscan_plan(1, 16384, 64, "bf16", "fwd")["path"] == "stream"
     assert L.lrscan_plan(1, 8192, 64, "bf16", "fwd")["path"] == "chunk"
@@ -339,17 +337,18 @@ def test_complex_chunked_plans(lib):
 
 def test_complex_stream_plans(lib):
     """The complex scan streams few-lane long sequences: 32-lane tiles (fp32
-    16-row windows, forward 256-step chunks, backward 128; bf16 32-row
-    windows, 512 and 256), and twice the real path's publication words (a
-    complex map is two 64-bit words, a state one)."""
+    forward 256-step chunks of 16-row windows with four summary and four
+    replay warps, backward 128-step chunks of 8-row windows with eight of
+    each; bf16 twice the rows), and twice the real path's publication words
+    (a complex map is two 64-bit words, a state one)."""
     pad = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    for dt, rows, chunks in (("f32", 16, (256, 128)), ("bf16", 32, (512, 256))):
-        for direction, chunk in zip(("fwd", "bwd"), chunks):
+    for dt, rows, chunks in (("f32", (16, 8), (256, 128)), ("bf16", (32, 16), (512, 256))):
+        for direction, r, chunk, warps in zip(("fwd", "bwd"), rows, chunks, (11, 19)):
             B, T, D = 1, 1 << 20, 64
             p = L.lrscan_plan_complex(B, T, D, dt, direction)
             assert p["path"] == "stream" and p["name"] == f"cstream_{dt}_d32" and p["exact"] == 0, p
-            assert p["rows_per_window"] == rows and p["subchunks"] * rows == chunk and p["kernels"] == 1
-            assert p["threads_per_cta"] == 11 * 32 and p["smem_bytes"] <= 227 * 1024
+            assert p["rows_per_window"] == r and p["subchunks"] * r == chunk and p["kernels"] == 1
+            assert p["threads_per_cta"] == warps * 32 and p["smem_bytes"] <= 227 * 1024
             ng, nc = 2, T // chunk
             assert p["workspace_bytes"] == 256 + pad(ng * nc * 32 * 16) + pad(ng * nc * 32 * 8), p
             assert p["ctas"] == min(ng * nc, 152)
@@ -364,18 +363,19 @@ def test_complex_stream_plans(lib):
 
 
 def test_stream_plans(lib):
-    """The persistent chunk-streaming path: four summary, four replay, two scan
-    warps and a ticket warp per CTA, one CTA per SM (no more than there are
-    chunk tickets), 256- to 1024-step chunks, its publication workspace
-    (ticket, a map and a state per chunk and lane), and refusals where it
-    cannot run."""
+    """The persistent chunk-streaming path: four (bf16 32-lane tiles: eight)
+    summary and as many replay warps, two scan warps and a ticket warp per
+    CTA, one CTA per SM (no more than there are chunk tickets), 256- to
+    1024-step chunks, its publication workspace (ticket, a map and a state per
+    chunk and lane), and refusals where it cannot run."""
     pad = lambda x: (x + 255) // 256 * 256
     # name: {direction: (rows per window, windows per chunk, ring stages)}
     shapes = {"stream_f32_d32": {"fwd": (32, 16, 20), "bwd": (32, 8, 20)},
               "stream_f32_d32_c256": {"fwd": (32, 8, 20), "bwd": (32, 8, 20)},
-              "stream_bf16_d32": {"fwd": (64, 16, 24), "bwd": (64, 8, 20)},
+              "stream_bf16_d32": {"fwd": (32, 32, 40), "bwd": (32, 16, 40)},
               "stream_bf16_d64": {"fwd": (32, 16, 24), "bwd": (32, 16, 20)},
               "stream_bf16_d64_c256": {"fwd": (32, 8, 24), "bwd": (32, 8, 20)}}
+    warps = {"stream_bf16_d32": 19}
     for dt, names in (("f32", ("stream_f32_d32", "stream_f32_d32_c256")),
                       ("bf16", ("stream_bf16_d32", "stream_bf16_d64", "stream_bf16_d64_c256"))):
         assert L.lrscan_num_variants("stream", dt) == len(names)
@@ -386,7 +386,7 @@ def test_stream_plans(lib):
                 p = L.lrscan_plan(B, T, D, dt, direction, path="stream", tile_variant=v)
                 assert p["path"] == "stream" and p["name"] == name and p["exact"] == 0, p
                 assert p["rows_per_window"] == rows and p["subchunks"] == nwin and p["kernels"] == 1
-                assert p["threads_per_cta"] == 11 * 32 and p["stages"] == stages
+                assert p["threads_per_cta"] == warps.get(name, 11) * 32 and p["stages"] == stages
                 assert p["smem_bytes"] <= 227 * 1024
                 dtl = p["lanes_per_cta"]
                 ng, nc = B * -(-D // dtl), -(-T // (nwin * rows))
