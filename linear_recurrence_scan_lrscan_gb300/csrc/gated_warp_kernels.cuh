@@ -1,0 +1,216 @@
+// Generated-decay forward with one warp per lane slice (triton_training_scan.py,
+// _samu_forward with the decay of _samu_precompute_decay rebuilt in the kernel,
+// as in gated_kernels.cuh).  The windowed tiles split time inside a CTA and
+// meet at two CTA barriers per window around a serial walk of the sub-chunk
+// maps; here each warp is on its own:
+//   - a warp owns LW lanes (V per thread) of one batch row over all T and
+//     streams its b tiles of W rows through a ring of NST stages with bulk
+//     tensor copies that it issues itself (lane 0), NST - 1 windows ahead;
+//   - its S = 32 / (LW / V) thread groups take consecutive L-row sub-chunks of
+//     the window: each builds its rows' decays (a = 2^(-nu2 E_t), E_t =
+//     exp(eta_t), one exponential per row of the window shared by shuffles),
+//     reduces its sub-chunk to the map h -> P h + Q, finds the state entering
+//     it by an inclusive shuffle scan of the groups' maps applied to the
+//     carried state, replays its rows, and writes out_t over b_t in the stage;
+//   - lane 0 sends the window out with a bulk tensor store and refills the
+//     stage of the window before (its store has read the stage by then).
+// L is odd, so the S groups' rows of one sub-chunk position fall in different
+// shared-memory banks (no conflicts on the loads and the in-place stores).
+// Every wait is bounded (LRSCAN_ETIMEOUT in the status word; the warp
+// returns after its copies in flight have landed).  The window maps
+// re-associate the recurrence: results agree with the sequential definition
+// to rounding.
+#pragma once
+
+#include "gated_kernels.cuh"
+#include "packed_f32x2.cuh"
+
+namespace lrscan {
+
+// Compiled shape: storage type, lanes per warp, lanes per thread (2 or 4),
+// rows per sub-chunk (odd), ring stages.  One warp per CTA.
+template <class St_, int LW_, int V_, int L_, int NST_>
+struct GWarpShape {
+    using St = St_;
+    static constexpr int LW = LW_, V = V_, G = LW_ / V_, S = 32 / G, L = L_, W = S * L_, NST = NST_;
+    static constexpr int ROWB = LW * static_cast<int>(sizeof(St));  // bytes of one tile row
+    static constexpr int TILE = W * ROWB;
+    static_assert((V == 2 || V == 4) && LW % V == 0 && 32 % G == 0 && G < 32, "whole thread groups per warp");
+    static_assert(L % 2 == 1, "odd sub-chunk rows: the groups' rows fall in different banks");
+    static_assert(W <= 32, "one row exponential per lane and window");
+    static_assert(ROWB % 16 == 0, "a bulk tensor copy moves whole 16-byte units per row");
+    static_assert(TILE % 128 == 0, "stages stay 128-byte aligned");
+    static_assert(NST >= 3, "a stage is refilled one window after its store");
+};
+
+// Shared memory: NST tiles, NST full barriers, the abort flag.
+template <class C>
+__host__ __device__ constexpr int gwarp_smem_bytes() {
+    return C::NST * C::TILE + C::NST * 8 + 16;
+}
+
+template <class C>
+__global__ void __launch_bounds__(32, 16)
+gwarp_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
+                 const float *__restrict__ eta, const float *__restrict__ nu_log, float *__restrict__ last, int T,
+                 int D, DevStatus *status, uint64_t timeout_ns) {
+    using St = typename C::St;
+    constexpr int V = C::V, G = C::G, S = C::S, L = C::L, W = C::W, NST = C::NST, LW = C::LW;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    auto tile = [&](int st) { return reinterpret_cast<St *>(smem_raw + st * C::TILE); };
+    auto full = [&](int st) { return smem_addr(smem_raw + NST * C::TILE + 8 * st); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + NST * C::TILE + NST * 8);
+    const int lane = threadIdx.x;
+    if (lane == 0) {
+        for (int st = 0; st < NST; ++st) mbar_init(full(st), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // the next launch's CTAs come in only when this grid's are past their
+    // main loop (with early launches, as many idle warps as working ones
+    // would sit on every SM)
+    pdl_wait();
+    const WaitCtx wc{status, abort_flag, timeout_ns};
+    const int d0 = blockIdx.x * LW;
+    const int brow = blockIdx.y;
+    const int nwin = (T + W - 1) / W;
+    const int s = lane / G;   // sub-chunk of this thread's group
+    const int g = lane % G;   // lanes V*g .. V*g + V - 1 of the slice
+    const int d = d0 + V * g;
+    // rows are 16-byte multiples here, so D is a multiple of 4: all V lanes or none
+    const bool lane_ok = d < D;
+    // window k: stage k % NST, phase (k / NST) & 1
+    auto issue = [&](int k) {
+        const int st = k % NST;
+        mbar_arrive_expect_tx(full(st), C::TILE);
+        tma_load_3d(smem_addr(tile(st)), &tm_b, d0, k * W, brow, full(st));
+    };
+    int issued = 0;
+    if (lane == 0) {
+        for (int k = 0; k < NST && k < nwin; ++k) issue(k);
+        issued = NST < nwin ? NST : nwin;
+    }
+    float nnu2[V];  // -nu2: the decay exponent is (-nu2) * E
+#pragma unroll
+    for (int v = 0; v < V; ++v) nnu2[v] = lane_ok ? -rate2(nu_log, d + v) : -0.0f;
+    const float *eta_row = eta + static_cast<size_t>(brow) * T;
+    // eta of row `lane` of windows k and k + 1
+    float ev = lane < W ? eta_at(eta_row, lane, T) : 0.0f;
+    float ev_next = lane < W ? eta_at(eta_row, W + lane, T) : 0.0f;
+    float carry[V];  // state entering the window (identical in every group)
+#pragma unroll
+    for (int v = 0; v < V; ++v) carry[v] = 0.0f;
+    int done = 0;
+    for (int k = 0; k < nwin; ++k) {
+        const int st = k % NST;
+        const float e_mine = exp_approx(ev);  // E of window row `lane`
+        ev = ev_next;
+        ev_next = lane < W ? eta_at(eta_row, (k + 2) * W + lane, T) : 0.0f;
+        float xa[L][V], xb[L][V];
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            const float e = __shfl_sync(0xffffffffu, e_mine, s * L + j);
+            float ej[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) ej[v] = e;
+            vmul(xa[j], nnu2, ej);
+#pragma unroll
+            for (int v = 0; v < V; ++v) xa[j][v] = ex2_approx(xa[j][v]);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(full(st), static_cast<uint32_t>((k / NST) & 1), wc,
+                                               kSiteConsumerFull)))
+            break;
+        St *tb = tile(st) + (s * L) * LW + V * g;
+#pragma unroll
+        for (int j = 0; j < L; ++j) unpack_lanes<St, V>(tb + j * LW, xb[j]);
+        const int nrows = T - (k * W + s * L);  // rows of this sub-chunk before T (may be <= 0 or > L)
+        if (nrows < L) {
+            // steps past T: exact identity steps (a = 1, b = 0)
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    xa[j][v] = j < nrows ? xa[j][v] : 1.0f;
+                    xb[j][v] = j < nrows ? xb[j][v] : 0.0f;
+                }
+            }
+        }
+        // the sub-chunk's map, rows in chain order
+        float P[V], Q[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) { P[v] = 1.0f; Q[v] = 0.0f; }
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            vmul(P, xa[j], P);
+            vfma(Q, xa[j], Q, xb[j]);
+        }
+        // inclusive scan over the groups: (P, Q) <- (P, Q) o (map of the
+        // groups before), the later map applied after the earlier one
+#pragma unroll
+        for (int off = G; off < 32; off *= 2) {
+            float pp[V], qq[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                pp[v] = __shfl_up_sync(0xffffffffu, P[v], off);
+                qq[v] = __shfl_up_sync(0xffffffffu, Q[v], off);
+            }
+            if (lane >= off) {
+                vfma(Q, P, qq, Q);
+                vmul(P, P, pp);
+            }
+        }
+        // state after this group's rows, then the state entering them
+        float z[V], h[V];
+        vfma(z, P, carry, Q);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const float up = __shfl_up_sync(0xffffffffu, z[v], G);
+            h[v] = s == 0 ? carry[v] : up;
+            carry[v] = __shfl_sync(0xffffffffu, z[v], 32 - G + g);
+        }
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            vfma(h, xa[j], h, xb[j]);
+            store_lanes<St, V>(tb + j * LW, h);
+        }
+        if (last != nullptr && lane_ok && k == nwin - 1 && s == S - 1) {
+            // the last group ends on step T - 1 or on identity steps after it
+#pragma unroll
+            for (int v = 0; v < V; ++v) last[static_cast<size_t>(brow) * D + d + v] = h[v];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(&tm_out, smem_addr(tile(st)), d0, k * W, brow);
+            bulk_commit();
+            // the store of window k - 1 has read its stage: refill it with
+            // window k - 1 + NST
+            if (k >= 1 && issued < nwin) {
+                bulk_wait_read<1>();
+                issue(issued);
+                ++issued;
+            }
+        }
+        done = k + 1;
+    }
+    pdl_trigger();
+    if (lane == 0) {
+        // after an abort: every copy issued has landed before the CTA's shared
+        // memory goes away (bounded, blind to the abort flag)
+        if (done < nwin) {
+            for (int k = done; k < issued; ++k) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(full(k % NST), static_cast<uint32_t>((k / NST) & 1))) {
+                    if (global_timer_ns() - t0 > wc.timeout_ns) {
+                        record_error(wc, kErrTimeout, kSiteDrain);
+                        break;
+                    }
+                }
+            }
+        }
+        bulk_wait<0>();  // every out store complete
+    }
+}
+
+}  // namespace lrscan

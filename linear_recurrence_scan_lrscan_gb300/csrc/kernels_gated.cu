@@ -5,6 +5,7 @@
 
 #include "gated_kernels.cuh"
 #include "gated_pipe_kernels.cuh"
+#include "gated_warp_kernels.cuh"
 #include "window_launch.cuh"
 
 namespace lrscan {
@@ -84,6 +85,40 @@ int launch_gpipe_fwd(const WinLaunch &L, const WinDirCfg &) {
                                      L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, L.last, static_cast<int>(L.T),
                                      static_cast<int>(L.D), L.status, L.timeout_ns);
     return e == cudaSuccess ? 0 : -1;
+}
+
+template <class C>
+int launch_gwarp_fwd(const WinLaunch &L, const WinDirCfg &) {
+    static unsigned long long mask = 0;
+    static std::mutex mu;
+    auto fn = gwarp_fwd_kernel<C>;
+    if (set_smem_attr(reinterpret_cast<const void *>(fn), L.device, &mask, &mu)) return -1;
+    const int nsl = static_cast<int>((L.D + C::LW - 1) / C::LW);
+    const cudaError_t e = launch_pdl(fn, dim3(nsl, static_cast<unsigned>(L.B)), dim3(32), gwarp_smem_bytes<C>(),
+                                     L.stream, *L.maps[0], *L.maps[1], L.eta, L.nu_log, L.last, static_cast<int>(L.T),
+                                     static_cast<int>(L.D), L.status, L.timeout_ns);
+    return e == cudaSuccess ? 0 : -1;
+}
+
+// Forward with one warp per lane slice (gated_warp_kernels.cuh): a CTA is one
+// warp over LW lanes; its tiles are LW lanes by W rows.
+template <class C>
+WinDirCfg gwarp_cfg() {
+    WinDirCfg d{};
+    d.dt = C::LW;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = C::S;
+    d.lane_scan = 1;
+    d.exact = 0;
+    d.w = C::W;
+    d.nstage = C::NST;
+    d.threads = 32;
+    d.smem = gwarp_smem_bytes<C>();
+    d.stage_bytes = C::TILE;
+    d.max_resident = 0;
+    d.launch = &launch_gwarp_fwd<C>;
+    return d;
 }
 
 // Forward with warp roles (gated_pipe_kernels.cuh): W-row windows, one lane per
@@ -174,6 +209,15 @@ using GWB_FF_16_1_8 = WinShape<float, 16, 1, 8, 2, 288, 2, false>;
 // the time).
 using GP_FF_16 = GPipeShape<float, 16, 2, 3, 12, 8, 5>;
 
+// GWarpShape<St, LW, V, L, NST>: lanes per warp, lanes per thread, rows per
+// sub-chunk, ring stages.
+// Measured on B=8 T=2048 D=2560 forward: fp32 57.5 us (gpipe_f32_w16 61.9,
+// 32-lane slices with four lanes per thread 58.2); bf16 42.6 us against
+// 38.1 us for the windowed tile (32-lane slices 46.7 us, 8-lane slices of
+// 3-row sub-chunks 57.0 us), so bf16 keeps the windowed tile.
+using GW_BF_16_7 = GWarpShape<bf16_t, 16, 2, 7, 8>;
+using GW_FF_16_7 = GWarpShape<float, 16, 2, 7, 6>;
+
 #define F(SH, N) gdir_cfg<SH, true>(N)
 #define B(SH, N) gdir_cfg<SH, false>(N)
 #define FW(SH, S, N) gwdir_cfg<SH, true>(S, N)
@@ -185,12 +229,14 @@ const WinVariant kGatedBF16[] = {
     {"gwin_bf16_d32_s8_n3", FW(GWF_BF_32_2_8, 8, 3), BW(GWB_BF_32_2_8_M5, 8, 3)},
     {"gwin_bf16_d32_s8_m4", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8_M4, 8, 2)},
     {"gwin_bf16_d32_s16", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8, 16, 2)},
+    {"gwarp_bf16_l16_r7", gwarp_cfg<GW_BF_16_7>(), BW(GWB_BF_32_2_8_M5, 8, 2)},
 };
 const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
     {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
     {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), BW(GWB_FF_16_1_8, 16, 2)},
     {"gpipe_f32_w16", gpdir_cfg<GP_FF_16>(), BW(GWB_FF_16_1_8, 16, 2)},
+    {"gwarp_f32_l16_r7", gwarp_cfg<GW_FF_16_7>(), BW(GWB_FF_16_1_8, 16, 2)},
 };
 #undef FW
 #undef BW

@@ -152,9 +152,8 @@ Occ occupancy(const WinVariant &var, int dir, int64_t B, int64_t D, const Geomet
     Occ o{};
     o.ctas = B * ((D + v.dt - 1) / v.dt);
     // the kernels' named barriers and mbarrier arrival counts take whole
-    // warps: a table entry whose threads are not (S * lanes-per-row + the
-    // producer warp) in whole warps never launches
-    if (v.threads < 64 || v.threads % 32 != 0) return o;
+    // warps: a table entry whose threads are not whole warps never launches
+    if (v.threads < 32 || v.threads % 32 != 0) return o;
     int r_smem = smem > g.smem_optin ? 0 : g.smem_per_sm / (smem + 1024);
     int r_thr = g.max_threads_per_sm / v.threads;
     o.resident = std::min(std::min(r_smem, r_thr), 32);
@@ -1235,10 +1234,11 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
-    } else if (dtype == LRSCAN_F32 && dir == 0 && B * ((D + 31) / 32) >= 4LL * g.sm_count &&
-               (vi = find_variant(tab, n, "gpipe_f32_w16", dir, B, D, g)) >= 0) {
-        // fp32 forward from four 32-lane tiles per SM: the tile with warp roles
-        // (61.9 us on B=8 T=2048 D=2560 fp32 against 65.9 us for the windowed tile)
+    } else if (dtype == LRSCAN_F32 && dir == 0 && B * ((D + 15) / 16) >= 8LL * g.sm_count &&
+               (vi = find_variant(tab, n, "gwarp_f32_l16_r7", dir, B, D, g)) >= 0) {
+        // fp32 forward from eight 16-lane slices per SM: one warp per slice
+        // (57.5 us on B=8 T=2048 D=2560 fp32 against 61.9 us for the tile with
+        // warp roles and 65.9 us for the windowed tile)
     } else if ((vi = find_variant(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8", dir, B, D,
                                   g)) >= 0) {
         // the windowed tiles (time split inside the CTA): the measured fastest in both
