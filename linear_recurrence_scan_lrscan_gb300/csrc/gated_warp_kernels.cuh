@@ -3,24 +3,28 @@
 // as in gated_kernels.cuh).  The windowed tiles split time inside a CTA and
 // meet at two CTA barriers per window around a serial walk of the sub-chunk
 // maps; here each warp is on its own:
-//   - a warp owns LW lanes (V per thread) of one batch row over all T and
-//     streams its b tiles of W rows through a ring of NST stages with bulk
+//   - a warp (a CTA) owns LW lanes (V per thread) of one batch row over all T
+//     and streams its b tiles of W rows through a ring of NST stages with bulk
 //     tensor copies that it issues itself (lane 0), NST - 1 windows ahead;
 //   - its S = 32 / (LW / V) thread groups take consecutive L-row sub-chunks of
 //     the window: each builds its rows' decays (a = 2^(-nu2 E_t), E_t =
-//     exp(eta_t), one exponential per row of the window shared by shuffles),
-//     reduces its sub-chunk to the map h -> P h + Q, finds the state entering
-//     it by an inclusive shuffle scan of the groups' maps applied to the
-//     carried state, replays its rows, and writes out_t over b_t in the stage;
+//     exp(eta_t), one exponential per row, taken by one thread of the group
+//     and shared by shuffles), reduces its sub-chunk to the map h -> P h + Q,
+//     finds the state entering it by an inclusive shuffle scan of the groups'
+//     maps applied to the carried state, replays its rows, and writes out_t
+//     over b_t in the stage;
 //   - lane 0 sends the window out with a bulk tensor store and refills the
 //     stage of the window before (its store has read the stage by then).
 // L is odd, so the S groups' rows of one sub-chunk position fall in different
 // shared-memory banks (no conflicts on the loads and the in-place stores).
-// Every wait is bounded (LRSCAN_ETIMEOUT in the status word; the warp
-// returns after its copies in flight have landed).  The window maps
-// re-associate the recurrence: results agree with the sequential definition
-// to rounding.
+// Rows past T take E = 0 and the copy's zero fill: exact identity steps, so a
+// window is one block of code from its loads to its stores.  Every wait is
+// bounded (LRSCAN_ETIMEOUT in the status word; the warp returns after its
+// copies in flight have landed).  The window maps re-associate the
+// recurrence: results agree with the sequential definition to rounding.
 #pragma once
+
+#include <cfloat>
 
 #include "gated_kernels.cuh"
 #include "packed_f32x2.cuh"
@@ -37,7 +41,7 @@ struct GWarpShape {
     static constexpr int TILE = W * ROWB;
     static_assert((V == 2 || V == 4) && LW % V == 0 && 32 % G == 0 && G < 32, "whole thread groups per warp");
     static_assert(L % 2 == 1, "odd sub-chunk rows: the groups' rows fall in different banks");
-    static_assert(W <= 32, "one row exponential per lane and window");
+    static constexpr int NE = (L + G - 1) / G;  // row exponentials per thread and window
     static_assert(ROWB % 16 == 0, "a bulk tensor copy moves whole 16-byte units per row");
     static_assert(TILE % 128 == 0, "stages stay 128-byte aligned");
     static_assert(NST >= 3, "a stage is refilled one window after its store");
@@ -50,7 +54,7 @@ __host__ __device__ constexpr int gwarp_smem_bytes() {
 }
 
 template <class C>
-__global__ void __launch_bounds__(32, 16)
+__global__ void __launch_bounds__(32, 8)
 gwarp_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
                  const float *__restrict__ eta, const float *__restrict__ nu_log, float *__restrict__ last, int T,
                  int D, DevStatus *status, uint64_t timeout_ns) {
@@ -91,50 +95,62 @@ gwarp_fwd_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant
         for (int k = 0; k < NST && k < nwin; ++k) issue(k);
         issued = NST < nwin ? NST : nwin;
     }
-    float nnu2[V];  // -nu2: the decay exponent is (-nu2) * E
+    // -nu2: the decay exponent is (-nu2) * E.  An infinite rate is taken as
+    // -FLT_MAX, so that the identity steps past T (E = 0) give 2^(-0) = 1 and
+    // not 2^NaN (a NaN rate stays NaN).
+    float nnu2[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) nnu2[v] = lane_ok ? -rate2(nu_log, d + v) : -0.0f;
+    for (int v = 0; v < V; ++v) {
+        const float r = lane_ok ? -rate2(nu_log, d + v) : -0.0f;
+        nnu2[v] = r < -FLT_MAX ? -FLT_MAX : r;
+    }
     const float *eta_row = eta + static_cast<size_t>(brow) * T;
-    // eta of row `lane` of windows k and k + 1
-    float ev = lane < W ? eta_at(eta_row, lane, T) : 0.0f;
-    float ev_next = lane < W ? eta_at(eta_row, W + lane, T) : 0.0f;
+    // thread g of group s takes the E of its group's rows g, g + G, ...: eta
+    // of those rows of windows k and k + 1
+    constexpr int NE = C::NE;
+    auto eta_of = [&](int k, int i) {
+        return g + G * i < L ? eta_at(eta_row, k * W + s * L + g + G * i, T) : 0.0f;
+    };
+    float ev[NE], ev_next[NE];
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+        ev[i] = eta_of(0, i);
+        ev_next[i] = eta_of(1, i);
+    }
     float carry[V];  // state entering the window (identical in every group)
 #pragma unroll
     for (int v = 0; v < V; ++v) carry[v] = 0.0f;
     int done = 0;
     for (int k = 0; k < nwin; ++k) {
         const int st = k % NST;
-        const float e_mine = exp_approx(ev);  // E of window row `lane`
-        ev = ev_next;
-        ev_next = lane < W ? eta_at(eta_row, (k + 2) * W + lane, T) : 0.0f;
+        // the tile first, so that one block of code runs from the loads and
+        // exponentials to the stores and the scheduler can overlap them
+        if (!__all_sync(0xffffffffu, mbar_wait(full(st), static_cast<uint32_t>((k / NST) & 1), wc,
+                                               kSiteConsumerFull)))
+            break;
+        // E of this group's rows g, g + G, ...; 0 past T, where the bulk copy
+        // has filled b with zeros: exact identity steps (a = 2^(-0) = 1, b = 0)
+        float e_mine[NE];
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+            const int t = k * W + s * L + g + G * i;
+            e_mine[i] = t < T ? exp_approx(ev[i]) : 0.0f;
+            ev[i] = ev_next[i];
+            ev_next[i] = eta_of(k + 2, i);
+        }
+        St *tb = tile(st) + (s * L) * LW + V * g;
         float xa[L][V], xb[L][V];
 #pragma unroll
+        for (int j = 0; j < L; ++j) unpack_lanes<St, V>(tb + j * LW, xb[j]);
+#pragma unroll
         for (int j = 0; j < L; ++j) {
-            const float e = __shfl_sync(0xffffffffu, e_mine, s * L + j);
+            const float e = __shfl_sync(0xffffffffu, e_mine[j / G], s * G + j % G);
             float ej[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) ej[v] = e;
             vmul(xa[j], nnu2, ej);
 #pragma unroll
             for (int v = 0; v < V; ++v) xa[j][v] = ex2_approx(xa[j][v]);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(full(st), static_cast<uint32_t>((k / NST) & 1), wc,
-                                               kSiteConsumerFull)))
-            break;
-        St *tb = tile(st) + (s * L) * LW + V * g;
-#pragma unroll
-        for (int j = 0; j < L; ++j) unpack_lanes<St, V>(tb + j * LW, xb[j]);
-        const int nrows = T - (k * W + s * L);  // rows of this sub-chunk before T (may be <= 0 or > L)
-        if (nrows < L) {
-            // steps past T: exact identity steps (a = 1, b = 0)
-#pragma unroll
-            for (int j = 0; j < L; ++j) {
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    xa[j][v] = j < nrows ? xa[j][v] : 1.0f;
-                    xb[j][v] = j < nrows ? xb[j][v] : 0.0f;
-                }
-            }
         }
         // the sub-chunk's map, rows in chain order
         float P[V], Q[V];

@@ -211,12 +211,19 @@ using GP_FF_16 = GPipeShape<float, 16, 2, 3, 12, 8, 5>;
 
 // GWarpShape<St, LW, V, L, NST>: lanes per warp, lanes per thread, rows per
 // sub-chunk, ring stages.
-// Measured on B=8 T=2048 D=2560 forward: fp32 57.5 us (gpipe_f32_w16 61.9,
-// 32-lane slices with four lanes per thread 58.2); bf16 42.6 us against
-// 38.1 us for the windowed tile (32-lane slices 46.7 us, 8-lane slices of
-// 3-row sub-chunks 57.0 us), so bf16 keeps the windowed tile.
-using GW_BF_16_7 = GWarpShape<bf16_t, 16, 2, 7, 8>;
-using GW_FF_16_7 = GWarpShape<float, 16, 2, 7, 6>;
+// GWarpShape<St, LW, V, L, NST>: lanes per warp, lanes per thread, rows per
+// sub-chunk, ring stages.  Measured on B=8 T=2048 D=2560 forward (CUDA
+// events): bf16 33.9 us with 15-row sub-chunks, 33.8 with 23, 35.1 before
+// the window was one block of code, 42.6 with 7 (windowed tile 38.1); fp32
+// 54.0 us with 15 (tile with warp roles 61.7).  Slower: 32-lane slices with
+// four lanes per thread (bf16 46.7 us), 8-lane slices (16-byte rows; 64.2),
+// 31-row sub-chunks (38.6), two warps per slice taking windows in turn and
+// handing the state over by an mbarrier (36.1) or a polled word (46.2), and a
+// software pipeline overlapping window k+1's summary with window k's replay
+// (54.2).
+using GW_BF_16_15 = GWarpShape<bf16_t, 16, 2, 15, 6>;
+using GW_BF_16_23 = GWarpShape<bf16_t, 16, 2, 23, 5>;
+using GW_FF_16_15 = GWarpShape<float, 16, 2, 15, 4>;
 
 #define F(SH, N) gdir_cfg<SH, true>(N)
 #define B(SH, N) gdir_cfg<SH, false>(N)
@@ -229,14 +236,15 @@ const WinVariant kGatedBF16[] = {
     {"gwin_bf16_d32_s8_n3", FW(GWF_BF_32_2_8, 8, 3), BW(GWB_BF_32_2_8_M5, 8, 3)},
     {"gwin_bf16_d32_s8_m4", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8_M4, 8, 2)},
     {"gwin_bf16_d32_s16", FW(GWF_BF_32_2_8, 8, 2), BW(GWB_BF_32_2_8, 16, 2)},
-    {"gwarp_bf16_l16_r7", gwarp_cfg<GW_BF_16_7>(), BW(GWB_BF_32_2_8_M5, 8, 2)},
+    {"gwarp_bf16_l16_r15", gwarp_cfg<GW_BF_16_15>(), BW(GWB_BF_32_2_8_M5, 8, 2)},
+    {"gwarp_bf16_l16_r23", gwarp_cfg<GW_BF_16_23>(), BW(GWB_BF_32_2_8_M5, 8, 2)},
 };
 const WinVariant kGatedF32[] = {
     {"gseq_f32_d32_v1", F(GFF_32_1, 8), B(GFB_32_1, 6)},
     {"gseq_f32_d64_v2", F(GFF_64_2, 6), B(GFB_64_2, 4)},
     {"gwin_f32_d32_s8", FW(GWF_FF_32_1_8, 8, 3), BW(GWB_FF_16_1_8, 16, 2)},
     {"gpipe_f32_w16", gpdir_cfg<GP_FF_16>(), BW(GWB_FF_16_1_8, 16, 2)},
-    {"gwarp_f32_l16_r7", gwarp_cfg<GW_FF_16_7>(), BW(GWB_FF_16_1_8, 16, 2)},
+    {"gwarp_f32_l16_r15", gwarp_cfg<GW_FF_16_15>(), BW(GWB_FF_16_1_8, 16, 2)},
 };
 #undef FW
 #undef BW
