@@ -1234,12 +1234,13 @@ int plan_gated(int64_t B, int64_t D, int dtype, int dir, bool aligned, const lrs
     if (force_v > 0) {
         if (force_v > n) return fail(LRSCAN_EINVAL, "tile_variant %d > %d variants", force_v, n);
         vi = force_v - 1;
-    } else if (dir == 0 && B * ((D + 15) / 16) >= 8LL * g.sm_count &&
+    } else if (B * ((D + 15) / 16) >= 8LL * g.sm_count &&
                (vi = find_variant(tab, n, dtype == LRSCAN_BF16 ? "gwarp_bf16_l16_r15" : "gwarp_f32_l16_r15", dir, B,
                                   D, g)) >= 0) {
-        // forward from eight 16-lane slices per SM: one warp per slice (B=8
-        // T=2048 D=2560: bf16 33.9 us against 38.1 us for the windowed tile;
-        // fp32 54.0 us against 61.7 us for the tile with warp roles)
+        // from eight 16-lane slices per SM: one warp per slice (B=8 T=2048
+        // D=2560: bf16 forward 33.9 us against 38.1 us for the windowed tile,
+        // backward 56.0 against 64.3 us; fp32 forward 54.0 us against 61.7 us
+        // for the tile with warp roles, backward 93.7 against 118.0 us)
     } else if ((vi = find_variant(tab, n, dtype == LRSCAN_BF16 ? "gwin_bf16_d32_s8" : "gwin_f32_d32_s8", dir, B, D,
                                   g)) >= 0) {
         // the windowed tiles (time split inside the CTA): the measured fastest in both
