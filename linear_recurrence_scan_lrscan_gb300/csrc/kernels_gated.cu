@@ -138,9 +138,19 @@ WinDirCfg gwarp_cfg() {
 }
 template <class C>
 WinDirCfg gwarp_bwd_cfg() {
-    WinDirCfg d = gwarp_cfg<C>();
+    WinDirCfg d{};
+    d.dt = C::LW;
+    d.v = C::V;
+    d.l = C::L;
+    d.s = C::S;
+    d.lane_scan = 1;
+    d.exact = 0;
+    d.w = C::W;
+    d.nstage = C::NST;
+    d.threads = 32;
     d.smem = gwarp_bwd_smem_bytes<C>();
     d.stage_bytes = 2 * C::TILE;
+    d.max_resident = 0;
     d.launch = &launch_gwarp_bwd<C>;
     return d;
 }
