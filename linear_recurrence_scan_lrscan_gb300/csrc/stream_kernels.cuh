@@ -431,13 +431,15 @@ struct StreamGeom {
     int sstage_bytes;  // summary stage
     int rstage_bytes;  // replay stage
     int rring_off;     // replay ring after the summary ring
-    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_req[slots], maps[NB], entries[NB], buf_free[NB]
+    int bar_off;       // sfull[NW*S], rfull[NW*SR], step_full[slots], step_req[slots], maps[NB], entries[NB],
+                       // buf_free[NB], mask_full[slots]
     int ticket_off;    // step tickets [slots]
     int tick_off;      // chunk tickets per buffer [NB] (-1: end mark)
     int map_off;       // window maps [NB][NWIN][DT][2K] floats (P, Q)
     int cmap_off;      // chunk maps [NB][DT][2K] floats
     int entry_off;     // window entering states [NB][NWIN][DT][K] floats
     int mask_off;      // carried-state calls: window reset masks [NB][NWIN][2] (step t, step t+1)
+    int tmask_off;     // carried-state calls: per ticket slot, each window's resets [slots][NWIN]
     int count_off;     // summary warps done per buffer [NB]
     int flag_off;      // abort flag
     int smem_bytes;
@@ -452,14 +454,15 @@ __host__ __device__ inline StreamGeom make_stream_geom() {
     g.rstage_bytes = K * (BWD ? 3 : 2) * g.tile_bytes;
     g.rring_off = C::NW * C::S * g.sstage_bytes;
     g.bar_off = g.rring_off + C::NW * C::SR * g.rstage_bytes;
-    const int nbar = C::NW * C::S + C::NW * C::SR + 2 * kStreamSlots + 3 * C::NB;
+    const int nbar = C::NW * C::S + C::NW * C::SR + 3 * kStreamSlots + 3 * C::NB;
     g.ticket_off = g.bar_off + nbar * 8;
     g.tick_off = g.ticket_off + kStreamSlots * 4;
     g.map_off = (g.tick_off + C::NB * 4 + 15) / 16 * 16;
     g.cmap_off = g.map_off + C::NB * C::NWIN * C::DT * 8 * K;
     g.entry_off = g.cmap_off + C::NB * C::DT * 8 * K;
     g.mask_off = g.entry_off + C::NB * C::NWIN * C::DT * 4 * K;
-    g.count_off = g.mask_off + C::NB * C::NWIN * 16;
+    g.tmask_off = g.mask_off + C::NB * C::NWIN * 16;
+    g.count_off = g.tmask_off + kStreamSlots * C::NWIN * 8;
     g.flag_off = g.count_off + C::NB * 4;
     g.smem_bytes = g.flag_off + 16;
     return g;
@@ -505,12 +508,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
     auto maps_bar = [&](int b) { return bar(BR + 2 * SLOTS + b); };
     auto entries_bar = [&](int b) { return bar(BR + 2 * SLOTS + NB + b); };
     auto buf_free = [&](int b) { return bar(BR + 2 * SLOTS + 2 * NB + b); };
+    auto mask_full = [&](int q) { return bar(BR + 2 * SLOTS + 3 * NB + q); };
     int *step_ticket = reinterpret_cast<int *>(smem_raw + geo.ticket_off);
     volatile int *tick_of = reinterpret_cast<volatile int *>(smem_raw + geo.tick_off);
     float *wmap = reinterpret_cast<float *>(smem_raw + geo.map_off);     // [NB][NWIN][DT][2K]
     float *cmap = reinterpret_cast<float *>(smem_raw + geo.cmap_off);    // [NB][DT][2K]
     float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off); // [NB][NWIN][DT][K]
     [[maybe_unused]] uint64_t *wmask = reinterpret_cast<uint64_t *>(smem_raw + geo.mask_off);  // [NB][NWIN][2]
+    // [slots][NWIN] (forward): bit r = a reset at step r of the window
+    [[maybe_unused]] uint64_t *tmask = reinterpret_cast<uint64_t *>(smem_raw + geo.tmask_off);
     unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
     if (threadIdx.x == 0) {
@@ -519,6 +525,7 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
         for (int q = 0; q < SLOTS; ++q) {
             mbar_init(step_full(q), 1);
             mbar_init(step_req(q), NW);
+            mbar_init(mask_full(q), 1);
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(maps_bar(b), 1);  // the last summary warp (or the end mark)
@@ -563,6 +570,53 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
 
     if (warp == 2 * NW + NSCAN) {
         // ------------------------------------------------------------ tickets
+        if constexpr (EXT && !BWD) {
+            if (sx.seg != nullptr) {
+                // forward carried-state calls with resets: the whole warp also turns
+                // each ticket's segment positions into its windows' reset
+                // masks, published (mask_full) after the ticket itself, about
+                // a chunk ahead of the summary that uses them (no global load
+                // on the summary warps' path)
+                static_assert(W == 32 && NWIN <= 32, "one ballot per window, one window per lane");
+                for (int j = 0;; ++j) {
+                    if (j >= 1) {
+                        const int m = j - 1;
+                        if (!warp_wait(step_req(m % SLOTS), static_cast<uint32_t>((m / SLOTS) & 1), wc,
+                                       kSiteProducerEmpty))
+                            return;
+                    }
+                    long long tj = 0;
+                    if (lane == 0) tj = static_cast<long long>(atomicAdd(sa.ticket, 1u));
+                    tj = __shfl_sync(0xffffffffu, tj, 0);
+                    const int tk = tj < total ? static_cast<int>(tj) : -1;
+                    if (lane == 0) {
+                        step_ticket[j % SLOTS] = tk;
+                        mbar_arrive(step_full(j % SLOTS));
+                    }
+                    if (tk < 0) return;
+                    {
+                        const Chunk ch = decode(tk);
+                        const int32_t *srow = sx.seg + static_cast<size_t>(ch.brow) * T;
+                        const int t0 = ch.c * CH;
+                        int pos[NWIN];
+#pragma unroll
+                        for (int wi = 0; wi < NWIN; ++wi) {
+                            const int t = t0 + wi * W + lane;
+                            pos[wi] = t < T ? __ldg(srow + t) : 1;
+                        }
+                        uint64_t mine = 0;
+#pragma unroll
+                        for (int wi = 0; wi < NWIN; ++wi) {
+                            const uint32_t m = __ballot_sync(0xffffffffu, pos[wi] == 0);
+                            if (lane == wi) mine = m;
+                        }
+                        if (lane < NWIN) tmask[(j % SLOTS) * NWIN + lane] = mine;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(mask_full(j % SLOTS));
+                }
+            }
+        }
         if (lane == 0) {
             // ticket 0 at once; ticket j >= 1 once every summary warp has asked
             // for it (at the start of its chunk j - 1, request slot (j-1) mod SLOTS)
@@ -605,9 +659,9 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
         };
         if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
         int tk = step_ticket[0];
-        // carried-state calls: segment positions of the current tile's rows and,
-        // loaded one tile ahead, of the next (backward: one row more, for a_{t+1})
-        [[maybe_unused]] SegRows<W + (BWD ? 1 : 0)> segc, segn;
+        // backward carried-state calls: segment positions of the current
+        // tile's rows and one more (for a_{t+1}), loaded one tile ahead
+        [[maybe_unused]] SegRows<W + 1> segc, segn;
         [[maybe_unused]] bool seg_next = false;
         for (int k = 0;; ++k) {
             const int b = k % NB;
@@ -665,7 +719,7 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 const int wbase = ch.c * CH + (r * NW + w) * W;
                 const int nrows = min(max(T - wbase, 0), W);
                 const int st = w * S + u % S;
-                if constexpr (EXT) {
+                if constexpr (EXT && BWD) {
                     if (sx.seg != nullptr) {
                         if (seg_next) segc = segn;
                         else segc.load(sx.seg, ch.brow, T, wbase, lane);
@@ -695,13 +749,20 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     if constexpr (EXT) {
                         uint64_t rc = 0, rn = 0;
                         if (sx.seg != nullptr) {
-                            bool row64 = false;
-                            const uint64_t full = segc.bits(&row64);
                             if constexpr (BWD) {
+                                bool row64 = false;
+                                const uint64_t full = segc.bits(&row64);
                                 rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
                                 rn = (full >> 1) | (static_cast<uint64_t>(row64) << 63);
                             } else {
-                                rc = full;
+                                // the ticket warp's masks for this chunk (its
+                                // ticket slot k % SLOTS)
+                                if (r == 0 && !warp_wait(mask_full(k % SLOTS), static_cast<uint32_t>((k / SLOTS) & 1),
+                                                         wc, kSiteStreamStep)) {
+                                    drain();
+                                    return;
+                                }
+                                rc = tmask[(k % SLOTS) * NWIN + r * NW + w];
                             }
                         }
                         mcur[r] = rc;
