@@ -25,7 +25,7 @@ int launch_stream(const WinLaunch &L, const WinDirCfg &) {
     for (int i = 0; i < PL::NOUT; ++i) m.out[i] = *L.maps[6 + i];
     const cudaError_t e = launch_pdl(fn, dim3(static_cast<unsigned>(L.grid)), dim3(C::THREADS), g.smem_bytes,
                                      L.stream, m, L.last, L.last_i, static_cast<int>(L.T), static_cast<int>(L.D),
-                                     L.status, L.timeout_ns, L.sa, L.sx);
+                                     L.status, L.timeout_ns, L.sa, L.sx, L.csx);
     return e == cudaSuccess ? 0 : -1;
 }
 
@@ -48,9 +48,7 @@ WinDirCfg stream_cfg() {
     d.stage_bytes = g.rstage_bytes;
     d.max_resident = 1;
     d.launch = &launch_stream<C, !FWD, false>;
-    // carried state and resets: the real scan's kernels
-    if constexpr (C::CPLX) d.launch_state = nullptr;
-    else d.launch_state = &launch_stream<C, !FWD, true>;
+    d.launch_state = &launch_stream<C, !FWD, true>;  // carried state and resets
     return d;
 }
 

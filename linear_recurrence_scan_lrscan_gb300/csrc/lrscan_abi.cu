@@ -672,7 +672,8 @@ int copy_or_zero(float *dst, const float *src, int64_t B, int64_t D, cudaStream_
 // all-ones), one launch.
 int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::initializer_list<void *> outs,
                float *last, float *last_i, int64_t B, int64_t T, int64_t D, int dtype, cudaStream_t st, int dev,
-               DeviceCtx *ctx, const lrscan_opts *opts, bool bwd, bool cplx, const StateArgs *sx = nullptr) {
+               DeviceCtx *ctx, const lrscan_opts *opts, bool bwd, bool cplx, const StateArgs *sx = nullptr,
+               const CStateArgs *csx = nullptr) {
     const WinDirCfg &v = dir_of(*ch.var, bwd ? 1 : 0);
     const int64_t ndt = (D + v.dt - 1) / v.dt;
     const int64_t ng = B * ndt;
@@ -716,7 +717,8 @@ int run_stream(const Choice &ch, std::initializer_list<const void *> ins, std::i
         return fail(LRSCAN_ECUDA, "clearing the streaming workspace failed");
     }
     if (sx) L.sx = *sx;
-    if ((sx ? v.launch_state : v.launch)(L, v))
+    if (csx) L.csx = *csx;
+    if ((sx || csx ? v.launch_state : v.launch)(L, v))
         return fail(LRSCAN_ECUDA, "launch of %s: %s", ch.var->name, cudaGetErrorString(cudaGetLastError()));
     return LRSCAN_OK;
 }
@@ -898,8 +900,6 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         return fail(LRSCAN_EINVAL, "unknown complex scan path %d", want);
     if ((want == kPathSeq || want == kPathWindow || want == kPathStream) && !aligned16)
         return fail(LRSCAN_EINVAL, "tiled paths need 16-byte aligned pointers and rows (D*elem %% 16 == 0)");
-    if (want == kPathStream && ext)
-        return fail(LRSCAN_EINVAL, "the chunk-streaming path carries no state or resets");
     // default chunk: 64 steps fp32, 128 bf16 (the same bytes per chunk row;
     // measured on few-lane complex scans: bf16 10-13 % faster than at 64)
     const int chunk = opts && opts->chunk_len ? opts->chunk_len : (dtype == LRSCAN_BF16 ? 128 : 64);
@@ -914,10 +914,10 @@ int plan_complex(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool align
         // they would without it; unaligned rows take the chunked kernels,
         // which carry state at any alignment.
         // In one pass (chunk streaming) from 32 chunks of 512 steps per lane
-        // group, without carried state or an asked-for chunk length.
+        // group, with or without carried state, unless a chunk length is asked for.
         const long long few = aligned16 ? static_cast<long long>(0.45 * g.sm_count * 32) : 32LL * g.sm_count * 32;
         if (B * D < few && T >= 16LL * chunk)
-            path = (aligned16 && !ext && T >= 32LL * 512 && !(opts && opts->chunk_len)) ? kPathStream : kPathChunk;
+            path = (aligned16 && T >= 32LL * 512 && !(opts && opts->chunk_len)) ? kPathStream : kPathChunk;
         else path = aligned16 ? kPathSeq : (ext ? kPathChunk : kPathPlain);
     } else {
         // seq and window both name the tiled variant table (sequential and windowed tiles)
@@ -1068,9 +1068,11 @@ int run_cfwd(const void *const in[4], void *out_r, void *out_i, float *last_r, f
     Choice ch;
     if ((rc = plan_complex(B, T, D, dtype, 0, al, opts, geometry_of(ctx), &ch, ext))) return rc;
     const size_t es = esize(dtype);
-    if (ch.path == kPathStream)
+    if (ch.path == kPathStream) {
+        const CStateArgs xs = cstate_slice(sx, nullptr, nullptr, 0, T, D, es);
         return run_stream(ch, {in[0], in[1], in[2], in[3]}, {out_r, out_i}, last_r, last_i, B, T, D, dtype, st, dev,
-                          ctx, opts, false, true);
+                          ctx, opts, false, true, nullptr, ext ? &xs : nullptr);
+    }
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
         if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;
@@ -1149,9 +1151,12 @@ int run_cbwd(const void *const in[6], void *const outp[4], int64_t B, int64_t T,
     const bool al = aligned16({in[0], in[1], in[2], in[3], in[4], in[5], outp[0], outp[1], outp[2], outp[3]}, D, dtype);
     Choice ch;
     if ((rc = plan_complex(B, T, D, dtype, 1, al, opts, geometry_of(ctx), &ch, ext))) return rc;
-    if (ch.path == kPathStream)
+    if (ch.path == kPathStream) {
+        const CStateArgs xs = cstate_slice(sx, in[0], in[1], 0, T, D, esize(dtype));
         return run_stream(ch, {in[0], in[1], in[2], in[3], in[4], in[5]}, {outp[0], outp[1], outp[2], outp[3]},
-                          nullptr, nullptr, B, T, D, dtype, st, dev, ctx, opts, true, true);
+                          nullptr, nullptr, B, T, D, dtype, st, dev, ctx, opts, true, true, nullptr,
+                          ext ? &xs : nullptr);
+    }
     if (ch.path == kPathChunk) {
         void *ws = nullptr;
         if ((rc = workspace_for(ctx, st, ch.workspace, opts, &ws))) return rc;

@@ -255,9 +255,10 @@ __device__ __forceinline__ void cxc_step(float xr, float xi, float hr, float hi,
 
 // Complex look-back: as stream_lookback, for complex maps (two words per lane
 // and chunk: P = (re, im), Q = (re, im)) and leaving states (one word).
-template <int DT, int V, int BATCH>
+template <int DT, int V, int BATCH, bool START = false>
 __device__ bool stream_lookback_cx(const StreamArgs &sa, int gi, int cc, int i0, float (&hr_in)[V],
-                                   float (&hi_in)[V], const WaitCtx &wc) {
+                                   float (&hi_in)[V], const WaitCtx &wc, const float *sr = nullptr,
+                                   const float *si = nullptr) {
     const int lane = threadIdx.x & 31;
     const size_t g0 = static_cast<size_t>(gi) * sa.nc;
     const float2 *states = reinterpret_cast<const float2 *>(sa.incl);
@@ -290,7 +291,16 @@ __device__ bool stream_lookback_cx(const StreamArgs &sa, int gi, int cc, int i0,
                 if (go) {
                     if (j - t < 0) {
 #pragma unroll
-                        for (int v = 0; v < V; ++v) { hr_in[v] = aQr[v]; hi_in[v] = aQi[v]; }
+                        for (int v = 0; v < V; ++v) {
+                            if (START && (sr != nullptr || si != nullptr)) {
+                                // the chain's start (h0 forward, grad_last backward)
+                                cx_step(aPr[v], aPi[v], sr != nullptr ? sr[v] : 0.0f, si != nullptr ? si[v] : 0.0f,
+                                        aQr[v], aQi[v], hr_in[v], hi_in[v]);
+                            } else {
+                                hr_in[v] = aQr[v];
+                                hi_in[v] = aQi[v];
+                            }
+                        }
                         done = true;
                         go = false;
                     } else {
@@ -481,8 +491,7 @@ template <class C, bool BWD, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, float *__restrict__ last_i, int T,
               int D, DevStatus *status, uint64_t timeout_ns, const __grid_constant__ StreamArgs sa,
-              const __grid_constant__ StateArgs sx) {
-    static_assert(!EXT || !C::CPLX, "carried state on the real scan");
+              const __grid_constant__ StateArgs sx, const __grid_constant__ CStateArgs cx) {
     using St = typename C::St;
     using PL = StreamPlanes<C, BWD>;
     constexpr int DT = C::DT, V = C::V, W = C::W, NW = C::NW, R = C::R, S = C::S, SR = C::SR, NSCAN = C::NSCAN;
@@ -571,13 +580,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
     if (warp == 2 * NW + NSCAN) {
         // ------------------------------------------------------------ tickets
         if constexpr (EXT && !BWD) {
-            if (sx.seg != nullptr) {
+            if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
                 // forward carried-state calls with resets: the whole warp also turns
                 // each ticket's segment positions into its windows' reset
                 // masks, published (mask_full) after the ticket itself, about
                 // a chunk ahead of the summary that uses them (no global load
                 // on the summary warps' path)
-                static_assert(W == 32 && NWIN <= 32, "one ballot per window, one window per lane");
+                static_assert(W <= 32 && 32 % W == 0 && (NWIN * W) % 32 == 0 && NWIN <= 32,
+                              "whole windows per ballot, one window per lane");
+                const int32_t *segp = C::CPLX ? cx.seg : sx.seg;
                 for (int j = 0;; ++j) {
                     if (j >= 1) {
                         const int m = j - 1;
@@ -596,19 +607,25 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     if (tk < 0) return;
                     {
                         const Chunk ch = decode(tk);
-                        const int32_t *srow = sx.seg + static_cast<size_t>(ch.brow) * T;
+                        const int32_t *srow = segp + static_cast<size_t>(ch.brow) * T;
                         const int t0 = ch.c * CH;
-                        int pos[NWIN];
+                        constexpr int NBAL = NWIN * W / 32;  // ballots of 32 rows
+                        constexpr int WPB = 32 / W;          // windows per ballot
+                        int pos[NBAL];
 #pragma unroll
-                        for (int wi = 0; wi < NWIN; ++wi) {
-                            const int t = t0 + wi * W + lane;
-                            pos[wi] = t < T ? __ldg(srow + t) : 1;
+                        for (int i = 0; i < NBAL; ++i) {
+                            const int t = t0 + i * 32 + lane;
+                            pos[i] = t < T ? __ldg(srow + t) : 1;
                         }
                         uint64_t mine = 0;
 #pragma unroll
-                        for (int wi = 0; wi < NWIN; ++wi) {
-                            const uint32_t m = __ballot_sync(0xffffffffu, pos[wi] == 0);
-                            if (lane == wi) mine = m;
+                        for (int i = 0; i < NBAL; ++i) {
+                            const uint32_t m = __ballot_sync(0xffffffffu, pos[i] == 0);
+#pragma unroll
+                            for (int q = 0; q < WPB; ++q) {
+                                const uint32_t mw = W == 32 ? m : ((m >> (q * W)) & ((1u << (W < 32 ? W : 0)) - 1u));
+                                if (lane == i * WPB + q) mine = mw;
+                            }
                         }
                         if (lane < NWIN) tmask[(j % SLOTS) * NWIN + lane] = mine;
                     }
@@ -720,13 +737,14 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 const int nrows = min(max(T - wbase, 0), W);
                 const int st = w * S + u % S;
                 if constexpr (EXT && BWD) {
-                    if (sx.seg != nullptr) {
+                    const int32_t *segp = C::CPLX ? cx.seg : sx.seg;
+                    if (segp != nullptr) {
                         if (seg_next) segc = segn;
-                        else segc.load(sx.seg, ch.brow, T, wbase, lane);
+                        else segc.load(segp, ch.brow, T, wbase, lane);
                         seg_next = false;
                         if (u + 1 < u_iss) {  // the next tile is out: its ticket is known and valid
                             const Chunk c1 = decode((u + 1) / R == k ? tk : tn);
-                            segn.load(sx.seg, c1.brow, T, c1.c * CH + (((u + 1) % R) * NW + w) * W, lane);
+                            segn.load(segp, c1.brow, T, c1.c * CH + (((u + 1) % R) * NW + w) * W, lane);
                             seg_next = true;
                         }
                     }
@@ -741,34 +759,34 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
 #pragma unroll
                     for (int q = 0; q < K; ++q) { P[r][v][q] = q == 0 ? 1.0f : 0.0f; Q[r][v][q] = 0.0f; }
                 }
+                // resets of the decays this window uses (backward: a_{t+1})
+                [[maybe_unused]] uint64_t rbits = 0;
+                if constexpr (EXT) {
+                    uint64_t rc = 0, rn = 0;
+                    if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
+                        if constexpr (BWD) {
+                            bool row64 = false;
+                            const uint64_t full = segc.bits(&row64);
+                            rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
+                            rn = (full >> 1) | (static_cast<uint64_t>(row64) << 63);
+                        } else {
+                            // the ticket warp's masks for this chunk (its
+                            // ticket slot k % SLOTS)
+                            if (r == 0 && !warp_wait(mask_full(k % SLOTS), static_cast<uint32_t>((k / SLOTS) & 1), wc,
+                                                     kSiteStreamStep)) {
+                                drain();
+                                return;
+                            }
+                            rc = tmask[(k % SLOTS) * NWIN + r * NW + w];
+                        }
+                    }
+                    mcur[r] = rc;
+                    mnext[r] = rn;
+                    rbits = BWD ? rn : rc;
+                }
                 if constexpr (!C::CPLX) {
                     const St *ta = stile(st, 0);
                     const St *tb = stile(st, 1);
-                    // resets of the decays this window uses (backward: a_{t+1})
-                    [[maybe_unused]] uint64_t rbits = 0;
-                    if constexpr (EXT) {
-                        uint64_t rc = 0, rn = 0;
-                        if (sx.seg != nullptr) {
-                            if constexpr (BWD) {
-                                bool row64 = false;
-                                const uint64_t full = segc.bits(&row64);
-                                rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
-                                rn = (full >> 1) | (static_cast<uint64_t>(row64) << 63);
-                            } else {
-                                // the ticket warp's masks for this chunk (its
-                                // ticket slot k % SLOTS)
-                                if (r == 0 && !warp_wait(mask_full(k % SLOTS), static_cast<uint32_t>((k / SLOTS) & 1),
-                                                         wc, kSiteStreamStep)) {
-                                    drain();
-                                    return;
-                                }
-                                rc = tmask[(k % SLOTS) * NWIN + r * NW + w];
-                            }
-                        }
-                        mcur[r] = rc;
-                        mnext[r] = rn;
-                        rbits = BWD ? rn : rc;
-                    }
                     for (int g8 = 0; g8 < nrows; g8 += 8) {
                         const int r0 = BWD ? ((nrows - 1 - g8) & ~7) : g8;  // groups of eight, chain order
                         float xa[8][V], xb[8][V];
@@ -807,6 +825,21 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                         load8<St, V, DT>(stile(st, 1), r0, lane, xi);
                         load8<St, V, DT>(stile(st, 2), r0, lane, br);
                         load8<St, V, DT>(stile(st, 3), r0, lane, bi);
+                        if constexpr (EXT) {
+                            // resets (a = 0) and, backward, the row past the end
+                            // (a'_T = 1), as selects ahead of the chain
+                            const uint32_t m8 = static_cast<uint32_t>(rbits >> r0) & 0xffu;
+                            const int pe = BWD ? T - 1 - (wbase + r0) : -1;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const bool z = (m8 >> q) & 1u;
+#pragma unroll
+                                for (int v = 0; v < V; ++v) {
+                                    xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
+                                    xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                                }
+                            }
+                        }
 #pragma unroll
                         for (int rr = 0; rr < 8; ++rr) {
                             const int row = BWD ? 7 - rr : rr;
@@ -951,7 +984,18 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 }
             } else {
                 float hr[V], hi[V];
-                if (!stream_lookback_cx<DT, V, 8 / V>(sa, ch.gi, ch.cc, i0, hr, hi, wc)) return;
+                // the chain's start: complex h0 forward, grad_last backward
+                const float *sr0 = nullptr, *si0 = nullptr;
+                if constexpr (EXT) {
+                    if (ch.x0 + i0 < D) {
+                        const size_t o0 = static_cast<size_t>(ch.brow) * D + ch.x0 + i0;
+                        const float *r0p = BWD ? cx.gl_r : cx.h0_r;
+                        const float *i0p = BWD ? cx.gl_i : cx.h0_i;
+                        sr0 = r0p != nullptr ? r0p + o0 : nullptr;
+                        si0 = i0p != nullptr ? i0p + o0 : nullptr;
+                    }
+                }
+                if (!stream_lookback_cx<DT, V, 8 / V, EXT>(sa, ch.gi, ch.cc, i0, hr, hi, wc, sr0, si0)) return;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const float *cp = cmap + (b * DT + i0 + v) * 4;
@@ -1170,12 +1214,26 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 }
             } else if constexpr (!BWD) {
                 // complex: out_t over b_t (planes 2, 3)
+                [[maybe_unused]] uint64_t rbits = 0;
+                if constexpr (EXT) rbits = wmask[(b * NWIN + wi) * 2];
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     float xr[8][V], xi[8][V], br[8][V], bi[8][V];
                     load8<St, V, DT>(rtile(st, 0), g8, lane, xr);
                     load8<St, V, DT>(rtile(st, 1), g8, lane, xi);
                     load8<St, V, DT>(rtile(st, 2), g8, lane, br);
                     load8<St, V, DT>(rtile(st, 3), g8, lane, bi);
+                    if constexpr (EXT) {
+                        const uint32_t m8 = static_cast<uint32_t>(rbits >> g8) & 0xffu;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const bool z = (m8 >> q) & 1u;
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                xr[q][v] = z ? 0.0f : xr[q][v];
+                                xi[q][v] = z ? 0.0f : xi[q][v];
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
                         if (g8 + rr < nrows) {
@@ -1194,6 +1252,21 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
             } else {
                 // complex backward: g = conj(a_{t+1}) g + grad_out; grad_b = g over
                 // grad_out (planes 4, 5), grad_a = g conj(h_{t-1}) over out (2, 3)
+                // EXT: resets of a_{t+1} (rnext) and of step t itself (rcur), and
+                // out_{-1} = h0
+                [[maybe_unused]] uint64_t rnext = 0, rcur = 0;
+                [[maybe_unused]] float h0r[V], h0i[V];
+                if constexpr (EXT) {
+                    rcur = wmask[(b * NWIN + wi) * 2];
+                    rnext = wmask[(b * NWIN + wi) * 2 + 1];
+                    const size_t hs = static_cast<size_t>(ch.brow) * D + d;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {  // read by the window holding step 0 only
+                        const bool in0 = wbase == 0 && d + v < D;
+                        h0r[v] = (in0 && cx.h0_r != nullptr) ? cx.h0_r[hs + v] : 0.0f;
+                        h0i[v] = (in0 && cx.h0_i != nullptr) ? cx.h0_i[hs + v] : 0.0f;
+                    }
+                }
                 for (int g8 = 0; g8 < nrows; g8 += 8) {
                     const int r0 = (nrows - 1 - g8) & ~7;
                     float xr[8][V], xi[8][V], hr[8][V], hi[8][V], gr[8][V], gi[8][V];
@@ -1203,6 +1276,31 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     load8<St, V, DT>(rtile(st, 3), r0, lane, hi);
                     load8<St, V, DT>(rtile(st, 4), r0, lane, gr);
                     load8<St, V, DT>(rtile(st, 5), r0, lane, gi);
+                    [[maybe_unused]] uint32_t zmask = 0;  // rows whose grad_a is +0 (resets)
+                    if constexpr (EXT) {
+                        // conj(a'_{t+1}): 0 where step t+1 starts a segment, 1 at
+                        // the row past the end (grad_last enters there);
+                        // out_{-1} = h0
+                        const uint32_t mn = static_cast<uint32_t>(rnext >> r0) & 0xffu;
+                        zmask = static_cast<uint32_t>(rcur >> r0) & 0xffu;
+                        const int pe = T - 1 - (wbase + r0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const bool z = (mn >> q) & 1u;
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
+                                xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                            }
+                        }
+                        if (wbase + r0 == 0) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v) {
+                                hr[0][v] = h0r[v];
+                                hi[0][v] = h0i[v];
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
                         const int row = 7 - rr;
@@ -1214,15 +1312,39 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                                          ngi[v]);
                                 h[v][0] = ngr[v];
                                 h[v][1] = ngi[v];
-                                // g * conj(h_{t-1})
+                                // g * conj(h_{t-1}); +0 where step t starts a segment
                                 gar[v] = __fmaf_rn(ngr[v], hr[row][v], __fmul_rn(ngi[v], hi[row][v]));
                                 gai[v] = __fmaf_rn(ngi[v], hr[row][v], -__fmul_rn(ngr[v], hi[row][v]));
+                                if constexpr (EXT) {
+                                    const bool z = (zmask >> row) & 1u;
+                                    gar[v] = z ? 0.0f : gar[v];
+                                    gai[v] = z ? 0.0f : gai[v];
+                                }
                             }
                             const int o = (r0 + row) * DT + lane * V;
                             store_lanes<St, V>(rtile(st, 4) + o, ngr);
                             store_lanes<St, V>(rtile(st, 5) + o, ngi);
                             store_lanes<St, V>(rtile(st, 2) + o, gar);
                             store_lanes<St, V>(rtile(st, 3) + o, gai);
+                        }
+                    }
+                }
+                if constexpr (EXT) {
+                    // grad_h0 = conj(a'_0) * g_0 from the window holding step 0
+                    // (h holds g_0), +0 where step 0 starts a segment
+                    if ((cx.gh0_r != nullptr || cx.gh0_i != nullptr) && wbase == 0 && d < D) {
+                        const size_t ao = static_cast<size_t>(ch.brow) * T * D + d;
+                        float ar0[V], ai0[V];
+                        unpack_lanes<St, V>(static_cast<const St *>(cx.ar) + ao, ar0);
+                        unpack_lanes<St, V>(static_cast<const St *>(cx.ai) + ao, ai0);
+                        const size_t hs = static_cast<size_t>(ch.brow) * D + d;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            const bool z = rcur & 1;
+                            const float gr0 = z ? 0.0f : __fmaf_rn(ar0[v], h[v][0], __fmul_rn(ai0[v], h[v][1]));
+                            const float gi0 = z ? 0.0f : __fmaf_rn(ar0[v], h[v][1], -__fmul_rn(ai0[v], h[v][0]));
+                            if (cx.gh0_r != nullptr) cx.gh0_r[hs + v] = gr0;
+                            if (cx.gh0_i != nullptr) cx.gh0_i[hs + v] = gi0;
                         }
                     }
                 }

@@ -321,12 +321,13 @@ def test_every_tile_variant_is_whole_warps(lib):
 def test_complex_chunked_plans(lib):
     """The complex scan's chunked path: automatic for few lanes (fewer than
     0.45 lane tiles of 32 per SM) and sequences too short to stream, or with
-    state or an asked-for chunk length; twice the real path's scratch (re and
+    an asked-for chunk length; twice the real path's scratch (re and
     im maps), flat or grouped prefix."""
     p = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "fwd", chunk_len=64)
     assert p["path"] == "chunk" and p["name"] == "cchunk64_v4_grouped" and p["kernels"] == 5, p
     assert L.lrscan_plan_complex(1, 8192, 64, "f32", "fwd")["path"] == "chunk"
-    assert L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", state=True)["path"] == "chunk"
+    assert L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", state=True)["path"] == "stream"
+    assert L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", state=True, chunk_len=64)["path"] == "chunk"
     assert p["workspace_bytes"] == 2 * L.lrscan_workspace_bytes(1, 1 << 20, 64, 64)
     flat = L.lrscan_plan_complex(1, 1 << 20, 64, "f32", "bwd", path="chunk", tile_variant=1)
     assert flat["kernels"] == 3 and flat["workspace_bytes"] == 4 * 16384 * 64 * 4
@@ -363,8 +364,7 @@ def test_complex_stream_plans(lib):
         L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", tile_variant=2)
     with pytest.raises(L.LrscanError):
         L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", aligned=False)
-    with pytest.raises(L.LrscanError):
-        L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)
+    assert L.lrscan_plan_complex(1, 1 << 16, 64, "f32", "fwd", path="stream", state=True)["path"] == "stream"
 
 
 def test_stream_plans(lib):

@@ -113,11 +113,30 @@ def test_stream_state_members_one_at_a_time(use):
     check_state_case(inp, path="stream", use=use, want_grad_h0=False)
 
 
-def test_complex_stream_refuses_state():
-    a = torch.rand(1, 64, 32, device="cuda")
-    h0 = torch.zeros(1, 32, device="cuda")
-    with pytest.raises(L.LrscanError):
-        L.lrscan_cfwd_state(a, a, a, a, h0=(h0, h0), path="stream")
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_complex_stream_carried_state(dt):
+    """The complex chunk-streaming kernels with complex h0, segment resets
+    (the forward's masks from the ticket warp, the backward's from per-tile
+    loads), grad_last and grad_h0 = conj(a'_0) g_0, against the oracle's
+    complex state functions: ragged lane tiles, partial chunks, one-step and
+    many-chunk sequences, a reset at step 0; then each state member alone."""
+    from test_gpu_complex import _cstate_inputs, check_cstate
+    for i, (B, T, D) in enumerate([(1, 5000, 64), (2, 3001, 96), (1, 9, 8), (2, 40000, 32), (1, 700, 32)]):
+        inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=990 + i)
+        if i % 2:
+            seg[:, 0] = 0  # a reset at step 0
+        plan, planb = check_cstate(inp, dt, h0, gl, seg, path="stream")
+        assert plan["path"] == "stream" and planb["path"] == "stream" and plan["name"].startswith("cstream_")
+    # the automatic plan streams few lanes and long sequences with state too
+    inp, h0, gl, seg = _cstate_inputs(1, 40000, 64, dt, seed=999)
+    plan, planb = check_cstate(inp, dt, h0, gl, seg)
+    assert plan["path"] == "stream" and planb["path"] == "stream"
+    # one member at a time: h0 and grad_last only (no resets), resets only
+    B, T, D = 1, 3000, 32
+    inp, h0, gl, seg = _cstate_inputs(B, T, D, dt, seed=998)
+    check_cstate(inp, dt, h0, gl, np.ones((B, T), dtype=np.int32), path="stream")
+    zero = [np.zeros((B, D), dtype=np.float32)] * 2
+    check_cstate(inp, dt, zero, zero, seg, path="stream")
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
