@@ -524,7 +524,8 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
     float *cmap = reinterpret_cast<float *>(smem_raw + geo.cmap_off);    // [NB][DT][2K]
     float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off); // [NB][NWIN][DT][K]
     [[maybe_unused]] uint64_t *wmask = reinterpret_cast<uint64_t *>(smem_raw + geo.mask_off);  // [NB][NWIN][2]
-    // [slots][NWIN] (forward): bit r = a reset at step r of the window
+    // [slots][NWIN]: bit r = a reset at step r of the window; backward
+    // (complex scan), bit W = one at the step after it
     [[maybe_unused]] uint64_t *tmask = reinterpret_cast<uint64_t *>(smem_raw + geo.tmask_off);
     unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
@@ -579,9 +580,10 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
 
     if (warp == 2 * NW + NSCAN) {
         // ------------------------------------------------------------ tickets
-        if constexpr (EXT && !BWD) {
+        if constexpr (EXT && (!BWD || C::CPLX)) {
             if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
-                // forward carried-state calls with resets: the whole warp also turns
+                // carried-state calls with resets (the real scan's forward, the
+                // complex scan's both directions): the whole warp also turns
                 // each ticket's segment positions into its windows' reset
                 // masks, published (mask_full) after the ticket itself, about
                 // a chunk ahead of the summary that uses them (no global load
@@ -626,6 +628,16 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                                 const uint32_t mw = W == 32 ? m : ((m >> (q * W)) & ((1u << (W < 32 ? W : 0)) - 1u));
                                 if (lane == i * WPB + q) mine = mw;
                             }
+                        }
+                        if constexpr (BWD) {
+                            // bit W: a reset at the step after the window (the
+                            // next window's first; after the chunk's last
+                            // window, the next chunk's first step)
+                            const int te = t0 + CH;
+                            const int pe = (lane == 0 && te < T) ? __ldg(srow + te) : 1;
+                            const uint64_t eb = __ballot_sync(0xffffffffu, pe == 0) & 1u;
+                            const uint64_t nb = __shfl_down_sync(0xffffffffu, mine, 1) & 1u;
+                            mine |= (lane == NWIN - 1 ? eb : nb) << W;
                         }
                         if (lane < NWIN) tmask[(j % SLOTS) * NWIN + lane] = mine;
                     }
@@ -676,8 +688,8 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
         };
         if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
         int tk = step_ticket[0];
-        // backward carried-state calls: segment positions of the current
-        // tile's rows and one more (for a_{t+1}), loaded one tile ahead
+        // the real scan's backward with resets: segment positions of the
+        // current tile's rows and one more (for a_{t+1}), loaded one tile ahead
         [[maybe_unused]] SegRows<W + 1> segc, segn;
         [[maybe_unused]] bool seg_next = false;
         for (int k = 0;; ++k) {
@@ -736,8 +748,8 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 const int wbase = ch.c * CH + (r * NW + w) * W;
                 const int nrows = min(max(T - wbase, 0), W);
                 const int st = w * S + u % S;
-                if constexpr (EXT && BWD) {
-                    const int32_t *segp = C::CPLX ? cx.seg : sx.seg;
+                if constexpr (EXT && BWD && !C::CPLX) {
+                    const int32_t *segp = sx.seg;
                     if (segp != nullptr) {
                         if (seg_next) segc = segn;
                         else segc.load(segp, ch.brow, T, wbase, lane);
@@ -764,7 +776,7 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 if constexpr (EXT) {
                     uint64_t rc = 0, rn = 0;
                     if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
-                        if constexpr (BWD) {
+                        if constexpr (BWD && !C::CPLX) {
                             bool row64 = false;
                             const uint64_t full = segc.bits(&row64);
                             rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
@@ -777,7 +789,13 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                                 drain();
                                 return;
                             }
-                            rc = tmask[(k % SLOTS) * NWIN + r * NW + w];
+                            const uint64_t full = tmask[(k % SLOTS) * NWIN + r * NW + w];
+                            if constexpr (BWD) {
+                                rc = full & ((1ull << W) - 1);
+                                rn = full >> 1;
+                            } else {
+                                rc = full;
+                            }
                         }
                     }
                     mcur[r] = rc;
