@@ -695,8 +695,9 @@ def run_complex_long_t(dev, peak, dtype="f32") -> dict:
     re/im planes (fp32, or bf16 storage of the same draws), |a|~U(0.9,0.999)
     with phases ~U(-pi,pi), b and grad_out ~N(0,1), drawn on the device from a
     seeded generator.  The automatic plan (chunk streaming) beside the chunked
-    path (complex chunk maps, grouped prefix); algorithmic bytes are 6
-    (forward) and 10 (backward) elements per (t, d)."""
+    path (complex chunk maps, grouped prefix), and the automatic plan with
+    carried state and resets; algorithmic bytes are 6 (forward) and 10
+    (backward) elements per (t, d)."""
     import math
 
     import torch
@@ -732,6 +733,25 @@ def run_complex_long_t(dev, peak, dtype="f32") -> dict:
             res.update(part)
         else:
             res[name] = part
+    # carried complex state: h0, a segment start every 4,096 steps, grad_last,
+    # grad_h0 (the automatic plan)
+    h0 = tuple(torch.empty(B, D, device=dev).normal_(generator=gen) for _ in range(2))
+    gl = tuple(torch.empty(B, D, device=dev).normal_(generator=gen) for _ in range(2))
+    gh0 = tuple(torch.empty(B, D, device=dev) for _ in range(2))
+    seg = (torch.arange(T, device=dev, dtype=torch.int32) % 4096).view(1, T).repeat(B, 1).contiguous()
+    fms = time_launches(lambda i: L.lrscan_cfwd_state(ar, ai, br, bi, h0=h0, segment_pos=seg, out_r=outs[0],
+                                                      out_i=outs[1], last_r=outs[2], last_i=outs[3]), 10, stream)
+    bms = time_launches(lambda i: L.lrscan_cbwd_state(ar, ai, outs[0], outs[1], gr, gi, h0=h0, segment_pos=seg,
+                                                      grad_last=gl, grads=grads, grad_h0=gh0), 10, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the long complex scan with carried state")
+    sfb, sbb = fb + 4 * B * T + 8 * B * D, bb + 4 * B * T + 24 * B * D
+    res["state"] = {"what": "complex h0, a segment start every 4,096 steps, grad_last, grad_h0",
+                    "fwd": {"ms": fms, "frac": sfb / (fms * 1e-3) / 1e9 / peak,
+                            "kernel": L.lrscan_plan_complex(B, T, D, dtype, "fwd", state=True)["name"]},
+                    "bwd": {"ms": bms, "frac": sbb / (bms * 1e-3) / 1e9 / peak,
+                            "kernel": L.lrscan_plan_complex(B, T, D, dtype, "bwd", state=True)["name"]},
+                    "elements/s": 2 * E / ((fms + bms) * 1e-3)}
     del ar, ai, br, bi, gr, gi, outs, grads
     torch.cuda.empty_cache()
     return res
@@ -795,8 +815,8 @@ def run_long_t(dev, peak) -> dict:
     (one warp per lane walks all maps) and with the grouped prefix, the
     chunked path at its own chunk lengths (grouped prefix over 512-step chunks
     forward, 128 backward), the single-pass chunk-streaming path, and the
-    automatic plan (streaming); then the automatic plan on bf16 storage of the
-    same draws.  Inputs are drawn on the device from a seeded generator
+    automatic plan (streaming), also with carried state and resets; then the
+    automatic plan on bf16 storage of the same draws.  Inputs are drawn on the device from a seeded generator
     (a~U(0.9,0.9999), b,g~N(0,1))."""
     import torch
 
@@ -830,6 +850,25 @@ def run_long_t(dev, peak) -> dict:
     if L.lrscan_sync_check() != 0:
         raise RuntimeError("device error while timing the long-sequence chunked path")
     res["auto"] = {d: L.lrscan_plan(B, T, D, "f32", d)["name"] for d in ("fwd", "bwd")}
+    # carried state: h0, a segment start every 4,096 steps, grad_last, grad_h0
+    # (the automatic plan); algorithmic bytes add the positions and the states
+    h0 = torch.empty(B, D, device=dev).normal_(generator=gen)
+    gl = torch.empty(B, D, device=dev).normal_(generator=gen)
+    gh0 = torch.empty(B, D, device=dev)
+    seg = (torch.arange(T, device=dev, dtype=torch.int32) % 4096).view(1, T).repeat(B, 1).contiguous()
+    fms = time_launches(lambda i: L.lrscan_fwd_state(a, b, h0=h0, segment_pos=seg, out=out, last=last), 10, stream)
+    bms = time_launches(lambda i: L.lrscan_bwd_state(a, out, g, h0=h0, segment_pos=seg, grad_last=gl, grad_a=ga,
+                                                     grad_b=gb, grad_h0=gh0), 10, stream)
+    if L.lrscan_sync_check() != 0:
+        raise RuntimeError("device error while timing the long scan with carried state")
+    fb, bb = 3 * E * 4 + 4 * B * T + 8 * B * D, 5 * E * 4 + 4 * B * T + 12 * B * D
+    res["auto_plan_state"] = {"what": "h0, a segment start every 4,096 steps, grad_last, grad_h0",
+                              "fwd_ms": fms, "bwd_ms": bms,
+                              "fwd_frac": fb / (fms * 1e-3) / 1e9 / peak,
+                              "bwd_frac": bb / (bms * 1e-3) / 1e9 / peak,
+                              "elements/s": 2 * E / ((fms + bms) * 1e-3),
+                              "kernels": {d: L.lrscan_plan(B, T, D, "f32", d, state=True)["name"]
+                                          for d in ("fwd", "bwd")}}
     a, b, g = a.bfloat16(), b.bfloat16(), g.bfloat16()
     out, ga, gb = torch.empty_like(a), torch.empty_like(a), torch.empty_like(a)
     fms = time_launches(lambda i: L.lrscan_fwd(a, b, out, last), 10, stream)

@@ -524,7 +524,8 @@ def lrscan_cfwd_state(ar, ai, br, bi, h0=None, segment_pos=None, *, out_r=None, 
                       last_i=None, path=None, chunk_len=None, tile_variant=None, workspace=None, stream=None):
     """Complex forward scan from the fp32 (re, im) [B, D] state h0, restarting
     where the int32 [B, T] segment_pos is 0; returns (out_r, out_i, last_r,
-    last_i).  Runs on the chunked path."""
+    last_i).  Runs where the plan puts it: the tiled kernels, chunk
+    streaming (few lanes, long sequences) or the chunked path."""
     if ar.ndim != 3 or any(t.shape != ar.shape for t in (ai, br, bi)):
         raise ValueError("lrscan expects matching [B, T, D] planes")
     code = _dtype_code(ar)
