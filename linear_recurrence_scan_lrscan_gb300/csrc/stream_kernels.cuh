@@ -815,11 +815,14 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                             // the end (a'_T = 1), as selects ahead of the chain
                             const uint32_t m8 = static_cast<uint32_t>(rbits >> r0) & 0xffu;
                             const int pe = BWD ? T - 1 - (wbase + r0) : -1;
+                            // warp-uniform: most groups have neither
+                            if (m8 != 0u || static_cast<unsigned>(pe) < 8u) {
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
+                                for (int q = 0; q < 8; ++q) {
 #pragma unroll
-                                for (int v = 0; v < V; ++v)
-                                    xa[q][v] = q == pe ? 1.0f : (((m8 >> q) & 1u) ? 0.0f : xa[q][v]);
+                                    for (int v = 0; v < V; ++v)
+                                        xa[q][v] = q == pe ? 1.0f : (((m8 >> q) & 1u) ? 0.0f : xa[q][v]);
+                                }
                             }
                         }
 #pragma unroll
@@ -848,13 +851,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                             // (a'_T = 1), as selects ahead of the chain
                             const uint32_t m8 = static_cast<uint32_t>(rbits >> r0) & 0xffu;
                             const int pe = BWD ? T - 1 - (wbase + r0) : -1;
+                            if (m8 != 0u || static_cast<unsigned>(pe) < 8u) {  // warp-uniform
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const bool z = (m8 >> q) & 1u;
+                                for (int q = 0; q < 8; ++q) {
+                                    const bool z = (m8 >> q) & 1u;
 #pragma unroll
-                                for (int v = 0; v < V; ++v) {
-                                    xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
-                                    xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                                    for (int v = 0; v < V; ++v) {
+                                        xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
+                                        xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                                    }
                                 }
                             }
                         }
@@ -1143,10 +1148,12 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     load8<St, V, DT>(tb, g8, lane, xb);
                     if constexpr (EXT) {
                         const uint32_t m8 = static_cast<uint32_t>(rbits >> g8) & 0xffu;
+                        if (m8 != 0u) {  // warp-uniform
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                            for (int q = 0; q < 8; ++q) {
 #pragma unroll
-                            for (int v = 0; v < V; ++v) xa[q][v] = ((m8 >> q) & 1u) ? 0.0f : xa[q][v];
+                                for (int v = 0; v < V; ++v) xa[q][v] = ((m8 >> q) & 1u) ? 0.0f : xa[q][v];
+                            }
                         }
                     }
 #pragma unroll
@@ -1191,11 +1198,13 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                         const uint32_t mn = static_cast<uint32_t>(rnext >> r0) & 0xffu;
                         zmask = static_cast<uint32_t>(rcur >> r0) & 0xffu;
                         const int pe = T - 1 - (wbase + r0);
+                        if (mn != 0u || static_cast<unsigned>(pe) < 8u) {  // warp-uniform
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                            for (int q = 0; q < 8; ++q) {
 #pragma unroll
-                            for (int v = 0; v < V; ++v)
-                                xa[q][v] = q == pe ? 1.0f : (((mn >> q) & 1u) ? 0.0f : xa[q][v]);
+                                for (int v = 0; v < V; ++v)
+                                    xa[q][v] = q == pe ? 1.0f : (((mn >> q) & 1u) ? 0.0f : xa[q][v]);
+                            }
                         }
                         if (wbase + r0 == 0) {
 #pragma unroll
@@ -1242,13 +1251,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     load8<St, V, DT>(rtile(st, 3), g8, lane, bi);
                     if constexpr (EXT) {
                         const uint32_t m8 = static_cast<uint32_t>(rbits >> g8) & 0xffu;
+                        if (m8 != 0u) {  // warp-uniform
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const bool z = (m8 >> q) & 1u;
+                            for (int q = 0; q < 8; ++q) {
+                                const bool z = (m8 >> q) & 1u;
 #pragma unroll
-                            for (int v = 0; v < V; ++v) {
-                                xr[q][v] = z ? 0.0f : xr[q][v];
-                                xi[q][v] = z ? 0.0f : xi[q][v];
+                                for (int v = 0; v < V; ++v) {
+                                    xr[q][v] = z ? 0.0f : xr[q][v];
+                                    xi[q][v] = z ? 0.0f : xi[q][v];
+                                }
                             }
                         }
                     }
@@ -1302,13 +1313,15 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                         const uint32_t mn = static_cast<uint32_t>(rnext >> r0) & 0xffu;
                         zmask = static_cast<uint32_t>(rcur >> r0) & 0xffu;
                         const int pe = T - 1 - (wbase + r0);
+                        if (mn != 0u || static_cast<unsigned>(pe) < 8u) {  // warp-uniform
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const bool z = (mn >> q) & 1u;
+                            for (int q = 0; q < 8; ++q) {
+                                const bool z = (mn >> q) & 1u;
 #pragma unroll
-                            for (int v = 0; v < V; ++v) {
-                                xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
-                                xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                                for (int v = 0; v < V; ++v) {
+                                    xr[q][v] = q == pe ? 1.0f : (z ? 0.0f : xr[q][v]);
+                                    xi[q][v] = q == pe ? 0.0f : (z ? 0.0f : xi[q][v]);
+                                }
                             }
                         }
                         if (wbase + r0 == 0) {
