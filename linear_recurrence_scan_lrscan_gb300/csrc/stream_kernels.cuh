@@ -355,34 +355,6 @@ __device__ bool stream_lookback_cx(const StreamArgs &sa, int gi, int cc, int i0,
     }
 }
 
-// Segment positions of rows t0 .. t0+NR-1 of batch row brow, lane l holding
-// rows l, 32 + l, ...: loaded ahead of their use (rows outside [0, T) read as
-// 1, no reset).
-template <int NR>
-struct SegRows {
-    static constexpr int N = (NR + 31) / 32;
-    int v[N];
-    __device__ __forceinline__ void load(const int32_t *seg, int brow, int T, int t0, int lane) {
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const int r = i * 32 + lane;
-            const int t = t0 + r;
-            v[i] = (r < NR && t >= 0 && t < T) ? __ldg(seg + static_cast<size_t>(brow) * T + t) : 1;
-        }
-    }
-    // bit r of the result for row r < 64 (the whole warp calls it); row 64, if
-    // any, in *row64
-    __device__ __forceinline__ uint64_t bits(bool *row64) const {
-        uint64_t m = 0;
-#pragma unroll
-        for (int i = 0; i < N && i < 2; ++i)
-            m |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, v[i] == 0)) << (32 * i);
-        if constexpr (N > 2) *row64 = __ballot_sync(0xffffffffu, v[2] == 0) & 1u;
-        else *row64 = false;
-        return m;
-    }
-};
-
 // Compiled shape: storage type, lanes per CTA, lanes per thread, rows per
 // window, summary (= replay) warps, windows per warp and chunk, summary and
 // replay stages per warp, scan warps, chunk buffers, complex scan (re / im
@@ -524,8 +496,8 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
     float *cmap = reinterpret_cast<float *>(smem_raw + geo.cmap_off);    // [NB][DT][2K]
     float *wentry = reinterpret_cast<float *>(smem_raw + geo.entry_off); // [NB][NWIN][DT][K]
     [[maybe_unused]] uint64_t *wmask = reinterpret_cast<uint64_t *>(smem_raw + geo.mask_off);  // [NB][NWIN][2]
-    // [slots][NWIN]: bit r = a reset at step r of the window; backward
-    // (complex scan), bit W = one at the step after it
+    // [slots][NWIN]: bit r = a reset at step r of the window; backward, bit W
+    // = one at the step after it
     [[maybe_unused]] uint64_t *tmask = reinterpret_cast<uint64_t *>(smem_raw + geo.tmask_off);
     unsigned int *wcount = reinterpret_cast<unsigned int *>(smem_raw + geo.count_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + geo.flag_off);
@@ -580,10 +552,9 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
 
     if (warp == 2 * NW + NSCAN) {
         // ------------------------------------------------------------ tickets
-        if constexpr (EXT && (!BWD || C::CPLX)) {
+        if constexpr (EXT) {
             if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
-                // carried-state calls with resets (the real scan's forward, the
-                // complex scan's both directions): the whole warp also turns
+                // carried-state calls with resets: the whole warp also turns
                 // each ticket's segment positions into its windows' reset
                 // masks, published (mask_full) after the ticket itself, about
                 // a chunk ahead of the summary that uses them (no global load
@@ -688,10 +659,6 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
         };
         if (!warp_wait(step_full(0), 0u, wc, kSiteStreamStep)) return;
         int tk = step_ticket[0];
-        // the real scan's backward with resets: segment positions of the
-        // current tile's rows and one more (for a_{t+1}), loaded one tile ahead
-        [[maybe_unused]] SegRows<W + 1> segc, segn;
-        [[maybe_unused]] bool seg_next = false;
         for (int k = 0;; ++k) {
             const int b = k % NB;
             if (tk < 0) {
@@ -748,19 +715,6 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 const int wbase = ch.c * CH + (r * NW + w) * W;
                 const int nrows = min(max(T - wbase, 0), W);
                 const int st = w * S + u % S;
-                if constexpr (EXT && BWD && !C::CPLX) {
-                    const int32_t *segp = sx.seg;
-                    if (segp != nullptr) {
-                        if (seg_next) segc = segn;
-                        else segc.load(segp, ch.brow, T, wbase, lane);
-                        seg_next = false;
-                        if (u + 1 < u_iss) {  // the next tile is out: its ticket is known and valid
-                            const Chunk c1 = decode((u + 1) / R == k ? tk : tn);
-                            segn.load(segp, c1.brow, T, c1.c * CH + (((u + 1) % R) * NW + w) * W, lane);
-                            seg_next = true;
-                        }
-                    }
-                }
                 if (!warp_wait(sfull(st), static_cast<uint32_t>((u / S) & 1), wc, kSiteConsumerFull)) {
                     drain();
                     return;
@@ -776,26 +730,19 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                 if constexpr (EXT) {
                     uint64_t rc = 0, rn = 0;
                     if ((C::CPLX ? cx.seg : sx.seg) != nullptr) {
-                        if constexpr (BWD && !C::CPLX) {
-                            bool row64 = false;
-                            const uint64_t full = segc.bits(&row64);
-                            rc = W < 64 ? (full & ((1ull << (W < 64 ? W : 0)) - 1)) : full;
-                            rn = (full >> 1) | (static_cast<uint64_t>(row64) << 63);
+                        // the ticket warp's masks for this chunk (its ticket
+                        // slot k % SLOTS)
+                        if (r == 0 && !warp_wait(mask_full(k % SLOTS), static_cast<uint32_t>((k / SLOTS) & 1), wc,
+                                                 kSiteStreamStep)) {
+                            drain();
+                            return;
+                        }
+                        const uint64_t full = tmask[(k % SLOTS) * NWIN + r * NW + w];
+                        if constexpr (BWD) {
+                            rc = full & ((1ull << W) - 1);
+                            rn = full >> 1;
                         } else {
-                            // the ticket warp's masks for this chunk (its
-                            // ticket slot k % SLOTS)
-                            if (r == 0 && !warp_wait(mask_full(k % SLOTS), static_cast<uint32_t>((k / SLOTS) & 1), wc,
-                                                     kSiteStreamStep)) {
-                                drain();
-                                return;
-                            }
-                            const uint64_t full = tmask[(k % SLOTS) * NWIN + r * NW + w];
-                            if constexpr (BWD) {
-                                rc = full & ((1ull << W) - 1);
-                                rn = full >> 1;
-                            } else {
-                                rc = full;
-                            }
+                            rc = full;
                         }
                     }
                     mcur[r] = rc;
