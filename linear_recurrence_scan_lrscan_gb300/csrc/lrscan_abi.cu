@@ -445,12 +445,13 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         // (eight summary and eight replay warps on 32-lane tiles) in both
         // directions, 0.78-0.81 forward and 0.84-0.93 backward at B=1 D=64,
         // B=1 D=256 and B=8 D=64 against at most 0.75 and 0.88 for the 64-lane
-        // variants; with carried state and resets the bf16 backward takes the
-        // 64-lane tile in 512-step chunks (B=1 T=2^22 D=64: 0.55 against 0.63
-        // ms; B=1 T=2^20 D=256: 0.52 against 0.62 ms)
+        // variants; with carried state and resets bf16 takes the 64-lane tile
+        // in 512-step chunks (B=1 T=2^22 D=64: forward 0.36 against 0.38 ms,
+        // backward 0.53 against 0.58 ms; B=1 T=2^20 D=256: 0.34 / 0.52
+        // against 0.38 / 0.57 ms)
         int vi = force_v > 0 ? force_v - 1 : 0;
         if (force_v == 0 && dtype == LRSCAN_F32) vi = dir == 0 && B * ((D + 31) / 32) >= 8 ? 1 : 0;
-        if (force_v == 0 && dtype == LRSCAN_BF16 && dir == 1 && ext) vi = 1;
+        if (force_v == 0 && dtype == LRSCAN_BF16 && ext) vi = 1;
         return plan_stream_variant(tab, vi, dir, B, T, D, 1, g, ch);
     } else if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix

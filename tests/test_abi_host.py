@@ -170,10 +170,10 @@ def test_occupancy_rule_few_lanes_long_sequence(lib):
         for state in (False, True):
             p = L.lrscan_plan(1, 1 << 20, 64, "f32", direction, state=state)
             assert p["path"] == "stream" and p["name"] == "stream_f32_d32" and p["kernels"] == 1, p
-            # bf16: the eight-warp 32-lane variant, except the backward with
-            # carried state and resets (the 64-lane tile)
+            # bf16: the eight-warp 32-lane variant, with carried state and
+            # resets the 64-lane tile
             q = L.lrscan_plan(1, 1 << 20, 64, "bf16", direction, state=state)
-            want = "stream_bf16_d64" if (state and direction == "bwd") else "stream_bf16_d32"
+            want = "stream_bf16_d64" if state else "stream_bf16_d32"
             assert q["path"] == "stream" and q["name"] == want, q
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "fwd", path="chunk", state=True)
     assert p["path"] == "chunk" and p["kernels"] == 5 and p["name"].startswith("chunk512"), p
