@@ -88,7 +88,8 @@ extern "C" {
                                   eight summary and eight replay warps (forward 1024, backward 512), 2 = 64-lane
                                   tiles (512), 3 = 64-lane tiles (256).  Auto takes it for few lanes and at least
                                   32 chunks of 512 steps per lane group: fp32 variant 2 for a forward from eight
-                                  lane groups, else 1; bf16 variant 1 */
+                                  lane groups, else 1; bf16 variant 2 for a forward from four 64-lane groups or
+                                  with carried state, else 1 */
 
 typedef struct lrscan_opts {
     int path;               /* LRSCAN_PATH_*; 0 = auto */

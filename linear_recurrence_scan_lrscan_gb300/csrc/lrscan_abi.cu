@@ -449,9 +449,13 @@ int plan_call(int64_t B, int64_t T, int64_t D, int dtype, int dir, bool aligned1
         // in 512-step chunks (B=1 T=2^22 D=64: forward 0.36 against 0.38 ms,
         // backward 0.53 against 0.58 ms; B=1 T=2^20 D=256: 0.34 / 0.52
         // against 0.38 / 0.57 ms)
+        // The bf16 forward from four 64-lane groups takes the 64-lane tile, its
+        // two lanes per thread stepping in packed fp32x2 instructions (B=1
+        // T=2^20 D=256: 0.279 against 0.294 ms; B=8 T=2^18 D=64: 0.151 against
+        // 0.160 ms; one group, B=1 D=64: 0.323 against 0.304 ms).
         int vi = force_v > 0 ? force_v - 1 : 0;
         if (force_v == 0 && dtype == LRSCAN_F32) vi = dir == 0 && B * ((D + 31) / 32) >= 8 ? 1 : 0;
-        if (force_v == 0 && dtype == LRSCAN_BF16 && ext) vi = 1;
+        if (force_v == 0 && dtype == LRSCAN_BF16 && (ext || (dir == 0 && B * ((D + 63) / 64) >= 4))) vi = 1;
         return plan_stream_variant(tab, vi, dir, B, T, D, 1, g, ch);
     } else if (path == kPathChunk) {
         // variant 1: flat per-lane prefix; variant 2: grouped prefix

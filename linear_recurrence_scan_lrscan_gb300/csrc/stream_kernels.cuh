@@ -40,6 +40,7 @@
 // word, and the kernel returns).
 #pragma once
 
+#include "packed_f32x2.cuh"
 #include "scan_common.cuh"
 #include "state_args.h"
 #include "stream_args.h"
@@ -776,10 +777,18 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                         for (int rr = 0; rr < 8; ++rr) {
                             const int row = BWD ? 7 - rr : rr;
                             if (r0 + row < nrows) {
+                                if constexpr (V == 2) {
+                                    // both lanes in one packed instruction (the
+                                    // scalar roundings)
+                                    mul_x2(P[r][0][0], P[r][1][0], xa[row][0], xa[row][1], P[r][0][0], P[r][1][0]);
+                                    fma_x2(Q[r][0][0], Q[r][1][0], xa[row][0], xa[row][1], Q[r][0][0], Q[r][1][0],
+                                           xb[row][0], xb[row][1]);
+                                } else {
 #pragma unroll
-                                for (int v = 0; v < V; ++v) {
-                                    P[r][v][0] = __fmul_rn(xa[row][v], P[r][v][0]);
-                                    Q[r][v][0] = __fmaf_rn(xa[row][v], Q[r][v][0], xb[row][v]);
+                                    for (int v = 0; v < V; ++v) {
+                                        P[r][v][0] = __fmul_rn(xa[row][v], P[r][v][0]);
+                                        Q[r][v][0] = __fmaf_rn(xa[row][v], Q[r][v][0], xb[row][v]);
+                                    }
                                 }
                             }
                         }
@@ -1107,8 +1116,14 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                     for (int rr = 0; rr < 8; ++rr) {
                         if (g8 + rr < nrows) {
                             float hv[V];
+                            if constexpr (V == 2) {
+                                fma_x2(h[0][0], h[1][0], xa[rr][0], xa[rr][1], h[0][0], h[1][0], xb[rr][0], xb[rr][1]);
+                                hv[0] = h[0][0];
+                                hv[1] = h[1][0];
+                            } else {
 #pragma unroll
-                            for (int v = 0; v < V; ++v) hv[v] = h[v][0] = __fmaf_rn(xa[rr][v], h[v][0], xb[rr][v]);
+                                for (int v = 0; v < V; ++v) hv[v] = h[v][0] = __fmaf_rn(xa[rr][v], h[v][0], xb[rr][v]);
+                            }
                             store_lanes<St, V>(tb + (g8 + rr) * DT + lane * V, hv);
                         }
                     }
@@ -1163,11 +1178,22 @@ stream_kernel(const __grid_constant__ StreamMaps tm, float *__restrict__ last, f
                         const int row = 7 - rr;
                         if (r0 + row < nrows) {
                             float gv[V], gav[V];
+                            if constexpr (V == 2) {
+                                fma_x2(h[0][0], h[1][0], xa[row][0], xa[row][1], h[0][0], h[1][0], xg[row][0],
+                                       xg[row][1]);
+                                mul_x2(gav[0], gav[1], h[0][0], h[1][0], xh[row][0], xh[row][1]);
+                                gv[0] = h[0][0];
+                                gv[1] = h[1][0];
+                            } else {
 #pragma unroll
-                            for (int v = 0; v < V; ++v) {
-                                gv[v] = h[v][0] = __fmaf_rn(xa[row][v], h[v][0], xg[row][v]);
-                                gav[v] = __fmul_rn(h[v][0], xh[row][v]);
-                                if constexpr (EXT) gav[v] = ((zmask >> row) & 1u) ? 0.0f : gav[v];
+                                for (int v = 0; v < V; ++v) {
+                                    gv[v] = h[v][0] = __fmaf_rn(xa[row][v], h[v][0], xg[row][v]);
+                                    gav[v] = __fmul_rn(h[v][0], xh[row][v]);
+                                }
+                            }
+                            if constexpr (EXT) {
+#pragma unroll
+                                for (int v = 0; v < V; ++v) gav[v] = ((zmask >> row) & 1u) ? 0.0f : gav[v];
                             }
                             store_lanes<St, V>(tb + (r0 + row) * DT + lane * V, gv);
                             store_lanes<St, V>(th + (r0 + row) * DT + lane * V, gav);

@@ -181,17 +181,19 @@ def test_occupancy_rule_few_lanes_long_sequence(lib):
     assert p["workspace_bytes"] == L.lrscan_workspace_bytes(1, 1 << 20, 64, 512)
     p = L.lrscan_plan(1, 1 << 20, 64, "f32", "bwd", path="chunk", state=True)
     assert p["path"] == "chunk" and p["rows_per_window"] == 128 and p["name"].endswith("_grouped"), p
-    # 32-lane tiles throughout; the fp32 forward takes 256-step chunks from
-    # eight lane groups, bf16 the eight-warp variant in both directions
+    # fp32 on 32-lane tiles (the forward in 256-step chunks from eight lane
+    # groups); bf16 on the eight-warp 32-lane variant, except the forward from
+    # four 64-lane groups (the 64-lane tile)
     want = {(1, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d32"),
             (8, 64, "f32"): ("stream_f32_d32_c256", "stream_f32_d32"),
             (1, 128, "f32"): ("stream_f32_d32", "stream_f32_d32"),
-            (1, 256, "bf16"): ("stream_bf16_d32", "stream_bf16_d32"),
-            (8, 64, "bf16"): ("stream_bf16_d32", "stream_bf16_d32")}
+            (1, 256, "bf16"): ("stream_bf16_d64", "stream_bf16_d32"),
+            (8, 64, "bf16"): ("stream_bf16_d64", "stream_bf16_d32")}
     for (B, D, dt), names in want.items():
         for direction, name in zip(("fwd", "bwd"), names):
             p = L.lrscan_plan(B, 1 << 18, D, dt, direction)
-            assert p["path"] == "stream" and p["name"] == name and p["lanes_per_cta"] == 32, (B, D, dt, p)
+            lanes = 64 if "_d64" in name else 32
+            assert p["path"] == "stream" and p["name"] == name and p["lanes_per_cta"] == lanes, (B, D, dt, p)
     # 32 chunks of 512 steps per lane group stream; fewer take the chunked path
     assert L.lrscan_plan(1, 16384, 64, "bf16", "fwd")["path"] == "stream"
     assert L.lrscan_plan(1, 8192, 64, "bf16", "fwd")["path"] == "chunk"
