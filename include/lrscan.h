@@ -79,8 +79,8 @@ extern "C" {
                                   chunk's map, a scan warp finds the entering state by looking back over the
                                   published maps and leaving states, and its replay warps run the chunk again
                                   while its tiles are still in L2.  Bulk-copy path (16-byte aligned rows); carries
-                                  state and resets (lrscan_fwd_state / lrscan_bwd_state, lrscan_cfwd_state / lrscan_cbwd_state); needs
-                                  workspace_bytes of device scratch like the
+                                  state and resets (lrscan_fwd_state / lrscan_bwd_state, lrscan_cfwd_state /
+                                  lrscan_cbwd_state); needs workspace_bytes of device scratch like the
                                   chunked path; agrees with the sequential definition to rounding, and two calls
                                   may differ in the last bits (which published states a look-back composes depends
                                   on timing).  tile_variant: fp32 1 = 32-lane tiles (forward 512-step chunks,
