@@ -112,6 +112,9 @@ def test_gated_full_size():
     this path agrees with the oracle to rounding (near-cancellation points
     allowed under the fp32 rule, and counted)."""
     w = GATED_WORKLOAD
+    # the automatic plan on this shape: one warp per 16-lane slice, both directions
+    for direction in ("fwd", "bwd"):
+        assert L.lrscan_plan_gated(w.B, w.T, w.D, w.dtype, direction)["name"] == "gwarp_bf16_l16_r15"
     inp = make_gated_inputs()
     etad, nud = inp["eta"].cuda(), inp["nu_log"].cuda()
     out, last = L.lrscan_fwd_gated(etad, nud, inp["b"].cuda())
