@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kSlots = 3;
 constexpr int kMaxDev = 64;
-constexpr int kTargetChunks = 8;             // chunks per call when the batch allows
+constexpr int kTargetChunks = 16;            // chunks per call when the batch allows
 constexpr size_t kSlotCap = size_t(1) << 30;  // staging per slot, unless one row needs more
 
 struct Pipe {
