@@ -368,7 +368,10 @@ int lrscan_cbwd_state(const void *ar, const void *ai, const void *out_r, const v
  * The backward needs lrscan_gated_workspace_bytes(B, T, D) bytes of scratch:
  * library-owned per (device, stream), or opts->workspace.  Paths:
  * LRSCAN_PATH_SEQ (tiled, 16-byte aligned rows) or LRSCAN_PATH_PLAIN; auto
- * picks seq when it can.  With T == 0 the forward sets last to 0 and the
+ * picks seq when it can.  Tiled kernels (tile_variant, named by
+ * lrscan_plan_gated): from eight 16-lane slices per SM one warp per slice
+ * (time split between its thread groups, no CTA barrier), else windowed tiles
+ * (time split inside the CTA).  With T == 0 the forward sets last to 0 and the
  * backward sets grad_nu_log to 0.
  */
 int lrscan_fwd_gated(const float *eta, const float *nu_log, const void *b, void *out, float *last,
